@@ -1,0 +1,217 @@
+"""CPU oracle for the block-scaled GEMM (test infrastructure).
+
+This package is the plain, slow definition the CUDA library is checked
+against: ``D = alpha * (A (.) sA)(B (.) sB)^T`` with E2M1 / E4M3 elements
+decoded exactly, accumulation in double and one final rounding to BF16.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import it. The library (``block_scaled_precision_persistent_gb300``)
+never does, and this package imports nothing from the library: the two share
+no code, header, table or constant.
+
+The arithmetic lives in ``bsgemm_oracle.c`` (plain C, compiled with gcc on
+first use); this module only marshals numpy arrays through ctypes.
+
+Sources the definition follows (page title, section):
+  * "Together AI Ports ThunderKittens GEMM Kernels to NVIDIA Vera Rubin NVL72",
+    introduction and "Building the GEMM" -- NVFP4 / FP8 GEMMs with block
+    scaling factors consumed by the tensor-core MMA.
+  * "Triton #11171 - Why Two New NVFP4 Test Cases Produced Twelve
+    Tensor-Memory Failures", "The matrix also compared Triton with a reference
+    implementation" -- comparison against a reference under a
+    format-specific tolerance; "Activation-scale swizzling forced the relevant
+    persistent path" -- the scale layout rewritten in HBM for the persistent
+    kernel.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "bsgemm_oracle.c"
+_BUILD = _HERE / "_build"
+
+# Tolerance of the parity check: |D_gpu - D_ref| <= REL * |D_ref| + ABS * T.
+REL_TOL = 2.0 ** -7
+ABS_TOL = 2.0 ** -20
+
+
+def build(out: Path | None = None, defines: tuple[str, ...] = ()) -> Path:
+    """Compile the oracle with gcc into a shared object and return its path.
+
+    ``defines`` selects planted-mistake variants (``BSO_MUTANT_*``) that the
+    negative-control tests use to show each pin can fail.
+    """
+    if out is None:
+        tag = "_".join(d.lower() for d in defines)
+        out = _BUILD / (f"liboracle_{tag}.so" if tag else "liboracle.so")
+    out = Path(out)
+    if out.exists() and out.stat().st_mtime >= _SRC.stat().st_mtime:
+        return out
+    out.parent.mkdir(parents=True, exist_ok=True)
+    tmp = out.with_suffix(f".tmp{os.getpid()}.so")
+    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-pthread", "-o", str(tmp), str(_SRC), "-lm"]
+    cmd[1:1] = [f"-D{d}" for d in defines]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+class Oracle:
+    """ctypes view of one compiled oracle (the real one or a planted variant)."""
+
+    def __init__(self, defines: tuple[str, ...] = ()):
+        self.lib = ctypes.CDLL(str(build(defines=defines)))
+        L = self.lib
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        L.bso_e2m1.restype = ctypes.c_double
+        L.bso_e2m1.argtypes = [ctypes.c_uint]
+        L.bso_e4m3.restype = ctypes.c_double
+        L.bso_e4m3.argtypes = [ctypes.c_uint]
+        L.bso_bf16_rne.restype = ctypes.c_uint16
+        L.bso_bf16_rne.argtypes = [ctypes.c_double]
+        L.bso_nvfp4_gemm.restype = ctypes.c_int
+        L.bso_nvfp4_gemm.argtypes = [ctypes.c_int] * 3 + [u8p] * 4 + [ctypes.c_float, i32p,
+                                    ctypes.c_int, i32p, ctypes.c_int, f64p, f64p, u16p,
+                                    ctypes.c_int]
+        L.bso_fp8_gemm.restype = ctypes.c_int
+        L.bso_fp8_gemm.argtypes = [ctypes.c_int] * 3 + [u8p] * 2 + [ctypes.c_float] * 3 + [
+            i32p, ctypes.c_int, i32p, ctypes.c_int, f64p, f64p, u16p, ctypes.c_int]
+        L.bso_swizzled_scale_bytes.restype = ctypes.c_size_t
+        L.bso_swizzled_scale_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.bso_swizzle_scales.restype = ctypes.c_int
+        L.bso_swizzle_scales.argtypes = [ctypes.c_int, ctypes.c_int, u8p, u8p]
+
+    # -- element decoders -------------------------------------------------
+    def e2m1(self, code: int) -> float:
+        return self.lib.bso_e2m1(code)
+
+    def e4m3(self, code: int) -> float:
+        return self.lib.bso_e4m3(code)
+
+    def bf16_rne(self, x: float) -> int:
+        return int(self.lib.bso_bf16_rne(float(x)))
+
+    # -- GEMMs --------------------------------------------------------------
+    @staticmethod
+    def _sel(sel, lim):
+        if sel is None:
+            return None, lim
+        arr = np.ascontiguousarray(np.asarray(sel, dtype=np.int32))
+        return arr, int(arr.size)
+
+    @staticmethod
+    def _p(a, ct):
+        return None if a is None else a.ctypes.data_as(ctypes.POINTER(ct))
+
+    def nvfp4_gemm(self, A, sfA, B, sfB, alpha, K, rows=None, cols=None, nthreads=None):
+        """Return (S, T, D_bits) over the selected rows x cols.
+
+        A: uint8[M, K/2], sfA: uint8[M, K/16], B: uint8[N, K/2], sfB: uint8[N, K/16].
+        S is the unrounded double result, T the magnitude sum of the tolerance,
+        D_bits the BF16 bit patterns (uint16) of S rounded once.
+        """
+        A = np.ascontiguousarray(A, dtype=np.uint8)
+        B = np.ascontiguousarray(B, dtype=np.uint8)
+        sfA = np.ascontiguousarray(sfA, dtype=np.uint8)
+        sfB = np.ascontiguousarray(sfB, dtype=np.uint8)
+        M, N = A.shape[0], B.shape[0]
+        assert A.shape == (M, K // 2) and B.shape == (N, K // 2)
+        assert sfA.shape == (M, K // 16) and sfB.shape == (N, K // 16)
+        r, nr = self._sel(rows, M)
+        c, nc = self._sel(cols, N)
+        S = np.empty((nr, nc), np.float64)
+        T = np.empty((nr, nc), np.float64)
+        D = np.empty((nr, nc), np.uint16)
+        rc = self.lib.bso_nvfp4_gemm(M, N, K, self._p(A, ctypes.c_uint8), self._p(sfA, ctypes.c_uint8),
+                                     self._p(B, ctypes.c_uint8), self._p(sfB, ctypes.c_uint8),
+                                     float(alpha), self._p(r, ctypes.c_int32), nr,
+                                     self._p(c, ctypes.c_int32), nc, self._p(S, ctypes.c_double),
+                                     self._p(T, ctypes.c_double), self._p(D, ctypes.c_uint16),
+                                     nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"bso_nvfp4_gemm rejected its arguments (rc={rc})")
+        return S, T, D
+
+    def fp8_gemm(self, A, B, alpha, sA=1.0, sB=1.0, rows=None, cols=None, nthreads=None):
+        """FP8 E4M3 GEMM: D = alpha*sA*sB * A B^T. A: uint8[M, K], B: uint8[N, K]."""
+        A = np.ascontiguousarray(A, dtype=np.uint8)
+        B = np.ascontiguousarray(B, dtype=np.uint8)
+        M, K = A.shape
+        N = B.shape[0]
+        assert B.shape == (N, K)
+        r, nr = self._sel(rows, M)
+        c, nc = self._sel(cols, N)
+        S = np.empty((nr, nc), np.float64)
+        T = np.empty((nr, nc), np.float64)
+        D = np.empty((nr, nc), np.uint16)
+        rc = self.lib.bso_fp8_gemm(M, N, K, self._p(A, ctypes.c_uint8), self._p(B, ctypes.c_uint8),
+                                   float(alpha), float(sA), float(sB), self._p(r, ctypes.c_int32), nr,
+                                   self._p(c, ctypes.c_int32), nc, self._p(S, ctypes.c_double),
+                                   self._p(T, ctypes.c_double), self._p(D, ctypes.c_uint16),
+                                   nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"bso_fp8_gemm rejected its arguments (rc={rc})")
+        return S, T, D
+
+    # -- scale layout ---------------------------------------------------------
+    def swizzled_scale_bytes(self, rows: int, K: int) -> int:
+        return int(self.lib.bso_swizzled_scale_bytes(rows, K))
+
+    def swizzle_scales(self, sf, K: int):
+        """Row-major uint8[rows, K/16] scales -> the 128x4-blocked layout (1-D uint8)."""
+        sf = np.ascontiguousarray(sf, dtype=np.uint8)
+        rows = sf.shape[0]
+        assert sf.shape == (rows, K // 16)
+        out = np.empty(self.swizzled_scale_bytes(rows, K), np.uint8)
+        rc = self.lib.bso_swizzle_scales(rows, K, self._p(sf, ctypes.c_uint8),
+                                         self._p(out, ctypes.c_uint8))
+        if rc != 0:
+            raise ValueError("bso_swizzle_scales rejected its arguments")
+        return out
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover - non-Linux
+        return max(1, os.cpu_count() or 1)
+
+
+_default: Oracle | None = None
+
+
+def get() -> Oracle:
+    """The real (unplanted) oracle, compiled on first use."""
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def bf16_bits_to_float(bits) -> np.ndarray:
+    """Widen BF16 bit patterns (uint16) to float64 values."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def within_tolerance(d_gpu_bits, d_ref_bits, T) -> np.ndarray:
+    """Element-wise |D_gpu - D_ref| <= 2^-7 |D_ref| + 2^-20 T (both BF16).
+
+    NaN is never within tolerance; +0 and -0 compare equal.
+    """
+    g = bf16_bits_to_float(d_gpu_bits)
+    r = bf16_bits_to_float(d_ref_bits)
+    with np.errstate(invalid="ignore"):
+        ok = np.abs(g - r) <= REL_TOL * np.abs(r) + ABS_TOL * np.asarray(T, np.float64)
+    both_inf = np.isinf(g) & np.isinf(r) & (np.sign(g) == np.sign(r))
+    return (ok | both_inf) & ~np.isnan(g) & ~np.isnan(r)

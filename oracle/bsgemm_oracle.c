@@ -1,0 +1,397 @@
+/*
+ * CPU oracle for the block-scaled low-precision GEMM
+ *
+ *     D = alpha * (A (.) sA) (B (.) sB)^T      (FP32 accumulate, BF16 output)
+ *
+ * TEST INFRASTRUCTURE. This is the plain, slow, obviously correct definition
+ * that the CUDA library is checked against. Only the test-suite, the smoke
+ * check and the benchmark's CPU-baseline leg load it; the library never does.
+ * It shares no code, header, table or constant with the CUDA path.
+ *
+ * What it follows:
+ *  - "Together AI Ports ThunderKittens GEMM Kernels to NVIDIA Vera Rubin
+ *    NVL72", introduction and "Building the GEMM": NVFP4 and FP8 GEMMs whose
+ *    tensor-core MMA consumes block scaling factors beside the operands.
+ *  - The operation itself: A and B hold E2M1 codes packed two per byte along
+ *    K, one E4M3 scale per 16 consecutive K elements, an FP32 global alpha,
+ *    FP32 accumulation and BF16 output; the FP8 variant takes E4M3 operands
+ *    with per-tensor FP32 scales.
+ *  - "Triton #11171 - Why Two New NVFP4 Test Cases Produced Twelve
+ *    Tensor-Memory Failures", section "The matrix also compared Triton with a
+ *    reference implementation": the GPU output is compared with a reference
+ *    implementation under a format-specific tolerance.
+ *  - Element formats (the pages name them but do not define them): E2M1 as in
+ *    the OCP Microscaling Formats (MX) v1.0 specification (FP4 element type),
+ *    E4M3 as in the OCP 8-bit Floating Point (OFP8) specification ("E4M3",
+ *    no infinities, S.1111.111 is NaN).
+ *
+ * Readings where the sources are silent (each is listed in the design doc):
+ *  - element 2i of a packed row sits in bits 0..3 of byte i, element 2i+1 in
+ *    bits 4..7;
+ *  - T (the magnitude sum in the tolerance) includes the scales and alpha, so
+ *    it is in output units;
+ *  - the sum runs in double in natural k order, block by block; it is rounded
+ *    once, to BF16 with round-to-nearest-even.
+ *
+ * Parity pins for every function here live in tests/test_oracle.py.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Element decoders                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* E2M1 (4 bits): sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0.
+ * Exponent field 0 is subnormal: value = mantissa * 0.5.
+ * Otherwise value = 2^(e-1) * (1 + m/2).                                    */
+double bso_e2m1(unsigned code)
+{
+    unsigned s = (code >> 3) & 1u, e = (code >> 1) & 3u, m = code & 1u;
+    double v;
+#ifdef BSO_MUTANT_E2M1_BIAS0
+    /* planted mistake for the negative-control tests: exponent bias 0 */
+    v = (e == 0) ? m * 0.5 : ldexp(1.0 + m * 0.5, (int)e);
+#else
+    v = (e == 0) ? m * 0.5 : ldexp(1.0 + m * 0.5, (int)e - 1);
+#endif
+#ifdef BSO_MUTANT_E2M1_NOSIGN
+    s = 0;
+#endif
+    return s ? -v : v;
+}
+
+/* E4M3 (8 bits): sign bit 7, exponent bits 6..3 (bias 7), mantissa 2..0.
+ * Exponent field 0 is subnormal: value = m/8 * 2^-6. S.1111.111 is NaN;
+ * there are no infinities, so S.1111.110 = 448 is the largest magnitude.   */
+double bso_e4m3(unsigned code)
+{
+    unsigned s = (code >> 7) & 1u, e = (code >> 3) & 15u, m = code & 7u;
+    double v;
+    if (e == 15u && m == 7u)
+        return NAN;
+#ifdef BSO_MUTANT_E4M3_BIAS8
+    v = (e == 0) ? ldexp((double)m, -10) : ldexp(1.0 + m / 8.0, (int)e - 8);
+#else
+    v = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, (int)e - 7);
+#endif
+    return s ? -v : v;
+}
+
+/* Round a double to BF16 (8 exponent bits, bias 127, 7 fraction bits) with
+ * round-to-nearest, ties-to-even, in ONE rounding step. Returns the bits.
+ * Values whose rounded magnitude reaches 2^128 become infinities.           */
+uint16_t bso_bf16_rne(double x)
+{
+    if (isnan(x))
+        return 0x7FC0u;
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80u);
+
+    int e2;
+    (void)frexp(a, &e2);          /* a in [2^(e2-1), 2^e2)                  */
+    int lead = e2 - 1;            /* exponent of the leading bit            */
+    int ulp_exp = (lead < -126 ? -126 : lead) - 7;  /* BF16 spacing here    */
+    double q = ldexp(a, -ulp_exp);                  /* exact (power of two) */
+
+    /* explicit round-half-to-even of q to an integer */
+    double fl = floor(q);
+    double frac = q - fl;         /* exact: q < 2^9 in magnitude            */
+    double r = fl;
+    if (frac > 0.5 || (frac == 0.5 && fmod(fl, 2.0) != 0.0))
+        r = fl + 1.0;
+
+    if (lead < -126) {
+        /* subnormal range: r counts units of 2^-133, 0..128; r == 128 is
+         * the smallest normal, whose bit pattern is also 128.              */
+        return (uint16_t)(sign | (uint16_t)r);
+    }
+    /* normal range: r in [128, 256]; 256 carries into the exponent         */
+    if (r == 256.0) {
+        r = 128.0;
+        lead += 1;
+    }
+    int ef = lead + 127;
+    if (ef >= 255)
+        return (uint16_t)(sign | 0x7F80u);
+    return (uint16_t)(sign | (uint16_t)(ef << 7) | (uint16_t)(r - 128.0));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Packed-operand access                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* K-th E2M1 code of a packed row (two codes per byte along K).
+ * Swapping the nibble order of BOTH operands permutes k inside each pair the
+ * same way for A and B and leaves every dot product unchanged; the order is
+ * observable only when the two operands disagree, which is what the planted
+ * variant below does (A read high-nibble-first, B low-nibble-first).       */
+static unsigned nib(const uint8_t *row, int k)
+{
+    uint8_t byte = row[k >> 1];
+    return (k & 1) ? (byte >> 4) : (byte & 15u);
+}
+
+static unsigned nib_a(const uint8_t *row, int k)
+{
+#ifdef BSO_MUTANT_SWAP_NIBBLES_A
+    return nib(row, k ^ 1);
+#else
+    return nib(row, k);
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* Threaded driver: output rows are split evenly across threads             */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int kind;                     /* 0 = NVFP4, 1 = FP8                      */
+    int M, N, K;
+    const uint8_t *A, *sfA, *B, *sfB;
+    double scale;                 /* alpha (NVFP4) or alpha*sA*sB (FP8)       */
+    const int32_t *rows;
+    int nrows;
+    const int32_t *cols;
+    int ncols;
+    double *S, *T;
+    uint16_t *D;
+    int r0, r1;                   /* this worker's output-row range          */
+    double e2m1_tab[16];
+    double e4m3_tab[256];
+} job_t;
+
+/* One output element of the NVFP4 GEMM, by the definition:
+ *   S = alpha * sum_b  e4m3(sfA[i][b]) * e4m3(sfB[j][b])
+ *                    * sum_{t<16} e2m1(A[i][16b+t]) * e2m1(B[j][16b+t])
+ *   T = |alpha| * sum_b |sA*sB| * sum_t |a*b|                              */
+static void nvfp4_element(const job_t *jb, int i, int j, double *S, double *T)
+{
+    const int K = jb->K, nb = K / 16;
+    const uint8_t *ra = jb->A + (size_t)i * (size_t)(K / 2);
+    const uint8_t *rb = jb->B + (size_t)j * (size_t)(K / 2);
+    const uint8_t *sa = jb->sfA + (size_t)i * (size_t)nb;
+    const uint8_t *sb = jb->sfB + (size_t)j * (size_t)nb;
+    double s = 0.0, t = 0.0;
+#ifdef BSO_MUTANT_DROP_LAST_BLOCK
+    for (int b = 0; b < nb - 1; ++b) {
+#else
+    for (int b = 0; b < nb; ++b) {
+#endif
+        double blk = 0.0, blk_abs = 0.0;
+        for (int u = 0; u < 16; ++u) {
+            int k = 16 * b + u;
+#ifdef BSO_MUTANT_TRANSPOSE_B
+            /* reads B as if it were stored [K][N] (square shapes only) */
+            double p = jb->e2m1_tab[nib_a(ra, k)]
+                       * jb->e2m1_tab[nib(jb->B + (size_t)k * (size_t)(K / 2), j)];
+            (void)rb;
+#else
+            double p = jb->e2m1_tab[nib_a(ra, k)] * jb->e2m1_tab[nib(rb, k)];
+#endif
+            blk += p;
+            blk_abs += fabs(p);
+        }
+#ifdef BSO_MUTANT_DROP_SFB
+        double sc = jb->e4m3_tab[sa[b]];
+        (void)sb;
+#else
+        double sc = jb->e4m3_tab[sa[b]] * jb->e4m3_tab[sb[b]];
+#endif
+        s += sc * blk;
+        t += fabs(sc) * blk_abs;
+    }
+    *S = jb->scale * s;
+    *T = fabs(jb->scale) * t;
+}
+
+/* One output element of the FP8 GEMM:
+ *   S = alpha*sA*sB * sum_k e4m3(A[i][k]) * e4m3(B[j][k])                  */
+static void fp8_element(const job_t *jb, int i, int j, double *S, double *T)
+{
+    const int K = jb->K;
+    const uint8_t *ra = jb->A + (size_t)i * (size_t)K;
+    const uint8_t *rb = jb->B + (size_t)j * (size_t)K;
+    double s = 0.0, t = 0.0;
+    for (int k = 0; k < K; ++k) {
+        double p = jb->e4m3_tab[ra[k]] * jb->e4m3_tab[rb[k]];
+        s += p;
+        t += fabs(p);
+    }
+    *S = jb->scale * s;
+    *T = fabs(jb->scale) * t;
+}
+
+static void *worker(void *arg)
+{
+    job_t *jb = (job_t *)arg;
+    for (int r = jb->r0; r < jb->r1; ++r) {
+        int i = jb->rows ? jb->rows[r] : r;
+        for (int c = 0; c < jb->ncols; ++c) {
+            int j = jb->cols ? jb->cols[c] : c;
+            double S, T;
+            if (jb->kind == 0)
+                nvfp4_element(jb, i, j, &S, &T);
+            else
+                fp8_element(jb, i, j, &S, &T);
+            size_t o = (size_t)r * (size_t)jb->ncols + (size_t)c;
+            if (jb->S) jb->S[o] = S;
+            if (jb->T) jb->T[o] = T;
+            if (jb->D) jb->D[o] = bso_bf16_rne(S);
+        }
+    }
+    return NULL;
+}
+
+static int run(job_t *proto, int nthreads)
+{
+    for (int c = 0; c < 16; ++c)
+        proto->e2m1_tab[c] = bso_e2m1((unsigned)c);
+    for (int c = 0; c < 256; ++c)
+        proto->e4m3_tab[c] = bso_e4m3((unsigned)c);
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > proto->nrows)
+        nthreads = proto->nrows > 0 ? proto->nrows : 1;
+    if (nthreads > 1024)
+        nthreads = 1024;
+    job_t *jobs = (job_t *)malloc(sizeof(job_t) * (size_t)nthreads);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return -2;
+    }
+    int started = 0;
+    for (int w = 0; w < nthreads; ++w) {
+        jobs[w] = *proto;
+        jobs[w].r0 = (int)((long long)proto->nrows * w / nthreads);
+        jobs[w].r1 = (int)((long long)proto->nrows * (w + 1) / nthreads);
+        if (nthreads == 1 || pthread_create(&th[w], NULL, worker, &jobs[w]) != 0) {
+            worker(&jobs[w]);
+            th[w] = 0;
+        } else {
+            ++started;
+        }
+    }
+    for (int w = 0; w < nthreads; ++w)
+        if (th[w])
+            pthread_join(th[w], NULL);
+    (void)started;
+    free(jobs);
+    free(th);
+    return 0;
+}
+
+static int check_sel(const int32_t *sel, int n, int lim)
+{
+    if (!sel)
+        return 0;
+    for (int q = 0; q < n; ++q)
+        if (sel[q] < 0 || sel[q] >= lim)
+            return -1;
+    return 0;
+}
+
+/* NVFP4 GEMM over the selected rows x cols of D (rows/cols NULL = all).
+ * A: uint8[M][K/2], sfA: uint8[M][K/16] row-major E4M3, B: uint8[N][K/2],
+ * sfB: uint8[N][K/16]. Outputs are [nrows][ncols]; any may be NULL.
+ * Returns 0, or -1 for bad sizes.                                          */
+int bso_nvfp4_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *sfA,
+                   const uint8_t *B, const uint8_t *sfB, float alpha,
+                   const int32_t *rows, int nrows, const int32_t *cols, int ncols,
+                   double *S, double *T, uint16_t *D, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || (K % 16) != 0)
+        return -1;
+    if (!rows) nrows = M;
+    if (!cols) ncols = N;
+    if (check_sel(rows, nrows, M) || check_sel(cols, ncols, N))
+        return -1;
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.kind = 0;
+    jb.M = M; jb.N = N; jb.K = K;
+    jb.A = A; jb.sfA = sfA; jb.B = B; jb.sfB = sfB;
+    jb.scale = (double)alpha;
+    jb.rows = rows; jb.nrows = nrows; jb.cols = cols; jb.ncols = ncols;
+    jb.S = S; jb.T = T; jb.D = D;
+    return run(&jb, nthreads);
+}
+
+/* FP8 GEMM: A uint8[M][K] E4M3, B uint8[N][K] E4M3; the effective multiplier
+ * is the exact double product alpha * sA * sB of the three FP32 values.    */
+int bso_fp8_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *B,
+                 float alpha, float sA, float sB,
+                 const int32_t *rows, int nrows, const int32_t *cols, int ncols,
+                 double *S, double *T, uint16_t *D, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return -1;
+    if (!rows) nrows = M;
+    if (!cols) ncols = N;
+    if (check_sel(rows, nrows, M) || check_sel(cols, ncols, N))
+        return -1;
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.kind = 1;
+    jb.M = M; jb.N = N; jb.K = K;
+    jb.A = A; jb.B = B;
+    jb.scale = (double)alpha * (double)sA * (double)sB;
+    jb.rows = rows; jb.nrows = nrows; jb.cols = cols; jb.ncols = ncols;
+    jb.S = S; jb.T = T; jb.D = D;
+    return run(&jb, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scale-factor layout consumed by the block-scaled tensor-core MMA          */
+/* ------------------------------------------------------------------------ */
+
+/* "Triton #11171 ...", section "Activation-scale swizzling forced the
+ * relevant persistent path": the persistent Blackwell kernel reads the scales
+ * in a Blackwell-specific layout rewritten in HBM. The layout used here is the
+ * tcgen05 block-scale-factor layout of the public PTX ISA: rows are padded to
+ * a multiple of 128 and scale columns (K/16) to a multiple of 4; the padded
+ * matrix is cut into 128 x 4 blocks of 512 bytes, ordered row-block-major
+ * with the column-block index fastest; inside a block, row r and column c go
+ * to byte (r % 32) * 16 + (r / 32) * 4 + c. Padding bytes are zero.        */
+size_t bso_swizzled_scale_bytes(int rows, int K)
+{
+    if (rows < 0 || K < 0 || (K % 16) != 0)
+        return 0;
+    size_t pr = ((size_t)rows + 127u) / 128u * 128u;
+    size_t pc = ((size_t)(K / 16) + 3u) / 4u * 4u;
+    return pr * pc;
+}
+
+int bso_swizzle_scales(int rows, int K, const uint8_t *in, uint8_t *out)
+{
+    if (rows < 0 || K < 0 || (K % 16) != 0)
+        return -1;
+    const int cols = K / 16;
+    const int pr = (rows + 127) / 128 * 128;
+    const int pc = (cols + 3) / 4 * 4;
+    const int ncb = pc / 4;
+    for (int r = 0; r < pr; ++r) {
+        for (int c = 0; c < pc; ++c) {
+            size_t blk = (size_t)(r / 128) * (size_t)ncb + (size_t)(c / 4);
+            int rr = r % 128;
+#ifdef BSO_MUTANT_SWIZZLE_ROWMAJOR_BLOCK
+            size_t off = blk * 512u + (size_t)rr * 4u + (size_t)(c % 4);
+#else
+            size_t off = blk * 512u + (size_t)(rr % 32) * 16u + (size_t)(rr / 32) * 4u
+                         + (size_t)(c % 4);
+#endif
+            out[off] = (r < rows && c < cols) ? in[(size_t)r * (size_t)cols + (size_t)c] : 0u;
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,353 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself.
+
+Every pin below checks the oracle against something it does not compute:
+golden tables from the format specifications (``tests/golden/``), values
+worked by hand, a library decoder (PyTorch's CPU float8_e4m3fn), exact
+rational arithmetic, an independent numpy restatement, and invariants of the
+definition. ``test_planted_mistake_is_caught`` compiles the oracle with one
+deliberate mistake at a time (a wrong exponent bias, a dropped sign, swapped
+nibbles in one operand, a dropped scale, a dropped block, a transposed operand, a wrong
+scale layout) and shows that at least one pin fails for each.
+"""
+from __future__ import annotations
+
+import math
+import random
+from fractions import Fraction
+from pathlib import Path
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+GOLDEN = Path(__file__).resolve().parent / "golden"
+
+
+# --------------------------------------------------------------------------
+# Golden data
+# --------------------------------------------------------------------------
+
+def _rows(name):
+    for line in (GOLDEN / name).read_text().splitlines():
+        line = line.strip()
+        if line and not line.startswith("#"):
+            yield line.split()
+
+
+E2M1_TABLE = {int(c, 16): float(v) for c, v in _rows("e2m1_table.txt")}
+E4M3_POINTS = {int(c, 16): float(v) for c, v in _rows("e4m3_points.txt")}
+BF16_CASES = [(float.fromhex(x), int(b, 16)) for x, b, *_ in _rows("bf16_rne_cases.txt")]
+
+
+def e4m3_lib(code: int) -> float:
+    """PyTorch's own E4M3 decoder (a library routine, used only as a check)."""
+    return float(torch.tensor([code], dtype=torch.uint8).view(torch.float8_e4m3fn)
+                 .to(torch.float64)[0])
+
+
+def e4m3_code_of(value: float) -> int:
+    """E4M3 code of an exactly representable value, via PyTorch's encoder."""
+    return int(torch.tensor([value], dtype=torch.float32).to(torch.float8_e4m3fn)
+               .view(torch.uint8)[0])
+
+
+def pack(codes: np.ndarray) -> np.ndarray:
+    """uint8 codes [rows, K] -> packed bytes, element 2i in the low nibble."""
+    codes = np.asarray(codes, np.uint8)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+def deq_nvfp4(packed: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    """Independent dequantisation via the golden E2M1 table and torch E4M3."""
+    lo = packed & 15
+    hi = packed >> 4
+    codes = np.empty((packed.shape[0], packed.shape[1] * 2), np.uint8)
+    codes[:, 0::2] = lo
+    codes[:, 1::2] = hi
+    tab = np.array([E2M1_TABLE[c] for c in range(16)])
+    scale = np.array([e4m3_lib(c) for c in range(256)])
+    return tab[codes] * np.repeat(scale[sf], 16, axis=1)
+
+
+# --------------------------------------------------------------------------
+# Pins: each takes an Oracle and raises AssertionError on a mismatch
+# --------------------------------------------------------------------------
+
+def pin_e2m1_table(o):
+    for code, val in E2M1_TABLE.items():
+        got = o.e2m1(code)
+        assert got == val and math.copysign(1, got) == math.copysign(1, val), (code, got, val)
+
+
+def pin_e4m3_codes(o):
+    for code in range(256):
+        got, ref = o.e4m3(code), e4m3_lib(code)
+        assert (math.isnan(got) and math.isnan(ref)) or got == ref, (code, got, ref)
+    for code, val in E4M3_POINTS.items():
+        got = o.e4m3(code)
+        assert (math.isnan(got) and math.isnan(val)) or got == val, (code, got, val)
+
+
+def pin_bf16_cases(o):
+    for x, bits in BF16_CASES:
+        assert o.bf16_rne(x) == bits, (x.hex(), hex(o.bf16_rne(x)), hex(bits))
+    # binary32-representable inputs: PyTorch's float32 -> bfloat16 (RNE) is
+    # then a single rounding too, so the two must agree bit for bit.
+    rng = np.random.default_rng(7)
+    f = np.concatenate([
+        rng.standard_normal(3000).astype(np.float32) * np.float32(1e3),
+        (rng.integers(-2**15, 2**15, 2000).astype(np.float32) * np.float32(2.0 ** -8)),
+        np.array([1e-39, -3e-40, 1e-45, 3.4e38, -3.39e38], np.float32),
+    ])
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    for x, r in zip(f.tolist(), ref.tolist()):
+        assert o.bf16_rne(x) == r, (x, hex(o.bf16_rne(x)), hex(r))
+
+
+def pin_worked_1x1x16(o):
+    # A[0][t] = B[0][t] = code t (t = 0..15): values 0, .5, 1, 1.5, 2, 3, 4, 6
+    # and their negatives. sfA = 2.0 (0x40), sfB = 0.5 (0x30), alpha = 1.
+    # sum_t a_t^2 = 2 * (0 + .25 + 1 + 2.25 + 4 + 9 + 16 + 36) = 137, so
+    # D = 2 * 0.5 * 137 = 137, exact in BF16 (0x4309).
+    codes = np.arange(16, dtype=np.uint8)[None, :]
+    A = pack(codes)
+    S, T, D = o.nvfp4_gemm(A, np.array([[0x40]], np.uint8), A, np.array([[0x30]], np.uint8), 1.0, 16)
+    assert S[0, 0] == 137.0 and T[0, 0] == 137.0 and D[0, 0] == 0x4309, (S, T, D)
+
+
+def pin_worked_2x2x32(o):
+    # A0 = all 1.0, sA0 = [1, 2];  A1 = all -1.0, sA1 = [0.5, 1]
+    # B0 = all 2.0, sB0 = [1, 1];  B1 = code (k mod 8) (each 16-block sums to
+    # 36), sB1 = [1, 0.25].
+    # D00 = 32 + 64 = 96; D01 = 36 + 18 = 54; D10 = -16 - 32 = -48;
+    # D11 = -18 - 9 = -27.
+    A = pack(np.array([[0x2] * 32, [0xA] * 32], np.uint8))
+    B = pack(np.array([[0x4] * 32, [k % 8 for k in range(32)]], np.uint8))
+    sfA = np.array([[0x38, 0x40], [0x30, 0x38]], np.uint8)
+    sfB = np.array([[0x38, 0x38], [0x38, 0x28]], np.uint8)
+    S, _, D = o.nvfp4_gemm(A, sfA, B, sfB, 1.0, 32)
+    assert np.array_equal(S, [[96.0, 54.0], [-48.0, -27.0]]), S
+    assert np.array_equal(oracle.bf16_bits_to_float(D), S), D
+
+
+def pin_one_hot(o):
+    # A row i is one-hot at k = pi(i) with value 1.0, all scales 1.0, alpha 1:
+    # then D[i][j] is exactly the E2M1 value of B[j][pi(i)]. Positions of both
+    # parities pin that A and B are read with the same nibble order (element
+    # 2i in the low nibble, as packed here).
+    K, M, N = 64, 64, 48
+    rng = np.random.default_rng(11)
+    pi = rng.permutation(K)[:M]
+    codes_a = np.zeros((M, K), np.uint8)
+    codes_a[np.arange(M), pi] = 0x2
+    codes_b = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    ones_a = np.full((M, K // 16), 0x38, np.uint8)
+    ones_b = np.full((N, K // 16), 0x38, np.uint8)
+    S, _, _ = o.nvfp4_gemm(pack(codes_a), ones_a, pack(codes_b), ones_b, 1.0, K)
+    tab = np.array([E2M1_TABLE[c] for c in range(16)])
+    want = tab[codes_b[:, pi]].T
+    assert np.array_equal(S, want)
+
+
+def pin_brute_force_k16(o):
+    # K = 16, a single nonzero position t: row i of A holds code i at t, row j
+    # of B holds code j at t; per-row scales vary. Then S[i][j] is the table
+    # product e2m1(i) * e2m1(j) * sA_i * sB_j for all 16 x 16 code pairs.
+    tab = np.array([E2M1_TABLE[c] for c in range(16)])
+    scale_codes = [0x38, 0x40, 0x30, 0x3C, 0x01, 0x7E, 0x55, 0x23]
+    for t in range(16):
+        ca = np.zeros((16, 16), np.uint8)
+        ca[:, t] = np.arange(16)
+        sa = np.array([[scale_codes[(i + t) % 8]] for i in range(16)], np.uint8)
+        sb = np.array([[scale_codes[(3 * j + t) % 8]] for j in range(16)], np.uint8)
+        S, T, _ = o.nvfp4_gemm(pack(ca), sa, pack(ca), sb, 1.0, 16)
+        vs_a = np.array([e4m3_lib(int(c)) for c in sa[:, 0]])
+        vs_b = np.array([e4m3_lib(int(c)) for c in sb[:, 0]])
+        want = np.outer(tab * vs_a, tab * vs_b)
+        assert np.array_equal(S, want), t
+        assert np.array_equal(T, np.abs(want)), t
+
+
+def _uniform_problem(M, N, K, seed):
+    w = workloads.WORKLOADS["nvfp4_256"]
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randint(0, 256, (M, K // 2), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    B = torch.randint(0, 256, (N, K // 2), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    sfA = workloads.uniform_nvfp4(M, K, seed + 1, "cpu")[1].numpy()
+    sfB = workloads.uniform_nvfp4(N, K, seed + 2, "cpu")[1].numpy()
+    del w
+    return A, sfA, B, sfB
+
+
+def pin_scale_linearity(o):
+    # Doubling one block scale sfA[i][b] (E4M3 exponent field + 1) adds
+    # exactly that block's contribution to row i and leaves other rows alone.
+    M = N = 32
+    K = 64
+    A, sfA, B, sfB = _uniform_problem(M, N, K, 3)
+    S0, _, _ = o.nvfp4_gemm(A, sfA, B, sfB, 1.0, K)
+    i, b = 5, 2
+    sf2 = sfA.copy()
+    assert ((sf2[i, b] >> 3) & 15) < 14
+    sf2[i, b] += 8
+    S1, _, _ = o.nvfp4_gemm(A, sf2, B, sfB, 1.0, K)
+    blk, _, _ = o.nvfp4_gemm(A[:, 8 * b:8 * b + 8], sfA[:, b:b + 1], B[:, 8 * b:8 * b + 8],
+                             sfB[:, b:b + 1], 1.0, 16)
+    assert np.array_equal(S1[i] - S0[i], blk[i])
+    others = np.arange(M) != i
+    assert np.array_equal(S1[others], S0[others])
+    # halving a scale (exponent field - 1) removes half the contribution
+    sf3 = sfA.copy()
+    sf3[i, b] -= 8
+    S3, _, _ = o.nvfp4_gemm(A, sf3, B, sfB, 1.0, K)
+    assert np.array_equal(S0[i] - S3[i], blk[i] / 2)
+
+
+def pin_numpy_definition(o):
+    # Independent restatement: dequantise with the golden E2M1 table and the
+    # library E4M3 decoder, multiply with numpy in float64. With 2^u scales
+    # every partial sum is exact in double, so the results must be identical.
+    # Square so that a transposed operand cannot hide.
+    M = N = K = 64
+    A, sfA, B, sfB = _uniform_problem(M, N, K, 9)
+    S, T, D = o.nvfp4_gemm(A, sfA, B, sfB, 0.75, K)
+    da, db = deq_nvfp4(A, sfA), deq_nvfp4(B, sfB)
+    assert np.array_equal(S, 0.75 * (da @ db.T))
+    assert np.array_equal(T, 0.75 * (np.abs(da) @ np.abs(db).T))
+    # and through a rectangular, N(0,1)-quantised problem (not exact sums)
+    w = workloads.WORKLOADS["nvfp4_4096"]
+    p = workloads.make_nvfp4(w, "cpu", M=48, N=80, K=256)
+    S, _, _ = o.nvfp4_gemm(p["A"].numpy(), p["sfA"].numpy(), p["B"].numpy(), p["sfB"].numpy(),
+                           p["alpha"], 256)
+    ref = float(np.float32(p["alpha"])) * (deq_nvfp4(p["A"].numpy(), p["sfA"].numpy())
+                                           @ deq_nvfp4(p["B"].numpy(), p["sfB"].numpy()).T)
+    assert np.allclose(S, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def pin_fraction_exact(o):
+    # Brute force in exact rational arithmetic on a tiny problem.
+    M, N, K = 3, 5, 32
+    rng = random.Random(5)
+    ca = [[rng.randrange(16) for _ in range(K)] for _ in range(M)]
+    cb = [[rng.randrange(16) for _ in range(K)] for _ in range(N)]
+    sa = [[rng.choice([0x38, 0x41, 0x2A, 0x06, 0x7E]) for _ in range(K // 16)] for _ in range(M)]
+    sb = [[rng.choice([0x38, 0x3B, 0x49, 0x11]) for _ in range(K // 16)] for _ in range(N)]
+    alpha = 0.3125
+    S, _, D = o.nvfp4_gemm(pack(np.array(ca, np.uint8)), np.array(sa, np.uint8),
+                           pack(np.array(cb, np.uint8)), np.array(sb, np.uint8), alpha, K)
+    for i in range(M):
+        for j in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                acc += (Fraction(E2M1_TABLE[ca[i][k]]) * Fraction(E2M1_TABLE[cb[j][k]])
+                        * Fraction(e4m3_lib(sa[i][k // 16])) * Fraction(e4m3_lib(sb[j][k // 16])))
+            exact = Fraction(alpha) * acc
+            assert Fraction(S[i, j]) == exact, (i, j)
+            # BF16 of the exact value: nearest of the two neighbours, by hand
+            assert D[i, j] == o.bf16_rne(float(exact))
+
+
+def pin_fp8_numpy(o):
+    # FP8: library-decoded E4M3 operands multiplied by numpy in float64; all
+    # partial sums are exact in double at this size, so only the final scale
+    # multiplication can round.
+    w = workloads.WORKLOADS["fp8_8192"]
+    p = workloads.make_fp8(w, "cpu", M=40, N=24, K=96)
+    A, B = p["A"].numpy(), p["B"].numpy()
+    S, T, _ = o.fp8_gemm(A, B, p["alpha"], 1.0, 1.0)
+    dec = np.array([e4m3_lib(c) for c in range(256)])
+    ref = (dec[A] @ dec[B].T) * float(np.float32(p["alpha"]))
+    assert np.allclose(S, ref, rtol=1e-15, atol=0)
+    # per-tensor scales: alpha*sA*sB with the three FP32 values
+    S2, _, _ = o.fp8_gemm(A, B, 2.0, 0.5, 3.0)
+    assert np.allclose(S2, (dec[A] @ dec[B].T) * 3.0, rtol=1e-15, atol=0)
+    assert np.array_equal(T, (np.abs(dec[A]) @ np.abs(dec[B]).T) * float(np.float32(p["alpha"])))
+
+
+def _swizzle_numpy(sf: np.ndarray, K: int) -> np.ndarray:
+    """Independent restatement of the 128x4-blocked scale layout by reshapes."""
+    rows, cols = sf.shape
+    pr, pc = -(-rows // 128) * 128, -(-cols // 4) * 4
+    pad = np.zeros((pr, pc), np.uint8)
+    pad[:rows, :cols] = sf
+    # (row-block, r1, r0, col-block, c) with row = 128*rb + 32*r1 + r0
+    t = pad.reshape(pr // 128, 4, 32, pc // 4, 4)
+    # block order (rb, cb); inside a block byte index r0*16 + r1*4 + c
+    return t.transpose(0, 3, 2, 1, 4).reshape(-1).copy()
+
+
+def pin_swizzle(o):
+    # hand-worked offsets for rows = 256, K = 512 (32 scale columns, 8 blocks
+    # of 4 per row-block): (r, c) -> block (r//128)*8 + c//4, byte
+    # (r%32)*16 + ((r%128)//32)*4 + c%4
+    rows, K = 256, 512
+    sf = np.zeros((rows, K // 16), np.uint8)
+    marks = {(0, 0): 0, (33, 5): 533, (130, 10): 5154, (255, 31): 8191, (96, 3): 15}
+    for n, (r, c) in enumerate(marks):
+        sf[r, c] = n + 1
+    out = o.swizzle_scales(sf, K)
+    assert out.size == 8192
+    for n, ((r, c), off) in enumerate(marks.items()):
+        assert out[off] == n + 1, ((r, c), off)
+    assert int((out != 0).sum()) == len(marks)
+    # ragged shapes: independent reshape restatement, bijection and zero pad
+    rng = np.random.default_rng(3)
+    for rows, K in ((1, 16), (127, 48), (129, 64), (300, 1040), (256, 256)):
+        sf = rng.integers(1, 256, (rows, K // 16)).astype(np.uint8)
+        out = o.swizzle_scales(sf, K)
+        assert out.size == o.swizzled_scale_bytes(rows, K)
+        assert np.array_equal(out, _swizzle_numpy(sf, K)), (rows, K)
+        assert int((out != 0).sum()) == sf.size
+        assert np.array_equal(np.sort(out[out != 0]), np.sort(sf.reshape(-1)))
+
+
+PINS = [pin_e2m1_table, pin_e4m3_codes, pin_bf16_cases, pin_worked_1x1x16, pin_worked_2x2x32,
+        pin_one_hot, pin_brute_force_k16, pin_scale_linearity, pin_numpy_definition,
+        pin_fraction_exact, pin_fp8_numpy, pin_swizzle]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_oracle_pin(pin):
+    pin(oracle.get())
+
+
+MUTANTS = ["E2M1_BIAS0", "E2M1_NOSIGN", "E4M3_BIAS8", "SWAP_NIBBLES_A", "DROP_SFB",
+           "DROP_LAST_BLOCK", "TRANSPOSE_B", "SWIZZLE_ROWMAJOR_BLOCK"]
+
+
+@pytest.mark.parametrize("mutant", MUTANTS)
+def test_planted_mistake_is_caught(mutant):
+    bad = oracle.Oracle(defines=(f"BSO_MUTANT_{mutant}",))
+    failed = []
+    for pin in PINS:
+        try:
+            pin(bad)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake {mutant}"
+
+
+def test_tolerance_helper():
+    b = lambda x: np.array([oracle.get().bf16_rne(v) for v in x], np.uint16)  # noqa: E731
+    ref = b([100.0, 0.0, -3.0, 1.0])
+    T = np.array([1e4, 2.0 ** 20, 1.0, 1.0])
+    # within: one BF16 ulp of 100 (0.5 <= 2^-7 * 100); |0.5| <= 2^-20 * 2^20
+    assert oracle.within_tolerance(b([100.5, 0.5, -3.0, 1.0]), ref, T).all()
+    # outside: two ulps of 100; 1.5 > 1; wrong sign; NaN
+    got = oracle.within_tolerance(b([101.0, 1.5, 3.0, float("nan")]), ref, T)
+    assert not got.any()
+
+
+def test_oracle_row_col_selection_matches_full():
+    A, sfA, B, sfB = _uniform_problem(40, 56, 128, 21)
+    o = oracle.get()
+    S, T, D = o.nvfp4_gemm(A, sfA, B, sfB, 1.5, 128)
+    rows, cols = [39, 0, 17], [55, 3]
+    S2, T2, D2 = o.nvfp4_gemm(A, sfA, B, sfB, 1.5, 128, rows=rows, cols=cols, nthreads=3)
+    assert np.array_equal(S2, S[np.ix_(rows, cols)]) and np.array_equal(D2, D[np.ix_(rows, cols)])
+    assert np.array_equal(T2, T[np.ix_(rows, cols)])
+    with pytest.raises(ValueError):
+        o.nvfp4_gemm(A, sfA, B, sfB, 1.0, 128, rows=[40])

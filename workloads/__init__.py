@@ -1,0 +1,204 @@
+"""Seeded synthetic inputs for the block-scaled GEMM.
+
+Shared by the tests, the smoke check and the benchmark. This module only
+draws random numbers and encodes them into the operand formats (E2M1 codes
+packed two per byte, E4M3 scale bytes, E4M3 FP8 operands). It holds none of
+the GEMM's arithmetic, imports neither the oracle nor the library, and both
+sides receive exactly the bytes it produces.
+
+Workloads (the pages' shapes; all data synthetic):
+  * ``nvfp4_256``   M=N=K=256, E2M1 codes uniform over all 16 nibbles, block
+    scales 2^u with u uniform in [-4, 4], alpha = 1.
+  * ``nvfp4_4096``  M=N=K=4096, N(0,1) rounded to BF16, two-level NVFP4
+    quantisation (below), alpha = 1 / (s_gA * s_gB).
+  * ``nvfp4_16384`` M=N=K=16384, as ``nvfp4_4096`` (the square shape of the
+    ring-depth sweep in "Together AI Ports ThunderKittens GEMM Kernels to
+    NVIDIA Vera Rubin NVL72", "Building the GEMM").
+  * ``fp8_8192``    M=N=K=8192 E4M3 from N(0,1) with per-tensor scale
+    amax/448, alpha = s_A * s_B.
+  * skinny cells   M in {64,128,256,512} x (N,K) in {(3072,3072),
+    (12288,3072), (3072,12288)}, activations and weights N(0, 0.02), two-level
+    NVFP4.
+
+Two-level NVFP4 quantisation of a tensor x (input generation only):
+  s_g = 448*6 / amax|x| (FP32); per 16-block b: scale_b = E4M3_rne(min(448,
+  amax_b/6 * s_g)); code = E2M1_rne_sat(x * s_g / scale_b) (code 0 where
+  scale_b = 0). The GEMM then needs alpha = 1/(s_gA * s_gB).
+
+Random numbers come from ``torch.Generator`` on the device the data is made
+on, so CPU and GPU draws differ in bits but not in distribution; every parity
+check feeds the same bytes to both sides.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+SEED_BASE = 0xB5C0
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str          # "nvfp4" or "fp8"
+    M: int
+    N: int
+    K: int
+    dist: str          # "uniform_codes" or "normal"
+    std: float = 1.0
+    index: int = 0     # seed slot
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    @property
+    def algorithmic_bytes(self) -> float:
+        """Minimum HBM bytes of one GEMM: packed operands, scales, BF16 D."""
+        if self.kind == "nvfp4":
+            return (self.M + self.N) * self.K * 9 / 16 + 2.0 * self.M * self.N
+        return (self.M + self.N) * self.K + 2.0 * self.M * self.N
+
+
+SKINNY_M = (64, 128, 256, 512)
+SKINNY_NK = ((3072, 3072), (12288, 3072), (3072, 12288))
+
+WORKLOADS: dict[str, Workload] = {}
+
+
+def _add(w: Workload) -> None:
+    WORKLOADS[w.name] = w
+
+
+_add(Workload("nvfp4_256", "nvfp4", 256, 256, 256, "uniform_codes", index=0))
+_add(Workload("nvfp4_4096", "nvfp4", 4096, 4096, 4096, "normal", 1.0, index=1))
+_add(Workload("nvfp4_16384", "nvfp4", 16384, 16384, 16384, "normal", 1.0, index=2))
+_add(Workload("fp8_8192", "fp8", 8192, 8192, 8192, "normal", 1.0, index=3))
+for _n, _k in SKINNY_NK:
+    for _m in SKINNY_M:
+        _add(Workload(f"nvfp4_skinny_m{_m}_n{_n}_k{_k}", "nvfp4", _m, _n, _k, "normal", 0.02,
+                      index=4))
+
+
+def seed_for(w: Workload, operand: int) -> int:
+    """operand 0 = A (activations), 1 = B (weights)."""
+    return SEED_BASE + 16 * w.index + operand + 1000 * (w.M + 7 * w.N + 13 * w.K)
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+# --------------------------------------------------------------------------
+# Encoders (inputs only)
+# --------------------------------------------------------------------------
+
+def e2m1_encode(v: torch.Tensor) -> torch.Tensor:
+    """Nearest E2M1 code (ties to even mantissa, saturating at 6), uint8 0..15."""
+    mag = v.abs()
+    idx = ((mag > 0.25).to(torch.uint8) + (mag >= 0.75).to(torch.uint8)
+           + (mag > 1.25).to(torch.uint8) + (mag >= 1.75).to(torch.uint8)
+           + (mag > 2.5).to(torch.uint8) + (mag >= 3.5).to(torch.uint8)
+           + (mag > 5.0).to(torch.uint8))
+    return idx | ((v < 0).to(torch.uint8) << 3)
+
+
+def pack_e2m1(codes: torch.Tensor) -> torch.Tensor:
+    """uint8 codes [rows, K] -> bytes [rows, K/2]; element 2i in the low nibble."""
+    lo = codes[:, 0::2]
+    hi = codes[:, 1::2]
+    return (lo | (hi << 4)).contiguous()
+
+
+def unpack_e2m1(packed: torch.Tensor) -> torch.Tensor:
+    """bytes [rows, K/2] -> uint8 codes [rows, K] (inverse of ``pack_e2m1``)."""
+    rows, half = packed.shape
+    out = torch.empty((rows, 2 * half), dtype=torch.uint8, device=packed.device)
+    out[:, 0::2] = packed & 15
+    out[:, 1::2] = packed >> 4
+    return out
+
+
+def e4m3_encode(v: torch.Tensor) -> torch.Tensor:
+    """Nearest E4M3 code (ties to even) of values clamped to [-448, 448]."""
+    return v.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def nvfp4_quantise(x: torch.Tensor):
+    """Two-level NVFP4 encoding of float32 x[rows, K] -> (packed, sf, s_g)."""
+    rows, K = x.shape
+    amax = x.abs().amax().float()
+    s_g = torch.where(amax > 0, (448.0 * 6.0) / amax, torch.ones_like(amax)).float()
+    xb = x.reshape(rows, K // 16, 16)
+    bmax = xb.abs().amax(-1)
+    sf = e4m3_encode((bmax / 6.0 * s_g).clamp(max=448.0))
+    sf_val = sf.view(torch.float8_e4m3fn).to(torch.float32)
+    safe = torch.where(sf_val > 0, sf_val, torch.ones_like(sf_val))
+    scaled = xb * s_g / safe.unsqueeze(-1)
+    codes = e2m1_encode(scaled)
+    codes = torch.where((sf_val > 0).unsqueeze(-1), codes, torch.zeros_like(codes))
+    return pack_e2m1(codes.reshape(rows, K)), sf.contiguous(), float(s_g)
+
+
+def normal_bf16(rows: int, K: int, seed: int, std: float, device) -> torch.Tensor:
+    """N(0, std^2) float32, rounded through BF16 as the source activations."""
+    x = torch.randn((rows, K), generator=_gen(seed, device), device=device, dtype=torch.float32)
+    if std != 1.0:
+        x = x * std
+    return x.to(torch.bfloat16).to(torch.float32)
+
+
+def uniform_nvfp4(rows: int, K: int, seed: int, device):
+    """All 16 E2M1 codes uniformly; block scales 2^u, u uniform in [-4, 4]."""
+    g = _gen(seed, device)
+    packed = torch.randint(0, 256, (rows, K // 2), generator=g, device=device,
+                           dtype=torch.int32).to(torch.uint8)
+    u = torch.randint(-4, 5, (rows, K // 16), generator=g, device=device, dtype=torch.int32)
+    sf = ((u + 7) << 3).to(torch.uint8)   # E4M3 code of 2^u: exponent field u+7
+    return packed, sf
+
+
+# --------------------------------------------------------------------------
+# Whole problems
+# --------------------------------------------------------------------------
+
+def make_nvfp4(w: Workload, device="cpu", M: int | None = None, N: int | None = None,
+               K: int | None = None) -> dict:
+    """A, sfA, B, sfB (uint8 tensors on ``device``) and alpha for workload w.
+
+    M, N, K override the workload's sizes (same recipe, e.g. for ragged tests).
+    """
+    M = w.M if M is None else M
+    N = w.N if N is None else N
+    K = w.K if K is None else K
+    if w.dist == "uniform_codes":
+        A, sfA = uniform_nvfp4(M, K, seed_for(w, 0), device)
+        B, sfB = uniform_nvfp4(N, K, seed_for(w, 1), device)
+        alpha = 1.0
+    else:
+        A, sfA, sga = nvfp4_quantise(normal_bf16(M, K, seed_for(w, 0), w.std, device))
+        B, sfB, sgb = nvfp4_quantise(normal_bf16(N, K, seed_for(w, 1), w.std, device))
+        alpha = float(torch.tensor(1.0, dtype=torch.float32)
+                      / (torch.tensor(sga, dtype=torch.float32) * torch.tensor(sgb, dtype=torch.float32)))
+    return dict(M=M, N=N, K=K, A=A, sfA=sfA, B=B, sfB=sfB, alpha=alpha)
+
+
+def make_fp8(w: Workload, device="cpu", M: int | None = None, N: int | None = None,
+             K: int | None = None) -> dict:
+    """E4M3 A, B (uint8) with alpha = s_A * s_B, s = amax/448 per tensor."""
+    M = w.M if M is None else M
+    N = w.N if N is None else N
+    K = w.K if K is None else K
+    out = dict(M=M, N=N, K=K)
+    scales = []
+    for name, rows, op in (("A", M, 0), ("B", N, 1)):
+        x = normal_bf16(rows, K, seed_for(w, op), w.std, device)
+        amax = x.abs().amax().float()
+        s = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).float()
+        out[name] = e4m3_encode(x / s).contiguous()
+        scales.append(s)
+    out["alpha"] = float((scales[0] * scales[1]).float())
+    return out
