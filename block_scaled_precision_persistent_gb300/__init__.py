@@ -1,0 +1,171 @@
+"""Block-scaled NVFP4 / FP8 GEMM for one GB300 GPU (sm_103a).
+
+    D = alpha * (A (.) sA)(B (.) sB)^T      FP32 accumulation, BF16 output
+
+Thin Python binding of the C ABI in ``include/bsgemm.h`` (``libbsgemm.so``,
+built in-tree by ``_build.build()``). Every function here has the name of its
+C entry point and only marshals arguments: tensors become device pointers,
+``stream=None`` becomes PyTorch's current CUDA stream, and a non-zero status
+raises :class:`BsgError`. All arithmetic runs in the library's CUDA kernels;
+there is no fallback. If the library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+__all__ = [
+    "BsgError", "load", "nvfp4_gemm", "nvfp4_gemm_swizzled", "nvfp4_swizzle_scales",
+    "nvfp4_swizzled_scale_bytes", "fp8_gemm", "bsg_reserve_workspace", "bsg_get_device_status",
+    "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_watchdog_selftest", "bsg_force_plan",
+    "bsg_select_plan", "bsg_last_launch_count", "bsg_error_string", "EXPORTED_SYMBOLS",
+    "BSG_OK", "BSG_ERR_INVALID_ARG", "BSG_ERR_MISALIGNED", "BSG_ERR_UNSUPPORTED_DEVICE",
+    "BSG_ERR_NO_PLAN", "BSG_ERR_CUDA", "BSG_ERR_DEVICE_TIMEOUT", "BSG_ERR_OUT_OF_MEMORY",
+]
+
+BSG_OK = 0
+BSG_ERR_INVALID_ARG = 1
+BSG_ERR_MISALIGNED = 2
+BSG_ERR_UNSUPPORTED_DEVICE = 3
+BSG_ERR_NO_PLAN = 4
+BSG_ERR_CUDA = 5
+BSG_ERR_DEVICE_TIMEOUT = 6
+BSG_ERR_OUT_OF_MEMORY = 7
+
+LIB_PATH = Path(__file__).resolve().parent / "libbsgemm.so"
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+# name -> (restype, argtypes), in the order of include/bsgemm.h
+_SIGNATURES = {
+    "nvfp4_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
+    "nvfp4_gemm_swizzled": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
+    "nvfp4_swizzle_scales": (_i, [_i, _i, _vp, _vp, _vp]),
+    "nvfp4_swizzled_scale_bytes": (ctypes.c_size_t, [_i, _i]),
+    "fp8_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
+    "bsg_reserve_workspace": (_i, [_i, ctypes.c_size_t]),
+    "bsg_get_device_status": (_i, [_vp]),
+    "bsg_last_status_word": (ctypes.c_uint32, []),
+    "bsg_set_watchdog_ns": (_i, [ctypes.c_uint64]),
+    "bsg_watchdog_selftest": (_i, [ctypes.c_uint64, _vp]),
+    "bsg_force_plan": (_i, [ctypes.c_char_p]),
+    "bsg_select_plan": (_i, [_i, _i, _i, _i, _i, ctypes.c_char_p, ctypes.c_size_t]),
+    "bsg_last_launch_count": (_i, []),
+    "bsg_error_string": (ctypes.c_char_p, [_i]),
+}
+EXPORTED_SYMBOLS = tuple(_SIGNATURES)
+
+_lib: ctypes.CDLL | None = None
+
+
+class BsgError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {bsg_error_string(code)} (status {code})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libbsgemm.so (built in-tree). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise ImportError(f"{LIB_PATH.name} is not built; run __graft_entry__.build() "
+                              "(or python -m block_scaled_precision_persistent_gb300._build)")
+        lib = ctypes.CDLL(str(LIB_PATH))
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream) if torch.cuda.is_available() else None
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != BSG_OK:
+        raise BsgError(rc, where)
+
+
+def nvfp4_gemm(M, N, K, A, sfA, B, sfB, alpha, D, stream=None) -> None:
+    """D[M,N] bf16 = alpha * (A*sA)(B*sB)^T with row-major uint8[rows, K/16] scales."""
+    _check(load().nvfp4_gemm(M, N, K, _ptr(A), _ptr(sfA), _ptr(B), _ptr(sfB), float(alpha),
+                             _ptr(D), _stream(stream)), "nvfp4_gemm")
+
+
+def nvfp4_gemm_swizzled(M, N, K, A, sfA_swz, B, sfB_swz, alpha, D, stream=None) -> None:
+    """As nvfp4_gemm, with scales already in the swizzled layout."""
+    _check(load().nvfp4_gemm_swizzled(M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), _ptr(sfB_swz),
+                                      float(alpha), _ptr(D), _stream(stream)), "nvfp4_gemm_swizzled")
+
+
+def nvfp4_swizzle_scales(rows, K, sf, sf_swz, stream=None) -> None:
+    _check(load().nvfp4_swizzle_scales(rows, K, _ptr(sf), _ptr(sf_swz), _stream(stream)),
+           "nvfp4_swizzle_scales")
+
+
+def nvfp4_swizzled_scale_bytes(rows, K) -> int:
+    return int(load().nvfp4_swizzled_scale_bytes(rows, K))
+
+
+def fp8_gemm(M, N, K, A, sA, B, sB, alpha, D, stream=None) -> None:
+    """D = alpha*sA*sB * A B^T, E4M3 operands; sA/sB device float tensors or None."""
+    _check(load().fp8_gemm(M, N, K, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), float(alpha), _ptr(D),
+                           _stream(stream)), "fp8_gemm")
+
+
+def bsg_reserve_workspace(device: int, nbytes: int) -> None:
+    _check(load().bsg_reserve_workspace(device, nbytes), "bsg_reserve_workspace")
+
+
+def bsg_get_device_status(stream=None) -> int:
+    """Synchronise and return (and clear) the device status code; does not raise."""
+    return int(load().bsg_get_device_status(_stream(stream)))
+
+
+def bsg_last_status_word() -> int:
+    return int(load().bsg_last_status_word())
+
+
+def bsg_set_watchdog_ns(ns: int) -> None:
+    _check(load().bsg_set_watchdog_ns(ns), "bsg_set_watchdog_ns")
+
+
+def bsg_watchdog_selftest(ns: int, stream=None) -> None:
+    _check(load().bsg_watchdog_selftest(ns, _stream(stream)), "bsg_watchdog_selftest")
+
+
+def bsg_force_plan(name: str | None) -> None:
+    _check(load().bsg_force_plan(name.encode() if name else None), "bsg_force_plan")
+
+
+def bsg_select_plan(kind: int, M: int, N: int, K: int, num_sms: int) -> str:
+    buf = ctypes.create_string_buffer(128)
+    _check(load().bsg_select_plan(kind, M, N, K, num_sms, buf, len(buf)), "bsg_select_plan")
+    return buf.value.decode()
+
+
+def bsg_last_launch_count() -> int:
+    return int(load().bsg_last_launch_count())
+
+
+def bsg_error_string(code: int) -> str:
+    try:
+        return load().bsg_error_string(code).decode()
+    except ImportError:
+        return f"status {code}"

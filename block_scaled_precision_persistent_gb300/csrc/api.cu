@@ -1,0 +1,418 @@
+// C ABI of the library: argument validation, the shape planner, tensor-map
+// encoding, the nvfp4_gemm scale workspace, the device status word.
+// Declarations and their contracts are in include/bsgemm.h.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "bsg_internal.h"
+#include "bsgemm.h"
+
+// Device status word written by bounded waits that run out (one per device).
+__device__ unsigned int g_bsg_status_word;
+
+namespace {
+
+using bsg::GemmArgs;
+using bsg::GemmMaps;
+using bsg::Kind;
+using bsg::PlanInfo;
+
+constexpr unsigned long long kDefaultWatchdogNs = 1000000000ull;
+constexpr int kMaxDevices = 64;
+
+std::atomic<unsigned long long> g_watchdog_ns{kDefaultWatchdogNs};
+std::mutex g_mu;
+int g_forced_plan = -1;                 // guarded by g_mu
+thread_local uint32_t t_last_status_word = 0;
+thread_local int t_last_launches = 0;
+
+struct DeviceState {
+    bool init = false;
+    int rc = BSG_OK;
+    int sms = 0;
+    unsigned int *status = nullptr;     // device address of g_bsg_status_word
+    uint8_t *ws = nullptr;              // nvfp4_gemm scale workspace
+    size_t ws_bytes = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// State of the current device, initialised once: compute capability check,
+// SM count, status-word address.
+int current_device(DeviceState **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return BSG_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.init) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            d.rc = BSG_ERR_CUDA;
+        } else if (major != 10 || minor != 3) {
+            d.rc = BSG_ERR_UNSUPPORTED_DEVICE;
+        } else if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_bsg_status_word) !=
+                   cudaSuccess) {
+            d.rc = BSG_ERR_CUDA;
+        } else {
+            d.rc = BSG_OK;
+        }
+        d.init = true;
+    }
+    *out = &d;
+    return d.rc;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t swizzled_bytes(int rows, int K)
+{
+    if (rows < 1 || K < 16 || (K % 16) != 0)
+        return 0;
+    const size_t pr = ((size_t)rows + 127u) / 128u * 128u;
+    const size_t pc = ((size_t)(K / 16) + 3u) / 4u * 4u;
+    return pr * pc;
+}
+
+// Planner: the default plan for a shape; -1 if none fits.
+int default_plan(Kind kind, int M, int N, int K, int num_sms)
+{
+    (void)M;
+    (void)K;
+    (void)num_sms;
+    const char *name = nullptr;
+    if (kind == Kind::NVFP4)
+        name = N <= 128 ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc1_128x256_s3_acc1";
+    else
+        name = N <= 128 ? "fp8_tc1_128x128_s6_acc2" : "fp8_tc1_128x256_s4_acc2";
+    return bsg::find_plan(name);
+}
+
+int choose_plan(Kind kind, int M, int N, int K, int num_sms, int *plan)
+{
+    int forced;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        forced = g_forced_plan;
+    }
+    if (forced >= 0) {
+        if (bsg::plan_info(forced).kind != kind)
+            return BSG_ERR_NO_PLAN;
+        *plan = forced;
+        return BSG_OK;
+    }
+    *plan = default_plan(kind, M, N, K, num_sms);
+    return *plan >= 0 ? BSG_OK : BSG_ERR_NO_PLAN;
+}
+
+int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *ptr, uint64_t inner,
+              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return BSG_ERR_CUDA;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t elem_strides[2] = {1, 1};
+    CUresult r = fn(map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, elem_strides,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BSG_OK : BSG_ERR_CUDA;
+}
+
+// Encode the maps and launch one persistent GEMM.
+int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const uint8_t *sfa,
+             const uint8_t *sfb, const float *sA, const float *sB, float alpha, void *D,
+             cudaStream_t stream, DeviceState *ds)
+{
+    int plan = -1;
+    int rc = choose_plan(kind, M, N, K, ds->sms, &plan);
+    if (rc != BSG_OK)
+        return rc;
+    const PlanInfo &pi = bsg::plan_info(plan);
+    const uint64_t row_bytes = kind == Kind::NVFP4 ? (uint64_t)K / 2u : (uint64_t)K;
+
+    GemmMaps maps;
+    if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes,
+                        128, (uint32_t)pi.bm)) != BSG_OK ||
+        (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, (uint64_t)N, row_bytes,
+                        128, (uint32_t)pi.bn)) != BSG_OK ||
+        (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)M,
+                        (uint64_t)N * 2u, 64, 32)) != BSG_OK)
+        return rc;
+
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.num_m_tiles = (M + pi.bm - 1) / pi.bm;
+    a.num_n_tiles = (N + pi.bn - 1) / pi.bn;
+    a.num_k_blocks = K / pi.k_block;
+    a.raster_group = 8;
+    a.sf_col_blocks = (K / 16 + 3) / 4;
+    a.sfb_row_blocks = (N + 127) / 128;
+    a.sfa = sfa;
+    a.sfb = sfb;
+    a.alpha = alpha;
+    a.sA = sA;
+    a.sB = sB;
+    a.status = ds->status;
+    a.timeout_ns = g_watchdog_ns.load();
+    const long long tiles = (long long)a.num_m_tiles * a.num_n_tiles;
+    const int grid = (int)(tiles < ds->sms ? tiles : ds->sms);
+    cudaError_t e = bsg::launch_gemm(plan, maps, a, grid, stream);
+    if (e != cudaSuccess)
+        return BSG_ERR_CUDA;
+    ++t_last_launches;
+    return BSG_OK;
+}
+
+int check_nvfp4_args(int M, int N, int K, const void *A, const void *sfA, const void *B,
+                     const void *sfB, void *D)
+{
+    if (!A || !sfA || !B || !sfB || !D)
+        return BSG_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 256 || (K % 256) != 0 || (N % 8) != 0)
+        return BSG_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(sfA) || !aligned16(B) || !aligned16(sfB) || !aligned16(D))
+        return BSG_ERR_MISALIGNED;
+    return BSG_OK;
+}
+
+// Grow the workspace of the current device (caller holds no lock).
+int ensure_workspace(DeviceState *ds, size_t bytes)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (ds->ws_bytes >= bytes)
+        return BSG_OK;
+    if (ds->ws) {
+        cudaFree(ds->ws);   // synchronises the device: no pending work still reads it
+        ds->ws = nullptr;
+        ds->ws_bytes = 0;
+    }
+    if (cudaMalloc(reinterpret_cast<void **>(&ds->ws), bytes) != cudaSuccess) {
+        cudaGetLastError();
+        ds->ws = nullptr;
+        return BSG_ERR_OUT_OF_MEMORY;
+    }
+    ds->ws_bytes = bytes;
+    return BSG_OK;
+}
+
+size_t round256(size_t x) { return (x + 255u) & ~(size_t)255u; }
+
+}  // namespace
+
+namespace bsg {
+int find_plan(const char *name)
+{
+    if (!name)
+        return -1;
+    for (int i = 0; i < num_plans(); ++i)
+        if (std::strcmp(plan_info(i).name, name) == 0)
+            return i;
+    return -1;
+}
+}  // namespace bsg
+
+extern "C" {
+
+int nvfp4_gemm_swizzled(int M, int N, int K, const void *A, const void *sfA_swz, const void *B,
+                        const void *sfB_swz, float alpha, void *D, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    int rc = check_nvfp4_args(M, N, K, A, sfA_swz, B, sfB_swz, D);
+    if (rc != BSG_OK)
+        return rc;
+    DeviceState *ds = nullptr;
+    if ((rc = current_device(&ds)) != BSG_OK)
+        return rc;
+    return run_gemm(Kind::NVFP4, M, N, K, A, B, static_cast<const uint8_t *>(sfA_swz),
+                    static_cast<const uint8_t *>(sfB_swz), nullptr, nullptr, alpha, D,
+                    reinterpret_cast<cudaStream_t>(stream), ds);
+}
+
+int nvfp4_gemm(int M, int N, int K, const void *A, const void *sfA, const void *B, const void *sfB,
+               float alpha, void *D, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    int rc = check_nvfp4_args(M, N, K, A, sfA, B, sfB, D);
+    if (rc != BSG_OK)
+        return rc;
+    DeviceState *ds = nullptr;
+    if ((rc = current_device(&ds)) != BSG_OK)
+        return rc;
+    const size_t bytes_a = round256(swizzled_bytes(M, K));
+    const size_t bytes_b = round256(swizzled_bytes(N, K));
+    if ((rc = ensure_workspace(ds, bytes_a + bytes_b)) != BSG_OK)
+        return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *swz_a = ds->ws;
+    uint8_t *swz_b = ds->ws + bytes_a;
+    if (bsg::launch_swizzle_scales(M, K, static_cast<const uint8_t *>(sfA), swz_a, s) != cudaSuccess ||
+        bsg::launch_swizzle_scales(N, K, static_cast<const uint8_t *>(sfB), swz_b, s) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    t_last_launches = 2;
+    return run_gemm(Kind::NVFP4, M, N, K, A, B, swz_a, swz_b, nullptr, nullptr, alpha, D, s, ds);
+}
+
+int nvfp4_swizzle_scales(int rows, int K, const void *sf, void *sf_swz, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    if (!sf || !sf_swz || rows < 1 || K < 16 || (K % 16) != 0)
+        return BSG_ERR_INVALID_ARG;
+    if (!aligned16(sf_swz))
+        return BSG_ERR_MISALIGNED;
+    DeviceState *ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc != BSG_OK)
+        return rc;
+    if (bsg::launch_swizzle_scales(rows, K, static_cast<const uint8_t *>(sf),
+                                   static_cast<uint8_t *>(sf_swz),
+                                   reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    t_last_launches = 1;
+    return BSG_OK;
+}
+
+size_t nvfp4_swizzled_scale_bytes(int rows, int K) { return swizzled_bytes(rows, K); }
+
+int fp8_gemm(int M, int N, int K, const void *A, const float *sA, const void *B, const float *sB,
+             float alpha, void *D, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    if (!A || !B || !D)
+        return BSG_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 128 || (K % 128) != 0 || (N % 8) != 0)
+        return BSG_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) ||
+        (sA && (reinterpret_cast<uintptr_t>(sA) & 3u)) || (sB && (reinterpret_cast<uintptr_t>(sB) & 3u)))
+        return BSG_ERR_MISALIGNED;
+    DeviceState *ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc != BSG_OK)
+        return rc;
+    return run_gemm(Kind::FP8, M, N, K, A, B, nullptr, nullptr, sA, sB, alpha, D,
+                    reinterpret_cast<cudaStream_t>(stream), ds);
+}
+
+int bsg_reserve_workspace(int device, size_t bytes)
+{
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    DeviceState *ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc == BSG_OK)
+        rc = ensure_workspace(ds, bytes);
+    cudaSetDevice(prev);
+    return rc;
+}
+
+int bsg_get_device_status(bsg_stream_t stream)
+{
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    DeviceState *ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc != BSG_OK)
+        return rc;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, ds->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(ds->status, 0, sizeof v) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        return BSG_ERR_CUDA;
+    t_last_status_word = v;
+    if (e != cudaSuccess)
+        return BSG_ERR_CUDA;
+    return v ? BSG_ERR_DEVICE_TIMEOUT : BSG_OK;
+}
+
+uint32_t bsg_last_status_word(void) { return t_last_status_word; }
+
+int bsg_set_watchdog_ns(uint64_t ns)
+{
+    g_watchdog_ns.store(ns ? (unsigned long long)ns : kDefaultWatchdogNs);
+    return BSG_OK;
+}
+
+int bsg_watchdog_selftest(uint64_t ns, bsg_stream_t stream)
+{
+    if (ns == 0)
+        return BSG_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc != BSG_OK)
+        return rc;
+    if (bsg::launch_watchdog_probe(ds->status, (unsigned long long)ns,
+                                   reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    return BSG_OK;
+}
+
+int bsg_force_plan(const char *name)
+{
+    int id = -1;
+    if (name && name[0]) {
+        id = bsg::find_plan(name);
+        if (id < 0)
+            return BSG_ERR_NO_PLAN;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_forced_plan = id;
+    return BSG_OK;
+}
+
+int bsg_select_plan(int kind, int M, int N, int K, int num_sms, char *name, size_t name_len)
+{
+    if ((kind != 0 && kind != 1) || M < 1 || N < 1 || K < 1 || num_sms < 1 || !name || name_len == 0)
+        return BSG_ERR_INVALID_ARG;
+    int plan = -1;
+    int rc = choose_plan(kind == 0 ? Kind::NVFP4 : Kind::FP8, M, N, K, num_sms, &plan);
+    if (rc != BSG_OK)
+        return rc;
+    std::strncpy(name, bsg::plan_info(plan).name, name_len - 1);
+    name[name_len - 1] = '\0';
+    return BSG_OK;
+}
+
+int bsg_last_launch_count(void) { return t_last_launches; }
+
+const char *bsg_error_string(int code)
+{
+    switch (code) {
+    case BSG_OK: return "ok";
+    case BSG_ERR_INVALID_ARG: return "invalid argument";
+    case BSG_ERR_MISALIGNED: return "misaligned pointer (16-byte alignment required)";
+    case BSG_ERR_UNSUPPORTED_DEVICE: return "unsupported device (compute capability 10.3 required)";
+    case BSG_ERR_NO_PLAN: return "no kernel plan for this request";
+    case BSG_ERR_CUDA: return "CUDA error";
+    case BSG_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case BSG_ERR_OUT_OF_MEMORY: return "workspace allocation failed";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// Internal host/device interface between the C ABI (api.cu) and the kernel
+// translation units. Not part of the public header.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bsg {
+
+enum class Kind : int { NVFP4 = 0, FP8 = 1 };
+
+// Everything a persistent GEMM launch needs besides its tensor maps.
+struct GemmArgs {
+    int M, N, K;
+    int num_m_tiles, num_n_tiles, num_k_blocks;
+    int raster_group;          // M tiles per rasterisation group
+    int sf_col_blocks;         // NVFP4: 4-scale column blocks per 128-row block (K/64)
+    int sfb_row_blocks;        // NVFP4: 128-row blocks of the swizzled B scales
+    const uint8_t *sfa;        // NVFP4: swizzled A scales
+    const uint8_t *sfb;        // NVFP4: swizzled B scales
+    float alpha;
+    const float *sA;           // FP8 per-tensor scales (device, may be null)
+    const float *sB;
+    unsigned int *status;      // device status word
+    unsigned long long timeout_ns;
+};
+
+// One compiled persistent-kernel configuration.
+struct PlanInfo {
+    const char *name;
+    Kind kind;
+    int bm, bn;                // CTA tile
+    int stages;                // smem ring depth
+    int num_acc;               // TMEM accumulator buffers
+    int k_block;               // K elements per ring stage
+    int smem_bytes;            // dynamic shared memory per CTA
+    int threads;
+    int tmem_cols;
+};
+
+int num_plans();
+const PlanInfo &plan_info(int id);
+int find_plan(const char *name);
+
+// Encoded tensor maps of one call.
+struct GemmMaps {
+    CUtensorMap a, b, d;
+};
+
+// Launch plan `id` with `grid` persistent CTAs. Returns a cudaError_t.
+cudaError_t launch_gemm(int id, const GemmMaps &maps, const GemmArgs &args, int grid,
+                        cudaStream_t stream);
+
+// Scale-layout prep kernel. Returns a cudaError_t.
+cudaError_t launch_swizzle_scales(int rows, int K, const uint8_t *sf, uint8_t *out,
+                                  cudaStream_t stream);
+
+// Watchdog probe: waits on an mbarrier nothing arrives on.
+cudaError_t launch_watchdog_probe(unsigned int *status, unsigned long long ns,
+                                  cudaStream_t stream);
+
+}  // namespace bsg

@@ -1,0 +1,436 @@
+// Persistent, warp-specialised block-scaled GEMM on the 5th-generation tensor
+// cores of sm_103a:
+//
+//     D[M][N] = bf16( alpha * sum_k (A[m][k] * sA) (B[n][k] * sB) )
+//
+// Design ("Together AI Ports ThunderKittens GEMM Kernels to NVIDIA Vera Rubin
+// NVL72", introduction): a loader warp streams A and B tiles into a ring of
+// shared-memory stages with TMA, one MMA thread drives tcgen05.mma with the
+// accumulator in tensor memory, and an epilogue warpgroup drains finished
+// accumulators to HBM; the kernel is persistent, so the next tile's loads
+// stream in while the previous tile's outputs drain. For NVFP4 the block
+// scales are copied from shared memory into tensor memory (tcgen05.cp) next
+// to the accumulators ("Building the GEMM": the scale factors need TMEM
+// columns beside the accumulators, which bounds the tile shape within the
+// 512 columns of this GPU).
+//
+// CTA roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer (one elected lane)
+//   warp 1      TMEM allocator + MMA issuer (one elected lane)
+//   warps 2..5  epilogue: TMEM -> registers -> *alpha -> BF16 -> swizzled
+//               smem -> TMA store; warp w reads TMEM lanes 32*(w%4)..+31
+//
+// Every mbarrier wait is bounded (see ptx.cuh): a wait that runs out records
+// BSG_ERR_DEVICE_TIMEOUT in the status word and the CTA drains and exits.
+#include <cuda_bf16.h>
+
+#include "bsg_internal.h"
+#include "ptx.cuh"
+
+namespace bsg {
+
+template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+struct Tile {
+    static constexpr bool kFp4 = KIND == Kind::NVFP4;
+    static constexpr int BM = 128;
+    static constexpr int ROW_BYTES = 128;                 // K bytes of one row per stage
+    static constexpr int K_BLOCK = kFp4 ? 256 : 128;      // K elements per stage
+    static constexpr int MMA_K_BYTES = 32;                // K bytes per tcgen05.mma
+    static constexpr int MMAS = ROW_BYTES / MMA_K_BYTES;  // MMAs per stage
+    static constexpr int A_BYTES = BM * ROW_BYTES;
+    static constexpr int B_BYTES = BN * ROW_BYTES;
+    // NVFP4 scales of one stage: 128 rows x 16 scales = four 512-byte blocks
+    static constexpr int SF_BLOCK_BYTES = 2048;
+    static constexpr int SFB_CHUNKS = kFp4 ? BN / 128 : 0;
+    static constexpr int SFA_BYTES = kFp4 ? SF_BLOCK_BYTES : 0;
+    static constexpr int SFB_BYTES = SFB_CHUNKS * SF_BLOCK_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_COLS = 64;                   // BF16 columns per store box
+    static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
+    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    // TMEM columns: NUM_ACC accumulators of BN columns, then one set of scale
+    // columns per ring stage (a stage's scales are overwritten only after the
+    // MMAs that read them completed, which the ring's empty barrier proves).
+    static constexpr int SFA_COLS = kFp4 ? 4 * MMAS : 0;
+    static constexpr int SFB_COLS = kFp4 ? 4 * SFB_CHUNKS * MMAS : 0;
+    static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
+    static constexpr int TMEM_USED = NUM_ACC * BN + STAGES * SF_COLS;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
+                                     : TMEM_USED <= 64  ? 64
+                                     : TMEM_USED <= 128 ? 128
+                                     : TMEM_USED <= 256 ? 256
+                                                        : 512;
+    static constexpr uint32_t IDESC = kFp4 ? idesc_nvfp4(BM, BN) : idesc_fp8(BM, BN);
+
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile N");
+    static_assert(!kFp4 || BN % 128 == 0, "NVFP4 scale blocks cover 128 rows");
+    static_assert(TMEM_USED <= 512, "TMEM: accumulators plus scales exceed 512 columns");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
+};
+
+// Tile id -> (m tile, n tile): groups of `raster_group` M tiles; inside a
+// group the M tile varies fastest, so the CTAs resident at one time share a
+// few A panels and a band of B panels in L2 ("Building the GEMM": tile
+// rasterisation order permuted for memory locality).
+__device__ __forceinline__ void raster_tile(int tile, const GemmArgs &a, int &mt, int &nt)
+{
+    const int per_group = a.raster_group * a.num_n_tiles;
+    const int g = tile / per_group;
+    const int first_m = g * a.raster_group;
+    const int gm = min(a.raster_group, a.num_m_tiles - first_m);
+    const int local = tile - g * per_group;
+    mt = first_m + local % gm;
+    nt = local / gm;
+}
+
+// Bounded wait with no status side effect, used only while draining.
+__device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity,
+                                                unsigned long long limit_ns)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > limit_ns)
+            return;
+}
+
+// Lane 0 waits (bounded); the verdict is broadcast so the warp stays
+// converged for the .sync.aligned tcgen05 loads that follow.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Watchdog &wd,
+                                          volatile int *abort_flag, uint32_t site, int lane)
+{
+    int ok = 0;
+    if (lane == 0)
+        ok = mbar_wait(bar, parity, wd, abort_flag, site) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok && lane != 0)
+        mbar_wait_quiet(bar, parity, wd.limit_ns);   // already complete: returns at once
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+__global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
+    gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmD, const GemmArgs args)
+{
+    using T = Tile<KIND, BN, STAGES, NUM_ACC>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const uint32_t s_epi = base + STAGES * T::STAGE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + STAGES * T::STAGE_BYTES + T::EPI_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t full0 = bar0;                              // [STAGES] TMA -> MMA
+    const uint32_t empty0 = bar0 + 8u * STAGES;               // [STAGES] MMA -> TMA
+    const uint32_t tfull0 = bar0 + 16u * STAGES;              // [NUM_ACC] MMA -> epilogue
+    const uint32_t tempty0 = tfull0 + 8u * NUM_ACC;           // [NUM_ACC] epilogue -> MMA
+    const uint32_t drain_bar = tempty0 + 8u * NUM_ACC;        // MMA teardown
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const Watchdog wd{args.status, args.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+        }
+        for (int a = 0; a < NUM_ACC; ++a) {
+            mbar_init(tfull0 + 8u * a, 1);
+            mbar_init(tempty0 + 8u * a, T::EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmD);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int num_tiles = args.num_m_tiles * args.num_n_tiles;
+    const int nkb = args.num_k_blocks;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------
+        // TMA producer
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, armed_mask = 0, armed_parity = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                int mt, nt;
+                raster_tile(tile, args, mt, nt);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wd, abort_flag, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * T::STAGE_BYTES;
+                    const uint32_t sb = sa + T::A_BYTES;
+                    const uint32_t fb = full0 + 8u * stage;
+                    uint32_t bytes = T::A_BYTES + T::B_BYTES;
+                    int nchunks = 0;
+                    if constexpr (T::kFp4) {
+                        nchunks = min(T::SFB_CHUNKS, args.sfb_row_blocks - nt * T::SFB_CHUNKS);
+                        bytes += T::SF_BLOCK_BYTES * (1 + nchunks);
+                    }
+                    mbar_arrive_expect_tx(fb, bytes);
+                    tma_load_2d(sa, &tmA, fb, kb * T::ROW_BYTES, mt * T::BM);
+                    tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN);
+                    if constexpr (T::kFp4) {
+                        // the stage's 16 scale columns are 4 consecutive
+                        // 512-byte blocks of the swizzled layout
+                        const uint32_t ssfa = sb + T::B_BYTES;
+                        const size_t cb = (size_t)kb * 4u;
+                        bulk_load(ssfa, args.sfa + ((size_t)mt * args.sf_col_blocks + cb) * 512u,
+                                  T::SF_BLOCK_BYTES, fb);
+                        for (int c = 0; c < nchunks; ++c) {
+                            const size_t rb = (size_t)nt * T::SFB_CHUNKS + (size_t)c;
+                            bulk_load(ssfa + T::SFA_BYTES + c * T::SF_BLOCK_BYTES,
+                                      args.sfb + (rb * args.sf_col_blocks + cb) * 512u,
+                                      T::SF_BLOCK_BYTES, fb);
+                        }
+                    }
+                    armed_mask |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let copies already issued land before the CTA goes away
+                for (int s = 0; s < STAGES; ++s)
+                    if ((armed_mask >> s) & 1u)
+                        mbar_wait_quiet(full0 + 8u * s, (armed_parity >> s) & 1u, wd.limit_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------
+        // MMA issuer
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                if (!mbar_wait(tempty0 + 8u * acc, acc_phase ^ 1u, wd, abort_flag, 2)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(full0 + 8u * stage, phase, wd, abort_flag, 3)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = base + stage * T::STAGE_BYTES;
+                    const uint32_t sb = sa + T::A_BYTES;
+                    if constexpr (T::kFp4) {
+                        const uint32_t sfa_t = tmem + (uint32_t)(NUM_ACC * BN + stage * T::SF_COLS);
+                        const uint32_t sfb_t = sfa_t + T::SFA_COLS;
+                        const uint32_t ssfa = sb + T::B_BYTES;
+                        const uint32_t ssfb = ssfa + T::SFA_BYTES;
+#pragma unroll
+                        for (int j = 0; j < T::MMAS; ++j) {
+                            tc_cp_32x128b_warpx4(sfa_t + 4u * j, desc_scale_32x16(ssfa + 512u * j));
+#pragma unroll
+                            for (int c = 0; c < T::SFB_CHUNKS; ++c)
+                                tc_cp_32x128b_warpx4(sfb_t + 4u * (j * T::SFB_CHUNKS + c),
+                                                     desc_scale_32x16(ssfb + T::SF_BLOCK_BYTES * c + 512u * j));
+                        }
+#pragma unroll
+                        for (int j = 0; j < T::MMAS; ++j)
+                            mma_nvfp4(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
+                                      desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                      sfa_t + 4u * j, sfb_t + 4u * j * T::SFB_CHUNKS,
+                                      (kb | j) != 0 ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < T::MMAS; ++j)
+                            mma_fp8(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
+                                    desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                    (kb | j) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(empty0 + 8u * stage);   // frees the stage once these MMAs finish
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                tc_commit(tfull0 + 8u * acc);         // accumulator ready for the epilogue
+                if (++acc == NUM_ACC) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // every MMA and copy issued above completes before TMEM is freed
+            tc_commit(drain_bar);
+            mbar_wait_quiet(drain_bar, 0, wd.limit_ns);
+        }
+    } else {
+        // ------------------------------------------------------------------
+        // Epilogue warpgroup
+        // ------------------------------------------------------------------
+        const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const uint32_t ebuf = s_epi + (uint32_t)(warp - 2) * 2u * T::EPI_BUF_BYTES;
+        float scale = args.alpha;
+        if constexpr (!T::kFp4) {
+            if (args.sA)
+                scale *= *args.sA;
+            if (args.sB)
+                scale *= *args.sB;
+        }
+        int acc = 0, buf = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            int mt, nt;
+            raster_tile(tile, args, mt, nt);
+            if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
+                break;
+            tc_fence_after_sync();
+            const uint32_t t_acc = tmem + lane_off + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int ch = 0; ch < BN / T::EPI_COLS; ++ch) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS, v0);
+                tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS + 32, v1);
+                tmem_ld_wait();
+                if (ch == BN / T::EPI_COLS - 1) {
+                    // the whole accumulator is in registers: hand it back
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(tempty0 + 8u * acc);
+                }
+                // the store that last read this staging buffer must be done
+                if (lane == 0)
+                    bulk_wait_group_read<1>();
+                __syncwarp();
+                const uint32_t sbuf = ebuf + (uint32_t)buf * T::EPI_BUF_BYTES;
+                const uint32_t row = sbuf + (uint32_t)lane * 128u;
+                // 128-byte swizzle: 16-byte chunk c of row r lands at chunk c ^ (r % 8)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(row + ((uint32_t)(c ^ (lane & 7)) << 4),
+                                 pack_bf16x2(__uint_as_float(v0[8 * c + 0]) * scale, __uint_as_float(v0[8 * c + 1]) * scale),
+                                 pack_bf16x2(__uint_as_float(v0[8 * c + 2]) * scale, __uint_as_float(v0[8 * c + 3]) * scale),
+                                 pack_bf16x2(__uint_as_float(v0[8 * c + 4]) * scale, __uint_as_float(v0[8 * c + 5]) * scale),
+                                 pack_bf16x2(__uint_as_float(v0[8 * c + 6]) * scale, __uint_as_float(v0[8 * c + 7]) * scale));
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(row + ((uint32_t)((c + 4) ^ (lane & 7)) << 4),
+                                 pack_bf16x2(__uint_as_float(v1[8 * c + 0]) * scale, __uint_as_float(v1[8 * c + 1]) * scale),
+                                 pack_bf16x2(__uint_as_float(v1[8 * c + 2]) * scale, __uint_as_float(v1[8 * c + 3]) * scale),
+                                 pack_bf16x2(__uint_as_float(v1[8 * c + 4]) * scale, __uint_as_float(v1[8 * c + 5]) * scale),
+                                 pack_bf16x2(__uint_as_float(v1[8 * c + 6]) * scale, __uint_as_float(v1[8 * c + 7]) * scale));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int x = nt * BN + ch * T::EPI_COLS;
+                    const int y = mt * T::BM + q * 32;
+                    if (x < args.N && y < args.M)
+                        tma_store_2d(&tmD, sbuf, x, y);
+                    bulk_commit_group();
+                }
+                buf ^= 1;
+            }
+            if (++acc == NUM_ACC) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (lane == 0)
+            bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Plans: the compiled configurations and their host launchers
+// ---------------------------------------------------------------------------
+template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+static cudaError_t launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
+                               cudaStream_t stream)
+{
+    using T = Tile<KIND, BN, STAGES, NUM_ACC>;
+    auto kern = gemm_persistent_kernel<KIND, BN, STAGES, NUM_ACC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(maps.a, maps.b, maps.d, args);
+    return cudaGetLastError();
+}
+
+template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+static constexpr PlanInfo make_plan(const char *name)
+{
+    using T = Tile<KIND, BN, STAGES, NUM_ACC>;
+    return PlanInfo{name, KIND, T::BM, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES, T::THREADS,
+                    T::TMEM_COLS};
+}
+
+#define BSG_PLANS(X)                                             \
+    X(Kind::NVFP4, 256, 3, 1, "nvfp4_tc1_128x256_s3_acc1")       \
+    X(Kind::NVFP4, 128, 5, 2, "nvfp4_tc1_128x128_s5_acc2")       \
+    X(Kind::FP8, 256, 4, 2, "fp8_tc1_128x256_s4_acc2")           \
+    X(Kind::FP8, 128, 6, 2, "fp8_tc1_128x128_s6_acc2")
+
+#define BSG_PLAN_INFO(K, BN, S, A, NAME) make_plan<K, BN, S, A>(NAME),
+static const PlanInfo kPlans[] = {BSG_PLANS(BSG_PLAN_INFO)};
+#undef BSG_PLAN_INFO
+
+int num_plans() { return (int)(sizeof(kPlans) / sizeof(kPlans[0])); }
+
+const PlanInfo &plan_info(int id) { return kPlans[id]; }
+
+cudaError_t launch_gemm(int id, const GemmMaps &maps, const GemmArgs &args, int grid,
+                        cudaStream_t stream)
+{
+    int i = 0;
+#define BSG_PLAN_LAUNCH(K, BN, S, A, NAME)                         \
+    if (id == i)                                                  \
+        return launch_impl<K, BN, S, A>(maps, args, grid, stream); \
+    ++i;
+    BSG_PLANS(BSG_PLAN_LAUNCH)
+#undef BSG_PLAN_LAUNCH
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace bsg

@@ -1,0 +1,92 @@
+// Scale-layout prep: row-major E4M3 block scales uint8[rows][K/16] -> the
+// tcgen05 block-scale layout that the persistent GEMM copies straight into
+// shared memory with one bulk copy per 128 rows x 16 scales.
+//
+// "Triton #11171 - Why Two New NVFP4 Test Cases Produced Twelve Tensor-Memory
+// Failures", "Activation-scale swizzling forced the relevant persistent path":
+// the persistent Blackwell kernel consumes scales rewritten in HBM into a
+// Blackwell-specific layout. Layout (public PTX ISA, tcgen05 block scaling):
+// rows padded to 128, scale columns padded to 4; 128x4 blocks of 512 bytes,
+// row-block-major with the column block fastest; inside a block row r and
+// column c go to byte (r%32)*16 + (r/32)*4 + c. Padding is zero.
+//
+// Each output 16-byte line holds the 4-byte column-block word of rows r0,
+// r0+32, r0+64, r0+96, so the kernel is a permutation of 32-bit words: a CTA
+// stages 128 rows x 64 scale columns in shared memory with coalesced reads and
+// writes 16 contiguous 512-byte blocks. HBM-bound; bytes in = bytes out.
+#include "bsg_internal.h"
+#include "ptx.cuh"
+
+namespace bsg {
+
+constexpr int kSwzBlocksPerCta = 16;        // 4-column blocks per CTA (64 scale columns)
+constexpr int kSwzThreads = 256;
+constexpr int kSwzPitchWords = 17;          // 16 words per staged row + 1 (bank spread)
+
+__global__ void __launch_bounds__(kSwzThreads)
+    swizzle_scales_kernel(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int rows,
+                          int cols, int ncb)
+{
+    __shared__ uint32_t tile[128 * kSwzPitchWords];
+    uint8_t *t8 = reinterpret_cast<uint8_t *>(tile);
+    const int rb = blockIdx.y;
+    const int cb0 = blockIdx.x * kSwzBlocksPerCta;
+    const int c0 = cb0 * 4;
+    const int span = kSwzBlocksPerCta * 4;  // 64 scale columns
+
+    for (int i = threadIdx.x; i < 128 * span; i += kSwzThreads) {
+        const int r = i / span, b = i % span;
+        const int row = rb * 128 + r, col = c0 + b;
+        uint8_t v = 0;
+        if (row < rows && col < cols)
+            v = in[(size_t)row * (size_t)cols + (size_t)col];
+        t8[r * (kSwzPitchWords * 4) + b] = v;
+    }
+    __syncthreads();
+
+    const int nblk = min(kSwzBlocksPerCta, ncb - cb0);
+    for (int i = threadIdx.x; i < nblk * 32; i += kSwzThreads) {
+        const int blk = i >> 5, r0 = i & 31;
+        uint4 v;
+        v.x = tile[(r0 + 0) * kSwzPitchWords + blk];
+        v.y = tile[(r0 + 32) * kSwzPitchWords + blk];
+        v.z = tile[(r0 + 64) * kSwzPitchWords + blk];
+        v.w = tile[(r0 + 96) * kSwzPitchWords + blk];
+        uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)rb * (size_t)ncb + (size_t)(cb0 + blk)) * 512u);
+        dst[r0] = v;
+    }
+}
+
+cudaError_t launch_swizzle_scales(int rows, int K, const uint8_t *sf, uint8_t *out,
+                                  cudaStream_t stream)
+{
+    const int cols = K / 16;
+    const int ncb = (cols + 3) / 4;
+    const int nrb = (rows + 127) / 128;
+    dim3 grid((ncb + kSwzBlocksPerCta - 1) / kSwzBlocksPerCta, nrb);
+    swizzle_scales_kernel<<<grid, kSwzThreads, 0, stream>>>(sf, out, rows, cols, ncb);
+    return cudaGetLastError();
+}
+
+// One thread waits, with the library's bounded wait, on an mbarrier that
+// nothing arrives on: after `ns` it records the timeout and returns.
+__global__ void watchdog_probe_kernel(unsigned int *status, unsigned long long ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        const Watchdog wd{status, ns};
+        (void)mbar_wait(smem_u32(&bar), 0, wd, &abort_flag, 0xFu);
+    }
+}
+
+cudaError_t launch_watchdog_probe(unsigned int *status, unsigned long long ns, cudaStream_t stream)
+{
+    watchdog_probe_kernel<<<1, 32, 0, stream>>>(status, ns);
+    return cudaGetLastError();
+}
+
+}  // namespace bsg

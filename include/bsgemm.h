@@ -1,0 +1,162 @@
+/*
+ * bsgemm.h -- C ABI of the block-scaled low-precision GEMM library for one
+ * GB300 GPU (sm_103a).
+ *
+ *     D = alpha * (A (.) sA) (B (.) sB)^T,   FP32 accumulation, BF16 output
+ *
+ * The operation is the NVFP4 / FP8 GEMM of "Together AI Ports ThunderKittens
+ * GEMM Kernels to NVIDIA Vera Rubin NVL72" (introduction; "Building the
+ * GEMM"): a tcgen05 tensor-core MMA that reads its operands from shared memory,
+ * accumulates in tensor memory and consumes one E4M3 scale per 16 K-elements
+ * (NVFP4) or per-tensor FP32 scales (FP8). The scale-layout prep call follows
+ * "Triton #11171 - Why Two New NVFP4 Test Cases Produced Twelve Tensor-Memory
+ * Failures", "Activation-scale swizzling forced the relevant persistent path":
+ * the persistent kernel reads scales in a layout rewritten in HBM beforehand.
+ *
+ * Conventions shared by every entry point
+ *  - All matrix arguments are DEVICE pointers on the current CUDA device,
+ *    owned by the caller. The library never frees or retains them.
+ *  - Row-major everywhere. A is [M][K], B is [N][K] (so the GEMM contracts
+ *    the contiguous K dimension of both), D is [M][N] BF16.
+ *  - NVFP4 operand rows hold E2M1 codes packed two per byte along K: element
+ *    2i in bits 0..3 of byte i, element 2i+1 in bits 4..7 (A: uint8[M][K/2]).
+ *  - Row-major NVFP4 scales: uint8[rows][K/16], one E4M3 code per 16
+ *    consecutive K-elements; scales are read as unsigned (the sign bit must be
+ *    clear) and must not be NaN.
+ *  - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
+ *    NULL = legacy default stream). No call synchronises except
+ *    bsg_get_device_status.
+ *  - Every function returns a bsg_status code; no exception crosses the ABI.
+ *    Argument errors are detected on the host before anything is launched.
+ *  - Sizes: M, N >= 1; N % 8 == 0 (16-byte BF16 rows for the TMA store);
+ *    NVFP4: K % 256 == 0; FP8: K % 128 == 0. Base pointers must be 16-byte
+ *    aligned.
+ *  - A GPU-side wait that exceeds the watchdog limit (default 1 s per wait)
+ *    makes the kernel record BSG_ERR_DEVICE_TIMEOUT in a device status word
+ *    and return instead of hanging; read it with bsg_get_device_status.
+ */
+#ifndef BSGEMM_H
+#define BSGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BSG_API __attribute__((visibility("default")))
+#else
+#define BSG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *bsg_stream_t;
+
+typedef enum bsg_status {
+    BSG_OK = 0,
+    BSG_ERR_INVALID_ARG = 1,        /* null pointer, bad size or multiple     */
+    BSG_ERR_MISALIGNED = 2,         /* a base pointer is not 16-byte aligned  */
+    BSG_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute 10.3     */
+    BSG_ERR_NO_PLAN = 4,            /* forced plan unknown or unfit for shape */
+    BSG_ERR_CUDA = 5,               /* a CUDA runtime / driver call failed    */
+    BSG_ERR_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait ran out        */
+    BSG_ERR_OUT_OF_MEMORY = 7       /* workspace allocation failed            */
+} bsg_status;
+
+/* ---------------------------------------------------------------------------
+ * NVFP4 GEMM with row-major scales.
+ *   A   : uint8[M][K/2]  E2M1 codes, two per byte
+ *   sfA : uint8[M][K/16] E4M3 block scales, row-major
+ *   B   : uint8[N][K/2]
+ *   sfB : uint8[N][K/16]
+ *   D   : bf16[M][N]; D = bf16_rn(alpha * sum_k a*sA * b*sB), FP32 accumulate
+ * Swizzles sfA and sfB into a library-owned per-device workspace (grown on
+ * demand with cudaMalloc; pre-size it with bsg_reserve_workspace before any
+ * stream capture), then runs nvfp4_gemm_swizzled. Calls on different streams
+ * of one device share that workspace and must not overlap in time.
+ * ------------------------------------------------------------------------- */
+BSG_API int nvfp4_gemm(int M, int N, int K,
+               const void *A, const void *sfA,
+               const void *B, const void *sfB,
+               float alpha, void *D, bsg_stream_t stream);
+
+/* Same GEMM with scales already in the swizzled layout produced by
+ * nvfp4_swizzle_scales (sfA_swz: nvfp4_swizzled_scale_bytes(M, K) bytes,
+ * sfB_swz: nvfp4_swizzled_scale_bytes(N, K) bytes). Allocates nothing.     */
+BSG_API int nvfp4_gemm_swizzled(int M, int N, int K,
+                        const void *A, const void *sfA_swz,
+                        const void *B, const void *sfB_swz,
+                        float alpha, void *D, bsg_stream_t stream);
+
+/* Scale-layout prep: row-major uint8[rows][K/16] -> the tcgen05 block-scale
+ * layout: rows padded to a multiple of 128, K/16 padded to a multiple of 4,
+ * 128x4 blocks of 512 bytes ordered row-block-major with the column block
+ * fastest; inside a block, (r, c) -> byte (r%32)*16 + (r/32)*4 + c. Padding
+ * is written as zero. Requires K % 16 == 0; sf_swz must hold
+ * nvfp4_swizzled_scale_bytes(rows, K) bytes. Bit-exact byte permutation.  */
+BSG_API int nvfp4_swizzle_scales(int rows, int K, const void *sf, void *sf_swz,
+                         bsg_stream_t stream);
+
+/* Size in bytes of the swizzled layout (0 for invalid sizes). Host only.  */
+BSG_API size_t nvfp4_swizzled_scale_bytes(int rows, int K);
+
+/* ---------------------------------------------------------------------------
+ * FP8 E4M3 GEMM with per-tensor FP32 scales.
+ *   A : uint8[M][K] E4M3, B : uint8[N][K] E4M3, D : bf16[M][N]
+ *   sA, sB: DEVICE pointers to one float each, or NULL for 1.0
+ *   D = bf16_rn(alpha * sA * sB * sum_k a*b), FP32 accumulate
+ * ------------------------------------------------------------------------- */
+BSG_API int fp8_gemm(int M, int N, int K,
+             const void *A, const float *sA,
+             const void *B, const float *sB,
+             float alpha, void *D, bsg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Runtime control
+ * ------------------------------------------------------------------------- */
+
+/* Grow the nvfp4_gemm scale workspace of `device` to at least `bytes`.    */
+BSG_API int bsg_reserve_workspace(int device, size_t bytes);
+
+/* Synchronise `stream`, then return and clear the device status word of the
+ * current device: BSG_OK, BSG_ERR_DEVICE_TIMEOUT (a bounded wait ran out) or
+ * BSG_ERR_CUDA (the stream reported an error).                            */
+BSG_API int bsg_get_device_status(bsg_stream_t stream);
+
+/* Raw status word of the last bsg_get_device_status call on this thread:
+ * 0, or (BSG_ERR_DEVICE_TIMEOUT << 16) | wait-site id.                    */
+BSG_API uint32_t bsg_last_status_word(void);
+
+/* Per-wait watchdog limit in nanoseconds used by later launches (0 restores
+ * the default of 1e9).                                                    */
+BSG_API int bsg_set_watchdog_ns(uint64_t ns);
+
+/* Launch a one-thread probe that waits, with the library's bounded wait, on
+ * an mbarrier that nothing ever arrives on. After `ns` nanoseconds it records
+ * BSG_ERR_DEVICE_TIMEOUT in the status word and returns: a test of the
+ * watchdog that faults and hangs nothing.                                 */
+BSG_API int bsg_watchdog_selftest(uint64_t ns, bsg_stream_t stream);
+
+/* Force the planner to one named plan for later calls (NULL or "" = choose
+ * automatically). Unknown names return BSG_ERR_NO_PLAN.                    */
+BSG_API int bsg_force_plan(const char *name);
+
+/* Name of the plan the planner picks for a shape on a GPU with `num_sms`
+ * SMs; kind 0 = NVFP4, 1 = FP8. Host only (no GPU needed).               */
+BSG_API int bsg_select_plan(int kind, int M, int N, int K, int num_sms,
+                    char *name, size_t name_len);
+
+/* Number of kernel launches the last GEMM call on this thread issued
+ * (swizzle passes included).                                               */
+BSG_API int bsg_last_launch_count(void);
+
+/* Human-readable name of a status code.                                    */
+BSG_API const char *bsg_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSGEMM_H */

@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+entry point the header declares, rejects bad arguments before launching
+anything, and its planner and error strings behave."""
+import re
+from pathlib import Path
+
+import pytest
+
+import __graft_entry__
+import block_scaled_precision_persistent_gb300 as bsg
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return bsg.load()
+
+
+def header_functions():
+    text = (ROOT / "include" / "bsgemm.h").read_text()
+    return re.findall(r"^BSG_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, re.M)
+
+
+def test_header_and_binding_agree():
+    names = header_functions()
+    assert len(names) >= 14
+    assert sorted(names) == sorted(bsg.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_only_declared_symbols_are_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", str(bsg.LIB_PATH)], capture_output=True,
+                         text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    ours = {n for n in exported if not n.startswith("_")}
+    assert ours == set(header_functions()), ours ^ set(header_functions())
+
+
+BAD = 0x1000  # a non-null, 16-byte-aligned fake pointer: never dereferenced
+
+
+@pytest.mark.parametrize("M,N,K", [(0, 8, 256), (8, 0, 256), (8, 8, 128), (8, 8, 300), (8, 12, 256),
+                                   (-1, 8, 256)])
+def test_nvfp4_bad_sizes(lib, M, N, K):
+    for fn in (lib.nvfp4_gemm, lib.nvfp4_gemm_swizzled):
+        assert fn(M, N, K, BAD, BAD, BAD, BAD, 1.0, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+
+
+def test_nvfp4_null_and_misaligned(lib):
+    assert lib.nvfp4_gemm(128, 128, 256, None, BAD, BAD, BAD, 1.0, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert lib.nvfp4_gemm(128, 128, 256, BAD + 8, BAD, BAD, BAD, 1.0, BAD, None) == bsg.BSG_ERR_MISALIGNED
+    assert lib.nvfp4_gemm_swizzled(128, 128, 256, BAD, BAD, BAD, BAD, 1.0, BAD + 2, None) == \
+        bsg.BSG_ERR_MISALIGNED
+
+
+def test_fp8_bad_args(lib):
+    assert lib.fp8_gemm(128, 128, 64, BAD, None, BAD, None, 1.0, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert lib.fp8_gemm(128, 128, 128, None, None, BAD, None, 1.0, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert lib.fp8_gemm(128, 128, 128, BAD, BAD + 1, BAD, None, 1.0, BAD, None) == bsg.BSG_ERR_MISALIGNED
+
+
+def test_swizzle_bad_args(lib):
+    assert lib.nvfp4_swizzle_scales(0, 256, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert lib.nvfp4_swizzle_scales(8, 24, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert lib.nvfp4_swizzle_scales(8, 256, BAD, BAD + 4, None) == bsg.BSG_ERR_MISALIGNED
+
+
+def test_swizzled_bytes(lib):
+    assert bsg.nvfp4_swizzled_scale_bytes(1, 16) == 128 * 4
+    assert bsg.nvfp4_swizzled_scale_bytes(128, 256) == 128 * 16
+    assert bsg.nvfp4_swizzled_scale_bytes(300, 1040) == 384 * 68
+    assert bsg.nvfp4_swizzled_scale_bytes(16384, 16384) == 16384 * 1024
+    assert bsg.nvfp4_swizzled_scale_bytes(10, 24) == 0
+
+
+def test_planner_enumeration(lib):
+    # every shape of the workloads picks a plan of its own kind; N <= 128
+    # takes the 128-wide tile, everything else the 256-wide one
+    for kind, prefix in ((0, "nvfp4_"), (1, "fp8_")):
+        for M in (1, 64, 256, 4096, 16384):
+            for N in (8, 128, 136, 256, 3072, 12288, 16384):
+                name = bsg.bsg_select_plan(kind, M, N, 4096, 152)
+                assert name.startswith(prefix), name
+                assert ("x128_" in name) == (N <= 128), (N, name)
+
+
+def test_forced_plan(lib):
+    with pytest.raises(bsg.BsgError) as e:
+        bsg.bsg_force_plan("no_such_plan")
+    assert e.value.code == bsg.BSG_ERR_NO_PLAN
+    bsg.bsg_force_plan("nvfp4_tc1_128x128_s5_acc2")
+    try:
+        assert bsg.bsg_select_plan(0, 4096, 4096, 4096, 152) == "nvfp4_tc1_128x128_s5_acc2"
+        with pytest.raises(bsg.BsgError):       # an NVFP4 plan cannot serve FP8
+            bsg.bsg_select_plan(1, 4096, 4096, 4096, 152)
+    finally:
+        bsg.bsg_force_plan(None)
+    assert bsg.bsg_select_plan(0, 4096, 4096, 4096, 152) == "nvfp4_tc1_128x256_s3_acc1"
+
+
+def test_error_strings(lib):
+    assert bsg.bsg_error_string(0) == "ok"
+    assert "timed out" in bsg.bsg_error_string(bsg.BSG_ERR_DEVICE_TIMEOUT)
+    assert bsg.bsg_error_string(99) == "unknown status"
