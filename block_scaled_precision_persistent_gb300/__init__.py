@@ -16,11 +16,12 @@ from pathlib import Path
 
 __all__ = [
     "BsgError", "load", "nvfp4_gemm", "nvfp4_gemm_swizzled", "nvfp4_swizzle_scales",
-    "nvfp4_swizzled_scale_bytes", "fp8_gemm", "bsg_reserve_workspace", "bsg_get_device_status",
+    "nvfp4_swizzled_scale_bytes", "nvfp4_gemm_noalloc", "fp8_gemm", "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_select_plan", "bsg_last_launch_count", "bsg_error_string", "EXPORTED_SYMBOLS",
     "BSG_OK", "BSG_ERR_INVALID_ARG", "BSG_ERR_MISALIGNED", "BSG_ERR_UNSUPPORTED_DEVICE",
     "BSG_ERR_NO_PLAN", "BSG_ERR_CUDA", "BSG_ERR_DEVICE_TIMEOUT", "BSG_ERR_OUT_OF_MEMORY",
+    "BSG_ERR_EXCEEDS_SCRATCH", "BSG_NOALLOC_SCRATCH_BYTES",
 ]
 
 BSG_OK = 0
@@ -31,6 +32,8 @@ BSG_ERR_NO_PLAN = 4
 BSG_ERR_CUDA = 5
 BSG_ERR_DEVICE_TIMEOUT = 6
 BSG_ERR_OUT_OF_MEMORY = 7
+BSG_ERR_EXCEEDS_SCRATCH = 8
+BSG_NOALLOC_SCRATCH_BYTES = 16 << 20     # fixed scratch of nvfp4_gemm_noalloc
 
 LIB_PATH = Path(__file__).resolve().parent / "libbsgemm.so"
 
@@ -42,6 +45,7 @@ _SIGNATURES = {
     "nvfp4_gemm_swizzled": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "nvfp4_swizzle_scales": (_i, [_i, _i, _vp, _vp, _vp]),
     "nvfp4_swizzled_scale_bytes": (ctypes.c_size_t, [_i, _i]),
+    "nvfp4_gemm_noalloc": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "fp8_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "bsg_reserve_workspace": (_i, [_i, ctypes.c_size_t]),
     "bsg_get_device_status": (_i, [_vp]),
@@ -121,6 +125,15 @@ def nvfp4_swizzle_scales(rows, K, sf, sf_swz, stream=None) -> None:
 
 def nvfp4_swizzled_scale_bytes(rows, K) -> int:
     return int(load().nvfp4_swizzled_scale_bytes(rows, K))
+
+
+def nvfp4_gemm_noalloc(M, N, K, A, sfA, B, sfB, alpha, D, stream=None) -> None:
+    """As nvfp4_gemm, but the swizzled scales go to the library's fixed device
+    scratch array (BSG_NOALLOC_SCRATCH_BYTES) instead of an allocated
+    workspace: for callers that cannot allocate device memory. Calls whose
+    work overlaps on the GPU share that array and race."""
+    _check(load().nvfp4_gemm_noalloc(M, N, K, _ptr(A), _ptr(sfA), _ptr(B), _ptr(sfB),
+                                     float(alpha), _ptr(D), _stream(stream)), "nvfp4_gemm_noalloc")
 
 
 def fp8_gemm(M, N, K, A, sA, B, sB, alpha, D, stream=None) -> None:

@@ -411,6 +411,7 @@ const char *bsg_error_string(int code)
     case BSG_ERR_CUDA: return "CUDA error";
     case BSG_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case BSG_ERR_OUT_OF_MEMORY: return "workspace allocation failed";
+    case BSG_ERR_EXCEEDS_SCRATCH: return "request exceeds the fixed scratch array of nvfp4_gemm_noalloc";
     default: return "unknown status";
     }
 }

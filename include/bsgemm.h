@@ -62,8 +62,13 @@ typedef enum bsg_status {
     BSG_ERR_NO_PLAN = 4,            /* forced plan unknown or unfit for shape */
     BSG_ERR_CUDA = 5,               /* a CUDA runtime / driver call failed    */
     BSG_ERR_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait ran out        */
-    BSG_ERR_OUT_OF_MEMORY = 7       /* workspace allocation failed            */
+    BSG_ERR_OUT_OF_MEMORY = 7,      /* workspace allocation failed            */
+    BSG_ERR_EXCEEDS_SCRATCH = 8     /* nvfp4_gemm_noalloc: scales do not fit
+                                       in its fixed scratch array            */
 } bsg_status;
+
+/* Size of the fixed device scratch array used by nvfp4_gemm_noalloc.      */
+#define BSG_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 /* ---------------------------------------------------------------------------
  * NVFP4 GEMM with row-major scales.
@@ -101,6 +106,32 @@ BSG_API int nvfp4_swizzle_scales(int rows, int K, const void *sf, void *sf_swz,
 
 /* Size in bytes of the swizzled layout (0 for invalid sizes). Host only.  */
 BSG_API size_t nvfp4_swizzled_scale_bytes(int rows, int K);
+
+/* NVFP4 GEMM with row-major scales that allocates nothing. The pages have no
+ * counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc -- for instance a runtime that has handed all device memory to
+ * its own pool allocator, or code running where a device allocation is not
+ * allowed (a host callback, a loop with a no-allocation rule).
+ *   Arguments, layouts and result are those of nvfp4_gemm.
+ *   Scratch: the swizzled scales of A and B go to one file-scope device
+ *   array of BSG_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads
+ *   the library holds until the process exits. A call needs
+ *   round256(nvfp4_swizzled_scale_bytes(M, K)) +
+ *   round256(nvfp4_swizzled_scale_bytes(N, K)) bytes of it (for example
+ *   M = N = 8192 at K = 16384); larger requests return
+ *   BSG_ERR_EXCEEDS_SCRATCH before anything is launched.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   with cudaGetSymbolAddress (with that device current); make that first
+ *   call before any stream capture.
+ *   Sharing: all calls share the one array, which keeps the last call's
+ *   contents. Each call rewrites every byte it reads, so nothing needs
+ *   clearing, but calls whose work overlaps on the GPU (different streams)
+ *   race on the array and must be serialised by the caller.
+ *   bsg_last_launch_count() afterwards reports the final GEMM launch only. */
+BSG_API int nvfp4_gemm_noalloc(int M, int N, int K,
+                               const void *A, const void *sfA,
+                               const void *B, const void *sfB,
+                               float alpha, void *D, bsg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * FP8 E4M3 GEMM with per-tensor FP32 scales.
