@@ -97,7 +97,9 @@ class ClockSampler:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
-        self.index = index
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        self.index = ids[index] if index < len(ids) and ids[index].isdigit() else index
         self.proc = None
         self.file = None
 
@@ -320,11 +322,12 @@ def cpu_baseline(w: workloads.Workload, p_host: dict, budget_s: float = 15.0) ->
     o = oracle.get()
     threads = oracle.default_threads()
     args = (p_host["A"], p_host["sfA"], p_host["B"], p_host["sfB"], p_host["alpha"], w.K)
+    # calibrate on one row per thread, then size the sample to ~budget_s
     t = time.perf_counter()
-    o.nvfp4_gemm(*args, rows=[0], nthreads=threads)
-    one = max(time.perf_counter() - t, 1e-3)
-    rows = max(1, min(w.M, int(budget_s / one)))
-    rows = max(threads, rows // threads * threads) if rows >= threads else rows
+    o.nvfp4_gemm(*args, rows=list(range(threads)), nthreads=threads)
+    per_round = max(time.perf_counter() - t, 1e-3)       # seconds per `threads` rows
+    rows = int(budget_s / per_round) * threads
+    rows = max(threads, min(w.M, rows))
     sel = list(range(0, w.M, max(1, w.M // rows)))[:rows]
     t = time.perf_counter()
     o.nvfp4_gemm(*args, rows=sel, nthreads=threads)
@@ -369,8 +372,11 @@ def run_ours(args, dist: Dist) -> None:
     plan = step.plan()
     traffic = NCU_TRAFFIC_BYTES.get((plan, w.name))
 
-    e2e = e2e_nvfp4(w, step, max(2, min(args.steps, 5)), 1)
-    e2e["value"] = dist.world * e2e["value"] if False else e2e["value"]
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_nvfp4(w, step, max(2, min(args.steps, 5)), 1)
+        e2e["ms_per_step"] = dist.max(e2e["ms_per_step"])
+        e2e["value"] = dist.world * w.flops / (e2e["ms_per_step"] * 1e-3) / 1e12
     secondary = {}
     if not args.no_secondary:
         secondary["fp8"] = secondary_fp8(dev, max(3, args.steps), args.warmup, pk, psrc)
@@ -396,7 +402,8 @@ def run_ours(args, dist: Dist) -> None:
                      "peak_source": f"{psrc} bf16 burst {pk['bf16_tflops']} x {FP4_PER_BF16:g} "
                                     "(nominal FP4/BF16 dense ratio)",
                      "frac_of_9pf": round(achieved / 9000.0, 4)},
-        "e2e": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in e2e.items()},
+        "e2e": None if e2e is None else
+               {k: (round(v, 4) if isinstance(v, float) else v) for k, v in e2e.items()},
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -459,6 +466,7 @@ def main() -> None:
                     choices=[n for n, w in workloads.WORKLOADS.items() if w.kind == "nvfp4"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

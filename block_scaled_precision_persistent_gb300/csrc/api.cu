@@ -103,10 +103,18 @@ int default_plan(Kind kind, int M, int N, int K, int num_sms)
     (void)K;
     (void)num_sms;
     const char *name = nullptr;
-    if (kind == Kind::NVFP4)
-        name = N <= 128 ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc1_128x256_s3_acc1";
-    else
-        name = N <= 128 ? "fp8_tc1_128x128_s6_acc2" : "fp8_tc1_128x256_s4_acc2";
+    const bool small_m = M <= 128;   // a 256-row pair tile would idle half its SMs
+    if (kind == Kind::NVFP4) {
+        if (small_m)
+            name = N <= 128 ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc1_128x256_s3_acc1";
+        else
+            name = N <= 128 ? "nvfp4_tc2_256x128_s6_acc2" : "nvfp4_tc2_256x256_s5_acc1";
+    } else {
+        if (small_m)
+            name = N <= 128 ? "fp8_tc1_128x128_s6_acc2" : "fp8_tc1_128x256_s4_acc2";
+        else
+            name = N <= 128 ? "fp8_tc1_128x128_s6_acc2" : "fp8_tc2_256x256_s6_acc2";
+    }
     return bsg::find_plan(name);
 }
 
@@ -128,7 +136,8 @@ int choose_plan(Kind kind, int M, int N, int K, int num_sms, int *plan)
 }
 
 int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *ptr, uint64_t inner,
-              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer)
+              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     auto fn = encode_fn();
     if (!fn)
@@ -138,7 +147,7 @@ int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *ptr, uint
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t elem_strides[2] = {1, 1};
     CUresult r = fn(map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, elem_strides,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? BSG_OK : BSG_ERR_CUDA;
 }
@@ -156,20 +165,35 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     const uint64_t row_bytes = kind == Kind::NVFP4 ? (uint64_t)K / 2u : (uint64_t)K;
 
     GemmMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    // A: 128 rows per CTA; B: the CTA's share of the tile's N rows
     if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes,
-                        128, (uint32_t)pi.bm)) != BSG_OK ||
+                        128, 128)) != BSG_OK ||
         (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, (uint64_t)N, row_bytes,
-                        128, (uint32_t)pi.bn)) != BSG_OK ||
+                        128, (uint32_t)(pi.bn / pi.cta_group))) != BSG_OK ||
         (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)M,
                         (uint64_t)N * 2u, 64, 32)) != BSG_OK)
         return rc;
+    if (pi.cta_group == 2 && kind == Kind::NVFP4) {
+        // swizzled scales viewed as rows of 256 bytes; one stage = 8 rows
+        if ((rc = encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, sfa, 256,
+                            swizzled_bytes(M, K) / 256u, 256, 256, 8, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+                BSG_OK ||
+            (rc = encode_2d(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, sfb, 256,
+                            swizzled_bytes(N, K) / 256u, 256, 256, 8, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+                BSG_OK)
+            return rc;
+    } else {
+        maps.sfa = maps.a;
+        maps.sfb = maps.a;
+    }
 
     GemmArgs a;
     std::memset(&a, 0, sizeof a);
     a.M = M;
     a.N = N;
     a.K = K;
-    a.num_m_tiles = (M + pi.bm - 1) / pi.bm;
+    a.num_m_tiles = (M + pi.tile_m - 1) / pi.tile_m;
     a.num_n_tiles = (N + pi.bn - 1) / pi.bn;
     a.num_k_blocks = K / pi.k_block;
     a.raster_group = 8;
@@ -182,8 +206,11 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     a.sB = sB;
     a.status = ds->status;
     a.timeout_ns = g_watchdog_ns.load();
-    const long long tiles = (long long)a.num_m_tiles * a.num_n_tiles;
-    const int grid = (int)(tiles < ds->sms ? tiles : ds->sms);
+    const long long ctas = (long long)a.num_m_tiles * a.num_n_tiles * pi.cta_group;
+    const int resident = bsg::max_resident_ctas(plan, ds->sms);
+    if (resident < pi.cta_group)
+        return BSG_ERR_CUDA;
+    const int grid = (int)(ctas < resident ? ctas : resident);
     cudaError_t e = bsg::launch_gemm(plan, maps, a, grid, stream);
     if (e != cudaSuccess)
         return BSG_ERR_CUDA;
@@ -228,6 +255,38 @@ size_t round256(size_t x) { return (x + 255u) & ~(size_t)255u; }
 }  // namespace
 
 namespace bsg {
+int num_plans() { return tc1_num_plans() + pair_num_plans(); }
+
+const PlanInfo &plan_info(int id)
+{
+    return id < tc1_num_plans() ? tc1_plan(id) : pair_plan(id - tc1_num_plans());
+}
+
+cudaError_t launch_gemm(int id, const GemmMaps &maps, const GemmArgs &args, int grid,
+                        cudaStream_t stream)
+{
+    if (id < tc1_num_plans())
+        return tc1_launch(id, maps, args, grid, stream);
+    return pair_launch(id - tc1_num_plans(), maps, args, grid, stream);
+}
+
+int max_resident_ctas(int id, int num_sms)
+{
+    if (id < tc1_num_plans())
+        return num_sms;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return 0;
+    static int cache[kMaxDevices][16] = {};
+    const int j = id - tc1_num_plans();
+    if (j >= 16)
+        return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (cache[dev][j] == 0)
+        cache[dev][j] = 2 * pair_max_clusters(j);
+    return cache[dev][j];
+}
+
 int find_plan(const char *name)
 {
     if (!name)

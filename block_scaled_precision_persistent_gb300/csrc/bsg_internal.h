@@ -31,7 +31,8 @@ struct GemmArgs {
 struct PlanInfo {
     const char *name;
     Kind kind;
-    int bm, bn;                // CTA tile
+    int cta_group;             // 1: one SM per tile; 2: a CTA pair shares one tile
+    int tile_m, bn;            // output tile of one scheduling unit (CTA or pair)
     int stages;                // smem ring depth
     int num_acc;               // TMEM accumulator buffers
     int k_block;               // K elements per ring stage
@@ -40,18 +41,34 @@ struct PlanInfo {
     int tmem_cols;
 };
 
+// Encoded tensor maps of one call (sfa / sfb only for CTA-pair NVFP4 plans).
+struct GemmMaps {
+    CUtensorMap a, b, d, sfa, sfb;
+};
+
+// Plan registry: the 1-SM plans (gemm_persistent.cu) followed by the
+// CTA-pair plans (gemm_pair.cu).
 int num_plans();
 const PlanInfo &plan_info(int id);
 int find_plan(const char *name);
 
-// Encoded tensor maps of one call.
-struct GemmMaps {
-    CUtensorMap a, b, d;
-};
-
-// Launch plan `id` with `grid` persistent CTAs. Returns a cudaError_t.
+// Launch plan `id` with `grid` CTAs (a multiple of 2 for pair plans).
 cudaError_t launch_gemm(int id, const GemmMaps &maps, const GemmArgs &args, int grid,
                         cudaStream_t stream);
+
+// Largest number of CTAs of plan `id` that are co-resident on the current
+// device (clusters x 2 for pair plans, SMs for 1-SM plans); 0 on error.
+int max_resident_ctas(int id, int num_sms);
+
+int tc1_num_plans();
+const PlanInfo &tc1_plan(int i);
+cudaError_t tc1_launch(int i, const GemmMaps &maps, const GemmArgs &args, int grid,
+                       cudaStream_t stream);
+int pair_num_plans();
+const PlanInfo &pair_plan(int i);
+cudaError_t pair_launch(int i, const GemmMaps &maps, const GemmArgs &args, int grid,
+                        cudaStream_t stream);
+int pair_max_clusters(int i);
 
 // Scale-layout prep kernel. Returns a cudaError_t.
 cudaError_t launch_swizzle_scales(int rows, int K, const uint8_t *sf, uint8_t *out,

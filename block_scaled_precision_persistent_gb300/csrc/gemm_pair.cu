@@ -1,0 +1,506 @@
+// CTA-pair persistent block-scaled GEMM: one 256 x BN output tile per pair of
+// CTAs on two SMs, computed by tcgen05.mma.cta_group::2 -- a single MMA
+// spans both CTAs' shared and tensor memory ("Together AI Ports ThunderKittens
+// GEMM Kernels to NVIDIA Vera Rubin NVL72", introduction: one MMA spans two
+// CTAs across two SMs, loaders / one MMA warp / a consumer warpgroup, and a
+// persistent kernel whose next tile streams in while the last one drains).
+//
+// Per CTA of the pair (rank r = 0 leader, 1 peer):
+//   A rows   [256*pm + 128*r, +128)      -> own smem (16 KiB per stage)
+//   B rows   [BN*nt + (BN/2)*r, +BN/2)    -> own smem; the MMA reads both halves
+//   NVFP4 scales: own 128 rows of A, all BN rows of B, written smem -> own TMEM
+//   D rows   [256*pm + 128*r, +128) x BN  in own TMEM, drained by own epilogue
+// Each CTA therefore loads half of B per output tile instead of all of it,
+// which halves the B bytes per SM and leaves room for a deeper ring.
+//
+// Roles: warp 0 TMA producer (both CTAs), warp 1 TMEM allocation (both) and
+// the MMA thread (leader), warps 2..5 the scale writers (both CTAs, NVFP4),
+// warps 6..9 the epilogue (both).
+//
+// NVFP4 scales: each CTA's producer loads a stage's scales first, on the
+// CTA's own barrier; four scale writers per CTA (one per TMEM sub-partition)
+// move them from shared memory into their TMEM lanes with tcgen05.st and
+// arrive on the leader's scale-ready barrier, which the MMA thread waits on
+// beside the A/B full barrier. Copying them with tcgen05.cp from the MMA
+// thread instead was measured to cost ~90 cycles per pair copy, 12 copies per
+// stage, which bounded the MMA rate.
+//
+// Synchronisation: every load of both CTAs completes on the LEADER's full
+// barrier (TMA .cta_group::2); the leader's MMA thread issues the pair MMAs
+// and commits with multicast to both CTAs' empty / accumulator-full
+// barriers; both epilogues arrive on the leader's accumulator-empty barrier.
+// No TMA multicast is used: each CTA fetches its own tiles.
+#include "bsg_internal.h"
+#include "gemm_common.cuh"
+#include "ptx.cuh"
+
+namespace bsg {
+
+template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+struct PairTile {
+    static constexpr bool kFp4 = KIND == Kind::NVFP4;
+    static constexpr int BM = 128;                        // rows per CTA
+    static constexpr int TILE_M = 256;                    // rows per pair
+    static constexpr int ROW_BYTES = 128;
+    static constexpr int K_BLOCK = kFp4 ? 256 : 128;
+    static constexpr int MMA_K_BYTES = 32;
+    static constexpr int MMAS = ROW_BYTES / MMA_K_BYTES;
+    static constexpr int B_ROWS = BN / 2;                 // B rows held by each CTA
+    static constexpr int A_BYTES = BM * ROW_BYTES;
+    static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
+    static constexpr int SF_BLOCK_BYTES = 2048;           // 128 rows x 16 scales
+    static constexpr int SFB_CHUNKS = kFp4 ? BN / 128 : 0;
+    static constexpr int SFA_BYTES = kFp4 ? SF_BLOCK_BYTES : 0;
+    static constexpr int SFB_BYTES = SFB_CHUNKS * SF_BLOCK_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_COLS = 64;
+    static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
+    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
+    static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 1;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
+    static constexpr int SCALE_WARPS = 4;                 // one per TMEM sub-partition (NVFP4 scales)
+    static constexpr int EPI_WARP0 = 2 + SCALE_WARPS;
+    static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // producer, MMA, scale warps, epilogue
+    static constexpr int SFA_COLS = kFp4 ? 4 * MMAS : 0;
+    static constexpr int SFB_COLS = kFp4 ? 4 * SFB_CHUNKS * MMAS : 0;
+    static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
+    static constexpr int TMEM_USED = NUM_ACC * BN + STAGES * SF_COLS;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
+                                     : TMEM_USED <= 64  ? 64
+                                     : TMEM_USED <= 128 ? 128
+                                     : TMEM_USED <= 256 ? 256
+                                                        : 512;
+    static constexpr uint32_t IDESC = kFp4 ? idesc_nvfp4(TILE_M, BN) : idesc_fp8(TILE_M, BN);
+
+    static_assert(BN % 128 == 0 && BN <= 256, "pair tile N: B halves of 64 or 128 rows");
+    static_assert(TMEM_USED <= 512, "TMEM: accumulators plus scales exceed 512 columns");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
+};
+
+template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+__global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmD,
+                     const __grid_constant__ CUtensorMap tmSFA,
+                     const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args)
+{
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const uint32_t s_epi = base + STAGES * T::STAGE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + STAGES * T::STAGE_BYTES + T::EPI_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t full0 = bar0;                     // [STAGES] loads -> MMA (leader's used)
+    const uint32_t empty0 = bar0 + 8u * STAGES;      // [STAGES] MMA -> loads (both CTAs)
+    const uint32_t tfull0 = bar0 + 16u * STAGES;     // [NUM_ACC] MMA -> epilogues (both)
+    const uint32_t tempty0 = tfull0 + 8u * NUM_ACC;  // [NUM_ACC] epilogues -> MMA (leader's)
+    const uint32_t drain_bar = tempty0 + 8u * NUM_ACC;
+    const uint32_t sfready0 = drain_bar + 8u;                // [STAGES] scales in TMEM (both CTAs) -> MMA (leader's)
+    const uint32_t sffull0 = sfready0 + 8u * STAGES;         // [STAGES] own scale loads -> own scale warps
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const Watchdog wd{args.status, args.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+        }
+        for (int a = 0; a < NUM_ACC; ++a) {
+            mbar_init(tfull0 + 8u * a, 1);
+            mbar_init(tempty0 + 8u * a, 2 * T::EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(sfready0 + 8u * s, 2 * T::SCALE_WARPS);
+            mbar_init(sffull0 + 8u * s, 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmD);
+        if constexpr (T::kFp4) {
+            prefetch_tensormap(&tmSFA);
+            prefetch_tensormap(&tmSFB);
+        }
+    }
+    __syncwarp();
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), T::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();          // both CTAs' barriers exist before any remote use
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int num_tiles = args.num_m_tiles * args.num_n_tiles;
+    const int nkb = args.num_k_blocks;
+    const int cluster_id = blockIdx.x >> 1;
+    const int num_clusters = gridDim.x >> 1;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------
+        // TMA producer (both CTAs): own A half, own B half, own scales
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+                int pm, nt;
+                raster_tile(tile, args, pm, nt);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wd, abort_flag, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * T::STAGE_BYTES;
+                    const uint32_t sb = sa + T::A_BYTES;
+                    const uint32_t fb = mapa_shared(full0 + 8u * stage, 0);
+                    if constexpr (T::kFp4) {
+                        // scales first, on this CTA's own barrier: its scale warps
+                        // write them into its TMEM while A and B are in flight.
+                        // 256-byte rows of the swizzled scale layout: a stage is
+                        // the 8 rows starting at (row_block * ncb + 4 kb) * 2.
+                        const uint32_t sfb = sffull0 + 8u * stage;
+                        mbar_arrive_expect_tx(sfb, T::SFA_BYTES + T::SFB_BYTES);
+                        const uint32_t ssfa = sb + T::B_BYTES;
+                        const int rba = 2 * pm + (int)rank;
+                        tma_load_2d(ssfa, &tmSFA, sfb, 0, (rba * args.sf_col_blocks + 4 * kb) * 2);
+#pragma unroll
+                        for (int c = 0; c < T::SFB_CHUNKS; ++c) {
+                            const int rbb = nt * T::SFB_CHUNKS + c;
+                            tma_load_2d(ssfa + T::SFA_BYTES + c * T::SF_BLOCK_BYTES, &tmSFB, sfb, 0,
+                                        (rbb * args.sf_col_blocks + 4 * kb) * 2);
+                        }
+                    }
+                    if (leader)
+                        mbar_arrive_expect_tx(full0 + 8u * stage, 2u * (T::A_BYTES + T::B_BYTES));
+                    tma_load_2d_pair(sa, &tmA, fb, kb * T::ROW_BYTES, pm * T::TILE_M + (int)rank * T::BM);
+                    tma_load_2d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN + (int)rank * T::B_ROWS);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let copies already issued land before the CTA goes away
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 200000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------
+        // MMA issuer: one thread of the leader drives both SMs' tensor cores
+        // ------------------------------------------------------------------
+        if (leader && lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+                if (!mbar_wait(tempty0 + 8u * acc, acc_phase ^ 1u, wd, abort_flag, 2)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(full0 + 8u * stage, phase, wd, abort_flag, 3)) {
+                        ok = false;
+                        break;
+                    }
+                    if constexpr (T::kFp4) {
+                        // the scale warps have written this stage's scales to TMEM
+                        if (!mbar_wait(sfready0 + 8u * stage, phase, wd, abort_flag, 5)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = base + stage * T::STAGE_BYTES;
+                    const uint32_t sb = sa + T::A_BYTES;
+                    if constexpr (T::kFp4) {
+                        const uint32_t sfa_t = tmem + (uint32_t)(NUM_ACC * BN + stage * T::SF_COLS);
+                        const uint32_t sfb_t = sfa_t + T::SFA_COLS;
+#pragma unroll
+                        for (int j = 0; j < T::MMAS; ++j)
+                            mma_nvfp4_pair(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
+                                           desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                           sfa_t + 4u * j, sfb_t + 4u * j * T::SFB_CHUNKS,
+                                           (kb | j) != 0 ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < T::MMAS; ++j)
+                            mma_fp8_pair(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
+                                         desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                         (kb | j) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair_multicast(empty0 + 8u * stage, 0x3);   // frees the stage in both CTAs
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                tc_commit_pair_multicast(tfull0 + 8u * acc, 0x3);          // both epilogues may drain
+                if (++acc == NUM_ACC) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            tc_commit_pair(drain_bar);
+            mbar_wait_quiet(drain_bar, 0, wd.limit_ns);
+        }
+    } else if (warp < T::EPI_WARP0) {
+        // ------------------------------------------------------------------
+        // Scale warps (NVFP4) (both CTAs: each writes its own TMEM): one per TMEM sub-partition
+        // (warp % 4), each writing the stage's block scales from shared
+        // memory into its own 32 TMEM lanes with tcgen05.st -- two store
+        // instructions per warp per stage, in parallel across the four
+        // sub-partitions -- then signalling the MMA thread.
+        // ------------------------------------------------------------------
+        if constexpr (T::kFp4) {
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    // a stage's scale columns are rewritten only after its
+                    // scales were reloaded, i.e. after the MMAs that read the
+                    // previous contents completed (empty -> producer -> sf full)
+                    if (!warp_wait(sffull0 + 8u * stage, phase, wd, abort_flag, 6, lane)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sfa_t = tmem + lane_off + (uint32_t)(NUM_ACC * BN + stage * T::SF_COLS);
+                    const uint32_t ssfa = base + stage * T::STAGE_BYTES + T::A_BYTES + T::B_BYTES;
+                    store_stage_scales<T::SFB_CHUNKS>(sfa_t, sfa_t + T::SFA_COLS, ssfa, ssfa + T::SFA_BYTES,
+                                                      lane);
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        // the stores have completed (wait::st): the leader's own
+                        // writers arrive locally, the peer's with a relaxed remote
+                        // arrive (a release at cluster scope measured ~1100 cycles)
+                        if (leader)
+                            mbar_arrive(sfready0 + 8u * stage);
+                        else
+                            mbar_arrive_remote_relaxed(mapa_shared(sfready0 + 8u * stage, 0));
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------
+        // Epilogue (both CTAs): own 128 rows of the pair's tile
+        // ------------------------------------------------------------------
+        const int q = warp & 3;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const uint32_t ebuf = s_epi + (uint32_t)(warp - T::EPI_WARP0) * 2u * T::EPI_BUF_BYTES;
+        float scale = args.alpha;
+        if constexpr (!T::kFp4) {
+            if (args.sA)
+                scale *= *args.sA;
+            if (args.sB)
+                scale *= *args.sB;
+        }
+        int acc = 0, buf = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
+            int pm, nt;
+            raster_tile(tile, args, pm, nt);
+            if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
+                break;
+            tc_fence_after_sync();
+            const uint32_t t_acc = tmem + lane_off + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int ch = 0; ch < BN / T::EPI_COLS; ++ch) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS, v0);
+                tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS + 32, v1);
+                tmem_ld_wait();
+                if (ch == BN / T::EPI_COLS - 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_cluster(mapa_shared(tempty0 + 8u * acc, 0));
+                }
+                if (lane == 0)
+                    bulk_wait_group_read<1>();
+                __syncwarp();
+                const uint32_t sbuf = ebuf + (uint32_t)buf * T::EPI_BUF_BYTES;
+                const uint32_t row = sbuf + (uint32_t)lane * 128u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(row + ((uint32_t)(c ^ (lane & 7)) << 4),
+                                 pack_bf16x2(__uint_as_float(v0[8 * c + 0]) * scale, __uint_as_float(v0[8 * c + 1]) * scale),
+                                 pack_bf16x2(__uint_as_float(v0[8 * c + 2]) * scale, __uint_as_float(v0[8 * c + 3]) * scale),
+                                 pack_bf16x2(__uint_as_float(v0[8 * c + 4]) * scale, __uint_as_float(v0[8 * c + 5]) * scale),
+                                 pack_bf16x2(__uint_as_float(v0[8 * c + 6]) * scale, __uint_as_float(v0[8 * c + 7]) * scale));
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(row + ((uint32_t)((c + 4) ^ (lane & 7)) << 4),
+                                 pack_bf16x2(__uint_as_float(v1[8 * c + 0]) * scale, __uint_as_float(v1[8 * c + 1]) * scale),
+                                 pack_bf16x2(__uint_as_float(v1[8 * c + 2]) * scale, __uint_as_float(v1[8 * c + 3]) * scale),
+                                 pack_bf16x2(__uint_as_float(v1[8 * c + 4]) * scale, __uint_as_float(v1[8 * c + 5]) * scale),
+                                 pack_bf16x2(__uint_as_float(v1[8 * c + 6]) * scale, __uint_as_float(v1[8 * c + 7]) * scale));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int x = nt * BN + ch * T::EPI_COLS;
+                    const int y = pm * T::TILE_M + (int)rank * T::BM + q * 32;
+                    if (x < args.N && y < args.M)
+                        tma_store_2d(&tmD, sbuf, x, y);
+                    bulk_commit_group();
+                }
+                buf ^= 1;
+            }
+            if (++acc == NUM_ACC) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (lane == 0)
+            bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // Reconverge each warp before the block barrier: the producer and MMA
+    // roles ran on lane 0 only, and the teardown below (tcgen05.dealloc) is a
+    // warp-collective instruction that needs all 32 lanes together.
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();          // no CTA leaves while its peer may still touch it
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem, T::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Plans and launchers
+// ---------------------------------------------------------------------------
+template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
+                                    cudaStream_t stream)
+{
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
+    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(T::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = T::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.d, maps.sfa, maps.sfb, args);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+static int pair_clusters_impl()
+{
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
+    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(T::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = T::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void *)kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+static constexpr PlanInfo make_pair_plan(const char *name)
+{
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
+    return PlanInfo{name, KIND, 2, T::TILE_M, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
+                    T::THREADS, T::TMEM_COLS};
+}
+
+#define BSG_PAIR_PLANS(X)                                        \
+    X(Kind::NVFP4, 256, 5, 1, "nvfp4_tc2_256x256_s5_acc1")       \
+    X(Kind::NVFP4, 128, 6, 2, "nvfp4_tc2_256x128_s6_acc2")       \
+    X(Kind::FP8, 256, 6, 2, "fp8_tc2_256x256_s6_acc2")
+
+#define BSG_PAIR_INFO(K, BN, S, A, NAME) make_pair_plan<K, BN, S, A>(NAME),
+static const PlanInfo kPairPlans[] = {BSG_PAIR_PLANS(BSG_PAIR_INFO)};
+#undef BSG_PAIR_INFO
+
+int pair_num_plans() { return (int)(sizeof(kPairPlans) / sizeof(kPairPlans[0])); }
+
+const PlanInfo &pair_plan(int i) { return kPairPlans[i]; }
+
+cudaError_t pair_launch(int id, const GemmMaps &maps, const GemmArgs &args, int grid,
+                        cudaStream_t stream)
+{
+    int i = 0;
+#define BSG_PAIR_LAUNCH(K, BN, S, A, NAME)                              \
+    if (id == i)                                                       \
+        return pair_launch_impl<K, BN, S, A>(maps, args, grid, stream); \
+    ++i;
+    BSG_PAIR_PLANS(BSG_PAIR_LAUNCH)
+#undef BSG_PAIR_LAUNCH
+    return cudaErrorInvalidValue;
+}
+
+int pair_max_clusters(int id)
+{
+    int i = 0;
+#define BSG_PAIR_OCC(K, BN, S, A, NAME)               \
+    if (id == i)                                     \
+        return pair_clusters_impl<K, BN, S, A>();     \
+    ++i;
+    BSG_PAIR_PLANS(BSG_PAIR_OCC)
+#undef BSG_PAIR_OCC
+    return 0;
+}
+
+}  // namespace bsg

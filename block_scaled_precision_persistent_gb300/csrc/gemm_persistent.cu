@@ -9,15 +9,16 @@
 // accumulator in tensor memory, and an epilogue warpgroup drains finished
 // accumulators to HBM; the kernel is persistent, so the next tile's loads
 // stream in while the previous tile's outputs drain. For NVFP4 the block
-// scales are copied from shared memory into tensor memory (tcgen05.cp) next
+// scales are written from shared memory into tensor memory (tcgen05.st) next
 // to the accumulators ("Building the GEMM": the scale factors need TMEM
 // columns beside the accumulators, which bounds the tile shape within the
 // 512 columns of this GPU).
 //
-// CTA roles (192 threads, one CTA per SM):
+// CTA roles (320 threads, one CTA per SM):
 //   warp 0      TMA producer (one elected lane)
 //   warp 1      TMEM allocator + MMA issuer (one elected lane)
-//   warps 2..5  epilogue: TMEM -> registers -> *alpha -> BF16 -> swizzled
+//   warps 2..5  NVFP4 scale writers smem -> TMEM (one per TMEM sub-partition)
+//   warps 6..9  epilogue: TMEM -> registers -> *alpha -> BF16 -> swizzled
 //               smem -> TMA store; warp w reads TMEM lanes 32*(w%4)..+31
 //
 // Every mbarrier wait is bounded (see ptx.cuh): a wait that runs out records
@@ -25,6 +26,7 @@
 #include <cuda_bf16.h>
 
 #include "bsg_internal.h"
+#include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace bsg {
@@ -49,9 +51,11 @@ struct Tile {
     static constexpr int EPI_COLS = 64;                   // BF16 columns per store box
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+    static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 1;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int SCALE_WARPS = 4;                 // one per TMEM sub-partition (NVFP4 scales)
+    static constexpr int EPI_WARP0 = 2 + SCALE_WARPS;
+    static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // producer, MMA, scale warps, epilogue
     // TMEM columns: NUM_ACC accumulators of BN columns, then one set of scale
     // columns per ring stage (a stage's scales are overwritten only after the
     // MMAs that read them completed, which the ring's empty barrier proves).
@@ -73,51 +77,6 @@ struct Tile {
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
 };
 
-// Tile id -> (m tile, n tile): groups of `raster_group` M tiles; inside a
-// group the M tile varies fastest, so the CTAs resident at one time share a
-// few A panels and a band of B panels in L2 ("Building the GEMM": tile
-// rasterisation order permuted for memory locality).
-__device__ __forceinline__ void raster_tile(int tile, const GemmArgs &a, int &mt, int &nt)
-{
-    const int per_group = a.raster_group * a.num_n_tiles;
-    const int g = tile / per_group;
-    const int first_m = g * a.raster_group;
-    const int gm = min(a.raster_group, a.num_m_tiles - first_m);
-    const int local = tile - g * per_group;
-    mt = first_m + local % gm;
-    nt = local / gm;
-}
-
-// Bounded wait with no status side effect, used only while draining.
-__device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity,
-                                                unsigned long long limit_ns)
-{
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_timer_ns() - t0 > limit_ns)
-            return;
-}
-
-// Lane 0 waits (bounded); the verdict is broadcast so the warp stays
-// converged for the .sync.aligned tcgen05 loads that follow.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Watchdog &wd,
-                                          volatile int *abort_flag, uint32_t site, int lane)
-{
-    int ok = 0;
-    if (lane == 0)
-        ok = mbar_wait(bar, parity, wd, abort_flag, site) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok && lane != 0)
-        mbar_wait_quiet(bar, parity, wd.limit_ns);   // already complete: returns at once
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
-{
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
 template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -137,6 +96,8 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     const uint32_t tfull0 = bar0 + 16u * STAGES;              // [NUM_ACC] MMA -> epilogue
     const uint32_t tempty0 = tfull0 + 8u * NUM_ACC;           // [NUM_ACC] epilogue -> MMA
     const uint32_t drain_bar = tempty0 + 8u * NUM_ACC;        // MMA teardown
+    const uint32_t sfready0 = drain_bar + 8u;                 // [STAGES] scales in TMEM -> MMA
+    const uint32_t sffull0 = sfready0 + 8u * STAGES;          // [STAGES] scale loads -> scale warps
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -154,12 +115,17 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
             mbar_init(tempty0 + 8u * a, T::EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(sfready0 + 8u * s, T::SCALE_WARPS);
+            mbar_init(sffull0 + 8u * s, 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
         prefetch_tensormap(&tmD);
     }
+    __syncwarp();
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
         tmem_relinquish();
@@ -190,29 +156,28 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                     const uint32_t sa = base + stage * T::STAGE_BYTES;
                     const uint32_t sb = sa + T::A_BYTES;
                     const uint32_t fb = full0 + 8u * stage;
-                    uint32_t bytes = T::A_BYTES + T::B_BYTES;
-                    int nchunks = 0;
                     if constexpr (T::kFp4) {
-                        nchunks = min(T::SFB_CHUNKS, args.sfb_row_blocks - nt * T::SFB_CHUNKS);
-                        bytes += T::SF_BLOCK_BYTES * (1 + nchunks);
-                    }
-                    mbar_arrive_expect_tx(fb, bytes);
-                    tma_load_2d(sa, &tmA, fb, kb * T::ROW_BYTES, mt * T::BM);
-                    tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN);
-                    if constexpr (T::kFp4) {
-                        // the stage's 16 scale columns are 4 consecutive
-                        // 512-byte blocks of the swizzled layout
+                        // scales first, on their own barrier: the scale warps can
+                        // copy them into TMEM while A and B are still in flight.
+                        // The stage's 16 scale columns are 4 consecutive
+                        // 512-byte blocks of the swizzled layout.
+                        const int nchunks = min(T::SFB_CHUNKS, args.sfb_row_blocks - nt * T::SFB_CHUNKS);
+                        const uint32_t sfb = sffull0 + 8u * stage;
+                        mbar_arrive_expect_tx(sfb, T::SF_BLOCK_BYTES * (1 + nchunks));
                         const uint32_t ssfa = sb + T::B_BYTES;
                         const size_t cb = (size_t)kb * 4u;
                         bulk_load(ssfa, args.sfa + ((size_t)mt * args.sf_col_blocks + cb) * 512u,
-                                  T::SF_BLOCK_BYTES, fb);
+                                  T::SF_BLOCK_BYTES, sfb);
                         for (int c = 0; c < nchunks; ++c) {
                             const size_t rb = (size_t)nt * T::SFB_CHUNKS + (size_t)c;
                             bulk_load(ssfa + T::SFA_BYTES + c * T::SF_BLOCK_BYTES,
                                       args.sfb + (rb * args.sf_col_blocks + cb) * 512u,
-                                      T::SF_BLOCK_BYTES, fb);
+                                      T::SF_BLOCK_BYTES, sfb);
                         }
                     }
+                    mbar_arrive_expect_tx(fb, T::A_BYTES + T::B_BYTES);
+                    tma_load_2d(sa, &tmA, fb, kb * T::ROW_BYTES, mt * T::BM);
+                    tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN);
                     armed_mask |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -224,8 +189,11 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
             if (!ok) {
                 // let copies already issued land before the CTA goes away
                 for (int s = 0; s < STAGES; ++s)
-                    if ((armed_mask >> s) & 1u)
+                    if ((armed_mask >> s) & 1u) {
                         mbar_wait_quiet(full0 + 8u * s, (armed_parity >> s) & 1u, wd.limit_ns);
+                        if constexpr (T::kFp4)
+                            mbar_wait_quiet(sffull0 + 8u * s, (armed_parity >> s) & 1u, wd.limit_ns);
+                    }
             }
         }
     } else if (warp == 1) {
@@ -248,22 +216,19 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                         ok = false;
                         break;
                     }
+                    if constexpr (T::kFp4) {
+                        // the scale warps have written this stage's scales to TMEM
+                        if (!mbar_wait(sfready0 + 8u * stage, phase, wd, abort_flag, 5)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                     tc_fence_after_sync();
                     const uint32_t sa = base + stage * T::STAGE_BYTES;
                     const uint32_t sb = sa + T::A_BYTES;
                     if constexpr (T::kFp4) {
                         const uint32_t sfa_t = tmem + (uint32_t)(NUM_ACC * BN + stage * T::SF_COLS);
                         const uint32_t sfb_t = sfa_t + T::SFA_COLS;
-                        const uint32_t ssfa = sb + T::B_BYTES;
-                        const uint32_t ssfb = ssfa + T::SFA_BYTES;
-#pragma unroll
-                        for (int j = 0; j < T::MMAS; ++j) {
-                            tc_cp_32x128b_warpx4(sfa_t + 4u * j, desc_scale_32x16(ssfa + 512u * j));
-#pragma unroll
-                            for (int c = 0; c < T::SFB_CHUNKS; ++c)
-                                tc_cp_32x128b_warpx4(sfb_t + 4u * (j * T::SFB_CHUNKS + c),
-                                                     desc_scale_32x16(ssfb + T::SF_BLOCK_BYTES * c + 512u * j));
-                        }
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_nvfp4(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
@@ -295,13 +260,51 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
             tc_commit(drain_bar);
             mbar_wait_quiet(drain_bar, 0, wd.limit_ns);
         }
+    } else if (warp < T::EPI_WARP0) {
+        // ------------------------------------------------------------------
+        // Scale warps (NVFP4) : one per TMEM sub-partition
+        // (warp % 4), each writing the stage's block scales from shared
+        // memory into its own 32 TMEM lanes with tcgen05.st -- two store
+        // instructions per warp per stage, in parallel across the four
+        // sub-partitions -- then signalling the MMA thread.
+        // ------------------------------------------------------------------
+        if constexpr (T::kFp4) {
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    // a stage's scale columns are rewritten only after its
+                    // scales were reloaded, i.e. after the MMAs that read the
+                    // previous contents completed (empty -> producer -> sf full)
+                    if (!warp_wait(sffull0 + 8u * stage, phase, wd, abort_flag, 6, lane)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sfa_t = tmem + lane_off + (uint32_t)(NUM_ACC * BN + stage * T::SF_COLS);
+                    const uint32_t ssfa = base + stage * T::STAGE_BYTES + T::A_BYTES + T::B_BYTES;
+                    store_stage_scales<T::SFB_CHUNKS>(sfa_t, sfa_t + T::SFA_COLS, ssfa, ssfa + T::SFA_BYTES,
+                                                      lane);
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(sfready0 + 8u * stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------------
         // Epilogue warpgroup
         // ------------------------------------------------------------------
         const int q = warp & 3;                       // TMEM lane quarter of this warp
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const uint32_t ebuf = s_epi + (uint32_t)(warp - 2) * 2u * T::EPI_BUF_BYTES;
+        const uint32_t ebuf = s_epi + (uint32_t)(warp - T::EPI_WARP0) * 2u * T::EPI_BUF_BYTES;
         float scale = args.alpha;
         if constexpr (!T::kFp4) {
             if (args.sA)
@@ -373,6 +376,10 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
         __syncwarp();
     }
 
+    // Reconverge each warp before the block barrier: the producer and MMA
+    // roles ran on lane 0 only, and the teardown below (tcgen05.dealloc) is a
+    // warp-collective instruction that needs all 32 lanes together.
+    __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 1) {
@@ -402,33 +409,33 @@ template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 static constexpr PlanInfo make_plan(const char *name)
 {
     using T = Tile<KIND, BN, STAGES, NUM_ACC>;
-    return PlanInfo{name, KIND, T::BM, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES, T::THREADS,
-                    T::TMEM_COLS};
+    return PlanInfo{name, KIND, 1, T::BM, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
+                    T::THREADS, T::TMEM_COLS};
 }
 
-#define BSG_PLANS(X)                                             \
+#define BSG_TC1_PLANS(X)                                         \
     X(Kind::NVFP4, 256, 3, 1, "nvfp4_tc1_128x256_s3_acc1")       \
     X(Kind::NVFP4, 128, 5, 2, "nvfp4_tc1_128x128_s5_acc2")       \
     X(Kind::FP8, 256, 4, 2, "fp8_tc1_128x256_s4_acc2")           \
     X(Kind::FP8, 128, 6, 2, "fp8_tc1_128x128_s6_acc2")
 
 #define BSG_PLAN_INFO(K, BN, S, A, NAME) make_plan<K, BN, S, A>(NAME),
-static const PlanInfo kPlans[] = {BSG_PLANS(BSG_PLAN_INFO)};
+static const PlanInfo kTc1Plans[] = {BSG_TC1_PLANS(BSG_PLAN_INFO)};
 #undef BSG_PLAN_INFO
 
-int num_plans() { return (int)(sizeof(kPlans) / sizeof(kPlans[0])); }
+int tc1_num_plans() { return (int)(sizeof(kTc1Plans) / sizeof(kTc1Plans[0])); }
 
-const PlanInfo &plan_info(int id) { return kPlans[id]; }
+const PlanInfo &tc1_plan(int i) { return kTc1Plans[i]; }
 
-cudaError_t launch_gemm(int id, const GemmMaps &maps, const GemmArgs &args, int grid,
-                        cudaStream_t stream)
+cudaError_t tc1_launch(int id, const GemmMaps &maps, const GemmArgs &args, int grid,
+                       cudaStream_t stream)
 {
     int i = 0;
 #define BSG_PLAN_LAUNCH(K, BN, S, A, NAME)                         \
     if (id == i)                                                  \
         return launch_impl<K, BN, S, A>(maps, args, grid, stream); \
     ++i;
-    BSG_PLANS(BSG_PLAN_LAUNCH)
+    BSG_TC1_PLANS(BSG_PLAN_LAUNCH)
 #undef BSG_PLAN_LAUNCH
     return cudaErrorInvalidValue;
 }

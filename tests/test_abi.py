@@ -82,13 +82,16 @@ def test_swizzled_bytes(lib):
 
 def test_planner_enumeration(lib):
     # every shape of the workloads picks a plan of its own kind; N <= 128
-    # takes the 128-wide tile, everything else the 256-wide one
+    # takes a 128-wide tile, everything else a 256-wide one; M <= 128 stays
+    # on one SM, larger M uses the CTA-pair tiles (except FP8 with N <= 128)
     for kind, prefix in ((0, "nvfp4_"), (1, "fp8_")):
-        for M in (1, 64, 256, 4096, 16384):
+        for M in (1, 64, 128, 129, 256, 4096, 16384):
             for N in (8, 128, 136, 256, 3072, 12288, 16384):
                 name = bsg.bsg_select_plan(kind, M, N, 4096, 152)
                 assert name.startswith(prefix), name
                 assert ("x128_" in name) == (N <= 128), (N, name)
+                pair = "_tc2_" in name
+                assert pair == (M > 128 and not (kind == 1 and N <= 128)), (M, N, name)
 
 
 def test_forced_plan(lib):
@@ -102,7 +105,7 @@ def test_forced_plan(lib):
             bsg.bsg_select_plan(1, 4096, 4096, 4096, 152)
     finally:
         bsg.bsg_force_plan(None)
-    assert bsg.bsg_select_plan(0, 4096, 4096, 4096, 152) == "nvfp4_tc1_128x256_s3_acc1"
+    assert bsg.bsg_select_plan(0, 4096, 4096, 4096, 152) == "nvfp4_tc2_256x256_s5_acc1"
 
 
 def test_error_strings(lib):

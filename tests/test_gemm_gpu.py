@@ -88,8 +88,9 @@ def oracle_nvfp4(p, rows=None, cols=None):
                                    rows=rows, cols=cols)
 
 
-NVFP4_PLANS = ["nvfp4_tc1_128x256_s3_acc1", "nvfp4_tc1_128x128_s5_acc2"]
-FP8_PLANS = ["fp8_tc1_128x256_s4_acc2", "fp8_tc1_128x128_s6_acc2"]
+NVFP4_PLANS = ["nvfp4_tc1_128x256_s3_acc1", "nvfp4_tc1_128x128_s5_acc2",
+               "nvfp4_tc2_256x256_s5_acc1", "nvfp4_tc2_256x128_s6_acc2"]
+FP8_PLANS = ["fp8_tc1_128x256_s4_acc2", "fp8_tc1_128x128_s6_acc2", "fp8_tc2_256x256_s6_acc2"]
 
 
 @pytest.fixture(params=[None] + NVFP4_PLANS, ids=["auto"] + NVFP4_PLANS)
@@ -175,13 +176,31 @@ def test_nvfp4_one_hot_decode(dev, nvfp4_plan, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 256), (200, 328, 512), (257, 392, 768), (130, 136, 1280),
-                                   (64, 3072, 3072)])
+                                   (64, 3072, 3072), (520, 648, 1024)])
 def test_nvfp4_ragged(dev, nvfp4_plan, M, N, K):
     """Tails in M and N (TMA zero fill and store clipping), several k-blocks."""
     p = workloads.make_nvfp4(workloads.WORKLOADS["nvfp4_4096"], "cpu", M=M, N=N, K=K)
     got = gpu_nvfp4(p, dev)
     _, T, ref = oracle_nvfp4(p)
     assert_close(got, ref, T, f"nvfp4 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("rep", [0, 1])
+def test_nvfp4_long_k(dev, nvfp4_plan, rep):
+    """K = 16384 (64 ring stages per tile, every stage with fresh 2^u scales),
+    full comparison: exercises the scale-copy / MMA ordering on every stage."""
+    w = workloads.WORKLOADS["nvfp4_256"]
+    g = torch.Generator().manual_seed(77 + rep)
+    M, N, K = 384, 512, 16384
+    p = dict(M=M, N=N, K=K, alpha=1.0,
+             A=torch.randint(0, 256, (M, K // 2), generator=g, dtype=torch.int32).to(torch.uint8),
+             B=torch.randint(0, 256, (N, K // 2), generator=g, dtype=torch.int32).to(torch.uint8),
+             sfA=workloads.uniform_nvfp4(M, K, 5 + rep, "cpu")[1],
+             sfB=workloads.uniform_nvfp4(N, K, 9 + rep, "cpu")[1])
+    del w
+    got = gpu_nvfp4(p, dev, "swizzled")
+    _, T, ref = oracle_nvfp4(p)
+    assert_close(got, ref, T, f"nvfp4 long K rep {rep}")
 
 
 def test_nvfp4_multi_tile_alpha(dev):
