@@ -273,12 +273,14 @@ def secondary_fp8(dev, steps: int, warmup: int, pk: dict, psrc: str) -> dict:
 
 
 def secondary_skinny(dev, steps: int, pk: dict, psrc: str) -> dict:
-    """Each cell timed cold: buffers rotated over > 4x L2 so every launch
-    reads its weights from HBM; median of per-launch CUDA-event times."""
+    """Each cell timed cold and back to back: a CUDA graph of one launch per
+    buffer set, the sets rotated over > 4x L2 so every launch reads its
+    weights from HBM, replayed `steps` times; per-launch time = median replay
+    time / launches in the graph."""
     import block_scaled_precision_persistent_gb300 as bsg
     out = {}
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    s = torch.cuda.current_stream()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     for name, w in workloads.WORKLOADS.items():
         if "skinny" not in name:
             continue
@@ -286,33 +288,43 @@ def secondary_skinny(dev, steps: int, pk: dict, psrc: str) -> dict:
         M, N, K = w.M, w.N, w.K
         swA = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
         swB = torch.empty(bsg.nvfp4_swizzled_scale_bytes(N, K), dtype=torch.uint8, device=dev)
-        bsg.nvfp4_swizzle_scales(M, K, p["sfA"], swA, s)
-        bsg.nvfp4_swizzle_scales(N, K, p["sfB"], swB, s)
+        bsg.nvfp4_swizzle_scales(M, K, p["sfA"], swA)
+        bsg.nvfp4_swizzle_scales(N, K, p["sfB"], swB)
         per = w.algorithmic_bytes
         copies = max(2, int(4 * l2 // per) + 1)
         sets = [(p["A"].clone(), swA.clone(), p["B"].clone(), swB.clone(),
                  torch.empty((M, N), dtype=torch.bfloat16, device=dev)) for _ in range(copies)]
-        for A, sa, B, sb, D in sets[:3]:
-            bsg.nvfp4_gemm_swizzled(M, N, K, A, sa, B, sb, p["alpha"], D, s)
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            for A, sa, B, sb, D in sets[:3]:
+                bsg.nvfp4_gemm_swizzled(M, N, K, A, sa, B, sb, p["alpha"], D)
         torch.cuda.synchronize()
-        evs = []
-        for i in range(max(steps, copies)):
-            A, sa, B, sb, D = sets[i % copies]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for A, sa, B, sb, D in sets:
+                bsg.nvfp4_gemm_swizzled(M, N, K, A, sa, B, sb, p["alpha"], D)
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(steps):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(s)
-            bsg.nvfp4_gemm_swizzled(M, N, K, A, sa, B, sb, p["alpha"], D, s)
-            b.record(s)
-            evs.append((a, b))
-        torch.cuda.synchronize()
-        us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) / copies)
+        if bsg.bsg_get_device_status() != bsg.BSG_OK:
+            raise RuntimeError(f"device status set during skinny cell {name}")
+        us = statistics.median(ts) * 1e3
         gbs = per / (us * 1e-6) / 1e9
         ideal_us = max(per / (pk["hbm_gbs"] * 1e9), w.flops / (pk["bf16_tflops"] * FP4_PER_BF16 * 1e12)) * 1e6
-        out[f"m{M}_n{N}_k{K}"] = {"us": round(us, 3), "hbm_gbs": round(gbs, 1),
-                                  "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
-                                  "frac_roofline": round(ideal_us / us, 4)}
-        del sets
+        out[f"m{M}_n{N}_k{K}"] = {"plan": bsg.bsg_select_plan(0, M, N, K, sms), "us": round(us, 3),
+                                  "hbm_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                                  "ideal_us": round(ideal_us, 3), "frac_roofline": round(ideal_us / us, 4)}
+        del g, sets
     return {"cells": out, "peak_hbm_gbs": pk["hbm_gbs"], "peak_source": psrc,
-            "timing": "cold L2 (buffers rotated over > 4x L2), median per-launch CUDA events"}
+            "timing": "cold L2 (buffer sets rotated over > 4x L2), CUDA graph of back-to-back launches, "
+                      "median over replays of graph time / launches"}
 
 
 def cpu_baseline(w: workloads.Workload, p_host: dict, budget_s: float = 15.0) -> dict:

@@ -96,20 +96,33 @@ size_t swizzled_bytes(int rows, int K)
     return pr * pc;
 }
 
-// Planner: the default plan for a shape; -1 if none fits.
+// Planner: the default plan for a shape; -1 if none fits. The rules follow
+// CUDA-graph timings of every plan on the skinny cells (M 64..512 x N 3072 /
+// 12288 x K 3072 / 12288, cold L2) and the square sizes:
+//   * NVFP4, M <= 256: the swap-AB split-K kernel when the weight tiles leave
+//     room to split K at least in two with the whole grid resident (N/128
+//     tiles x 2 <= SMs); above 128 activation rows only for long K (>= 8192),
+//     where streaming the weights dominates its fixed costs;
+//   * otherwise, while 128 x 128 output tiles number at most 4 per SM, the
+//     1-SM 128 x 128 kernel (more CTAs in flight than 256-wide tiles);
+//   * M <= 128 beyond that: the 1-SM 128 x 256 kernel; larger M: the CTA
+//     pair (256 x 128 for N <= 128, else 256 x 256).
 int default_plan(Kind kind, int M, int N, int K, int num_sms)
 {
-    (void)M;
-    (void)K;
-    (void)num_sms;
     const char *name = nullptr;
-    const bool small_m = M <= 128;   // a 256-row pair tile would idle half its SMs
+    const long long tiles128 = (long long)((M + 127) / 128) * (long long)((N + 127) / 128);
+    const bool few_tiles = tiles128 <= 4LL * num_sms;
     if (kind == Kind::NVFP4) {
-        if (small_m)
-            name = N <= 128 ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc1_128x256_s3_acc1";
+        const int weight_tiles = (N + 127) / 128;
+        const bool can_split = 2 * weight_tiles <= num_sms && K >= 512;
+        if (M <= 256 && can_split && (M <= 128 || K >= 8192))
+            name = M <= 64 ? "nvfp4_skinny_m64_s6" : M <= 128 ? "nvfp4_skinny_m128_s3" : "nvfp4_skinny_m256_s4";
+        else if (few_tiles || N <= 128)
+            name = M <= 128 || few_tiles ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc2_256x128_s6_acc2";
         else
-            name = N <= 128 ? "nvfp4_tc2_256x128_s6_acc2" : "nvfp4_tc2_256x256_s5_acc1";
+            name = M <= 128 ? "nvfp4_tc1_128x256_s3_acc1" : "nvfp4_tc2_256x256_s5_acc1";
     } else {
+        const bool small_m = M <= 128;   // a 256-row pair tile would idle half its SMs
         if (small_m)
             name = N <= 128 ? "fp8_tc1_128x128_s6_acc2" : "fp8_tc1_128x256_s4_acc2";
         else
@@ -126,7 +139,8 @@ int choose_plan(Kind kind, int M, int N, int K, int num_sms, int *plan)
         forced = g_forced_plan;
     }
     if (forced >= 0) {
-        if (bsg::plan_info(forced).kind != kind)
+        const PlanInfo &fp = bsg::plan_info(forced);
+        if (fp.kind != kind || (fp.family == bsg::Family::SKINNY && M > fp.tile_m))
             return BSG_ERR_NO_PLAN;
         *plan = forced;
         return BSG_OK;
@@ -152,6 +166,75 @@ int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *ptr, uint
     return r == CUDA_SUCCESS ? BSG_OK : BSG_ERR_CUDA;
 }
 
+// Resident clusters of `splits` CTAs for skinny plan id on the current
+// device (cached; splits a power of two <= 8).
+int skinny_cluster_capacity(int id, int splits)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || id < 0 || id >= 8)
+        return 0;
+    static int cache[kMaxDevices][8][4] = {};
+    const int j = splits == 2 ? 1 : splits == 4 ? 2 : splits == 8 ? 3 : 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (cache[dev][id][j] == 0)
+        cache[dev][id][j] = bsg::skinny_max_clusters(id, splits);
+    return cache[dev][id][j];
+}
+
+int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A, const void *B,
+               const uint8_t *sfa, const uint8_t *sfb, float alpha, void *D, cudaStream_t stream,
+               DeviceState *ds);
+
+// Swap-AB split-K launch for skinny M: weight tiles of 128 rows on grid x,
+// the K split on grid y (one thread-block cluster per weight tile).
+int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A, const void *B,
+               const uint8_t *sfa, const uint8_t *sfb, float alpha, void *D, cudaStream_t stream,
+               DeviceState *ds)
+{
+    const int id = plan - bsg::tc1_num_plans() - bsg::pair_num_plans();
+    const int num_n_tiles = (N + pi.bn - 1) / pi.bn;
+    const int num_k_blocks = K / pi.k_block;
+    // split K as far as the whole grid stays resident at once: the largest
+    // S in {1, 2, 4, 8}, S <= K/256, whose clusters all fit on the device
+    int splits = 1;
+    for (int s = 2; s <= 8; s *= 2)
+        if (s <= num_k_blocks && num_n_tiles <= skinny_cluster_capacity(id, s))
+            splits = s;
+    const uint64_t row_bytes = (uint64_t)K / 2u;
+    GemmMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    int rc;
+    if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes,
+                        128, (uint32_t)pi.tile_m)) != BSG_OK ||
+        (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, (uint64_t)N, row_bytes,
+                        128, (uint32_t)pi.bn)) != BSG_OK ||
+        (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)M,
+                        (uint64_t)N * 2u, (uint32_t)(pi.bn / splits), (uint32_t)pi.tile_m,
+                        CU_TENSOR_MAP_SWIZZLE_NONE)) != BSG_OK)
+        return rc;
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.num_m_tiles = 1;
+    a.num_n_tiles = num_n_tiles;
+    a.num_k_blocks = num_k_blocks;
+    a.raster_group = 1;
+    a.sf_col_blocks = (K / 16 + 3) / 4;
+    a.sfb_row_blocks = (N + 127) / 128;
+    a.sfx_row_blocks = (M + 127) / 128;
+    a.sfa = sfa;
+    a.sfb = sfb;
+    a.alpha = alpha;
+    a.status = ds->status;
+    a.timeout_ns = g_watchdog_ns.load();
+    if (bsg::skinny_launch(id, maps, a, splits, stream) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    ++t_last_launches;
+    return BSG_OK;
+}
+
 // Encode the maps and launch one persistent GEMM.
 int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const uint8_t *sfa,
              const uint8_t *sfb, const float *sA, const float *sB, float alpha, void *D,
@@ -163,6 +246,8 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
         return rc;
     const PlanInfo &pi = bsg::plan_info(plan);
     const uint64_t row_bytes = kind == Kind::NVFP4 ? (uint64_t)K / 2u : (uint64_t)K;
+    if (pi.family == bsg::Family::SKINNY)
+        return run_skinny(plan, pi, M, N, K, A, B, sfa, sfb, alpha, D, stream, ds);
 
     GemmMaps maps;
     std::memset(&maps, 0, sizeof maps);
@@ -196,7 +281,7 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     a.num_m_tiles = (M + pi.tile_m - 1) / pi.tile_m;
     a.num_n_tiles = (N + pi.bn - 1) / pi.bn;
     a.num_k_blocks = K / pi.k_block;
-    a.raster_group = 8;
+    a.raster_group = 8;                 // M tiles per rasterisation group (L2 reuse of B)
     a.sf_col_blocks = (K / 16 + 3) / 4;
     a.sfb_row_blocks = (N + 127) / 128;
     a.sfa = sfa;
@@ -255,11 +340,14 @@ size_t round256(size_t x) { return (x + 255u) & ~(size_t)255u; }
 }  // namespace
 
 namespace bsg {
-int num_plans() { return tc1_num_plans() + pair_num_plans(); }
+int num_plans() { return tc1_num_plans() + pair_num_plans() + skinny_num_plans(); }
 
 const PlanInfo &plan_info(int id)
 {
-    return id < tc1_num_plans() ? tc1_plan(id) : pair_plan(id - tc1_num_plans());
+    if (id < tc1_num_plans())
+        return tc1_plan(id);
+    id -= tc1_num_plans();
+    return id < pair_num_plans() ? pair_plan(id) : skinny_plan(id - pair_num_plans());
 }
 
 cudaError_t launch_gemm(int id, const GemmMaps &maps, const GemmArgs &args, int grid,

@@ -11,6 +11,10 @@ namespace bsg {
 
 enum class Kind : int { NVFP4 = 0, FP8 = 1 };
 
+// Kernel families: persistent 1-SM tiles, persistent CTA-pair tiles, and the
+// swap-AB split-K kernel for skinny M.
+enum class Family : int { TC1 = 0, PAIR = 1, SKINNY = 2 };
+
 // Everything a persistent GEMM launch needs besides its tensor maps.
 struct GemmArgs {
     int M, N, K;
@@ -18,6 +22,7 @@ struct GemmArgs {
     int raster_group;          // M tiles per rasterisation group
     int sf_col_blocks;         // NVFP4: 4-scale column blocks per 128-row block (K/64)
     int sfb_row_blocks;        // NVFP4: 128-row blocks of the swizzled B scales
+    int sfx_row_blocks;        // skinny NVFP4: 128-row blocks of the swizzled A scales
     const uint8_t *sfa;        // NVFP4: swizzled A scales
     const uint8_t *sfb;        // NVFP4: swizzled B scales
     float alpha;
@@ -31,8 +36,10 @@ struct GemmArgs {
 struct PlanInfo {
     const char *name;
     Kind kind;
+    Family family;
     int cta_group;             // 1: one SM per tile; 2: a CTA pair shares one tile
-    int tile_m, bn;            // output tile of one scheduling unit (CTA or pair)
+    int tile_m, bn;            // output tile of one scheduling unit (CTA or pair);
+                               // skinny: max activation rows, weight rows per CTA
     int stages;                // smem ring depth
     int num_acc;               // TMEM accumulator buffers
     int k_block;               // K elements per ring stage
@@ -46,8 +53,8 @@ struct GemmMaps {
     CUtensorMap a, b, d, sfa, sfb;
 };
 
-// Plan registry: the 1-SM plans (gemm_persistent.cu) followed by the
-// CTA-pair plans (gemm_pair.cu).
+// Plan registry: the 1-SM plans (gemm_persistent.cu), then the CTA-pair plans
+// (gemm_pair.cu), then the skinny plans (gemm_skinny.cu).
 int num_plans();
 const PlanInfo &plan_info(int id);
 int find_plan(const char *name);
@@ -69,6 +76,14 @@ const PlanInfo &pair_plan(int i);
 cudaError_t pair_launch(int i, const GemmMaps &maps, const GemmArgs &args, int grid,
                         cudaStream_t stream);
 int pair_max_clusters(int i);
+int skinny_num_plans();
+const PlanInfo &skinny_plan(int i);
+// maps.d: D with a {128 / splits, tile_m} box (no swizzle).
+cudaError_t skinny_launch(int i, const GemmMaps &maps, const GemmArgs &args, int splits,
+                          cudaStream_t stream);
+// Thread-block clusters of `splits` CTAs of skinny plan i that fit on the
+// device at once (0 if the query fails).
+int skinny_max_clusters(int i, int splits);
 
 // Scale-layout prep kernel. Returns a cudaError_t.
 cudaError_t launch_swizzle_scales(int rows, int K, const uint8_t *sf, uint8_t *out,

@@ -461,7 +461,7 @@ template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 static constexpr PlanInfo make_pair_plan(const char *name)
 {
     using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
-    return PlanInfo{name, KIND, 2, T::TILE_M, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
+    return PlanInfo{name, KIND, Family::PAIR, 2, T::TILE_M, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
                     T::THREADS, T::TMEM_COLS};
 }
 

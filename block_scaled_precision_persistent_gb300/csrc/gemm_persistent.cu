@@ -409,7 +409,7 @@ template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 static constexpr PlanInfo make_plan(const char *name)
 {
     using T = Tile<KIND, BN, STAGES, NUM_ACC>;
-    return PlanInfo{name, KIND, 1, T::BM, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
+    return PlanInfo{name, KIND, Family::TC1, 1, T::BM, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
                     T::THREADS, T::TMEM_COLS};
 }
 

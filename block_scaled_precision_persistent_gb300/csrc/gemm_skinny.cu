@@ -1,0 +1,505 @@
+// Skinny-M NVFP4 GEMM (M <= 256 activation rows, large N x K weights): the
+// memory-bound weight-streaming shape of a projection layer.
+//
+// A regular 128 x 256 output tiling gives such shapes only ceil(N/256) tiles
+// per 128 rows -- 12 to 48 CTAs on a 152-SM GPU -- and every CTA walks all of
+// K, so most SMs idle and the weights stream through a handful of them. This
+// kernel instead
+//   * swaps the operands: it computes D^T = (B * sB)(A * sA)^T, so 128 weight
+//     rows are the MMA's M side and the (padded) activation rows its N side;
+//   * splits K across a thread-block cluster of S CTAs (S in {1, 2, 4, 8},
+//     chosen by the host so that the whole grid is resident at once) so that
+//     (N/128) * S CTAs stream disjoint weight bytes in parallel;
+//   * reduces the S partial accumulators inside the cluster, with no partials
+//     in HBM and no cluster-wide barrier on the critical path: weight row n of
+//     the tile belongs to CTA n / (128/S). Every CTA pushes the rows it does
+//     not own straight from TMEM into the owner's shared memory (st.async,
+//     16 bytes at a time, each completing bytes on the owner's mbarrier); the
+//     owner sums the S terms of its rows in rank order (deterministic),
+//     stages them as BF16 in shared memory and writes its [M x 128/S] block
+//     of D with one TMA store. The receive area aliases the owner's drained
+//     stage ring, so a sender pushes only after every peer has said that its
+//     ring is free (one relaxed remote arrive per peer once its MMAs have
+//     completed).
+// The first stages' loads are issued by the initialising thread before the
+// block-wide setup barrier, so HBM latency overlaps TMEM allocation.
+// Everything else follows the persistent 1-SM kernel: TMA producer warp, one
+// MMA thread (tcgen05.mma kind::mxf4nvf4 block_scale, FP32 accumulator in
+// TMEM), four scale-writer warps (tcgen05.st, one per TMEM sub-partition),
+// four epilogue warps.
+#include <cuda_bf16.h>
+
+#include "bsg_internal.h"
+#include "gemm_common.cuh"
+#include "ptx.cuh"
+
+namespace bsg {
+
+template <int M_PAD, int STAGES>
+struct SkinnyTile {
+    static constexpr int BW = 128;                        // weight rows per CTA (MMA M)
+    static constexpr int ROW_BYTES = 128;
+    static constexpr int K_BLOCK = 256;
+    static constexpr int MMA_K_BYTES = 32;
+    static constexpr int MMAS = ROW_BYTES / MMA_K_BYTES;
+    static constexpr int W_BYTES = BW * ROW_BYTES;        // weights (MMA A operand)
+    static constexpr int X_BYTES = M_PAD * ROW_BYTES;     // activations (MMA B operand)
+    static constexpr int SF_BLOCK_BYTES = 2048;
+    static constexpr int SFX_CHUNKS = (M_PAD + 127) / 128;
+    static constexpr int SFW_BYTES = SF_BLOCK_BYTES;
+    static constexpr int SFX_BYTES = SFX_CHUNKS * SF_BLOCK_BYTES;
+    static constexpr int STAGE_BYTES = W_BYTES + X_BYTES + SFW_BYTES + SFX_BYTES;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    // receive area: FP32 [sender rank][column / 4][owned row][column % 4]
+    // (S x 128/S = 128 rows): 32 lanes pushing or reading the same 4 columns
+    // of consecutive rows touch 512 consecutive bytes
+    static constexpr int RECV_BYTES = BW * M_PAD * 4;
+    // output staging, BF16 [M_PAD][128/S], placed after the receive area
+    static constexpr int OUT_BYTES = M_PAD * BW * 2;
+    static constexpr int NUM_BARS = 3 * STAGES + 4;
+    static constexpr int BAR_BYTES = NUM_BARS * 8 + 16;
+    // the receive and staging areas get shared memory of their own when it
+    // fits beside the ring (peers may then push as soon as their own MMAs are
+    // done); otherwise they alias the drained ring and a sender first waits
+    // for every peer to report its ring free
+    static constexpr bool OWN_RECV = 1024 + RING_BYTES + RECV_BYTES + OUT_BYTES + BAR_BYTES <= 232448;
+    static constexpr int RECV_OFF = OWN_RECV ? RING_BYTES : 0;
+    static constexpr int AREA = OWN_RECV ? RING_BYTES + RECV_BYTES + OUT_BYTES
+                                         : (RING_BYTES > RECV_BYTES + OUT_BYTES ? RING_BYTES
+                                                                                : RECV_BYTES + OUT_BYTES);
+    static constexpr int SMEM_BYTES = 1024 + AREA + BAR_BYTES;
+    static constexpr int SCALE_WARPS = 4;
+    static constexpr int EPI_WARP0 = 2 + SCALE_WARPS;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+    static constexpr int SFA_COLS = 4 * MMAS;                     // weights' scales
+    static constexpr int SFB_COLS = 4 * SFX_CHUNKS * MMAS;        // activations' scales
+    static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
+    static constexpr int TMEM_USED = M_PAD + STAGES * SF_COLS;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
+                                     : TMEM_USED <= 64  ? 64
+                                     : TMEM_USED <= 128 ? 128
+                                     : TMEM_USED <= 256 ? 256
+                                                        : 512;
+    // CTAs per SM the shared memory and TMEM budgets allow (228 KiB and 512
+    // columns per SM, 1 KiB of shared memory reserved per CTA)
+    static constexpr int CTAS_PER_SM = (2 * (SMEM_BYTES + 1024) <= 233472 && 2 * TMEM_COLS <= 512) ? 2 : 1;
+    static constexpr uint32_t IDESC = idesc_nvfp4(BW, M_PAD);
+
+    static_assert(M_PAD % 32 == 0 && M_PAD >= 32 && M_PAD <= 256, "activation tile");
+    static_assert(TMEM_USED <= 512, "TMEM: accumulator plus scales exceed 512 columns");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
+};
+
+// args: num_n_tiles = weight tiles (N/128), num_k_blocks = K/256 (whole K);
+// the split count S is the cluster size (gridDim.y), a power of two <= 8 and
+// <= num_k_blocks.
+// The owned block's reduction, spread over the epilogue's threads: item
+// (cq, r) sums columns [4 cq, 4 cq + 4) of owned row r over the S partials in
+// the receive area, in rank order, scales them and stages them as BF16
+// [m][r] (row stride rpo) for the TMA store.
+template <int S>
+__device__ __forceinline__ void reduce_owned(const uint8_t *recv, __nv_bfloat16 *out, int rpo, int live_cols,
+                                             float alpha, int t, int nthreads)
+{
+    const int items = (live_cols / 4) * rpo;
+    const int slot_bytes = rpo * live_cols * 4;
+    for (int idx = t; idx < items; idx += nthreads) {
+        const uint8_t *p = recv + idx * 16;          // [cq][r] with r fastest: idx == cq * rpo + r
+        float4 v[S];
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+            v[s] = *reinterpret_cast<const float4 *>(p + s * slot_bytes);
+        float4 a = v[0];
+#pragma unroll
+        for (int s = 1; s < S; ++s) {
+            a.x += v[s].x;
+            a.y += v[s].y;
+            a.z += v[s].z;
+            a.w += v[s].w;
+        }
+        const int r = idx % rpo;
+        const int m0 = (idx / rpo) * 4;
+        out[(m0 + 0) * rpo + r] = __float2bfloat16_rn(a.x * alpha);
+        out[(m0 + 1) * rpo + r] = __float2bfloat16_rn(a.y * alpha);
+        out[(m0 + 2) * rpo + r] = __float2bfloat16_rn(a.z * alpha);
+        out[(m0 + 3) * rpo + r] = __float2bfloat16_rn(a.w * alpha);
+    }
+}
+
+template <int M_PAD, int STAGES>
+__global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
+                                  SkinnyTile<M_PAD, STAGES>::CTAS_PER_SM)
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmD, const GemmArgs args)
+{
+    using T = SkinnyTile<M_PAD, STAGES>;
+    if (threadIdx.x == 0) {              // before any parameter read: the descriptor fetches overlap it
+        prefetch_tensormap(&tmW);
+        prefetch_tensormap(&tmX);
+        prefetch_tensormap(&tmD);
+    }
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + T::AREA);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t full0 = bar0;                       // [STAGES] operands -> MMA
+    const uint32_t empty0 = full0 + 8u * STAGES;       // [STAGES] MMA done -> producer
+    const uint32_t sfready0 = empty0 + 8u * STAGES;    // [STAGES] scales in TMEM -> MMA
+    const uint32_t tfull = sfready0 + 8u * STAGES;     // accumulator complete -> epilogue
+    const uint32_t drain_bar = tfull + 8u;
+    const uint32_t peer_free = drain_bar + 8u;         // every peer's ring may be written
+    const uint32_t rx = peer_free + 8u;                // the peers' rows have landed here
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const Watchdog wd{args.status, args.timeout_ns};
+    const int nt = blockIdx.x;                          // weight tile
+    const int S = gridDim.y;                            // K split == cluster size
+    const int split = blockIdx.y;
+    const uint32_t rank = cluster_ctarank();
+    const int kb0 = (int)((long long)args.num_k_blocks * split / S);
+    const int kb1 = (int)((long long)args.num_k_blocks * (split + 1) / S);
+    const int nkb = kb1 - kb0;
+    const int rpo = T::BW / S;                          // weight rows each CTA owns
+    const int live_cols = min(M_PAD, (args.M + 31) / 32 * 32);   // accumulator columns in use
+
+    // Producer step i: weights, activations and both scale blocks of k-block
+    // kb0 + i into ring stage i % STAGES, all counted on that stage's full
+    // barrier (the scale writers wait on it too).
+    auto produce = [&](int i) -> bool {
+        const int stage = i % STAGES;
+        const uint32_t phase = (uint32_t)(i / STAGES) & 1u;
+        if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wd, abort_flag, 1))
+            return false;
+        const int kb = kb0 + i;
+        const uint32_t sw = base + stage * T::STAGE_BYTES;
+        const uint32_t sx = sw + T::W_BYTES;
+        const uint32_t ssw = sx + T::X_BYTES;
+        const uint32_t ssx = ssw + T::SFW_BYTES;
+        const uint32_t fb = full0 + 8u * stage;
+        const int nchunks = min(T::SFX_CHUNKS, args.sfx_row_blocks);
+        mbar_arrive_expect_tx(fb, T::W_BYTES + T::X_BYTES + T::SF_BLOCK_BYTES * (1 + nchunks));
+        const size_t cb = (size_t)kb * 4u;
+        // weights' scales (row block nt), activations' scales (row blocks 0..)
+        bulk_load(ssw, args.sfb + ((size_t)nt * args.sf_col_blocks + cb) * 512u, T::SF_BLOCK_BYTES, fb);
+        for (int c = 0; c < nchunks; ++c)
+            bulk_load(ssx + c * T::SF_BLOCK_BYTES, args.sfa + ((size_t)c * args.sf_col_blocks + cb) * 512u,
+                      T::SF_BLOCK_BYTES, fb);
+        tma_load_2d(sw, &tmW, fb, kb * T::ROW_BYTES, nt * T::BW);
+        tma_load_2d(sx, &tmX, fb, kb * T::ROW_BYTES, 0);
+        return true;
+    };
+
+    const int first = min(STAGES, nkb);
+    bool producing = true;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+            mbar_init(sfready0 + 8u * s, T::SCALE_WARPS);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(drain_bar, 1);
+        mbar_init(peer_free, S > 1 ? (uint32_t)(S - 1) : 1u);
+        mbar_init(rx, 1);
+        *abort_flag = 0;
+        fence_mbar_init();               // initialised barriers: visible to the TMA unit and the peers
+        for (int i = 0; i < first && producing; ++i)
+            producing = produce(i);
+        if (S > 1)                       // the peers' rows, pushed with complete_tx
+            mbar_arrive_expect_tx(rx, (uint32_t)((S - 1) * rpo * live_cols * 4));
+    }
+    __syncwarp();
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (S > 1)
+        cluster_arrive_relaxed();        // this CTA's barriers are initialised
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0)
+            for (int i = first; i < nkb && producing; ++i)
+                producing = produce(i);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------
+        // MMA issuer
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int i = 0; i < nkb; ++i) {
+                if (!mbar_wait(full0 + 8u * stage, phase, wd, abort_flag, 3) ||
+                    !mbar_wait(sfready0 + 8u * stage, phase, wd, abort_flag, 5)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sw = base + stage * T::STAGE_BYTES;
+                const uint32_t sx = sw + T::W_BYTES;
+                const uint32_t sfa_t = tmem + (uint32_t)(M_PAD + stage * T::SF_COLS);
+                const uint32_t sfb_t = sfa_t + T::SFA_COLS;
+#pragma unroll
+                for (int j = 0; j < T::MMAS; ++j)
+                    mma_nvfp4(tmem, desc_kmajor_sw128(sw + T::MMA_K_BYTES * j),
+                              desc_kmajor_sw128(sx + T::MMA_K_BYTES * j), T::IDESC, sfa_t + 4u * j,
+                              sfb_t + 4u * j * T::SFX_CHUNKS, (i | j) != 0 ? 1u : 0u);
+                tc_commit(empty0 + 8u * stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (ok && nkb > 0)
+                tc_commit(tfull);
+            tc_commit(drain_bar);
+            mbar_wait_quiet(drain_bar, 0, wd.limit_ns);
+        }
+    } else if (warp < T::EPI_WARP0) {
+        // ------------------------------------------------------------------
+        // Scale writers: weights' scales as the MMA's A-side scales,
+        // activations' as its B-side scales
+        // ------------------------------------------------------------------
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int i = 0; i < nkb; ++i) {
+            if (!warp_wait(full0 + 8u * stage, phase, wd, abort_flag, 6, lane))
+                break;
+            const uint32_t ssw = base + stage * T::STAGE_BYTES + T::W_BYTES + T::X_BYTES;
+            const uint32_t sfa_t = tmem + lane_off + (uint32_t)(M_PAD + stage * T::SF_COLS);
+            store_stage_scales<T::SFX_CHUNKS>(sfa_t, sfa_t + T::SFA_COLS, ssw, ssw + T::SFW_BYTES, lane);
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(sfready0 + 8u * stage);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------
+        // Epilogue: TMEM lane n (warp q = n / 32) holds weight row n of the
+        // tile, column m its dot product with activation row m. Receive area:
+        // FP32 [sender rank][column / 4][owned row][column % 4], one slot of
+        // rpo * live_cols floats per rank.
+        // ------------------------------------------------------------------
+        const int q = warp & 3;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int n = q * 32 + lane;
+        const int owner = n / rpo;
+        const int orow = n - owner * rpo;               // row within the owner's share
+        const int et = threadIdx.x - 32 * T::EPI_WARP0; // 0 .. 127
+        const float alpha = args.alpha;
+        uint8_t *const recv = gbase + T::RECV_OFF;
+        __nv_bfloat16 *const out = reinterpret_cast<__nv_bfloat16 *>(recv + T::RECV_BYTES);
+        const int own_lo = (int)rank * rpo;             // rows this CTA owns: [own_lo, own_lo + rpo)
+        const bool have = nkb > 0 && warp_wait(tfull, 0, wd, abort_flag, 4, lane);
+        if (have)
+            tc_fence_after_sync();
+        if (S == 1) {
+            if (have) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < live_cols; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem + lane_off + (uint32_t)c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        out[(c0 + i) * T::BW + n] = __float2bfloat16_rn(__uint_as_float(v[i]) * alpha);
+                }
+            }
+        } else {
+            cluster_wait();              // every CTA of the cluster has initialised its barriers
+            bool may_push = true;
+            if (!T::OWN_RECV) {
+                if (have && warp == T::EPI_WARP0 && lane == 0)
+                    for (int p = 0; p < S; ++p)  // this CTA's ring is drained: peers may push into it
+                        if (p != (int)rank)
+                            mbar_arrive_remote_relaxed(mapa_shared(peer_free, (uint32_t)p));
+                may_push = warp_wait(peer_free, 0, wd, abort_flag, 7, lane);
+            }
+            // every row of the partial into its owner's slot for this rank:
+            // the owned rows locally, the others pushed to their CTA
+            const int slot_bytes = rpo * live_cols * 4;
+            const uint32_t group_bytes = (uint32_t)rpo * 16u;
+            if (have && may_push) {
+                const uint32_t my_slot = smem_u32(recv) + (uint32_t)((int)rank * slot_bytes) + (uint32_t)orow * 16u;
+                const uint32_t dst = mapa_shared(my_slot, (uint32_t)owner);
+                const uint32_t recv_bar = mapa_shared(rx, (uint32_t)owner);
+                float4 *const local = reinterpret_cast<float4 *>(recv + (int)rank * slot_bytes + orow * 16);
+#pragma unroll 1
+                for (int c0 = 0; c0 < live_cols; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem + lane_off + (uint32_t)c0, v);
+                    tmem_ld_wait();
+                    if (owner == (int)rank) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            local[(c0 / 4 + j) * rpo] =
+                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_async_v4(dst + (uint32_t)(c0 / 4 + j) * group_bytes, v[4 * j], v[4 * j + 1],
+                                        v[4 * j + 2], v[4 * j + 3], recv_bar);
+                    }
+                }
+            }
+            const bool rows_in = warp_wait(rx, 0, wd, abort_flag, 8, lane);
+            named_bar_sync(1, 32 * T::EPI_WARPS);        // the owned rows' local writes
+            if (have && rows_in) {
+                switch (S) {
+                case 2: reduce_owned<2>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS); break;
+                case 4: reduce_owned<4>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS); break;
+                default: reduce_owned<8>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS); break;
+                }
+            }
+        }
+        // one TMA store of this CTA's [M x 128/S] block of D (rows >= M and
+        // columns >= N are clipped by the tensor map)
+        fence_proxy_async_smem();
+        named_bar_sync(1, 32 * T::EPI_WARPS);
+        if (warp == T::EPI_WARP0 && lane == 0) {
+            tma_store_2d(&tmD, smem_u32(out), nt * T::BW + own_lo, 0);
+            bulk_commit_group();
+            bulk_wait_group_read<0>();   // the staging must outlive the read
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Plans and launchers
+// ---------------------------------------------------------------------------
+template <int M_PAD, int STAGES>
+static cudaError_t skinny_launch_impl(const GemmMaps &maps, const GemmArgs &args, int splits,
+                                      cudaStream_t stream)
+{
+    using T = SkinnyTile<M_PAD, STAGES>;
+    auto kern = gemm_skinny_kernel<M_PAD, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)args.num_n_tiles, (unsigned)splits, 1);
+    cfg.blockDim = dim3(T::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = T::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)splits;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, maps.b, maps.a, maps.d, args);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+template <int M_PAD, int STAGES>
+static int skinny_clusters_impl(int splits)
+{
+    using T = SkinnyTile<M_PAD, STAGES>;
+    auto kern = gemm_skinny_kernel<M_PAD, STAGES>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, (unsigned)splits, 1);
+    cfg.blockDim = dim3(T::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = T::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)splits;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void *)kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int M_PAD, int STAGES>
+static constexpr PlanInfo make_skinny_plan(const char *name)
+{
+    using T = SkinnyTile<M_PAD, STAGES>;
+    return PlanInfo{name, Kind::NVFP4, Family::SKINNY, 1, M_PAD, T::BW, STAGES, 1, T::K_BLOCK,
+                    T::SMEM_BYTES, T::THREADS, T::TMEM_COLS};
+}
+
+// activation rows covered (M <= M_PAD), stages; m64_s3 and m128_s3 fit two
+// CTAs per SM
+#define BSG_SKINNY_PLANS(X)                                   \
+    X(64, 3, "nvfp4_skinny_m64_s3")                           \
+    X(64, 6, "nvfp4_skinny_m64_s6")                           \
+    X(128, 3, "nvfp4_skinny_m128_s3")                         \
+    X(256, 4, "nvfp4_skinny_m256_s4")
+
+#define BSG_SKINNY_INFO(MP, S, NAME) make_skinny_plan<MP, S>(NAME),
+static const PlanInfo kSkinnyPlans[] = {BSG_SKINNY_PLANS(BSG_SKINNY_INFO)};
+#undef BSG_SKINNY_INFO
+
+int skinny_num_plans() { return (int)(sizeof(kSkinnyPlans) / sizeof(kSkinnyPlans[0])); }
+
+const PlanInfo &skinny_plan(int i) { return kSkinnyPlans[i]; }
+
+cudaError_t skinny_launch(int id, const GemmMaps &maps, const GemmArgs &args, int splits,
+                          cudaStream_t stream)
+{
+    int i = 0;
+#define BSG_SKINNY_LAUNCH(MP, S, NAME)                                          \
+    if (id == i)                                                               \
+        return skinny_launch_impl<MP, S>(maps, args, splits, stream);        \
+    ++i;
+    BSG_SKINNY_PLANS(BSG_SKINNY_LAUNCH)
+#undef BSG_SKINNY_LAUNCH
+    return cudaErrorInvalidValue;
+}
+
+int skinny_max_clusters(int id, int splits)
+{
+    int i = 0;
+#define BSG_SKINNY_OCC(MP, S, NAME)                    \
+    if (id == i)                                      \
+        return skinny_clusters_impl<MP, S>(splits);    \
+    ++i;
+    BSG_SKINNY_PLANS(BSG_SKINNY_OCC)
+#undef BSG_SKINNY_OCC
+    return 0;
+}
+
+}  // namespace bsg

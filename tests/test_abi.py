@@ -81,17 +81,50 @@ def test_swizzled_bytes(lib):
 
 
 def test_planner_enumeration(lib):
-    # every shape of the workloads picks a plan of its own kind; N <= 128
-    # takes a 128-wide tile, everything else a 256-wide one; M <= 128 stays
-    # on one SM, larger M uses the CTA-pair tiles (except FP8 with N <= 128)
+    # every shape picks a plan of its own kind, by the planner's rules
+    sms = 152
     for kind, prefix in ((0, "nvfp4_"), (1, "fp8_")):
-        for M in (1, 64, 128, 129, 256, 4096, 16384):
+        for M in (1, 64, 65, 128, 129, 256, 257, 512, 4096, 16384):
             for N in (8, 128, 136, 256, 3072, 12288, 16384):
-                name = bsg.bsg_select_plan(kind, M, N, 4096, 152)
-                assert name.startswith(prefix), name
-                assert ("x128_" in name) == (N <= 128), (N, name)
-                pair = "_tc2_" in name
-                assert pair == (M > 128 and not (kind == 1 and N <= 128)), (M, N, name)
+                for K in (256, 4096, 12288):
+                    name = bsg.bsg_select_plan(kind, M, N, K, sms)
+                    assert name.startswith(prefix), name
+                    tiles128 = -(-M // 128) * -(-N // 128)
+                    few = tiles128 <= 4 * sms
+                    if kind == 1:
+                        assert ("x128_" in name) == (N <= 128), (N, name)
+                        assert ("_tc2_" in name) == (M > 128 and N > 128), (M, N, name)
+                        continue
+                    split = 2 * -(-N // 128) <= sms and K >= 512
+                    if M <= 256 and split and (M <= 128 or K >= 8192):
+                        mpad = 64 if M <= 64 else 128 if M <= 128 else 256
+                        assert name.startswith(f"nvfp4_skinny_m{mpad}_"), (M, N, K, name)
+                    elif few or N <= 128:
+                        want = "tc1_128x128" if (M <= 128 or few) else "tc2_256x128"
+                        assert want in name, (M, N, K, name)
+                    else:
+                        want = "tc1_128x256" if M <= 128 else "tc2_256x256"
+                        assert want in name, (M, N, K, name)
+
+
+def test_planner_headline_shapes(lib):
+    # the shapes the benchmarks time
+    assert bsg.bsg_select_plan(0, 16384, 16384, 16384, 152) == "nvfp4_tc2_256x256_s5_acc1"
+    assert bsg.bsg_select_plan(1, 8192, 8192, 8192, 152) == "fp8_tc2_256x256_s6_acc2"
+    assert bsg.bsg_select_plan(0, 64, 3072, 3072, 152) == "nvfp4_skinny_m64_s6"
+    assert bsg.bsg_select_plan(0, 256, 3072, 12288, 152) == "nvfp4_skinny_m256_s4"
+    assert bsg.bsg_select_plan(0, 256, 3072, 3072, 152) == "nvfp4_tc1_128x128_s5_acc2"
+    assert bsg.bsg_select_plan(0, 512, 12288, 3072, 152) == "nvfp4_tc1_128x128_s5_acc2"
+
+
+def test_forced_skinny_plan_needs_small_m(lib):
+    bsg.bsg_force_plan("nvfp4_skinny_m64_s6")
+    try:
+        assert bsg.bsg_select_plan(0, 64, 3072, 3072, 152) == "nvfp4_skinny_m64_s6"
+        with pytest.raises(bsg.BsgError):       # 65 activation rows do not fit
+            bsg.bsg_select_plan(0, 65, 3072, 3072, 152)
+    finally:
+        bsg.bsg_force_plan(None)
 
 
 def test_forced_plan(lib):

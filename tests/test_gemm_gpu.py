@@ -260,6 +260,30 @@ def test_nvfp4_skinny_cells(dev, name):
     assert_close(got, ref, T, name)
 
 
+SKINNY_PLANS = {"nvfp4_skinny_m64_s3": 64, "nvfp4_skinny_m64_s6": 64, "nvfp4_skinny_m128_s3": 128,
+                "nvfp4_skinny_m256_s4": 256}
+
+
+@pytest.mark.parametrize("plan", list(SKINNY_PLANS))
+@pytest.mark.parametrize("M,N,K", [(1, 136, 256), (16, 256, 512), (48, 1024, 1024), (37, 392, 1280),
+                                   (64, 3072, 3072), (100, 1000, 2304), (256, 520, 4096), (200, 8, 512),
+                                   (64, 16384, 512)])
+def test_nvfp4_skinny_kernel(dev, plan, M, N, K):
+    """The swap-AB split-K kernel forced on every shape it can serve: ragged
+    M and N, every cluster size (1, 2, 4 and 8 K splits, some not dividing
+    the k-blocks evenly), and a wide N whose split is capped by residency."""
+    if M > SKINNY_PLANS[plan]:
+        pytest.skip("activation rows exceed the plan's tile")
+    bsg.bsg_force_plan(plan)
+    try:
+        p = workloads.make_nvfp4(workloads.WORKLOADS["nvfp4_4096"], "cpu", M=M, N=N, K=K)
+        got = gpu_nvfp4(p, dev)
+    finally:
+        bsg.bsg_force_plan(None)
+    _, T, ref = oracle_nvfp4(p)
+    assert_close(got, ref, T, f"{plan} {M}x{N}x{K}")
+
+
 # ---------------------------------------------------------------------------
 # FP8
 # ---------------------------------------------------------------------------
