@@ -468,6 +468,60 @@ def run_reference(args, dist: Dist) -> None:
     }), flush=True)
 
 
+def run_case(args) -> None:
+    """One GEMM shape alone (--case nvfp4:MxNxK or fp8:MxNxK, optionally a
+    forced --plan): `warmup` untimed then `steps` timed launches, inputs
+    resident. Used for profiler captures of a single kernel and for ad-hoc
+    timings; prints one JSON line."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_scaled_precision_persistent_gb300 as bsg
+    kind, shape = args.case.split(":")
+    M, N, K = (int(x) for x in shape.lower().split("x"))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = torch.cuda.current_stream()
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if kind == "nvfp4":
+        p = workloads.make_nvfp4(workloads.WORKLOADS["nvfp4_4096"], dev, M=M, N=N, K=K)
+        sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+        sb = torch.empty(bsg.nvfp4_swizzled_scale_bytes(N, K), dtype=torch.uint8, device=dev)
+        bsg.nvfp4_swizzle_scales(M, K, p["sfA"], sa, s)
+        bsg.nvfp4_swizzle_scales(N, K, p["sfB"], sb, s)
+
+        def call():
+            bsg.nvfp4_gemm_swizzled(M, N, K, p["A"], sa, p["B"], sb, p["alpha"], D, s)
+    elif kind == "fp8":
+        q = workloads.make_fp8(workloads.WORKLOADS["fp8_8192"], dev, M=M, N=N, K=K)
+
+        def call():
+            bsg.fp8_gemm(M, N, K, q["A"], None, q["B"], None, q["alpha"], D, s)
+    else:
+        raise SystemExit(f"unknown case kind {kind!r}")
+    bsg.bsg_force_plan(args.plan)
+    try:
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            call()
+            b.record(s)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        plan = bsg.bsg_select_plan(0 if kind == "nvfp4" else 1, M, N, K,
+                                   torch.cuda.get_device_properties(0).multi_processor_count)
+    finally:
+        bsg.bsg_force_plan(None)
+    if bsg.bsg_get_device_status() != bsg.BSG_OK:
+        raise SystemExit("device status reported an error")
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    print(json.dumps({"case": args.case, "plan": plan, "ms": round(ms, 5),
+                      "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 2)}), flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -480,7 +534,13 @@ def main() -> None:
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--case", default=None,
+                    help="time one shape alone instead of the benchmark: nvfp4:MxNxK or fp8:MxNxK")
+    ap.add_argument("--plan", default=None, help="with --case: force this plan")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     dist = Dist(args.gpus) if args.impl == "ours" or args.gpus > 1 else Dist(1)

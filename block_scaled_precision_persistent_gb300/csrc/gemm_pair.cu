@@ -341,10 +341,18 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                 tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS + 32, v1);
                 tmem_ld_wait();
                 if (ch == BN / T::EPI_COLS - 1) {
+                    // the accumulator is read out (tcgen05.wait::ld): the MMA
+                    // may reuse it. The leader's epilogue arrives locally, the
+                    // peer's with a relaxed remote arrive (a release at cluster
+                    // scope measured ~1100 cycles).
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive_cluster(mapa_shared(tempty0 + 8u * acc, 0));
+                    if (lane == 0) {
+                        if (leader)
+                            mbar_arrive(tempty0 + 8u * acc);
+                        else
+                            mbar_arrive_remote_relaxed(mapa_shared(tempty0 + 8u * acc, 0));
+                    }
                 }
                 if (lane == 0)
                     bulk_wait_group_read<1>();
