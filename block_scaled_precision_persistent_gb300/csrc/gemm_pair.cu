@@ -53,10 +53,16 @@ struct PairTile {
     static constexpr int SFA_BYTES = kFp4 ? SF_BLOCK_BYTES : 0;
     static constexpr int SFB_BYTES = SFB_CHUNKS * SF_BLOCK_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    static constexpr int EPI_WARPS = 4;
+    // Epilogue warps: each drains 32 TMEM lanes x 128 columns. 256-wide NVFP4
+    // tiles (one accumulator, so every tile's drain stalls the MMA) use two
+    // per sub-partition to release TMEM sooner; FP8 tiles (two accumulators,
+    // drain overlapped) and 128-wide tiles use one.
+    static constexpr int EPI_WARPS = (kFp4 && BN == 256) ? 8 : 4;
     static constexpr int EPI_COLS = 64;
+    static constexpr int EPI_CHUNKS = BN * 4 / EPI_WARPS / EPI_COLS;   // 64-column chunks per warp (2 or 4)
+    static constexpr int EPI_BUFS = EPI_CHUNKS == 2 ? 1 : 2;           // 4 KiB staging buffers per warp
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
-    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
+    static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
     static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 1;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
     static constexpr int SCALE_WARPS = 4;                 // one per TMEM sub-partition (NVFP4 scales)
@@ -317,7 +323,9 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
         // ------------------------------------------------------------------
         const int q = warp & 3;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const uint32_t ebuf = s_epi + (uint32_t)(warp - T::EPI_WARP0) * 2u * T::EPI_BUF_BYTES;
+        constexpr int COLS_PER_WARP = T::EPI_CHUNKS * T::EPI_COLS;   // 128 or 256 columns per warp
+        const int h = (warp - T::EPI_WARP0) / 4;                  // column block of this warp
+        const uint32_t ebuf = s_epi + (uint32_t)(warp - T::EPI_WARP0) * T::EPI_BUFS * T::EPI_BUF_BYTES;
         float scale = args.alpha;
         if constexpr (!T::kFp4) {
             if (args.sA)
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
             if (args.sB)
                 scale *= *args.sB;
         }
-        int acc = 0, buf = 0;
+        int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
             int pm, nt;
@@ -333,56 +341,81 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
             if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
                 break;
             tc_fence_after_sync();
-            const uint32_t t_acc = tmem + lane_off + (uint32_t)(acc * BN);
-#pragma unroll 1
-            for (int ch = 0; ch < BN / T::EPI_COLS; ++ch) {
-                uint32_t v0[32], v1[32];
-                tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS, v0);
-                tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS + 32, v1);
-                tmem_ld_wait();
-                if (ch == BN / T::EPI_COLS - 1) {
-                    // the accumulator is read out (tcgen05.wait::ld): the MMA
-                    // may reuse it. The leader's epilogue arrives locally, the
-                    // peer's with a relaxed remote arrive (a release at cluster
-                    // scope measured ~1100 cycles).
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (leader)
-                            mbar_arrive(tempty0 + 8u * acc);
-                        else
-                            mbar_arrive_remote_relaxed(mapa_shared(tempty0 + 8u * acc, 0));
-                    }
+            const uint32_t t_acc = tmem + lane_off + (uint32_t)(acc * BN + h * COLS_PER_WARP);
+            // 64 TMEM columns -> alpha -> BF16 pairs
+            auto drain = [&](int ch, uint32_t (&pk)[32]) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS + 32 * half, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[16 * half + i] =
+                            pack_bf16x2(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
                 }
-                if (lane == 0)
-                    bulk_wait_group_read<1>();
+            };
+            // one 64-column chunk from registers into a 128B-swizzled staging
+            // buffer, once the store that last used the buffer has read it
+            auto stage_out = [&](const uint32_t (&pk)[32], uint32_t sbuf) {
+                if (lane == 0) {
+                    if constexpr (T::EPI_BUFS == 1)
+                        bulk_wait_group_read<0>();
+                    else
+                        bulk_wait_group_read<1>();
+                }
                 __syncwarp();
-                const uint32_t sbuf = ebuf + (uint32_t)buf * T::EPI_BUF_BYTES;
                 const uint32_t row = sbuf + (uint32_t)lane * 128u;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    st_shared_v4(row + ((uint32_t)(c ^ (lane & 7)) << 4),
-                                 pack_bf16x2(__uint_as_float(v0[8 * c + 0]) * scale, __uint_as_float(v0[8 * c + 1]) * scale),
-                                 pack_bf16x2(__uint_as_float(v0[8 * c + 2]) * scale, __uint_as_float(v0[8 * c + 3]) * scale),
-                                 pack_bf16x2(__uint_as_float(v0[8 * c + 4]) * scale, __uint_as_float(v0[8 * c + 5]) * scale),
-                                 pack_bf16x2(__uint_as_float(v0[8 * c + 6]) * scale, __uint_as_float(v0[8 * c + 7]) * scale));
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    st_shared_v4(row + ((uint32_t)((c + 4) ^ (lane & 7)) << 4),
-                                 pack_bf16x2(__uint_as_float(v1[8 * c + 0]) * scale, __uint_as_float(v1[8 * c + 1]) * scale),
-                                 pack_bf16x2(__uint_as_float(v1[8 * c + 2]) * scale, __uint_as_float(v1[8 * c + 3]) * scale),
-                                 pack_bf16x2(__uint_as_float(v1[8 * c + 4]) * scale, __uint_as_float(v1[8 * c + 5]) * scale),
-                                 pack_bf16x2(__uint_as_float(v1[8 * c + 6]) * scale, __uint_as_float(v1[8 * c + 7]) * scale));
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(row + ((uint32_t)(c ^ (lane & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                                 pk[4 * c + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
+            };
+            auto store_chunk = [&](int ch, uint32_t sbuf) {
                 if (lane == 0) {
-                    const int x = nt * BN + ch * T::EPI_COLS;
+                    const int x = nt * BN + h * COLS_PER_WARP + ch * T::EPI_COLS;
                     const int y = pm * T::TILE_M + (int)rank * T::BM + q * 32;
                     if (x < args.N && y < args.M)
                         tma_store_2d(&tmD, sbuf, x, y);
                     bulk_commit_group();
                 }
-                buf ^= 1;
+            };
+            auto release = [&]() {      // the accumulator is read out (tcgen05.wait::ld): the MMA may reuse it
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader)
+                        mbar_arrive(tempty0 + 8u * acc);
+                    else
+                        mbar_arrive_remote_relaxed(mapa_shared(tempty0 + 8u * acc, 0));
+                }
+            };
+            if constexpr (T::EPI_CHUNKS == 2) {
+                // first chunk staged, second held in registers: TMEM is released
+                // before either TMA store is issued
+                uint32_t pk0[32], pk1[32];
+                drain(0, pk0);
+                stage_out(pk0, ebuf);
+                drain(1, pk1);
+                release();
+                store_chunk(0, ebuf);
+                stage_out(pk1, ebuf);
+                store_chunk(1, ebuf);
+            } else {
+                // four chunks through two alternating buffers; TMEM is released
+                // after the last chunk's read
+#pragma unroll 1
+                for (int ch = 0; ch < T::EPI_CHUNKS; ++ch) {
+                    uint32_t pk[32];
+                    drain(ch, pk);
+                    if (ch == T::EPI_CHUNKS - 1)
+                        release();
+                    const uint32_t sbuf = ebuf + (uint32_t)(ch & 1) * T::EPI_BUF_BYTES;
+                    stage_out(pk, sbuf);
+                    store_chunk(ch, sbuf);
+                }
             }
             if (++acc == NUM_ACC) {
                 acc = 0;
