@@ -42,7 +42,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per GEMM launch from an ncu capture of the current kernel
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (plan, workload);
 # the summary it comes from is named in the comment. None = not captured.
-NCU_TRAFFIC_BYTES: dict[tuple[str, str], float] = {}
+NCU_TRAFFIC_BYTES: dict[tuple[str, str], float] = {
+    # profiles/gemm_pair_nvfp4_256x256_s5_acc1_16384.md: 1.415 GB read + 0.520 GB written
+    ("nvfp4_tc2_256x256_s5_acc1", "nvfp4_16384"): 1414565000 + 520475392,
+}
 
 
 def peaks() -> tuple[dict, str]:
@@ -56,36 +59,11 @@ def peaks() -> tuple[dict, str]:
 # distributed plumbing (torchrun); N independent replicas, no collective on
 # the data path -- the barrier and the max-reduce of the timing only
 # ---------------------------------------------------------------------------
-class Dist:
-    def __init__(self, gpus: int):
-        self.world = int(os.environ.get("WORLD_SIZE", "1"))
-        self.rank = int(os.environ.get("RANK", "0"))
-        self.local = int(os.environ.get("LOCAL_RANK", "0"))
-        if self.world != gpus:
-            raise SystemExit(f"--gpus {gpus} but WORLD_SIZE={self.world}")
-        self.pg = False
-        if self.world > 1:
-            import torch.distributed as dist
-            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
-            self.pg = True
-
-    def barrier(self):
-        if self.pg:
-            import torch.distributed as dist
-            dist.barrier()
-
-    def max(self, x: float) -> float:
-        if not self.pg:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    def close(self):
-        if self.pg:
-            import torch.distributed as dist
-            dist.destroy_process_group()
+def Dist(gpus: int):
+    """One process per GPU (torchrun's environment), NCCL; the ranks are
+    independent replicas and only the timing crosses them."""
+    from block_scaled_precision_persistent_gb300.replicas import Ranks
+    return Ranks("nccl", expected_world=gpus)
 
 
 # ---------------------------------------------------------------------------
@@ -316,15 +294,66 @@ def secondary_skinny(dev, steps: int, pk: dict, psrc: str) -> dict:
         if bsg.bsg_get_device_status() != bsg.BSG_OK:
             raise RuntimeError(f"device status set during skinny cell {name}")
         us = statistics.median(ts) * 1e3
+        # warm L2: the same graph shape over one buffer set, so weights stay in L2
+        gw = torch.cuda.CUDAGraph()
+        A, sa, B, sb, D = sets[0]
+        with torch.cuda.graph(gw):
+            for _ in range(copies):
+                bsg.nvfp4_gemm_swizzled(M, N, K, A, sa, B, sb, p["alpha"], D)
+        gw.replay()
+        torch.cuda.synchronize()
+        tw = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            gw.replay()
+            b.record()
+            torch.cuda.synchronize()
+            tw.append(a.elapsed_time(b) / copies)
+        us_warm = statistics.median(tw) * 1e3
         gbs = per / (us * 1e-6) / 1e9
         ideal_us = max(per / (pk["hbm_gbs"] * 1e9), w.flops / (pk["bf16_tflops"] * FP4_PER_BF16 * 1e12)) * 1e6
         out[f"m{M}_n{N}_k{K}"] = {"plan": bsg.bsg_select_plan(0, M, N, K, sms), "us": round(us, 3),
                                   "hbm_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
-                                  "ideal_us": round(ideal_us, 3), "frac_roofline": round(ideal_us / us, 4)}
-        del g, sets
+                                  "ideal_us": round(ideal_us, 3), "frac_roofline": round(ideal_us / us, 4),
+                                  "us_warm_l2": round(us_warm, 3)}
+        del g, gw, sets
     return {"cells": out, "peak_hbm_gbs": pk["hbm_gbs"], "peak_source": psrc,
             "timing": "cold L2 (buffer sets rotated over > 4x L2), CUDA graph of back-to-back launches, "
-                      "median over replays of graph time / launches"}
+                      "median over replays of graph time / launches; us_warm_l2: the same over one "
+                      "buffer set (weights L2-resident)"}
+
+
+def secondary_swizzle(dev, steps: int, pk: dict, psrc: str) -> dict:
+    """The scale-layout prep alone (timed separately from the GEMM): one
+    operand's row-major [16384][1024] E4M3 scales into the swizzled layout;
+    bytes = read + write. Inputs rotate over > 4x L2 (cold)."""
+    import block_scaled_precision_persistent_gb300 as bsg
+    rows, K = 16384, 16384
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    nbytes = rows * (K // 16)
+    copies = max(2, int(4 * l2 // (2 * nbytes)) + 1)
+    src = [torch.randint(0, 256, (rows, K // 16), dtype=torch.uint8, device=dev) for _ in range(copies)]
+    dst = [torch.empty(bsg.nvfp4_swizzled_scale_bytes(rows, K), dtype=torch.uint8, device=dev)
+           for _ in range(copies)]
+    s = torch.cuda.current_stream()
+    for i in range(3):
+        bsg.nvfp4_swizzle_scales(rows, K, src[i % copies], dst[i % copies], s)
+    torch.cuda.synchronize()
+    evs = []
+    for i in range(max(steps, copies)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        bsg.nvfp4_swizzle_scales(rows, K, src[i % copies], dst[i % copies], s)
+        b.record(s)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+    moved = nbytes + bsg.nvfp4_swizzled_scale_bytes(rows, K)
+    gbs = moved / (us * 1e-6) / 1e9
+    return {"shape": f"{rows} rows x K={K}", "us": round(us, 3), "gb_s": round(gbs, 1),
+            "frac_hbm": round(gbs / pk["hbm_gbs"], 4), "peak_source": psrc,
+            "timing": "cold (inputs rotated over > 4x L2), median per-launch CUDA events"}
 
 
 def cpu_baseline(w: workloads.Workload, p_host: dict, budget_s: float = 15.0) -> dict:
@@ -393,6 +422,7 @@ def run_ours(args, dist: Dist) -> None:
     if not args.no_secondary:
         secondary["fp8"] = secondary_fp8(dev, max(3, args.steps), args.warmup, pk, psrc)
         secondary["skinny"] = secondary_skinny(dev, 20, pk, psrc)
+        secondary["swizzle"] = secondary_swizzle(dev, 20, pk, psrc)
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, host_copy(step), args.cpu_seconds)

@@ -361,3 +361,33 @@ def test_stream_ordering(dev):
         got = gpu_nvfp4(p, dev, "swizzled", stream=s)
     _, T, ref = oracle_nvfp4(p)
     assert_close(got, ref, T, "side stream")
+
+
+# ---------------------------------------------------------------------------
+# Replicas: a GEMM split by output columns into per-rank calls
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_column_shards_concatenate(dev, world):
+    """The calls a column-split job makes, run one after another on this GPU:
+    rank r multiplies A by its rows [n0, n1) of B (with those rows' scales)
+    into its own [M, n1 - n0] block; the blocks, concatenated, match the
+    unsharded oracle result."""
+    from block_scaled_precision_persistent_gb300.replicas import shard_range
+    M, N, K = 300, 648, 1024
+    p = workloads.make_nvfp4(workloads.WORKLOADS["nvfp4_4096"], "cpu", M=M, N=N, K=K)
+    A, sfA = p["A"].to(dev), p["sfA"].to(dev)
+    blocks = []
+    for r in range(world):
+        n0, n1 = shard_range(N, world, r)
+        B = p["B"][n0:n1].contiguous().to(dev)
+        sfB = p["sfB"][n0:n1].contiguous().to(dev)
+        flat, D = new_out(M, n1 - n0, dev)
+        bsg.nvfp4_gemm(M, n1 - n0, K, A, sfA, B, sfB, p["alpha"], D)
+        torch.cuda.synchronize()
+        assert bsg.bsg_get_device_status() == bsg.BSG_OK
+        assert_guard(flat)
+        blocks.append(bits(D))
+    got = np.concatenate(blocks, axis=1)
+    _, T, ref = oracle_nvfp4(p)
+    assert_close(got, ref, T, f"{world} column shards")
