@@ -112,13 +112,29 @@ def fp8_plan(request, dev):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("rows,K", [(1, 16), (127, 48), (129, 64), (300, 1040), (256, 256),
-                                    (4096, 4096), (1000, 16384)])
+                                    (300, 512), (4096, 4096), (1000, 16384)])
 def test_swizzle_bit_exact(dev, rows, K):
     rng = np.random.default_rng(rows * 7 + K)
     sf = rng.integers(0, 256, (rows, K // 16)).astype(np.uint8)
     want = oracle.get().swizzle_scales(sf, K)
     out = torch.full((want.size,), 0xAB, dtype=torch.uint8, device=dev)   # padding must be zeroed
     bsg.nvfp4_swizzle_scales(rows, K, torch.from_numpy(sf).to(dev), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("offset", [1, 4, 8])
+def test_swizzle_unaligned_input(dev, offset):
+    """Row-major scales that start off a 16-byte boundary (a sliced buffer):
+    the kernel takes its byte path and the result is still bit-exact."""
+    rows, K = 300, 4096
+    rng = np.random.default_rng(offset)
+    sf = rng.integers(0, 256, (rows, K // 16)).astype(np.uint8)
+    want = oracle.get().swizzle_scales(sf, K)
+    buf = torch.zeros(sf.size + 64, dtype=torch.uint8, device=dev)
+    buf[offset:offset + sf.size] = torch.from_numpy(sf.reshape(-1)).to(dev)
+    out = torch.full((want.size,), 0xAB, dtype=torch.uint8, device=dev)
+    bsg.nvfp4_swizzle_scales(rows, K, buf[offset:], out)
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), want)
 
