@@ -2,7 +2,9 @@
 
 This package is the plain, slow definition the CUDA library is checked
 against: ``D = alpha * (A (.) sA)(B (.) sB)^T`` with E2M1 / E4M3 elements
-decoded exactly, accumulation in double and one final rounding to BF16.
+decoded exactly, accumulation in double and one final rounding to BF16; the
+scale layout the tensor core reads; and the two-level NVFP4 quantisation
+(BF16 -> E2M1 codes + E4M3 block scales + a global scale) in front of it.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import it. The library (``block_scaled_precision_persistent_gb300``)
@@ -90,6 +92,10 @@ class Oracle:
         L.bso_swizzled_scale_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
         L.bso_swizzle_scales.restype = ctypes.c_int
         L.bso_swizzle_scales.argtypes = [ctypes.c_int, ctypes.c_int, u8p, u8p]
+        L.bso_nvfp4_quantize.restype = ctypes.c_int
+        L.bso_nvfp4_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_uint16),
+                                         u8p, u8p, ctypes.POINTER(ctypes.c_float),
+                                         ctypes.POINTER(ctypes.c_float)]
 
     # -- element decoders -------------------------------------------------
     def e2m1(self, code: int) -> float:
@@ -164,6 +170,23 @@ class Oracle:
         return S, T, D
 
     # -- scale layout ---------------------------------------------------------
+    def nvfp4_quantize(self, x_bf16_bits):
+        """Two-level NVFP4 quantisation of BF16 X (uint16 bit patterns
+        [rows, K]) -> (packed uint8[rows, K/2], scales uint8[rows, K/16]
+        row-major, amax, s_g) with amax and s_g as float32 values."""
+        X = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+        rows, K = X.shape
+        packed = np.zeros((rows, K // 2), np.uint8)
+        sf = np.zeros((rows, K // 16), np.uint8)
+        amax = ctypes.c_float(0.0)
+        sg = ctypes.c_float(0.0)
+        rc = self.lib.bso_nvfp4_quantize(rows, K, X.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),
+                                         self._p(packed, ctypes.c_uint8), self._p(sf, ctypes.c_uint8),
+                                         ctypes.byref(amax), ctypes.byref(sg))
+        if rc != 0:
+            raise ValueError(f"bso_nvfp4_quantize: bad arguments ({rows}x{K})")
+        return packed, sf, np.float32(amax.value), np.float32(sg.value)
+
     def swizzled_scale_bytes(self, rows: int, K: int) -> int:
         return int(self.lib.bso_swizzled_scale_bytes(rows, K))
 

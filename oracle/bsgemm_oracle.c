@@ -20,6 +20,9 @@
  *    Tensor-Memory Failures", section "The matrix also compared Triton with a
  *    reference implementation": the GPU output is compared with a reference
  *    implementation under a format-specific tolerance.
+ *  - "Triton #11171 ...": a shared NVFP4 quantisation step in front of the
+ *    GEMM; written out here as the two-level scheme described above
+ *    bso_nvfp4_quantize.
  *  - Element formats (the pages name them but do not define them): E2M1 as in
  *    the OCP Microscaling Formats (MX) v1.0 specification (FP4 element type),
  *    E4M3 as in the OCP 8-bit Floating Point (OFP8) specification ("E4M3",
@@ -391,6 +394,149 @@ int bso_swizzle_scales(int rows, int K, const uint8_t *in, uint8_t *out)
                          + (size_t)(c % 4);
 #endif
             out[off] = (r < rows && c < cols) ? in[(size_t)r * (size_t)cols + (size_t)c] : 0u;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Two-level NVFP4 quantisation: BF16 -> E2M1 codes + E4M3 block scales      */
+/* ------------------------------------------------------------------------ */
+
+/* "Triton #11171 - Why Two New NVFP4 Test Cases Produced Twelve
+ * Tensor-Memory Failures" names a shared NVFP4 quantisation step in front of
+ * the block-scaled GEMM; the pages give no formula. The scheme written out
+ * here is the plainest reading (listed in the design doc):
+ *
+ *   amax  = max |x| over the whole tensor                    (exact)
+ *   s_g   = 2688 / amax   (448 * 6; 1 when amax == 0)         (FP32, rounded once)
+ *   per block of 16 consecutive elements along K:
+ *     bmax  = max |x| over the block                         (exact)
+ *     sc    = (bmax / 6) * s_g                               (FP32, two roundings, this order)
+ *     scale = nearest E4M3 (ties to even), saturated at 448  (positive, sign bit 0)
+ *     if scale decodes to 0: every code of the block is 0
+ *     else code_k = nearest E2M1 (ties to even), saturated at 6, of
+ *                   (x_k * s_g) / scale                      (FP32, two roundings, this order)
+ *                   with the sign of that quotient (so a tiny negative gives -0, code 8)
+ *
+ * so that the largest |x| of the tensor lands on 6 * 448. Each decision that
+ * picks a code is taken in FP32 with every operation rounded once, in the
+ * order above: the precision of the GPU kernel, so that both sides decide
+ * ties identically. Inputs must be finite. Element 2i of a row goes to the
+ * low nibble of byte i, as everywhere in this file.                         */
+
+/* Nearest E4M3 code (ties to the even code) of v >= 0, saturated at 448:
+ * binary search over the positive finite codes 0x00..0x7E, whose decoded
+ * values rise with the code. */
+static unsigned e4m3_nearest(float v)
+{
+    if (!(v > 0.0f))
+        return 0u;
+#ifdef BSO_MUTANT_Q_E4M3_CEIL
+    for (unsigned c = 0; c < 0x7Fu; ++c)
+        if (bso_e4m3(c) >= (double)v)
+            return c;
+    return 0x7Eu;
+#endif
+    if ((double)v >= bso_e4m3(0x7Eu))
+        return 0x7Eu;
+    unsigned lo = 0u, hi = 0x7Eu;            /* decode(lo) <= v < decode(hi) */
+    while (hi - lo > 1u) {
+        unsigned mid = (lo + hi) / 2u;
+        if (bso_e4m3(mid) <= (double)v)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    double dl = (double)v - bso_e4m3(lo), dh = bso_e4m3(hi) - (double)v;
+    if (dl < dh)
+        return lo;
+    if (dh < dl)
+        return hi;
+    return (lo & 1u) ? hi : lo;              /* tie: the code with an even mantissa */
+}
+
+/* Nearest E2M1 code (ties to the even code) of y, saturated at +-6; the
+ * sign bit is the sign of y (so -0.0 and tiny negatives give code 8). */
+static unsigned e2m1_nearest(float y)
+{
+    const unsigned s = signbit(y) ? 8u : 0u;
+    const double m = fabs((double)y);
+    unsigned best = 0u;
+    double bd = -1.0;
+    for (unsigned c = 0; c < 8u; ++c) {
+        double d = fabs(bso_e2m1(c) - m);
+#ifdef BSO_MUTANT_Q_TIES_AWAY
+        if (bd < 0.0 || d < bd || (d == bd && bso_e2m1(c) > bso_e2m1(best))) {
+#else
+        if (bd < 0.0 || d < bd || (d == bd && (c & 1u) == 0u && (best & 1u) != 0u)) {
+#endif
+            best = c;
+            bd = d;
+        }
+    }
+    return s | best;
+}
+
+static float bf16_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* X: BF16 bit patterns uint16[rows][K]; outputs packed uint8[rows][K/2],
+ * row-major scales uint8[rows][K/16], and the tensor's amax and s_g. */
+int bso_nvfp4_quantize(int rows, int K, const uint16_t *X, uint8_t *packed, uint8_t *sf,
+                       float *amax_out, float *sg_out)
+{
+    if (rows < 0 || K < 16 || (K % 16) != 0)
+        return -1;
+    float amax = 0.0f;
+    for (size_t i = 0; i < (size_t)rows * (size_t)K; ++i) {
+        float a = fabsf(bf16_to_float(X[i]));
+        if (a > amax)
+            amax = a;
+    }
+    const float s_g = amax > 0.0f ? 2688.0f / amax : 1.0f;
+    *amax_out = amax;
+    *sg_out = s_g;
+    const int nb = K / 16;
+    for (int r = 0; r < rows; ++r) {
+        const uint16_t *xr = X + (size_t)r * (size_t)K;
+        uint8_t *pr = packed + (size_t)r * (size_t)(K / 2);
+        for (int b = 0; b < nb; ++b) {
+            float bmax = 0.0f;
+            for (int k = 0; k < 16; ++k) {
+                float a = fabsf(bf16_to_float(xr[16 * b + k]));
+                if (a > bmax)
+                    bmax = a;
+            }
+            const float sc = (bmax / 6.0f) * s_g;
+            const unsigned scode = e4m3_nearest(sc);
+            sf[(size_t)r * (size_t)nb + (size_t)b] = (uint8_t)scode;
+            const float sv = (float)bso_e4m3(scode);
+            unsigned codes[16];
+            for (int k = 0; k < 16; ++k) {
+                if (sv == 0.0f) {
+                    codes[k] = 0u;
+                    continue;
+                }
+#ifdef BSO_MUTANT_Q_NO_SG
+                const float y = bf16_to_float(xr[16 * b + k]) / sv;
+#else
+                const float y = (bf16_to_float(xr[16 * b + k]) * s_g) / sv;
+#endif
+                codes[k] = e2m1_nearest(y);
+            }
+            for (int k = 0; k < 16; k += 2) {
+#ifdef BSO_MUTANT_Q_SWAP_NIBBLES
+                pr[8 * b + k / 2] = (uint8_t)(codes[k + 1] | (codes[k] << 4));
+#else
+                pr[8 * b + k / 2] = (uint8_t)(codes[k] | (codes[k + 1] << 4));
+#endif
+            }
         }
     }
     return 0;

@@ -7,7 +7,9 @@ rational arithmetic, an independent numpy restatement, and invariants of the
 definition. ``test_planted_mistake_is_caught`` compiles the oracle with one
 deliberate mistake at a time (a wrong exponent bias, a dropped sign, swapped
 nibbles in one operand, a dropped scale, a dropped block, a transposed operand, a wrong
-scale layout) and shows that at least one pin fails for each.
+scale layout; in the quantiser, ties rounded away from zero, a dropped global
+scale, swapped nibbles, block scales rounded up) and shows that at least one
+pin fails for each.
 """
 from __future__ import annotations
 
@@ -304,9 +306,125 @@ def pin_swizzle(o):
         assert np.array_equal(np.sort(out[out != 0]), np.sort(sf.reshape(-1)))
 
 
+# --------------------------------------------------------------------------
+# Two-level NVFP4 quantisation
+# --------------------------------------------------------------------------
+
+def _bf16_bits(values) -> np.ndarray:
+    t = torch.tensor(np.asarray(values, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _bits_to_f32(bits) -> np.ndarray:
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32)
+
+
+E4M3_LIB = np.array([e4m3_lib(c) for c in range(0x7F)])      # positive finite codes, library-decoded
+E2M1_MAG = np.array([E2M1_TABLE[c] for c in range(8)])       # golden table
+
+
+def _unpack(packed: np.ndarray) -> np.ndarray:
+    out = np.empty((packed.shape[0], packed.shape[1] * 2), np.uint8)
+    out[:, 0::2] = packed & 15
+    out[:, 1::2] = packed >> 4
+    return out
+
+
+def pin_quantize_worked(o):
+    """The hand-worked two-row case of tests/golden/nvfp4_quantize_case.txt."""
+    rows = {}
+    for t in _rows("nvfp4_quantize_case.txt"):
+        rows.setdefault(t[0], []).append(t[1:])
+    X = np.zeros((2, 32), np.uint16)
+    for r in rows["x"]:
+        X[int(r[0])] = _bf16_bits([float(v) for v in r[1:]])
+    packed, sf, amax, sg = o.nvfp4_quantize(X)
+    for r in rows["packed"]:
+        assert [int(b, 16) for b in r[1:]] == packed[int(r[0])].tolist(), ("packed", r[0])
+    for r in rows["scales"]:
+        assert [int(b, 16) for b in r[1:]] == sf[int(r[0])].tolist(), ("scales", r[0])
+    assert float(amax) == float(rows["amax"][0][0]) and float(sg) == float(rows["sg"][0][0])
+
+
+def _random_bf16(rows, K, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, K)).astype(np.float32) * np.float32(scale)
+    return _bf16_bits(x)
+
+
+def pin_quantize_nearest_bruteforce(o):
+    """Every scale is the nearest positive E4M3 value (library-decoded, ties to
+    the even code, saturating at 448) to (bmax / 6) * s_g, and every code the
+    nearest E2M1 value (golden table, ties to even, saturating at 6) to
+    x * s_g / scale -- each quantity computed here in numpy float32."""
+    X = _random_bf16(7, 96, 11)
+    packed, sf, amax, sg = o.nvfp4_quantize(X)
+    x = _bits_to_f32(X)
+    assert amax == np.abs(x).max()
+    assert sg == np.float32(2688.0) / np.float32(amax)
+    codes = _unpack(packed)
+    for r in range(x.shape[0]):
+        for b in range(x.shape[1] // 16):
+            blk = x[r, 16 * b:16 * b + 16]
+            sc = (np.float32(np.abs(blk).max()) / np.float32(6.0)) * sg
+            d = np.abs(E4M3_LIB - float(min(sc, np.float32(448.0))))
+            best = np.flatnonzero(d == d.min())
+            want = best[0] if len(best) == 1 else [c for c in best if c % 2 == 0][0]
+            assert sf[r, b] == want, (r, b, sc)
+            sv = np.float32(E4M3_LIB[sf[r, b]])
+            for k in range(16):
+                c = int(codes[r, 16 * b + k])
+                if sv == 0:
+                    assert c == 0
+                    continue
+                y = (blk[k] * sg) / sv
+                dd = np.abs(E2M1_MAG - abs(float(y)))
+                cand = np.flatnonzero(dd == dd.min())
+                mag = cand[0] if len(cand) == 1 else [m for m in cand if m % 2 == 0][0]
+                assert c == (mag | (8 if np.signbit(y) else 0)), (r, b, k, float(y), c)
+
+
+def pin_quantize_scale_invariance(o):
+    """Scaling X by a power of two leaves codes and scales unchanged and
+    scales amax by it and s_g by its inverse, exactly."""
+    X = _random_bf16(5, 64, 12)
+    ref = o.nvfp4_quantize(X)
+    for j in (-3, 5):
+        Xj = _bf16_bits(_bits_to_f32(X) * np.float32(2.0 ** j))
+        got = o.nvfp4_quantize(Xj)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), j
+        assert got[2] == ref[2] * np.float32(2.0 ** j) and got[3] == ref[3] * np.float32(2.0 ** -j), j
+
+
+def pin_quantize_amax_element(o):
+    """The largest |x| of the tensor lands on +-6 with a block scale of 448."""
+    X = _random_bf16(4, 80, 13)
+    packed, sf, amax, sg = o.nvfp4_quantize(X)
+    x = _bits_to_f32(X)
+    r, k = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert sf[r, k // 16] == 0x7E
+    assert _unpack(packed)[r, k] == (15 if x[r, k] < 0 else 7)
+
+
+def pin_quantize_dequant_bound(o):
+    """Dequantised values e2m1(code) * scale / s_g are within one scale step
+    (the E2M1 spacing is at most 2 below 6, saturation adds under 0.5) of x."""
+    X = _random_bf16(6, 128, 14, scale=3.0)
+    packed, sf, amax, sg = o.nvfp4_quantize(X)
+    x = _bits_to_f32(X).astype(np.float64)
+    codes = _unpack(packed)
+    val = E2M1_MAG[codes & 7] * np.where(codes & 8, -1.0, 1.0)
+    sv = E4M3_LIB[sf].repeat(16, axis=1)
+    deq = val * sv / float(sg)
+    step = sv / float(sg)
+    assert np.all(np.abs(deq - x) <= 1.001 * step)
+
+
 PINS = [pin_e2m1_table, pin_e4m3_codes, pin_bf16_cases, pin_worked_1x1x16, pin_worked_2x2x32,
         pin_one_hot, pin_brute_force_k16, pin_scale_linearity, pin_numpy_definition,
-        pin_fraction_exact, pin_fp8_numpy, pin_swizzle]
+        pin_fraction_exact, pin_fp8_numpy, pin_swizzle, pin_quantize_worked,
+        pin_quantize_nearest_bruteforce, pin_quantize_scale_invariance, pin_quantize_amax_element,
+        pin_quantize_dequant_bound]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -315,7 +433,8 @@ def test_oracle_pin(pin):
 
 
 MUTANTS = ["E2M1_BIAS0", "E2M1_NOSIGN", "E4M3_BIAS8", "SWAP_NIBBLES_A", "DROP_SFB",
-           "DROP_LAST_BLOCK", "TRANSPOSE_B", "SWIZZLE_ROWMAJOR_BLOCK"]
+           "DROP_LAST_BLOCK", "TRANSPOSE_B", "SWIZZLE_ROWMAJOR_BLOCK", "Q_TIES_AWAY", "Q_NO_SG",
+           "Q_SWAP_NIBBLES", "Q_E4M3_CEIL"]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
