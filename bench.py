@@ -324,6 +324,37 @@ def secondary_skinny(dev, steps: int, pk: dict, psrc: str) -> dict:
                       "buffer set (weights L2-resident)"}
 
 
+def secondary_quantize(dev, steps: int, pk: dict, psrc: str) -> dict:
+    """Two-level NVFP4 quantisation of a BF16 [16384][16384] matrix (one
+    operand of the headline GEMM): memset + amax pass + quantise pass.
+    Algorithmic bytes: X read twice (the global amax precedes every block's
+    scale), codes and swizzled scales written. X (512 MiB) exceeds L2."""
+    import block_scaled_precision_persistent_gb300 as bsg
+    rows, K = 16384, 16384
+    x = torch.randn((rows, K), device=dev, dtype=torch.float32).to(torch.bfloat16)
+    packed = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    swz = torch.empty(bsg.nvfp4_swizzled_scale_bytes(rows, K), dtype=torch.uint8, device=dev)
+    gl = torch.empty(2, dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        bsg.nvfp4_quantize(rows, K, x, packed, swz, None, gl, s)
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        bsg.nvfp4_quantize(rows, K, x, packed, swz, None, gl, s)
+        b.record(s)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+    moved = 2 * (2 * rows * K) + rows * K // 2 + bsg.nvfp4_swizzled_scale_bytes(rows, K)
+    gbs = moved / (us * 1e-6) / 1e9
+    return {"shape": f"bf16 {rows} x {K}", "us": round(us, 2), "gb_s": round(gbs, 1),
+            "frac_hbm": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": moved, "peak_source": psrc,
+            "launches": 2, "timing": "median per-call CUDA events (memset + 2 kernels), X > L2"}
+
+
 def secondary_swizzle(dev, steps: int, pk: dict, psrc: str) -> dict:
     """The scale-layout prep alone (timed separately from the GEMM): one
     operand's row-major [16384][1024] E4M3 scales into the swizzled layout;
@@ -423,6 +454,7 @@ def run_ours(args, dist: Dist) -> None:
         secondary["fp8"] = secondary_fp8(dev, max(3, args.steps), args.warmup, pk, psrc)
         secondary["skinny"] = secondary_skinny(dev, 20, pk, psrc)
         secondary["swizzle"] = secondary_swizzle(dev, 20, pk, psrc)
+        secondary["quantize"] = secondary_quantize(dev, 20, pk, psrc)
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, host_copy(step), args.cpu_seconds)

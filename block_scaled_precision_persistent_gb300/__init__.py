@@ -15,7 +15,7 @@ import ctypes
 from pathlib import Path
 
 __all__ = [
-    "BsgError", "load", "nvfp4_gemm", "nvfp4_gemm_swizzled", "nvfp4_swizzle_scales",
+    "BsgError", "load", "nvfp4_gemm", "nvfp4_gemm_swizzled", "nvfp4_swizzle_scales", "nvfp4_quantize",
     "nvfp4_swizzled_scale_bytes", "nvfp4_gemm_noalloc", "fp8_gemm", "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_select_plan", "bsg_last_launch_count", "bsg_error_string", "EXPORTED_SYMBOLS",
@@ -45,6 +45,7 @@ _SIGNATURES = {
     "nvfp4_gemm_swizzled": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "nvfp4_swizzle_scales": (_i, [_i, _i, _vp, _vp, _vp]),
     "nvfp4_swizzled_scale_bytes": (ctypes.c_size_t, [_i, _i]),
+    "nvfp4_quantize": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_gemm_noalloc": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "fp8_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "bsg_reserve_workspace": (_i, [_i, ctypes.c_size_t]),
@@ -125,6 +126,15 @@ def nvfp4_swizzle_scales(rows, K, sf, sf_swz, stream=None) -> None:
 
 def nvfp4_swizzled_scale_bytes(rows, K) -> int:
     return int(load().nvfp4_swizzled_scale_bytes(rows, K))
+
+
+def nvfp4_quantize(rows, K, X, packed, sf_swz, sf_rowmajor, global_scales, stream=None) -> None:
+    """Two-level NVFP4 quantisation of BF16 X[rows, K] into packed codes,
+    swizzled (and optionally row-major) E4M3 block scales, and
+    global_scales[0:2] = (amax, s_g) on the device; alpha for the GEMM is
+    1 / (s_gA * s_gB)."""
+    _check(load().nvfp4_quantize(rows, K, _ptr(X), _ptr(packed), _ptr(sf_swz), _ptr(sf_rowmajor),
+                                 _ptr(global_scales), _stream(stream)), "nvfp4_quantize")
 
 
 def nvfp4_gemm_noalloc(M, N, K, A, sfA, B, sfB, alpha, D, stream=None) -> None:

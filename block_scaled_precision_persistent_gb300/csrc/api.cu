@@ -427,6 +427,27 @@ int nvfp4_gemm(int M, int N, int K, const void *A, const void *sfA, const void *
     return run_gemm(Kind::NVFP4, M, N, K, A, B, swz_a, swz_b, nullptr, nullptr, alpha, D, s, ds);
 }
 
+int nvfp4_quantize(int rows, int K, const void *X, void *packed, void *sf_swz, void *sf_rowmajor,
+                   float *global, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    if (!X || !packed || !sf_swz || !global || rows < 1 || K < 16 || (K % 16) != 0)
+        return BSG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(packed) || !aligned16(sf_swz) ||
+        (reinterpret_cast<uintptr_t>(global) & 7u) != 0)
+        return BSG_ERR_MISALIGNED;
+    DeviceState *ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc != BSG_OK)
+        return rc;
+    if (bsg::launch_nvfp4_quantize(rows, K, X, static_cast<uint8_t *>(packed), static_cast<uint8_t *>(sf_swz),
+                                   static_cast<uint8_t *>(sf_rowmajor), global, ds->sms,
+                                   reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    t_last_launches = 2;
+    return BSG_OK;
+}
+
 int nvfp4_swizzle_scales(int rows, int K, const void *sf, void *sf_swz, bsg_stream_t stream)
 {
     t_last_launches = 0;

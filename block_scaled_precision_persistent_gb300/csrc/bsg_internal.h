@@ -89,6 +89,10 @@ int skinny_max_clusters(int i, int splits);
 cudaError_t launch_swizzle_scales(int rows, int K, const uint8_t *sf, uint8_t *out,
                                   cudaStream_t stream);
 
+// Two-level NVFP4 quantisation: memset of global[0], amax kernel, quantiser.
+cudaError_t launch_nvfp4_quantize(int rows, int K, const void *X, uint8_t *packed, uint8_t *sf_swz,
+                                  uint8_t *sf_rm, float *global, int num_sms, cudaStream_t stream);
+
 // Watchdog probe: waits on an mbarrier nothing arrives on.
 cudaError_t launch_watchdog_probe(unsigned int *status, unsigned long long ns,
                                   cudaStream_t stream);

@@ -1,0 +1,267 @@
+// Two-level NVFP4 quantisation of a BF16 matrix: the step in front of the
+// block-scaled GEMM ("Triton #11171 - Why Two New NVFP4 Test Cases Produced
+// Twelve Tensor-Memory Failures" names a shared NVFP4 quantisation there).
+//
+//   amax  = max |x| over the tensor
+//   s_g   = 2688 / amax (448 * 6; 1 if amax == 0)
+//   per 16-element block along K, bmax = max |x|:
+//     scale = E4M3 (round to nearest even, saturating at 448) of (bmax / 6) * s_g
+//     code  = E2M1 (round to nearest even, saturating at 6) of (x * s_g) / scale,
+//             0 for every element of a block whose scale is 0
+//
+// The codes are defined with every float operation rounded once, in this
+// order, so they are a function of the inputs alone. The kernel computes them
+// with approximate reciprocals and checks, per block and per 8 elements, that
+// both ends of a band around the approximation round to the same code; only
+// where a rounding threshold lies inside the band does it compute the exact
+// quotients (__fdiv_rn / __fmul_rn). Two launches: a global-amax reduction
+// (one HBM read of X), then the quantiser (second read of X, writes codes and
+// scales). X is read with 16-byte loads.
+//
+// Outputs: codes packed two per byte along K (element 2i in the low nibble),
+// block scales directly in the tcgen05 block-scale layout the GEMM reads
+// (rows padded to 128, scale columns to 4, 512-byte blocks of 128 rows x 4
+// scales, byte (r % 32) * 16 + (r / 32) * 4 + c inside a block, padding zero)
+// and, optionally, row-major.
+#include <cuda_bf16.h>
+
+#include "bsg_internal.h"
+#include "ptx.cuh"
+
+namespace bsg {
+
+namespace {
+
+constexpr int kAmaxThreads = 256;
+constexpr int kQThreads = 256;
+constexpr int kQRows = 128;                 // rows per quantiser CTA (one swizzled row block)
+constexpr int kQBlocks = 16;                // 16-element blocks per row per CTA (four 4-column groups)
+constexpr int kQPitch = 5;                  // words per staged row of scales (4 + 1, bank spread)
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// max |x| of the 8 BF16 values in a 16-byte vector
+__device__ __forceinline__ float absmax8(uint4 v)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, fabsf(bf16_bits_to_float(w[i] & 0xFFFFu)));
+        m = fmaxf(m, fabsf(bf16_bits_to_float(w[i] >> 16)));
+    }
+    return m;
+}
+
+// E4M3 code (round to nearest even, saturating at the largest finite 448)
+__device__ __forceinline__ uint32_t e4m3_code(float v)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+    return r & 0xFFu;
+}
+
+// E4M3 codes of two values: the common code if they agree, else 0x100
+__device__ __forceinline__ uint32_t e4m3_code2(float a, float b)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(a), "f"(b));
+    const uint32_t lo = r & 0xFFu, hi = (uint32_t)r >> 8;
+    return lo == hi ? lo : 0x100u;
+}
+
+// approximate reciprocal (within one unit in the last place)
+__device__ __forceinline__ float rcp_approx(float v)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// value of a non-negative finite E4M3 code (exponent bias 7, 3 mantissa bits)
+__device__ __forceinline__ float e4m3_value(uint32_t c)
+{
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    if (e == 0u)
+        return (float)m * 0.001953125f;                        // m * 2^-9
+    return __uint_as_float(((e + 120u) << 23) | (m << 20));    // (1 + m/8) * 2^(e-7)
+}
+
+// four bytes of two E2M1 codes each (round to nearest even, saturating at
+// 6); element 2i is the low nibble of byte i
+__device__ __forceinline__ uint32_t e2m1_pack8(const float (&y)[8])
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+    return r;
+}
+
+// Exact codes of 8 BF16 values (4 words): E2M1(RN(RN(x * s_g) / sv)). Kept
+// out of line so that the common path never executes it.
+__device__ __noinline__ uint32_t e2m1_exact8(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, float s_g,
+                                             float sv)
+{
+    const uint32_t w[4] = {w0, w1, w2, w3};
+    float y[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        y[2 * j] = __fdiv_rn(__fmul_rn(bf16_bits_to_float(w[j] & 0xFFFFu), s_g), sv);
+        y[2 * j + 1] = __fdiv_rn(__fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), s_g), sv);
+    }
+    return e2m1_pack8(y);
+}
+
+__global__ void __launch_bounds__(kAmaxThreads)
+    amax_kernel(const uint4 *__restrict__ x, size_t n_vec, unsigned int *__restrict__ amax_bits)
+{
+    float m = 0.0f;
+    const size_t stride = (size_t)gridDim.x * kAmaxThreads;
+    size_t i = (size_t)blockIdx.x * kAmaxThreads + threadIdx.x;
+    for (; i + 3 * stride < n_vec; i += 4 * stride) {        // four 16-byte loads in flight
+        const uint4 a = __ldg(x + i), b = __ldg(x + i + stride);
+        const uint4 c = __ldg(x + i + 2 * stride), d = __ldg(x + i + 3 * stride);
+        m = fmaxf(m, fmaxf(fmaxf(absmax8(a), absmax8(b)), fmaxf(absmax8(c), absmax8(d))));
+    }
+    for (; i < n_vec; i += stride)
+        m = fmaxf(m, absmax8(__ldg(x + i)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float wmax[kAmaxThreads / 32];
+    if ((threadIdx.x & 31) == 0)
+        wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = wmax[0];
+        for (int w = 1; w < kAmaxThreads / 32; ++w)
+            b = fmaxf(b, wmax[w]);
+        atomicMax(amax_bits, __float_as_uint(b));           // b >= 0: bit order is value order
+    }
+}
+
+// One CTA: rows [128 y, +128) x 16-element blocks [16 x, +16).
+__global__ void __launch_bounds__(kQThreads)
+    quantize_kernel(const __nv_bfloat16 *__restrict__ X, int rows, int K, uint8_t *__restrict__ packed,
+                    uint8_t *__restrict__ sf_swz, uint8_t *__restrict__ sf_rm, float *__restrict__ global)
+{
+    __shared__ uint32_t tile[kQRows * kQPitch];
+    uint8_t *t8 = reinterpret_cast<uint8_t *>(tile);
+    const int nb = K / 16;                          // scale columns
+    const int ncb = (nb + 3) / 4;                   // 4-column groups (swizzled layout)
+    const float amax = global[0];
+    const float s_g = amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f;
+    const float sg6 = s_g * 0.16666667163372039794921875f;      // s_g * RN(1/6), for the fast scale path
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        global[1] = s_g;
+
+#pragma unroll 2
+    for (int i = 0; i < kQRows * kQBlocks / kQThreads; ++i) {
+        const int idx = threadIdx.x + kQThreads * i;
+        const int r = idx / kQBlocks, cl = idx % kQBlocks;          // 16 consecutive threads: one row
+        const int row = blockIdx.y * kQRows + r, cb = blockIdx.x * kQBlocks + cl;
+        uint32_t scode = 0u;
+        if (row < rows && cb < nb) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(X + (size_t)row * (size_t)K + 16 * (size_t)cb);
+            const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+            const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            // bmax: max |x| on BF16 pairs (exact)
+            __nv_bfloat162 m2 = __habs2(*reinterpret_cast<const __nv_bfloat162 *>(&w[0]));
+#pragma unroll
+            for (int j = 1; j < 8; ++j)
+                m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j])));
+            const float bmax = fmaxf(__low2float(m2), __high2float(m2));
+            // scale = E4M3(RN(RN(bmax / 6) * s_g)). bmax * (s_g / 6) is within a
+            // few units in the last place of that value; where the E4M3 codes of
+            // the band around it (x (1 -+ 2^-20)) agree, they are the code (no
+            // E4M3 rounding threshold lies inside the band); otherwise the
+            // value is computed exactly.
+            const float sc = bmax * sg6;
+            scode = e4m3_code2(sc * 0.99999904632568359375f, sc * 1.00000095367431640625f);
+            if (scode > 0xFFu)                  // rare: an E4M3 threshold lies within the band
+                scode = e4m3_code(__fmul_rn(__fdiv_rn(bmax, 6.0f), s_g));
+            const float sv = e4m3_value(scode);
+            uint2 out = make_uint2(0u, 0u);
+            if (sv > 0.0f) {
+                // code_k = E2M1(RN(RN(x_k * s_g) / sv)). x_k * s_g * approx(1 / sv)
+                // is within ~2^-21 (relative) of that quotient, so the band
+                // x_k * k * (1 -+ 2^-20), k = s_g / sv, contains it. Where both
+                // ends of the band convert to the same codes, no E2M1 rounding
+                // threshold lies inside it and every value in it -- the exact
+                // quotient included -- has those codes. Where they differ (a
+                // threshold or tie is that close), the quotient is computed
+                // exactly.
+                const float k = s_g * rcp_approx(sv);
+                const float k_lo = k * 0.99999904632568359375f;   // 1 - 2^-20
+                const float k_hi = k * 1.00000095367431640625f;   // 1 + 2^-20
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float lo[8], hi[8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float xa = bf16_bits_to_float(w[4 * h + j] & 0xFFFFu);
+                        const float xb = __uint_as_float(w[4 * h + j] & 0xFFFF0000u);
+                        lo[2 * j] = xa * k_lo;
+                        lo[2 * j + 1] = xb * k_lo;
+                        hi[2 * j] = xa * k_hi;
+                        hi[2 * j + 1] = xb * k_hi;
+                    }
+                    uint32_t c = e2m1_pack8(lo);
+                    if (c != e2m1_pack8(hi))          // rare: a threshold lies within the band
+                        c = e2m1_exact8(w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3], s_g, sv);
+                    (h == 0 ? out.x : out.y) = c;
+                }
+            }
+            *reinterpret_cast<uint2 *>(packed + (size_t)row * (size_t)(K / 2) + 8 * (size_t)cb) = out;
+            if (sf_rm)
+                sf_rm[(size_t)row * (size_t)nb + cb] = (uint8_t)scode;
+        }
+        t8[r * (kQPitch * 4) + cl] = (uint8_t)scode;              // zero for padding rows / columns
+    }
+    __syncthreads();
+
+    // four 512-byte blocks of the swizzled layout: line l of group g holds
+    // the 4-scale words of rows l, l+32, l+64, l+96
+    const int g = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int cg = blockIdx.x * (kQBlocks / 4) + g;
+    if (threadIdx.x < 4 * 32 && cg < ncb) {
+        uint4 v;
+        v.x = tile[(l + 0) * kQPitch + g];
+        v.y = tile[(l + 32) * kQPitch + g];
+        v.z = tile[(l + 64) * kQPitch + g];
+        v.w = tile[(l + 96) * kQPitch + g];
+        reinterpret_cast<uint4 *>(sf_swz + ((size_t)blockIdx.y * (size_t)ncb + (size_t)cg) * 512u)[l] = v;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_nvfp4_quantize(int rows, int K, const void *X, uint8_t *packed, uint8_t *sf_swz,
+                                  uint8_t *sf_rm, float *global, int num_sms, cudaStream_t stream)
+{
+    cudaError_t e = cudaMemsetAsync(global, 0, sizeof(float), stream);
+    if (e != cudaSuccess)
+        return e;
+    const size_t n_vec = (size_t)rows * (size_t)K / 8;        // 16-byte vectors of 8 BF16
+    size_t blocks = (n_vec + kAmaxThreads - 1) / kAmaxThreads;
+    const size_t cap = (size_t)num_sms * 8;
+    if (blocks > cap)
+        blocks = cap;
+    amax_kernel<<<(unsigned)blocks, kAmaxThreads, 0, stream>>>(static_cast<const uint4 *>(X), n_vec,
+                                                                reinterpret_cast<unsigned int *>(global));
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    const int nb = K / 16;
+    dim3 grid((unsigned)((nb + kQBlocks - 1) / kQBlocks), (unsigned)((rows + kQRows - 1) / kQRows));
+    quantize_kernel<<<grid, kQThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(X), rows, K, packed,
+                                                     sf_swz, sf_rm, global);
+    return cudaGetLastError();
+}
+
+}  // namespace bsg

@@ -107,6 +107,29 @@ BSG_API int nvfp4_swizzle_scales(int rows, int K, const void *sf, void *sf_swz,
 /* Size in bytes of the swizzled layout (0 for invalid sizes). Host only.  */
 BSG_API size_t nvfp4_swizzled_scale_bytes(int rows, int K);
 
+/* ---------------------------------------------------------------------------
+ * Two-level NVFP4 quantisation of a BF16 matrix (the step in front of the
+ * GEMM: "Triton #11171 - Why Two New NVFP4 Test Cases Produced Twelve
+ * Tensor-Memory Failures" names a shared NVFP4 quantisation; the scheme is
+ * this library's reading of it):
+ *   amax  = max |x| over the matrix;  s_g = 2688 / amax (1 if amax == 0)
+ *   per 16 consecutive K elements, bmax = max |x|:
+ *     scale = E4M3 nearest-even (saturating at 448) of (bmax / 6) * s_g
+ *     code  = E2M1 nearest-even (saturating at 6) of (x * s_g) / scale
+ *             (0 where scale is 0), every step in FP32 rounded once
+ * so that D = A_q B_q^T / (s_gA s_gB): pass alpha = 1 / (s_gA * s_gB) to the
+ * GEMM.
+ *   X           : bf16[rows][K] row-major, device, 16-byte aligned
+ *   packed      : uint8[rows][K/2] out (element 2i in the low nibble), 16-byte aligned
+ *   sf_swz      : uint8[nvfp4_swizzled_scale_bytes(rows, K)] out, the layout
+ *                 nvfp4_gemm_swizzled reads (padding written zero), 16-byte aligned
+ *   sf_rowmajor : uint8[rows][K/16] out, or NULL
+ *   global      : float[2] device out: global[0] = amax, global[1] = s_g; 8-byte aligned
+ * Requires rows >= 1, K % 16 == 0, finite inputs. Stream-ordered: one
+ * 4-byte memset and two kernels; allocates nothing.                       */
+BSG_API int nvfp4_quantize(int rows, int K, const void *X, void *packed, void *sf_swz,
+                           void *sf_rowmajor, float *global, bsg_stream_t stream);
+
 /* NVFP4 GEMM with row-major scales that allocates nothing. The pages have no
  * counterpart to this entry point; it exists for callers that cannot call
  * cudaMalloc -- for instance a runtime that has handed all device memory to

@@ -145,3 +145,15 @@ def test_error_strings(lib):
     assert bsg.bsg_error_string(0) == "ok"
     assert "timed out" in bsg.bsg_error_string(bsg.BSG_ERR_DEVICE_TIMEOUT)
     assert bsg.bsg_error_string(99) == "unknown status"
+
+
+def test_quantize_bad_args(lib):
+    q = lib.nvfp4_quantize
+    assert q(0, 256, BAD, BAD, BAD, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert q(8, 24, BAD, BAD, BAD, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG          # K % 16
+    assert q(8, 256, None, BAD, BAD, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert q(8, 256, BAD, BAD, BAD, None, None, None) == bsg.BSG_ERR_INVALID_ARG         # no global
+    assert q(8, 256, BAD + 2, BAD, BAD, None, BAD, None) == bsg.BSG_ERR_MISALIGNED       # X
+    assert q(8, 256, BAD, BAD + 8, BAD, None, BAD, None) == bsg.BSG_ERR_MISALIGNED       # packed
+    assert q(8, 256, BAD, BAD, BAD + 4, None, BAD, None) == bsg.BSG_ERR_MISALIGNED       # sf_swz
+    assert q(8, 256, BAD, BAD, BAD, None, BAD + 4, None) == bsg.BSG_ERR_MISALIGNED       # global
