@@ -33,8 +33,12 @@ __device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity,
             return;
 }
 
-// Lane 0 waits (bounded); the verdict is broadcast so the warp stays
-// converged for the .sync.aligned tcgen05 loads that follow.
+// Lane 0 waits (bounded) and the verdict is broadcast, so the warp stays
+// converged for the .sync.aligned tcgen05 instructions that follow. The other
+// lanes are ordered after lane 0's acquiring wait by the warp barrier; they do
+// not poll the mbarrier themselves (a per-lane poll that starts by reading
+// the global timer was measured to add hundreds of cycles per wait, which on
+// the scale writers' path cost the pair kernel ~10 %).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Watchdog &wd,
                                           volatile int *abort_flag, uint32_t site, int lane)
 {
@@ -42,8 +46,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
     if (lane == 0)
         ok = mbar_wait(bar, parity, wd, abort_flag, site) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok && lane != 0)
-        mbar_wait_quiet(bar, parity, wd.limit_ns);   // already complete: returns at once
+    __syncwarp();
     return ok != 0;
 }
 
