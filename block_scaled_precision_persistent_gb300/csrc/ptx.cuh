@@ -80,6 +80,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 {
     if (mbar_try_wait(bar, parity))
         return true;
+    // spin a while before starting the clock: reading the global timer is
+    // slow, and most waits on the MMA's critical path end within these polls
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+        if (mbar_try_wait(bar, parity))
+            return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
