@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (plan, workload);
 # the summary it comes from is named in the comment. None = not captured.
 NCU_TRAFFIC_BYTES: dict[tuple[str, str], float] = {
-    # profiles/gemm_pair_nvfp4_256x256_s5_acc1_16384.md: 1.415 GB read + 0.520 GB written
-    ("nvfp4_tc2_256x256_s5_acc1", "nvfp4_16384"): 1414565000 + 520475392,
+    # profiles/gemm_pair_nvfp4_256x256_s5_acc1_16384.md: 1.399 GB read + 0.520 GB written
+    ("nvfp4_tc2_256x256_s5_acc1", "nvfp4_16384"): 1399263000 + 519851776,
 }
 
 
@@ -532,17 +532,41 @@ def run_reference(args, dist: Dist) -> None:
 
 def run_case(args) -> None:
     """One GEMM shape alone (--case nvfp4:MxNxK or fp8:MxNxK, optionally a
-    forced --plan): `warmup` untimed then `steps` timed launches, inputs
+    forced --plan), or the NVFP4 quantiser on BF16 ROWSxK (--case quantize:ROWSxK): `warmup` untimed then `steps` timed launches, inputs
     resident. Used for profiler captures of a single kernel and for ad-hoc
     timings; prints one JSON line."""
     import __graft_entry__
     __graft_entry__.build()
     import block_scaled_precision_persistent_gb300 as bsg
     kind, shape = args.case.split(":")
-    M, N, K = (int(x) for x in shape.lower().split("x"))
+    dims = [int(x) for x in shape.lower().split("x")]
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     s = torch.cuda.current_stream()
+    if kind == "quantize":
+        rows, K = dims
+        g = torch.Generator(device="cpu").manual_seed(0xB5C0)
+        x = torch.randn((rows, K), generator=g).to(torch.bfloat16).to(dev)
+        packed = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+        swz = torch.empty(bsg.nvfp4_swizzled_scale_bytes(rows, K), dtype=torch.uint8, device=dev)
+        gl = torch.empty(2, dtype=torch.float32, device=dev)
+        for _ in range(args.warmup):
+            bsg.nvfp4_quantize(rows, K, x, packed, swz, None, gl, s)
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            bsg.nvfp4_quantize(rows, K, x, packed, swz, None, gl, s)
+            b.record(s)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+        moved = 2 * (2 * rows * K) + rows * K // 2 + bsg.nvfp4_swizzled_scale_bytes(rows, K)
+        print(json.dumps({"case": args.case, "us": round(us, 2), "gb_s": round(moved / (us * 1e-6) / 1e9, 1)}),
+              flush=True)
+        return
+    M, N, K = dims
     D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     if kind == "nvfp4":
         p = workloads.make_nvfp4(workloads.WORKLOADS["nvfp4_4096"], dev, M=M, N=N, K=K)
@@ -597,7 +621,8 @@ def main() -> None:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--case", default=None,
-                    help="time one shape alone instead of the benchmark: nvfp4:MxNxK or fp8:MxNxK")
+                    help="time one shape alone instead of the benchmark: nvfp4:MxNxK, fp8:MxNxK or "
+                         "quantize:ROWSxK")
     ap.add_argument("--plan", default=None, help="with --case: force this plan")
     args = ap.parse_args()
     if args.case:

@@ -103,19 +103,49 @@ __device__ __forceinline__ uint32_t e2m1_pack8(const float (&y)[8])
     return r;
 }
 
-// Exact codes of 8 BF16 values (4 words): E2M1(RN(RN(x * s_g) / sv)). Kept
-// out of line so that the common path never executes it.
-__device__ __noinline__ uint32_t e2m1_exact8(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, float s_g,
-                                             float sv)
+// Exact codes where the fast path's band straddles an E2M1 rounding threshold
+// (about 0.5 % of elements on BF16 data: exact ties are common). c_lo / c_hi: the 8 codes (4 bytes, 2 per byte) of the band's ends. Where a
+// nibble differs, the two codes are neighbours and the threshold between them
+// is mid = (m + m') / 2 with at most 3 significant bits; scale sv has at most
+// 4, so mid * sv is exact, and t = RN(x * s_g) lies within a factor 1 +- 2^-20
+// of it, so fma(-mid, sv, t) = t - mid * sv exactly (Sterbenz). Then
+//   RN(t / sv) == mid  <=>  -ulp_below(mid)/2 <= (t - mid*sv)/sv <= ulp(mid)/2
+// (mid has an even last mantissa bit, so the half-way cases round to it), in
+// which case the E2M1 tie goes to the code with the even mantissa; otherwise
+// the sign of t - mid*sv picks the code. No division.
+__device__ __forceinline__ uint32_t e2m1_fix8(uint32_t c_lo, uint32_t c_hi, uint32_t w0, uint32_t w1, uint32_t w2,
+                                               uint32_t w3, float s_g, float sv)
 {
-    const uint32_t w[4] = {w0, w1, w2, w3};
-    float y[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        y[2 * j] = __fdiv_rn(__fmul_rn(bf16_bits_to_float(w[j] & 0xFFFFu), s_g), sv);
-        y[2 * j + 1] = __fdiv_rn(__fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), s_g), sv);
+    uint32_t out = c_lo;
+    uint32_t diff = c_lo ^ c_hi;
+    while (diff != 0u) {                                    // usually one nibble
+        const int e = (__ffs(diff) - 1) >> 2;
+        diff &= ~(15u << (4 * e));
+        const uint32_t a = (c_lo >> (4 * e)) & 15u, b = (c_hi >> (4 * e)) & 15u;
+        const uint32_t ma = a & 7u, mb = b & 7u;
+        const uint32_t lo_mag = min(ma, mb), hi_mag = max(ma, mb);   // neighbours
+        // midpoint between E2M1 magnitudes lo_mag and lo_mag + 1:
+        // .25 .75 1.25 1.75 (step .5), then 2.5 3.5, then 5
+        const float mid = lo_mag < 4u ? 0.25f + 0.5f * (float)lo_mag
+                                      : (lo_mag < 6u ? (float)lo_mag - 1.5f : 5.0f);
+        // its unit in the last place above (2^(exponent - 23)) and below
+        // (half of that when mid is a power of two: only .25)
+        const uint32_t mb_bits = __float_as_uint(mid);
+        const float ulp_up = __uint_as_float((mb_bits & 0x7F800000u) - (23u << 23));
+        const float ulp_dn = (mb_bits & 0x007FFFFFu) ? ulp_up : 0.5f * ulp_up;
+        const int wi = e >> 1;                              // selected without indexing (no local memory)
+        const uint32_t word = wi == 0 ? w0 : wi == 1 ? w1 : wi == 2 ? w2 : w3;
+        const float x = (e & 1) ? __uint_as_float(word & 0xFFFF0000u) : bf16_bits_to_float(word & 0xFFFFu);
+        const float t = fabsf(__fmul_rn(x, s_g));
+        const float d = fmaf(-mid, sv, t);                  // exact: t - mid * sv
+        uint32_t mag;
+        if (d <= 0.5f * ulp_up * sv && d >= -0.5f * ulp_dn * sv)
+            mag = (lo_mag & 1u) ? hi_mag : lo_mag;          // RN(t / sv) == mid: tie to the even code
+        else
+            mag = d > 0.0f ? hi_mag : lo_mag;
+        out = (out & ~(15u << (4 * e))) | (((a & 8u) | mag) << (4 * e));
     }
-    return e2m1_pack8(y);
+    return out;
 }
 
 __global__ void __launch_bounds__(kAmaxThreads)
@@ -213,8 +243,9 @@ __global__ void __launch_bounds__(kQThreads)
                         hi[2 * j + 1] = xb * k_hi;
                     }
                     uint32_t c = e2m1_pack8(lo);
-                    if (c != e2m1_pack8(hi))          // rare: a threshold lies within the band
-                        c = e2m1_exact8(w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3], s_g, sv);
+                    const uint32_t ch = e2m1_pack8(hi);
+                    if (c != ch)                      // a threshold lies within the band
+                        c = e2m1_fix8(c, ch, w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3], s_g, sv);
                     (h == 0 ? out.x : out.y) = c;
                 }
             }
