@@ -82,12 +82,13 @@ class Oracle:
         L.bso_bf16_rne.restype = ctypes.c_uint16
         L.bso_bf16_rne.argtypes = [ctypes.c_double]
         L.bso_nvfp4_gemm.restype = ctypes.c_int
-        L.bso_nvfp4_gemm.argtypes = [ctypes.c_int] * 3 + [u8p] * 4 + [ctypes.c_float, i32p,
-                                    ctypes.c_int, i32p, ctypes.c_int, f64p, f64p, u16p,
+        f32p = ctypes.POINTER(ctypes.c_float)
+        L.bso_nvfp4_gemm.argtypes = [ctypes.c_int] * 3 + [u8p] * 4 + [ctypes.c_float, f32p, f32p,
+                                    i32p, ctypes.c_int, i32p, ctypes.c_int, f64p, f64p, u16p,
                                     ctypes.c_int]
         L.bso_fp8_gemm.restype = ctypes.c_int
         L.bso_fp8_gemm.argtypes = [ctypes.c_int] * 3 + [u8p] * 2 + [ctypes.c_float] * 3 + [
-            i32p, ctypes.c_int, i32p, ctypes.c_int, f64p, f64p, u16p, ctypes.c_int]
+            f32p, f32p, i32p, ctypes.c_int, i32p, ctypes.c_int, f64p, f64p, u16p, ctypes.c_int]
         L.bso_swizzled_scale_bytes.restype = ctypes.c_size_t
         L.bso_swizzled_scale_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
         L.bso_swizzle_scales.restype = ctypes.c_int
@@ -119,12 +120,24 @@ class Oracle:
     def _p(a, ct):
         return None if a is None else a.ctypes.data_as(ctypes.POINTER(ct))
 
-    def nvfp4_gemm(self, A, sfA, B, sfB, alpha, K, rows=None, cols=None, nthreads=None):
+    @staticmethod
+    def _vec(v, n):
+        if v is None:
+            return None
+        arr = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+        assert arr.shape == (n,), (arr.shape, n)
+        return arr
+
+    def nvfp4_gemm(self, A, sfA, B, sfB, alpha, K, rows=None, cols=None, nthreads=None,
+                   bias=None, gamma=None):
         """Return (S, T, D_bits) over the selected rows x cols.
 
         A: uint8[M, K/2], sfA: uint8[M, K/16], B: uint8[N, K/2], sfB: uint8[N, K/16].
-        S is the unrounded double result, T the magnitude sum of the tolerance,
-        D_bits the BF16 bit patterns (uint16) of S rounded once.
+        bias: float32[N] or None, gamma: float32[M] or None (the epilogue
+        S' = gamma[i] * (S + bias[j])). S is the unrounded double result, T the
+        magnitude sum of the tolerance, D_bits the BF16 bit patterns (uint16)
+        of S rounded once. Rows come in logical (computed) order; see
+        scatter_rows for the scattered output placement.
         """
         A = np.ascontiguousarray(A, dtype=np.uint8)
         B = np.ascontiguousarray(B, dtype=np.uint8)
@@ -133,6 +146,7 @@ class Oracle:
         M, N = A.shape[0], B.shape[0]
         assert A.shape == (M, K // 2) and B.shape == (N, K // 2)
         assert sfA.shape == (M, K // 16) and sfB.shape == (N, K // 16)
+        bias, gamma = self._vec(bias, N), self._vec(gamma, M)
         r, nr = self._sel(rows, M)
         c, nc = self._sel(cols, N)
         S = np.empty((nr, nc), np.float64)
@@ -140,7 +154,8 @@ class Oracle:
         D = np.empty((nr, nc), np.uint16)
         rc = self.lib.bso_nvfp4_gemm(M, N, K, self._p(A, ctypes.c_uint8), self._p(sfA, ctypes.c_uint8),
                                      self._p(B, ctypes.c_uint8), self._p(sfB, ctypes.c_uint8),
-                                     float(alpha), self._p(r, ctypes.c_int32), nr,
+                                     float(alpha), self._p(bias, ctypes.c_float),
+                                     self._p(gamma, ctypes.c_float), self._p(r, ctypes.c_int32), nr,
                                      self._p(c, ctypes.c_int32), nc, self._p(S, ctypes.c_double),
                                      self._p(T, ctypes.c_double), self._p(D, ctypes.c_uint16),
                                      nthreads or default_threads())
@@ -148,26 +163,45 @@ class Oracle:
             raise ValueError(f"bso_nvfp4_gemm rejected its arguments (rc={rc})")
         return S, T, D
 
-    def fp8_gemm(self, A, B, alpha, sA=1.0, sB=1.0, rows=None, cols=None, nthreads=None):
-        """FP8 E4M3 GEMM: D = alpha*sA*sB * A B^T. A: uint8[M, K], B: uint8[N, K]."""
+    def fp8_gemm(self, A, B, alpha, sA=1.0, sB=1.0, rows=None, cols=None, nthreads=None,
+                 bias=None, gamma=None):
+        """FP8 E4M3 GEMM: D = alpha*sA*sB * A B^T. A: uint8[M, K], B: uint8[N, K];
+        bias / gamma as for nvfp4_gemm."""
         A = np.ascontiguousarray(A, dtype=np.uint8)
         B = np.ascontiguousarray(B, dtype=np.uint8)
         M, K = A.shape
         N = B.shape[0]
         assert B.shape == (N, K)
+        bias, gamma = self._vec(bias, N), self._vec(gamma, M)
         r, nr = self._sel(rows, M)
         c, nc = self._sel(cols, N)
         S = np.empty((nr, nc), np.float64)
         T = np.empty((nr, nc), np.float64)
         D = np.empty((nr, nc), np.uint16)
         rc = self.lib.bso_fp8_gemm(M, N, K, self._p(A, ctypes.c_uint8), self._p(B, ctypes.c_uint8),
-                                   float(alpha), float(sA), float(sB), self._p(r, ctypes.c_int32), nr,
+                                   float(alpha), float(sA), float(sB), self._p(bias, ctypes.c_float),
+                                   self._p(gamma, ctypes.c_float), self._p(r, ctypes.c_int32), nr,
                                    self._p(c, ctypes.c_int32), nc, self._p(S, ctypes.c_double),
                                    self._p(T, ctypes.c_double), self._p(D, ctypes.c_uint16),
                                    nthreads or default_threads())
         if rc != 0:
             raise ValueError(f"bso_fp8_gemm rejected its arguments (rc={rc})")
         return S, T, D
+
+    @staticmethod
+    def scatter_rows(D_rows, scatter, out):
+        """Scattered output placement ("Triton #11171 ...", section "Scatter
+        changes where output rows are written"): logical computed row i goes to
+        physical row scatter[i] of `out` (modified in place and returned). A
+        destination outside [0, out rows) writes nothing -- a negative index
+        marks a row to drop. Destinations must be distinct."""
+        D_rows = np.asarray(D_rows)
+        dst = np.asarray(scatter, dtype=np.int64)
+        assert dst.shape == (D_rows.shape[0],)
+        for i in range(dst.size):
+            if 0 <= dst[i] < out.shape[0]:
+                out[dst[i]] = D_rows[i]
+        return out
 
     # -- scale layout ---------------------------------------------------------
     def nvfp4_quantize(self, x_bf16_bits):

@@ -28,7 +28,7 @@
  *    E4M3 as in the OCP 8-bit Floating Point (OFP8) specification ("E4M3",
  *    no infinities, S.1111.111 is NaN).
  *
- * Readings where the sources are silent (each is listed in the design doc):
+ * Readings where the sources are silent:
  *  - element 2i of a packed row sits in bits 0..3 of byte i, element 2i+1 in
  *    bits 4..7;
  *  - T (the magnitude sum in the tolerance) includes the scales and alpha, so
@@ -161,6 +161,8 @@ typedef struct {
     int M, N, K;
     const uint8_t *A, *sfA, *B, *sfB;
     double scale;                 /* alpha (NVFP4) or alpha*sA*sB (FP8)       */
+    const float *bias;            /* [N] added per output column, or NULL    */
+    const float *gamma;           /* [M] per-row multiplier, or NULL         */
     const int32_t *rows;
     int nrows;
     const int32_t *cols;
@@ -233,6 +235,42 @@ static void fp8_element(const job_t *jb, int i, int j, double *S, double *T)
     *T = fabs(jb->scale) * t;
 }
 
+/* Epilogue variants ("Triton #11171 ...", section "The ordinary variants
+ * also exercise the shared bias route" and the two sections before it):
+ * the matmul result gets the shared bias added, is multiplied by the per-row
+ * gamma, and (outside this function) its row is written to a scattered
+ * position. Reading: bias is indexed by output column j, gamma by logical
+ * output row i, bias comes before gamma:
+ *     S' = gamma[i] * (S + bias[j]),   T' = |gamma[i]| * (T + |bias[j]|)
+ * Both are FP32 inputs widened exactly to double; still one rounding.      */
+static void epilogue(const job_t *jb, int i, int j, double *S, double *T)
+{
+    if (jb->bias) {
+#ifdef BSO_MUTANT_EPI_BIAS_BY_ROW
+        double b = (double)jb->bias[i < jb->N ? i : 0];
+#else
+        double b = (double)jb->bias[j];
+#endif
+#ifdef BSO_MUTANT_EPI_GAMMA_FIRST
+        if (jb->gamma) {
+            *S *= (double)jb->gamma[i];
+            *T *= fabs((double)jb->gamma[i]);
+        }
+        *S += b;
+        *T += fabs(b);
+        return;
+#else
+        *S += b;
+        *T += fabs(b);
+#endif
+    }
+    if (jb->gamma) {
+        double g = (double)jb->gamma[i];
+        *S *= g;
+        *T *= fabs(g);
+    }
+}
+
 static void *worker(void *arg)
 {
     job_t *jb = (job_t *)arg;
@@ -245,6 +283,7 @@ static void *worker(void *arg)
                 nvfp4_element(jb, i, j, &S, &T);
             else
                 fp8_element(jb, i, j, &S, &T);
+            epilogue(jb, i, j, &S, &T);
             size_t o = (size_t)r * (size_t)jb->ncols + (size_t)c;
             if (jb->S) jb->S[o] = S;
             if (jb->T) jb->T[o] = T;
@@ -306,10 +345,12 @@ static int check_sel(const int32_t *sel, int n, int lim)
 
 /* NVFP4 GEMM over the selected rows x cols of D (rows/cols NULL = all).
  * A: uint8[M][K/2], sfA: uint8[M][K/16] row-major E4M3, B: uint8[N][K/2],
- * sfB: uint8[N][K/16]. Outputs are [nrows][ncols]; any may be NULL.
+ * sfB: uint8[N][K/16]; bias float[N] and gamma float[M] may be NULL (see
+ * epilogue above). Outputs are [nrows][ncols]; any may be NULL.
  * Returns 0, or -1 for bad sizes.                                          */
 int bso_nvfp4_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *sfA,
                    const uint8_t *B, const uint8_t *sfB, float alpha,
+                   const float *bias, const float *gamma,
                    const int32_t *rows, int nrows, const int32_t *cols, int ncols,
                    double *S, double *T, uint16_t *D, int nthreads)
 {
@@ -325,6 +366,7 @@ int bso_nvfp4_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *sfA,
     jb.M = M; jb.N = N; jb.K = K;
     jb.A = A; jb.sfA = sfA; jb.B = B; jb.sfB = sfB;
     jb.scale = (double)alpha;
+    jb.bias = bias; jb.gamma = gamma;
     jb.rows = rows; jb.nrows = nrows; jb.cols = cols; jb.ncols = ncols;
     jb.S = S; jb.T = T; jb.D = D;
     return run(&jb, nthreads);
@@ -334,6 +376,7 @@ int bso_nvfp4_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *sfA,
  * is the exact double product alpha * sA * sB of the three FP32 values.    */
 int bso_fp8_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *B,
                  float alpha, float sA, float sB,
+                 const float *bias, const float *gamma,
                  const int32_t *rows, int nrows, const int32_t *cols, int ncols,
                  double *S, double *T, uint16_t *D, int nthreads)
 {
@@ -349,6 +392,7 @@ int bso_fp8_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *B,
     jb.M = M; jb.N = N; jb.K = K;
     jb.A = A; jb.B = B;
     jb.scale = (double)alpha * (double)sA * (double)sB;
+    jb.bias = bias; jb.gamma = gamma;
     jb.rows = rows; jb.nrows = nrows; jb.cols = cols; jb.ncols = ncols;
     jb.S = S; jb.T = T; jb.D = D;
     return run(&jb, nthreads);
@@ -406,7 +450,7 @@ int bso_swizzle_scales(int rows, int K, const uint8_t *in, uint8_t *out)
 /* "Triton #11171 - Why Two New NVFP4 Test Cases Produced Twelve
  * Tensor-Memory Failures" names a shared NVFP4 quantisation step in front of
  * the block-scaled GEMM; the pages give no formula. The scheme written out
- * here is the plainest reading (listed in the design doc):
+ * here is the plainest reading:
  *
  *   amax  = max |x| over the whole tensor                    (exact)
  *   s_g   = 2688 / amax   (448 * 6; 1 when amax == 0)         (FP32, rounded once)

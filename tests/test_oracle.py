@@ -8,7 +8,8 @@ definition. ``test_planted_mistake_is_caught`` compiles the oracle with one
 deliberate mistake at a time (a wrong exponent bias, a dropped sign, swapped
 nibbles in one operand, a dropped scale, a dropped block, a transposed operand, a wrong
 scale layout; in the quantiser, ties rounded away from zero, a dropped global
-scale, swapped nibbles, block scales rounded up) and shows that at least one
+scale, swapped nibbles, block scales rounded up; in the epilogue, gamma
+applied before the bias, bias indexed by row) and shows that at least one
 pin fails for each.
 """
 from __future__ import annotations
@@ -269,6 +270,84 @@ def pin_fp8_numpy(o):
     assert np.array_equal(T, (np.abs(dec[A]) @ np.abs(dec[B]).T) * float(np.float32(p["alpha"])))
 
 
+def pin_epilogue_worked(o):
+    """Bias, gamma and scatter on the hand-worked case of
+    tests/golden/nvfp4_epilogue_case.txt (values and signs exact)."""
+    g = {}
+    for t in _rows("nvfp4_epilogue_case.txt"):
+        g.setdefault(t[0], []).append(t[1:])
+    ac = [int(c, 16) for c in g["acodes"][0]]
+    bc = [int(c, 16) for c in g["bcodes"][0]]
+    A = pack(np.array([[c] * 16 for c in ac], np.uint8))
+    B = pack(np.array([[c] * 16 for c in bc], np.uint8))
+    sfA = np.full((len(ac), 1), 0x38, np.uint8)
+    sfB = np.full((len(bc), 1), 0x38, np.uint8)
+    bias = np.array([float(v) for v in g["bias"][0]], np.float32)
+    gamma = np.array([float(v) for v in g["gamma"][0]], np.float32)
+    S, T, D = o.nvfp4_gemm(A, sfA, B, sfB, float(g["alpha"][0][0]), 16, bias=bias, gamma=gamma)
+    Dv = oracle.bf16_bits_to_float(D)
+    for r in g["D"]:
+        i = int(r[0])
+        want = [float(v) for v in r[1:]]
+        assert S[i].tolist() == want and Dv[i].tolist() == want, (i, S[i], want)
+        assert [math.copysign(1, v) for v in Dv[i]] == [math.copysign(1, v) for v in want], i
+    for r in g["T"]:
+        assert T[int(r[0])].tolist() == [float(v) for v in r[1:]], ("T", r[0])
+    out = np.full(D.shape, 0x7FC0, np.uint16)
+    o.scatter_rows(D, [int(v) for v in g["scatter"][0]], out)
+    outv = oracle.bf16_bits_to_float(out)
+    for r in g["out"]:
+        want = np.array([float(v) for v in r[1:]])
+        got = outv[int(r[0])]
+        assert np.array_equal(np.isnan(got), np.isnan(want)), r[0]
+        assert np.array_equal(got[~np.isnan(want)], want[~np.isnan(want)]), (r[0], got, want)
+
+
+def pin_epilogue_numpy(o):
+    # Independent restatement of the epilogue in numpy (float64) on a
+    # rectangular problem with 2^u scales (all sums exact): bias broadcast
+    # over rows, gamma over columns, bias before gamma. Also FP8.
+    M, N, K = 24, 40, 64
+    A, sfA, B, sfB = _uniform_problem(M, N, K, 13)
+    rng = np.random.default_rng(4)
+    bias = rng.standard_normal(N).astype(np.float32)
+    gamma = rng.standard_normal(M).astype(np.float32)
+    S, T, _ = o.nvfp4_gemm(A, sfA, B, sfB, 0.75, K, bias=bias, gamma=gamma)
+    da, db = deq_nvfp4(A, sfA), deq_nvfp4(B, sfB)
+    ref = (0.75 * (da @ db.T) + bias.astype(np.float64)[None, :]) * gamma.astype(np.float64)[:, None]
+    assert np.allclose(S, ref, rtol=1e-15, atol=0)
+    Tref = (0.75 * (np.abs(da) @ np.abs(db).T) + np.abs(bias.astype(np.float64))[None, :]) \
+        * np.abs(gamma.astype(np.float64))[:, None]
+    assert np.allclose(T, Tref, rtol=1e-15, atol=0)
+    # gamma alone and bias alone
+    Sg, _, _ = o.nvfp4_gemm(A, sfA, B, sfB, 0.75, K, gamma=gamma)
+    assert np.allclose(Sg, 0.75 * (da @ db.T) * gamma.astype(np.float64)[:, None], rtol=1e-15, atol=0)
+    Sb, _, _ = o.nvfp4_gemm(A, sfA, B, sfB, 0.75, K, bias=bias)
+    assert np.allclose(Sb, 0.75 * (da @ db.T) + bias.astype(np.float64)[None, :], rtol=1e-15, atol=0)
+    w = workloads.WORKLOADS["fp8_8192"]
+    p = workloads.make_fp8(w, "cpu", M=M, N=N, K=96)
+    dec = np.array([e4m3_lib(c) for c in range(256)])
+    S8, _, _ = o.fp8_gemm(p["A"].numpy(), p["B"].numpy(), 2.0, 0.5, 3.0, bias=bias, gamma=gamma)
+    ref8 = ((dec[p["A"].numpy()] @ dec[p["B"].numpy()].T) * 3.0 + bias.astype(np.float64)[None, :]) \
+        * gamma.astype(np.float64)[:, None]
+    assert np.allclose(S8, ref8, rtol=1e-15, atol=0)
+
+
+def pin_scatter_permutation(o):
+    # Scatter by a permutation, then gather back by the same permutation,
+    # gives the logical rows; dropped rows keep the prefill.
+    D = np.arange(7 * 3, dtype=np.uint16).reshape(7, 3)
+    perm = np.random.default_rng(2).permutation(7)
+    out = o.scatter_rows(D, perm, np.zeros((7, 3), np.uint16))
+    assert np.array_equal(out[perm], D)
+    drop = perm.copy()
+    drop[[1, 4]] = -1
+    out2 = o.scatter_rows(D, drop, np.full((7, 3), 999, np.uint16))
+    kept = drop >= 0
+    assert np.array_equal(out2[drop[kept]], D[kept])
+    assert (np.delete(out2, drop[kept], axis=0) == 999).all()
+
+
 def _swizzle_numpy(sf: np.ndarray, K: int) -> np.ndarray:
     """Independent restatement of the 128x4-blocked scale layout by reshapes."""
     rows, cols = sf.shape
@@ -424,7 +503,7 @@ PINS = [pin_e2m1_table, pin_e4m3_codes, pin_bf16_cases, pin_worked_1x1x16, pin_w
         pin_one_hot, pin_brute_force_k16, pin_scale_linearity, pin_numpy_definition,
         pin_fraction_exact, pin_fp8_numpy, pin_swizzle, pin_quantize_worked,
         pin_quantize_nearest_bruteforce, pin_quantize_scale_invariance, pin_quantize_amax_element,
-        pin_quantize_dequant_bound]
+        pin_quantize_dequant_bound, pin_epilogue_worked, pin_epilogue_numpy, pin_scatter_permutation]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -434,7 +513,7 @@ def test_oracle_pin(pin):
 
 MUTANTS = ["E2M1_BIAS0", "E2M1_NOSIGN", "E4M3_BIAS8", "SWAP_NIBBLES_A", "DROP_SFB",
            "DROP_LAST_BLOCK", "TRANSPOSE_B", "SWIZZLE_ROWMAJOR_BLOCK", "Q_TIES_AWAY", "Q_NO_SG",
-           "Q_SWAP_NIBBLES", "Q_E4M3_CEIL"]
+           "Q_SWAP_NIBBLES", "Q_E4M3_CEIL", "EPI_GAMMA_FIRST", "EPI_BIAS_BY_ROW"]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
