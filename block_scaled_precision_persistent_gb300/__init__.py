@@ -16,7 +16,8 @@ from pathlib import Path
 
 __all__ = [
     "BsgError", "load", "nvfp4_gemm", "nvfp4_gemm_swizzled", "nvfp4_swizzle_scales", "nvfp4_quantize",
-    "nvfp4_swizzled_scale_bytes", "nvfp4_gemm_noalloc", "fp8_gemm", "bsg_reserve_workspace", "bsg_get_device_status",
+    "nvfp4_swizzled_scale_bytes", "nvfp4_gemm_noalloc", "fp8_gemm", "nvfp4_gemm_ex", "fp8_gemm_ex",
+    "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_select_plan", "bsg_last_launch_count", "bsg_error_string", "EXPORTED_SYMBOLS",
     "BSG_OK", "BSG_ERR_INVALID_ARG", "BSG_ERR_MISALIGNED", "BSG_ERR_UNSUPPORTED_DEVICE",
@@ -48,6 +49,8 @@ _SIGNATURES = {
     "nvfp4_quantize": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_gemm_noalloc": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "fp8_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
+    "nvfp4_gemm_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
+    "fp8_gemm_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "bsg_reserve_workspace": (_i, [_i, ctypes.c_size_t]),
     "bsg_get_device_status": (_i, [_vp]),
     "bsg_last_status_word": (ctypes.c_uint32, []),
@@ -150,6 +153,24 @@ def fp8_gemm(M, N, K, A, sA, B, sB, alpha, D, stream=None) -> None:
     """D = alpha*sA*sB * A B^T, E4M3 operands; sA/sB device float tensors or None."""
     _check(load().fp8_gemm(M, N, K, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), float(alpha), _ptr(D),
                            _stream(stream)), "fp8_gemm")
+
+
+def nvfp4_gemm_ex(M, N, K, A, sfA_swz, B, sfB_swz, alpha, bias, gamma, scatter, m_out, D,
+                  stream=None) -> None:
+    """As nvfp4_gemm_swizzled with the fused epilogue
+    D[scatter[m]][n] = bf16(gamma[m] * (alpha * acc[m][n] + bias[n])):
+    bias float32[N], gamma float32[M], scatter int32[M] (each None to omit);
+    D has m_out rows (m_out == M without scatter)."""
+    _check(load().nvfp4_gemm_ex(M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), _ptr(sfB_swz), float(alpha),
+                                _ptr(bias), _ptr(gamma), _ptr(scatter), int(m_out), _ptr(D),
+                                _stream(stream)), "nvfp4_gemm_ex")
+
+
+def fp8_gemm_ex(M, N, K, A, sA, B, sB, alpha, bias, gamma, scatter, m_out, D, stream=None) -> None:
+    """As fp8_gemm with the fused epilogue of nvfp4_gemm_ex."""
+    _check(load().fp8_gemm_ex(M, N, K, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), float(alpha), _ptr(bias),
+                              _ptr(gamma), _ptr(scatter), int(m_out), _ptr(D), _stream(stream)),
+           "fp8_gemm_ex")
 
 
 def bsg_reserve_workspace(device: int, nbytes: int) -> None:

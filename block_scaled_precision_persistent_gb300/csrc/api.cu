@@ -181,15 +181,36 @@ int skinny_cluster_capacity(int id, int splits)
     return cache[dev][id][j];
 }
 
+// Epilogue operands of one call (all null: the plain GEMM).
+struct Epilogue {
+    const float *bias = nullptr;
+    const float *gamma = nullptr;
+    const int32_t *scatter = nullptr;
+    int m_out = 0;
+};
+
+void set_epilogue(GemmArgs &a, const Epilogue &e, void *D)
+{
+    a.bias = e.bias;
+    a.gamma = e.gamma;
+    a.scatter = e.scatter;
+    a.d = static_cast<uint16_t *>(D);
+    a.m_out = e.m_out;
+}
+
 int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A, const void *B,
-               const uint8_t *sfa, const uint8_t *sfb, float alpha, void *D, cudaStream_t stream,
-               DeviceState *ds);
+               const uint8_t *sfa, const uint8_t *sfb, float alpha, void *D, const Epilogue &epi,
+               cudaStream_t stream, DeviceState *ds);
+
+// Rows of D: M, or m_out when rows are scattered (the tensor map of D then
+// only describes the buffer; the scattered rows are stored without it).
+uint64_t d_rows(int M, const Epilogue &e) { return (uint64_t)(e.scatter ? e.m_out : M); }
 
 // Swap-AB split-K launch for skinny M: weight tiles of 128 rows on grid x,
 // the K split on grid y (one thread-block cluster per weight tile).
 int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A, const void *B,
-               const uint8_t *sfa, const uint8_t *sfb, float alpha, void *D, cudaStream_t stream,
-               DeviceState *ds)
+               const uint8_t *sfa, const uint8_t *sfb, float alpha, void *D, const Epilogue &epi,
+               cudaStream_t stream, DeviceState *ds)
 {
     const int id = plan - bsg::tc1_num_plans() - bsg::pair_num_plans();
     const int num_n_tiles = (N + pi.bn - 1) / pi.bn;
@@ -208,7 +229,7 @@ int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A,
                         128, (uint32_t)pi.tile_m)) != BSG_OK ||
         (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, (uint64_t)N, row_bytes,
                         128, (uint32_t)pi.bn)) != BSG_OK ||
-        (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)M,
+        (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, d_rows(M, epi),
                         (uint64_t)N * 2u, (uint32_t)(pi.bn / splits), (uint32_t)pi.tile_m,
                         CU_TENSOR_MAP_SWIZZLE_NONE)) != BSG_OK)
         return rc;
@@ -229,6 +250,7 @@ int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A,
     a.alpha = alpha;
     a.status = ds->status;
     a.timeout_ns = g_watchdog_ns.load();
+    set_epilogue(a, epi, D);
     if (bsg::skinny_launch(id, maps, a, splits, stream) != cudaSuccess)
         return BSG_ERR_CUDA;
     ++t_last_launches;
@@ -238,7 +260,7 @@ int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A,
 // Encode the maps and launch one persistent GEMM.
 int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const uint8_t *sfa,
              const uint8_t *sfb, const float *sA, const float *sB, float alpha, void *D,
-             cudaStream_t stream, DeviceState *ds)
+             cudaStream_t stream, DeviceState *ds, const Epilogue &epi = Epilogue())
 {
     int plan = -1;
     int rc = choose_plan(kind, M, N, K, ds->sms, &plan);
@@ -247,7 +269,7 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     const PlanInfo &pi = bsg::plan_info(plan);
     const uint64_t row_bytes = kind == Kind::NVFP4 ? (uint64_t)K / 2u : (uint64_t)K;
     if (pi.family == bsg::Family::SKINNY)
-        return run_skinny(plan, pi, M, N, K, A, B, sfa, sfb, alpha, D, stream, ds);
+        return run_skinny(plan, pi, M, N, K, A, B, sfa, sfb, alpha, D, epi, stream, ds);
 
     GemmMaps maps;
     std::memset(&maps, 0, sizeof maps);
@@ -256,7 +278,7 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
                         128, 128)) != BSG_OK ||
         (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, (uint64_t)N, row_bytes,
                         128, (uint32_t)(pi.bn / pi.cta_group))) != BSG_OK ||
-        (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)M,
+        (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, d_rows(M, epi),
                         (uint64_t)N * 2u, 64, 32)) != BSG_OK)
         return rc;
     if (pi.cta_group == 2 && kind == Kind::NVFP4) {
@@ -291,6 +313,7 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     a.sB = sB;
     a.status = ds->status;
     a.timeout_ns = g_watchdog_ns.load();
+    set_epilogue(a, epi, D);
     const long long ctas = (long long)a.num_m_tiles * a.num_n_tiles * pi.cta_group;
     const int resident = bsg::max_resident_ctas(plan, ds->sms);
     if (resident < pi.cta_group)
@@ -311,6 +334,31 @@ int check_nvfp4_args(int M, int N, int K, const void *A, const void *sfA, const 
     if (M < 1 || N < 1 || K < 256 || (K % 256) != 0 || (N % 8) != 0)
         return BSG_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(sfA) || !aligned16(B) || !aligned16(sfB) || !aligned16(D))
+        return BSG_ERR_MISALIGNED;
+    return BSG_OK;
+}
+
+int check_fp8_args(int M, int N, int K, const void *A, const float *sA, const void *B, const float *sB,
+                   void *D)
+{
+    if (!A || !B || !D)
+        return BSG_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 128 || (K % 128) != 0 || (N % 8) != 0)
+        return BSG_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) ||
+        (sA && (reinterpret_cast<uintptr_t>(sA) & 3u)) || (sB && (reinterpret_cast<uintptr_t>(sB) & 3u)))
+        return BSG_ERR_MISALIGNED;
+    return BSG_OK;
+}
+
+// bias 16-byte aligned (read as float4), gamma and scatter 4-byte aligned;
+// m_out == M without scatter, >= 1 with it.
+int check_epilogue_args(int M, const float *bias, const float *gamma, const int32_t *scatter, int m_out)
+{
+    if (scatter ? m_out < 1 : m_out != M)
+        return BSG_ERR_INVALID_ARG;
+    if ((bias && !aligned16(bias)) || (gamma && (reinterpret_cast<uintptr_t>(gamma) & 3u)) ||
+        (scatter && (reinterpret_cast<uintptr_t>(scatter) & 3u)))
         return BSG_ERR_MISALIGNED;
     return BSG_OK;
 }
@@ -473,19 +521,56 @@ int fp8_gemm(int M, int N, int K, const void *A, const float *sA, const void *B,
              float alpha, void *D, bsg_stream_t stream)
 {
     t_last_launches = 0;
-    if (!A || !B || !D)
-        return BSG_ERR_INVALID_ARG;
-    if (M < 1 || N < 1 || K < 128 || (K % 128) != 0 || (N % 8) != 0)
-        return BSG_ERR_INVALID_ARG;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(D) ||
-        (sA && (reinterpret_cast<uintptr_t>(sA) & 3u)) || (sB && (reinterpret_cast<uintptr_t>(sB) & 3u)))
-        return BSG_ERR_MISALIGNED;
+    int rc = check_fp8_args(M, N, K, A, sA, B, sB, D);
+    if (rc != BSG_OK)
+        return rc;
     DeviceState *ds = nullptr;
-    int rc = current_device(&ds);
+    rc = current_device(&ds);
     if (rc != BSG_OK)
         return rc;
     return run_gemm(Kind::FP8, M, N, K, A, B, nullptr, nullptr, sA, sB, alpha, D,
                     reinterpret_cast<cudaStream_t>(stream), ds);
+}
+
+int nvfp4_gemm_ex(int M, int N, int K, const void *A, const void *sfA_swz, const void *B,
+                  const void *sfB_swz, float alpha, const float *bias, const float *gamma,
+                  const int32_t *scatter, int m_out, void *D, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    int rc = check_nvfp4_args(M, N, K, A, sfA_swz, B, sfB_swz, D);
+    if (rc != BSG_OK || (rc = check_epilogue_args(M, bias, gamma, scatter, m_out)) != BSG_OK)
+        return rc;
+    DeviceState *ds = nullptr;
+    if ((rc = current_device(&ds)) != BSG_OK)
+        return rc;
+    Epilogue e;
+    e.bias = bias;
+    e.gamma = gamma;
+    e.scatter = scatter;
+    e.m_out = m_out;
+    return run_gemm(Kind::NVFP4, M, N, K, A, B, static_cast<const uint8_t *>(sfA_swz),
+                    static_cast<const uint8_t *>(sfB_swz), nullptr, nullptr, alpha, D,
+                    reinterpret_cast<cudaStream_t>(stream), ds, e);
+}
+
+int fp8_gemm_ex(int M, int N, int K, const void *A, const float *sA, const void *B, const float *sB,
+                float alpha, const float *bias, const float *gamma, const int32_t *scatter, int m_out,
+                void *D, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    int rc = check_fp8_args(M, N, K, A, sA, B, sB, D);
+    if (rc != BSG_OK || (rc = check_epilogue_args(M, bias, gamma, scatter, m_out)) != BSG_OK)
+        return rc;
+    DeviceState *ds = nullptr;
+    if ((rc = current_device(&ds)) != BSG_OK)
+        return rc;
+    Epilogue e;
+    e.bias = bias;
+    e.gamma = gamma;
+    e.scatter = scatter;
+    e.m_out = m_out;
+    return run_gemm(Kind::FP8, M, N, K, A, B, nullptr, nullptr, sA, sB, alpha, D,
+                    reinterpret_cast<cudaStream_t>(stream), ds, e);
 }
 
 int bsg_reserve_workspace(int device, size_t bytes)

@@ -30,7 +30,17 @@ struct GemmArgs {
     const float *sB;
     unsigned int *status;      // device status word
     unsigned long long timeout_ns;
+    // Fused epilogue variants, read only by the kernels instantiated with
+    // EPI = true: D[dst(m)][n] = bf16(gamma[m] * (alpha * acc[m][n] + bias[n]))
+    const float *bias;         // [N] FP32 added to every row, or null
+    const float *gamma;        // [M] FP32 per-row multiplier, or null
+    const int *scatter;        // [M] row of D that computed row m goes to, or null
+    uint16_t *d;               // D (BF16 bits, row pitch N) for the scattered stores
+    int m_out;                 // rows of D when scattered
 };
+
+// True when a call needs the epilogue-variant kernels.
+inline bool has_epilogue(const GemmArgs &a) { return a.bias || a.gamma || a.scatter; }
 
 // One compiled persistent-kernel configuration.
 struct PlanInfo {

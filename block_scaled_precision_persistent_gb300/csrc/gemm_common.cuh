@@ -56,6 +56,88 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// ---------------------------------------------------------------------------
+// Epilogue variants ("Triton #11171 - Why Two New NVFP4 Test Cases Produced
+// Twelve Tensor-Memory Failures", sections on scatter, gamma and the shared
+// bias route): D[dst(m)][n] = bf16(gamma[m] * (alpha * acc[m][n] + bias[n])).
+// ---------------------------------------------------------------------------
+
+// Per-row operands of computed row `row`: gamma (1 without one) and the row
+// of D it is written to (-1: none -- a row past M, or a scatter index
+// outside [0, m_out)).
+struct RowEpi {
+    float gamma;
+    int dst;
+};
+
+__device__ __forceinline__ RowEpi load_row_epi(const GemmArgs &a, int row)
+{
+    RowEpi e{1.0f, -1};
+    if (row < a.M) {
+        if (a.gamma)
+            e.gamma = __ldg(a.gamma + row);
+        e.dst = row;
+        if (a.scatter) {
+            const int d = __ldg(a.scatter + row);
+            e.dst = (d >= 0 && d < a.m_out) ? d : -1;
+        }
+    }
+    return e;
+}
+
+// Bias of output column n (-0 without one, or past N: adding -0 changes
+// nothing) and gamma of output row m (1 without one, or past M).
+__device__ __forceinline__ float epi_bias(const GemmArgs &a, int n)
+{
+    return (a.bias && n < a.N) ? __ldg(a.bias + n) : -0.0f;
+}
+
+__device__ __forceinline__ float epi_gamma(const GemmArgs &a, int m)
+{
+    return (a.gamma && m < a.M) ? __ldg(a.gamma + m) : 1.0f;
+}
+
+// 32 accumulator columns [col, col + 32) of one row -> 16 BF16 pairs:
+// bf16(fma(acc, scale, bias[c]) * g). A missing bias adds -0, which leaves
+// every product unchanged (the sign of a zero included); columns past N take
+// no bias (they are never stored). bias + col is 16-byte aligned (bias is,
+// and col is a multiple of 32); every lane reads the same 128 bytes.
+__device__ __forceinline__ void convert32_epi(const uint32_t (&v)[32], uint32_t *pk, float scale, float g,
+                                              const float *bias, int col, int N)
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float4 b = make_float4(-0.0f, -0.0f, -0.0f, -0.0f);
+        if (bias && col + 4 * j < N)
+            b = __ldg(reinterpret_cast<const float4 *>(bias + col) + j);
+        pk[2 * j] = pack_bf16x2(fmaf(__uint_as_float(v[4 * j]), scale, b.x) * g,
+                                fmaf(__uint_as_float(v[4 * j + 1]), scale, b.y) * g);
+        pk[2 * j + 1] = pack_bf16x2(fmaf(__uint_as_float(v[4 * j + 2]), scale, b.z) * g,
+                                    fmaf(__uint_as_float(v[4 * j + 3]), scale, b.w) * g);
+    }
+}
+
+// Scattered store of a warp's 32-row x 64-column BF16 chunk, staged with the
+// 128-byte swizzle (row r's 16-byte piece c at r * 128 + ((c ^ (r % 8)) * 16)
+// of sbuf) for columns [x, x + 64) of D. Four rows per step: each group of
+// eight lanes reads one row's 128 bytes (conflict-free) and writes them to
+// row dst(r) of D, so every group's store is one contiguous 128-byte run.
+// `dst` is the calling lane's own row destination (-1: not written). Columns
+// at or past N are skipped 8 at a time (N % 8 == 0).
+__device__ __forceinline__ void scatter_chunk(const uint8_t *sbuf, int dst, uint16_t *D, int N, int x, int lane)
+{
+    const int c = lane & 7;
+    const int col = x + 8 * c;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int r = 4 * it + (lane >> 3);
+        const int d = __shfl_sync(0xffffffffu, dst, r);
+        const uint4 val = *reinterpret_cast<const uint4 *>(sbuf + r * 128 + ((c ^ (r & 7)) << 4));
+        if (d >= 0 && col < N)
+            *reinterpret_cast<uint4 *>(D + (size_t)d * (size_t)N + (size_t)col) = val;
+    }
+}
+
 // Writes one ring stage's NVFP4 block scales from shared memory into the
 // calling warp's TMEM sub-partition (taddr carries the warp's lane base).
 // The layout is the one the tensor core reads for a 128-row operand with one

@@ -85,7 +85,8 @@ struct PairTile {
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
 };
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+// EPI: the epilogue-variant instantiation (bias, gamma, scattered rows).
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool EPI>
 __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
@@ -338,21 +339,30 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
         for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
             int pm, nt;
             raster_tile(tile, args, pm, nt);
+            RowEpi re{1.0f, -1};
+            if constexpr (EPI)
+                re = load_row_epi(args, pm * T::TILE_M + (int)rank * T::BM + q * 32 + lane);
             if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
                 break;
             tc_fence_after_sync();
             const uint32_t t_acc = tmem + lane_off + (uint32_t)(acc * BN + h * COLS_PER_WARP);
-            // 64 TMEM columns -> alpha -> BF16 pairs
+            const int x0 = nt * BN + h * COLS_PER_WARP;            // first column of this warp
+            // 64 TMEM columns -> alpha (bias, gamma) -> BF16 pairs
             auto drain = [&](int ch, uint32_t (&pk)[32]) {
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS + 32 * half, v);
                     tmem_ld_wait();
+                    if constexpr (EPI) {
+                        convert32_epi(v, pk + 16 * half, scale, re.gamma, args.bias,
+                                      x0 + ch * T::EPI_COLS + 32 * half, args.N);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[16 * half + i] =
-                            pack_bf16x2(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
+                        for (int i = 0; i < 16; ++i)
+                            pk[16 * half + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * scale,
+                                                            __uint_as_float(v[2 * i + 1]) * scale);
+                    }
                 }
             };
             // one 64-column chunk from registers into a 128B-swizzled staging
@@ -374,8 +384,10 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                 __syncwarp();
             };
             auto store_chunk = [&](int ch, uint32_t sbuf) {
-                if (lane == 0) {
-                    const int x = nt * BN + h * COLS_PER_WARP + ch * T::EPI_COLS;
+                const int x = x0 + ch * T::EPI_COLS;
+                if (EPI && args.scatter) {
+                    scatter_chunk(gbase + (sbuf - base), re.dst, args.d, args.N, x, lane);
+                } else if (lane == 0) {
                     const int y = pm * T::TILE_M + (int)rank * T::BM + q * 32;
                     if (x < args.N && y < args.M)
                         tma_store_2d(&tmD, sbuf, x, y);
@@ -448,7 +460,8 @@ static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, 
                                     cudaStream_t stream)
 {
     using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
-    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC>;
+    auto kern = has_epilogue(args) ? gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, true>
+                                   : gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_BYTES);
     if (e != cudaSuccess)
@@ -475,7 +488,7 @@ template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 static int pair_clusters_impl()
 {
     using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
-    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC>;
+    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, false>;   // the EPI instantiation has the same footprint
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) !=
         cudaSuccess)
         return 0;

@@ -77,7 +77,8 @@ struct Tile {
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
 };
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+// EPI: the epilogue-variant instantiation (bias, gamma, scattered rows).
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool EPI>
 __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -317,6 +318,9 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int mt, nt;
             raster_tile(tile, args, mt, nt);
+            RowEpi re{1.0f, -1};
+            if constexpr (EPI)
+                re = load_row_epi(args, mt * T::BM + q * 32 + lane);
             if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
                 break;
             tc_fence_after_sync();
@@ -340,29 +344,44 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                 __syncwarp();
                 const uint32_t sbuf = ebuf + (uint32_t)buf * T::EPI_BUF_BYTES;
                 const uint32_t row = sbuf + (uint32_t)lane * 128u;
+                const int x = nt * BN + ch * T::EPI_COLS;
                 // 128-byte swizzle: 16-byte chunk c of row r lands at chunk c ^ (r % 8)
+                if constexpr (EPI) {
+                    uint32_t pk[32];
+                    convert32_epi(v0, pk, scale, re.gamma, args.bias, x, args.N);
+                    convert32_epi(v1, pk + 16, scale, re.gamma, args.bias, x + 32, args.N);
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    st_shared_v4(row + ((uint32_t)(c ^ (lane & 7)) << 4),
-                                 pack_bf16x2(__uint_as_float(v0[8 * c + 0]) * scale, __uint_as_float(v0[8 * c + 1]) * scale),
-                                 pack_bf16x2(__uint_as_float(v0[8 * c + 2]) * scale, __uint_as_float(v0[8 * c + 3]) * scale),
-                                 pack_bf16x2(__uint_as_float(v0[8 * c + 4]) * scale, __uint_as_float(v0[8 * c + 5]) * scale),
-                                 pack_bf16x2(__uint_as_float(v0[8 * c + 6]) * scale, __uint_as_float(v0[8 * c + 7]) * scale));
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(row + ((uint32_t)(c ^ (lane & 7)) << 4), pk[4 * c], pk[4 * c + 1],
+                                     pk[4 * c + 2], pk[4 * c + 3]);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    st_shared_v4(row + ((uint32_t)((c + 4) ^ (lane & 7)) << 4),
-                                 pack_bf16x2(__uint_as_float(v1[8 * c + 0]) * scale, __uint_as_float(v1[8 * c + 1]) * scale),
-                                 pack_bf16x2(__uint_as_float(v1[8 * c + 2]) * scale, __uint_as_float(v1[8 * c + 3]) * scale),
-                                 pack_bf16x2(__uint_as_float(v1[8 * c + 4]) * scale, __uint_as_float(v1[8 * c + 5]) * scale),
-                                 pack_bf16x2(__uint_as_float(v1[8 * c + 6]) * scale, __uint_as_float(v1[8 * c + 7]) * scale));
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int x = nt * BN + ch * T::EPI_COLS;
-                    const int y = mt * T::BM + q * 32;
-                    if (x < args.N && y < args.M)
-                        tma_store_2d(&tmD, sbuf, x, y);
-                    bulk_commit_group();
+                    for (int c = 0; c < 4; ++c)
+                        st_shared_v4(row + ((uint32_t)(c ^ (lane & 7)) << 4),
+                                     pack_bf16x2(__uint_as_float(v0[8 * c + 0]) * scale, __uint_as_float(v0[8 * c + 1]) * scale),
+                                     pack_bf16x2(__uint_as_float(v0[8 * c + 2]) * scale, __uint_as_float(v0[8 * c + 3]) * scale),
+                                     pack_bf16x2(__uint_as_float(v0[8 * c + 4]) * scale, __uint_as_float(v0[8 * c + 5]) * scale),
+                                     pack_bf16x2(__uint_as_float(v0[8 * c + 6]) * scale, __uint_as_float(v0[8 * c + 7]) * scale));
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        st_shared_v4(row + ((uint32_t)((c + 4) ^ (lane & 7)) << 4),
+                                     pack_bf16x2(__uint_as_float(v1[8 * c + 0]) * scale, __uint_as_float(v1[8 * c + 1]) * scale),
+                                     pack_bf16x2(__uint_as_float(v1[8 * c + 2]) * scale, __uint_as_float(v1[8 * c + 3]) * scale),
+                                     pack_bf16x2(__uint_as_float(v1[8 * c + 4]) * scale, __uint_as_float(v1[8 * c + 5]) * scale),
+                                     pack_bf16x2(__uint_as_float(v1[8 * c + 6]) * scale, __uint_as_float(v1[8 * c + 7]) * scale));
+                }
+                if (EPI && args.scatter) {
+                    __syncwarp();
+                    scatter_chunk(gbase + (sbuf - base), re.dst, args.d, args.N, x, lane);
+                } else {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int y = mt * T::BM + q * 32;
+                        if (x < args.N && y < args.M)
+                            tma_store_2d(&tmD, sbuf, x, y);
+                        bulk_commit_group();
+                    }
                 }
                 buf ^= 1;
             }
@@ -396,7 +415,8 @@ static cudaError_t launch_impl(const GemmMaps &maps, const GemmArgs &args, int g
                                cudaStream_t stream)
 {
     using T = Tile<KIND, BN, STAGES, NUM_ACC>;
-    auto kern = gemm_persistent_kernel<KIND, BN, STAGES, NUM_ACC>;
+    auto kern = has_epilogue(args) ? gemm_persistent_kernel<KIND, BN, STAGES, NUM_ACC, true>
+                                   : gemm_persistent_kernel<KIND, BN, STAGES, NUM_ACC, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_BYTES);
     if (e != cudaSuccess)

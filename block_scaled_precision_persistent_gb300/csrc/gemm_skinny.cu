@@ -98,10 +98,11 @@ struct SkinnyTile {
 // The owned block's reduction, spread over the epilogue's threads: item
 // (cq, r) sums columns [4 cq, 4 cq + 4) of owned row r over the S partials in
 // the receive area, in rank order, scales them and stages them as BF16
-// [m][r] (row stride rpo) for the TMA store.
-template <int S>
+// [m][r] (row stride rpo) for the store. EPI: owned row r is output column
+// n0 + r (its bias), column m output row m (its gamma).
+template <int S, bool EPI>
 __device__ __forceinline__ void reduce_owned(const uint8_t *recv, __nv_bfloat16 *out, int rpo, int live_cols,
-                                             float alpha, int t, int nthreads)
+                                             float alpha, int t, int nthreads, const GemmArgs &args, int n0)
 {
     const int items = (live_cols / 4) * rpo;
     const int slot_bytes = rpo * live_cols * 4;
@@ -121,14 +122,23 @@ __device__ __forceinline__ void reduce_owned(const uint8_t *recv, __nv_bfloat16 
         }
         const int r = idx % rpo;
         const int m0 = (idx / rpo) * 4;
-        out[(m0 + 0) * rpo + r] = __float2bfloat16_rn(a.x * alpha);
-        out[(m0 + 1) * rpo + r] = __float2bfloat16_rn(a.y * alpha);
-        out[(m0 + 2) * rpo + r] = __float2bfloat16_rn(a.z * alpha);
-        out[(m0 + 3) * rpo + r] = __float2bfloat16_rn(a.w * alpha);
+        if constexpr (EPI) {
+            const float b = epi_bias(args, n0 + r);
+            out[(m0 + 0) * rpo + r] = __float2bfloat16_rn(fmaf(a.x, alpha, b) * epi_gamma(args, m0 + 0));
+            out[(m0 + 1) * rpo + r] = __float2bfloat16_rn(fmaf(a.y, alpha, b) * epi_gamma(args, m0 + 1));
+            out[(m0 + 2) * rpo + r] = __float2bfloat16_rn(fmaf(a.z, alpha, b) * epi_gamma(args, m0 + 2));
+            out[(m0 + 3) * rpo + r] = __float2bfloat16_rn(fmaf(a.w, alpha, b) * epi_gamma(args, m0 + 3));
+        } else {
+            out[(m0 + 0) * rpo + r] = __float2bfloat16_rn(a.x * alpha);
+            out[(m0 + 1) * rpo + r] = __float2bfloat16_rn(a.y * alpha);
+            out[(m0 + 2) * rpo + r] = __float2bfloat16_rn(a.z * alpha);
+            out[(m0 + 3) * rpo + r] = __float2bfloat16_rn(a.w * alpha);
+        }
     }
 }
 
-template <int M_PAD, int STAGES>
+// EPI: the epilogue-variant instantiation (bias, gamma, scattered rows).
+template <int M_PAD, int STAGES, bool EPI>
 __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
                                   SkinnyTile<M_PAD, STAGES>::CTAS_PER_SM)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -312,14 +322,20 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
             tc_fence_after_sync();
         if (S == 1) {
             if (have) {
+                const float b = EPI ? epi_bias(args, nt * T::BW + n) : 0.0f;
 #pragma unroll 1
                 for (int c0 = 0; c0 < live_cols; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tmem + lane_off + (uint32_t)c0, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        out[(c0 + i) * T::BW + n] = __float2bfloat16_rn(__uint_as_float(v[i]) * alpha);
+                    for (int i = 0; i < 32; ++i) {
+                        if constexpr (EPI)
+                            out[(c0 + i) * T::BW + n] = __float2bfloat16_rn(
+                                fmaf(__uint_as_float(v[i]), alpha, b) * epi_gamma(args, c0 + i));
+                        else
+                            out[(c0 + i) * T::BW + n] = __float2bfloat16_rn(__uint_as_float(v[i]) * alpha);
+                    }
                 }
             }
         } else {
@@ -363,21 +379,39 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
             const bool rows_in = warp_wait(rx, 0, wd, abort_flag, 8, lane);
             named_bar_sync(1, 32 * T::EPI_WARPS);        // the owned rows' local writes
             if (have && rows_in) {
+                const int n0 = nt * T::BW + own_lo;
                 switch (S) {
-                case 2: reduce_owned<2>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS); break;
-                case 4: reduce_owned<4>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS); break;
-                default: reduce_owned<8>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS); break;
+                case 2: reduce_owned<2, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, args, n0); break;
+                case 4: reduce_owned<4, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, args, n0); break;
+                default: reduce_owned<8, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, args, n0); break;
                 }
             }
         }
-        // one TMA store of this CTA's [M x 128/S] block of D (rows >= M and
-        // columns >= N are clipped by the tensor map)
-        fence_proxy_async_smem();
-        named_bar_sync(1, 32 * T::EPI_WARPS);
-        if (warp == T::EPI_WARP0 && lane == 0) {
-            tma_store_2d(&tmD, smem_u32(out), nt * T::BW + own_lo, 0);
-            bulk_commit_group();
-            bulk_wait_group_read<0>();   // the staging must outlive the read
+        if (EPI && args.scatter) {
+            // scattered rows: staged row m (128/S BF16) to row scatter[m] of
+            // D, in 16-byte pieces; consecutive threads take consecutive
+            // pieces of one row
+            named_bar_sync(1, 32 * T::EPI_WARPS);
+            const int pieces = rpo / 8;
+            const int col0 = nt * T::BW + own_lo;
+            for (int p = et; p < args.M * pieces; p += 32 * T::EPI_WARPS) {
+                const int m = p / pieces;
+                const int col = col0 + 8 * (p - m * pieces);
+                const int d = __ldg(args.scatter + m);
+                if (d >= 0 && d < args.m_out && col < args.N)
+                    *reinterpret_cast<uint4 *>(args.d + (size_t)d * (size_t)args.N + (size_t)col) =
+                        *reinterpret_cast<const uint4 *>(out + m * rpo + (col - col0));
+            }
+        } else {
+            // one TMA store of this CTA's [M x 128/S] block of D (rows >= M
+            // and columns >= N are clipped by the tensor map)
+            fence_proxy_async_smem();
+            named_bar_sync(1, 32 * T::EPI_WARPS);
+            if (warp == T::EPI_WARP0 && lane == 0) {
+                tma_store_2d(&tmD, smem_u32(out), nt * T::BW + own_lo, 0);
+                bulk_commit_group();
+                bulk_wait_group_read<0>();   // the staging must outlive the read
+            }
         }
     }
 
@@ -398,7 +432,7 @@ static cudaError_t skinny_launch_impl(const GemmMaps &maps, const GemmArgs &args
                                       cudaStream_t stream)
 {
     using T = SkinnyTile<M_PAD, STAGES>;
-    auto kern = gemm_skinny_kernel<M_PAD, STAGES>;
+    auto kern = has_epilogue(args) ? gemm_skinny_kernel<M_PAD, STAGES, true> : gemm_skinny_kernel<M_PAD, STAGES, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_BYTES);
     if (e == cudaSuccess)
@@ -428,7 +462,7 @@ template <int M_PAD, int STAGES>
 static int skinny_clusters_impl(int splits)
 {
     using T = SkinnyTile<M_PAD, STAGES>;
-    auto kern = gemm_skinny_kernel<M_PAD, STAGES>;
+    auto kern = gemm_skinny_kernel<M_PAD, STAGES, false>;   // the EPI instantiation has the same footprint
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

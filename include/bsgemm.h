@@ -168,6 +168,45 @@ BSG_API int fp8_gemm(int M, int N, int K,
              float alpha, void *D, bsg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Fused epilogue variants: shared bias, per-row gamma, scattered output rows
+ * ("Triton #11171 - Why Two New NVFP4 Test Cases Produced Twelve
+ * Tensor-Memory Failures", sections "Scatter changes where output rows are
+ * written", "Gamma adds a per-row scaling input" and "The ordinary variants
+ * also exercise the shared bias route": the NVFP4 x dense matmul plus bias,
+ * optional gamma, optional scatter). Reading of the order (the pages list
+ * the steps, not a formula):
+ *     D[dst(m)][n] = bf16_rn( gamma[m] * (alpha * acc[m][n] + bias[n]) )
+ * computed in FP32 in the GEMM's epilogue (one FMA, one multiply, one
+ * rounding to BF16); acc as for nvfp4_gemm_swizzled / fp8_gemm (for FP8,
+ * alpha stands for alpha * sA * sB).
+ *   bias    : DEVICE float[N], 16-byte aligned, or NULL (no bias)
+ *   gamma   : DEVICE float[M], 4-byte aligned, or NULL (gamma = 1)
+ *   scatter : DEVICE int32[M], 4-byte aligned, or NULL (dst(m) = m). Computed
+ *             row m is written to row scatter[m] of D; an index outside
+ *             [0, m_out) -- e.g. -1 for a padding row -- writes nothing.
+ *             Indices must be distinct (two rows sent to one destination:
+ *             which one lands is unspecified). Rows of D that no index
+ *             names are left as they were.
+ *   m_out   : rows of D (D is bf16[m_out][N], row pitch N, 16-byte aligned).
+ *             Without scatter m_out must equal M; with it m_out >= 1.
+ * Other arguments, layouts and errors as nvfp4_gemm_swizzled / fp8_gemm;
+ * allocates nothing. With bias, gamma and scatter all NULL the call is
+ * exactly nvfp4_gemm_swizzled / fp8_gemm. Only the scatter indices are
+ * range-checked (on the GPU, per row); the caller guarantees the lengths.
+ * ------------------------------------------------------------------------- */
+BSG_API int nvfp4_gemm_ex(int M, int N, int K,
+                          const void *A, const void *sfA_swz,
+                          const void *B, const void *sfB_swz,
+                          float alpha, const float *bias, const float *gamma,
+                          const int32_t *scatter, int m_out, void *D, bsg_stream_t stream);
+
+BSG_API int fp8_gemm_ex(int M, int N, int K,
+                        const void *A, const float *sA,
+                        const void *B, const float *sB,
+                        float alpha, const float *bias, const float *gamma,
+                        const int32_t *scatter, int m_out, void *D, bsg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Runtime control
  * ------------------------------------------------------------------------- */
 

@@ -157,3 +157,24 @@ def test_quantize_bad_args(lib):
     assert q(8, 256, BAD, BAD + 8, BAD, None, BAD, None) == bsg.BSG_ERR_MISALIGNED       # packed
     assert q(8, 256, BAD, BAD, BAD + 4, None, BAD, None) == bsg.BSG_ERR_MISALIGNED       # sf_swz
     assert q(8, 256, BAD, BAD, BAD, None, BAD + 4, None) == bsg.BSG_ERR_MISALIGNED       # global
+
+
+def test_epilogue_bad_args(lib):
+    """nvfp4_gemm_ex / fp8_gemm_ex: operand checks as the plain calls, then
+    m_out == M without scatter (>= 1 with it), bias 16-byte and gamma /
+    scatter 4-byte alignment; all rejected before any launch."""
+    nv = lambda *e: lib.nvfp4_gemm_ex(128, 64, 256, BAD, BAD, BAD, BAD, 1.0, *e, BAD, None)  # noqa: E731
+    f8 = lambda *e: lib.fp8_gemm_ex(128, 64, 128, BAD, None, BAD, None, 1.0, *e, BAD, None)  # noqa: E731
+    for fn in (nv, f8):
+        assert fn(None, None, None, 100) == bsg.BSG_ERR_INVALID_ARG            # m_out != M
+        assert fn(BAD, None, None, 127) == bsg.BSG_ERR_INVALID_ARG
+        assert fn(None, None, BAD, 0) == bsg.BSG_ERR_INVALID_ARG               # scatter, no rows
+        assert fn(BAD + 4, None, None, 128) == bsg.BSG_ERR_MISALIGNED          # bias
+        assert fn(None, BAD + 2, None, 128) == bsg.BSG_ERR_MISALIGNED          # gamma
+        assert fn(None, None, BAD + 1, 7) == bsg.BSG_ERR_MISALIGNED            # scatter
+    assert lib.nvfp4_gemm_ex(128, 64, 300, BAD, BAD, BAD, BAD, 1.0, None, None, None, 128, BAD, None) == \
+        bsg.BSG_ERR_INVALID_ARG
+    assert lib.fp8_gemm_ex(128, 64, 128, BAD, BAD + 1, BAD, None, 1.0, None, None, None, 128, BAD, None) == \
+        bsg.BSG_ERR_MISALIGNED
+    assert lib.nvfp4_gemm_ex(128, 64, 256, BAD, BAD, BAD, BAD, 1.0, None, None, None, 128, None, None) == \
+        bsg.BSG_ERR_INVALID_ARG                                                # no D

@@ -202,3 +202,27 @@ def make_fp8(w: Workload, device="cpu", M: int | None = None, N: int | None = No
         scales.append(s)
     out["alpha"] = float((scales[0] * scales[1]).float())
     return out
+
+
+def make_epilogue(M: int, N: int, seed: int, m_out: int | None = None, drop: float = 0.0,
+                  bias_std: float = 1.0, device="cpu") -> dict:
+    """Inputs of the GEMM epilogue variants ("Triton #11171 - Why Two New
+    NVFP4 Test Cases Produced Twelve Tensor-Memory Failures", the scatter,
+    gamma and shared-bias sections; the pages give no distributions):
+
+      bias    float32[N] ~ N(0, bias_std^2)
+      gamma   float32[M] ~ N(1, 0.5^2)  (mostly positive, some negative)
+      scatter int32[M]: a random injective map of the computed rows into
+              [0, m_out) (m_out >= M, default M: a random permutation), a
+              fraction ``drop`` of its entries then set to -1 (not written)
+    """
+    m_out = M if m_out is None else m_out
+    if m_out < M:
+        raise ValueError("an injective scatter needs m_out >= M")
+    g = _gen(SEED_BASE + 7919 * seed + 31 * M + N, "cpu")
+    bias = (torch.randn(N, generator=g, dtype=torch.float32) * bias_std).contiguous()
+    gamma = (1.0 + 0.5 * torch.randn(M, generator=g, dtype=torch.float32)).contiguous()
+    scatter = torch.randperm(m_out, generator=g)[:M].to(torch.int32)
+    if drop > 0:
+        scatter[torch.rand(M, generator=g) < drop] = -1
+    return {k: v.to(device) for k, v in dict(bias=bias, gamma=gamma, scatter=scatter).items()}
