@@ -9,8 +9,9 @@ sweep shape), inputs resident in HBM, larger than L2.
 Prints ONE JSON line (rank 0). Besides the contract's keys it carries the
 dominant kernel's roofline (CUDA-event duration of the GEMM launches inside
 the timed region), the CPU oracle timed on a bounded sample, the clocks seen
-during the timed region, and secondary lines for the FP8 8192^3 GEMM and the
-skinny-M sweep (HBM GB/s).
+during the timed region, and secondary lines for the FP8 8192^3 GEMM, the
+skinny-M sweep (HBM GB/s), the scale swizzle, the NVFP4 quantiser and the
+fused epilogue variants (bias, gamma, scattered rows).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -355,6 +356,93 @@ def secondary_quantize(dev, steps: int, pk: dict, psrc: str) -> dict:
             "launches": 2, "timing": "median per-call CUDA events (memset + 2 kernels), X > L2"}
 
 
+def graph_us(calls: dict, launches: int, replays: int) -> dict:
+    """Per-launch device time of each call in `calls` (name -> callable): one
+    CUDA graph of `launches` back-to-back calls per name (captured after
+    three warm calls on a side stream), the graphs then replayed in turn,
+    round after round, so that clock or power drift falls on every variant
+    alike; median over `replays` rounds of replay time / launches. Keeps the
+    host's per-call cost (tensor-map encoding, launch) out of the number."""
+    side = torch.cuda.Stream()
+    graphs = {}
+    for name, call in calls.items():
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(launches):
+                call()
+        g.replay()
+        torch.cuda.synchronize()
+        graphs[name] = g
+    ts = {name: [] for name in calls}
+    for _ in range(replays):
+        for name, g in graphs.items():
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record()
+            g.replay()
+            t1.record()
+            torch.cuda.synchronize()
+            ts[name].append(t0.elapsed_time(t1) * 1e3 / launches)
+    del graphs
+    return {name: statistics.median(v) for name, v in ts.items()}
+
+
+def secondary_epilogue(dev, step: Nvfp4Step, steps: int, pk: dict, psrc: str) -> dict:
+    """The NVFP4 GEMM with the fused epilogue variants (nvfp4_gemm_ex): the
+    plain call, bias + gamma, and bias + gamma + a scatter permutation of
+    the rows, on the same resident operands: 16384^3 (the headline step's
+    buffers, larger than L2), 4096^3, and the 64 x 3072 x 3072 skinny cell
+    (weights L2-resident). Timed as CUDA graphs of back-to-back launches
+    (graph_us); vs_plain = plain time / variant time."""
+    import block_scaled_precision_persistent_gb300 as bsg
+    step()                                     # swizzled scales of the step are current
+    torch.cuda.synchronize()
+    keep = []
+
+    def problem(name):
+        w = workloads.WORKLOADS[name]
+        p = workloads.make_nvfp4(w, dev)
+        sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(w.M, w.K), dtype=torch.uint8, device=dev)
+        sb = torch.empty(bsg.nvfp4_swizzled_scale_bytes(w.N, w.K), dtype=torch.uint8, device=dev)
+        bsg.nvfp4_swizzle_scales(w.M, w.K, p["sfA"], sa)
+        bsg.nvfp4_swizzle_scales(w.N, w.K, p["sfB"], sb)
+        D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+        keep.append((p, sa, sb, D))
+        return (w.M, w.N, w.K, p["A"], sa, p["B"], sb, p["alpha"], D, w.std)
+
+    shapes = {
+        "nvfp4_16384": ((step.w.M, step.w.N, step.w.K, step.A, step.swA, step.B, step.swB, step.alpha,
+                         step.D, step.w.std), 4),
+        "nvfp4_4096": (problem("nvfp4_4096"), 32),
+        "nvfp4_skinny_m64_n3072_k3072": (problem("nvfp4_skinny_m64_n3072_k3072"), 32),
+    }
+    out = {}
+    for wname, ((M, N, K, A, sa, B, sb, alpha, D, std), launches) in shapes.items():
+        e = workloads.make_epilogue(M, N, seed=3, bias_std=float(K) ** 0.5 * std * std, device=dev)
+        variants = {"plain": (None, None, None), "bias": (e["bias"], None, None), "gamma": (None, e["gamma"], None),
+                    "bias_gamma": (e["bias"], e["gamma"], None),
+                    "bias_gamma_scatter": (e["bias"], e["gamma"], e["scatter"])}
+        calls = {v: (lambda b=b, g=g, sc=sc: bsg.nvfp4_gemm_ex(M, N, K, A, sa, B, sb, alpha, b, g, sc, M, D))
+                 for v, (b, g, sc) in variants.items()}
+        times = graph_us(calls, launches, steps)
+        cells = {v: {"us": round(us, 3), "tflops": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1)}
+                 for v, us in times.items()}
+        for v in cells.values():
+            v["vs_plain"] = round(cells["plain"]["us"] / v["us"], 4)
+        out[wname] = dict(cells, plan=bsg.bsg_select_plan(0, M, N, K, 152), launches_per_graph=launches)
+    if bsg.bsg_get_device_status() != bsg.BSG_OK:
+        raise SystemExit("device status reported an error in the epilogue-variant timing")
+    del keep
+    peak = pk["bf16_tflops"] * FP4_PER_BF16
+    return {"shapes": out, "roofline_peak_tflops": peak, "peak_source": psrc,
+            "timing": "CUDA graph of back-to-back launches per variant, the variants' graphs replayed in "
+                      "turn, median over rounds of graph time / launches; "
+                      "operands resident (16384^3 larger than L2; 4096^3 and the skinny cell L2-resident)"}
+
+
 def secondary_swizzle(dev, steps: int, pk: dict, psrc: str) -> dict:
     """The scale-layout prep alone (timed separately from the GEMM): one
     operand's row-major [16384][1024] E4M3 scales into the swizzled layout;
@@ -455,6 +543,7 @@ def run_ours(args, dist: Dist) -> None:
         secondary["skinny"] = secondary_skinny(dev, 20, pk, psrc)
         secondary["swizzle"] = secondary_swizzle(dev, 20, pk, psrc)
         secondary["quantize"] = secondary_quantize(dev, 20, pk, psrc)
+        secondary["epilogue"] = secondary_epilogue(dev, step, 10, pk, psrc)
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, host_copy(step), args.cpu_seconds)
@@ -575,8 +664,12 @@ def run_case(args) -> None:
         bsg.nvfp4_swizzle_scales(M, K, p["sfA"], sa, s)
         bsg.nvfp4_swizzle_scales(N, K, p["sfB"], sb, s)
 
+        epi = set(args.epi.split(",")) if args.epi else set()
+        e = workloads.make_epilogue(M, N, seed=3, bias_std=float(K) ** 0.5, device=dev)
+        eb, eg, es = (e[k] if k in epi else None for k in ("bias", "gamma", "scatter"))
+
         def call():
-            bsg.nvfp4_gemm_swizzled(M, N, K, p["A"], sa, p["B"], sb, p["alpha"], D, s)
+            bsg.nvfp4_gemm_ex(M, N, K, p["A"], sa, p["B"], sb, p["alpha"], eb, eg, es, M, D, s)
     elif kind == "fp8":
         q = workloads.make_fp8(workloads.WORKLOADS["fp8_8192"], dev, M=M, N=N, K=K)
 
@@ -624,6 +717,8 @@ def main() -> None:
                     help="time one shape alone instead of the benchmark: nvfp4:MxNxK, fp8:MxNxK or "
                          "quantize:ROWSxK")
     ap.add_argument("--plan", default=None, help="with --case: force this plan")
+    ap.add_argument("--epi", default=None,
+                    help="with --case nvfp4: fused epilogue options, comma list of bias,gamma,scatter")
     args = ap.parse_args()
     if args.case:
         run_case(args)

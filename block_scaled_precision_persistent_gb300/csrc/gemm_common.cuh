@@ -97,23 +97,94 @@ __device__ __forceinline__ float epi_gamma(const GemmArgs &a, int m)
     return (a.gamma && m < a.M) ? __ldg(a.gamma + m) : 1.0f;
 }
 
-// 32 accumulator columns [col, col + 32) of one row -> 16 BF16 pairs:
-// bf16(fma(acc, scale, bias[c]) * g). A missing bias adds -0, which leaves
-// every product unchanged (the sign of a zero included); columns past N take
-// no bias (they are never stored). bias + col is 16-byte aligned (bias is,
-// and col is a multiple of 32); every lane reads the same 128 bytes.
-__device__ __forceinline__ void convert32_epi(const uint32_t (&v)[32], uint32_t *pk, float scale, float g,
-                                              const float *bias, int col, int N)
+// The bias of columns [x0, x0 + ncols) into L1, 64 bytes per lane, issued
+// before the accumulator wait: the epilogue's bias loads then hit L1 instead
+// of waiting on L2 between the TMEM read and the TMEM release.
+__device__ __forceinline__ void prefetch_bias(const GemmArgs &a, int x0, int ncols, int lane)
+{
+    const int c = x0 + 16 * lane;
+    if (a.bias && 16 * lane < ncols && c < a.N)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(a.bias + c));
+}
+
+// Bias of columns [col, col + 32) as 8 float4. bias + col is 16-byte
+// aligned (bias is, col is a multiple of 32); every lane reads the same 128
+// bytes. FULL: all 32 columns are below N (unconditional loads); otherwise
+// columns at or past N read as -0 (never stored).
+template <bool FULL>
+__device__ __forceinline__ void load_bias32(const float *bias, int col, int N, float4 (&b)[8])
+{
+    const float4 *p = reinterpret_cast<const float4 *>(bias + col);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (FULL || col + 4 * j < N)
+            b[j] = __ldg(p + j);
+        else
+            b[j] = make_float4(-0.0f, -0.0f, -0.0f, -0.0f);
+    }
+}
+
+// 32 accumulator columns of one row -> 16 BF16 pairs of
+// bf16(fma(acc, scale, bias[c]) * g), the multiply only with a gamma.
+template <bool GAMMA>
+__device__ __forceinline__ void convert32_bias(const uint32_t (&v)[32], uint32_t *pk, float scale, float g,
+                                               const float4 (&b)[8])
 {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        float4 b = make_float4(-0.0f, -0.0f, -0.0f, -0.0f);
-        if (bias && col + 4 * j < N)
-            b = __ldg(reinterpret_cast<const float4 *>(bias + col) + j);
-        pk[2 * j] = pack_bf16x2(fmaf(__uint_as_float(v[4 * j]), scale, b.x) * g,
-                                fmaf(__uint_as_float(v[4 * j + 1]), scale, b.y) * g);
-        pk[2 * j + 1] = pack_bf16x2(fmaf(__uint_as_float(v[4 * j + 2]), scale, b.z) * g,
-                                    fmaf(__uint_as_float(v[4 * j + 3]), scale, b.w) * g);
+        float x0 = fmaf(__uint_as_float(v[4 * j]), scale, b[j].x);
+        float x1 = fmaf(__uint_as_float(v[4 * j + 1]), scale, b[j].y);
+        float x2 = fmaf(__uint_as_float(v[4 * j + 2]), scale, b[j].z);
+        float x3 = fmaf(__uint_as_float(v[4 * j + 3]), scale, b[j].w);
+        if (GAMMA) {
+            x0 *= g;
+            x1 *= g;
+            x2 *= g;
+            x3 *= g;
+        }
+        pk[2 * j] = pack_bf16x2(x0, x1);
+        pk[2 * j + 1] = pack_bf16x2(x2, x3);
+    }
+}
+
+// 32 accumulator columns of one row -> 16 BF16 pairs of bf16(acc * scale).
+__device__ __forceinline__ void convert32(const uint32_t (&v)[32], uint32_t *pk, float scale)
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
+}
+
+// The epilogue-variant conversion of 64 accumulator columns of one row (two
+// 32-column reads) starting at output column x. Each case takes as few
+// instructions per element as it can, on uniform branches:
+//   no bias:  bf16(acc * (scale * gamma))           (gamma folded into the
+//             row's scale: one multiply, as the plain epilogue)
+//   bias:     bf16(fma(acc, scale, bias[c]) [* gamma])
+// The FP32 evaluation order is the kernel's; it differs from the exact
+// gamma * (alpha * acc + bias) only by FP32 rounding before the BF16 one.
+__device__ __forceinline__ void convert64_epi(const uint32_t (&v0)[32], const uint32_t (&v1)[32], uint32_t (&pk)[32],
+                                              float scale, const RowEpi &re, const GemmArgs &a, int x)
+{
+    if (!a.bias) {
+        const float sg = scale * re.gamma;
+        convert32(v0, pk, sg);
+        convert32(v1, pk + 16, sg);
+        return;
+    }
+    float4 b[8];
+    const bool full = x + 64 <= a.N;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t(&v)[32] = h ? v1 : v0;
+        if (full)
+            load_bias32<true>(a.bias, x + 32 * h, a.N, b);
+        else
+            load_bias32<false>(a.bias, x + 32 * h, a.N, b);
+        if (a.gamma)
+            convert32_bias<true>(v, pk + 16 * h, scale, re.gamma, b);
+        else
+            convert32_bias<false>(v, pk + 16 * h, scale, 1.0f, b);
     }
 }
 

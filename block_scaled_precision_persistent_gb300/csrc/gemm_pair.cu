@@ -339,30 +339,30 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
         for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
             int pm, nt;
             raster_tile(tile, args, pm, nt);
+            const int x0 = nt * BN + h * COLS_PER_WARP;            // first column of this warp
             RowEpi re{1.0f, -1};
-            if constexpr (EPI)
+            if constexpr (EPI) {
                 re = load_row_epi(args, pm * T::TILE_M + (int)rank * T::BM + q * 32 + lane);
+                prefetch_bias(args, x0, COLS_PER_WARP, lane);
+            }
             if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
                 break;
             tc_fence_after_sync();
             const uint32_t t_acc = tmem + lane_off + (uint32_t)(acc * BN + h * COLS_PER_WARP);
-            const int x0 = nt * BN + h * COLS_PER_WARP;            // first column of this warp
-            // 64 TMEM columns -> alpha (bias, gamma) -> BF16 pairs
-            auto drain = [&](int ch, uint32_t (&pk)[32]) {
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS + 32 * half, v);
-                    tmem_ld_wait();
-                    if constexpr (EPI) {
-                        convert32_epi(v, pk + 16 * half, scale, re.gamma, args.bias,
-                                      x0 + ch * T::EPI_COLS + 32 * half, args.N);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[16 * half + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * scale,
-                                                            __uint_as_float(v[2 * i + 1]) * scale);
-                    }
+            // chunk ch's 64 TMEM columns: both 32-column reads issued back to
+            // back, completed by one tcgen05.wait::ld
+            auto load_chunk = [&](int ch, uint32_t (&v0)[32], uint32_t (&v1)[32]) {
+                tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS, v0);
+                tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS + 32, v1);
+            };
+            // chunk ch's 64 FP32 columns -> alpha (bias, gamma) -> 32 BF16 pairs
+            auto convert_chunk = [&](int ch, const uint32_t (&v0)[32], const uint32_t (&v1)[32],
+                                     uint32_t (&pk)[32]) {
+                if constexpr (EPI) {
+                    convert64_epi(v0, v1, pk, scale, re, args, x0 + ch * T::EPI_COLS);
+                } else {
+                    convert32(v0, pk, scale);
+                    convert32(v1, pk + 16, scale);
                 }
             };
             // one 64-column chunk from registers into a 128B-swizzled staging
@@ -405,25 +405,41 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                 }
             };
             if constexpr (T::EPI_CHUNKS == 2) {
-                // first chunk staged, second held in registers: TMEM is released
-                // before either TMA store is issued
-                uint32_t pk0[32], pk1[32];
-                drain(0, pk0);
-                stage_out(pk0, ebuf);
-                drain(1, pk1);
-                release();
-                store_chunk(0, ebuf);
-                stage_out(pk1, ebuf);
+                // chunk 0 read, converted and staged; chunk 1 read, then TMEM
+                // is released at once -- chunk 1's conversion and both TMA
+                // stores overlap the next tile's MMAs
+                uint32_t pk[32];
+                {
+                    uint32_t v0[32], v1[32];
+                    load_chunk(0, v0, v1);
+                    tmem_ld_wait();
+                    convert_chunk(0, v0, v1, pk);
+                }
+                stage_out(pk, ebuf);
+                {
+                    uint32_t v0[32], v1[32];
+                    load_chunk(1, v0, v1);
+                    tmem_ld_wait();
+                    release();
+                    store_chunk(0, ebuf);
+                    convert_chunk(1, v0, v1, pk);
+                }
+                stage_out(pk, ebuf);
                 store_chunk(1, ebuf);
             } else {
                 // four chunks through two alternating buffers; TMEM is released
-                // after the last chunk's read
+                // right after the last chunk's read, before its conversion
 #pragma unroll 1
                 for (int ch = 0; ch < T::EPI_CHUNKS; ++ch) {
                     uint32_t pk[32];
-                    drain(ch, pk);
-                    if (ch == T::EPI_CHUNKS - 1)
-                        release();
+                    {
+                        uint32_t v0[32], v1[32];
+                        load_chunk(ch, v0, v1);
+                        tmem_ld_wait();
+                        if (ch == T::EPI_CHUNKS - 1)
+                            release();
+                        convert_chunk(ch, v0, v1, pk);
+                    }
                     const uint32_t sbuf = ebuf + (uint32_t)(ch & 1) * T::EPI_BUF_BYTES;
                     stage_out(pk, sbuf);
                     store_chunk(ch, sbuf);

@@ -319,8 +319,10 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
             int mt, nt;
             raster_tile(tile, args, mt, nt);
             RowEpi re{1.0f, -1};
-            if constexpr (EPI)
+            if constexpr (EPI) {
                 re = load_row_epi(args, mt * T::BM + q * 32 + lane);
+                prefetch_bias(args, nt * BN, BN, lane);
+            }
             if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
                 break;
             tc_fence_after_sync();
@@ -330,6 +332,7 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                 uint32_t v0[32], v1[32];
                 tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS, v0);
                 tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS + 32, v1);
+                const int x = nt * BN + ch * T::EPI_COLS;
                 tmem_ld_wait();
                 if (ch == BN / T::EPI_COLS - 1) {
                     // the whole accumulator is in registers: hand it back
@@ -344,12 +347,10 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                 __syncwarp();
                 const uint32_t sbuf = ebuf + (uint32_t)buf * T::EPI_BUF_BYTES;
                 const uint32_t row = sbuf + (uint32_t)lane * 128u;
-                const int x = nt * BN + ch * T::EPI_COLS;
                 // 128-byte swizzle: 16-byte chunk c of row r lands at chunk c ^ (r % 8)
                 if constexpr (EPI) {
                     uint32_t pk[32];
-                    convert32_epi(v0, pk, scale, re.gamma, args.bias, x, args.N);
-                    convert32_epi(v1, pk + 16, scale, re.gamma, args.bias, x + 32, args.N);
+                    convert64_epi(v0, v1, pk, scale, re, args, x);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         st_shared_v4(row + ((uint32_t)(c ^ (lane & 7)) << 4), pk[4 * c], pk[4 * c + 1],

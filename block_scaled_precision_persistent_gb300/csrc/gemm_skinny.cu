@@ -58,16 +58,19 @@ struct SkinnyTile {
     static constexpr int OUT_BYTES = M_PAD * BW * 2;
     static constexpr int NUM_BARS = 3 * STAGES + 4;
     static constexpr int BAR_BYTES = NUM_BARS * 8 + 16;
+    // epilogue-variant operands, staged once per CTA: gamma and destination
+    // row of the M_PAD activation rows, bias of the tile's BW weight rows
+    static constexpr int EPI_BYTES = (2 * M_PAD + BW) * 4;
     // the receive and staging areas get shared memory of their own when it
     // fits beside the ring (peers may then push as soon as their own MMAs are
     // done); otherwise they alias the drained ring and a sender first waits
     // for every peer to report its ring free
-    static constexpr bool OWN_RECV = 1024 + RING_BYTES + RECV_BYTES + OUT_BYTES + BAR_BYTES <= 232448;
+    static constexpr bool OWN_RECV = 1024 + RING_BYTES + RECV_BYTES + OUT_BYTES + EPI_BYTES + BAR_BYTES <= 232448;
     static constexpr int RECV_OFF = OWN_RECV ? RING_BYTES : 0;
     static constexpr int AREA = OWN_RECV ? RING_BYTES + RECV_BYTES + OUT_BYTES
                                          : (RING_BYTES > RECV_BYTES + OUT_BYTES ? RING_BYTES
                                                                                 : RECV_BYTES + OUT_BYTES);
-    static constexpr int SMEM_BYTES = 1024 + AREA + BAR_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + AREA + EPI_BYTES + BAR_BYTES;
     static constexpr int SCALE_WARPS = 4;
     static constexpr int EPI_WARP0 = 2 + SCALE_WARPS;
     static constexpr int EPI_WARPS = 4;
@@ -98,11 +101,12 @@ struct SkinnyTile {
 // The owned block's reduction, spread over the epilogue's threads: item
 // (cq, r) sums columns [4 cq, 4 cq + 4) of owned row r over the S partials in
 // the receive area, in rank order, scales them and stages them as BF16
-// [m][r] (row stride rpo) for the store. EPI: owned row r is output column
-// n0 + r (its bias), column m output row m (its gamma).
+// [m][r] (row stride rpo) for the store. EPI: s_bias[r] is the bias of
+// owned row r (an output column), s_gamma[m] the gamma of output row m.
 template <int S, bool EPI>
 __device__ __forceinline__ void reduce_owned(const uint8_t *recv, __nv_bfloat16 *out, int rpo, int live_cols,
-                                             float alpha, int t, int nthreads, const GemmArgs &args, int n0)
+                                             float alpha, int t, int nthreads, const float *s_gamma,
+                                             const float *s_bias)
 {
     const int items = (live_cols / 4) * rpo;
     const int slot_bytes = rpo * live_cols * 4;
@@ -123,11 +127,11 @@ __device__ __forceinline__ void reduce_owned(const uint8_t *recv, __nv_bfloat16 
         const int r = idx % rpo;
         const int m0 = (idx / rpo) * 4;
         if constexpr (EPI) {
-            const float b = epi_bias(args, n0 + r);
-            out[(m0 + 0) * rpo + r] = __float2bfloat16_rn(fmaf(a.x, alpha, b) * epi_gamma(args, m0 + 0));
-            out[(m0 + 1) * rpo + r] = __float2bfloat16_rn(fmaf(a.y, alpha, b) * epi_gamma(args, m0 + 1));
-            out[(m0 + 2) * rpo + r] = __float2bfloat16_rn(fmaf(a.z, alpha, b) * epi_gamma(args, m0 + 2));
-            out[(m0 + 3) * rpo + r] = __float2bfloat16_rn(fmaf(a.w, alpha, b) * epi_gamma(args, m0 + 3));
+            const float b = s_bias[r];
+            out[(m0 + 0) * rpo + r] = __float2bfloat16_rn(fmaf(a.x, alpha, b) * s_gamma[m0 + 0]);
+            out[(m0 + 1) * rpo + r] = __float2bfloat16_rn(fmaf(a.y, alpha, b) * s_gamma[m0 + 1]);
+            out[(m0 + 2) * rpo + r] = __float2bfloat16_rn(fmaf(a.z, alpha, b) * s_gamma[m0 + 2]);
+            out[(m0 + 3) * rpo + r] = __float2bfloat16_rn(fmaf(a.w, alpha, b) * s_gamma[m0 + 3]);
         } else {
             out[(m0 + 0) * rpo + r] = __float2bfloat16_rn(a.x * alpha);
             out[(m0 + 1) * rpo + r] = __float2bfloat16_rn(a.y * alpha);
@@ -154,7 +158,10 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *const gbase = smem_raw + (base - raw);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + T::AREA);
+    float *const s_gamma = reinterpret_cast<float *>(gbase + T::AREA);   // [M_PAD]
+    int *const s_dst = reinterpret_cast<int *>(s_gamma + M_PAD);          // [M_PAD]
+    float *const s_bias = reinterpret_cast<float *>(s_dst + M_PAD);       // [BW]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + T::AREA + T::EPI_BYTES);
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t full0 = bar0;                       // [STAGES] operands -> MMA
     const uint32_t empty0 = full0 + 8u * STAGES;       // [STAGES] MMA done -> producer
@@ -317,12 +324,28 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
         uint8_t *const recv = gbase + T::RECV_OFF;
         __nv_bfloat16 *const out = reinterpret_cast<__nv_bfloat16 *>(recv + T::RECV_BYTES);
         const int own_lo = (int)rank * rpo;             // rows this CTA owns: [own_lo, own_lo + rpo)
+        if constexpr (EPI) {
+            // the epilogue operands into shared memory while the MMAs run:
+            // gamma and destination row (-1: not written) of every
+            // activation row, bias of the owned weight rows
+            for (int m = et; m < M_PAD; m += 32 * T::EPI_WARPS) {
+                s_gamma[m] = epi_gamma(args, m);
+                int d = m < args.M ? m : -1;
+                if (args.scatter && m < args.M) {
+                    d = __ldg(args.scatter + m);
+                    d = (d >= 0 && d < args.m_out) ? d : -1;
+                }
+                s_dst[m] = d;
+            }
+            for (int r = et; r < T::BW; r += 32 * T::EPI_WARPS)
+                s_bias[r] = epi_bias(args, nt * T::BW + (S > 1 ? own_lo : 0) + r);
+            named_bar_sync(1, 32 * T::EPI_WARPS);
+        }
         const bool have = nkb > 0 && warp_wait(tfull, 0, wd, abort_flag, 4, lane);
         if (have)
             tc_fence_after_sync();
         if (S == 1) {
             if (have) {
-                const float b = EPI ? epi_bias(args, nt * T::BW + n) : 0.0f;
 #pragma unroll 1
                 for (int c0 = 0; c0 < live_cols; c0 += 32) {
                     uint32_t v[32];
@@ -332,7 +355,7 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
                     for (int i = 0; i < 32; ++i) {
                         if constexpr (EPI)
                             out[(c0 + i) * T::BW + n] = __float2bfloat16_rn(
-                                fmaf(__uint_as_float(v[i]), alpha, b) * epi_gamma(args, c0 + i));
+                                fmaf(__uint_as_float(v[i]), alpha, s_bias[n]) * s_gamma[c0 + i]);
                         else
                             out[(c0 + i) * T::BW + n] = __float2bfloat16_rn(__uint_as_float(v[i]) * alpha);
                     }
@@ -379,11 +402,10 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
             const bool rows_in = warp_wait(rx, 0, wd, abort_flag, 8, lane);
             named_bar_sync(1, 32 * T::EPI_WARPS);        // the owned rows' local writes
             if (have && rows_in) {
-                const int n0 = nt * T::BW + own_lo;
                 switch (S) {
-                case 2: reduce_owned<2, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, args, n0); break;
-                case 4: reduce_owned<4, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, args, n0); break;
-                default: reduce_owned<8, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, args, n0); break;
+                case 2: reduce_owned<2, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, s_gamma, s_bias); break;
+                case 4: reduce_owned<4, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, s_gamma, s_bias); break;
+                default: reduce_owned<8, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, s_gamma, s_bias); break;
                 }
             }
         }
@@ -397,8 +419,8 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
             for (int p = et; p < args.M * pieces; p += 32 * T::EPI_WARPS) {
                 const int m = p / pieces;
                 const int col = col0 + 8 * (p - m * pieces);
-                const int d = __ldg(args.scatter + m);
-                if (d >= 0 && d < args.m_out && col < args.N)
+                const int d = s_dst[m];
+                if (d >= 0 && col < args.N)
                     *reinterpret_cast<uint4 *>(args.d + (size_t)d * (size_t)args.N + (size_t)col) =
                         *reinterpret_cast<const uint4 *>(out + m * rpo + (col - col0));
             }
