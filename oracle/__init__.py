@@ -93,6 +93,13 @@ class Oracle:
         L.bso_swizzled_scale_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
         L.bso_swizzle_scales.restype = ctypes.c_int
         L.bso_swizzle_scales.argtypes = [ctypes.c_int, ctypes.c_int, u8p, u8p]
+        L.bso_nvfp4_grouped_gemm.restype = ctypes.c_int
+        L.bso_nvfp4_grouped_gemm.argtypes = [ctypes.c_int] * 4 + [u8p] * 4 + [i32p, ctypes.c_float, f32p, f32p,
+                                                                         f64p, f64p, u16p, ctypes.c_int]
+        L.bso_grouped_scale_bytes.restype = ctypes.c_size_t
+        L.bso_grouped_scale_bytes.argtypes = [ctypes.c_int] * 3
+        L.bso_swizzle_scales_grouped.restype = ctypes.c_int
+        L.bso_swizzle_scales_grouped.argtypes = [ctypes.c_int] * 3 + [i32p, u8p, u8p]
         L.bso_nvfp4_quantize.restype = ctypes.c_int
         L.bso_nvfp4_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_uint16),
                                          u8p, u8p, ctypes.POINTER(ctypes.c_float),
@@ -187,6 +194,54 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"bso_fp8_gemm rejected its arguments (rc={rc})")
         return S, T, D
+
+    def nvfp4_grouped_gemm(self, A, sfA, B, sfB, offs, alpha, K, bias=None, gamma=None, nthreads=None):
+        """Grouped (ragged) NVFP4 GEMM: rows [offs[e], offs[e+1]) of A times
+        B[e]^T for each slice e. A: uint8[M, K/2], sfA: uint8[M, K/16],
+        B: uint8[E, N, K/2], sfB: uint8[E, N, K/16], offs: int32[E+1],
+        bias: float32[E, N] or None, gamma: float32[M] or None.
+        Returns (S, T, D_bits), each [M, N] in row order."""
+        A = np.ascontiguousarray(A, dtype=np.uint8)
+        sfA = np.ascontiguousarray(sfA, dtype=np.uint8)
+        B = np.ascontiguousarray(B, dtype=np.uint8)
+        sfB = np.ascontiguousarray(sfB, dtype=np.uint8)
+        offs = np.ascontiguousarray(offs, dtype=np.int32)
+        E, N = B.shape[0], B.shape[1]
+        M = A.shape[0]
+        assert B.shape == (E, N, K // 2) and sfB.shape == (E, N, K // 16) and offs.shape == (E + 1,)
+        assert A.shape == (M, K // 2) and sfA.shape == (M, K // 16)
+        if bias is not None:
+            bias = np.ascontiguousarray(np.asarray(bias, dtype=np.float32))
+            assert bias.shape == (E, N)
+        gamma = self._vec(gamma, M)
+        S = np.empty((M, N), np.float64)
+        T = np.empty((M, N), np.float64)
+        D = np.empty((M, N), np.uint16)
+        rc = self.lib.bso_nvfp4_grouped_gemm(E, M, N, K, self._p(A, ctypes.c_uint8), self._p(sfA, ctypes.c_uint8),
+                                             self._p(B, ctypes.c_uint8), self._p(sfB, ctypes.c_uint8),
+                                             self._p(offs, ctypes.c_int32), float(alpha),
+                                             self._p(bias, ctypes.c_float), self._p(gamma, ctypes.c_float),
+                                             self._p(S, ctypes.c_double), self._p(T, ctypes.c_double),
+                                             self._p(D, ctypes.c_uint16), nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"bso_nvfp4_grouped_gemm rejected its arguments (rc={rc})")
+        return S, T, D
+
+    def grouped_scale_bytes(self, E: int, M: int, K: int) -> int:
+        return int(self.lib.bso_grouped_scale_bytes(E, M, K))
+
+    def swizzle_scales_grouped(self, sf, offs, K: int):
+        """Row-major uint8[M, K/16] scales of a grouped A -> the per-slice
+        swizzled layout (1-D uint8 of grouped_scale_bytes(E, M, K))."""
+        sf = np.ascontiguousarray(sf, dtype=np.uint8)
+        offs = np.ascontiguousarray(offs, dtype=np.int32)
+        E, M = offs.size - 1, sf.shape[0]
+        out = np.empty(self.grouped_scale_bytes(E, M, K), np.uint8)
+        rc = self.lib.bso_swizzle_scales_grouped(E, M, K, self._p(offs, ctypes.c_int32),
+                                                 self._p(sf, ctypes.c_uint8), self._p(out, ctypes.c_uint8))
+        if rc != 0:
+            raise ValueError("bso_swizzle_scales_grouped rejected its arguments")
+        return out
 
     @staticmethod
     def scatter_rows(D_rows, scatter, out):

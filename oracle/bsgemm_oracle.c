@@ -444,6 +444,93 @@ int bso_swizzle_scales(int rows, int K, const uint8_t *in, uint8_t *out)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Grouped (ragged, routed) NVFP4 GEMM                                        */
+/* ------------------------------------------------------------------------ */
+
+/* "Triton #11171 - Why Two New NVFP4 Test Cases Produced Twelve
+ * Tensor-Memory Failures", section "Ragged mode added routing rather than a
+ * plain matrix": routed activation rows form expert slices, and each slice
+ * is multiplied by the dense right-hand side of its own slice. Written out:
+ * the rows of A are grouped into E consecutive slices, slice e being rows
+ * [offs[e], offs[e+1]); for those rows
+ *     S[i][j] = alpha * sum_b sA[i][b] sB_e[j][b] sum_t a(i, 16b+t) b_e(j, 16b+t)
+ * followed by the epilogue of bso_nvfp4_gemm with bias_e = bias + e*N and
+ * gamma[i]. That is: each slice is an ordinary NVFP4 GEMM of its own.
+ *   A: uint8[M][K/2], sfA: uint8[M][K/16]   (rows grouped by slice)
+ *   B: uint8[E][N][K/2], sfB: uint8[E][N][K/16]
+ *   offs: int32[E+1] with offs[0] = 0, nondecreasing, offs[E] = M
+ *   bias: float[E][N] or NULL; gamma: float[M] or NULL
+ * Outputs are [M][N] in row order; any may be NULL. Returns 0, or -1 for
+ * bad sizes or offsets.                                                     */
+int bso_nvfp4_grouped_gemm(int E, int M, int N, int K, const uint8_t *A, const uint8_t *sfA,
+                           const uint8_t *B, const uint8_t *sfB, const int32_t *offs, float alpha,
+                           const float *bias, const float *gamma, double *S, double *T, uint16_t *D,
+                           int nthreads)
+{
+    if (E < 1 || M < 0 || N < 0 || K < 0 || (K % 16) != 0 || !offs)
+        return -1;
+    if (offs[0] != 0 || offs[E] != M)
+        return -1;
+    for (int e = 0; e < E; ++e)
+        if (offs[e + 1] < offs[e])
+            return -1;
+    const size_t arow = (size_t)(K / 2), srow = (size_t)(K / 16);
+    for (int e = 0; e < E; ++e) {
+        const int r0 = offs[e], rows = offs[e + 1] - offs[e];
+        if (rows == 0)
+            continue;
+#ifdef BSO_MUTANT_GROUP_SHIFT
+        const int be = (e + 1) % E;      /* planted: the next slice's right-hand side */
+#else
+        const int be = e;
+#endif
+        const size_t o = (size_t)r0 * (size_t)N;
+        int rc = bso_nvfp4_gemm(rows, N, K, A + (size_t)r0 * arow, sfA + (size_t)r0 * srow,
+                                B + (size_t)be * (size_t)N * arow, sfB + (size_t)be * (size_t)N * srow,
+                                alpha, bias ? bias + (size_t)e * (size_t)N : NULL,
+                                gamma ? gamma + r0 : NULL, NULL, 0, NULL, 0,
+                                S ? S + o : NULL, T ? T + o : NULL, D ? D + o : NULL, nthreads);
+        if (rc != 0)
+            return rc;
+    }
+    return 0;
+}
+
+/* Scale layout of a grouped A: the swizzled layout above, applied to each
+ * slice on its own, the slices' 128-row blocks concatenated in slice order
+ * -- slice e starts at 128-row block sum_{e'<e} ceil(rows_e' / 128), so
+ * every tile of 128 rows of one slice reads one block row. The buffer holds
+ * (ceil(M/128) + E) block rows (an upper bound of the sum, since sizes
+ * are not known on the host); block rows past the slices' are zero.       */
+size_t bso_grouped_scale_bytes(int E, int M, int K)
+{
+    if (E < 1 || M < 0 || K < 0 || (K % 16) != 0)
+        return 0;
+    size_t pc = ((size_t)(K / 16) + 3u) / 4u * 4u;
+    return ((size_t)(M + 127) / 128u + (size_t)E) * 128u * pc;
+}
+
+int bso_swizzle_scales_grouped(int E, int M, int K, const int32_t *offs, const uint8_t *in, uint8_t *out)
+{
+    if (E < 1 || M < 0 || K < 0 || (K % 16) != 0 || !offs || offs[0] != 0 || offs[E] != M)
+        return -1;
+    for (int e = 0; e < E; ++e)
+        if (offs[e + 1] < offs[e])
+            return -1;
+    const size_t cols = (size_t)(K / 16);
+    const size_t block_row_bytes = 128u * ((cols + 3u) / 4u * 4u);
+    memset(out, 0, bso_grouped_scale_bytes(E, M, K));
+    size_t brow = 0;
+    for (int e = 0; e < E; ++e) {
+        const int rows = offs[e + 1] - offs[e];
+        if (bso_swizzle_scales(rows, K, in + (size_t)offs[e] * cols, out + brow * block_row_bytes) != 0)
+            return -1;
+        brow += ((size_t)rows + 127u) / 128u;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Two-level NVFP4 quantisation: BF16 -> E2M1 codes + E4M3 block scales      */
 /* ------------------------------------------------------------------------ */
 

@@ -9,7 +9,8 @@ deliberate mistake at a time (a wrong exponent bias, a dropped sign, swapped
 nibbles in one operand, a dropped scale, a dropped block, a transposed operand, a wrong
 scale layout; in the quantiser, ties rounded away from zero, a dropped global
 scale, swapped nibbles, block scales rounded up; in the epilogue, gamma
-applied before the bias, bias indexed by row) and shows that at least one
+applied before the bias, bias indexed by row; in the grouped GEMM, a slice
+multiplied by the next slice's right-hand side) and shows that at least one
 pin fails for each.
 """
 from __future__ import annotations
@@ -348,6 +349,97 @@ def pin_scatter_permutation(o):
     assert (np.delete(out2, drop[kept], axis=0) == 999).all()
 
 
+def pin_grouped_worked(o):
+    """tests/golden/nvfp4_grouped_case.txt: two slices with their own
+    right-hand sides, without and with bias / gamma (values exact)."""
+    g = {}
+    for t in _rows("nvfp4_grouped_case.txt"):
+        g.setdefault(t[0], []).append(t[1:])
+    offs = [int(v) for v in g["offs"][0]]
+    row = lambda c: [int(c, 16)] * 16  # noqa: E731
+    A = pack(np.array([row(c) for c in g["acodes"][0]], np.uint8))
+    B = np.stack([pack(np.array([row(c) for c in g[f"b{e}codes"][0]], np.uint8)) for e in (0, 1)])
+    M, N = A.shape[0], B.shape[1]
+    sfA = np.full((M, 1), 0x38, np.uint8)
+    sfB = np.full((2, N, 1), 0x38, np.uint8)
+    alpha = float(g["alpha"][0][0])
+    S, T, D = o.nvfp4_grouped_gemm(A, sfA, B, sfB, offs, alpha, 16)
+    for r in g["plain"]:
+        assert S[int(r[0])].tolist() == [float(v) for v in r[1:]], ("plain", r[0], S[int(r[0])])
+    assert np.array_equal(T, np.abs(S))      # every product of a row has one sign
+    bias = np.array([[float(v) for v in g["bias0"][0]], [float(v) for v in g["bias1"][0]]], np.float32)
+    gamma = np.array([float(v) for v in g["gamma"][0]], np.float32)
+    S, _, D = o.nvfp4_grouped_gemm(A, sfA, B, sfB, offs, alpha, 16, bias=bias, gamma=gamma)
+    for r in g["D"]:
+        want = [float(v) for v in r[1:]]
+        assert S[int(r[0])].tolist() == want and oracle.bf16_bits_to_float(D[int(r[0])]).tolist() == want, r[0]
+
+
+def pin_grouped_single_slice_is_plain(o):
+    # E = 1: one slice covering every row is exactly the ordinary GEMM
+    M, N, K = 40, 24, 64
+    A, sfA, B, sfB = _uniform_problem(M, N, K, 17)
+    S0, T0, D0 = o.nvfp4_gemm(A, sfA, B, sfB, 0.625, K)
+    S1, T1, D1 = o.nvfp4_grouped_gemm(A, sfA, B[None], sfB[None], [0, M], 0.625, K)
+    assert np.array_equal(S0, S1) and np.array_equal(T0, T1) and np.array_equal(D0, D1)
+
+
+def pin_grouped_numpy(o):
+    # Independent restatement over ragged slices (one empty): dequantise
+    # with the golden table and the library E4M3 decoder, multiply each
+    # slice by its own right-hand side in float64, add that slice's bias,
+    # scale rows by gamma. 2^u scales: every sum exact.
+    M, N, K, E = 45, 16, 64, 4
+    offs = [0, 7, 7, 30, 45]
+    A, sfA, _, _ = _uniform_problem(M, N, K, 23)
+    Bs, sBs = zip(*[_uniform_problem(M, N, K, 40 + e)[2:] for e in range(E)])
+    B, sfB = np.stack(Bs), np.stack(sBs)
+    rng = np.random.default_rng(8)
+    bias = rng.standard_normal((E, N)).astype(np.float32)
+    gamma = rng.standard_normal(M).astype(np.float32)
+    S, T, _ = o.nvfp4_grouped_gemm(A, sfA, B, sfB, offs, 1.5, K, bias=bias, gamma=gamma)
+    da = deq_nvfp4(A, sfA)
+    ref = np.empty((M, N))
+    for e in range(E):
+        r0, r1 = offs[e], offs[e + 1]
+        ref[r0:r1] = (1.5 * (da[r0:r1] @ deq_nvfp4(B[e], sfB[e]).T) + bias[e].astype(np.float64)) \
+            * gamma[r0:r1, None].astype(np.float64)
+    assert np.allclose(S, ref, rtol=1e-15, atol=0)
+    with pytest.raises(ValueError):
+        o.nvfp4_grouped_gemm(A, sfA, B, sfB, [0, 7, 6, 30, 45], 1.5, K)    # decreasing offsets
+
+
+def pin_grouped_scale_layout(o):
+    # Each slice is swizzled on its own and starts a new 128-row block row:
+    # the byte of (row, col) of slice e sits in block row
+    # blk0(e) + (row - offs[e]) // 128, written out here from the layout's
+    # definition (row r, column c of a 128 x 4 block at (r%32)*16 + (r//32)*4
+    # + c%4, blocks column-block fastest), padding zero.
+    K, offs = 96, [0, 130, 130, 200]
+    M, cols = offs[-1], K // 16
+    ncb = (cols + 3) // 4
+    sf = np.random.default_rng(3).integers(1, 256, (M, cols)).astype(np.uint8)
+    got = o.swizzle_scales_grouped(sf, offs, K)
+    assert got.size == (-(-M // 128) + 3) * 128 * ncb * 4
+    want = np.zeros_like(got)
+    brow = 0
+    for e in range(3):
+        for r in range(offs[e], offs[e + 1]):
+            lr = r - offs[e]
+            for c in range(cols):
+                blk = (brow + lr // 128) * ncb + c // 4
+                rr = lr % 128
+                want[blk * 512 + (rr % 32) * 16 + (rr // 32) * 4 + c % 4] = sf[r, c]
+        brow += -(-(offs[e + 1] - offs[e]) // 128)
+    assert np.array_equal(got, want)
+    # hand-worked landmarks: slice 2 (rows 130..199) starts at block row 2
+    # (slice 0 fills two block rows, slice 1 none): its first row's scale 0 is
+    # byte 2 * ncb * 512; row 199 (local 69: 69 % 32 = 5, 69 // 32 = 2),
+    # scale 5 (column block 1, c % 4 = 1) is byte (2*ncb + 1)*512 + 5*16 + 2*4 + 1.
+    assert got[2 * ncb * 512] == sf[130, 0]
+    assert got[(2 * ncb + 1) * 512 + 5 * 16 + 2 * 4 + 1] == sf[199, 5]
+
+
 def _swizzle_numpy(sf: np.ndarray, K: int) -> np.ndarray:
     """Independent restatement of the 128x4-blocked scale layout by reshapes."""
     rows, cols = sf.shape
@@ -503,7 +595,8 @@ PINS = [pin_e2m1_table, pin_e4m3_codes, pin_bf16_cases, pin_worked_1x1x16, pin_w
         pin_one_hot, pin_brute_force_k16, pin_scale_linearity, pin_numpy_definition,
         pin_fraction_exact, pin_fp8_numpy, pin_swizzle, pin_quantize_worked,
         pin_quantize_nearest_bruteforce, pin_quantize_scale_invariance, pin_quantize_amax_element,
-        pin_quantize_dequant_bound, pin_epilogue_worked, pin_epilogue_numpy, pin_scatter_permutation]
+        pin_quantize_dequant_bound, pin_epilogue_worked, pin_epilogue_numpy, pin_scatter_permutation,
+        pin_grouped_worked, pin_grouped_single_slice_is_plain, pin_grouped_numpy, pin_grouped_scale_layout]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -513,7 +606,8 @@ def test_oracle_pin(pin):
 
 MUTANTS = ["E2M1_BIAS0", "E2M1_NOSIGN", "E4M3_BIAS8", "SWAP_NIBBLES_A", "DROP_SFB",
            "DROP_LAST_BLOCK", "TRANSPOSE_B", "SWIZZLE_ROWMAJOR_BLOCK", "Q_TIES_AWAY", "Q_NO_SG",
-           "Q_SWAP_NIBBLES", "Q_E4M3_CEIL", "EPI_GAMMA_FIRST", "EPI_BIAS_BY_ROW"]
+           "Q_SWAP_NIBBLES", "Q_E4M3_CEIL", "EPI_GAMMA_FIRST", "EPI_BIAS_BY_ROW",
+           "GROUP_SHIFT"]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
