@@ -17,6 +17,7 @@ from pathlib import Path
 __all__ = [
     "BsgError", "load", "nvfp4_gemm", "nvfp4_gemm_swizzled", "nvfp4_swizzle_scales", "nvfp4_quantize",
     "nvfp4_swizzled_scale_bytes", "nvfp4_gemm_noalloc", "fp8_gemm", "nvfp4_gemm_ex", "fp8_gemm_ex",
+    "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes",
     "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_select_plan", "bsg_last_launch_count", "bsg_error_string", "EXPORTED_SYMBOLS",
@@ -51,6 +52,10 @@ _SIGNATURES = {
     "fp8_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "nvfp4_gemm_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "fp8_gemm_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
+    "nvfp4_grouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp,
+                                _vp]),
+    "nvfp4_swizzle_scales_grouped": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp]),
+    "nvfp4_grouped_scale_bytes": (ctypes.c_size_t, [_i, _i, _i]),
     "bsg_reserve_workspace": (_i, [_i, ctypes.c_size_t]),
     "bsg_get_device_status": (_i, [_vp]),
     "bsg_last_status_word": (ctypes.c_uint32, []),
@@ -171,6 +176,27 @@ def fp8_gemm_ex(M, N, K, A, sA, B, sB, alpha, bias, gamma, scatter, m_out, D, st
     _check(load().fp8_gemm_ex(M, N, K, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), float(alpha), _ptr(bias),
                               _ptr(gamma), _ptr(scatter), int(m_out), _ptr(D), _stream(stream)),
            "fp8_gemm_ex")
+
+
+def nvfp4_grouped_gemm(E, M, N, K, A, sfA_swz, B, sfB_swz, offs, alpha, bias, gamma, scatter, m_out, D,
+                       stream=None) -> None:
+    """Grouped (ragged, routed) NVFP4 GEMM: rows [offs[e], offs[e+1]) of A
+    times B[e]^T for each of the E slices; offs is a device int32[E+1]
+    tensor, B uint8[E, N, K/2], bias float32[E, N] or None; the epilogue as
+    nvfp4_gemm_ex."""
+    _check(load().nvfp4_grouped_gemm(E, M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), _ptr(sfB_swz), _ptr(offs),
+                                     float(alpha), _ptr(bias), _ptr(gamma), _ptr(scatter), int(m_out), _ptr(D),
+                                     _stream(stream)), "nvfp4_grouped_gemm")
+
+
+def nvfp4_swizzle_scales_grouped(E, M, K, offs, sf, sf_swz, stream=None) -> None:
+    """Per-slice scale layout of a grouped A (see nvfp4_grouped_gemm)."""
+    _check(load().nvfp4_swizzle_scales_grouped(E, M, K, _ptr(offs), _ptr(sf), _ptr(sf_swz), _stream(stream)),
+           "nvfp4_swizzle_scales_grouped")
+
+
+def nvfp4_grouped_scale_bytes(E, M, K) -> int:
+    return int(load().nvfp4_grouped_scale_bytes(E, M, K))
 
 
 def bsg_reserve_workspace(device: int, nbytes: int) -> None:

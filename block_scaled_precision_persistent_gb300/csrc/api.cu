@@ -11,6 +11,7 @@
 
 #include "bsg_internal.h"
 #include "bsgemm.h"
+#include "group.cuh"
 
 // Device status word written by bounded waits that run out (one per device).
 __device__ unsigned int g_bsg_status_word;
@@ -326,6 +327,76 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     return BSG_OK;
 }
 
+// Grouped (ragged) NVFP4 GEMM: the 1-SM kernel's grouped instantiation, one
+// 128-row tile row per 128 rows of each slice. The slice table is built on
+// the device from offs, so the grid is sized for the bound on the tile rows,
+// ceil(M/128) + E; CTAs past the actual tiles exit at once.
+int run_grouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, const void *B,
+                const uint8_t *sfb, const int32_t *offs, float alpha, const Epilogue &epi, void *D,
+                cudaStream_t stream, DeviceState *ds)
+{
+    const long long mt_bound = (long long)(M + 127) / 128 + E;
+    int plan;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        plan = g_forced_plan;
+    }
+    if (plan >= 0) {
+        const PlanInfo &fp = bsg::plan_info(plan);
+        if (fp.kind != Kind::NVFP4 || fp.family != bsg::Family::TC1)
+            return BSG_ERR_NO_PLAN;
+    } else {
+        // 128-wide tiles while they number at most 4 per SM, else 256-wide
+        const long long tiles128 = mt_bound * (long long)((N + 127) / 128);
+        plan = bsg::find_plan(tiles128 <= 4LL * ds->sms ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc1_128x256_s3_acc1");
+        if (plan < 0)
+            return BSG_ERR_NO_PLAN;
+    }
+    const PlanInfo &pi = bsg::plan_info(plan);
+    const uint64_t row_bytes = (uint64_t)K / 2u;
+    GemmMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    int rc;
+    if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes, 128,
+                        128)) != BSG_OK ||
+        (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, (uint64_t)E * (uint64_t)N,
+                        row_bytes, 128, (uint32_t)pi.bn)) != BSG_OK ||
+        (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, d_rows(M, epi),
+                        (uint64_t)N * 2u, 64, 32)) != BSG_OK)
+        return rc;
+    maps.sfa = maps.a;
+    maps.sfb = maps.a;
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.num_m_tiles = (int)mt_bound;      // bound only: the kernel counts the slices' tile rows
+    a.num_n_tiles = (N + pi.bn - 1) / pi.bn;
+    a.num_k_blocks = K / pi.k_block;
+    a.raster_group = 8;
+    a.sf_col_blocks = (K / 16 + 3) / 4;
+    a.sfb_row_blocks = (N + 127) / 128;
+    a.sfa = sfa;
+    a.sfb = sfb;
+    a.alpha = alpha;
+    a.status = ds->status;
+    a.timeout_ns = g_watchdog_ns.load();
+    set_epilogue(a, epi, D);
+    a.num_groups = E;
+    a.group_offs = offs;
+    a.sfb_group_bytes = swizzled_bytes(N, K);
+    const long long ctas = mt_bound * a.num_n_tiles;
+    const int resident = bsg::max_resident_ctas(plan, ds->sms);
+    if (resident < 1)
+        return BSG_ERR_CUDA;
+    const int grid = (int)(ctas < resident ? ctas : resident);
+    if (bsg::launch_gemm(plan, maps, a, grid, stream) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    ++t_last_launches;
+    return BSG_OK;
+}
+
 int check_nvfp4_args(int M, int N, int K, const void *A, const void *sfA, const void *B,
                      const void *sfB, void *D)
 {
@@ -571,6 +642,58 @@ int fp8_gemm_ex(int M, int N, int K, const void *A, const float *sA, const void 
     e.m_out = m_out;
     return run_gemm(Kind::FP8, M, N, K, A, B, nullptr, nullptr, sA, sB, alpha, D,
                     reinterpret_cast<cudaStream_t>(stream), ds, e);
+}
+
+size_t nvfp4_grouped_scale_bytes(int E, int M, int K)
+{
+    if (E < 1 || E > bsg::kMaxGroups || M < 0 || K < 16 || (K % 16) != 0)
+        return 0;
+    return ((size_t)(M + 127) / 128u + (size_t)E) * 128u * ((size_t)(K / 16 + 3) / 4u * 4u);
+}
+
+int nvfp4_swizzle_scales_grouped(int E, int M, int K, const int32_t *offs, const void *sf, void *sf_swz,
+                                 bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    if (!offs || !sf || !sf_swz || E < 1 || E > bsg::kMaxGroups || M < 1 || K < 16 || (K % 16) != 0)
+        return BSG_ERR_INVALID_ARG;
+    if (!aligned16(sf_swz) || (reinterpret_cast<uintptr_t>(offs) & 3u))
+        return BSG_ERR_MISALIGNED;
+    DeviceState *ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc != BSG_OK)
+        return rc;
+    if (bsg::launch_swizzle_scales_grouped(E, M, K, offs, static_cast<const uint8_t *>(sf),
+                                           static_cast<uint8_t *>(sf_swz),
+                                           reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    t_last_launches = 1;
+    return BSG_OK;
+}
+
+int nvfp4_grouped_gemm(int E, int M, int N, int K, const void *A, const void *sfA_swz, const void *B,
+                       const void *sfB_swz, const int32_t *offs, float alpha, const float *bias,
+                       const float *gamma, const int32_t *scatter, int m_out, void *D, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    if (!offs || E < 1 || E > bsg::kMaxGroups)
+        return BSG_ERR_INVALID_ARG;
+    int rc = check_nvfp4_args(M, N, K, A, sfA_swz, B, sfB_swz, D);
+    if (rc != BSG_OK || (rc = check_epilogue_args(M, bias, gamma, scatter, m_out)) != BSG_OK)
+        return rc;
+    if (reinterpret_cast<uintptr_t>(offs) & 3u)
+        return BSG_ERR_MISALIGNED;
+    DeviceState *ds = nullptr;
+    if ((rc = current_device(&ds)) != BSG_OK)
+        return rc;
+    Epilogue e;
+    e.bias = bias;
+    e.gamma = gamma;
+    e.scatter = scatter;
+    e.m_out = m_out;
+    return run_grouped(E, M, N, K, A, static_cast<const uint8_t *>(sfA_swz), B,
+                       static_cast<const uint8_t *>(sfB_swz), offs, alpha, e, D,
+                       reinterpret_cast<cudaStream_t>(stream), ds);
 }
 
 int bsg_reserve_workspace(int device, size_t bytes)

@@ -37,7 +37,18 @@ struct GemmArgs {
     const int *scatter;        // [M] row of D that computed row m goes to, or null
     uint16_t *d;               // D (BF16 bits, row pitch N) for the scattered stores
     int m_out;                 // rows of D when scattered
+    // Grouped (ragged) GEMM, read only by the GROUPED instantiation: A's
+    // rows are num_groups slices by group_offs (device int32[E+1]); slice e
+    // multiplies B rows [e*N, e*N + N), whose swizzled scales start
+    // e * sfb_group_bytes bytes into sfb, and adds bias + e*N
+    int num_groups;
+    const int *group_offs;
+    size_t sfb_group_bytes;
 };
+
+// Kernel instantiations: the plain epilogue, the epilogue variants, and the
+// grouped GEMM (which always has the variants' epilogue).
+enum KernelMode : int { kModePlain = 0, kModeEpi = 1, kModeGrouped = 2 };
 
 // True when a call needs the epilogue-variant kernels.
 inline bool has_epilogue(const GemmArgs &a) { return a.bias || a.gamma || a.scatter; }
@@ -98,6 +109,11 @@ int skinny_max_clusters(int i, int splits);
 // Scale-layout prep kernel. Returns a cudaError_t.
 cudaError_t launch_swizzle_scales(int rows, int K, const uint8_t *sf, uint8_t *out,
                                   cudaStream_t stream);
+
+// Per-slice scale-layout prep of a grouped A (offs: device int32[E+1]);
+// out holds (ceil(rows / 128) + E) block rows.
+cudaError_t launch_swizzle_scales_grouped(int E, int rows, int K, const int *offs, const uint8_t *sf,
+                                          uint8_t *out, cudaStream_t stream);
 
 // Two-level NVFP4 quantisation: memset of global[0], amax kernel, quantiser.
 cudaError_t launch_nvfp4_quantize(int rows, int K, const void *X, uint8_t *packed, uint8_t *sf_swz,

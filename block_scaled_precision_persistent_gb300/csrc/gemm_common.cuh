@@ -12,15 +12,21 @@ namespace bsg {
 // group the M tile varies fastest, so the CTAs resident at one time share a
 // few A panels and a band of B panels in L2 ("Building the GEMM": tile
 // rasterisation order permuted for memory locality).
-__device__ __forceinline__ void raster_tile(int tile, const GemmArgs &a, int &mt, int &nt)
+__device__ __forceinline__ void raster_tile(int tile, int raster_group, int num_m_tiles, int num_n_tiles, int &mt,
+                                            int &nt)
 {
-    const int per_group = a.raster_group * a.num_n_tiles;
+    const int per_group = raster_group * num_n_tiles;
     const int g = tile / per_group;
-    const int first_m = g * a.raster_group;
-    const int gm = min(a.raster_group, a.num_m_tiles - first_m);
+    const int first_m = g * raster_group;
+    const int gm = min(raster_group, num_m_tiles - first_m);
     const int local = tile - g * per_group;
     mt = first_m + local % gm;
     nt = local / gm;
+}
+
+__device__ __forceinline__ void raster_tile(int tile, const GemmArgs &a, int &mt, int &nt)
+{
+    raster_tile(tile, a.raster_group, a.num_m_tiles, a.num_n_tiles, mt, nt);
 }
 
 // Bounded wait with no status side effect, used only while draining.
@@ -63,17 +69,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 // ---------------------------------------------------------------------------
 
 // Per-row operands of computed row `row`: gamma (1 without one) and the row
-// of D it is written to (-1: none -- a row past M, or a scatter index
-// outside [0, m_out)).
+// of D it is written to (-1: none -- a row at or past row_end (M, or the end
+// of a grouped GEMM's slice), or a scatter index outside [0, m_out)).
 struct RowEpi {
     float gamma;
     int dst;
 };
 
-__device__ __forceinline__ RowEpi load_row_epi(const GemmArgs &a, int row)
+__device__ __forceinline__ RowEpi load_row_epi(const GemmArgs &a, int row, int row_end)
 {
     RowEpi e{1.0f, -1};
-    if (row < a.M) {
+    if (row < row_end) {
         if (a.gamma)
             e.gamma = __ldg(a.gamma + row);
         e.dst = row;
@@ -100,11 +106,11 @@ __device__ __forceinline__ float epi_gamma(const GemmArgs &a, int m)
 // The bias of columns [x0, x0 + ncols) into L1, 64 bytes per lane, issued
 // before the accumulator wait: the epilogue's bias loads then hit L1 instead
 // of waiting on L2 between the TMEM read and the TMEM release.
-__device__ __forceinline__ void prefetch_bias(const GemmArgs &a, int x0, int ncols, int lane)
+__device__ __forceinline__ void prefetch_bias(const float *bias, int N, int x0, int ncols, int lane)
 {
     const int c = x0 + 16 * lane;
-    if (a.bias && 16 * lane < ncols && c < a.N)
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(a.bias + c));
+    if (bias && 16 * lane < ncols && c < N)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(bias + c));
 }
 
 // Bias of columns [col, col + 32) as 8 float4. bias + col is 16-byte
@@ -156,7 +162,8 @@ __device__ __forceinline__ void convert32(const uint32_t (&v)[32], uint32_t *pk,
 }
 
 // The epilogue-variant conversion of 64 accumulator columns of one row (two
-// 32-column reads) starting at output column x. Each case takes as few
+// 32-column reads) starting at output column x; bias is the row's bias
+// vector (a grouped GEMM's slice's), or null. Each case takes as few
 // instructions per element as it can, on uniform branches:
 //   no bias:  bf16(acc * (scale * gamma))           (gamma folded into the
 //             row's scale: one multiply, as the plain epilogue)
@@ -164,9 +171,10 @@ __device__ __forceinline__ void convert32(const uint32_t (&v)[32], uint32_t *pk,
 // The FP32 evaluation order is the kernel's; it differs from the exact
 // gamma * (alpha * acc + bias) only by FP32 rounding before the BF16 one.
 __device__ __forceinline__ void convert64_epi(const uint32_t (&v0)[32], const uint32_t (&v1)[32], uint32_t (&pk)[32],
-                                              float scale, const RowEpi &re, const GemmArgs &a, int x)
+                                              float scale, const RowEpi &re, const GemmArgs &a, const float *bias,
+                                              int x)
 {
-    if (!a.bias) {
+    if (!bias) {
         const float sg = scale * re.gamma;
         convert32(v0, pk, sg);
         convert32(v1, pk + 16, sg);
@@ -178,9 +186,9 @@ __device__ __forceinline__ void convert64_epi(const uint32_t (&v0)[32], const ui
     for (int h = 0; h < 2; ++h) {
         const uint32_t(&v)[32] = h ? v1 : v0;
         if (full)
-            load_bias32<true>(a.bias, x + 32 * h, a.N, b);
+            load_bias32<true>(bias, x + 32 * h, a.N, b);
         else
-            load_bias32<false>(a.bias, x + 32 * h, a.N, b);
+            load_bias32<false>(bias, x + 32 * h, a.N, b);
         if (a.gamma)
             convert32_bias<true>(v, pk + 16 * h, scale, re.gamma, b);
         else

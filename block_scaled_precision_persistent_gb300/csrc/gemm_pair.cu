@@ -342,8 +342,8 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
             const int x0 = nt * BN + h * COLS_PER_WARP;            // first column of this warp
             RowEpi re{1.0f, -1};
             if constexpr (EPI) {
-                re = load_row_epi(args, pm * T::TILE_M + (int)rank * T::BM + q * 32 + lane);
-                prefetch_bias(args, x0, COLS_PER_WARP, lane);
+                re = load_row_epi(args, pm * T::TILE_M + (int)rank * T::BM + q * 32 + lane, args.M);
+                prefetch_bias(args.bias, args.N, x0, COLS_PER_WARP, lane);
             }
             if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
                 break;
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
             auto convert_chunk = [&](int ch, const uint32_t (&v0)[32], const uint32_t (&v1)[32],
                                      uint32_t (&pk)[32]) {
                 if constexpr (EPI) {
-                    convert64_epi(v0, v1, pk, scale, re, args, x0 + ch * T::EPI_COLS);
+                    convert64_epi(v0, v1, pk, scale, re, args, args.bias, x0 + ch * T::EPI_COLS);
                 } else {
                     convert32(v0, pk, scale);
                     convert32(v1, pk + 16, scale);

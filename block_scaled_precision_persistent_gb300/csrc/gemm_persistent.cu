@@ -27,6 +27,7 @@
 
 #include "bsg_internal.h"
 #include "gemm_common.cuh"
+#include "group.cuh"
 #include "ptx.cuh"
 
 namespace bsg {
@@ -77,14 +78,20 @@ struct Tile {
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
 };
 
-// EPI: the epilogue-variant instantiation (bias, gamma, scattered rows).
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool EPI>
+// MODE: kModePlain, kModeEpi (bias, gamma, scattered rows) or kModeGrouped
+// (the grouped GEMM over ragged row slices, NVFP4 only, with the variants'
+// epilogue).
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MODE>
 __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmD, const GemmArgs args)
 {
     using T = Tile<KIND, BN, STAGES, NUM_ACC>;
+    constexpr bool EPI = MODE != kModePlain;
+    constexpr bool GROUPED = MODE == kModeGrouped;
+    static_assert(!GROUPED || (T::kFp4 && T::SMEM_BYTES + kGroupTableBytes <= 232448),
+                  "grouped GEMM: NVFP4 plans whose shared memory has room for the slice table");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -101,6 +108,9 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     const uint32_t sffull0 = sfready0 + 8u * STAGES;          // [STAGES] scale loads -> scale warps
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // grouped: slice boundaries and first 128-row tile of each slice (group.cuh)
+    int *const s_go = reinterpret_cast<int *>(tmem_slot + 4);
+    int *const s_gb = s_go + (kMaxGroups + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -131,12 +141,30 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
         tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
         tmem_relinquish();
     }
+    if constexpr (GROUPED) {
+        if (warp == 2)
+            build_group_table(args.group_offs, args.num_groups, args.M, s_go, s_gb, lane);
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int num_tiles = args.num_m_tiles * args.num_n_tiles;
+    // grouped: one 128-row tile row per 128 rows of each slice
+    const int num_m_tiles = GROUPED ? s_gb[args.num_groups] : args.num_m_tiles;
+    const int num_tiles = num_m_tiles * args.num_n_tiles;
     const int nkb = args.num_k_blocks;
+    // m tile -> its slice, first row of A, end of the slice's rows
+    auto tile_rows = [&](int mt, int &g, int &row0, int &row_end) {
+        if constexpr (GROUPED) {
+            g = group_of_block(s_gb, args.num_groups, mt);
+            row0 = s_go[g] + (mt - s_gb[g]) * T::BM;
+            row_end = s_go[g + 1];
+        } else {
+            g = 0;
+            row0 = mt * T::BM;
+            row_end = args.M;
+        }
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------------
@@ -147,8 +175,10 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
             uint32_t phase = 0, armed_mask = 0, armed_parity = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                int mt, nt;
-                raster_tile(tile, args, mt, nt);
+                int mt, nt, g, row0, row_end;
+                raster_tile(tile, args.raster_group, num_m_tiles, args.num_n_tiles, mt, nt);
+                tile_rows(mt, g, row0, row_end);
+                const uint8_t *const sfb_g = args.sfb + (size_t)g * args.sfb_group_bytes;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wd, abort_flag, 1)) {
                         ok = false;
@@ -172,13 +202,13 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                         for (int c = 0; c < nchunks; ++c) {
                             const size_t rb = (size_t)nt * T::SFB_CHUNKS + (size_t)c;
                             bulk_load(ssfa + T::SFA_BYTES + c * T::SF_BLOCK_BYTES,
-                                      args.sfb + (rb * args.sf_col_blocks + cb) * 512u,
+                                      sfb_g + (rb * args.sf_col_blocks + cb) * 512u,
                                       T::SF_BLOCK_BYTES, sfb);
                         }
                     }
                     mbar_arrive_expect_tx(fb, T::A_BYTES + T::B_BYTES);
-                    tma_load_2d(sa, &tmA, fb, kb * T::ROW_BYTES, mt * T::BM);
-                    tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN);
+                    tma_load_2d(sa, &tmA, fb, kb * T::ROW_BYTES, row0);
+                    tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, g * args.N + nt * BN);
                     armed_mask |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -258,8 +288,12 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                 }
             }
             // every MMA and copy issued above completes before TMEM is freed
-            tc_commit(drain_bar);
-            mbar_wait_quiet(drain_bar, 0, wd.limit_ns);
+            // (a grouped GEMM's grid is sized for a bound on its tiles: a CTA
+            // past the actual ones issued nothing and has nothing to drain)
+            if ((int)blockIdx.x < num_tiles) {
+                tc_commit(drain_bar);
+                mbar_wait_quiet(drain_bar, 0, wd.limit_ns);
+            }
         }
     } else if (warp < T::EPI_WARP0) {
         // ------------------------------------------------------------------
@@ -316,12 +350,18 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
         int acc = 0, buf = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            int mt, nt;
-            raster_tile(tile, args, mt, nt);
+            int mt, nt, g, row0, row_end;
+            raster_tile(tile, args.raster_group, num_m_tiles, args.num_n_tiles, mt, nt);
+            tile_rows(mt, g, row0, row_end);
+            const float *const bias = args.bias ? args.bias + (size_t)g * args.N : nullptr;
+            const int y = row0 + q * 32;              // first row of this warp's 32
+            // rows of the warp that TMA could store past the slice's end: the
+            // warp stores its rows one by one instead (as scattered rows)
+            const bool per_row = EPI && (args.scatter || (GROUPED && y + 32 > row_end));
             RowEpi re{1.0f, -1};
             if constexpr (EPI) {
-                re = load_row_epi(args, mt * T::BM + q * 32 + lane);
-                prefetch_bias(args, nt * BN, BN, lane);
+                re = load_row_epi(args, y + lane, row_end);
+                prefetch_bias(bias, args.N, nt * BN, BN, lane);
             }
             if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
                 break;
@@ -350,7 +390,7 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                 // 128-byte swizzle: 16-byte chunk c of row r lands at chunk c ^ (r % 8)
                 if constexpr (EPI) {
                     uint32_t pk[32];
-                    convert64_epi(v0, v1, pk, scale, re, args, x);
+                    convert64_epi(v0, v1, pk, scale, re, args, bias, x);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         st_shared_v4(row + ((uint32_t)(c ^ (lane & 7)) << 4), pk[4 * c], pk[4 * c + 1],
@@ -371,14 +411,13 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                                      pack_bf16x2(__uint_as_float(v1[8 * c + 4]) * scale, __uint_as_float(v1[8 * c + 5]) * scale),
                                      pack_bf16x2(__uint_as_float(v1[8 * c + 6]) * scale, __uint_as_float(v1[8 * c + 7]) * scale));
                 }
-                if (EPI && args.scatter) {
+                if (per_row) {
                     __syncwarp();
                     scatter_chunk(gbase + (sbuf - base), re.dst, args.d, args.N, x, lane);
                 } else {
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        const int y = mt * T::BM + q * 32;
                         if (x < args.N && y < args.M)
                             tma_store_2d(&tmD, sbuf, x, y);
                         bulk_commit_group();
@@ -411,19 +450,32 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
 // ---------------------------------------------------------------------------
 // Plans: the compiled configurations and their host launchers
 // ---------------------------------------------------------------------------
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MODE>
+static cudaError_t launch_mode(const GemmMaps &maps, const GemmArgs &args, int grid, cudaStream_t stream)
+{
+    using T = Tile<KIND, BN, STAGES, NUM_ACC>;
+    constexpr int smem = T::SMEM_BYTES + (MODE == kModeGrouped ? kGroupTableBytes : 0);
+    auto kern = gemm_persistent_kernel<KIND, BN, STAGES, NUM_ACC, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<grid, T::THREADS, smem, stream>>>(maps.a, maps.b, maps.d, args);
+    return cudaGetLastError();
+}
+
 template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 static cudaError_t launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
                                cudaStream_t stream)
 {
-    using T = Tile<KIND, BN, STAGES, NUM_ACC>;
-    auto kern = has_epilogue(args) ? gemm_persistent_kernel<KIND, BN, STAGES, NUM_ACC, true>
-                                   : gemm_persistent_kernel<KIND, BN, STAGES, NUM_ACC, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         T::SMEM_BYTES);
-    if (e != cudaSuccess)
-        return e;
-    kern<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(maps.a, maps.b, maps.d, args);
-    return cudaGetLastError();
+    if (args.group_offs) {
+        if constexpr (KIND == Kind::NVFP4)
+            return launch_mode<KIND, BN, STAGES, NUM_ACC, kModeGrouped>(maps, args, grid, stream);
+        else
+            return cudaErrorInvalidValue;          // grouped GEMMs are NVFP4 only
+    }
+    if (has_epilogue(args))
+        return launch_mode<KIND, BN, STAGES, NUM_ACC, kModeEpi>(maps, args, grid, stream);
+    return launch_mode<KIND, BN, STAGES, NUM_ACC, kModePlain>(maps, args, grid, stream);
 }
 
 template <Kind KIND, int BN, int STAGES, int NUM_ACC>

@@ -15,6 +15,7 @@
 // stages 128 rows x 64 scale columns in shared memory with coalesced reads and
 // writes 16 contiguous 512-byte blocks. HBM-bound; bytes in = bytes out.
 #include "bsg_internal.h"
+#include "group.cuh"
 #include "ptx.cuh"
 
 namespace bsg {
@@ -23,9 +24,13 @@ constexpr int kSwzBlocksPerCta = 16;        // 4-column blocks per CTA (64 scale
 constexpr int kSwzThreads = 256;
 constexpr int kSwzPitchWords = 17;          // 16 words per staged row + 1 (bank spread)
 
+// GROUPED: the rows are E slices (offs, device); slice e is swizzled on its
+// own from block row sb[e] on (group.cuh), and block rows past the slices'
+// (grid y covers ceil(rows / 128) + E) are written as zeros.
+template <bool GROUPED>
 __global__ void __launch_bounds__(kSwzThreads)
     swizzle_scales_kernel(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int rows,
-                          int cols, int ncb, int vec16)
+                          int cols, int ncb, int vec16, const int *offs, int E)
 {
     __shared__ uint32_t tile[128 * kSwzPitchWords];
     uint8_t *t8 = reinterpret_cast<uint8_t *>(tile);
@@ -33,6 +38,20 @@ __global__ void __launch_bounds__(kSwzThreads)
     const int cb0 = blockIdx.x * kSwzBlocksPerCta;
     const int c0 = cb0 * 4;
     const int span = kSwzBlocksPerCta * 4;  // 64 scale columns
+    int row0 = rb * 128, row_end = rows;    // source rows of this block row: [row0, row_end)
+    if constexpr (GROUPED) {
+        __shared__ int so[kMaxGroups + 1], sb[kMaxGroups + 1];
+        if (threadIdx.x < 32)
+            build_group_table(offs, E, rows, so, sb, threadIdx.x);
+        __syncthreads();
+        if (rb < sb[E]) {
+            const int e = group_of_block(sb, E, rb);
+            row0 = so[e] + (rb - sb[e]) * 128;
+            row_end = so[e + 1];
+        } else {
+            row0 = row_end = 0;             // past the slices: zeros
+        }
+    }
 
     if (vec16) {
         // 16-byte loads (host-checked: 16-byte aligned base, cols % 16 == 0):
@@ -40,9 +59,9 @@ __global__ void __launch_bounds__(kSwzThreads)
         // past the matrix
         for (int i = threadIdx.x; i < 128 * (span / 16); i += kSwzThreads) {
             const int r = i >> 2, q = i & 3;
-            const int row = rb * 128 + r, col = c0 + 16 * q;
+            const int row = row0 + r, col = c0 + 16 * q;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (row < rows && col < cols)
+            if (row < row_end && col < cols)
                 v = __ldg(reinterpret_cast<const uint4 *>(in + (size_t)row * (size_t)cols + (size_t)col));
             uint32_t *w = tile + r * kSwzPitchWords + 4 * q;
             w[0] = v.x;
@@ -53,9 +72,9 @@ __global__ void __launch_bounds__(kSwzThreads)
     } else {
         for (int i = threadIdx.x; i < 128 * span; i += kSwzThreads) {
             const int r = i / span, b = i % span;
-            const int row = rb * 128 + r, col = c0 + b;
+            const int row = row0 + r, col = c0 + b;
             uint8_t v = 0;
-            if (row < rows && col < cols)
+            if (row < row_end && col < cols)
                 v = in[(size_t)row * (size_t)cols + (size_t)col];
             t8[r * (kSwzPitchWords * 4) + b] = v;
         }
@@ -83,7 +102,19 @@ cudaError_t launch_swizzle_scales(int rows, int K, const uint8_t *sf, uint8_t *o
     const int nrb = (rows + 127) / 128;
     dim3 grid((ncb + kSwzBlocksPerCta - 1) / kSwzBlocksPerCta, nrb);
     const int vec16 = (cols % 16) == 0 && (reinterpret_cast<uintptr_t>(sf) & 15u) == 0;
-    swizzle_scales_kernel<<<grid, kSwzThreads, 0, stream>>>(sf, out, rows, cols, ncb, vec16);
+    swizzle_scales_kernel<false><<<grid, kSwzThreads, 0, stream>>>(sf, out, rows, cols, ncb, vec16, nullptr, 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swizzle_scales_grouped(int E, int rows, int K, const int *offs, const uint8_t *sf,
+                                          uint8_t *out, cudaStream_t stream)
+{
+    const int cols = K / 16;
+    const int ncb = (cols + 3) / 4;
+    const int nrb = (rows + 127) / 128 + E;     // bound on the slices' block rows
+    dim3 grid((ncb + kSwzBlocksPerCta - 1) / kSwzBlocksPerCta, nrb);
+    const int vec16 = (cols % 16) == 0 && (reinterpret_cast<uintptr_t>(sf) & 15u) == 0;
+    swizzle_scales_kernel<true><<<grid, kSwzThreads, 0, stream>>>(sf, out, rows, cols, ncb, vec16, offs, E);
     return cudaGetLastError();
 }
 

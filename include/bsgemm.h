@@ -207,6 +207,53 @@ BSG_API int fp8_gemm_ex(int M, int N, int K,
                         const int32_t *scatter, int m_out, void *D, bsg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Grouped (ragged, routed) NVFP4 GEMM -- the MoE expert matmul ("Triton
+ * #11171 - Why Two New NVFP4 Test Cases Produced Twelve Tensor-Memory
+ * Failures", section "Ragged mode added routing rather than a plain matrix":
+ * routed activation rows form slices, and each slice is multiplied by the
+ * dense right-hand side of its own slice):
+ *   for each slice e in [0, E) and offs[e] <= m < offs[e+1]:
+ *     D[dst(m)][n] = bf16_rn( gamma[m] * (alpha * sum_k a(m,k) sA * b_e(n,k) sB_e + bias[e][n]) )
+ * with dst / gamma / scatter / m_out exactly as nvfp4_gemm_ex.
+ *   A       : uint8[M][K/2], rows grouped by slice (slice e = rows offs[e] .. offs[e+1]-1)
+ *   sfA_swz : A's scales in the per-slice layout of nvfp4_swizzle_scales_grouped
+ *   B       : uint8[E][N][K/2], the slices' right-hand sides
+ *   sfB_swz : E swizzled scale sets of N rows, each nvfp4_swizzled_scale_bytes(N, K)
+ *             bytes, back to back (nvfp4_swizzle_scales on the [E*N][K/16] matrix
+ *             gives exactly this when N % 128 == 0)
+ *   offs    : DEVICE int32[E+1], 4-byte aligned: offs[0] = 0, nondecreasing,
+ *             offs[E] = M. Read on the GPU (no host synchronisation). Any other
+ *             sequence is clamped there to a nondecreasing one in [0, M], so
+ *             that nothing is read or written out of bounds; its result is
+ *             unspecified.
+ *   bias    : DEVICE float[E][N], 16-byte aligned, or NULL
+ * 1 <= E <= 1024 slices; slices may be empty. Sizes, alignment and errors as
+ * nvfp4_gemm_ex. One launch; allocates nothing.
+ * ------------------------------------------------------------------------- */
+BSG_API int nvfp4_grouped_gemm(int E, int M, int N, int K,
+                               const void *A, const void *sfA_swz,
+                               const void *B, const void *sfB_swz,
+                               const int32_t *offs, float alpha,
+                               const float *bias, const float *gamma,
+                               const int32_t *scatter, int m_out, void *D, bsg_stream_t stream);
+
+/* Scale layout of a grouped A: row-major uint8[M][K/16] scales -> the
+ * swizzled layout of nvfp4_swizzle_scales applied to each slice on its own,
+ * slice e starting at 128-row block row sum_{e'<e} ceil(rows_e' / 128), so
+ * that every 128-row tile of one slice reads one block row. offs as for
+ * nvfp4_grouped_gemm (device, read on the GPU). sf_swz must hold
+ * nvfp4_grouped_scale_bytes(E, M, K) bytes, 16-byte aligned; block rows past
+ * the slices' are written as zeros. Requires M >= 1, K % 16 == 0, 1 <= E <=
+ * 1024. Bit-exact byte permutation.                                        */
+BSG_API int nvfp4_swizzle_scales_grouped(int E, int M, int K, const int32_t *offs, const void *sf,
+                                         void *sf_swz, bsg_stream_t stream);
+
+/* Bytes of the grouped layout: (ceil(M/128) + E) block rows of 128 rows x
+ * K/16 (padded to 4) scales -- a bound on any split of M rows into E
+ * slices (0 for invalid sizes). Host only.                                 */
+BSG_API size_t nvfp4_grouped_scale_bytes(int E, int M, int K);
+
+/* ---------------------------------------------------------------------------
  * Runtime control
  * ------------------------------------------------------------------------- */
 

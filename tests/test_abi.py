@@ -178,3 +178,31 @@ def test_epilogue_bad_args(lib):
         bsg.BSG_ERR_MISALIGNED
     assert lib.nvfp4_gemm_ex(128, 64, 256, BAD, BAD, BAD, BAD, 1.0, None, None, None, 128, None, None) == \
         bsg.BSG_ERR_INVALID_ARG                                                # no D
+
+
+def test_grouped_bad_args(lib):
+    """nvfp4_grouped_gemm / nvfp4_swizzle_scales_grouped reject bad slice
+    counts, missing offsets and misalignment before any launch."""
+    g = lambda E, offs, *rest: lib.nvfp4_grouped_gemm(E, 128, 64, 256, BAD, BAD, BAD, BAD, offs, 1.0,  # noqa: E731
+                                                      *rest)
+    ok_epi = (None, None, None, 128, BAD, None)
+    assert g(0, BAD, *ok_epi) == bsg.BSG_ERR_INVALID_ARG                     # no slices
+    assert g(1025, BAD, *ok_epi) == bsg.BSG_ERR_INVALID_ARG                  # too many slices
+    assert g(4, None, *ok_epi) == bsg.BSG_ERR_INVALID_ARG                    # no offsets
+    assert g(4, BAD + 2, *ok_epi) == bsg.BSG_ERR_MISALIGNED                  # offsets
+    assert g(4, BAD, None, None, None, 100, BAD, None) == bsg.BSG_ERR_INVALID_ARG   # m_out != M
+    assert g(4, BAD, BAD + 4, None, None, 128, BAD, None) == bsg.BSG_ERR_MISALIGNED  # bias
+    assert lib.nvfp4_grouped_gemm(4, 128, 60, 256, BAD, BAD, BAD, BAD, BAD, 1.0, *ok_epi) == \
+        bsg.BSG_ERR_INVALID_ARG                                               # N % 8
+    s = lib.nvfp4_swizzle_scales_grouped
+    assert s(0, 128, 256, BAD, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert s(4, 0, 256, BAD, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert s(4, 128, 24, BAD, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG       # K % 16
+    assert s(4, 128, 256, None, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert s(4, 128, 256, BAD, BAD, BAD + 8, None) == bsg.BSG_ERR_MISALIGNED
+    # bound: (ceil(M/128) + E) block rows of 128 x pad4(K/16)
+    assert bsg.nvfp4_grouped_scale_bytes(1, 128, 256) == 2 * 128 * 16
+    assert bsg.nvfp4_grouped_scale_bytes(3, 300, 1040) == (3 + 3) * 128 * 68
+    assert bsg.nvfp4_grouped_scale_bytes(0, 128, 256) == 0
+    import oracle
+    assert bsg.nvfp4_grouped_scale_bytes(5, 1000, 512) == oracle.get().grouped_scale_bytes(5, 1000, 512)

@@ -226,3 +226,68 @@ def make_epilogue(M: int, N: int, seed: int, m_out: int | None = None, drop: flo
     if drop > 0:
         scatter[torch.rand(M, generator=g) < drop] = -1
     return {k: v.to(device) for k, v in dict(bias=bias, gamma=gamma, scatter=scatter).items()}
+
+
+# --------------------------------------------------------------------------
+# Grouped (ragged, routed) GEMM inputs
+# --------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class GroupedWorkload:
+    """An MoE expert matmul: `tokens` tokens each routed to `top_k` distinct
+    experts out of `E` (uniformly, seeded), so M = tokens * top_k routed rows
+    in slices of ragged size; every expert's weights are N x K."""
+    name: str
+    E: int
+    tokens: int
+    top_k: int
+    N: int
+    K: int
+    index: int = 5
+
+    @property
+    def M(self) -> int:
+        return self.tokens * self.top_k
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    @property
+    def algorithmic_bytes(self) -> float:
+        """Packed A and all E weight matrices with their scales, BF16 D."""
+        return (self.M + self.E * self.N) * self.K * 9 / 16 + 2.0 * self.M * self.N
+
+
+GROUPED_WORKLOADS: dict[str, GroupedWorkload] = {
+    # 1024 tokens x top-8 of 64 experts (about 128 rows per expert), expert
+    # up-projection 4096 x 7168
+    "moe_e64_t1024_k8": GroupedWorkload("moe_e64_t1024_k8", 64, 1024, 8, 4096, 7168),
+}
+
+
+def routing(E: int, tokens: int, top_k: int, seed: int):
+    """Route each token to top_k distinct experts (uniform, seeded); the
+    routed rows sorted by (expert, token). Returns (offs int32[E+1], dst
+    int32[M]) where dst[row] = token * top_k + slot: the row's place in
+    token order (the scatter back from expert order)."""
+    g = _gen(SEED_BASE + 104729 * seed + E, "cpu")
+    choice = torch.stack([torch.randperm(E, generator=g)[:top_k] for _ in range(tokens)])   # [tokens, top_k]
+    expert = choice.reshape(-1)                        # row t*top_k + s -> expert
+    order = torch.sort(expert * tokens + torch.arange(tokens).repeat_interleave(top_k), stable=True).indices
+    counts = torch.bincount(expert, minlength=E)
+    offs = torch.zeros(E + 1, dtype=torch.int32)
+    offs[1:] = torch.cumsum(counts, 0).to(torch.int32)
+    return offs, order.to(torch.int32)
+
+
+def make_grouped(E: int, M: int, N: int, K: int, seed: int, device="cpu", std: float = 1.0) -> dict:
+    """A [M][K/2] + row-major sfA, B [E][N][K/2] + sfB [E][N][K/16] (one
+    two-level quantisation over all E * N weight rows, so one alpha serves
+    every slice), from N(0, std^2) through BF16."""
+    A, sfA, sga = nvfp4_quantise(normal_bf16(M, K, SEED_BASE + 7 * seed, std, device))
+    B, sfB, sgb = nvfp4_quantise(normal_bf16(E * N, K, SEED_BASE + 7 * seed + 1, std, device))
+    alpha = float(torch.tensor(1.0, dtype=torch.float32)
+                  / (torch.tensor(sga, dtype=torch.float32) * torch.tensor(sgb, dtype=torch.float32)))
+    return dict(E=E, M=M, N=N, K=K, A=A, sfA=sfA, B=B.reshape(E, N, K // 2), sfB=sfB.reshape(E, N, K // 16),
+                alpha=alpha)
