@@ -10,8 +10,9 @@ Prints ONE JSON line (rank 0). Besides the contract's keys it carries the
 dominant kernel's roofline (CUDA-event duration of the GEMM launches inside
 the timed region), the CPU oracle timed on a bounded sample, the clocks seen
 during the timed region, and secondary lines for the FP8 8192^3 GEMM, the
-skinny-M sweep (HBM GB/s), the scale swizzle, the NVFP4 quantiser and the
-fused epilogue variants (bias, gamma, scattered rows).
+skinny-M sweep (HBM GB/s), the scale swizzle, the NVFP4 quantiser, the
+fused epilogue variants (bias, gamma, scattered rows) and the grouped (MoE)
+GEMM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -443,6 +444,61 @@ def secondary_epilogue(dev, step: Nvfp4Step, steps: int, pk: dict, psrc: str) ->
                       "operands resident (16384^3 larger than L2; 4096^3 and the skinny cell L2-resident)"}
 
 
+class GroupedProblem:
+    """The MoE workload on the device: routing offsets, the per-slice
+    swizzled A scales, the experts' swizzled B scales, D in token order."""
+
+    def __init__(self, w, dev):
+        import block_scaled_precision_persistent_gb300 as bsg
+        self.bsg, self.w = bsg, w
+        offs, dst = workloads.routing(w.E, w.tokens, w.top_k, seed=1)
+        self.offs, self.dst = offs.to(dev), dst.to(dev)
+        p = workloads.make_grouped(w.E, w.M, w.N, w.K, seed=1, device=dev)
+        self.A, self.B, self.alpha = p["A"], p["B"], p["alpha"]
+        self.sa = torch.empty(bsg.nvfp4_grouped_scale_bytes(w.E, w.M, w.K), dtype=torch.uint8, device=dev)
+        bsg.nvfp4_swizzle_scales_grouped(w.E, w.M, w.K, self.offs, p["sfA"], self.sa)
+        # the experts' [E*N][K/16] scales swizzle as one matrix (N % 128 == 0)
+        assert w.N % 128 == 0
+        self.sb = torch.empty(w.E * bsg.nvfp4_swizzled_scale_bytes(w.N, w.K), dtype=torch.uint8, device=dev)
+        bsg.nvfp4_swizzle_scales(w.E * w.N, w.K, p["sfB"].reshape(w.E * w.N, -1), self.sb)
+        self.D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        del p
+
+    def __call__(self, scatter=True):
+        w = self.w
+        self.bsg.nvfp4_grouped_gemm(w.E, w.M, w.N, w.K, self.A, self.sa, self.B, self.sb, self.offs, self.alpha,
+                                    None, None, self.dst if scatter else None, w.M, self.D)
+
+
+def secondary_grouped(dev, steps: int, pk: dict, psrc: str) -> dict:
+    """The grouped (MoE) NVFP4 GEMM: 64 experts, 1024 tokens x top-8 (8192
+    routed rows, ~128 per expert), 4096 x 7168 weights per expert, D written
+    in token order (scatter) and in expert order. HBM-bound: algorithmic
+    bytes = packed A + all experts' packed weights and scales + BF16 D
+    (1.16 GB, of which the weights 1.09 GB), larger than L2. Timed as
+    interleaved CUDA graphs of back-to-back launches (graph_us)."""
+    import block_scaled_precision_persistent_gb300 as bsg
+    w = workloads.GROUPED_WORKLOADS["moe_e64_t1024_k8"]
+    g = GroupedProblem(w, dev)
+    times = graph_us({"scatter": lambda: g(True), "expert_order": lambda: g(False)}, 8, steps)
+    if bsg.bsg_get_device_status() != bsg.BSG_OK:
+        raise SystemExit("device status reported an error in the grouped GEMM timing")
+    out = {}
+    for k, us in times.items():
+        gbs = w.algorithmic_bytes / (us * 1e-6) / 1e9
+        out[k] = {"us": round(us, 2), "tflops": round(w.flops / (us * 1e-6) / 1e12, 1), "hbm_gbs": round(gbs, 1),
+                  "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+    ideal = max(w.algorithmic_bytes / (pk["hbm_gbs"] * 1e9), w.flops / (pk["bf16_tflops"] * FP4_PER_BF16 * 1e12))
+    g()
+    plan = bsg.bsg_last_plan_name()
+    del g
+    return {"workload": w.name, "E": w.E, "M": w.M, "N": w.N, "K": w.K, "plan": plan, "variants": out,
+            "ideal_us": round(ideal * 1e6, 2), "algorithmic_bytes": w.algorithmic_bytes, "peak_hbm_gbs": pk["hbm_gbs"],
+            "peak_source": psrc,
+            "timing": "CUDA graph of 8 back-to-back launches per variant, replayed in turn; median per launch"}
+
+
 def secondary_swizzle(dev, steps: int, pk: dict, psrc: str) -> dict:
     """The scale-layout prep alone (timed separately from the GEMM): one
     operand's row-major [16384][1024] E4M3 scales into the swizzled layout;
@@ -544,6 +600,7 @@ def run_ours(args, dist: Dist) -> None:
         secondary["swizzle"] = secondary_swizzle(dev, 20, pk, psrc)
         secondary["quantize"] = secondary_quantize(dev, 20, pk, psrc)
         secondary["epilogue"] = secondary_epilogue(dev, step, 10, pk, psrc)
+        secondary["grouped"] = secondary_grouped(dev, 15, pk, psrc)
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, host_copy(step), args.cpu_seconds)
@@ -621,14 +678,16 @@ def run_reference(args, dist: Dist) -> None:
 
 def run_case(args) -> None:
     """One GEMM shape alone (--case nvfp4:MxNxK or fp8:MxNxK, optionally a
-    forced --plan), or the NVFP4 quantiser on BF16 ROWSxK (--case quantize:ROWSxK): `warmup` untimed then `steps` timed launches, inputs
-    resident. Used for profiler captures of a single kernel and for ad-hoc
+    forced --plan), the NVFP4 quantiser on BF16 ROWSxK (--case
+    quantize:ROWSxK), or a grouped workload (--case grouped:NAME, e.g.
+    grouped:moe_e64_t1024_k8): `warmup` untimed then `steps` timed launches,
+    inputs resident. Used for profiler captures of a single kernel and for ad-hoc
     timings; prints one JSON line."""
     import __graft_entry__
     __graft_entry__.build()
     import block_scaled_precision_persistent_gb300 as bsg
     kind, shape = args.case.split(":")
-    dims = [int(x) for x in shape.lower().split("x")]
+    dims = [] if kind == "grouped" else [int(x) for x in shape.lower().split("x")]
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     s = torch.cuda.current_stream()
@@ -654,6 +713,30 @@ def run_case(args) -> None:
         moved = 2 * (2 * rows * K) + rows * K // 2 + bsg.nvfp4_swizzled_scale_bytes(rows, K)
         print(json.dumps({"case": args.case, "us": round(us, 2), "gb_s": round(moved / (us * 1e-6) / 1e9, 1)}),
               flush=True)
+        return
+    if kind == "grouped":
+        w = workloads.GROUPED_WORKLOADS[shape]
+        g = GroupedProblem(w, dev)
+        bsg.bsg_force_plan(args.plan)
+        try:
+            for _ in range(args.warmup):
+                g()
+            torch.cuda.synchronize()
+            evs = []
+            for _ in range(args.steps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                g()
+                b.record(s)
+                evs.append((a, b))
+            torch.cuda.synchronize()
+        finally:
+            bsg.bsg_force_plan(None)
+        if bsg.bsg_get_device_status() != bsg.BSG_OK:
+            raise SystemExit("device status reported an error")
+        us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+        print(json.dumps({"case": args.case, "us": round(us, 2),
+                          "gb_s": round(w.algorithmic_bytes / (us * 1e-6) / 1e9, 1)}), flush=True)
         return
     M, N, K = dims
     D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)

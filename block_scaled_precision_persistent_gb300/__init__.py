@@ -20,7 +20,7 @@ __all__ = [
     "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes",
     "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_watchdog_selftest", "bsg_force_plan",
-    "bsg_select_plan", "bsg_last_launch_count", "bsg_error_string", "EXPORTED_SYMBOLS",
+    "bsg_select_plan", "bsg_last_launch_count", "bsg_last_plan_name", "bsg_error_string", "EXPORTED_SYMBOLS",
     "BSG_OK", "BSG_ERR_INVALID_ARG", "BSG_ERR_MISALIGNED", "BSG_ERR_UNSUPPORTED_DEVICE",
     "BSG_ERR_NO_PLAN", "BSG_ERR_CUDA", "BSG_ERR_DEVICE_TIMEOUT", "BSG_ERR_OUT_OF_MEMORY",
     "BSG_ERR_EXCEEDS_SCRATCH", "BSG_NOALLOC_SCRATCH_BYTES",
@@ -64,6 +64,7 @@ _SIGNATURES = {
     "bsg_force_plan": (_i, [ctypes.c_char_p]),
     "bsg_select_plan": (_i, [_i, _i, _i, _i, _i, ctypes.c_char_p, ctypes.c_size_t]),
     "bsg_last_launch_count": (_i, []),
+    "bsg_last_plan_name": (ctypes.c_char_p, []),
     "bsg_error_string": (ctypes.c_char_p, [_i]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
@@ -232,6 +233,11 @@ def bsg_select_plan(kind: int, M: int, N: int, K: int, num_sms: int) -> str:
 
 def bsg_last_launch_count() -> int:
     return int(load().bsg_last_launch_count())
+
+
+def bsg_last_plan_name() -> str:
+    """Plan of the last GEMM launch on this thread ("" before any)."""
+    return load().bsg_last_plan_name().decode()
 
 
 def bsg_error_string(code: int) -> str:

@@ -31,6 +31,7 @@ std::mutex g_mu;
 int g_forced_plan = -1;                 // guarded by g_mu
 thread_local uint32_t t_last_status_word = 0;
 thread_local int t_last_launches = 0;
+thread_local const char *t_last_plan = "";      // plan of the last GEMM launch on this thread
 
 struct DeviceState {
     bool init = false;
@@ -255,6 +256,7 @@ int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A,
     if (bsg::skinny_launch(id, maps, a, splits, stream) != cudaSuccess)
         return BSG_ERR_CUDA;
     ++t_last_launches;
+    t_last_plan = pi.name;
     return BSG_OK;
 }
 
@@ -324,6 +326,7 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     if (e != cudaSuccess)
         return BSG_ERR_CUDA;
     ++t_last_launches;
+    t_last_plan = pi.name;
     return BSG_OK;
 }
 
@@ -394,6 +397,7 @@ int run_grouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, c
     if (bsg::launch_gemm(plan, maps, a, grid, stream) != cudaSuccess)
         return BSG_ERR_CUDA;
     ++t_last_launches;
+    t_last_plan = pi.name;
     return BSG_OK;
 }
 
@@ -775,6 +779,8 @@ int bsg_select_plan(int kind, int M, int N, int K, int num_sms, char *name, size
 }
 
 int bsg_last_launch_count(void) { return t_last_launches; }
+
+const char *bsg_last_plan_name(void) { return t_last_plan; }
 
 const char *bsg_error_string(int code)
 {

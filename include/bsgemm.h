@@ -292,6 +292,10 @@ BSG_API int bsg_select_plan(int kind, int M, int N, int K, int num_sms,
  * (swizzle passes included).                                               */
 BSG_API int bsg_last_launch_count(void);
 
+/* Plan name of the last GEMM kernel launched on this thread ("" before any;
+ * a static string owned by the library).                                   */
+BSG_API const char *bsg_last_plan_name(void);
+
 /* Human-readable name of a status code.                                    */
 BSG_API const char *bsg_error_string(int code);
 
