@@ -93,6 +93,10 @@ class Oracle:
         L.bso_swizzled_scale_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
         L.bso_swizzle_scales.restype = ctypes.c_int
         L.bso_swizzle_scales.argtypes = [ctypes.c_int, ctypes.c_int, u8p, u8p]
+        L.bso_nvfp4_dense_gemm.restype = ctypes.c_int
+        L.bso_nvfp4_dense_gemm.argtypes = [ctypes.c_int] * 3 + [u8p, u8p, u16p, ctypes.c_float, f32p, f32p,
+                                                                i32p, ctypes.c_int, i32p, ctypes.c_int, f64p, f64p,
+                                                                u16p, ctypes.c_int]
         L.bso_nvfp4_grouped_gemm.restype = ctypes.c_int
         L.bso_nvfp4_grouped_gemm.argtypes = [ctypes.c_int] * 4 + [u8p] * 4 + [i32p, ctypes.c_float, f32p, f32p,
                                                                          f64p, f64p, u16p, ctypes.c_int]
@@ -193,6 +197,32 @@ class Oracle:
                                    nthreads or default_threads())
         if rc != 0:
             raise ValueError(f"bso_fp8_gemm rejected its arguments (rc={rc})")
+        return S, T, D
+
+    def nvfp4_dense_gemm(self, A, sfA, B_bf16_bits, alpha, K, rows=None, cols=None, nthreads=None,
+                         bias=None, gamma=None):
+        """NVFP4 x dense-BF16 GEMM: A uint8[M, K/2] with sfA uint8[M, K/16],
+        B uint16[N, K] BF16 bit patterns. Returns (S, T, D_bits) over the
+        selected rows x cols, with the epilogue of nvfp4_gemm."""
+        A = np.ascontiguousarray(A, dtype=np.uint8)
+        sfA = np.ascontiguousarray(sfA, dtype=np.uint8)
+        B = np.ascontiguousarray(B_bf16_bits, dtype=np.uint16)
+        M, N = A.shape[0], B.shape[0]
+        assert A.shape == (M, K // 2) and sfA.shape == (M, K // 16) and B.shape == (N, K)
+        bias, gamma = self._vec(bias, N), self._vec(gamma, M)
+        r, nr = self._sel(rows, M)
+        c, nc = self._sel(cols, N)
+        S = np.empty((nr, nc), np.float64)
+        T = np.empty((nr, nc), np.float64)
+        D = np.empty((nr, nc), np.uint16)
+        rc = self.lib.bso_nvfp4_dense_gemm(M, N, K, self._p(A, ctypes.c_uint8), self._p(sfA, ctypes.c_uint8),
+                                           self._p(B, ctypes.c_uint16), float(alpha), self._p(bias, ctypes.c_float),
+                                           self._p(gamma, ctypes.c_float), self._p(r, ctypes.c_int32), nr,
+                                           self._p(c, ctypes.c_int32), nc, self._p(S, ctypes.c_double),
+                                           self._p(T, ctypes.c_double), self._p(D, ctypes.c_uint16),
+                                           nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"bso_nvfp4_dense_gemm rejected its arguments (rc={rc})")
         return S, T, D
 
     def nvfp4_grouped_gemm(self, A, sfA, B, sfB, offs, alpha, K, bias=None, gamma=None, nthreads=None):

@@ -157,7 +157,7 @@ static unsigned nib_a(const uint8_t *row, int k)
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
-    int kind;                     /* 0 = NVFP4, 1 = FP8                      */
+    int kind;                     /* 0 = NVFP4, 1 = FP8, 2 = NVFP4 x BF16   */
     int M, N, K;
     const uint8_t *A, *sfA, *B, *sfB;
     double scale;                 /* alpha (NVFP4) or alpha*sA*sB (FP8)       */
@@ -271,6 +271,46 @@ static void epilogue(const job_t *jb, int i, int j, double *S, double *T)
     }
 }
 
+/* BF16 bit pattern -> its exact value (BF16 is the top half of binary32). */
+static double bf16_value(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* One output element of the NVFP4 x dense-BF16 GEMM: A block-scaled E2M1,
+ * B plain BF16 values (B holds uint16 bit patterns, [N][K]):
+ *   S = alpha * sum_b sA[i][b] * sum_t e2m1(A[i][16b+t]) * B[j][16b+t]    */
+static void dense_element(const job_t *jb, int i, int j, double *S, double *T)
+{
+    const int K = jb->K, nb = K / 16;
+    const uint8_t *ra = jb->A + (size_t)i * (size_t)(K / 2);
+    const uint8_t *sa = jb->sfA + (size_t)i * (size_t)nb;
+    const uint16_t *rb = (const uint16_t *)(const void *)jb->B + (size_t)j * (size_t)K;
+    double s = 0.0, t = 0.0;
+    for (int b = 0; b < nb; ++b) {
+        double blk = 0.0, blk_abs = 0.0;
+        for (int u = 0; u < 16; ++u) {
+            int k = 16 * b + u;
+            double p = jb->e2m1_tab[nib_a(ra, k)] * bf16_value(rb[k]);
+            blk += p;
+            blk_abs += fabs(p);
+        }
+#ifdef BSO_MUTANT_DENSE_DROP_SFA
+        double sc = 1.0;
+        (void)sa;
+#else
+        double sc = jb->e4m3_tab[sa[b]];
+#endif
+        s += sc * blk;
+        t += fabs(sc) * blk_abs;
+    }
+    *S = jb->scale * s;
+    *T = fabs(jb->scale) * t;
+}
+
 static void *worker(void *arg)
 {
     job_t *jb = (job_t *)arg;
@@ -281,8 +321,10 @@ static void *worker(void *arg)
             double S, T;
             if (jb->kind == 0)
                 nvfp4_element(jb, i, j, &S, &T);
-            else
+            else if (jb->kind == 1)
                 fp8_element(jb, i, j, &S, &T);
+            else
+                dense_element(jb, i, j, &S, &T);
             epilogue(jb, i, j, &S, &T);
             size_t o = (size_t)r * (size_t)jb->ncols + (size_t)c;
             if (jb->S) jb->S[o] = S;
@@ -392,6 +434,37 @@ int bso_fp8_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *B,
     jb.M = M; jb.N = N; jb.K = K;
     jb.A = A; jb.B = B;
     jb.scale = (double)alpha * (double)sA * (double)sB;
+    jb.bias = bias; jb.gamma = gamma;
+    jb.rows = rows; jb.nrows = nrows; jb.cols = cols; jb.ncols = ncols;
+    jb.S = S; jb.T = T; jb.D = D;
+    return run(&jb, nthreads);
+}
+
+/* NVFP4 x dense-BF16 GEMM ("Triton #11171 - Why Two New NVFP4 Test Cases
+ * Produced Twelve Tensor-Memory Failures", opening: an NVFP4-scaled
+ * activation times a dense BF16 or FP16 operand): A: uint8[M][K/2] E2M1
+ * codes with sfA: uint8[M][K/16] E4M3 block scales, B: uint16[N][K] BF16 bit
+ * patterns, each a plain value; bias / gamma as bso_nvfp4_gemm. The sum runs
+ * in double block by block (each product a * sA * b has at most 2 + 4 + 8
+ * significant bits, so it is exact), then the epilogue, then one BF16
+ * rounding.                                                                 */
+int bso_nvfp4_dense_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *sfA, const uint16_t *B,
+                         float alpha, const float *bias, const float *gamma,
+                         const int32_t *rows, int nrows, const int32_t *cols, int ncols,
+                         double *S, double *T, uint16_t *D, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || (K % 16) != 0)
+        return -1;
+    if (!rows) nrows = M;
+    if (!cols) ncols = N;
+    if (check_sel(rows, nrows, M) || check_sel(cols, ncols, N))
+        return -1;
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.kind = 2;
+    jb.M = M; jb.N = N; jb.K = K;
+    jb.A = A; jb.sfA = sfA; jb.B = (const uint8_t *)(const void *)B;
+    jb.scale = (double)alpha;
     jb.bias = bias; jb.gamma = gamma;
     jb.rows = rows; jb.nrows = nrows; jb.cols = cols; jb.ncols = ncols;
     jb.S = S; jb.T = T; jb.D = D;

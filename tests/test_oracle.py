@@ -10,7 +10,8 @@ nibbles in one operand, a dropped scale, a dropped block, a transposed operand, 
 scale layout; in the quantiser, ties rounded away from zero, a dropped global
 scale, swapped nibbles, block scales rounded up; in the epilogue, gamma
 applied before the bias, bias indexed by row; in the grouped GEMM, a slice
-multiplied by the next slice's right-hand side) and shows that at least one
+multiplied by the next slice's right-hand side; in the NVFP4 x dense GEMM,
+A's block scales dropped) and shows that at least one
 pin fails for each.
 """
 from __future__ import annotations
@@ -440,6 +441,48 @@ def pin_grouped_scale_layout(o):
     assert got[(2 * ncb + 1) * 512 + 5 * 16 + 2 * 4 + 1] == sf[199, 5]
 
 
+def pin_dense_worked(o):
+    """tests/golden/nvfp4_dense_case.txt: block-scaled E2M1 A times BF16 B."""
+    want = {int(r[1]): [float(v) for v in r[2:]] for r in _rows("nvfp4_dense_case.txt") if r[0] == "D"}
+    A = pack(np.array([[0x2] * 32, [k % 8 for k in range(32)]], np.uint8))
+    sfA = np.array([[0x40, 0x30], [0x38, 0x38]], np.uint8)
+    B = _bf16_bits([[0.25] * 16 + [-3.0] * 16, [1.5] * 32])
+    S, _, D = o.nvfp4_dense_gemm(A, sfA, B, 1.0, 32)
+    for i, row in want.items():
+        assert S[i].tolist() == row and oracle.bf16_bits_to_float(D[i]).tolist() == row, (i, S[i])
+
+
+def pin_dense_reduces_to_nvfp4(o):
+    # B's BF16 values exactly the E2M1 values of packed codes with unit
+    # scales: the dense GEMM is then the (pinned) NVFP4 GEMM with B's scales
+    # all 1.0, bit for bit.
+    M, N, K = 24, 40, 128
+    A, sfA, Bp, _ = _uniform_problem(M, N, K, 31)
+    codes = np.empty((N, K), np.uint8)
+    codes[:, 0::2], codes[:, 1::2] = Bp & 15, Bp >> 4
+    B_bf16 = _bf16_bits(np.array([E2M1_TABLE[c] for c in codes.reshape(-1)]).reshape(N, K))
+    ones = np.full((N, K // 16), 0x38, np.uint8)
+    S0, T0, D0 = o.nvfp4_gemm(A, sfA, Bp, ones, 0.75, K)
+    S1, T1, D1 = o.nvfp4_dense_gemm(A, sfA, B_bf16, 0.75, K)
+    assert np.array_equal(S0, S1) and np.array_equal(T0, T1) and np.array_equal(D0, D1)
+
+
+def pin_dense_numpy(o):
+    # Independent restatement: dequantised A (golden table, library E4M3)
+    # times the BF16 values of B (widened by bit shift), numpy float64.
+    M, N, K = 20, 36, 256
+    A, sfA, _, _ = _uniform_problem(M, N, K, 33)
+    B = _random_bf16(N, K, 34)
+    S, T, _ = o.nvfp4_dense_gemm(A, sfA, B, 1.25, K)
+    bv = _bits_to_f32(B).astype(np.float64)
+    ref = 1.25 * (deq_nvfp4(A, sfA) @ bv.T)
+    assert np.allclose(S, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert np.allclose(T, 1.25 * (np.abs(deq_nvfp4(A, sfA)) @ np.abs(bv).T), rtol=1e-12)
+    rows, cols = [19, 0, 7], [35, 2]
+    S2, _, _ = o.nvfp4_dense_gemm(A, sfA, B, 1.25, K, rows=rows, cols=cols)
+    assert np.array_equal(S2, S[np.ix_(rows, cols)])
+
+
 def _swizzle_numpy(sf: np.ndarray, K: int) -> np.ndarray:
     """Independent restatement of the 128x4-blocked scale layout by reshapes."""
     rows, cols = sf.shape
@@ -596,7 +639,8 @@ PINS = [pin_e2m1_table, pin_e4m3_codes, pin_bf16_cases, pin_worked_1x1x16, pin_w
         pin_fraction_exact, pin_fp8_numpy, pin_swizzle, pin_quantize_worked,
         pin_quantize_nearest_bruteforce, pin_quantize_scale_invariance, pin_quantize_amax_element,
         pin_quantize_dequant_bound, pin_epilogue_worked, pin_epilogue_numpy, pin_scatter_permutation,
-        pin_grouped_worked, pin_grouped_single_slice_is_plain, pin_grouped_numpy, pin_grouped_scale_layout]
+        pin_grouped_worked, pin_grouped_single_slice_is_plain, pin_grouped_numpy, pin_grouped_scale_layout,
+        pin_dense_worked, pin_dense_reduces_to_nvfp4, pin_dense_numpy]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -607,7 +651,7 @@ def test_oracle_pin(pin):
 MUTANTS = ["E2M1_BIAS0", "E2M1_NOSIGN", "E4M3_BIAS8", "SWAP_NIBBLES_A", "DROP_SFB",
            "DROP_LAST_BLOCK", "TRANSPOSE_B", "SWIZZLE_ROWMAJOR_BLOCK", "Q_TIES_AWAY", "Q_NO_SG",
            "Q_SWAP_NIBBLES", "Q_E4M3_CEIL", "EPI_GAMMA_FIRST", "EPI_BIAS_BY_ROW",
-           "GROUP_SHIFT"]
+           "GROUP_SHIFT", "DENSE_DROP_SFA"]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
