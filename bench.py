@@ -677,8 +677,8 @@ def run_reference(args, dist: Dist) -> None:
 
 
 def run_case(args) -> None:
-    """One GEMM shape alone (--case nvfp4:MxNxK or fp8:MxNxK, optionally a
-    forced --plan), the NVFP4 quantiser on BF16 ROWSxK (--case
+    """One GEMM shape alone (--case nvfp4:MxNxK, fp8:MxNxK or dense:MxNxK for
+    NVFP4 x dense BF16, optionally a forced --plan), the NVFP4 quantiser on BF16 ROWSxK (--case
     quantize:ROWSxK), or a grouped workload (--case grouped:NAME, e.g.
     grouped:moe_e64_t1024_k8): `warmup` untimed then `steps` timed launches,
     inputs resident. Used for profiler captures of a single kernel and for ad-hoc
@@ -753,6 +753,13 @@ def run_case(args) -> None:
 
         def call():
             bsg.nvfp4_gemm_ex(M, N, K, p["A"], sa, p["B"], sb, p["alpha"], eb, eg, es, M, D, s)
+    elif kind == "dense":
+        pd = workloads.make_dense(M, N, K, seed=1, device=dev)
+        sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+        bsg.nvfp4_swizzle_scales(M, K, pd["sfA"], sa, s)
+
+        def call():
+            bsg.nvfp4_dense_gemm(M, N, K, pd["A"], sa, pd["B"], pd["alpha"], None, None, None, M, D, s)
     elif kind == "fp8":
         q = workloads.make_fp8(workloads.WORKLOADS["fp8_8192"], dev, M=M, N=N, K=K)
 
@@ -773,8 +780,7 @@ def run_case(args) -> None:
             b.record(s)
             evs.append((a, b))
         torch.cuda.synchronize()
-        plan = bsg.bsg_select_plan(0 if kind == "nvfp4" else 1, M, N, K,
-                                   torch.cuda.get_device_properties(0).multi_processor_count)
+        plan = bsg.bsg_last_plan_name()
     finally:
         bsg.bsg_force_plan(None)
     if bsg.bsg_get_device_status() != bsg.BSG_OK:

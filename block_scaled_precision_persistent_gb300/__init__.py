@@ -17,7 +17,7 @@ from pathlib import Path
 __all__ = [
     "BsgError", "load", "nvfp4_gemm", "nvfp4_gemm_swizzled", "nvfp4_swizzle_scales", "nvfp4_quantize",
     "nvfp4_swizzled_scale_bytes", "nvfp4_gemm_noalloc", "fp8_gemm", "nvfp4_gemm_ex", "fp8_gemm_ex",
-    "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes",
+    "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes", "nvfp4_dense_gemm",
     "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_select_plan", "bsg_last_launch_count", "bsg_last_plan_name", "bsg_error_string", "EXPORTED_SYMBOLS",
@@ -52,6 +52,7 @@ _SIGNATURES = {
     "fp8_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "nvfp4_gemm_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "fp8_gemm_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
+    "nvfp4_dense_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "nvfp4_grouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp,
                                 _vp]),
     "nvfp4_swizzle_scales_grouped": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp]),
@@ -177,6 +178,13 @@ def fp8_gemm_ex(M, N, K, A, sA, B, sB, alpha, bias, gamma, scatter, m_out, D, st
     _check(load().fp8_gemm_ex(M, N, K, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), float(alpha), _ptr(bias),
                               _ptr(gamma), _ptr(scatter), int(m_out), _ptr(D), _stream(stream)),
            "fp8_gemm_ex")
+
+
+def nvfp4_dense_gemm(M, N, K, A, sfA_swz, B, alpha, bias, gamma, scatter, m_out, D, stream=None) -> None:
+    """NVFP4 activations (E2M1 codes + swizzled E4M3 scales) times dense BF16
+    weights B[N, K]; the epilogue as nvfp4_gemm_ex."""
+    _check(load().nvfp4_dense_gemm(M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), float(alpha), _ptr(bias), _ptr(gamma),
+                                   _ptr(scatter), int(m_out), _ptr(D), _stream(stream)), "nvfp4_dense_gemm")
 
 
 def nvfp4_grouped_gemm(E, M, N, K, A, sfA_swz, B, sfB_swz, offs, alpha, bias, gamma, scatter, m_out, D,

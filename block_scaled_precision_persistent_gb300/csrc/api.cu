@@ -123,6 +123,8 @@ int default_plan(Kind kind, int M, int N, int K, int num_sms)
             name = M <= 128 || few_tiles ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc2_256x128_s6_acc2";
         else
             name = M <= 128 ? "nvfp4_tc1_128x256_s3_acc1" : "nvfp4_tc2_256x256_s5_acc1";
+    } else if (kind == Kind::NVFP4_BF16) {
+        name = few_tiles || N <= 128 ? "nvfp4bf16_tc1_128x128_s5_acc2" : "nvfp4bf16_tc1_128x256_s3_acc2";
     } else {
         const bool small_m = M <= 128;   // a 256-row pair tile would idle half its SMs
         if (small_m)
@@ -270,16 +272,23 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     if (rc != BSG_OK)
         return rc;
     const PlanInfo &pi = bsg::plan_info(plan);
-    const uint64_t row_bytes = kind == Kind::NVFP4 ? (uint64_t)K / 2u : (uint64_t)K;
+    const bool dense = kind == Kind::NVFP4_BF16;
+    // bytes per row: packed E2M1 (K/2), E4M3 (K), or for the dense kind packed
+    // A and BF16 B (2K)
+    const uint64_t row_bytes = kind == Kind::FP8 ? (uint64_t)K : (uint64_t)K / 2u;
+    const uint64_t b_row_bytes = dense ? 2u * (uint64_t)K : row_bytes;
     if (pi.family == bsg::Family::SKINNY)
         return run_skinny(plan, pi, M, N, K, A, B, sfa, sfb, alpha, D, epi, stream, ds);
 
     GemmMaps maps;
     std::memset(&maps, 0, sizeof maps);
-    // A: 128 rows per CTA; B: the CTA's share of the tile's N rows
+    // A: 128 rows per CTA (dense: 32 bytes of codes per row and stage,
+    // unswizzled, expanded in shared memory); B: the CTA's share of the
+    // tile's N rows, 128 bytes per row and stage
     if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes,
-                        128, 128)) != BSG_OK ||
-        (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, (uint64_t)N, row_bytes,
+                        dense ? 32 : 128, 128,
+                        dense ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B)) != BSG_OK ||
+        (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, b_row_bytes, (uint64_t)N, b_row_bytes,
                         128, (uint32_t)(pi.bn / pi.cta_group))) != BSG_OK ||
         (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, d_rows(M, epi),
                         (uint64_t)N * 2u, 64, 32)) != BSG_OK)
@@ -700,6 +709,32 @@ int nvfp4_grouped_gemm(int E, int M, int N, int K, const void *A, const void *sf
                        reinterpret_cast<cudaStream_t>(stream), ds);
 }
 
+int nvfp4_dense_gemm(int M, int N, int K, const void *A, const void *sfA_swz, const void *B, float alpha,
+                     const float *bias, const float *gamma, const int32_t *scatter, int m_out, void *D,
+                     bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    if (!A || !sfA_swz || !B || !D)
+        return BSG_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 64 || (K % 64) != 0 || (N % 8) != 0)
+        return BSG_ERR_INVALID_ARG;
+    int rc = check_epilogue_args(M, bias, gamma, scatter, m_out);
+    if (rc != BSG_OK)
+        return rc;
+    if (!aligned16(A) || !aligned16(sfA_swz) || !aligned16(B) || !aligned16(D))
+        return BSG_ERR_MISALIGNED;
+    DeviceState *ds = nullptr;
+    if ((rc = current_device(&ds)) != BSG_OK)
+        return rc;
+    Epilogue e;
+    e.bias = bias;
+    e.gamma = gamma;
+    e.scatter = scatter;
+    e.m_out = m_out;
+    return run_gemm(Kind::NVFP4_BF16, M, N, K, A, B, static_cast<const uint8_t *>(sfA_swz), nullptr, nullptr,
+                    nullptr, alpha, D, reinterpret_cast<cudaStream_t>(stream), ds, e);
+}
+
 int bsg_reserve_workspace(int device, size_t bytes)
 {
     int prev = 0;
@@ -767,10 +802,10 @@ int bsg_force_plan(const char *name)
 
 int bsg_select_plan(int kind, int M, int N, int K, int num_sms, char *name, size_t name_len)
 {
-    if ((kind != 0 && kind != 1) || M < 1 || N < 1 || K < 1 || num_sms < 1 || !name || name_len == 0)
+    if (kind < 0 || kind > 2 || M < 1 || N < 1 || K < 1 || num_sms < 1 || !name || name_len == 0)
         return BSG_ERR_INVALID_ARG;
     int plan = -1;
-    int rc = choose_plan(kind == 0 ? Kind::NVFP4 : Kind::FP8, M, N, K, num_sms, &plan);
+    int rc = choose_plan(static_cast<Kind>(kind), M, N, K, num_sms, &plan);
     if (rc != BSG_OK)
         return rc;
     std::strncpy(name, bsg::plan_info(plan).name, name_len - 1);

@@ -9,7 +9,9 @@
 
 namespace bsg {
 
-enum class Kind : int { NVFP4 = 0, FP8 = 1 };
+// NVFP4: block-scaled E2M1 x E2M1; FP8: E4M3 x E4M3; NVFP4_BF16: block-scaled
+// E2M1 activations x dense BF16 weights.
+enum class Kind : int { NVFP4 = 0, FP8 = 1, NVFP4_BF16 = 2 };
 
 // Kernel families: persistent 1-SM tiles, persistent CTA-pair tiles, and the
 // swap-AB split-K kernel for skinny M.

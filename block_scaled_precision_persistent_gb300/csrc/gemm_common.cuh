@@ -217,6 +217,73 @@ __device__ __forceinline__ void scatter_chunk(const uint8_t *sbuf, int dst, uint
     }
 }
 
+// ---------------------------------------------------------------------------
+// NVFP4 -> BF16 expansion: the A operand of the NVFP4 x dense-BF16 GEMM. An
+// E2M1 value (at most 2 significant bits, |x| <= 6) times its E4M3 scale (at
+// most 4 significant bits, 2^-9 .. 448) has at most 6 significant bits and
+// lies in BF16's normal range, so the expanded operand is exact and the
+// BF16 MMA computes the definition up to the FP32 accumulation order.
+// ---------------------------------------------------------------------------
+
+// Four E2M1 codes (nibbles 0..3 of x, in element order) -> four BF16 values:
+// elements 0, 1 in w01 and 2, 3 in w23 (low half first). The magnitudes
+// 0 .5 1 1.5 2 3 4 6 are BF16 0x0000 0x3F00 0x3F80 0x3FC0 0x4000 0x4040
+// 0x4080 0x40C0; byte permutes pick their low and high bytes by the code's
+// three magnitude bits, a third and fourth interleave them, and the code's
+// sign bit becomes the BF16 sign.
+__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t x, uint32_t &w01, uint32_t &w23)
+{
+    const uint32_t sel = x & 0x7777u;
+    uint32_t lo, hi;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0xC0800000u), "r"(0xC0804000u), "r"(sel));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3F3F3F00u), "r"(0x40404040u), "r"(sel));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(w01) : "r"(lo), "r"(hi), "r"(0x5140u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(w23) : "r"(lo), "r"(hi), "r"(0x7362u));
+    w01 |= ((x & 0x8u) << 12) | ((x & 0x80u) << 24);
+    w23 |= ((x & 0x800u) << 4) | ((x & 0x8000u) << 16);
+}
+
+// An E4M3 scale code (sign bit ignored: scales are unsigned) -> its BF16
+// value in both halves. Normal codes map exponent e to e + 120 with the
+// three mantissa bits on top; subnormals are m * 2^-9.
+__device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t code)
+{
+    const uint32_t e = (code >> 3) & 15u, m = code & 7u;
+    const float f = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0x1p-9f;
+    const uint32_t b = __float_as_uint(f) >> 16;
+    return b | (b << 16);
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// One row of a 64-element stage: 32 packed bytes of E2M1 codes at src
+// (16-byte aligned; element 2i in the low nibble of byte i) and the row's
+// four block scales (byte b of sc scales elements 16b..16b+15) -> 64 BF16 in
+// row r of a 128B-swizzled K-major tile at shared address tile: 16-byte
+// chunk c (elements 8c..8c+7) at r * 128 + ((c ^ (r % 8)) * 16), the layout
+// the MMA's shared-memory descriptor reads.
+__device__ __forceinline__ void expand_row_nvfp4_bf16(const uint8_t *src, uint32_t sc, uint32_t tile, int r)
+{
+    const uint4 p0 = *reinterpret_cast<const uint4 *>(src);
+    const uint4 p1 = *reinterpret_cast<const uint4 *>(src + 16);
+    const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const uint32_t row = tile + (uint32_t)r * 128u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t s2 = e4m3_to_bf16x2((sc >> (8 * (c >> 1))) & 0xFFu);
+        uint32_t w0, w1, w2, w3;
+        e2m1x4_to_bf16(words[c] & 0xFFFFu, w0, w1);
+        e2m1x4_to_bf16(words[c] >> 16, w2, w3);
+        st_shared_v4(row + ((uint32_t)(c ^ (r & 7)) << 4), mul_bf16x2(w0, s2), mul_bf16x2(w1, s2),
+                     mul_bf16x2(w2, s2), mul_bf16x2(w3, s2));
+    }
+}
+
 // Writes one ring stage's NVFP4 block scales from shared memory into the
 // calling warp's TMEM sub-partition (taddr carries the warp's lane base).
 // The layout is the one the tensor core reads for a 128-row operand with one

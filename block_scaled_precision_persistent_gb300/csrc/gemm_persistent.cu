@@ -35,9 +35,13 @@ namespace bsg {
 template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 struct Tile {
     static constexpr bool kFp4 = KIND == Kind::NVFP4;
+    // NVFP4 activations x dense BF16 weights: A arrives as E2M1 codes plus
+    // block scales and is expanded to BF16 in shared memory by the four
+    // warps that write NVFP4 scales in the other kind (kind::f16 MMA)
+    static constexpr bool kDense = KIND == Kind::NVFP4_BF16;
     static constexpr int BM = 128;
     static constexpr int ROW_BYTES = 128;                 // K bytes of one row per stage
-    static constexpr int K_BLOCK = kFp4 ? 256 : 128;      // K elements per stage
+    static constexpr int K_BLOCK = kFp4 ? 256 : kDense ? 64 : 128;   // K elements per stage
     static constexpr int MMA_K_BYTES = 32;                // K bytes per tcgen05.mma
     static constexpr int MMAS = ROW_BYTES / MMA_K_BYTES;  // MMAs per stage
     static constexpr int A_BYTES = BM * ROW_BYTES;
@@ -47,7 +51,12 @@ struct Tile {
     static constexpr int SFB_CHUNKS = kFp4 ? BN / 128 : 0;
     static constexpr int SFA_BYTES = kFp4 ? SF_BLOCK_BYTES : 0;
     static constexpr int SFB_BYTES = SFB_CHUNKS * SF_BLOCK_BYTES;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    // dense: A's packed codes (128 rows x 32 bytes, TMA) and their scales
+    // (one 512-byte block of the swizzled layout: 128 rows x 4 scales)
+    static constexpr int APK_BYTES = kDense ? BM * 32 : 0;
+    static constexpr int ASF_BYTES = kDense ? 512 : 0;
+    static constexpr int STAGE_BYTES =
+        (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES + APK_BYTES + ASF_BYTES + 1023) / 1024 * 1024;
     static constexpr int EPI_WARPS = 4;
     static constexpr int EPI_COLS = 64;                   // BF16 columns per store box
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
@@ -69,7 +78,7 @@ struct Tile {
                                      : TMEM_USED <= 128 ? 128
                                      : TMEM_USED <= 256 ? 256
                                                         : 512;
-    static constexpr uint32_t IDESC = kFp4 ? idesc_nvfp4(BM, BN) : idesc_fp8(BM, BN);
+    static constexpr uint32_t IDESC = kFp4 ? idesc_nvfp4(BM, BN) : kDense ? idesc_bf16(BM, BN) : idesc_fp8(BM, BN);
 
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile N");
     static_assert(!kFp4 || BN % 128 == 0, "NVFP4 scale blocks cover 128 rows");
@@ -206,9 +215,21 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                                       T::SF_BLOCK_BYTES, sfb);
                         }
                     }
-                    mbar_arrive_expect_tx(fb, T::A_BYTES + T::B_BYTES);
-                    tma_load_2d(sa, &tmA, fb, kb * T::ROW_BYTES, row0);
-                    tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, g * args.N + nt * BN);
+                    if constexpr (T::kDense) {
+                        // A's codes and scales on the expansion barrier, B on the full one
+                        const uint32_t sfb = sffull0 + 8u * stage;
+                        const uint32_t sapk = sb + T::B_BYTES;
+                        mbar_arrive_expect_tx(sfb, T::APK_BYTES + T::ASF_BYTES);
+                        tma_load_2d(sapk, &tmA, sfb, kb * 32, row0);
+                        bulk_load(sapk + T::APK_BYTES, args.sfa + ((size_t)mt * args.sf_col_blocks + kb) * 512u,
+                                  T::ASF_BYTES, sfb);
+                        mbar_arrive_expect_tx(fb, T::B_BYTES);
+                        tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN);
+                    } else {
+                        mbar_arrive_expect_tx(fb, T::A_BYTES + T::B_BYTES);
+                        tma_load_2d(sa, &tmA, fb, kb * T::ROW_BYTES, row0);
+                        tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, g * args.N + nt * BN);
+                    }
                     armed_mask |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -222,7 +243,7 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                 for (int s = 0; s < STAGES; ++s)
                     if ((armed_mask >> s) & 1u) {
                         mbar_wait_quiet(full0 + 8u * s, (armed_parity >> s) & 1u, wd.limit_ns);
-                        if constexpr (T::kFp4)
+                        if constexpr (T::kFp4 || T::kDense)
                             mbar_wait_quiet(sffull0 + 8u * s, (armed_parity >> s) & 1u, wd.limit_ns);
                     }
             }
@@ -247,8 +268,9 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                         ok = false;
                         break;
                     }
-                    if constexpr (T::kFp4) {
-                        // the scale warps have written this stage's scales to TMEM
+                    if constexpr (T::kFp4 || T::kDense) {
+                        // the scale warps have written this stage's scales to
+                        // TMEM (NVFP4) / its expanded A to shared memory (dense)
                         if (!mbar_wait(sfready0 + 8u * stage, phase, wd, abort_flag, 5)) {
                             ok = false;
                             break;
@@ -266,6 +288,12 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                                       desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
                                       sfa_t + 4u * j, sfb_t + 4u * j * T::SFB_CHUNKS,
                                       (kb | j) != 0 ? 1u : 0u);
+                    } else if constexpr (T::kDense) {
+#pragma unroll
+                        for (int j = 0; j < T::MMAS; ++j)
+                            mma_bf16(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
+                                     desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                     (kb | j) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
@@ -323,6 +351,39 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                                                       lane);
                     tmem_st_wait();
                     tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(sfready0 + 8u * stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        } else if constexpr (T::kDense) {
+            // ----------------------------------------------------------------
+            // Expansion warps (NVFP4 x BF16): row r = 32 (warp % 4) + lane of
+            // the stage's A, from E2M1 codes and block scales to BF16 in the
+            // 128B-swizzled tile the MMA reads, then a proxy fence (generic
+            // writes -> tensor-core reads) and the stage's ready barrier
+            // ----------------------------------------------------------------
+            const int r = (warp & 3) * 32 + lane;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    // the stage's codes were reloaded after the MMAs that read
+                    // its previous expansion completed (empty -> producer)
+                    if (!warp_wait(sffull0 + 8u * stage, phase, wd, abort_flag, 6, lane)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t *apk = gbase + stage * T::STAGE_BYTES + T::A_BYTES + T::B_BYTES;
+                    const uint32_t sc = *reinterpret_cast<const uint32_t *>(apk + T::APK_BYTES + (r & 31) * 16 +
+                                                                             (r >> 5) * 4);
+                    expand_row_nvfp4_bf16(apk + r * 32, sc, base + stage * T::STAGE_BYTES, r);
+                    fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(sfready0 + 8u * stage);
@@ -490,7 +551,9 @@ static constexpr PlanInfo make_plan(const char *name)
     X(Kind::NVFP4, 256, 3, 1, "nvfp4_tc1_128x256_s3_acc1")       \
     X(Kind::NVFP4, 128, 5, 2, "nvfp4_tc1_128x128_s5_acc2")       \
     X(Kind::FP8, 256, 4, 2, "fp8_tc1_128x256_s4_acc2")           \
-    X(Kind::FP8, 128, 6, 2, "fp8_tc1_128x128_s6_acc2")
+    X(Kind::FP8, 128, 6, 2, "fp8_tc1_128x128_s6_acc2")           \
+    X(Kind::NVFP4_BF16, 256, 3, 2, "nvfp4bf16_tc1_128x256_s3_acc2") \
+    X(Kind::NVFP4_BF16, 128, 5, 2, "nvfp4bf16_tc1_128x128_s5_acc2")
 
 #define BSG_PLAN_INFO(K, BN, S, A, NAME) make_plan<K, BN, S, A>(NAME),
 static const PlanInfo kTc1Plans[] = {BSG_TC1_PLANS(BSG_PLAN_INFO)};

@@ -206,3 +206,18 @@ def test_grouped_bad_args(lib):
     assert bsg.nvfp4_grouped_scale_bytes(0, 128, 256) == 0
     import oracle
     assert bsg.nvfp4_grouped_scale_bytes(5, 1000, 512) == oracle.get().grouped_scale_bytes(5, 1000, 512)
+
+
+def test_dense_bad_args_and_plans(lib):
+    """nvfp4_dense_gemm: K % 64, N % 8, nulls, alignment and the epilogue
+    rules are checked before any launch; the planner's dense plans."""
+    d = lambda M, N, K, *p: lib.nvfp4_dense_gemm(M, N, K, *p)  # noqa: E731
+    ok = (BAD, BAD, BAD, 1.0, None, None, None)
+    assert d(128, 64, 96, *ok, 128, BAD, None) == bsg.BSG_ERR_INVALID_ARG        # K % 64
+    assert d(128, 60, 128, *ok, 128, BAD, None) == bsg.BSG_ERR_INVALID_ARG       # N % 8
+    assert d(0, 64, 128, *ok, 0, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert d(128, 64, 128, None, BAD, BAD, 1.0, None, None, None, 128, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert d(128, 64, 128, *ok, 100, BAD, None) == bsg.BSG_ERR_INVALID_ARG       # m_out != M
+    assert d(128, 64, 128, BAD, BAD, BAD + 2, 1.0, None, None, None, 128, BAD, None) == bsg.BSG_ERR_MISALIGNED
+    assert bsg.bsg_select_plan(2, 4096, 4096, 4096, 152) == "nvfp4bf16_tc1_128x256_s3_acc2"
+    assert bsg.bsg_select_plan(2, 256, 256, 4096, 152) == "nvfp4bf16_tc1_128x128_s5_acc2"
