@@ -10,8 +10,10 @@
 namespace bsg {
 
 // NVFP4: block-scaled E2M1 x E2M1; FP8: E4M3 x E4M3; NVFP4_BF16: block-scaled
-// E2M1 activations x dense BF16 weights.
-enum class Kind : int { NVFP4 = 0, FP8 = 1, NVFP4_BF16 = 2 };
+// E2M1 activations x dense BF16 weights. NVFP4_BF16_TMEM is not a kind of
+// call but a kernel variant of NVFP4_BF16 (the expanded A staged in tensor
+// memory instead of shared memory); its plans report kind NVFP4_BF16.
+enum class Kind : int { NVFP4 = 0, FP8 = 1, NVFP4_BF16 = 2, NVFP4_BF16_TMEM = 3 };
 
 // Kernel families: persistent 1-SM tiles, persistent CTA-pair tiles, and the
 // swap-AB split-K kernel for skinny M.

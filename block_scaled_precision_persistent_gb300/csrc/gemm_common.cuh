@@ -263,25 +263,35 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
 
 // One row of a 64-element stage: 32 packed bytes of E2M1 codes at src
 // (16-byte aligned; element 2i in the low nibble of byte i) and the row's
-// four block scales (byte b of sc scales elements 16b..16b+15) -> 64 BF16 in
-// row r of a 128B-swizzled K-major tile at shared address tile: 16-byte
-// chunk c (elements 8c..8c+7) at r * 128 + ((c ^ (r % 8)) * 16), the layout
-// the MMA's shared-memory descriptor reads.
-__device__ __forceinline__ void expand_row_nvfp4_bf16(const uint8_t *src, uint32_t sc, uint32_t tile, int r)
+// four block scales (byte b of sc scales elements 16b..16b+15) -> 64 BF16 as
+// 32 words, element 2w in the low half of word w.
+__device__ __forceinline__ void expand_row_nvfp4_bf16(const uint8_t *src, uint32_t sc, uint32_t (&w)[32])
 {
     const uint4 p0 = *reinterpret_cast<const uint4 *>(src);
     const uint4 p1 = *reinterpret_cast<const uint4 *>(src + 16);
     const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-    const uint32_t row = tile + (uint32_t)r * 128u;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
         const uint32_t s2 = e4m3_to_bf16x2((sc >> (8 * (c >> 1))) & 0xFFu);
         uint32_t w0, w1, w2, w3;
         e2m1x4_to_bf16(words[c] & 0xFFFFu, w0, w1);
         e2m1x4_to_bf16(words[c] >> 16, w2, w3);
-        st_shared_v4(row + ((uint32_t)(c ^ (r & 7)) << 4), mul_bf16x2(w0, s2), mul_bf16x2(w1, s2),
-                     mul_bf16x2(w2, s2), mul_bf16x2(w3, s2));
+        w[4 * c] = mul_bf16x2(w0, s2);
+        w[4 * c + 1] = mul_bf16x2(w1, s2);
+        w[4 * c + 2] = mul_bf16x2(w2, s2);
+        w[4 * c + 3] = mul_bf16x2(w3, s2);
     }
+}
+
+// The expanded row r into a 128B-swizzled K-major tile at shared address
+// tile: 16-byte chunk c (elements 8c..8c+7) at r * 128 + ((c ^ (r % 8)) *
+// 16), the layout the MMA's shared-memory descriptor reads.
+__device__ __forceinline__ void store_row_sw128(const uint32_t (&w)[32], uint32_t tile, int r)
+{
+    const uint32_t row = tile + (uint32_t)r * 128u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        st_shared_v4(row + ((uint32_t)(c ^ (r & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
 // Writes one ring stage's NVFP4 block scales from shared memory into the

@@ -63,7 +63,16 @@ struct PairTile {
     static constexpr int EPI_BUFS = EPI_CHUNKS == 2 ? 1 : 2;           // 4 KiB staging buffers per warp
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-    static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 1;
+    // mbarrier layout (8 bytes each): full, empty per stage; full, empty per
+    // accumulator; the drain barrier; scale-ready, scale-full per stage
+    static constexpr int BAR_FULL = 0;
+    static constexpr int BAR_EMPTY = BAR_FULL + STAGES;
+    static constexpr int BAR_TFULL = BAR_EMPTY + STAGES;
+    static constexpr int BAR_TEMPTY = BAR_TFULL + NUM_ACC;
+    static constexpr int BAR_DRAIN = BAR_TEMPTY + NUM_ACC;
+    static constexpr int BAR_SFREADY = BAR_DRAIN + 1;
+    static constexpr int BAR_SFFULL = BAR_SFREADY + STAGES;
+    static constexpr int NUM_BARS = BAR_SFFULL + STAGES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
     static constexpr int SCALE_WARPS = 4;                 // one per TMEM sub-partition (NVFP4 scales)
     static constexpr int EPI_WARP0 = 2 + SCALE_WARPS;
@@ -102,13 +111,13 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
     const uint32_t s_epi = base + STAGES * T::STAGE_BYTES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + STAGES * T::STAGE_BYTES + T::EPI_BYTES);
     const uint32_t bar0 = smem_u32(bars);
-    const uint32_t full0 = bar0;                     // [STAGES] loads -> MMA (leader's used)
-    const uint32_t empty0 = bar0 + 8u * STAGES;      // [STAGES] MMA -> loads (both CTAs)
-    const uint32_t tfull0 = bar0 + 16u * STAGES;     // [NUM_ACC] MMA -> epilogues (both)
-    const uint32_t tempty0 = tfull0 + 8u * NUM_ACC;  // [NUM_ACC] epilogues -> MMA (leader's)
-    const uint32_t drain_bar = tempty0 + 8u * NUM_ACC;
-    const uint32_t sfready0 = drain_bar + 8u;                // [STAGES] scales in TMEM (both CTAs) -> MMA (leader's)
-    const uint32_t sffull0 = sfready0 + 8u * STAGES;         // [STAGES] own scale loads -> own scale warps
+    const uint32_t full0 = bar0 + 8u * T::BAR_FULL;          // [STAGES] loads -> MMA (leader's used)
+    const uint32_t empty0 = bar0 + 8u * T::BAR_EMPTY;        // [STAGES] MMA -> loads (both CTAs)
+    const uint32_t tfull0 = bar0 + 8u * T::BAR_TFULL;        // [NUM_ACC] MMA -> epilogues (both)
+    const uint32_t tempty0 = bar0 + 8u * T::BAR_TEMPTY;      // [NUM_ACC] epilogues -> MMA (leader's)
+    const uint32_t drain_bar = bar0 + 8u * T::BAR_DRAIN;
+    const uint32_t sfready0 = bar0 + 8u * T::BAR_SFREADY;    // [STAGES] scales in TMEM (both CTAs) -> MMA (leader's)
+    const uint32_t sffull0 = bar0 + 8u * T::BAR_SFFULL;      // [STAGES] own scale loads -> own scale warps
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 

@@ -38,13 +38,18 @@ struct Tile {
     // NVFP4 activations x dense BF16 weights: A arrives as E2M1 codes plus
     // block scales and is expanded to BF16 in shared memory by the four
     // warps that write NVFP4 scales in the other kind (kind::f16 MMA)
-    static constexpr bool kDense = KIND == Kind::NVFP4_BF16;
+    static constexpr bool kDense = KIND == Kind::NVFP4_BF16 || KIND == Kind::NVFP4_BF16_TMEM;
+    // dense variant: the expanded A staged in tensor memory (32 columns per
+    // stage: 64 BF16 per row), the MMA reading A from there, which frees the
+    // 16 KB of shared memory per stage for more ring stages
+    static constexpr bool kTmemA = KIND == Kind::NVFP4_BF16_TMEM;
     static constexpr int BM = 128;
     static constexpr int ROW_BYTES = 128;                 // K bytes of one row per stage
     static constexpr int K_BLOCK = kFp4 ? 256 : kDense ? 64 : 128;   // K elements per stage
     static constexpr int MMA_K_BYTES = 32;                // K bytes per tcgen05.mma
     static constexpr int MMAS = ROW_BYTES / MMA_K_BYTES;  // MMAs per stage
-    static constexpr int A_BYTES = BM * ROW_BYTES;
+    static constexpr int A_BYTES = kTmemA ? 0 : BM * ROW_BYTES;
+    static constexpr int A_COLS = kTmemA ? ROW_BYTES / 4 : 0;          // TMEM columns of one stage's A
     static constexpr int B_BYTES = BN * ROW_BYTES;
     // NVFP4 scales of one stage: 128 rows x 16 scales = four 512-byte blocks
     static constexpr int SF_BLOCK_BYTES = 2048;
@@ -61,7 +66,16 @@ struct Tile {
     static constexpr int EPI_COLS = 64;                   // BF16 columns per store box
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
-    static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 1;
+    // mbarrier layout (8 bytes each): full, empty per stage; full, empty per
+    // accumulator; the drain barrier; scale-ready, scale-full per stage
+    static constexpr int BAR_FULL = 0;
+    static constexpr int BAR_EMPTY = BAR_FULL + STAGES;
+    static constexpr int BAR_TFULL = BAR_EMPTY + STAGES;
+    static constexpr int BAR_TEMPTY = BAR_TFULL + NUM_ACC;
+    static constexpr int BAR_DRAIN = BAR_TEMPTY + NUM_ACC;
+    static constexpr int BAR_SFREADY = BAR_DRAIN + 1;
+    static constexpr int BAR_SFFULL = BAR_SFREADY + STAGES;
+    static constexpr int NUM_BARS = BAR_SFFULL + STAGES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
     static constexpr int SCALE_WARPS = 4;                 // one per TMEM sub-partition (NVFP4 scales)
     static constexpr int EPI_WARP0 = 2 + SCALE_WARPS;
@@ -72,7 +86,7 @@ struct Tile {
     static constexpr int SFA_COLS = kFp4 ? 4 * MMAS : 0;
     static constexpr int SFB_COLS = kFp4 ? 4 * SFB_CHUNKS * MMAS : 0;
     static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
-    static constexpr int TMEM_USED = NUM_ACC * BN + STAGES * SF_COLS;
+    static constexpr int TMEM_USED = NUM_ACC * BN + STAGES * (SF_COLS + A_COLS);
     static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
                                      : TMEM_USED <= 64  ? 64
                                      : TMEM_USED <= 128 ? 128
@@ -108,13 +122,13 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     const uint32_t s_epi = base + STAGES * T::STAGE_BYTES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + STAGES * T::STAGE_BYTES + T::EPI_BYTES);
     const uint32_t bar0 = smem_u32(bars);
-    const uint32_t full0 = bar0;                              // [STAGES] TMA -> MMA
-    const uint32_t empty0 = bar0 + 8u * STAGES;               // [STAGES] MMA -> TMA
-    const uint32_t tfull0 = bar0 + 16u * STAGES;              // [NUM_ACC] MMA -> epilogue
-    const uint32_t tempty0 = tfull0 + 8u * NUM_ACC;           // [NUM_ACC] epilogue -> MMA
-    const uint32_t drain_bar = tempty0 + 8u * NUM_ACC;        // MMA teardown
-    const uint32_t sfready0 = drain_bar + 8u;                 // [STAGES] scales in TMEM -> MMA
-    const uint32_t sffull0 = sfready0 + 8u * STAGES;          // [STAGES] scale loads -> scale warps
+    const uint32_t full0 = bar0 + 8u * T::BAR_FULL;           // [STAGES] TMA -> MMA
+    const uint32_t empty0 = bar0 + 8u * T::BAR_EMPTY;         // [STAGES] MMA -> TMA
+    const uint32_t tfull0 = bar0 + 8u * T::BAR_TFULL;         // [NUM_ACC] MMA -> epilogue
+    const uint32_t tempty0 = bar0 + 8u * T::BAR_TEMPTY;       // [NUM_ACC] epilogue -> MMA
+    const uint32_t drain_bar = bar0 + 8u * T::BAR_DRAIN;      // MMA teardown
+    const uint32_t sfready0 = bar0 + 8u * T::BAR_SFREADY;     // [STAGES] scales in TMEM -> MMA
+    const uint32_t sffull0 = bar0 + 8u * T::BAR_SFFULL;       // [STAGES] scale loads -> scale warps
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     // grouped: slice boundaries and first 128-row tile of each slice (group.cuh)
@@ -288,6 +302,13 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                                       desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
                                       sfa_t + 4u * j, sfb_t + 4u * j * T::SFB_CHUNKS,
                                       (kb | j) != 0 ? 1u : 0u);
+                    } else if constexpr (T::kTmemA) {
+                        const uint32_t a_t = tmem + (uint32_t)(NUM_ACC * BN + stage * T::A_COLS);
+#pragma unroll
+                        for (int j = 0; j < T::MMAS; ++j)
+                            mma_bf16_tmem_a(d_tmem, a_t + (uint32_t)(j * T::MMA_K_BYTES / 4),
+                                            desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                            (kb | j) != 0 ? 1u : 0u);
                     } else if constexpr (T::kDense) {
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
@@ -382,8 +403,19 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                     const uint8_t *apk = gbase + stage * T::STAGE_BYTES + T::A_BYTES + T::B_BYTES;
                     const uint32_t sc = *reinterpret_cast<const uint32_t *>(apk + T::APK_BYTES + (r & 31) * 16 +
                                                                              (r >> 5) * 4);
-                    expand_row_nvfp4_bf16(apk + r * 32, sc, base + stage * T::STAGE_BYTES, r);
-                    fence_proxy_async_smem();
+                    uint32_t w[32];
+                    expand_row_nvfp4_bf16(apk + r * 32, sc, w);
+                    if constexpr (T::kTmemA) {
+                        // lane r of this warp's sub-partition, the stage's 32 A columns
+                        tmem_st_32x32b_x32(tmem + ((uint32_t)((warp & 3) * 32) << 16) +
+                                               (uint32_t)(NUM_ACC * BN + stage * T::A_COLS),
+                                           w);
+                        tmem_st_wait();
+                        tc_fence_before_sync();
+                    } else {
+                        store_row_sw128(w, base + stage * T::STAGE_BYTES, r);
+                        fence_proxy_async_smem();
+                    }
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(sfready0 + 8u * stage);
@@ -543,7 +575,9 @@ template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 static constexpr PlanInfo make_plan(const char *name)
 {
     using T = Tile<KIND, BN, STAGES, NUM_ACC>;
-    return PlanInfo{name, KIND, Family::TC1, 1, T::BM, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
+    // the TMEM-staged dense variant serves calls of kind NVFP4_BF16
+    constexpr Kind kind = KIND == Kind::NVFP4_BF16_TMEM ? Kind::NVFP4_BF16 : KIND;
+    return PlanInfo{name, kind, Family::TC1, 1, T::BM, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
                     T::THREADS, T::TMEM_COLS};
 }
 
@@ -553,7 +587,9 @@ static constexpr PlanInfo make_plan(const char *name)
     X(Kind::FP8, 256, 4, 2, "fp8_tc1_128x256_s4_acc2")           \
     X(Kind::FP8, 128, 6, 2, "fp8_tc1_128x128_s6_acc2")           \
     X(Kind::NVFP4_BF16, 256, 3, 2, "nvfp4bf16_tc1_128x256_s3_acc2") \
-    X(Kind::NVFP4_BF16, 128, 5, 2, "nvfp4bf16_tc1_128x128_s5_acc2")
+    X(Kind::NVFP4_BF16, 128, 5, 2, "nvfp4bf16_tc1_128x128_s5_acc2") \
+    X(Kind::NVFP4_BF16_TMEM, 256, 5, 1, "nvfp4bf16_tc1_128x256_s5_acc1_tmema") \
+    X(Kind::NVFP4_BF16_TMEM, 128, 8, 2, "nvfp4bf16_tc1_128x128_s8_acc2_tmema")
 
 #define BSG_PLAN_INFO(K, BN, S, A, NAME) make_plan<K, BN, S, A>(NAME),
 static const PlanInfo kTc1Plans[] = {BSG_TC1_PLANS(BSG_PLAN_INFO)};
