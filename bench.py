@@ -11,8 +11,8 @@ dominant kernel's roofline (CUDA-event duration of the GEMM launches inside
 the timed region), the CPU oracle timed on a bounded sample, the clocks seen
 during the timed region, and secondary lines for the FP8 8192^3 GEMM, the
 skinny-M sweep (HBM GB/s), the scale swizzle, the NVFP4 quantiser, the
-fused epilogue variants (bias, gamma, scattered rows) and the grouped (MoE)
-GEMM.
+fused epilogue variants (bias, gamma, scattered rows), the grouped (MoE)
+GEMM and the NVFP4 x dense-BF16 GEMM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -499,6 +499,35 @@ def secondary_grouped(dev, steps: int, pk: dict, psrc: str) -> dict:
             "timing": "CUDA graph of 8 back-to-back launches per variant, replayed in turn; median per launch"}
 
 
+def secondary_dense(dev, steps: int, pk: dict, psrc: str) -> dict:
+    """NVFP4 activations x dense BF16 weights (nvfp4_dense_gemm): 8192^3 and
+    an 8192 x 256 x 8192 weight GEMM (the pages' case has N = 256). A is
+    expanded to BF16 on the fly and the BF16 tensor core computes, so the
+    roofline is the measured BF16 GEMM peak. CUDA graphs, median per launch."""
+    import block_scaled_precision_persistent_gb300 as bsg
+    out = {}
+    for (M, N, K), launches in (((8192, 8192, 8192), 4), ((8192, 256, 8192), 16)):
+        p = workloads.make_dense(M, N, K, seed=1, device=dev)
+        sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+        bsg.nvfp4_swizzle_scales(M, K, p["sfA"], sa)
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def call():
+            bsg.nvfp4_dense_gemm(M, N, K, p["A"], sa, p["B"], p["alpha"], None, None, None, M, D)
+        us = graph_us({"dense": call}, launches, steps)["dense"]
+        call()
+        plan = bsg.bsg_last_plan_name()
+        tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+        out[f"{M}x{N}x{K}"] = {"plan": plan, "us": round(us, 2), "tflops": round(tf, 1),
+                               "frac_bf16": round(tf / pk["bf16_tflops"], 4)}
+        del p, sa, D
+    if bsg.bsg_get_device_status() != bsg.BSG_OK:
+        raise SystemExit("device status reported an error in the dense GEMM timing")
+    return {"shapes": out, "roofline_peak_tflops": pk["bf16_tflops"],
+            "peak_source": f"{psrc} bf16 burst (the MMA is kind::f16 on BF16 operands)",
+            "timing": "CUDA graph of back-to-back launches, median over replays per launch"}
+
+
 def secondary_swizzle(dev, steps: int, pk: dict, psrc: str) -> dict:
     """The scale-layout prep alone (timed separately from the GEMM): one
     operand's row-major [16384][1024] E4M3 scales into the swizzled layout;
@@ -601,6 +630,7 @@ def run_ours(args, dist: Dist) -> None:
         secondary["quantize"] = secondary_quantize(dev, 20, pk, psrc)
         secondary["epilogue"] = secondary_epilogue(dev, step, 10, pk, psrc)
         secondary["grouped"] = secondary_grouped(dev, 15, pk, psrc)
+        secondary["dense"] = secondary_dense(dev, 10, pk, psrc)
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, host_copy(step), args.cpu_seconds)
