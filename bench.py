@@ -45,8 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (plan, workload);
 # the summary it comes from is named in the comment. None = not captured.
 NCU_TRAFFIC_BYTES: dict[tuple[str, str], float] = {
-    # profiles/gemm_pair_nvfp4_256x256_s5_acc1_16384.md: 1.405 GB read + 0.520 GB written
-    ("nvfp4_tc2_256x256_s5_acc1", "nvfp4_16384"): 1405161472 + 520169984,
+    # profiles/gemm_pair_nvfp4_256x256_s5_acc1_16384.md (raster group 16): 1.143 GB read + 0.520 GB written
+    ("nvfp4_tc2_256x256_s5_acc1", "nvfp4_16384"): 1143024384 + 520135168,
 }
 
 
@@ -721,6 +721,7 @@ def run_case(args) -> None:
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     s = torch.cuda.current_stream()
+    bsg.bsg_set_raster_group(args.raster)
     if kind == "quantize":
         rows, K = dims
         g = torch.Generator(device="cpu").manual_seed(0xB5C0)
@@ -816,7 +817,7 @@ def run_case(args) -> None:
     if bsg.bsg_get_device_status() != bsg.BSG_OK:
         raise SystemExit("device status reported an error")
     ms = statistics.median(a.elapsed_time(b) for a, b in evs)
-    print(json.dumps({"case": args.case, "plan": plan, "ms": round(ms, 5),
+    print(json.dumps({"case": args.case, "plan": plan, "raster": args.raster or 16, "ms": round(ms, 5),
                       "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 2)}), flush=True)
 
 
@@ -836,6 +837,8 @@ def main() -> None:
                     help="time one shape alone instead of the benchmark: nvfp4:MxNxK, fp8:MxNxK or "
                          "quantize:ROWSxK")
     ap.add_argument("--plan", default=None, help="with --case: force this plan")
+    ap.add_argument("--raster", type=int, default=0,
+                    help="with --case: M tiles per rasterisation group (0: the library default)")
     ap.add_argument("--epi", default=None,
                     help="with --case nvfp4: fused epilogue options, comma list of bias,gamma,scatter")
     args = ap.parse_args()

@@ -27,6 +27,11 @@ constexpr unsigned long long kDefaultWatchdogNs = 1000000000ull;
 constexpr int kMaxDevices = 64;
 
 std::atomic<unsigned long long> g_watchdog_ns{kDefaultWatchdogNs};
+// M tiles per rasterisation group (L2 reuse of B). Swept on GB300 over 1..32:
+// 16 beat 8 on every alternating repeat (FP8 8192^3 +2.1 %, NVFP4 16384^3
+// +0.9 %); L2-resident shapes do not depend on it.
+constexpr int kDefaultRasterGroup = 16;
+std::atomic<int> g_raster_group{kDefaultRasterGroup};
 std::mutex g_mu;
 int g_forced_plan = -1;                 // guarded by g_mu
 thread_local uint32_t t_last_status_word = 0;
@@ -318,7 +323,7 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     a.num_m_tiles = (M + pi.tile_m - 1) / pi.tile_m;
     a.num_n_tiles = (N + pi.bn - 1) / pi.bn;
     a.num_k_blocks = K / pi.k_block;
-    a.raster_group = 8;                 // M tiles per rasterisation group (L2 reuse of B)
+    a.raster_group = g_raster_group.load();   // M tiles per rasterisation group (L2 reuse of B)
     a.sf_col_blocks = (K / 16 + 3) / 4;
     a.sfb_row_blocks = (N + 127) / 128;
     a.sfa = sfa;
@@ -389,7 +394,7 @@ int run_grouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, c
     a.num_m_tiles = (int)mt_bound;      // bound only: the kernel counts the slices' tile rows
     a.num_n_tiles = (N + pi.bn - 1) / pi.bn;
     a.num_k_blocks = K / pi.k_block;
-    a.raster_group = 8;
+    a.raster_group = g_raster_group.load();
     a.sf_col_blocks = (K / 16 + 3) / 4;
     a.sfb_row_blocks = (N + 127) / 128;
     a.sfa = sfa;
@@ -773,6 +778,14 @@ uint32_t bsg_last_status_word(void) { return t_last_status_word; }
 int bsg_set_watchdog_ns(uint64_t ns)
 {
     g_watchdog_ns.store(ns ? (unsigned long long)ns : kDefaultWatchdogNs);
+    return BSG_OK;
+}
+
+int bsg_set_raster_group(int m_tiles)
+{
+    if (m_tiles < 0 || m_tiles > 1024)
+        return BSG_ERR_INVALID_ARG;
+    g_raster_group.store(m_tiles == 0 ? kDefaultRasterGroup : m_tiles);
     return BSG_OK;
 }
 

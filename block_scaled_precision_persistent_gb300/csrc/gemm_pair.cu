@@ -544,10 +544,15 @@ static constexpr PlanInfo make_pair_plan(const char *name)
                     T::THREADS, T::TMEM_COLS};
 }
 
+// The first plan of each kind and shape is the planner's; the shallower
+// rings are there for the stage sweep (bsg_force_plan).
 #define BSG_PAIR_PLANS(X)                                        \
     X(Kind::NVFP4, 256, 5, 1, "nvfp4_tc2_256x256_s5_acc1")       \
     X(Kind::NVFP4, 128, 6, 2, "nvfp4_tc2_256x128_s6_acc2")       \
-    X(Kind::FP8, 256, 6, 2, "fp8_tc2_256x256_s6_acc2")
+    X(Kind::FP8, 256, 6, 2, "fp8_tc2_256x256_s6_acc2")           \
+    X(Kind::NVFP4, 256, 4, 1, "nvfp4_tc2_256x256_s4_acc1")       \
+    X(Kind::NVFP4, 256, 3, 1, "nvfp4_tc2_256x256_s3_acc1")       \
+    X(Kind::FP8, 256, 4, 2, "fp8_tc2_256x256_s4_acc2")
 
 #define BSG_PAIR_INFO(K, BN, S, A, NAME) make_pair_plan<K, BN, S, A>(NAME),
 static const PlanInfo kPairPlans[] = {BSG_PAIR_PLANS(BSG_PAIR_INFO)};

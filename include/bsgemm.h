@@ -292,6 +292,12 @@ BSG_API uint32_t bsg_last_status_word(void);
  * the default of 1e9).                                                    */
 BSG_API int bsg_set_watchdog_ns(uint64_t ns);
 
+/* Tuning lever: M tiles per rasterisation group of the tile kernels (the
+ * tile order walks the group's M tiles fastest, so that the CTAs resident at
+ * one time share a band of B in L2) for later launches; 0 restores the
+ * default of 16. 1 <= m_tiles <= 1024. Process-wide.                       */
+BSG_API int bsg_set_raster_group(int m_tiles);
+
 /* Launch a one-thread probe that waits, with the library's bounded wait, on
  * an mbarrier that nothing ever arrives on. After `ns` nanoseconds it records
  * BSG_ERR_DEVICE_TIMEOUT in the status word and returns: a test of the
