@@ -130,8 +130,9 @@ int default_plan(Kind kind, int M, int N, int K, int num_sms)
             name = M <= 128 ? "nvfp4_tc1_128x256_s3_acc1" : "nvfp4_tc2_256x256_s5_acc1";
     } else if (kind == Kind::NVFP4_BF16) {
         // expanded A staged in TMEM (5 or 8 stages) measured 1.2x the
-        // shared-memory expansion (3 or 5 stages); 128 x 128 tiles only where
-        // N leaves no 256-wide tile
+        // shared-memory expansion (3 or 5 stages), and the 1-SM 128 x 256
+        // tile 1.1x the CTA-pair 256 x 256 one (8 stages); 128 x 128 tiles
+        // only where N leaves no 256-wide tile
         name = N <= 128 ? "nvfp4bf16_tc1_128x128_s8_acc2_tmema" : "nvfp4bf16_tc1_128x256_s5_acc1_tmema";
     } else {
         const bool small_m = M <= 128;   // a 256-row pair tile would idle half its SMs

@@ -39,25 +39,34 @@ namespace bsg {
 template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 struct PairTile {
     static constexpr bool kFp4 = KIND == Kind::NVFP4;
+    // NVFP4 activations x dense BF16 weights: each CTA expands its own 128
+    // rows of A (E2M1 codes + block scales) into its own TMEM, 32 columns per
+    // stage, with the warps that write NVFP4 scales in the other kind; the
+    // leader's pair MMA (kind::f16) reads A from both CTAs' TMEM
+    static constexpr bool kDense = KIND == Kind::NVFP4_BF16_TMEM;
     static constexpr int BM = 128;                        // rows per CTA
     static constexpr int TILE_M = 256;                    // rows per pair
     static constexpr int ROW_BYTES = 128;
-    static constexpr int K_BLOCK = kFp4 ? 256 : 128;
+    static constexpr int K_BLOCK = kFp4 ? 256 : kDense ? 64 : 128;
     static constexpr int MMA_K_BYTES = 32;
     static constexpr int MMAS = ROW_BYTES / MMA_K_BYTES;
     static constexpr int B_ROWS = BN / 2;                 // B rows held by each CTA
-    static constexpr int A_BYTES = BM * ROW_BYTES;
+    static constexpr int A_BYTES = kDense ? 0 : BM * ROW_BYTES;
     static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
+    static constexpr int APK_BYTES = kDense ? BM * 32 : 0;   // dense: this CTA's codes (128 rows x 32 bytes)
+    static constexpr int ASF_BYTES = kDense ? 512 : 0;       // and their scales (one 512-byte block)
+    static constexpr int A_COLS = kDense ? ROW_BYTES / 4 : 0; // TMEM columns of one stage's expanded A
     static constexpr int SF_BLOCK_BYTES = 2048;           // 128 rows x 16 scales
     static constexpr int SFB_CHUNKS = kFp4 ? BN / 128 : 0;
     static constexpr int SFA_BYTES = kFp4 ? SF_BLOCK_BYTES : 0;
     static constexpr int SFB_BYTES = SFB_CHUNKS * SF_BLOCK_BYTES;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int STAGE_BYTES =
+        (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES + APK_BYTES + ASF_BYTES + 1023) / 1024 * 1024;
     // Epilogue warps: each drains 32 TMEM lanes x 128 columns. 256-wide NVFP4
     // tiles (one accumulator, so every tile's drain stalls the MMA) use two
     // per sub-partition to release TMEM sooner; FP8 tiles (two accumulators,
     // drain overlapped) and 128-wide tiles use one.
-    static constexpr int EPI_WARPS = (kFp4 && BN == 256) ? 8 : 4;
+    static constexpr int EPI_WARPS = ((kFp4 || kDense) && BN == 256) ? 8 : 4;
     static constexpr int EPI_COLS = 64;
     static constexpr int EPI_CHUNKS = BN * 4 / EPI_WARPS / EPI_COLS;   // 64-column chunks per warp (2 or 4)
     static constexpr int EPI_BUFS = EPI_CHUNKS == 2 ? 1 : 2;           // 4 KiB staging buffers per warp
@@ -80,13 +89,14 @@ struct PairTile {
     static constexpr int SFA_COLS = kFp4 ? 4 * MMAS : 0;
     static constexpr int SFB_COLS = kFp4 ? 4 * SFB_CHUNKS * MMAS : 0;
     static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
-    static constexpr int TMEM_USED = NUM_ACC * BN + STAGES * SF_COLS;
+    static constexpr int TMEM_USED = NUM_ACC * BN + STAGES * (SF_COLS + A_COLS);
     static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
                                      : TMEM_USED <= 64  ? 64
                                      : TMEM_USED <= 128 ? 128
                                      : TMEM_USED <= 256 ? 256
                                                         : 512;
-    static constexpr uint32_t IDESC = kFp4 ? idesc_nvfp4(TILE_M, BN) : idesc_fp8(TILE_M, BN);
+    static constexpr uint32_t IDESC =
+        kFp4 ? idesc_nvfp4(TILE_M, BN) : kDense ? idesc_bf16(TILE_M, BN) : idesc_fp8(TILE_M, BN);
 
     static_assert(BN % 128 == 0 && BN <= 256, "pair tile N: B halves of 64 or 128 rows");
     static_assert(TMEM_USED <= 512, "TMEM: accumulators plus scales exceed 512 columns");
@@ -202,9 +212,30 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                                         (rbb * args.sf_col_blocks + 4 * kb) * 2);
                         }
                     }
-                    if (leader)
-                        mbar_arrive_expect_tx(full0 + 8u * stage, 2u * (T::A_BYTES + T::B_BYTES));
-                    tma_load_2d_pair(sa, &tmA, fb, kb * T::ROW_BYTES, pm * T::TILE_M + (int)rank * T::BM);
+                    if constexpr (T::kDense) {
+                        // this CTA's codes and scales on its own expansion
+                        // barrier; its B half on the leader's full barrier
+                        // (a CTA whose 128 rows all lie past M has no scale
+                        // block to read: its codes are zero-filled, so
+                        // whatever scales its shared memory holds give zeros,
+                        // and its rows are never stored)
+                        const uint32_t sfb = sffull0 + 8u * stage;
+                        const uint32_t sapk = sb + T::B_BYTES;
+                        const int sf_row = 2 * pm + (int)rank;
+                        const bool rows_in = sf_row * T::BM < args.M;
+                        mbar_arrive_expect_tx(sfb, T::APK_BYTES + (rows_in ? T::ASF_BYTES : 0));
+                        tma_load_2d(sapk, &tmA, sfb, kb * 32, pm * T::TILE_M + (int)rank * T::BM);
+                        if (rows_in)
+                            bulk_load(sapk + T::APK_BYTES,
+                                      args.sfa + ((size_t)sf_row * args.sf_col_blocks + kb) * 512u, T::ASF_BYTES,
+                                      sfb);
+                        if (leader)
+                            mbar_arrive_expect_tx(full0 + 8u * stage, 2u * T::B_BYTES);
+                    } else {
+                        if (leader)
+                            mbar_arrive_expect_tx(full0 + 8u * stage, 2u * (T::A_BYTES + T::B_BYTES));
+                        tma_load_2d_pair(sa, &tmA, fb, kb * T::ROW_BYTES, pm * T::TILE_M + (int)rank * T::BM);
+                    }
                     tma_load_2d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN + (int)rank * T::B_ROWS);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -239,8 +270,9 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                         ok = false;
                         break;
                     }
-                    if constexpr (T::kFp4) {
-                        // the scale warps have written this stage's scales to TMEM
+                    if constexpr (T::kFp4 || T::kDense) {
+                        // the scale warps have written this stage's scales
+                        // (NVFP4) / expanded A (dense) to both CTAs' TMEM
                         if (!mbar_wait(sfready0 + 8u * stage, phase, wd, abort_flag, 5)) {
                             ok = false;
                             break;
@@ -258,6 +290,13 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                                            desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
                                            sfa_t + 4u * j, sfb_t + 4u * j * T::SFB_CHUNKS,
                                            (kb | j) != 0 ? 1u : 0u);
+                    } else if constexpr (T::kDense) {
+                        const uint32_t a_t = tmem + (uint32_t)(NUM_ACC * BN + stage * T::A_COLS);
+#pragma unroll
+                        for (int j = 0; j < T::MMAS; ++j)
+                            mma_bf16_pair_tmem_a(d_tmem, a_t + (uint32_t)(j * T::MMA_K_BYTES / 4),
+                                                 desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                                 (kb | j) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
@@ -315,6 +354,43 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                         // the stores have completed (wait::st): the leader's own
                         // writers arrive locally, the peer's with a relaxed remote
                         // arrive (a release at cluster scope measured ~1100 cycles)
+                        if (leader)
+                            mbar_arrive(sfready0 + 8u * stage);
+                        else
+                            mbar_arrive_remote_relaxed(mapa_shared(sfready0 + 8u * stage, 0));
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        } else if constexpr (T::kDense) {
+            // expansion warps (both CTAs): row r of this CTA's 128 rows of A
+            // from codes + block scales to BF16 in its own TMEM lanes, then
+            // the leader's ready barrier (as the scale writers above)
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            const int r = (warp & 3) * 32 + lane;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!warp_wait(sffull0 + 8u * stage, phase, wd, abort_flag, 6, lane)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint8_t *apk = gbase + stage * T::STAGE_BYTES + T::A_BYTES + T::B_BYTES;
+                    const uint32_t sc = *reinterpret_cast<const uint32_t *>(apk + T::APK_BYTES + (r & 31) * 16 +
+                                                                             (r >> 5) * 4);
+                    uint32_t w[32];
+                    expand_row_nvfp4_bf16(apk + r * 32, sc, w);
+                    tmem_st_32x32b_x32(tmem + lane_off + (uint32_t)(NUM_ACC * BN + stage * T::A_COLS), w);
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
                         if (leader)
                             mbar_arrive(sfready0 + 8u * stage);
                         else
@@ -540,7 +616,9 @@ template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 static constexpr PlanInfo make_pair_plan(const char *name)
 {
     using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
-    return PlanInfo{name, KIND, Family::PAIR, 2, T::TILE_M, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
+    // the TMEM-staged dense pair serves calls of kind NVFP4_BF16
+    constexpr Kind kind = KIND == Kind::NVFP4_BF16_TMEM ? Kind::NVFP4_BF16 : KIND;
+    return PlanInfo{name, kind, Family::PAIR, 2, T::TILE_M, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
                     T::THREADS, T::TMEM_COLS};
 }
 
@@ -552,7 +630,8 @@ static constexpr PlanInfo make_pair_plan(const char *name)
     X(Kind::FP8, 256, 6, 2, "fp8_tc2_256x256_s6_acc2")           \
     X(Kind::NVFP4, 256, 4, 1, "nvfp4_tc2_256x256_s4_acc1")       \
     X(Kind::NVFP4, 256, 3, 1, "nvfp4_tc2_256x256_s3_acc1")       \
-    X(Kind::FP8, 256, 4, 2, "fp8_tc2_256x256_s4_acc2")
+    X(Kind::FP8, 256, 4, 2, "fp8_tc2_256x256_s4_acc2")           \
+    X(Kind::NVFP4_BF16_TMEM, 256, 8, 1, "nvfp4bf16_tc2_256x256_s8_acc1_tmema")
 
 #define BSG_PAIR_INFO(K, BN, S, A, NAME) make_pair_plan<K, BN, S, A>(NAME),
 static const PlanInfo kPairPlans[] = {BSG_PAIR_PLANS(BSG_PAIR_INFO)};

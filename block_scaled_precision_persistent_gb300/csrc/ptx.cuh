@@ -508,6 +508,19 @@ __device__ __forceinline__ void mma_nvfp4_pair(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
+// Pair MMA with BF16 operands, A from tensor memory (each CTA's own 128
+// rows at the same TMEM address), B from both CTAs' shared memory.
+__device__ __forceinline__ void mma_bf16_pair_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                     uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_fp8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate)
 {

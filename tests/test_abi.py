@@ -220,5 +220,5 @@ def test_dense_bad_args_and_plans(lib):
     assert d(128, 64, 128, *ok, 100, BAD, None) == bsg.BSG_ERR_INVALID_ARG       # m_out != M
     assert d(128, 64, 128, BAD, BAD, BAD + 2, 1.0, None, None, None, 128, BAD, None) == bsg.BSG_ERR_MISALIGNED
     assert bsg.bsg_select_plan(2, 4096, 4096, 4096, 152) == "nvfp4bf16_tc1_128x256_s5_acc1_tmema"
-    assert bsg.bsg_select_plan(2, 256, 256, 4096, 152) == "nvfp4bf16_tc1_128x256_s5_acc1_tmema"
+    assert bsg.bsg_select_plan(2, 128, 4096, 4096, 152) == "nvfp4bf16_tc1_128x256_s5_acc1_tmema"
     assert bsg.bsg_select_plan(2, 4096, 128, 4096, 152) == "nvfp4bf16_tc1_128x128_s8_acc2_tmema"

@@ -25,7 +25,8 @@ pytestmark = pytest.mark.gpu
 SENTINEL = 0x7FC1
 GUARD = 256
 PLANS = [None, "nvfp4bf16_tc1_128x128_s5_acc2", "nvfp4bf16_tc1_128x256_s3_acc2",
-         "nvfp4bf16_tc1_128x256_s5_acc1_tmema", "nvfp4bf16_tc1_128x128_s8_acc2_tmema"]
+         "nvfp4bf16_tc1_128x256_s5_acc1_tmema", "nvfp4bf16_tc1_128x128_s8_acc2_tmema",
+         "nvfp4bf16_tc2_256x256_s8_acc1_tmema"]
 
 
 @pytest.fixture(scope="module")
