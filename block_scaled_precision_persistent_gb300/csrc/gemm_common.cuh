@@ -283,6 +283,39 @@ __device__ __forceinline__ void expand_row_nvfp4_bf16(const uint8_t *src, uint32
     }
 }
 
+// Half a row: elements [32 hc, 32 hc + 32) of the stage's 64 (16 packed
+// bytes at src + 16 hc, scale bytes 2 hc and 2 hc + 1 of sc) -> 16 words,
+// element 2w in the low half of word w. The dense kernels give each half to
+// its own warp, so that the expansion's latency per stage is halved.
+__device__ __forceinline__ void expand_half_row_nvfp4_bf16(const uint8_t *src, uint32_t sc, int hc,
+                                                           uint32_t (&w)[16])
+{
+    const uint4 p = *reinterpret_cast<const uint4 *>(src + 16 * hc);
+    const uint32_t words[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t s2 = e4m3_to_bf16x2((sc >> (8 * (2 * hc + (c >> 1)))) & 0xFFu);
+        uint32_t w0, w1, w2, w3;
+        e2m1x4_to_bf16(words[c] & 0xFFFFu, w0, w1);
+        e2m1x4_to_bf16(words[c] >> 16, w2, w3);
+        w[4 * c] = mul_bf16x2(w0, s2);
+        w[4 * c + 1] = mul_bf16x2(w1, s2);
+        w[4 * c + 2] = mul_bf16x2(w2, s2);
+        w[4 * c + 3] = mul_bf16x2(w3, s2);
+    }
+}
+
+// Chunks [4 hc, 4 hc + 4) of row r (expanded half hc) into a 128B-swizzled
+// K-major tile at shared address tile (see store_row_sw128).
+__device__ __forceinline__ void store_half_row_sw128(const uint32_t (&w)[16], uint32_t tile, int r, int hc)
+{
+    const uint32_t row = tile + (uint32_t)r * 128u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        st_shared_v4(row + ((uint32_t)((4 * hc + c) ^ (r & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2],
+                     w[4 * c + 3]);
+}
+
 // The expanded row r into a 128B-swizzled K-major tile at shared address
 // tile: 16-byte chunk c (elements 8c..8c+7) at r * 128 + ((c ^ (r % 8)) *
 // 16), the layout the MMA's shared-memory descriptor reads.

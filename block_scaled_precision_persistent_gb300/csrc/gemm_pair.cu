@@ -66,7 +66,9 @@ struct PairTile {
     // tiles (one accumulator, so every tile's drain stalls the MMA) use two
     // per sub-partition to release TMEM sooner; FP8 tiles (two accumulators,
     // drain overlapped) and 128-wide tiles use one.
-    static constexpr int EPI_WARPS = ((kFp4 || kDense) && BN == 256) ? 8 : 4;
+    // (dense: 4, since its eight expansion warps would otherwise leave too
+    // few registers per thread for the epilogue variants)
+    static constexpr int EPI_WARPS = (kFp4 && BN == 256) ? 8 : 4;
     static constexpr int EPI_COLS = 64;
     static constexpr int EPI_CHUNKS = BN * 4 / EPI_WARPS / EPI_COLS;   // 64-column chunks per warp (2 or 4)
     static constexpr int EPI_BUFS = EPI_CHUNKS == 2 ? 1 : 2;           // 4 KiB staging buffers per warp
@@ -83,7 +85,9 @@ struct PairTile {
     static constexpr int BAR_SFFULL = BAR_SFREADY + STAGES;
     static constexpr int NUM_BARS = BAR_SFFULL + STAGES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
-    static constexpr int SCALE_WARPS = 4;                 // one per TMEM sub-partition (NVFP4 scales)
+    // NVFP4: one scale writer per TMEM sub-partition; dense: two expansion
+    // warps per sub-partition, each taking half of every row
+    static constexpr int SCALE_WARPS = kDense ? 8 : 4;
     static constexpr int EPI_WARP0 = 2 + SCALE_WARPS;
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // producer, MMA, scale warps, epilogue
     static constexpr int SFA_COLS = kFp4 ? 4 * MMAS : 0;
@@ -366,11 +370,13 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                 }
             }
         } else if constexpr (T::kDense) {
-            // expansion warps (both CTAs): row r of this CTA's 128 rows of A
-            // from codes + block scales to BF16 in its own TMEM lanes, then
-            // the leader's ready barrier (as the scale writers above)
+            // expansion warps (both CTAs), two per TMEM sub-partition: row r
+            // of this CTA's 128 rows of A, column half hc, from codes + block
+            // scales to BF16 in its own TMEM lanes, then the leader's ready
+            // barrier (as the scale writers above)
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
             const int r = (warp & 3) * 32 + lane;
+            const int hc = (warp - 2) >> 2;                // column half of the row
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -384,9 +390,9 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                     const uint8_t *apk = gbase + stage * T::STAGE_BYTES + T::A_BYTES + T::B_BYTES;
                     const uint32_t sc = *reinterpret_cast<const uint32_t *>(apk + T::APK_BYTES + (r & 31) * 16 +
                                                                              (r >> 5) * 4);
-                    uint32_t w[32];
-                    expand_row_nvfp4_bf16(apk + r * 32, sc, w);
-                    tmem_st_32x32b_x32(tmem + lane_off + (uint32_t)(NUM_ACC * BN + stage * T::A_COLS), w);
+                    uint32_t w[16];
+                    expand_half_row_nvfp4_bf16(apk + r * 32, sc, hc, w);
+                    tmem_st_32x32b_x16(tmem + lane_off + (uint32_t)(NUM_ACC * BN + stage * T::A_COLS + 16 * hc), w);
                     tmem_st_wait();
                     tc_fence_before_sync();
                     __syncwarp();

@@ -77,7 +77,9 @@ struct Tile {
     static constexpr int BAR_SFFULL = BAR_SFREADY + STAGES;
     static constexpr int NUM_BARS = BAR_SFFULL + STAGES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
-    static constexpr int SCALE_WARPS = 4;                 // one per TMEM sub-partition (NVFP4 scales)
+    // NVFP4: one scale writer per TMEM sub-partition; dense: two expansion
+    // warps per sub-partition, each taking half of every row
+    static constexpr int SCALE_WARPS = kDense ? 8 : 4;
     static constexpr int EPI_WARP0 = 2 + SCALE_WARPS;
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // producer, MMA, scale warps, epilogue
     // TMEM columns: NUM_ACC accumulators of BN columns, then one set of scale
@@ -383,12 +385,14 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
             }
         } else if constexpr (T::kDense) {
             // ----------------------------------------------------------------
-            // Expansion warps (NVFP4 x BF16): row r = 32 (warp % 4) + lane of
-            // the stage's A, from E2M1 codes and block scales to BF16 in the
-            // 128B-swizzled tile the MMA reads, then a proxy fence (generic
-            // writes -> tensor-core reads) and the stage's ready barrier
+            // Expansion warps (NVFP4 x BF16), two per TMEM sub-partition: row
+            // r = 32 (warp % 4) + lane of the stage's A, column half hc, from
+            // E2M1 codes and block scales to BF16 -- into TMEM (one
+            // tcgen05.st of 16 columns) or the 128B-swizzled shared tile the
+            // MMA reads (then a proxy fence) -- then the stage's ready barrier
             // ----------------------------------------------------------------
             const int r = (warp & 3) * 32 + lane;
+            const int hc = (warp - 2) >> 2;
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -400,20 +404,21 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                         ok = false;
                         break;
                     }
+                    tc_fence_after_sync();
                     const uint8_t *apk = gbase + stage * T::STAGE_BYTES + T::A_BYTES + T::B_BYTES;
                     const uint32_t sc = *reinterpret_cast<const uint32_t *>(apk + T::APK_BYTES + (r & 31) * 16 +
                                                                              (r >> 5) * 4);
-                    uint32_t w[32];
-                    expand_row_nvfp4_bf16(apk + r * 32, sc, w);
+                    uint32_t w[16];
+                    expand_half_row_nvfp4_bf16(apk + r * 32, sc, hc, w);
                     if constexpr (T::kTmemA) {
-                        // lane r of this warp's sub-partition, the stage's 32 A columns
-                        tmem_st_32x32b_x32(tmem + ((uint32_t)((warp & 3) * 32) << 16) +
-                                               (uint32_t)(NUM_ACC * BN + stage * T::A_COLS),
+                        // lane r of this warp's sub-partition, 16 of the stage's 32 A columns
+                        tmem_st_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) +
+                                               (uint32_t)(NUM_ACC * BN + stage * T::A_COLS + 16 * hc),
                                            w);
                         tmem_st_wait();
                         tc_fence_before_sync();
                     } else {
-                        store_row_sw128(w, base + stage * T::STAGE_BYTES, r);
+                        store_half_row_sw128(w, base + stage * T::STAGE_BYTES, r, hc);
                         fence_proxy_async_smem();
                     }
                     __syncwarp();
