@@ -225,22 +225,26 @@ __device__ __forceinline__ void scatter_chunk(const uint8_t *sbuf, int dst, uint
 // BF16 MMA computes the definition up to the FP32 accumulation order.
 // ---------------------------------------------------------------------------
 
-// Four E2M1 codes (nibbles 0..3 of x, in element order) -> four BF16 values:
-// elements 0, 1 in w01 and 2, 3 in w23 (low half first). The magnitudes
-// 0 .5 1 1.5 2 3 4 6 are BF16 0x0000 0x3F00 0x3F80 0x3FC0 0x4000 0x4040
-// 0x4080 0x40C0; byte permutes pick their low and high bytes by the code's
-// three magnitude bits, a third and fourth interleave them, and the code's
-// sign bit becomes the BF16 sign.
+// Four E2M1 codes (nibbles 0..3 of x, x < 2^16, in element order) -> four
+// BF16 values: elements 0, 1 in w01 and 2, 3 in w23 (low half first). The
+// magnitudes 0 .5 1 1.5 2 3 4 6 are BF16 0x0000 0x3F00 0x3F80 0x3FC0 0x4000
+// 0x4040 0x4080 0x40C0; byte permutes pick their low and high bytes by the
+// code's three magnitude bits and a second pair interleaves them. The codes'
+// sign bits (bits 3, 7, 11, 15 of x) are bit 7 of bytes 0, 1 of x << 4 and of
+// x, so one more permute per word moves them to bits 15 and 31.
 __device__ __forceinline__ void e2m1x4_to_bf16(uint32_t x, uint32_t &w01, uint32_t &w23)
 {
     const uint32_t sel = x & 0x7777u;
-    uint32_t lo, hi;
+    const uint32_t x4 = x << 4;
+    uint32_t lo, hi, s01, s23;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0xC0800000u), "r"(0xC0804000u), "r"(sel));
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3F3F3F00u), "r"(0x40404040u), "r"(sel));
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(w01) : "r"(lo), "r"(hi), "r"(0x5140u));
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(w23) : "r"(lo), "r"(hi), "r"(0x7362u));
-    w01 |= ((x & 0x8u) << 12) | ((x & 0x80u) << 24);
-    w23 |= ((x & 0x800u) << 4) | ((x & 0x8000u) << 16);
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s01) : "r"(x), "r"(x4), "r"(0x0040u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s23) : "r"(x), "r"(x4), "r"(0x1050u));
+    w01 |= s01 & 0x80008000u;
+    w23 |= s23 & 0x80008000u;
 }
 
 // An E4M3 scale code (sign bit ignored: scales are unsigned) -> its BF16
