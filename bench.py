@@ -342,17 +342,42 @@ def secondary_skinny(dev, steps: int, pk: dict, psrc: str) -> dict:
             torch.cuda.synchronize()
             tw.append(a.elapsed_time(b) / copies)
         us_warm = statistics.median(tw) * 1e3
+        # the same cold graph with programmatic dependent launch: each
+        # launch's prologue overlaps the previous launch's tail
+        bsg.bsg_set_pdl(True)
+        try:
+            gp = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gp):
+                for A, sa, B, sb, D in sets:
+                    bsg.nvfp4_gemm_swizzled(M, N, K, A, sa, B, sb, p["alpha"], D)
+        finally:
+            bsg.bsg_set_pdl(False)
+        gp.replay()
+        torch.cuda.synchronize()
+        tp = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            gp.replay()
+            b.record()
+            torch.cuda.synchronize()
+            tp.append(a.elapsed_time(b) / copies)
+        if bsg.bsg_get_device_status() != bsg.BSG_OK:
+            raise RuntimeError(f"device status set during the PDL run of skinny cell {name}")
+        us_pdl = statistics.median(tp) * 1e3
         gbs = per / (us * 1e-6) / 1e9
         ideal_us = max(per / (pk["hbm_gbs"] * 1e9), w.flops / (pk["bf16_tflops"] * FP4_PER_BF16 * 1e12)) * 1e6
         out[f"m{M}_n{N}_k{K}"] = {"plan": bsg.bsg_select_plan(0, M, N, K, sms), "us": round(us, 3),
                                   "hbm_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
                                   "ideal_us": round(ideal_us, 3), "frac_roofline": round(ideal_us / us, 4),
-                                  "us_warm_l2": round(us_warm, 3)}
-        del g, gw, sets
+                                  "us_warm_l2": round(us_warm, 3), "us_pdl": round(us_pdl, 3),
+                                  "hbm_gbs_pdl": round(per / (us_pdl * 1e-6) / 1e9, 1)}
+        del g, gw, gp, sets
     return {"cells": out, "peak_hbm_gbs": pk["hbm_gbs"], "peak_source": psrc,
             "timing": "cold L2 (buffer sets rotated over > 4x L2), CUDA graph of back-to-back launches, "
                       "median over replays of graph time / launches; us_warm_l2: the same over one "
-                      "buffer set (weights L2-resident)"}
+                      "buffer set (weights L2-resident); us_pdl: the cold graph with programmatic "
+                      "dependent launch"}
 
 
 def secondary_quantize(dev, steps: int, pk: dict, psrc: str) -> dict:

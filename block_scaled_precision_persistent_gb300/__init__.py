@@ -19,7 +19,7 @@ __all__ = [
     "nvfp4_swizzled_scale_bytes", "nvfp4_gemm_noalloc", "fp8_gemm", "nvfp4_gemm_ex", "fp8_gemm_ex",
     "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes", "nvfp4_dense_gemm",
     "bsg_reserve_workspace", "bsg_get_device_status",
-    "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_watchdog_selftest", "bsg_force_plan",
+    "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_set_pdl", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_select_plan", "bsg_last_launch_count", "bsg_last_plan_name", "bsg_error_string", "EXPORTED_SYMBOLS",
     "BSG_OK", "BSG_ERR_INVALID_ARG", "BSG_ERR_MISALIGNED", "BSG_ERR_UNSUPPORTED_DEVICE",
     "BSG_ERR_NO_PLAN", "BSG_ERR_CUDA", "BSG_ERR_DEVICE_TIMEOUT", "BSG_ERR_OUT_OF_MEMORY",
@@ -62,6 +62,7 @@ _SIGNATURES = {
     "bsg_last_status_word": (ctypes.c_uint32, []),
     "bsg_set_watchdog_ns": (_i, [ctypes.c_uint64]),
     "bsg_set_raster_group": (_i, [_i]),
+    "bsg_set_pdl": (_i, [_i]),
     "bsg_watchdog_selftest": (_i, [ctypes.c_uint64, _vp]),
     "bsg_force_plan": (_i, [ctypes.c_char_p]),
     "bsg_select_plan": (_i, [_i, _i, _i, _i, _i, ctypes.c_char_p, ctypes.c_size_t]),
@@ -224,6 +225,11 @@ def bsg_last_status_word() -> int:
 
 def bsg_set_watchdog_ns(ns: int) -> None:
     _check(load().bsg_set_watchdog_ns(ns), "bsg_set_watchdog_ns")
+
+
+def bsg_set_pdl(on: bool) -> None:
+    """Programmatic dependent launch for later GEMM launches (off by default)."""
+    _check(load().bsg_set_pdl(1 if on else 0), "bsg_set_pdl")
 
 
 def bsg_set_raster_group(m_tiles: int) -> None:

@@ -32,6 +32,7 @@ std::atomic<unsigned long long> g_watchdog_ns{kDefaultWatchdogNs};
 // +0.9 %); L2-resident shapes do not depend on it.
 constexpr int kDefaultRasterGroup = 16;
 std::atomic<int> g_raster_group{kDefaultRasterGroup};
+std::atomic<int> g_pdl{0};              // programmatic dependent launch (off by default)
 std::mutex g_mu;
 int g_forced_plan = -1;                 // guarded by g_mu
 thread_local uint32_t t_last_status_word = 0;
@@ -264,6 +265,7 @@ int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A,
     a.status = ds->status;
     a.timeout_ns = g_watchdog_ns.load();
     set_epilogue(a, epi, D);
+    a.pdl = g_pdl.load();
     if (bsg::skinny_launch(id, maps, a, splits, stream) != cudaSuccess)
         return BSG_ERR_CUDA;
     ++t_last_launches;
@@ -335,6 +337,7 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     a.status = ds->status;
     a.timeout_ns = g_watchdog_ns.load();
     set_epilogue(a, epi, D);
+    a.pdl = g_pdl.load();
     const long long ctas = (long long)a.num_m_tiles * a.num_n_tiles * pi.cta_group;
     const int resident = bsg::max_resident_ctas(plan, ds->sms);
     if (resident < pi.cta_group)
@@ -407,6 +410,7 @@ int run_grouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, c
     a.num_groups = E;
     a.group_offs = offs;
     a.sfb_group_bytes = swizzled_bytes(N, K);
+    a.pdl = g_pdl.load();
     const long long ctas = mt_bound * a.num_n_tiles;
     const int resident = bsg::max_resident_ctas(plan, ds->sms);
     if (resident < 1)
@@ -779,6 +783,14 @@ uint32_t bsg_last_status_word(void) { return t_last_status_word; }
 int bsg_set_watchdog_ns(uint64_t ns)
 {
     g_watchdog_ns.store(ns ? (unsigned long long)ns : kDefaultWatchdogNs);
+    return BSG_OK;
+}
+
+int bsg_set_pdl(int on)
+{
+    if (on != 0 && on != 1)
+        return BSG_ERR_INVALID_ARG;
+    g_pdl.store(on);
     return BSG_OK;
 }
 

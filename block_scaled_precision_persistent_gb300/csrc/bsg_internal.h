@@ -48,6 +48,9 @@ struct GemmArgs {
     int num_groups;
     const int *group_offs;
     size_t sfb_group_bytes;
+    // host only: launch with programmatic stream serialisation (the kernel's
+    // prologue may overlap the previous kernel on the stream)
+    int pdl;
 };
 
 // Kernel instantiations: the plain epilogue, the epilogue variants, and the

@@ -174,6 +174,9 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
     __syncthreads();
     cluster_sync_all();          // both CTAs' barriers exist before any remote use
     tc_fence_after_sync();
+    griddep_wait();              // a dependent launch: the previous grid's writes are visible
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
     const uint32_t tmem = *tmem_slot;
     const int num_tiles = args.num_m_tiles * args.num_n_tiles;
     const int nkb = args.num_k_blocks;
@@ -578,13 +581,15 @@ static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, 
     cfg.blockDim = dim3(T::THREADS, 1, 1);
     cfg.dynamicSmemBytes = T::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = args.pdl ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.d, maps.sfa, maps.sfb, args);
     if (e != cudaSuccess)
         return e;

@@ -167,12 +167,17 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
         tmem_relinquish();
     }
     if constexpr (GROUPED) {
-        if (warp == 2)
+        if (warp == 2) {
+            griddep_wait();      // the routing offsets may come from the previous grid
             build_group_table(args.group_offs, args.num_groups, args.M, s_go, s_gb, lane);
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    griddep_wait();              // a dependent launch: the previous grid's writes are visible
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
     const uint32_t tmem = *tmem_slot;
     // grouped: one 128-row tile row per 128 rows of each slice
     const int num_m_tiles = GROUPED ? s_gb[args.num_groups] : args.num_m_tiles;
@@ -557,7 +562,19 @@ static cudaError_t launch_mode(const GemmMaps &maps, const GemmArgs &args, int g
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
-    kern<<<grid, T::THREADS, smem, stream>>>(maps.a, maps.b, maps.d, args);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(T::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = args.pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, maps.a, maps.b, maps.d, args);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

@@ -227,8 +227,10 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
         mbar_init(rx, 1);
         *abort_flag = 0;
         fence_mbar_init();               // initialised barriers: visible to the TMA unit and the peers
+        griddep_wait();                  // a dependent launch: the previous grid's writes are visible
         for (int i = 0; i < first && producing; ++i)
             producing = produce(i);
+        griddep_launch_dependents();     // the whole grid is resident: the next launch may set up
         if (S > 1)                       // the peers' rows, pushed with complete_tx
             mbar_arrive_expect_tx(rx, (uint32_t)((S - 1) * rpo * live_cols * 4));
     }
@@ -325,6 +327,7 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
         __nv_bfloat16 *const out = reinterpret_cast<__nv_bfloat16 *>(recv + T::RECV_BYTES);
         const int own_lo = (int)rank * rpo;             // rows this CTA owns: [own_lo, own_lo + rpo)
         if constexpr (EPI) {
+            griddep_wait();
             // the epilogue operands into shared memory while the MMAs run:
             // gamma and destination row (-1: not written) of every
             // activation row, bias of the owned weight rows
@@ -467,13 +470,15 @@ static cudaError_t skinny_launch_impl(const GemmMaps &maps, const GemmArgs &args
     cfg.blockDim = dim3(T::THREADS, 1, 1);
     cfg.dynamicSmemBytes = T::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = (unsigned)splits;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = args.pdl ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, maps.b, maps.a, maps.d, args);
     if (e != cudaSuccess)
         return e;

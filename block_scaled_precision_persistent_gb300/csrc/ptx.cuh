@@ -307,6 +307,20 @@ __host__ __device__ constexpr uint32_t idesc_fp8(int M, int N)
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Programmatic dependent launch: wait until the grid this launch depends on
+// has completed and its memory is visible (returns at once for a launch
+// without such a dependency); and let the dependent launch start its
+// prologue early.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Instruction descriptor, kind::f16 with BF16 operands: D format F32 (1) in
 // bits 4..5, A and B format BF16 (1) in bits 7..9 and 10..12, K-major, N>>3
 // in bits 17..22, M>>4 in bits 24..28.

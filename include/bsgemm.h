@@ -292,6 +292,14 @@ BSG_API uint32_t bsg_last_status_word(void);
  * the default of 1e9).                                                    */
 BSG_API int bsg_set_watchdog_ns(uint64_t ns);
 
+/* Programmatic dependent launch for later GEMM launches (1 on, 0 off, the
+ * default): each kernel's prologue (barrier set-up, tensor-memory
+ * allocation, descriptor prefetch) may then overlap the end of the previous
+ * kernel on the same stream; every kernel still waits for that kernel's
+ * completion before its first dependent global access, so results do not
+ * change. Process-wide.                                                    */
+BSG_API int bsg_set_pdl(int on);
+
 /* Tuning lever: M tiles per rasterisation group of the tile kernels (the
  * tile order walks the group's M tiles fastest, so that the CTAs resident at
  * one time share a band of B in L2) for later launches; 0 restores the
