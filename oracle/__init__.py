@@ -94,7 +94,7 @@ class Oracle:
         L.bso_swizzle_scales.restype = ctypes.c_int
         L.bso_swizzle_scales.argtypes = [ctypes.c_int, ctypes.c_int, u8p, u8p]
         L.bso_nvfp4_dense_gemm.restype = ctypes.c_int
-        L.bso_nvfp4_dense_gemm.argtypes = [ctypes.c_int] * 3 + [u8p, u8p, u16p, ctypes.c_float, f32p, f32p,
+        L.bso_nvfp4_dense_gemm.argtypes = [ctypes.c_int] * 3 + [u8p, u8p, u16p, ctypes.c_int, ctypes.c_float, f32p, f32p,
                                                                 i32p, ctypes.c_int, i32p, ctypes.c_int, f64p, f64p,
                                                                 u16p, ctypes.c_int]
         L.bso_nvfp4_grouped_gemm.restype = ctypes.c_int
@@ -199,11 +199,13 @@ class Oracle:
             raise ValueError(f"bso_fp8_gemm rejected its arguments (rc={rc})")
         return S, T, D
 
-    def nvfp4_dense_gemm(self, A, sfA, B_bf16_bits, alpha, K, rows=None, cols=None, nthreads=None,
-                         bias=None, gamma=None):
-        """NVFP4 x dense-BF16 GEMM: A uint8[M, K/2] with sfA uint8[M, K/16],
-        B uint16[N, K] BF16 bit patterns. Returns (S, T, D_bits) over the
-        selected rows x cols, with the epilogue of nvfp4_gemm."""
+    def nvfp4_dense_gemm(self, A, sfA, B_bits, alpha, K, rows=None, cols=None, nthreads=None,
+                         bias=None, gamma=None, b_f16=False):
+        """NVFP4 x dense GEMM: A uint8[M, K/2] with sfA uint8[M, K/16], B
+        uint16[N, K] bit patterns of BF16 (default) or FP16 (b_f16) values.
+        Returns (S, T, D_bits) over the selected rows x cols, with the
+        epilogue of nvfp4_gemm."""
+        B_bf16_bits = B_bits
         A = np.ascontiguousarray(A, dtype=np.uint8)
         sfA = np.ascontiguousarray(sfA, dtype=np.uint8)
         B = np.ascontiguousarray(B_bf16_bits, dtype=np.uint16)
@@ -216,7 +218,8 @@ class Oracle:
         T = np.empty((nr, nc), np.float64)
         D = np.empty((nr, nc), np.uint16)
         rc = self.lib.bso_nvfp4_dense_gemm(M, N, K, self._p(A, ctypes.c_uint8), self._p(sfA, ctypes.c_uint8),
-                                           self._p(B, ctypes.c_uint16), float(alpha), self._p(bias, ctypes.c_float),
+                                           self._p(B, ctypes.c_uint16), 1 if b_f16 else 0, float(alpha),
+                                           self._p(bias, ctypes.c_float),
                                            self._p(gamma, ctypes.c_float), self._p(r, ctypes.c_int32), nr,
                                            self._p(c, ctypes.c_int32), nc, self._p(S, ctypes.c_double),
                                            self._p(T, ctypes.c_double), self._p(D, ctypes.c_uint16),

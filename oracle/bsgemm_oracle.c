@@ -157,7 +157,7 @@ static unsigned nib_a(const uint8_t *row, int k)
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
-    int kind;                     /* 0 = NVFP4, 1 = FP8, 2 = NVFP4 x BF16   */
+    int kind;                     /* 0 = NVFP4, 1 = FP8, 2 = NVFP4 x BF16, 3 = NVFP4 x FP16 */
     int M, N, K;
     const uint8_t *A, *sfA, *B, *sfB;
     double scale;                 /* alpha (NVFP4) or alpha*sA*sB (FP8)       */
@@ -271,6 +271,25 @@ static void epilogue(const job_t *jb, int i, int j, double *S, double *T)
     }
 }
 
+/* IEEE binary16 bit pattern -> its exact value: sign, 5 exponent bits (bias
+ * 15, field 0 subnormal: m * 2^-24), 10 fraction bits; field 31 is Inf/NaN. */
+static double f16_value(uint16_t h)
+{
+    const int sgn = (h >> 15) & 1, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+#ifdef BSO_MUTANT_F16_BIAS16
+        v = ldexp(1024.0 + (double)m, e - 26);
+#else
+        v = ldexp(1024.0 + (double)m, e - 25);
+#endif
+    return sgn ? -v : v;
+}
+
 /* BF16 bit pattern -> its exact value (BF16 is the top half of binary32). */
 static double bf16_value(uint16_t b)
 {
@@ -280,8 +299,8 @@ static double bf16_value(uint16_t b)
     return (double)f;
 }
 
-/* One output element of the NVFP4 x dense-BF16 GEMM: A block-scaled E2M1,
- * B plain BF16 values (B holds uint16 bit patterns, [N][K]):
+/* One output element of the NVFP4 x dense GEMM: A block-scaled E2M1, B plain
+ * BF16 (kind 2) or FP16 (kind 3) values (uint16 bit patterns, [N][K]):
  *   S = alpha * sum_b sA[i][b] * sum_t e2m1(A[i][16b+t]) * B[j][16b+t]    */
 static void dense_element(const job_t *jb, int i, int j, double *S, double *T)
 {
@@ -294,7 +313,7 @@ static void dense_element(const job_t *jb, int i, int j, double *S, double *T)
         double blk = 0.0, blk_abs = 0.0;
         for (int u = 0; u < 16; ++u) {
             int k = 16 * b + u;
-            double p = jb->e2m1_tab[nib_a(ra, k)] * bf16_value(rb[k]);
+            double p = jb->e2m1_tab[nib_a(ra, k)] * (jb->kind == 3 ? f16_value(rb[k]) : bf16_value(rb[k]));
             blk += p;
             blk_abs += fabs(p);
         }
@@ -324,7 +343,7 @@ static void *worker(void *arg)
             else if (jb->kind == 1)
                 fp8_element(jb, i, j, &S, &T);
             else
-                dense_element(jb, i, j, &S, &T);
+                dense_element(jb, i, j, &S, &T);   /* kinds 2 and 3 */
             epilogue(jb, i, j, &S, &T);
             size_t o = (size_t)r * (size_t)jb->ncols + (size_t)c;
             if (jb->S) jb->S[o] = S;
@@ -443,13 +462,14 @@ int bso_fp8_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *B,
 /* NVFP4 x dense-BF16 GEMM ("Triton #11171 - Why Two New NVFP4 Test Cases
  * Produced Twelve Tensor-Memory Failures", opening: an NVFP4-scaled
  * activation times a dense BF16 or FP16 operand): A: uint8[M][K/2] E2M1
- * codes with sfA: uint8[M][K/16] E4M3 block scales, B: uint16[N][K] BF16 bit
- * patterns, each a plain value; bias / gamma as bso_nvfp4_gemm. The sum runs
- * in double block by block (each product a * sA * b has at most 2 + 4 + 8
+ * codes with sfA: uint8[M][K/16] E4M3 block scales, B: uint16[N][K] bit
+ * patterns, each a plain BF16 value (b_f16 = 0) or IEEE binary16 value
+ * (b_f16 = 1); bias / gamma as bso_nvfp4_gemm. The sum runs
+ * in double block by block (each product a * sA * b has at most 2 + 4 + 11
  * significant bits, so it is exact), then the epilogue, then one BF16
  * rounding.                                                                 */
 int bso_nvfp4_dense_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *sfA, const uint16_t *B,
-                         float alpha, const float *bias, const float *gamma,
+                         int b_f16, float alpha, const float *bias, const float *gamma,
                          const int32_t *rows, int nrows, const int32_t *cols, int ncols,
                          double *S, double *T, uint16_t *D, int nthreads)
 {
@@ -461,7 +481,7 @@ int bso_nvfp4_dense_gemm(int M, int N, int K, const uint8_t *A, const uint8_t *s
         return -1;
     job_t jb;
     memset(&jb, 0, sizeof jb);
-    jb.kind = 2;
+    jb.kind = b_f16 ? 3 : 2;
     jb.M = M; jb.N = N; jb.K = K;
     jb.A = A; jb.sfA = sfA; jb.B = (const uint8_t *)(const void *)B;
     jb.scale = (double)alpha;

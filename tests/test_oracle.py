@@ -483,6 +483,53 @@ def pin_dense_numpy(o):
     assert np.array_equal(S2, S[np.ix_(rows, cols)])
 
 
+def pin_dense_f16_worked(o):
+    """tests/golden/nvfp4_dense_f16_case.txt: block-scaled E2M1 A times FP16
+    B, with a value BF16 cannot hold, the smallest subnormal and the largest
+    finite FP16 value."""
+    rows = _rows("nvfp4_dense_f16_case.txt")
+    bsrc = {int(r[1]): (int(r[2], 16), int(r[3], 16)) for r in rows if r[0] == "B"}
+    B = np.array([[bsrc[n][0]] * 16 + [bsrc[n][1]] * 16 for n in (0, 1)], np.uint16)
+    A = pack(np.array([[0x2] * 16 + [0x9] * 16], np.uint8))
+    sfA = np.array([[0x38, 0x48]], np.uint8)
+    S, _, D = o.nvfp4_dense_gemm(A, sfA, B, 1.0, 32, b_f16=True)
+    for r in rows:
+        if r[0] == "S":
+            assert S[int(r[1])].tolist() == [float(v) for v in r[2:]], S
+        elif r[0] == "D":
+            assert oracle.bf16_bits_to_float(D[int(r[1])]).tolist() == [float(v) for v in r[2:]], D
+
+
+def _random_f16_bits(rows, K, seed):
+    """Random finite IEEE binary16 bit patterns over the whole range
+    (normal and subnormal, both signs; exponent field 31 left out)."""
+    rng = np.random.default_rng(seed)
+    bits = rng.integers(0, 1 << 16, (rows, K), dtype=np.uint32).astype(np.uint16)
+    inf_nan = (bits & 0x7C00) == 0x7C00
+    bits[inf_nan] ^= 0x4000
+    return bits
+
+
+def pin_dense_f16_numpy(o):
+    # Independent restatement: dequantised A times B decoded by numpy's own
+    # float16 type, in float64; and FP16 B holding the same values as a
+    # BF16 B (E2M1 values fit both) gives the BF16 result bit for bit.
+    M, N, K = 12, 24, 128
+    A, sfA, Bp, _ = _uniform_problem(M, N, K, 35)
+    B = _random_f16_bits(N, K, 36)
+    S, T, _ = o.nvfp4_dense_gemm(A, sfA, B, 0.5, K, b_f16=True)
+    bv = B.view(np.float16).astype(np.float64)
+    ref = 0.5 * (deq_nvfp4(A, sfA) @ bv.T)
+    assert np.allclose(S, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert np.allclose(T, 0.5 * (np.abs(deq_nvfp4(A, sfA)) @ np.abs(bv).T), rtol=1e-12)
+    codes = np.empty((N, K), np.uint8)
+    codes[:, 0::2], codes[:, 1::2] = Bp & 15, Bp >> 4
+    vals = np.array([E2M1_TABLE[c] for c in codes.reshape(-1)]).reshape(N, K)
+    got = o.nvfp4_dense_gemm(A, sfA, vals.astype(np.float16).view(np.uint16), 0.5, K, b_f16=True)
+    want = o.nvfp4_dense_gemm(A, sfA, _bf16_bits(vals), 0.5, K)
+    assert all(np.array_equal(g, w) for g, w in zip(got, want))
+
+
 def _swizzle_numpy(sf: np.ndarray, K: int) -> np.ndarray:
     """Independent restatement of the 128x4-blocked scale layout by reshapes."""
     rows, cols = sf.shape
@@ -640,7 +687,8 @@ PINS = [pin_e2m1_table, pin_e4m3_codes, pin_bf16_cases, pin_worked_1x1x16, pin_w
         pin_quantize_nearest_bruteforce, pin_quantize_scale_invariance, pin_quantize_amax_element,
         pin_quantize_dequant_bound, pin_epilogue_worked, pin_epilogue_numpy, pin_scatter_permutation,
         pin_grouped_worked, pin_grouped_single_slice_is_plain, pin_grouped_numpy, pin_grouped_scale_layout,
-        pin_dense_worked, pin_dense_reduces_to_nvfp4, pin_dense_numpy]
+        pin_dense_worked, pin_dense_reduces_to_nvfp4, pin_dense_numpy, pin_dense_f16_worked,
+        pin_dense_f16_numpy]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -651,7 +699,7 @@ def test_oracle_pin(pin):
 MUTANTS = ["E2M1_BIAS0", "E2M1_NOSIGN", "E4M3_BIAS8", "SWAP_NIBBLES_A", "DROP_SFB",
            "DROP_LAST_BLOCK", "TRANSPOSE_B", "SWIZZLE_ROWMAJOR_BLOCK", "Q_TIES_AWAY", "Q_NO_SG",
            "Q_SWAP_NIBBLES", "Q_E4M3_CEIL", "EPI_GAMMA_FIRST", "EPI_BIAS_BY_ROW",
-           "GROUP_SHIFT", "DENSE_DROP_SFA"]
+           "GROUP_SHIFT", "DENSE_DROP_SFA", "F16_BIAS16"]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
