@@ -554,26 +554,30 @@ def secondary_grouped(dev, steps: int, pk: dict, psrc: str) -> dict:
 
 
 def secondary_dense(dev, steps: int, pk: dict, psrc: str) -> dict:
-    """NVFP4 activations x dense BF16 weights (nvfp4_dense_gemm): 8192^3 and
-    an 8192 x 256 x 8192 weight GEMM (the pages' case has N = 256). A is
-    expanded to BF16 on the fly and the BF16 tensor core computes, so the
-    roofline is the measured BF16 GEMM peak. CUDA graphs, median per launch."""
+    """NVFP4 activations x dense weights (nvfp4_dense_gemm with BF16 B,
+    nvfp4_dense_f16_gemm with FP16 B): 8192^3 in both, and an 8192 x 256 x
+    8192 weight GEMM (the pages' case has N = 256) in BF16. A is expanded to
+    B's type on the fly and the 16-bit tensor core computes, so the roofline
+    is the measured BF16 GEMM peak (FP16 runs at the same nominal rate).
+    CUDA graphs, median per launch."""
     import block_scaled_precision_persistent_gb300 as bsg
     out = {}
-    for (M, N, K), launches in (((8192, 8192, 8192), 4), ((8192, 256, 8192), 16)):
-        p = workloads.make_dense(M, N, K, seed=1, device=dev)
+    for (M, N, K), launches, f16 in (((8192, 8192, 8192), 4, False), ((8192, 8192, 8192), 4, True),
+                                     ((8192, 256, 8192), 16, False)):
+        p = workloads.make_dense(M, N, K, seed=1, device=dev, b_dtype=torch.float16 if f16 else torch.bfloat16)
         sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
         bsg.nvfp4_swizzle_scales(M, K, p["sfA"], sa)
         D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        dense = bsg.nvfp4_dense_f16_gemm if f16 else bsg.nvfp4_dense_gemm
 
         def call():
-            bsg.nvfp4_dense_gemm(M, N, K, p["A"], sa, p["B"], p["alpha"], None, None, None, M, D)
+            dense(M, N, K, p["A"], sa, p["B"], p["alpha"], None, None, None, M, D)
         us = graph_us({"dense": call}, launches, steps)["dense"]
         call()
         plan = bsg.bsg_last_plan_name()
         tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
-        out[f"{M}x{N}x{K}"] = {"plan": plan, "us": round(us, 2), "tflops": round(tf, 1),
-                               "frac_bf16": round(tf / pk["bf16_tflops"], 4)}
+        out[f"{M}x{N}x{K}" + ("_f16" if f16 else "")] = {"plan": plan, "us": round(us, 2), "tflops": round(tf, 1),
+                                                         "frac_bf16": round(tf / pk["bf16_tflops"], 4)}
         del p, sa, D
     if bsg.bsg_get_device_status() != bsg.BSG_OK:
         raise SystemExit("device status reported an error in the dense GEMM timing")
@@ -761,8 +765,8 @@ def run_reference(args, dist: Dist) -> None:
 
 
 def run_case(args) -> None:
-    """One GEMM shape alone (--case nvfp4:MxNxK, fp8:MxNxK or dense:MxNxK for
-    NVFP4 x dense BF16, optionally a forced --plan), the NVFP4 quantiser on BF16 ROWSxK (--case
+    """One GEMM shape alone (--case nvfp4:MxNxK, fp8:MxNxK, dense:MxNxK or
+    densef16:MxNxK for NVFP4 x dense BF16 / FP16, optionally a forced --plan), the NVFP4 quantiser on BF16 ROWSxK (--case
     quantize:ROWSxK), or a grouped workload (--case grouped:NAME, e.g.
     grouped:moe_e64_t1024_k8): `warmup` untimed then `steps` timed launches,
     inputs resident. Used for profiler captures of a single kernel and for ad-hoc
@@ -838,13 +842,15 @@ def run_case(args) -> None:
 
         def call():
             bsg.nvfp4_gemm_ex(M, N, K, p["A"], sa, p["B"], sb, p["alpha"], eb, eg, es, M, D, s)
-    elif kind == "dense":
-        pd = workloads.make_dense(M, N, K, seed=1, device=dev)
+    elif kind in ("dense", "densef16"):
+        f16 = kind == "densef16"
+        pd = workloads.make_dense(M, N, K, seed=1, device=dev, b_dtype=torch.float16 if f16 else torch.bfloat16)
         sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
         bsg.nvfp4_swizzle_scales(M, K, pd["sfA"], sa, s)
+        dense = bsg.nvfp4_dense_f16_gemm if f16 else bsg.nvfp4_dense_gemm
 
         def call():
-            bsg.nvfp4_dense_gemm(M, N, K, pd["A"], sa, pd["B"], pd["alpha"], None, None, None, M, D, s)
+            dense(M, N, K, pd["A"], sa, pd["B"], pd["alpha"], None, None, None, M, D, s)
     elif kind == "fp8":
         q = workloads.make_fp8(workloads.WORKLOADS["fp8_8192"], dev, M=M, N=N, K=K)
 

@@ -18,6 +18,7 @@ __all__ = [
     "BsgError", "load", "nvfp4_gemm", "nvfp4_gemm_swizzled", "nvfp4_swizzle_scales", "nvfp4_quantize",
     "nvfp4_swizzled_scale_bytes", "nvfp4_gemm_noalloc", "fp8_gemm", "nvfp4_gemm_ex", "fp8_gemm_ex",
     "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes", "nvfp4_dense_gemm",
+    "nvfp4_dense_f16_gemm",
     "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_set_pdl", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_select_plan", "bsg_last_launch_count", "bsg_last_plan_name", "bsg_error_string", "EXPORTED_SYMBOLS",
@@ -53,6 +54,7 @@ _SIGNATURES = {
     "nvfp4_gemm_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "fp8_gemm_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "nvfp4_dense_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
+    "nvfp4_dense_f16_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "nvfp4_grouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp,
                                 _vp]),
     "nvfp4_swizzle_scales_grouped": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp]),
@@ -187,6 +189,13 @@ def nvfp4_dense_gemm(M, N, K, A, sfA_swz, B, alpha, bias, gamma, scatter, m_out,
     weights B[N, K]; the epilogue as nvfp4_gemm_ex."""
     _check(load().nvfp4_dense_gemm(M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), float(alpha), _ptr(bias), _ptr(gamma),
                                    _ptr(scatter), int(m_out), _ptr(D), _stream(stream)), "nvfp4_dense_gemm")
+
+
+def nvfp4_dense_f16_gemm(M, N, K, A, sfA_swz, B, alpha, bias, gamma, scatter, m_out, D, stream=None) -> None:
+    """As nvfp4_dense_gemm with FP16 weights B[N, K]."""
+    _check(load().nvfp4_dense_f16_gemm(M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), float(alpha), _ptr(bias),
+                                       _ptr(gamma), _ptr(scatter), int(m_out), _ptr(D), _stream(stream)),
+           "nvfp4_dense_f16_gemm")
 
 
 def nvfp4_grouped_gemm(E, M, N, K, A, sfA_swz, B, sfB_swz, offs, alpha, bias, gamma, scatter, m_out, D,

@@ -276,7 +276,7 @@ int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A,
 // Encode the maps and launch one persistent GEMM.
 int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const uint8_t *sfa,
              const uint8_t *sfb, const float *sA, const float *sB, float alpha, void *D,
-             cudaStream_t stream, DeviceState *ds, const Epilogue &epi = Epilogue())
+             cudaStream_t stream, DeviceState *ds, const Epilogue &epi = Epilogue(), bool b_f16 = false)
 {
     int plan = -1;
     int rc = choose_plan(kind, M, N, K, ds->sms, &plan);
@@ -327,6 +327,7 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     a.num_n_tiles = (N + pi.bn - 1) / pi.bn;
     a.num_k_blocks = K / pi.k_block;
     a.raster_group = g_raster_group.load();   // M tiles per rasterisation group (L2 reuse of B)
+    a.b_f16 = b_f16 ? 1 : 0;
     a.sf_col_blocks = (K / 16 + 3) / 4;
     a.sfb_row_blocks = (N + 127) / 128;
     a.sfa = sfa;
@@ -722,9 +723,9 @@ int nvfp4_grouped_gemm(int E, int M, int N, int K, const void *A, const void *sf
                        reinterpret_cast<cudaStream_t>(stream), ds);
 }
 
-int nvfp4_dense_gemm(int M, int N, int K, const void *A, const void *sfA_swz, const void *B, float alpha,
-                     const float *bias, const float *gamma, const int32_t *scatter, int m_out, void *D,
-                     bsg_stream_t stream)
+static int dense_gemm(bool b_f16, int M, int N, int K, const void *A, const void *sfA_swz, const void *B,
+                      float alpha, const float *bias, const float *gamma, const int32_t *scatter, int m_out,
+                      void *D, bsg_stream_t stream)
 {
     t_last_launches = 0;
     if (!A || !sfA_swz || !B || !D)
@@ -745,7 +746,21 @@ int nvfp4_dense_gemm(int M, int N, int K, const void *A, const void *sfA_swz, co
     e.scatter = scatter;
     e.m_out = m_out;
     return run_gemm(Kind::NVFP4_BF16, M, N, K, A, B, static_cast<const uint8_t *>(sfA_swz), nullptr, nullptr,
-                    nullptr, alpha, D, reinterpret_cast<cudaStream_t>(stream), ds, e);
+                    nullptr, alpha, D, reinterpret_cast<cudaStream_t>(stream), ds, e, b_f16);
+}
+
+int nvfp4_dense_gemm(int M, int N, int K, const void *A, const void *sfA_swz, const void *B, float alpha,
+                     const float *bias, const float *gamma, const int32_t *scatter, int m_out, void *D,
+                     bsg_stream_t stream)
+{
+    return dense_gemm(false, M, N, K, A, sfA_swz, B, alpha, bias, gamma, scatter, m_out, D, stream);
+}
+
+int nvfp4_dense_f16_gemm(int M, int N, int K, const void *A, const void *sfA_swz, const void *B, float alpha,
+                         const float *bias, const float *gamma, const int32_t *scatter, int m_out, void *D,
+                         bsg_stream_t stream)
+{
+    return dense_gemm(true, M, N, K, A, sfA_swz, B, alpha, bias, gamma, scatter, m_out, D, stream);
 }
 
 int bsg_reserve_workspace(int device, size_t bytes)

@@ -10,7 +10,7 @@
 namespace bsg {
 
 // NVFP4: block-scaled E2M1 x E2M1; FP8: E4M3 x E4M3; NVFP4_BF16: block-scaled
-// E2M1 activations x dense BF16 weights. NVFP4_BF16_TMEM is not a kind of
+// E2M1 activations x dense BF16 (or, with GemmArgs::b_f16, FP16) weights. NVFP4_BF16_TMEM is not a kind of
 // call but a kernel variant of NVFP4_BF16 (the expanded A staged in tensor
 // memory instead of shared memory); its plans report kind NVFP4_BF16.
 enum class Kind : int { NVFP4 = 0, FP8 = 1, NVFP4_BF16 = 2, NVFP4_BF16_TMEM = 3 };
@@ -48,6 +48,9 @@ struct GemmArgs {
     int num_groups;
     const int *group_offs;
     size_t sfb_group_bytes;
+    // NVFP4 x dense kind: B holds FP16 values (A is expanded to FP16 and the
+    // MMA runs kind::f16 with F16 operands) instead of BF16
+    int b_f16;
     // host only: launch with programmatic stream serialisation (the kernel's
     // prologue may overlap the previous kernel on the stream)
     int pdl;

@@ -218,44 +218,99 @@ __device__ __forceinline__ void scatter_chunk(const uint8_t *sbuf, int dst, uint
 }
 
 // ---------------------------------------------------------------------------
-// NVFP4 -> BF16 expansion: the A operand of the NVFP4 x dense-BF16 GEMM. An
-// E2M1 value (at most 2 significant bits, |x| <= 6) times its E4M3 scale (at
-// most 4 significant bits, 2^-9 .. 448) has at most 6 significant bits and
-// lies in BF16's normal range, so the expanded operand is exact and the
-// BF16 MMA computes the definition up to the FP32 accumulation order.
+// NVFP4 -> BF16 / FP16 expansion: the A operand of the NVFP4 x dense GEMM.
+// An E2M1 value (at most 2 significant bits, |x| <= 6) times its E4M3 scale
+// (at most 4 significant bits, 2^-9 .. 448) has at most 6 significant bits
+// and lies in the normal range of BF16 and of FP16, so the expanded operand
+// is exact and the 16-bit MMA computes the definition up to the FP32
+// accumulation order.
 // ---------------------------------------------------------------------------
 
-// Four E2M1 codes (nibbles 0..3 of x, x < 2^16, in element order) -> four
-// BF16 values: elements 0, 1 in w01 and 2, 3 in w23 (low half first). The
-// magnitudes 0 .5 1 1.5 2 3 4 6 are BF16 0x0000 0x3F00 0x3F80 0x3FC0 0x4000
-// 0x4040 0x4080 0x40C0; byte permutes pick their low and high bytes by the
-// code's three magnitude bits and a second pair interleaves them. The codes'
-// sign bits (bits 3, 7, 11, 15 of x) are bit 7 of bytes 0, 1 of x << 4 and of
-// x, so one more permute per word moves them to bits 15 and 31.
-__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t x, uint32_t &w01, uint32_t &w23)
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
-    const uint32_t sel = x & 0x7777u;
-    const uint32_t x4 = x << 4;
-    uint32_t lo, hi, s01, s23;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0xC0800000u), "r"(0xC0804000u), "r"(sel));
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3F3F3F00u), "r"(0x40404040u), "r"(sel));
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(w01) : "r"(lo), "r"(hi), "r"(0x5140u));
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(w23) : "r"(lo), "r"(hi), "r"(0x7362u));
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s01) : "r"(x), "r"(x4), "r"(0x0040u));
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s23) : "r"(x), "r"(x4), "r"(0x1050u));
-    w01 |= s01 & 0x80008000u;
-    w23 |= s23 & 0x80008000u;
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
 }
 
-// An E4M3 scale code (sign bit ignored: scales are unsigned) -> its BF16
-// value in both halves. Normal codes map exponent e to e + 120 with the
-// three mantissa bits on top; subnormals are m * 2^-9.
-__device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t code)
+// The sign bits of eight E2M1 codes (bits 3, 7, ..., 31 of x) at bits 15 and
+// 31 of the four output words: sign bit 8i + 3 is bit 7 of byte i of x << 4,
+// sign bit 8i + 7 bit 7 of byte i of x, so one byte permute per word moves
+// them (the other bits are cleared by the caller's mask).
+__device__ __forceinline__ void e2m1x8_signs(uint32_t x, uint32_t (&s)[4])
 {
-    const uint32_t e = (code >> 3) & 15u, m = code & 7u;
-    const float f = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0x1p-9f;
-    const uint32_t b = __float_as_uint(f) >> 16;
-    return b | (b << 16);
+    const uint32_t x4 = x << 4;
+    s[0] = prmt(x, x4, 0x0040u);
+    s[1] = prmt(x, x4, 0x1050u);
+    s[2] = prmt(x, x4, 0x2060u);
+    s[3] = prmt(x, x4, 0x3070u);
+}
+
+// Eight E2M1 codes (nibble i of x is element i) -> eight BF16 values in four
+// words, element 2w in the low half of word w. The magnitudes 0 .5 1 1.5 2 3
+// 4 6 are BF16 0x0000 0x3F00 0x3F80 0x3FC0 0x4000 0x4040 0x4080 0x40C0; byte
+// permutes pick their low and high bytes by the code's three magnitude bits
+// (the selector nibbles; bit 3 of each is cleared, as it would select sign
+// replication) and a second pair interleaves them.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t x, uint32_t (&w)[4])
+{
+    const uint32_t sel_lo = x & 0x7777u, sel_hi = (x >> 16) & 0x7777u;
+    uint32_t s[4];
+    e2m1x8_signs(x, s);
+    const uint32_t lo_a = prmt(0xC0800000u, 0xC0804000u, sel_lo);
+    const uint32_t hi_a = prmt(0x3F3F3F00u, 0x40404040u, sel_lo);
+    const uint32_t lo_b = prmt(0xC0800000u, 0xC0804000u, sel_hi);
+    const uint32_t hi_b = prmt(0x3F3F3F00u, 0x40404040u, sel_hi);
+    w[0] = prmt(lo_a, hi_a, 0x5140u) | (s[0] & 0x80008000u);
+    w[1] = prmt(lo_a, hi_a, 0x7362u) | (s[1] & 0x80008000u);
+    w[2] = prmt(lo_b, hi_b, 0x5140u) | (s[2] & 0x80008000u);
+    w[3] = prmt(lo_b, hi_b, 0x7362u) | (s[3] & 0x80008000u);
+}
+
+// Eight E2M1 codes -> eight FP16 values, laid out as e2m1x8_to_bf16. In FP16
+// every magnitude (0x0000 0x3800 0x3C00 0x3E00 0x4000 0x4200 0x4400 0x4600)
+// has a zero low byte, so one permute picks four high bytes and two more
+// spread them into the halves.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t x, uint32_t (&w)[4])
+{
+    const uint32_t sel_lo = x & 0x7777u, sel_hi = (x >> 16) & 0x7777u;
+    uint32_t s[4];
+    e2m1x8_signs(x, s);
+    const uint32_t hb_a = prmt(0x3E3C3800u, 0x46444240u, sel_lo);
+    const uint32_t hb_b = prmt(0x3E3C3800u, 0x46444240u, sel_hi);
+    w[0] = prmt(hb_a, 0u, 0x1404u) | (s[0] & 0x80008000u);
+    w[1] = prmt(hb_a, 0u, 0x3424u) | (s[1] & 0x80008000u);
+    w[2] = prmt(hb_b, 0u, 0x1404u) | (s[2] & 0x80008000u);
+    w[3] = prmt(hb_b, 0u, 0x3424u) | (s[3] & 0x80008000u);
+}
+
+// Two E4M3 scale codes (bytes 0 and 1 of pair; sign bits ignored, scales are
+// unsigned) -> their FP16 values, each broadcast to both halves of a word.
+// Every E4M3 value is an FP16 value, so the hardware conversion is exact.
+__device__ __forceinline__ void e4m3x2_to_f16x2(uint32_t pair, uint32_t &s0, uint32_t &s1)
+{
+    const uint16_t p = (uint16_t)(pair & 0x7F7Fu);
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(p));
+    s0 = prmt(h, 0u, 0x1010u);
+    s1 = prmt(h, 0u, 0x3232u);
+}
+
+// The same to BF16: E4M3 -> FP16 -> FP32 -> BF16, each step exact (an E4M3
+// value has at most 4 significant bits and lies within every one of these
+// types' normal range).
+__device__ __forceinline__ void e4m3x2_to_bf16x2(uint32_t pair, uint32_t &s0, uint32_t &s1)
+{
+    const uint16_t p = (uint16_t)(pair & 0x7F7Fu);
+    uint32_t h, b;
+    float f0, f1;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(p));
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(f0), "=f"(f1)
+        : "r"(h));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(f1), "f"(f0));   // f1 to the upper half
+    s0 = prmt(b, 0u, 0x1010u);
+    s1 = prmt(b, 0u, 0x3232u);
 }
 
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
@@ -265,52 +320,46 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
     return d;
 }
 
-// One row of a 64-element stage: 32 packed bytes of E2M1 codes at src
-// (16-byte aligned; element 2i in the low nibble of byte i) and the row's
-// four block scales (byte b of sc scales elements 16b..16b+15) -> 64 BF16 as
-// 32 words, element 2w in the low half of word w.
-__device__ __forceinline__ void expand_row_nvfp4_bf16(const uint8_t *src, uint32_t sc, uint32_t (&w)[32])
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b)
 {
-    const uint4 p0 = *reinterpret_cast<const uint4 *>(src);
-    const uint4 p1 = *reinterpret_cast<const uint4 *>(src + 16);
-    const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint32_t s2 = e4m3_to_bf16x2((sc >> (8 * (c >> 1))) & 0xFFu);
-        uint32_t w0, w1, w2, w3;
-        e2m1x4_to_bf16(words[c] & 0xFFFFu, w0, w1);
-        e2m1x4_to_bf16(words[c] >> 16, w2, w3);
-        w[4 * c] = mul_bf16x2(w0, s2);
-        w[4 * c + 1] = mul_bf16x2(w1, s2);
-        w[4 * c + 2] = mul_bf16x2(w2, s2);
-        w[4 * c + 3] = mul_bf16x2(w3, s2);
-    }
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 // Half a row: elements [32 hc, 32 hc + 32) of the stage's 64 (16 packed
-// bytes at src + 16 hc, scale bytes 2 hc and 2 hc + 1 of sc) -> 16 words,
-// element 2w in the low half of word w. The dense kernels give each half to
-// its own warp, so that the expansion's latency per stage is halved.
-__device__ __forceinline__ void expand_half_row_nvfp4_bf16(const uint8_t *src, uint32_t sc, int hc,
-                                                           uint32_t (&w)[16])
+// bytes at src + 16 hc, scale bytes 2 hc and 2 hc + 1 of sc) -> 16 words of
+// BF16 (F16 = false) or FP16 (F16 = true) pairs, element 2w in the low half
+// of word w. Either product is exact: at most 6 significant bits, between
+// 2^-10 and 2688 in magnitude. The dense kernels give each half to its own
+// warp, so that the expansion's latency per stage is halved.
+template <bool F16>
+__device__ __forceinline__ void expand_half_row_nvfp4(const uint8_t *src, uint32_t sc, int hc, uint32_t (&w)[16])
 {
     const uint4 p = *reinterpret_cast<const uint4 *>(src + 16 * hc);
     const uint32_t words[4] = {p.x, p.y, p.z, p.w};
+    uint32_t s2[2];
+    if constexpr (F16)
+        e4m3x2_to_f16x2(sc >> (16 * hc), s2[0], s2[1]);
+    else
+        e4m3x2_to_bf16x2(sc >> (16 * hc), s2[0], s2[1]);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint32_t s2 = e4m3_to_bf16x2((sc >> (8 * (2 * hc + (c >> 1)))) & 0xFFu);
-        uint32_t w0, w1, w2, w3;
-        e2m1x4_to_bf16(words[c] & 0xFFFFu, w0, w1);
-        e2m1x4_to_bf16(words[c] >> 16, w2, w3);
-        w[4 * c] = mul_bf16x2(w0, s2);
-        w[4 * c + 1] = mul_bf16x2(w1, s2);
-        w[4 * c + 2] = mul_bf16x2(w2, s2);
-        w[4 * c + 3] = mul_bf16x2(w3, s2);
+        uint32_t v[4];
+        if constexpr (F16)
+            e2m1x8_to_f16(words[c], v);
+        else
+            e2m1x8_to_bf16(words[c], v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[4 * c + i] = F16 ? mul_f16x2(v[i], s2[c >> 1]) : mul_bf16x2(v[i], s2[c >> 1]);
     }
 }
 
 // Chunks [4 hc, 4 hc + 4) of row r (expanded half hc) into a 128B-swizzled
-// K-major tile at shared address tile (see store_row_sw128).
+// K-major tile at shared address tile: 16-byte chunk c (elements 8c..8c+7)
+// of row r at r * 128 + ((c ^ (r % 8)) * 16), the layout the MMA's
+// shared-memory descriptor reads.
 __device__ __forceinline__ void store_half_row_sw128(const uint32_t (&w)[16], uint32_t tile, int r, int hc)
 {
     const uint32_t row = tile + (uint32_t)r * 128u;
@@ -318,17 +367,6 @@ __device__ __forceinline__ void store_half_row_sw128(const uint32_t (&w)[16], ui
     for (int c = 0; c < 4; ++c)
         st_shared_v4(row + ((uint32_t)((4 * hc + c) ^ (r & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2],
                      w[4 * c + 3]);
-}
-
-// The expanded row r into a 128B-swizzled K-major tile at shared address
-// tile: 16-byte chunk c (elements 8c..8c+7) at r * 128 + ((c ^ (r % 8)) *
-// 16), the layout the MMA's shared-memory descriptor reads.
-__device__ __forceinline__ void store_row_sw128(const uint32_t (&w)[32], uint32_t tile, int r)
-{
-    const uint32_t row = tile + (uint32_t)r * 128u;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-        st_shared_v4(row + ((uint32_t)(c ^ (r & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
 // Writes one ring stage's NVFP4 block scales from shared memory into the

@@ -101,6 +101,7 @@ struct PairTile {
                                                         : 512;
     static constexpr uint32_t IDESC =
         kFp4 ? idesc_nvfp4(TILE_M, BN) : kDense ? idesc_bf16(TILE_M, BN) : idesc_fp8(TILE_M, BN);
+    static constexpr uint32_t IDESC_F16 = idesc_f16(TILE_M, BN);   // dense kind with FP16 B
 
     static_assert(BN % 128 == 0 && BN <= 256, "pair tile N: B halves of 64 or 128 rows");
     static_assert(TMEM_USED <= 512, "TMEM: accumulators plus scales exceed 512 columns");
@@ -180,6 +181,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
     const uint32_t tmem = *tmem_slot;
     const int num_tiles = args.num_m_tiles * args.num_n_tiles;
     const int nkb = args.num_k_blocks;
+    const bool b_f16 = args.b_f16 != 0;   // dense kind: B (and the expanded A) are FP16, not BF16
     const int cluster_id = blockIdx.x >> 1;
     const int num_clusters = gridDim.x >> 1;
 
@@ -265,6 +267,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
+            const uint32_t idesc = b_f16 ? T::IDESC_F16 : T::IDESC;
             for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
                 if (!mbar_wait(tempty0 + 8u * acc, acc_phase ^ 1u, wd, abort_flag, 2)) {
                     ok = false;
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_nvfp4_pair(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
-                                           desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                           desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                            sfa_t + 4u * j, sfb_t + 4u * j * T::SFB_CHUNKS,
                                            (kb | j) != 0 ? 1u : 0u);
                     } else if constexpr (T::kDense) {
@@ -302,13 +305,13 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_bf16_pair_tmem_a(d_tmem, a_t + (uint32_t)(j * T::MMA_K_BYTES / 4),
-                                                 desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                                 desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                                  (kb | j) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_fp8_pair(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
-                                         desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                         desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                          (kb | j) != 0 ? 1u : 0u);
                     }
                     tc_commit_pair_multicast(empty0 + 8u * stage, 0x3);   // frees the stage in both CTAs
@@ -394,7 +397,10 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                     const uint32_t sc = *reinterpret_cast<const uint32_t *>(apk + T::APK_BYTES + (r & 31) * 16 +
                                                                              (r >> 5) * 4);
                     uint32_t w[16];
-                    expand_half_row_nvfp4_bf16(apk + r * 32, sc, hc, w);
+                    if (b_f16)
+                        expand_half_row_nvfp4<true>(apk + r * 32, sc, hc, w);
+                    else
+                        expand_half_row_nvfp4<false>(apk + r * 32, sc, hc, w);
                     tmem_st_32x32b_x16(tmem + lane_off + (uint32_t)(NUM_ACC * BN + stage * T::A_COLS + 16 * hc), w);
                     tmem_st_wait();
                     tc_fence_before_sync();

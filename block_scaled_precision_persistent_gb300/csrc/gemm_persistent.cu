@@ -95,6 +95,7 @@ struct Tile {
                                      : TMEM_USED <= 256 ? 256
                                                         : 512;
     static constexpr uint32_t IDESC = kFp4 ? idesc_nvfp4(BM, BN) : kDense ? idesc_bf16(BM, BN) : idesc_fp8(BM, BN);
+    static constexpr uint32_t IDESC_F16 = idesc_f16(BM, BN);   // dense kind with FP16 B
 
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile N");
     static_assert(!kFp4 || BN % 128 == 0, "NVFP4 scale blocks cover 128 rows");
@@ -183,6 +184,7 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     const int num_m_tiles = GROUPED ? s_gb[args.num_groups] : args.num_m_tiles;
     const int num_tiles = num_m_tiles * args.num_n_tiles;
     const int nkb = args.num_k_blocks;
+    const bool b_f16 = args.b_f16 != 0;   // dense kind: B (and the expanded A) are FP16, not BF16
     // m tile -> its slice, first row of A, end of the slice's rows
     auto tile_rows = [&](int mt, int &g, int &row0, int &row_end) {
         if constexpr (GROUPED) {
@@ -277,6 +279,7 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
+            const uint32_t idesc = b_f16 ? T::IDESC_F16 : T::IDESC;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 if (!mbar_wait(tempty0 + 8u * acc, acc_phase ^ 1u, wd, abort_flag, 2)) {
                     ok = false;
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_nvfp4(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
-                                      desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                      desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                       sfa_t + 4u * j, sfb_t + 4u * j * T::SFB_CHUNKS,
                                       (kb | j) != 0 ? 1u : 0u);
                     } else if constexpr (T::kTmemA) {
@@ -314,19 +317,19 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_bf16_tmem_a(d_tmem, a_t + (uint32_t)(j * T::MMA_K_BYTES / 4),
-                                            desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                            desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                             (kb | j) != 0 ? 1u : 0u);
                     } else if constexpr (T::kDense) {
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_bf16(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
-                                     desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                     desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                      (kb | j) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_fp8(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
-                                    desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), T::IDESC,
+                                    desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                     (kb | j) != 0 ? 1u : 0u);
                     }
                     tc_commit(empty0 + 8u * stage);   // frees the stage once these MMAs finish
@@ -414,7 +417,10 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                     const uint32_t sc = *reinterpret_cast<const uint32_t *>(apk + T::APK_BYTES + (r & 31) * 16 +
                                                                              (r >> 5) * 4);
                     uint32_t w[16];
-                    expand_half_row_nvfp4_bf16(apk + r * 32, sc, hc, w);
+                    if (b_f16)
+                        expand_half_row_nvfp4<true>(apk + r * 32, sc, hc, w);
+                    else
+                        expand_half_row_nvfp4<false>(apk + r * 32, sc, hc, w);
                     if constexpr (T::kTmemA) {
                         // lane r of this warp's sub-partition, 16 of the stage's 32 A columns
                         tmem_st_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) +

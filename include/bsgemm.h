@@ -207,23 +207,28 @@ BSG_API int fp8_gemm_ex(int M, int N, int K,
                         const int32_t *scatter, int m_out, void *D, bsg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * NVFP4 x dense-BF16 GEMM ("Triton #11171 - Why Two New NVFP4 Test Cases
- * Produced Twelve Tensor-Memory Failures", opening: an NVFP4-scaled
- * activation times a dense BF16 operand, with the shared bias route and the
- * optional gamma and scatter):
+ * NVFP4 x dense-BF16 / dense-FP16 GEMM ("Triton #11171 - Why Two New NVFP4
+ * Test Cases Produced Twelve Tensor-Memory Failures", opening: an
+ * NVFP4-scaled activation times a dense BF16 or FP16 operand, with the
+ * shared bias route and the optional gamma and scatter):
  *   D[dst(m)][n] = bf16_rn( gamma[m] * (alpha * sum_k a(m,k) sA(m,k/16) * b(n,k) + bias[n]) )
  *   A       : uint8[M][K/2] E2M1 codes (element 2i in the low nibble)
  *   sfA_swz : A's E4M3 block scales in the swizzled layout (nvfp4_swizzle_scales)
- *   B       : bf16[N][K] row-major (K contiguous), plain values
- *   bias, gamma, scatter, m_out, D: as nvfp4_gemm_ex
- * The codes times their scales are exact in BF16 (at most 6 significant
- * bits, in range), so the kernel expands A to BF16 and runs the BF16 tensor
- * core; the sum is FP32. Requires K % 64 == 0, N % 8 == 0, 16-byte aligned
+ *   B       : nvfp4_dense_gemm: bf16[N][K]; nvfp4_dense_f16_gemm: IEEE
+ *             binary16 [N][K]; row-major (K contiguous), plain values
+ *   bias, gamma, scatter, m_out, D: as nvfp4_gemm_ex (D is BF16 in both)
+ * The codes times their scales are exact in BF16 and in FP16 (at most 6
+ * significant bits, magnitudes 2^-10 .. 2688), so the kernel expands A to
+ * B's type and runs the 16-bit tensor core; the sum is FP32. Requires K % 64 == 0, N % 8 == 0, 16-byte aligned
  * A, sfA_swz, B, D. One launch; allocates nothing.
  * ------------------------------------------------------------------------- */
 BSG_API int nvfp4_dense_gemm(int M, int N, int K, const void *A, const void *sfA_swz, const void *B,
                              float alpha, const float *bias, const float *gamma, const int32_t *scatter,
                              int m_out, void *D, bsg_stream_t stream);
+
+BSG_API int nvfp4_dense_f16_gemm(int M, int N, int K, const void *A, const void *sfA_swz, const void *B,
+                                 float alpha, const float *bias, const float *gamma, const int32_t *scatter,
+                                 int m_out, void *D, bsg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Grouped (ragged, routed) NVFP4 GEMM -- the MoE expert matmul ("Triton

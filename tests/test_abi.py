@@ -208,10 +208,12 @@ def test_grouped_bad_args(lib):
     assert bsg.nvfp4_grouped_scale_bytes(5, 1000, 512) == oracle.get().grouped_scale_bytes(5, 1000, 512)
 
 
-def test_dense_bad_args_and_plans(lib):
-    """nvfp4_dense_gemm: K % 64, N % 8, nulls, alignment and the epilogue
-    rules are checked before any launch; the planner's dense plans."""
-    d = lambda M, N, K, *p: lib.nvfp4_dense_gemm(M, N, K, *p)  # noqa: E731
+@pytest.mark.parametrize("entry", ["nvfp4_dense_gemm", "nvfp4_dense_f16_gemm"])
+def test_dense_bad_args_and_plans(lib, entry):
+    """nvfp4_dense_gemm / nvfp4_dense_f16_gemm: K % 64, N % 8, nulls,
+    alignment and the epilogue rules are checked before any launch; the
+    planner's dense plans."""
+    d = lambda M, N, K, *p: getattr(lib, entry)(M, N, K, *p)  # noqa: E731
     ok = (BAD, BAD, BAD, 1.0, None, None, None)
     assert d(128, 64, 96, *ok, 128, BAD, None) == bsg.BSG_ERR_INVALID_ARG        # K % 64
     assert d(128, 60, 128, *ok, 128, BAD, None) == bsg.BSG_ERR_INVALID_ARG       # N % 8
