@@ -77,6 +77,7 @@ struct PlanInfo {
     int smem_bytes;            // dynamic shared memory per CTA
     int threads;
     int tmem_cols;
+    int mc = 1;                // CTA pairs per cluster sharing A by multicast (pair plans)
 };
 
 // Encoded tensor maps of one call (sfa / sfb only for CTA-pair NVFP4 plans).

@@ -29,14 +29,25 @@
 // barrier (TMA .cta_group::2); the leader's MMA thread issues the pair MMAs
 // and commits with multicast to both CTAs' empty / accumulator-full
 // barriers; both epilogues arrive on the leader's accumulator-empty barrier.
-// No TMA multicast is used: each CTA fetches its own tiles.
+//
+// Multicast of A (MC = 2; "Together AI Ports ThunderKittens GEMM Kernels to
+// NVIDIA Vera Rubin NVL72", introduction: loads shared across a cluster so
+// that each tile is fetched once for several consumers). A cluster of four
+// CTAs holds two pairs p = 0, 1 on the N tiles 2q and 2q + 1 of the same M
+// tile, so CTA r of either pair needs the same 128 rows of A. Each of the two
+// loads 64 of them and multicasts them to both (TMA .multicast::cluster with
+// .cta_group::2: each copy signals its destination pair's leader barrier),
+// which halves the A bytes each SM fetches from L2. A stage is then refilled
+// only after BOTH pairs' MMAs have read it: every MMA commit that frees a
+// stage goes to all four CTAs' empty barriers, which count two arrivals.
+// With MC = 1 each CTA fetches its own tiles.
 #include "bsg_internal.h"
 #include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace bsg {
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC = 1>
 struct PairTile {
     static constexpr bool kFp4 = KIND == Kind::NVFP4;
     // NVFP4 activations x dense BF16 weights: each CTA expands its own 128
@@ -44,6 +55,7 @@ struct PairTile {
     // stage, with the warps that write NVFP4 scales in the other kind; the
     // leader's pair MMA (kind::f16) reads A from both CTAs' TMEM
     static constexpr bool kDense = KIND == Kind::NVFP4_BF16_TMEM;
+    static constexpr int CLUSTER = 2 * MC;                // CTAs per cluster (MC pairs sharing A)
     static constexpr int BM = 128;                        // rows per CTA
     static constexpr int TILE_M = 256;                    // rows per pair
     static constexpr int ROW_BYTES = 128;
@@ -104,21 +116,23 @@ struct PairTile {
     static constexpr uint32_t IDESC_F16 = idesc_f16(TILE_M, BN);   // dense kind with FP16 B
 
     static_assert(BN % 128 == 0 && BN <= 256, "pair tile N: B halves of 64 or 128 rows");
+    static_assert(MC == 1 || (MC == 2 && !kDense), "A multicast: two pairs, operands loaded by TMA");
     static_assert(TMEM_USED <= 512, "TMEM: accumulators plus scales exceed 512 columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
 };
 
 // EPI: the epilogue-variant instantiation (bias, gamma, scattered rows).
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool EPI>
-__global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
+// MC: pairs per cluster sharing A by multicast (1 or 2).
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC, bool EPI>
+__global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD,
                      const __grid_constant__ CUtensorMap tmSFA,
                      const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args)
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -138,14 +152,17 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t rank = crank & 1u;           // within the pair: 0 leader, 1 peer
+    const uint32_t pidx = crank >> 1;           // pair within the cluster (MC = 2)
+    const uint32_t lead = crank & ~1u;          // cluster rank of this pair's leader
     const bool leader = rank == 0;
     const Watchdog wd{args.status, args.timeout_ns};
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8u * s, 1);
-            mbar_init(empty0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, MC);   // one commit per pair that reads the stage
         }
         for (int a = 0; a < NUM_ACC; ++a) {
             mbar_init(tfull0 + 8u * a, 1);
@@ -179,11 +196,20 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
     if (threadIdx.x == 0)
         griddep_launch_dependents();
     const uint32_t tmem = *tmem_slot;
-    const int num_tiles = args.num_m_tiles * args.num_n_tiles;
+    // a scheduling unit is MC adjacent N tiles of one M tile: pair p of the
+    // cluster takes N tile MC q + p (past the last N tile it computes zeros
+    // from zero-filled loads and stores nothing, but still shares its A)
+    const int num_q = (args.num_n_tiles + MC - 1) / MC;
+    const int num_tiles = args.num_m_tiles * num_q;
     const int nkb = args.num_k_blocks;
     const bool b_f16 = args.b_f16 != 0;   // dense kind: B (and the expanded A) are FP16, not BF16
-    const int cluster_id = blockIdx.x >> 1;
-    const int num_clusters = gridDim.x >> 1;
+    const int cluster_id = blockIdx.x / T::CLUSTER;
+    const int num_clusters = gridDim.x / T::CLUSTER;
+    auto tile_coords = [&](int tile, int &pm, int &nt) {
+        int q;
+        raster_tile(tile, args.raster_group, args.num_m_tiles, num_q, pm, q);
+        nt = q * MC + (int)pidx;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------------
@@ -195,7 +221,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
             bool ok = true;
             for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
                 int pm, nt;
-                raster_tile(tile, args, pm, nt);
+                tile_coords(tile, pm, nt);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wd, abort_flag, 1)) {
                         ok = false;
@@ -203,7 +229,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                     }
                     const uint32_t sa = base + stage * T::STAGE_BYTES;
                     const uint32_t sb = sa + T::A_BYTES;
-                    const uint32_t fb = mapa_shared(full0 + 8u * stage, 0);
+                    const uint32_t fb = mapa_shared(full0 + 8u * stage, lead);
                     if constexpr (T::kFp4) {
                         // scales first, on this CTA's own barrier: its scale warps
                         // write them into its TMEM while A and B are in flight.
@@ -243,7 +269,16 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                     } else {
                         if (leader)
                             mbar_arrive_expect_tx(full0 + 8u * stage, 2u * (T::A_BYTES + T::B_BYTES));
-                        tma_load_2d_pair(sa, &tmA, fb, kb * T::ROW_BYTES, pm * T::TILE_M + (int)rank * T::BM);
+                        if constexpr (MC == 1) {
+                            tma_load_2d_pair(sa, &tmA, fb, kb * T::ROW_BYTES, pm * T::TILE_M + (int)rank * T::BM);
+                        } else {
+                            // rows [64 p, 64 p + 64) of this CTA's 128 A rows, into
+                            // the same offset of CTA r of both pairs
+                            constexpr int QR = T::BM / MC;
+                            tma_load_2d_pair_multicast(sa + pidx * (QR * T::ROW_BYTES), &tmA, fb, kb * T::ROW_BYTES,
+                                                       pm * T::TILE_M + (int)rank * T::BM + (int)pidx * QR,
+                                                       (uint16_t)((1u << rank) | (1u << (2u + rank))));
+                        }
                     }
                     tma_load_2d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN + (int)rank * T::B_ROWS);
                     if (++stage == STAGES) {
@@ -314,7 +349,9 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                                          desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                          (kb | j) != 0 ? 1u : 0u);
                     }
-                    tc_commit_pair_multicast(empty0 + 8u * stage, 0x3);   // frees the stage in both CTAs
+                    // frees the stage in both CTAs (MC = 2: in all four, whose
+                    // A this pair's loads also filled)
+                    tc_commit_pair_multicast(empty0 + 8u * stage, MC == 1 ? 0x3 : 0xF);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -322,7 +359,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                 }
                 if (!ok)
                     break;
-                tc_commit_pair_multicast(tfull0 + 8u * acc, 0x3);          // both epilogues may drain
+                tc_commit_pair_multicast(tfull0 + 8u * acc, (uint16_t)(0x3u << lead));   // both epilogues may drain
                 if (++acc == NUM_ACC) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -367,7 +404,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                         if (leader)
                             mbar_arrive(sfready0 + 8u * stage);
                         else
-                            mbar_arrive_remote_relaxed(mapa_shared(sfready0 + 8u * stage, 0));
+                            mbar_arrive_remote_relaxed(mapa_shared(sfready0 + 8u * stage, lead));
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -409,7 +446,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                         if (leader)
                             mbar_arrive(sfready0 + 8u * stage);
                         else
-                            mbar_arrive_remote_relaxed(mapa_shared(sfready0 + 8u * stage, 0));
+                            mbar_arrive_remote_relaxed(mapa_shared(sfready0 + 8u * stage, lead));
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -438,7 +475,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
         uint32_t acc_phase = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
             int pm, nt;
-            raster_tile(tile, args, pm, nt);
+            tile_coords(tile, pm, nt);
             const int x0 = nt * BN + h * COLS_PER_WARP;            // first column of this warp
             RowEpi re{1.0f, -1};
             if constexpr (EPI) {
@@ -501,7 +538,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
                     if (leader)
                         mbar_arrive(tempty0 + 8u * acc);
                     else
-                        mbar_arrive_remote_relaxed(mapa_shared(tempty0 + 8u * acc, 0));
+                        mbar_arrive_remote_relaxed(mapa_shared(tempty0 + 8u * acc, lead));
                 }
             };
             if constexpr (T::EPI_CHUNKS == 2) {
@@ -571,13 +608,13 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC>::THREADS, 
 // ---------------------------------------------------------------------------
 // Plans and launchers
 // ---------------------------------------------------------------------------
-template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC>
 static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
                                     cudaStream_t stream)
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
-    auto kern = has_epilogue(args) ? gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, true>
-                                   : gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, false>;
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC>;
+    auto kern = has_epilogue(args) ? gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, true>
+                                   : gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_BYTES);
     if (e != cudaSuccess)
@@ -589,7 +626,7 @@ static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, 
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = T::CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -602,21 +639,21 @@ static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, 
     return cudaGetLastError();
 }
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC>
 static int pair_clusters_impl()
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
-    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, false>;   // the EPI instantiation has the same footprint
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC>;
+    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, false>;   // the EPI instantiation has the same footprint
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) !=
         cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
+    cfg.gridDim = dim3(T::CLUSTER, 1, 1);
     cfg.blockDim = dim3(T::THREADS, 1, 1);
     cfg.dynamicSmemBytes = T::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = T::CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -629,28 +666,32 @@ static int pair_clusters_impl()
     return n;
 }
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC>
 static constexpr PlanInfo make_pair_plan(const char *name)
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC>;
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC>;
     // the TMEM-staged dense pair serves calls of kind NVFP4_BF16
     constexpr Kind kind = KIND == Kind::NVFP4_BF16_TMEM ? Kind::NVFP4_BF16 : KIND;
     return PlanInfo{name, kind, Family::PAIR, 2, T::TILE_M, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
-                    T::THREADS, T::TMEM_COLS};
+                    T::THREADS, T::TMEM_COLS, MC};
 }
 
 // The first plan of each kind and shape is the planner's; the shallower
-// rings are there for the stage sweep (bsg_force_plan).
-#define BSG_PAIR_PLANS(X)                                        \
-    X(Kind::NVFP4, 256, 5, 1, "nvfp4_tc2_256x256_s5_acc1")       \
-    X(Kind::NVFP4, 128, 6, 2, "nvfp4_tc2_256x128_s6_acc2")       \
-    X(Kind::FP8, 256, 6, 2, "fp8_tc2_256x256_s6_acc2")           \
-    X(Kind::NVFP4, 256, 4, 1, "nvfp4_tc2_256x256_s4_acc1")       \
-    X(Kind::NVFP4, 256, 3, 1, "nvfp4_tc2_256x256_s3_acc1")       \
-    X(Kind::FP8, 256, 4, 2, "fp8_tc2_256x256_s4_acc2")           \
-    X(Kind::NVFP4_BF16_TMEM, 256, 8, 1, "nvfp4bf16_tc2_256x256_s8_acc1_tmema")
+// rings are there for the stage sweep, the "_mca" plans (two pairs per
+// cluster sharing A by multicast) for the multicast comparison
+// (bsg_force_plan).
+#define BSG_PAIR_PLANS(X)                                              \
+    X(Kind::NVFP4, 256, 5, 1, 1, "nvfp4_tc2_256x256_s5_acc1")          \
+    X(Kind::NVFP4, 128, 6, 2, 1, "nvfp4_tc2_256x128_s6_acc2")          \
+    X(Kind::FP8, 256, 6, 2, 1, "fp8_tc2_256x256_s6_acc2")              \
+    X(Kind::NVFP4, 256, 4, 1, 1, "nvfp4_tc2_256x256_s4_acc1")          \
+    X(Kind::NVFP4, 256, 3, 1, 1, "nvfp4_tc2_256x256_s3_acc1")          \
+    X(Kind::FP8, 256, 4, 2, 1, "fp8_tc2_256x256_s4_acc2")              \
+    X(Kind::NVFP4_BF16_TMEM, 256, 8, 1, 1, "nvfp4bf16_tc2_256x256_s8_acc1_tmema") \
+    X(Kind::NVFP4, 256, 5, 1, 2, "nvfp4_tc2x2_256x256_s5_acc1_mca")    \
+    X(Kind::FP8, 256, 6, 2, 2, "fp8_tc2x2_256x256_s6_acc2_mca")
 
-#define BSG_PAIR_INFO(K, BN, S, A, NAME) make_pair_plan<K, BN, S, A>(NAME),
+#define BSG_PAIR_INFO(K, BN, S, A, MC, NAME) make_pair_plan<K, BN, S, A, MC>(NAME),
 static const PlanInfo kPairPlans[] = {BSG_PAIR_PLANS(BSG_PAIR_INFO)};
 #undef BSG_PAIR_INFO
 
@@ -662,9 +703,9 @@ cudaError_t pair_launch(int id, const GemmMaps &maps, const GemmArgs &args, int 
                         cudaStream_t stream)
 {
     int i = 0;
-#define BSG_PAIR_LAUNCH(K, BN, S, A, NAME)                              \
-    if (id == i)                                                       \
-        return pair_launch_impl<K, BN, S, A>(maps, args, grid, stream); \
+#define BSG_PAIR_LAUNCH(K, BN, S, A, MC, NAME)                              \
+    if (id == i)                                                           \
+        return pair_launch_impl<K, BN, S, A, MC>(maps, args, grid, stream); \
     ++i;
     BSG_PAIR_PLANS(BSG_PAIR_LAUNCH)
 #undef BSG_PAIR_LAUNCH
@@ -674,9 +715,9 @@ cudaError_t pair_launch(int id, const GemmMaps &maps, const GemmArgs &args, int 
 int pair_max_clusters(int id)
 {
     int i = 0;
-#define BSG_PAIR_OCC(K, BN, S, A, NAME)               \
-    if (id == i)                                     \
-        return pair_clusters_impl<K, BN, S, A>();     \
+#define BSG_PAIR_OCC(K, BN, S, A, MC, NAME)            \
+    if (id == i)                                      \
+        return pair_clusters_impl<K, BN, S, A, MC>();  \
     ++i;
     BSG_PAIR_PLANS(BSG_PAIR_OCC)
 #undef BSG_PAIR_OCC
