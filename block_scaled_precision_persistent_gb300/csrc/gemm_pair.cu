@@ -542,9 +542,9 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREA
                 }
             };
             if constexpr (T::EPI_CHUNKS == 2) {
-                // chunk 0 read, converted and staged; chunk 1 read, then TMEM
-                // is released at once -- chunk 1's conversion and both TMA
-                // stores overlap the next tile's MMAs
+                // chunk 0 read and converted; chunk 1 read, then TMEM is
+                // released at once -- staging both chunks, chunk 1's
+                // conversion and both TMA stores overlap the next tile's MMAs
                 uint32_t pk[32];
                 {
                     uint32_t v0[32], v1[32];
@@ -552,12 +552,12 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREA
                     tmem_ld_wait();
                     convert_chunk(0, v0, v1, pk);
                 }
-                stage_out(pk, ebuf);
                 {
                     uint32_t v0[32], v1[32];
                     load_chunk(1, v0, v1);
                     tmem_ld_wait();
                     release();
+                    stage_out(pk, ebuf);
                     store_chunk(0, ebuf);
                     convert_chunk(1, v0, v1, pk);
                 }
