@@ -638,7 +638,35 @@ def cpu_baseline(w: workloads.Workload, p_host: dict, budget_s: float = 15.0) ->
     flops = 2.0 * len(sel) * w.N * w.K
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(sel)} of {w.M} output rows x all {w.N} columns, K={w.K} "
-                      f"({dt:.1f} s of CPU work)", "seconds": dt}
+                      f"({dt:.1f} s of CPU work)", "seconds": dt,
+            "full_matrix_seconds_extrapolated": round(dt * w.M / len(sel), 1)}
+
+
+def cpu_configs() -> dict:
+    """The oracle, as it stands, on the whole of each smaller configuration
+    (every output element): NVFP4 256^3 and 4096^3, FP8 8192^3 and the twelve
+    skinny cells. Inputs are generated on the host with the same seeded
+    recipes as the GPU runs. Opt-in (--cpu-configs): about a minute of CPU."""
+    import oracle
+    o = oracle.get()
+    threads = oracle.default_threads()
+    out = {}
+    names = ["nvfp4_256", "nvfp4_4096", "fp8_8192"] + [n for n in workloads.WORKLOADS if "skinny" in n]
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        if w.kind == "fp8":
+            q = workloads.make_fp8(w, "cpu")
+            args = (q["A"].numpy(), q["B"].numpy(), q["alpha"])
+            t = time.perf_counter()
+            o.fp8_gemm(*args, nthreads=threads)
+        else:
+            p = workloads.make_nvfp4(w, "cpu")
+            args = (p["A"].numpy(), p["sfA"].numpy(), p["B"].numpy(), p["sfB"].numpy(), p["alpha"], w.K)
+            t = time.perf_counter()
+            o.nvfp4_gemm(*args, nthreads=threads)
+        dt = time.perf_counter() - t
+        out[name] = {"seconds": round(dt, 3), "gflops": round(w.flops / dt / 1e9, 2)}
+    return {"cores": threads, "kind": "oracle", "scope": "every output element", "configs": out}
 
 
 def host_copy(step: Nvfp4Step) -> dict:
@@ -692,6 +720,9 @@ def run_ours(args, dist: Dist) -> None:
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, host_copy(step), args.cpu_seconds)
+        cpu["gpu_over_oracle"] = round(value / cpu["value"], 1)
+        if args.cpu_configs:
+            cpu["full_configs"] = cpu_configs()
 
     line = {
         "metric": "NVFP4 GEMM TFLOPS at 16384^3 (whole hot path: scale prep + persistent GEMM)",
@@ -893,6 +924,8 @@ def main() -> None:
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-configs", action="store_true",
+                    help="also time the oracle on every output of the smaller configurations")
     ap.add_argument("--case", default=None,
                     help="time one shape alone instead of the benchmark: nvfp4:MxNxK, fp8:MxNxK or "
                          "quantize:ROWSxK")
