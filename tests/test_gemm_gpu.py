@@ -249,6 +249,33 @@ def check_sampled_nvfp4(p, D, rows, cols, what):
     assert_close(Dh[:, cols], ref, T, f"{what} sampled cols")
 
 
+def test_nvfp4_output_beyond_2g_elements(dev):
+    """Maximum-size edge: D holds more than 2^31 elements (47104^2 BF16,
+    4.4 GB), so output offsets run past 4 GB. Default plan through the
+    row-major entry; rows across the whole range (first, last, and tile rows
+    near the 2^31-element boundary) and columns against the oracle, and the
+    guard tail untouched."""
+    M = N = 47104
+    K = 256
+    A, sfA = workloads.uniform_nvfp4(M, K, 71, dev)
+    B, sfB = workloads.uniform_nvfp4(N, K, 72, dev)
+    p = dict(M=M, N=N, K=K, A=A, sfA=sfA, B=B, sfB=sfB, alpha=0.5)
+    flat, D = new_out(M, N, dev)
+    bsg.nvfp4_gemm(M, N, K, A, sfA, B, sfB, p["alpha"], D)
+    torch.cuda.synchronize()
+    assert bsg.bsg_get_device_status() == bsg.BSG_OK
+    assert_guard(flat)
+    boundary = (1 << 31) // N                     # first row whose elements lie past 2^31
+    rows = [0, 255, boundary - 1, boundary, boundary + 1, 45311, M - 1]
+    cols = [0, 127, 31000, N - 1]
+    _, T, ref = oracle_nvfp4(p, rows=rows)
+    assert_close(bits(D[rows]), ref, T, "beyond 2^31: rows")
+    _, T, ref = oracle_nvfp4(p, cols=cols)
+    assert_close(bits(D[:, cols]), ref, T, "beyond 2^31: cols")
+    del flat, D
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("name", ["nvfp4_4096", "nvfp4_16384"])
 def test_nvfp4_full_size_sampled(dev, name):
     """Full-size workloads in the benchmark's launch configuration (default

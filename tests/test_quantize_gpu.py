@@ -4,7 +4,8 @@ Codes, row-major and swizzled block scales, amax and s_g are compared bit for
 bit (a quantised code is an integer decided in FP32 on both sides). The
 hand-worked case of tests/golden/nvfp4_quantize_case.txt, ragged shapes that
 span several 128-row x 256-element tiles, an all-zero matrix, signed zeros,
-the full 16384 x 16384 size, and a quantise -> GEMM chain are covered.
+the full 16384 x 16384 size, an input of more than 2^31 elements, and a
+quantise -> GEMM chain are covered.
 """
 from __future__ import annotations
 
@@ -128,3 +129,40 @@ def test_quantize_then_gemm(dev):
     _, T, ref = o.nvfp4_gemm(qa[0], qa[1], qb[0], qb[1], alpha, K)
     got = D.view(torch.int16).cpu().numpy().view(np.uint16)
     assert oracle.within_tolerance(got, ref, T).all()
+
+
+def test_quantize_beyond_2g_elements(dev):
+    """Maximum-size edge: 40960 x 53248 BF16 (2.18e9 elements, 4.4 GB), so
+    input and output offsets run past 2^31 elements. N(0,1) data generated on
+    the device with the tensor's largest magnitude planted in the last row;
+    the oracle quantises sampled rows that include it (so its global scale is
+    the whole tensor's) and every output of those rows must match bit for
+    bit, in the codes and in both scale layouts."""
+    rows, K = 40960, 53248
+    g = torch.Generator(device=dev).manual_seed(91)
+    x = torch.randn((rows, K), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    x[rows - 1, K - 7] = -1000.0                 # |x| <= ~7 elsewhere at this size
+    packed = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    swz = torch.empty((bsg.nvfp4_swizzled_scale_bytes(rows, K),), dtype=torch.uint8, device=dev)
+    rm = torch.empty((rows, K // 16), dtype=torch.uint8, device=dev)
+    gl = torch.full((2,), -1.0, dtype=torch.float32, device=dev)
+    bsg.nvfp4_quantize(rows, K, x, packed, swz, rm, gl)
+    torch.cuda.synchronize()
+    assert bsg.bsg_get_device_status() == bsg.BSG_OK
+    sel = [0, 127, 20479, 40191, 40960 - 129, rows - 1]
+    xb = x[sel].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    o = oracle.get()
+    p_ref, sf_ref, amax_ref, sg_ref = o.nvfp4_quantize(xb)
+    glh = gl.cpu().numpy()
+    assert amax_ref == 1000.0 and glh[0] == amax_ref and glh[1] == sg_ref, (glh, amax_ref, sg_ref)
+    assert np.array_equal(packed[sel].cpu().numpy(), p_ref)
+    assert np.array_equal(rm[sel].cpu().numpy(), sf_ref)
+    # swizzled layout: byte of (row, scale column c) in its 128 x 4 block
+    ncb = (K // 16 + 3) // 4
+    sw = swz.cpu().numpy()
+    for i, r in enumerate(sel):
+        c = np.arange(K // 16)
+        off = ((r // 128) * ncb + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
+        assert np.array_equal(sw[off], sf_ref[i]), r
+    del x, packed, swz, rm
+    torch.cuda.empty_cache()
