@@ -180,6 +180,23 @@ int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *ptr, uint
     return r == CUDA_SUCCESS ? BSG_OK : BSG_ERR_CUDA;
 }
 
+// A 3-D view: inner x mid x outer elements, byte strides of mid and outer.
+int encode_3d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t mid, uint64_t outer, uint64_t mid_stride,
+              uint64_t outer_stride, uint32_t box_inner, uint32_t box_mid, uint32_t box_outer)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return BSG_ERR_CUDA;
+    cuuint64_t dims[3] = {inner, mid, outer};
+    cuuint64_t strides[2] = {mid_stride, outer_stride};
+    cuuint32_t box[3] = {box_inner, box_mid, box_outer};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, elem_strides,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BSG_OK : BSG_ERR_CUDA;
+}
+
 // Resident clusters of `splits` CTAs for skinny plan id on the current
 // device (cached; splits a power of two <= 8).
 int skinny_cluster_capacity(int id, int splits)
@@ -310,8 +327,10 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
         if ((rc = encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, sfa, 256,
                             swizzled_bytes(M, K) / 256u, 256, 256, 8, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
                 BSG_OK ||
-            (rc = encode_2d(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, sfb, 256,
-                            swizzled_bytes(N, K) / 256u, 256, 256, 8, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+            // B's: 256-byte rows x (rows of one 128-row block) x row blocks,
+            // so that one copy takes a stage's blocks of all the tile's rows
+            (rc = encode_3d(&maps.sfb, sfb, 256, (uint64_t)K / 32u, ((uint64_t)N + 127u) / 128u, 256,
+                            (uint64_t)K / 32u * 256u, 256, 8, (uint32_t)(pi.bn / 256 > 0 ? 2 : 1))) !=
                 BSG_OK)
             return rc;
     } else {

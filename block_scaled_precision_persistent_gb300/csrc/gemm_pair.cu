@@ -240,12 +240,10 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREA
                         const uint32_t ssfa = sb + T::B_BYTES;
                         const int rba = 2 * pm + (int)rank;
                         tma_load_2d(ssfa, &tmSFA, sfb, 0, (rba * args.sf_col_blocks + 4 * kb) * 2);
-#pragma unroll
-                        for (int c = 0; c < T::SFB_CHUNKS; ++c) {
-                            const int rbb = nt * T::SFB_CHUNKS + c;
-                            tma_load_2d(ssfa + T::SFA_BYTES + c * T::SF_BLOCK_BYTES, &tmSFB, sfb, 0,
-                                        (rbb * args.sf_col_blocks + 4 * kb) * 2);
-                        }
+                        // all SFB_CHUNKS 128-row blocks of B's scales in one
+                        // copy: a 3-D view (256-byte rows, rows of a row block,
+                        // row blocks), box 8 rows x SFB_CHUNKS row blocks
+                        tma_load_3d(ssfa + T::SFA_BYTES, &tmSFB, sfb, 0, 8 * kb, nt * T::SFB_CHUNKS);
                     }
                     if constexpr (T::kDense) {
                         // this CTA's codes and scales on its own expansion
