@@ -45,8 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (plan, workload);
 # the summary it comes from is named in the comment. None = not captured.
 NCU_TRAFFIC_BYTES: dict[tuple[str, str], float] = {
-    # profiles/gemm_pair_nvfp4_256x256_s5_acc1_16384.md (raster group 16): 1.154 GB read + 0.521 GB written
-    ("nvfp4_tc2_256x256_s5_acc1", "nvfp4_16384"): 1153643520 + 521060352,
+    # profiles/gemm_pair_nvfp4_256x256_s5_acc1_16384.md (raster group 16): 1.118 GB read + 0.520 GB written
+    ("nvfp4_tc2_256x256_s5_acc1", "nvfp4_16384"): 1118412544 + 520391680,
 }
 
 
