@@ -669,6 +669,30 @@ def cpu_configs() -> dict:
     return {"cores": threads, "kind": "oracle", "scope": "every output element", "configs": out}
 
 
+def ingress_roofline(bsg, w: workloads.Workload, plan: str, gemm_ms: float, clocks: dict) -> dict | None:
+    """The headline kernel against the rate at which an SM can take operands
+    in: bytes each CTA must load per k-block (its 128 A rows and BN/2 B rows
+    of 128 bytes, A's 2 KiB and B's BN/128 x 2 KiB of block scales) times the
+    k-blocks a CTA runs on average, per SM cycle, against the probe's
+    measured ceiling (bsg_measure_ingress, 32 MiB L2-resident source)."""
+    if not plan.startswith("nvfp4_tc2_256x"):
+        return None
+    bn = int(plan.split("_")[2].split("x")[1])
+    per_kblock = 128 * 128 + (bn // 2) * 128 + 2048 + (bn // 128) * 2048
+    tiles = -(-w.M // 256) * -(-w.N // bn)
+    grid = torch.cuda.get_device_properties(0).multi_processor_count
+    kblocks_per_cta = 2.0 * tiles * (w.K // 256) / grid
+    mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz")
+    if not mhz:
+        return None
+    achieved = kblocks_per_cta * per_kblock / (gemm_ms * 1e-3 * mhz * 1e6)
+    peak, total = bsg.bsg_measure_ingress(32 << 20, 4)
+    return {"bound": "per-SM operand ingress", "bytes_per_kblock_per_cta": per_kblock,
+            "achieved_bytes_per_cycle_per_sm": round(achieved, 2), "peak_bytes_per_cycle_per_sm": round(peak, 2),
+            "frac": round(achieved / peak, 4), "probe_total_gbs": round(total, 1),
+            "cycles": f"SM clock {mhz:.0f} MHz (median sampled under load)"}
+
+
 def host_copy(step: Nvfp4Step) -> dict:
     return {"A": step.A.cpu().numpy(), "sfA": step.sfA.cpu().numpy(), "B": step.B.cpu().numpy(),
             "sfB": step.sfB.cpu().numpy(), "alpha": step.alpha}
@@ -702,6 +726,9 @@ def run_ours(args, dist: Dist) -> None:
     peak = pk["bf16_tflops"] * FP4_PER_BF16
     plan = step.plan()
     traffic = NCU_TRAFFIC_BYTES.get((plan, w.name))
+    ingress = None
+    if dist.rank == 0:
+        ingress = ingress_roofline(bsg, w, plan, gemm_avg, clocks)
 
     e2e = None
     if not args.no_e2e:
@@ -740,7 +767,7 @@ def run_ours(args, dist: Dist) -> None:
                      "kernel": plan,
                      "peak_source": f"{psrc} bf16 burst {pk['bf16_tflops']} x {FP4_PER_BF16:g} "
                                     "(nominal FP4/BF16 dense ratio)",
-                     "frac_of_9pf": round(achieved / 9000.0, 4)},
+                     "frac_of_9pf": round(achieved / 9000.0, 4), "ingress": ingress},
         "e2e": None if e2e is None else
                {k: (round(v, 4) if isinstance(v, float) else v) for k, v in e2e.items()},
         "gpu_launches": launches,

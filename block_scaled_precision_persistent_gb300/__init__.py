@@ -21,6 +21,7 @@ __all__ = [
     "nvfp4_dense_f16_gemm",
     "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_set_pdl", "bsg_watchdog_selftest", "bsg_force_plan",
+    "bsg_measure_ingress",
     "bsg_select_plan", "bsg_last_launch_count", "bsg_last_plan_name", "bsg_error_string", "EXPORTED_SYMBOLS",
     "BSG_OK", "BSG_ERR_INVALID_ARG", "BSG_ERR_MISALIGNED", "BSG_ERR_UNSUPPORTED_DEVICE",
     "BSG_ERR_NO_PLAN", "BSG_ERR_CUDA", "BSG_ERR_DEVICE_TIMEOUT", "BSG_ERR_OUT_OF_MEMORY",
@@ -66,6 +67,7 @@ _SIGNATURES = {
     "bsg_set_raster_group": (_i, [_i]),
     "bsg_set_pdl": (_i, [_i]),
     "bsg_watchdog_selftest": (_i, [ctypes.c_uint64, _vp]),
+    "bsg_measure_ingress": (_i, [ctypes.c_size_t, _i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
     "bsg_force_plan": (_i, [ctypes.c_char_p]),
     "bsg_select_plan": (_i, [_i, _i, _i, _i, _i, ctypes.c_char_p, ctypes.c_size_t]),
     "bsg_last_launch_count": (_i, []),
@@ -248,6 +250,14 @@ def bsg_set_raster_group(m_tiles: int) -> None:
 
 def bsg_watchdog_selftest(ns: int, stream=None) -> None:
     _check(load().bsg_watchdog_selftest(ns, _stream(stream)), "bsg_watchdog_selftest")
+
+
+def bsg_measure_ingress(src_bytes: int = 32 << 20, stages: int = 4) -> tuple[float, float]:
+    """Operand-ingress probe: (bytes per SM clock cycle per SM, total GB/s)."""
+    per_sm, total = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    _check(load().bsg_measure_ingress(int(src_bytes), int(stages), ctypes.byref(per_sm), ctypes.byref(total)),
+           "bsg_measure_ingress")
+    return per_sm.value, total.value
 
 
 def bsg_force_plan(name: str | None) -> None:

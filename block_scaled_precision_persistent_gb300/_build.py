@@ -19,7 +19,7 @@ INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = PKG / "libbsgemm.so"
 SOURCES = ("api.cu", "gemm_persistent.cu", "gemm_pair.cu", "gemm_skinny.cu", "swizzle.cu", "noalloc.cu",
-           "quantize.cu")
+           "quantize.cu", "probe.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden,-O2",
          f"-I{INCLUDE}", f"-I{CSRC}"]

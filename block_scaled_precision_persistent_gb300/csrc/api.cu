@@ -7,6 +7,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 #include <string>
 
 #include "bsg_internal.h"
@@ -852,6 +853,63 @@ int bsg_watchdog_selftest(uint64_t ns, bsg_stream_t stream)
                                    reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return BSG_ERR_CUDA;
     return BSG_OK;
+}
+
+int bsg_measure_ingress(size_t src_bytes, int stages, double *bytes_per_cycle_per_sm, double *total_gbs)
+{
+    if (!bytes_per_cycle_per_sm || stages < 1 || stages > bsg::probe_max_stages() ||
+        src_bytes < (size_t)4 * (size_t)bsg::probe_slot_bytes())
+        return BSG_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc != BSG_OK)
+        return rc;
+    const int iters = 4000;
+    uint8_t *src = nullptr;
+    unsigned long long *cyc = nullptr;
+    cudaStream_t st = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    float ms = 0.0f;
+    rc = BSG_ERR_CUDA;
+    if (cudaMalloc(&src, src_bytes) == cudaSuccess && cudaMalloc(&cyc, sizeof(unsigned long long) * ds->sms) == cudaSuccess &&
+        cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess && cudaEventCreate(&e0) == cudaSuccess &&
+        cudaEventCreate(&e1) == cudaSuccess && cudaMemsetAsync(src, 0x5A, src_bytes, st) == cudaSuccess &&
+        // one untimed pass (first touch of the source), then the timed one
+        bsg::launch_ingress_probe(src, src_bytes, stages, iters, ds->sms, ds->status, g_watchdog_ns.load(), cyc,
+                                  st) == cudaSuccess &&
+        cudaEventRecord(e0, st) == cudaSuccess &&
+        bsg::launch_ingress_probe(src, src_bytes, stages, iters, ds->sms, ds->status, g_watchdog_ns.load(), cyc,
+                                  st) == cudaSuccess &&
+        cudaEventRecord(e1, st) == cudaSuccess && cudaStreamSynchronize(st) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess) {
+        std::vector<unsigned long long> c((size_t)ds->sms);
+        unsigned int word = 0;
+        if (cudaMemcpy(c.data(), cyc, sizeof(unsigned long long) * ds->sms, cudaMemcpyDeviceToHost) == cudaSuccess &&
+            cudaMemcpy(&word, ds->status, sizeof word, cudaMemcpyDeviceToHost) == cudaSuccess) {
+            if (word != 0) {
+                rc = BSG_ERR_DEVICE_TIMEOUT;
+            } else {
+                double mean = 0.0;
+                for (unsigned long long v : c)
+                    mean += (double)v;
+                mean /= (double)ds->sms;
+                const double per_cta = (double)iters * (double)bsg::probe_slot_bytes();
+                *bytes_per_cycle_per_sm = mean > 0.0 ? per_cta / mean : 0.0;
+                if (total_gbs)
+                    *total_gbs = ms > 0.0f ? per_cta * ds->sms / ((double)ms * 1e-3) / 1e9 : 0.0;
+                rc = BSG_OK;
+            }
+        }
+    }
+    if (e0)
+        cudaEventDestroy(e0);
+    if (e1)
+        cudaEventDestroy(e1);
+    if (st)
+        cudaStreamDestroy(st);
+    cudaFree(src);
+    cudaFree(cyc);
+    return rc;
 }
 
 int bsg_force_plan(const char *name)

@@ -134,4 +134,13 @@ cudaError_t launch_nvfp4_quantize(int rows, int K, const void *X, uint8_t *packe
 cudaError_t launch_watchdog_probe(unsigned int *status, unsigned long long ns,
                                   cudaStream_t stream);
 
+// Operand-ingress probe (probe.cu): `ctas` CTAs, one per SM, each keeping
+// `stages` slots of probe_slot_bytes() of bulk copies in flight for `iters`
+// refills; cycles[i] = CTA i's elapsed SM cycles.
+cudaError_t launch_ingress_probe(const uint8_t *src, size_t src_bytes, int stages, int iters, int ctas,
+                                 unsigned int *status, unsigned long long timeout_ns, unsigned long long *cycles,
+                                 cudaStream_t stream);
+int probe_slot_bytes();
+int probe_max_stages();
+
 }  // namespace bsg

@@ -317,6 +317,22 @@ BSG_API int bsg_set_raster_group(int m_tiles);
  * watchdog that faults and hangs nothing.                                 */
 BSG_API int bsg_watchdog_selftest(uint64_t ns, bsg_stream_t stream);
 
+/* Operand-ingress probe: the rate at which one SM takes bytes into its
+ * shared memory through the copy engine with nothing else running -- the
+ * ceiling on a tile kernel's k-block period, whose loaders bring A, B and
+ * their scales into shared memory ("Together AI Ports ThunderKittens GEMM
+ * Kernels to NVIDIA Vera Rubin NVL72", introduction).
+ *   src_bytes : source buffer size (>= 128 KiB); 32 MiB keeps it in L2
+ *   stages    : 1..6 slots of 32 KiB copies in flight per SM
+ *   bytes_per_cycle_per_sm : out, bytes per SM clock cycle, averaged over SMs
+ *   total_gbs : out (may be NULL), bytes of all SMs per second
+ * One CTA per SM, 4000 refills per slot, after one untimed pass. Blocking:
+ * allocates and frees its own buffers and stream, so it is a measurement
+ * routine, not one for a hot path. A wait that runs out returns
+ * BSG_ERR_DEVICE_TIMEOUT (and leaves the status word set, as the GEMMs do). */
+BSG_API int bsg_measure_ingress(size_t src_bytes, int stages, double *bytes_per_cycle_per_sm,
+                                double *total_gbs);
+
 /* Force the planner to one named plan for later calls (NULL or "" = choose
  * automatically). Unknown names return BSG_ERR_NO_PLAN.                    */
 BSG_API int bsg_force_plan(const char *name);

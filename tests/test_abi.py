@@ -224,3 +224,15 @@ def test_dense_bad_args_and_plans(lib, entry):
     assert bsg.bsg_select_plan(2, 4096, 4096, 4096, 152) == "nvfp4bf16_tc1_128x256_s5_acc1_tmema"
     assert bsg.bsg_select_plan(2, 128, 4096, 4096, 152) == "nvfp4bf16_tc1_128x256_s5_acc1_tmema"
     assert bsg.bsg_select_plan(2, 4096, 128, 4096, 152) == "nvfp4bf16_tc1_128x128_s8_acc2_tmema"
+
+
+def test_ingress_probe_bad_args(lib):
+    """bsg_measure_ingress checks its arguments before touching the GPU."""
+    import ctypes
+    out = ctypes.c_double(0.0)
+    m = lib.bsg_measure_ingress
+    m.argtypes = [ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    assert m(32 << 20, 0, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG       # stages < 1
+    assert m(32 << 20, 7, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG       # stages > 6
+    assert m(64 << 10, 2, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG       # source < 128 KiB
+    assert m(32 << 20, 2, None, None) == bsg.BSG_ERR_INVALID_ARG                    # no output
