@@ -260,6 +260,42 @@ class Oracle:
             raise ValueError(f"bso_nvfp4_grouped_gemm rejected its arguments (rc={rc})")
         return S, T, D
 
+    def nvfp4_dense_grouped_gemm(self, A, sfA, B_bits, offs, alpha, K, bias=None, gamma=None, b_f16=False,
+                                 nthreads=None):
+        """Grouped (routed) NVFP4 x dense GEMM ("Triton #11171 - Why Two New
+        NVFP4 Test Cases Produced Twelve Tensor-Memory Failures", section
+        "Ragged mode added routing rather than a plain matrix", with the
+        dense BF16 / FP16 right-hand side of the opening): rows
+        [offs[e], offs[e+1]) of A times B_bits[e]^T for each slice e, each
+        slice exactly nvfp4_dense_gemm on its own rows with bias[e] and its
+        rows' gamma. A: uint8[M, K/2], sfA: uint8[M, K/16] row-major,
+        B_bits: uint16[E, N, K] (BF16, or FP16 with b_f16), offs: int32[E+1]
+        with offs[0] = 0, nondecreasing, offs[E] = M; bias: float32[E, N] or
+        None; gamma: float32[M] or None. Returns (S, T, D_bits), [M, N]."""
+        A = np.ascontiguousarray(A, dtype=np.uint8)
+        sfA = np.ascontiguousarray(sfA, dtype=np.uint8)
+        B = np.ascontiguousarray(B_bits, dtype=np.uint16)
+        offs = [int(v) for v in np.asarray(offs).reshape(-1)]
+        E, N, M = B.shape[0], B.shape[1], A.shape[0]
+        assert B.shape == (E, N, K) and len(offs) == E + 1
+        if offs[0] != 0 or offs[E] != M or any(offs[e] > offs[e + 1] for e in range(E)):
+            raise ValueError("offs must start at 0, not decrease, and end at M")
+        if bias is not None:
+            bias = np.asarray(bias, dtype=np.float32)
+            assert bias.shape == (E, N)
+        gamma = None if gamma is None else np.asarray(gamma, dtype=np.float32).reshape(M)
+        S = np.zeros((M, N), np.float64)
+        T = np.zeros((M, N), np.float64)
+        D = np.zeros((M, N), np.uint16)
+        for e in range(E):
+            r0, r1 = offs[e], offs[e + 1]
+            if r1 == r0:
+                continue
+            S[r0:r1], T[r0:r1], D[r0:r1] = self.nvfp4_dense_gemm(
+                A[r0:r1], sfA[r0:r1], B[e], alpha, K, nthreads=nthreads,
+                bias=None if bias is None else bias[e], gamma=None if gamma is None else gamma[r0:r1], b_f16=b_f16)
+        return S, T, D
+
     def grouped_scale_bytes(self, E: int, M: int, K: int) -> int:
         return int(self.lib.bso_grouped_scale_bytes(E, M, K))
 

@@ -530,6 +530,51 @@ def pin_dense_f16_numpy(o):
     assert all(np.array_equal(g, w) for g, w in zip(got, want))
 
 
+def pin_dense_grouped_worked(o):
+    """tests/golden/nvfp4_dense_grouped_case.txt: two slices, per-slice
+    right-hand side and bias."""
+    want = {int(r[1]): [float(v) for v in r[2:]] for r in _rows("nvfp4_dense_grouped_case.txt") if r[0] == "D"}
+    rows = np.array([[0x2] * 32, [k % 8 for k in range(32)], [0x2] * 32], np.uint8)
+    A = pack(rows)
+    sfA = np.array([[0x40, 0x30], [0x38, 0x38], [0x40, 0x30]], np.uint8)
+    b0 = [[0.25] * 16 + [-3.0] * 16, [1.5] * 32]
+    B = np.stack([_bf16_bits(b0), _bf16_bits(b0[::-1])])
+    bias = np.array([[1, 2], [10, 20]], np.float32)
+    S, _, D = o.nvfp4_dense_grouped_gemm(A, sfA, B, [0, 2, 3], 1.0, 32, bias=bias)
+    for i, row in want.items():
+        assert S[i].tolist() == row and oracle.bf16_bits_to_float(D[i]).tolist() == row, (i, S[i])
+
+
+def pin_dense_grouped_numpy(o):
+    # Independent restatement over ragged slices (one empty), both 16-bit
+    # right-hand-side types: dequantised A rows of slice e times B[e]'s
+    # values, plus bias[e], times the rows' gamma; E = 1 is the plain GEMM.
+    M, N, K = 21, 16, 128
+    A, sfA, _, _ = _uniform_problem(M, N, K, 37)
+    offs = [0, 5, 5, 13, 21]
+    E = len(offs) - 1
+    rng = np.random.default_rng(38)
+    bias = rng.standard_normal((E, N)).astype(np.float32)
+    gamma = rng.standard_normal(M).astype(np.float32)
+    deq = deq_nvfp4(A, sfA)
+    for f16 in (False, True):
+        if f16:
+            B = np.stack([_random_f16_bits(N, K, 39 + e) for e in range(E)])
+            bv = B.view(np.float16).astype(np.float64)
+        else:
+            B = np.stack([_random_bf16(N, K, 39 + e) for e in range(E)])
+            bv = _bits_to_f32(B).astype(np.float64)
+        S, _, _ = o.nvfp4_dense_grouped_gemm(A, sfA, B, offs, 0.75, K, bias=bias, gamma=gamma, b_f16=f16)
+        ref = np.zeros((M, N))
+        for e in range(E):
+            r = slice(offs[e], offs[e + 1])
+            ref[r] = gamma[r, None].astype(np.float64) * (0.75 * (deq[r] @ bv[e].T) + bias[e].astype(np.float64))
+        assert np.allclose(S, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max()), f16
+        S1, T1, D1 = o.nvfp4_dense_grouped_gemm(A, sfA, B[:1], [0, M], 0.75, K, b_f16=f16)
+        S0, T0, D0 = o.nvfp4_dense_gemm(A, sfA, B[0], 0.75, K, b_f16=f16)
+        assert np.array_equal(S1, S0) and np.array_equal(T1, T0) and np.array_equal(D1, D0)
+
+
 def _swizzle_numpy(sf: np.ndarray, K: int) -> np.ndarray:
     """Independent restatement of the 128x4-blocked scale layout by reshapes."""
     rows, cols = sf.shape
@@ -688,7 +733,7 @@ PINS = [pin_e2m1_table, pin_e4m3_codes, pin_bf16_cases, pin_worked_1x1x16, pin_w
         pin_quantize_dequant_bound, pin_epilogue_worked, pin_epilogue_numpy, pin_scatter_permutation,
         pin_grouped_worked, pin_grouped_single_slice_is_plain, pin_grouped_numpy, pin_grouped_scale_layout,
         pin_dense_worked, pin_dense_reduces_to_nvfp4, pin_dense_numpy, pin_dense_f16_worked,
-        pin_dense_f16_numpy]
+        pin_dense_f16_numpy, pin_dense_grouped_worked, pin_dense_grouped_numpy]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
