@@ -547,9 +547,33 @@ def secondary_grouped(dev, steps: int, pk: dict, psrc: str) -> dict:
     g()
     plan = bsg.bsg_last_plan_name()
     del g
+    # the pages' own ragged matrix multiplies routed NVFP4 rows by dense
+    # 16-bit expert weights: the same routing with BF16 weights [E][N][K]
+    # (nvfp4_dense_grouped_gemm), D in token order
+    offs, dst = workloads.routing(w.E, w.tokens, w.top_k, seed=1)
+    offs, dst = offs.to(dev), dst.to(dev)
+    pd = workloads.make_dense_grouped(w.E, w.M, w.N, w.K, seed=1, device=dev)
+    sa = torch.empty(bsg.nvfp4_grouped_scale_bytes(w.E, w.M, w.K), dtype=torch.uint8, device=dev)
+    bsg.nvfp4_swizzle_scales_grouped(w.E, w.M, w.K, offs, pd["sfA"], sa)
+    D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+
+    def dense_call():
+        bsg.nvfp4_dense_grouped_gemm(w.E, w.M, w.N, w.K, pd["A"], sa, pd["B"], offs, pd["alpha"], None, None, dst,
+                                     w.M, D)
+    us = graph_us({"dense": dense_call}, 4, steps)["dense"]
+    dense_call()
+    dplan = bsg.bsg_last_plan_name()
+    if bsg.bsg_get_device_status() != bsg.BSG_OK:
+        raise SystemExit("device status reported an error in the grouped dense GEMM timing")
+    dbytes = w.M * w.K * 9 // 16 + w.E * w.N * w.K * 2 + w.M * w.N * 2
+    dgbs = dbytes / (us * 1e-6) / 1e9
+    dense = {"plan": dplan, "us": round(us, 2), "tflops": round(w.flops / (us * 1e-6) / 1e12, 1),
+             "hbm_gbs": round(dgbs, 1), "frac_hbm": round(dgbs / pk["hbm_gbs"], 4), "algorithmic_bytes": dbytes,
+             "ideal_us": round(max(dbytes / (pk["hbm_gbs"] * 1e9), w.flops / (pk["bf16_tflops"] * 1e12)) * 1e6, 2)}
+    del pd, sa, D
     return {"workload": w.name, "E": w.E, "M": w.M, "N": w.N, "K": w.K, "plan": plan, "variants": out,
             "ideal_us": round(ideal * 1e6, 2), "algorithmic_bytes": w.algorithmic_bytes, "peak_hbm_gbs": pk["hbm_gbs"],
-            "peak_source": psrc,
+            "peak_source": psrc, "dense_bf16_weights": dense,
             "timing": "CUDA graph of 8 back-to-back launches per variant, replayed in turn; median per launch"}
 
 

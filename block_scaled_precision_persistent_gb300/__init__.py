@@ -18,7 +18,7 @@ __all__ = [
     "BsgError", "load", "nvfp4_gemm", "nvfp4_gemm_swizzled", "nvfp4_swizzle_scales", "nvfp4_quantize",
     "nvfp4_swizzled_scale_bytes", "nvfp4_gemm_noalloc", "fp8_gemm", "nvfp4_gemm_ex", "fp8_gemm_ex",
     "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes", "nvfp4_dense_gemm",
-    "nvfp4_dense_f16_gemm",
+    "nvfp4_dense_f16_gemm", "nvfp4_dense_grouped_gemm", "nvfp4_dense_f16_grouped_gemm",
     "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_set_pdl", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_measure_ingress",
@@ -56,6 +56,10 @@ _SIGNATURES = {
     "fp8_gemm_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "nvfp4_dense_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "nvfp4_dense_f16_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
+    "nvfp4_dense_grouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp,
+                                      _vp]),
+    "nvfp4_dense_f16_grouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i,
+                                          _vp, _vp]),
     "nvfp4_grouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp,
                                 _vp]),
     "nvfp4_swizzle_scales_grouped": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp]),
@@ -250,6 +254,23 @@ def bsg_set_raster_group(m_tiles: int) -> None:
 
 def bsg_watchdog_selftest(ns: int, stream=None) -> None:
     _check(load().bsg_watchdog_selftest(ns, _stream(stream)), "bsg_watchdog_selftest")
+
+
+def nvfp4_dense_grouped_gemm(E, M, N, K, A, sfA_swz, B, offs, alpha, bias, gamma, scatter, m_out, D,
+                             stream=None) -> None:
+    """Grouped (routed) NVFP4 x dense BF16 GEMM: rows offs[e]..offs[e+1] of A
+    times B[e] (bf16 [E, N, K]); the epilogue as nvfp4_grouped_gemm."""
+    _check(load().nvfp4_dense_grouped_gemm(E, M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), _ptr(offs), float(alpha),
+                                           _ptr(bias), _ptr(gamma), _ptr(scatter), int(m_out), _ptr(D),
+                                           _stream(stream)), "nvfp4_dense_grouped_gemm")
+
+
+def nvfp4_dense_f16_grouped_gemm(E, M, N, K, A, sfA_swz, B, offs, alpha, bias, gamma, scatter, m_out, D,
+                                 stream=None) -> None:
+    """As nvfp4_dense_grouped_gemm with FP16 right-hand sides."""
+    _check(load().nvfp4_dense_f16_grouped_gemm(E, M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), _ptr(offs),
+                                               float(alpha), _ptr(bias), _ptr(gamma), _ptr(scatter), int(m_out),
+                                               _ptr(D), _stream(stream)), "nvfp4_dense_f16_grouped_gemm")
 
 
 def bsg_measure_ingress(src_bytes: int = 32 << 20, stages: int = 4) -> tuple[float, float]:

@@ -380,9 +380,19 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
 // 128-row tile row per 128 rows of each slice. The slice table is built on
 // the device from offs, so the grid is sized for the bound on the tile rows,
 // ceil(M/128) + E; CTAs past the actual tiles exit at once.
+// True for the dense (NVFP4 x 16-bit) plans the grouped GEMM runs: A staged
+// in TMEM, and room beside the ring for the slice table.
+static bool grouped_dense_plan(const PlanInfo &pi)
+{
+    const size_t n = std::strlen(pi.name);
+    return pi.kind == Kind::NVFP4_BF16 && pi.family == bsg::Family::TC1 && n > 6 &&
+           std::strcmp(pi.name + n - 6, "_tmema") == 0 && pi.smem_bytes + bsg::kGroupTableBytes <= 232448;
+}
+
+// dense: the right-hand sides are 16-bit (BF16, or FP16 with b_f16) [E][N][K]
 int run_grouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, const void *B,
                 const uint8_t *sfb, const int32_t *offs, float alpha, const Epilogue &epi, void *D,
-                cudaStream_t stream, DeviceState *ds)
+                cudaStream_t stream, DeviceState *ds, bool dense = false, bool b_f16 = false)
 {
     const long long mt_bound = (long long)(M + 127) / 128 + E;
     int plan;
@@ -392,24 +402,30 @@ int run_grouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, c
     }
     if (plan >= 0) {
         const PlanInfo &fp = bsg::plan_info(plan);
-        if (fp.kind != Kind::NVFP4 || fp.family != bsg::Family::TC1)
+        if (dense ? !grouped_dense_plan(fp) : (fp.kind != Kind::NVFP4 || fp.family != bsg::Family::TC1))
             return BSG_ERR_NO_PLAN;
     } else {
         // 128-wide tiles while they number at most 4 per SM, else 256-wide
         const long long tiles128 = mt_bound * (long long)((N + 127) / 128);
-        plan = bsg::find_plan(tiles128 <= 4LL * ds->sms ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc1_128x256_s3_acc1");
+        const bool few = tiles128 <= 4LL * ds->sms;
+        plan = bsg::find_plan(dense ? (few ? "nvfp4bf16_tc1_128x128_s8_acc2_tmema" : "nvfp4bf16_tc1_128x256_s5_acc1_tmema")
+                                    : (few ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc1_128x256_s3_acc1"));
         if (plan < 0)
             return BSG_ERR_NO_PLAN;
     }
     const PlanInfo &pi = bsg::plan_info(plan);
     const uint64_t row_bytes = (uint64_t)K / 2u;
+    const uint64_t b_row_bytes = dense ? 2u * (uint64_t)K : row_bytes;
     GemmMaps maps;
     std::memset(&maps, 0, sizeof maps);
     int rc;
-    if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes, 128,
-                        128)) != BSG_OK ||
-        (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, (uint64_t)E * (uint64_t)N,
-                        row_bytes, 128, (uint32_t)pi.bn)) != BSG_OK ||
+    // dense: A's codes unswizzled, 32 bytes a row per 64-K stage (expanded
+    // on the GPU); B 16-bit, 128 bytes a row per stage
+    if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes,
+                        dense ? 32 : 128, 128,
+                        dense ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B)) != BSG_OK ||
+        (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, b_row_bytes, (uint64_t)E * (uint64_t)N,
+                        b_row_bytes, 128, (uint32_t)pi.bn)) != BSG_OK ||
         (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, d_rows(M, epi),
                         (uint64_t)N * 2u, 64, 32)) != BSG_OK)
         return rc;
@@ -434,7 +450,8 @@ int run_grouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, c
     set_epilogue(a, epi, D);
     a.num_groups = E;
     a.group_offs = offs;
-    a.sfb_group_bytes = swizzled_bytes(N, K);
+    a.sfb_group_bytes = dense ? 0 : swizzled_bytes(N, K);
+    a.b_f16 = b_f16 ? 1 : 0;
     a.pdl = g_pdl.load();
     const long long ctas = mt_bound * a.num_n_tiles;
     const int resident = bsg::max_resident_ctas(plan, ds->sms);
@@ -785,6 +802,49 @@ int nvfp4_dense_f16_gemm(int M, int N, int K, const void *A, const void *sfA_swz
                          bsg_stream_t stream)
 {
     return dense_gemm(true, M, N, K, A, sfA_swz, B, alpha, bias, gamma, scatter, m_out, D, stream);
+}
+
+static int dense_grouped_gemm(bool b_f16, int E, int M, int N, int K, const void *A, const void *sfA_swz,
+                              const void *B, const int32_t *offs, float alpha, const float *bias,
+                              const float *gamma, const int32_t *scatter, int m_out, void *D, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    if (!A || !sfA_swz || !B || !D || !offs || E < 1 || E > bsg::kMaxGroups)
+        return BSG_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 64 || (K % 64) != 0 || (N % 8) != 0)
+        return BSG_ERR_INVALID_ARG;
+    int rc = check_epilogue_args(M, bias, gamma, scatter, m_out);
+    if (rc != BSG_OK)
+        return rc;
+    if (!aligned16(A) || !aligned16(sfA_swz) || !aligned16(B) || !aligned16(D) ||
+        (reinterpret_cast<uintptr_t>(offs) & 3u))
+        return BSG_ERR_MISALIGNED;
+    DeviceState *ds = nullptr;
+    if ((rc = current_device(&ds)) != BSG_OK)
+        return rc;
+    Epilogue e;
+    e.bias = bias;
+    e.gamma = gamma;
+    e.scatter = scatter;
+    e.m_out = m_out;
+    return run_grouped(E, M, N, K, A, static_cast<const uint8_t *>(sfA_swz), B, nullptr, offs, alpha, e, D,
+                       reinterpret_cast<cudaStream_t>(stream), ds, true, b_f16);
+}
+
+int nvfp4_dense_grouped_gemm(int E, int M, int N, int K, const void *A, const void *sfA_swz, const void *B,
+                             const int32_t *offs, float alpha, const float *bias, const float *gamma,
+                             const int32_t *scatter, int m_out, void *D, bsg_stream_t stream)
+{
+    return dense_grouped_gemm(false, E, M, N, K, A, sfA_swz, B, offs, alpha, bias, gamma, scatter, m_out, D,
+                              stream);
+}
+
+int nvfp4_dense_f16_grouped_gemm(int E, int M, int N, int K, const void *A, const void *sfA_swz, const void *B,
+                                 const int32_t *offs, float alpha, const float *bias, const float *gamma,
+                                 const int32_t *scatter, int m_out, void *D, bsg_stream_t stream)
+{
+    return dense_grouped_gemm(true, E, M, N, K, A, sfA_swz, B, offs, alpha, bias, gamma, scatter, m_out, D,
+                              stream);
 }
 
 int bsg_reserve_workspace(int device, size_t bytes)

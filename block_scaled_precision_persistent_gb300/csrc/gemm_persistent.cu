@@ -116,8 +116,8 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     using T = Tile<KIND, BN, STAGES, NUM_ACC>;
     constexpr bool EPI = MODE != kModePlain;
     constexpr bool GROUPED = MODE == kModeGrouped;
-    static_assert(!GROUPED || (T::kFp4 && T::SMEM_BYTES + kGroupTableBytes <= 232448),
-                  "grouped GEMM: NVFP4 plans whose shared memory has room for the slice table");
+    static_assert(!GROUPED || ((T::kFp4 || T::kTmemA) && T::SMEM_BYTES + kGroupTableBytes <= 232448),
+                  "grouped GEMM: NVFP4 or TMEM-staged dense plans whose shared memory has room for the slice table");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                         bulk_load(sapk + T::APK_BYTES, args.sfa + ((size_t)mt * args.sf_col_blocks + kb) * 512u,
                                   T::ASF_BYTES, sfb);
                         mbar_arrive_expect_tx(fb, T::B_BYTES);
-                        tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN);
+                        tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, g * args.N + nt * BN);
                     } else {
                         mbar_arrive_expect_tx(fb, T::A_BYTES + T::B_BYTES);
                         tma_load_2d(sa, &tmA, fb, kb * T::ROW_BYTES, row0);
@@ -589,10 +589,13 @@ static cudaError_t launch_impl(const GemmMaps &maps, const GemmArgs &args, int g
                                cudaStream_t stream)
 {
     if (args.group_offs) {
-        if constexpr (KIND == Kind::NVFP4)
+        // grouped GEMMs: NVFP4, and NVFP4 x dense with A staged in TMEM
+        if constexpr (KIND == Kind::NVFP4 ||
+                      (KIND == Kind::NVFP4_BF16_TMEM &&
+                       Tile<KIND, BN, STAGES, NUM_ACC>::SMEM_BYTES + kGroupTableBytes <= 232448))
             return launch_mode<KIND, BN, STAGES, NUM_ACC, kModeGrouped>(maps, args, grid, stream);
         else
-            return cudaErrorInvalidValue;          // grouped GEMMs are NVFP4 only
+            return cudaErrorInvalidValue;
     }
     if (has_epilogue(args))
         return launch_mode<KIND, BN, STAGES, NUM_ACC, kModeEpi>(maps, args, grid, stream);

@@ -261,6 +261,34 @@ BSG_API int nvfp4_grouped_gemm(int E, int M, int N, int K,
                                const float *bias, const float *gamma,
                                const int32_t *scatter, int m_out, void *D, bsg_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Grouped (routed) NVFP4 x dense GEMM: the pages' ragged mode with a dense
+ * BF16 (nvfp4_dense_grouped_gemm) or FP16 (nvfp4_dense_f16_grouped_gemm)
+ * right-hand side ("Triton #11171 - Why Two New NVFP4 Test Cases Produced
+ * Twelve Tensor-Memory Failures", section "Ragged mode added routing rather
+ * than a plain matrix", and its opening for the dense operand):
+ *   for each slice e in [0, E) and offs[e] <= m < offs[e+1]:
+ *     D[dst(m)][n] = bf16_rn( gamma[m] * (alpha * sum_k a(m,k) sA(m,k/16) * b_e(n,k) + bias[e][n]) )
+ *   A       : uint8[M][K/2] E2M1 codes, rows grouped by slice
+ *   sfA_swz : A's scales in the per-slice layout of nvfp4_swizzle_scales_grouped
+ *   B       : 16-bit [E][N][K] row-major (K contiguous), plain values
+ *   offs, bias ([E][N]), gamma, scatter, m_out, D: as nvfp4_grouped_gemm
+ * Requires K % 64 == 0, N % 8 == 0, 16-byte aligned A, sfA_swz, B, D and a
+ * 4-byte aligned offs; 1 <= E <= 1024, slices may be empty. One launch;
+ * allocates nothing. Runs only the plans that stage the expanded A in tensor
+ * memory and leave room for the slice table (a forced plan otherwise gives
+ * BSG_ERR_NO_PLAN).
+ * ------------------------------------------------------------------------- */
+BSG_API int nvfp4_dense_grouped_gemm(int E, int M, int N, int K, const void *A, const void *sfA_swz,
+                                     const void *B, const int32_t *offs, float alpha, const float *bias,
+                                     const float *gamma, const int32_t *scatter, int m_out, void *D,
+                                     bsg_stream_t stream);
+
+BSG_API int nvfp4_dense_f16_grouped_gemm(int E, int M, int N, int K, const void *A, const void *sfA_swz,
+                                         const void *B, const int32_t *offs, float alpha, const float *bias,
+                                         const float *gamma, const int32_t *scatter, int m_out, void *D,
+                                         bsg_stream_t stream);
+
 /* Scale layout of a grouped A: row-major uint8[M][K/16] scales -> the
  * swizzled layout of nvfp4_swizzle_scales applied to each slice on its own,
  * slice e starting at 128-row block row sum_{e'<e} ceil(rows_e' / 128), so

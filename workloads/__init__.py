@@ -293,6 +293,19 @@ def make_grouped(E: int, M: int, N: int, K: int, seed: int, device="cpu", std: f
                 alpha=alpha)
 
 
+def make_dense_grouped(E: int, M: int, N: int, K: int, seed: int, device="cpu", std: float = 1.0,
+                       b_dtype: torch.dtype = torch.bfloat16) -> dict:
+    """Grouped NVFP4 x dense inputs: A two-level NVFP4 (row-major sfA) from
+    N(0, std^2) through BF16, B [E][N][K] = N(0, std^2) drawn in FP32 and
+    rounded to b_dtype, alpha = 1 / s_gA."""
+    A, sfA, sga = nvfp4_quantise(normal_bf16(M, K, SEED_BASE + 13 * seed, std, device))
+    B = torch.randn((E * N, K), generator=_gen(SEED_BASE + 13 * seed + 1, device), device=device,
+                    dtype=torch.float32)
+    B = (B * std if std != 1.0 else B).to(b_dtype).reshape(E, N, K).contiguous()
+    alpha = float(torch.tensor(1.0, dtype=torch.float32) / torch.tensor(sga, dtype=torch.float32))
+    return dict(E=E, M=M, N=N, K=K, A=A, sfA=sfA, B=B, alpha=alpha)
+
+
 def make_dense(M: int, N: int, K: int, seed: int, device="cpu", std: float = 1.0,
                b_dtype: torch.dtype = torch.bfloat16) -> dict:
     """NVFP4 x dense inputs: A two-level NVFP4 (row-major sfA) from
