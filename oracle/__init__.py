@@ -296,6 +296,45 @@ class Oracle:
                 bias=None if bias is None else bias[e], gamma=None if gamma is None else gamma[r0:r1], b_f16=b_f16)
         return S, T, D
 
+    def nvfp4_dense_kgrouped_gemm(self, A, sfA, B_bits, koffs, alpha, K, bias=None, gamma=None, b_f16=False,
+                                  nthreads=None):
+        """Inner-expert (K-ragged) NVFP4 x dense GEMM ("Triton #11171 - Why
+        Two New NVFP4 Test Cases Produced Twelve Tensor-Memory Failures",
+        section "Why `pad_a` represents the K-ragged boundary": the ragged
+        dimension is A's K, padded per slice): K is split into E slices at
+        koffs, and slice e gives its own output
+            D[e] = epilogue( alpha * A[:, K_e] (x) sA  .  B[:, K_e]^T )
+        with bias[e] and gamma -- each slice exactly nvfp4_dense_gemm on its
+        columns. koffs: koffs[0] = 0, nondecreasing, koffs[E] = K, every one
+        a multiple of 16 (a whole scale block). An empty slice sums nothing.
+        A: uint8[M, K/2], sfA: uint8[M, K/16], B_bits: uint16[N, K] (BF16, or
+        FP16 with b_f16). Returns (S, T, D_bits), each [E, M, N]."""
+        A = np.ascontiguousarray(A, dtype=np.uint8)
+        sfA = np.ascontiguousarray(sfA, dtype=np.uint8)
+        B = np.ascontiguousarray(B_bits, dtype=np.uint16)
+        koffs = [int(v) for v in np.asarray(koffs).reshape(-1)]
+        E, M, N = len(koffs) - 1, A.shape[0], B.shape[0]
+        assert A.shape == (M, K // 2) and sfA.shape == (M, K // 16) and B.shape == (N, K)
+        if koffs[0] != 0 or koffs[E] != K or any(koffs[e] > koffs[e + 1] or koffs[e] % 16 for e in range(E)):
+            raise ValueError("koffs must start at 0, not decrease, end at K and fall on 16-element blocks")
+        if bias is not None:
+            bias = np.asarray(bias, dtype=np.float32)
+            assert bias.shape == (E, N)
+        S = np.zeros((E, M, N), np.float64)
+        T = np.zeros((E, M, N), np.float64)
+        D = np.zeros((E, M, N), np.uint16)
+        for e in range(E):
+            k0, k1 = koffs[e], koffs[e + 1]
+            if k1 > k0:
+                a, sa, b, k = A[:, k0 // 2:k1 // 2], sfA[:, k0 // 16:k1 // 16], B[:, k0:k1], k1 - k0
+            else:   # an empty slice: one block of zero codes sums to exactly zero
+                a, sa, b, k = (np.zeros((M, 8), np.uint8), np.full((M, 1), 0x38, np.uint8),
+                               np.zeros((N, 16), np.uint16), 16)
+            S[e], T[e], D[e] = self.nvfp4_dense_gemm(a, sa, b, alpha, k, nthreads=nthreads,
+                                                     bias=None if bias is None else bias[e], gamma=gamma,
+                                                     b_f16=b_f16)
+        return S, T, D
+
     def grouped_scale_bytes(self, E: int, M: int, K: int) -> int:
         return int(self.lib.bso_grouped_scale_bytes(E, M, K))
 

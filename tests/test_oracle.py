@@ -575,6 +575,45 @@ def pin_dense_grouped_numpy(o):
         assert np.array_equal(S1, S0) and np.array_equal(T1, T0) and np.array_equal(D1, D0)
 
 
+def pin_dense_kragged_worked(o):
+    """tests/golden/nvfp4_dense_kragged_case.txt: two slices of K, each its
+    own output, the second with a bias row."""
+    want = {(int(r[1]), int(r[2])): [float(v) for v in r[3:]] for r in _rows("nvfp4_dense_kragged_case.txt")
+            if r[0] == "D"}
+    A = pack(np.array([[0x2] * 32, [k % 8 for k in range(32)]], np.uint8))
+    sfA = np.array([[0x40, 0x30], [0x38, 0x38]], np.uint8)
+    B = _bf16_bits([[0.25] * 16 + [-3.0] * 16, [1.5] * 32])
+    bias = np.array([[0, 0], [100, 0]], np.float32)
+    S, _, D = o.nvfp4_dense_kgrouped_gemm(A, sfA, B, [0, 16, 32], 1.0, 32, bias=bias)
+    for (e, i), row in want.items():
+        assert S[e, i].tolist() == row and oracle.bf16_bits_to_float(D[e, i]).tolist() == row, (e, i, S[e, i])
+
+
+def pin_dense_kragged_partition(o):
+    # The slices' sums partition the whole contraction: without bias the
+    # unrounded sums over any split of K (an empty slice included) add up
+    # to the plain GEMM's, exactly in double for these short sums; and a
+    # numpy restatement of each slice in both 16-bit types.
+    M, N, K = 9, 16, 256
+    A, sfA, _, _ = _uniform_problem(M, N, K, 41)
+    deq = deq_nvfp4(A, sfA)
+    koffs = [0, 48, 48, 160, 256]
+    gamma = np.random.default_rng(42).standard_normal(M).astype(np.float32)
+    for f16 in (False, True):
+        B = _random_f16_bits(N, K, 43) if f16 else _random_bf16(N, K, 43)
+        bv = B.view(np.float16).astype(np.float64) if f16 else _bits_to_f32(B).astype(np.float64)
+        S, T, _ = o.nvfp4_dense_kgrouped_gemm(A, sfA, B, koffs, 0.5, K, b_f16=f16)
+        S0, T0, _ = o.nvfp4_dense_gemm(A, sfA, B, 0.5, K, b_f16=f16)
+        assert np.allclose(S.sum(axis=0), S0, rtol=1e-12, atol=1e-12 * np.abs(S0).max()), f16
+        assert np.allclose(T.sum(axis=0), T0, rtol=1e-12), f16
+        assert not S[1].any()                                    # the empty slice
+        Sg, _, _ = o.nvfp4_dense_kgrouped_gemm(A, sfA, B, koffs, 0.5, K, gamma=gamma, b_f16=f16)
+        for e in range(len(koffs) - 1):
+            k = slice(koffs[e], koffs[e + 1])
+            ref = gamma[:, None].astype(np.float64) * (0.5 * (deq[:, k] @ bv[:, k].T))
+            assert np.allclose(Sg[e], ref, rtol=1e-12, atol=1e-12 * max(np.abs(ref).max(), 1.0)), (f16, e)
+
+
 def _swizzle_numpy(sf: np.ndarray, K: int) -> np.ndarray:
     """Independent restatement of the 128x4-blocked scale layout by reshapes."""
     rows, cols = sf.shape
@@ -733,7 +772,8 @@ PINS = [pin_e2m1_table, pin_e4m3_codes, pin_bf16_cases, pin_worked_1x1x16, pin_w
         pin_quantize_dequant_bound, pin_epilogue_worked, pin_epilogue_numpy, pin_scatter_permutation,
         pin_grouped_worked, pin_grouped_single_slice_is_plain, pin_grouped_numpy, pin_grouped_scale_layout,
         pin_dense_worked, pin_dense_reduces_to_nvfp4, pin_dense_numpy, pin_dense_f16_worked,
-        pin_dense_f16_numpy, pin_dense_grouped_worked, pin_dense_grouped_numpy]
+        pin_dense_f16_numpy, pin_dense_grouped_worked, pin_dense_grouped_numpy, pin_dense_kragged_worked,
+        pin_dense_kragged_partition]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
