@@ -19,6 +19,7 @@ __all__ = [
     "nvfp4_swizzled_scale_bytes", "nvfp4_gemm_noalloc", "fp8_gemm", "nvfp4_gemm_ex", "fp8_gemm_ex",
     "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes", "nvfp4_dense_gemm",
     "nvfp4_dense_f16_gemm", "nvfp4_dense_grouped_gemm", "nvfp4_dense_f16_grouped_gemm",
+    "nvfp4_dense_kgrouped_gemm", "nvfp4_dense_f16_kgrouped_gemm",
     "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_set_pdl", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_measure_ingress",
@@ -58,6 +59,9 @@ _SIGNATURES = {
     "nvfp4_dense_f16_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "nvfp4_dense_grouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp,
                                       _vp]),
+    "nvfp4_dense_kgrouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]),
+    "nvfp4_dense_f16_kgrouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
+                                           _vp]),
     "nvfp4_dense_f16_grouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i,
                                           _vp, _vp]),
     "nvfp4_grouped_gemm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp,
@@ -271,6 +275,21 @@ def nvfp4_dense_f16_grouped_gemm(E, M, N, K, A, sfA_swz, B, offs, alpha, bias, g
     _check(load().nvfp4_dense_f16_grouped_gemm(E, M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), _ptr(offs),
                                                float(alpha), _ptr(bias), _ptr(gamma), _ptr(scatter), int(m_out),
                                                _ptr(D), _stream(stream)), "nvfp4_dense_f16_grouped_gemm")
+
+
+def nvfp4_dense_kgrouped_gemm(E, M, N, K, A, sfA_swz, B, koffs, alpha, bias, gamma, D, stream=None) -> None:
+    """Inner-expert (K-ragged) NVFP4 x dense BF16 GEMM: slice e of K (koffs,
+    device int32[E+1]) gives D[e] (bf16 [E, M, N]) with bias[e] and gamma."""
+    _check(load().nvfp4_dense_kgrouped_gemm(E, M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), _ptr(koffs), float(alpha),
+                                            _ptr(bias), _ptr(gamma), _ptr(D), _stream(stream)),
+           "nvfp4_dense_kgrouped_gemm")
+
+
+def nvfp4_dense_f16_kgrouped_gemm(E, M, N, K, A, sfA_swz, B, koffs, alpha, bias, gamma, D, stream=None) -> None:
+    """As nvfp4_dense_kgrouped_gemm with an FP16 right-hand side."""
+    _check(load().nvfp4_dense_f16_kgrouped_gemm(E, M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), _ptr(koffs),
+                                                float(alpha), _ptr(bias), _ptr(gamma), _ptr(D), _stream(stream)),
+           "nvfp4_dense_f16_kgrouped_gemm")
 
 
 def bsg_measure_ingress(src_bytes: int = 32 << 20, stages: int = 4) -> tuple[float, float]:

@@ -465,6 +465,73 @@ int run_grouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, c
     return BSG_OK;
 }
 
+// K-ragged (inner-expert) NVFP4 x dense GEMM: koffs splits K into E slices
+// and slice e writes rows [e*M, e*M + M) of D. Tiles: E x M/128 x N/BN.
+int run_kgrouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, const void *B, const int32_t *koffs,
+                 float alpha, const Epilogue &epi, void *D, cudaStream_t stream, DeviceState *ds, bool b_f16)
+{
+    const long long m_tiles = (M + 127) / 128;
+    int plan;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        plan = g_forced_plan;
+    }
+    if (plan >= 0) {
+        if (!grouped_dense_plan(bsg::plan_info(plan)))
+            return BSG_ERR_NO_PLAN;
+    } else {
+        const long long tiles128 = (long long)E * m_tiles * (long long)((N + 127) / 128);
+        plan = bsg::find_plan(tiles128 <= 4LL * ds->sms ? "nvfp4bf16_tc1_128x128_s8_acc2_tmema"
+                                                       : "nvfp4bf16_tc1_128x256_s5_acc1_tmema");
+        if (plan < 0)
+            return BSG_ERR_NO_PLAN;
+    }
+    const PlanInfo &pi = bsg::plan_info(plan);
+    const uint64_t row_bytes = (uint64_t)K / 2u;
+    GemmMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    int rc;
+    if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes, 32, 128,
+                        CU_TENSOR_MAP_SWIZZLE_NONE)) != BSG_OK ||
+        (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, 2u * (uint64_t)K, (uint64_t)N,
+                        2u * (uint64_t)K, 128, (uint32_t)pi.bn)) != BSG_OK ||
+        (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)E * (uint64_t)M,
+                        (uint64_t)N * 2u, 64, 32)) != BSG_OK)
+        return rc;
+    maps.sfa = maps.a;
+    maps.sfb = maps.a;
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.num_m_tiles = (int)m_tiles;
+    a.num_n_tiles = (N + pi.bn - 1) / pi.bn;
+    a.num_k_blocks = K / pi.k_block;
+    a.raster_group = g_raster_group.load();
+    a.sf_col_blocks = (K / 16 + 3) / 4;
+    a.sfa = sfa;
+    a.alpha = alpha;
+    a.status = ds->status;
+    a.timeout_ns = g_watchdog_ns.load();
+    set_epilogue(a, epi, D);
+    a.num_groups = E;
+    a.group_offs = koffs;
+    a.k_grouped = 1;
+    a.b_f16 = b_f16 ? 1 : 0;
+    a.pdl = g_pdl.load();
+    const long long ctas = (long long)E * m_tiles * a.num_n_tiles;
+    const int resident = bsg::max_resident_ctas(plan, ds->sms);
+    if (resident < 1)
+        return BSG_ERR_CUDA;
+    const int grid = (int)(ctas < resident ? ctas : resident);
+    if (bsg::launch_gemm(plan, maps, a, grid, stream) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    ++t_last_launches;
+    t_last_plan = pi.name;
+    return BSG_OK;
+}
+
 int check_nvfp4_args(int M, int N, int K, const void *A, const void *sfA, const void *B,
                      const void *sfB, void *D)
 {
@@ -829,6 +896,46 @@ static int dense_grouped_gemm(bool b_f16, int E, int M, int N, int K, const void
     e.m_out = m_out;
     return run_grouped(E, M, N, K, A, static_cast<const uint8_t *>(sfA_swz), B, nullptr, offs, alpha, e, D,
                        reinterpret_cast<cudaStream_t>(stream), ds, true, b_f16);
+}
+
+static int dense_kgrouped_gemm(bool b_f16, int E, int M, int N, int K, const void *A, const void *sfA_swz,
+                               const void *B, const int32_t *koffs, float alpha, const float *bias,
+                               const float *gamma, void *D, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    if (!A || !sfA_swz || !B || !D || !koffs || E < 1 || E > bsg::kMaxGroups)
+        return BSG_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 64 || (K % 64) != 0 || (N % 8) != 0)
+        return BSG_ERR_INVALID_ARG;
+    int rc = check_epilogue_args(M, bias, gamma, nullptr, M);
+    if (rc != BSG_OK)
+        return rc;
+    if (!aligned16(A) || !aligned16(sfA_swz) || !aligned16(B) || !aligned16(D) ||
+        (reinterpret_cast<uintptr_t>(koffs) & 3u))
+        return BSG_ERR_MISALIGNED;
+    DeviceState *ds = nullptr;
+    if ((rc = current_device(&ds)) != BSG_OK)
+        return rc;
+    Epilogue e;
+    e.bias = bias;
+    e.gamma = gamma;
+    e.m_out = M;
+    return run_kgrouped(E, M, N, K, A, static_cast<const uint8_t *>(sfA_swz), B, koffs, alpha, e, D,
+                        reinterpret_cast<cudaStream_t>(stream), ds, b_f16);
+}
+
+int nvfp4_dense_kgrouped_gemm(int E, int M, int N, int K, const void *A, const void *sfA_swz, const void *B,
+                              const int32_t *koffs, float alpha, const float *bias, const float *gamma, void *D,
+                              bsg_stream_t stream)
+{
+    return dense_kgrouped_gemm(false, E, M, N, K, A, sfA_swz, B, koffs, alpha, bias, gamma, D, stream);
+}
+
+int nvfp4_dense_f16_kgrouped_gemm(int E, int M, int N, int K, const void *A, const void *sfA_swz, const void *B,
+                                  const int32_t *koffs, float alpha, const float *bias, const float *gamma, void *D,
+                                  bsg_stream_t stream)
+{
+    return dense_kgrouped_gemm(true, E, M, N, K, A, sfA_swz, B, koffs, alpha, bias, gamma, D, stream);
 }
 
 int nvfp4_dense_grouped_gemm(int E, int M, int N, int K, const void *A, const void *sfA_swz, const void *B,

@@ -48,6 +48,10 @@ struct GemmArgs {
     int num_groups;
     const int *group_offs;
     size_t sfb_group_bytes;
+    // K-ragged (inner-expert) GEMM, read only by the KGROUPED instantiation:
+    // group_offs (device int32[E+1]) splits K instead of M, and slice e
+    // writes rows [e*M, e*M + M) of D with bias + e*N
+    int k_grouped;
     // NVFP4 x dense kind: B holds FP16 values (A is expanded to FP16 and the
     // MMA runs kind::f16 with F16 operands) instead of BF16
     int b_f16;
@@ -56,9 +60,10 @@ struct GemmArgs {
     int pdl;
 };
 
-// Kernel instantiations: the plain epilogue, the epilogue variants, and the
-// grouped GEMM (which always has the variants' epilogue).
-enum KernelMode : int { kModePlain = 0, kModeEpi = 1, kModeGrouped = 2 };
+// Kernel instantiations: the plain epilogue, the epilogue variants, the
+// grouped GEMM and the K-ragged GEMM (both always with the variants'
+// epilogue).
+enum KernelMode : int { kModePlain = 0, kModeEpi = 1, kModeGrouped = 2, kModeKGrouped = 3 };
 
 // True when a call needs the epilogue-variant kernels.
 inline bool has_epilogue(const GemmArgs &a) { return a.bias || a.gamma || a.scatter; }

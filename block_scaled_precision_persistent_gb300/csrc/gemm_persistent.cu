@@ -116,8 +116,11 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     using T = Tile<KIND, BN, STAGES, NUM_ACC>;
     constexpr bool EPI = MODE != kModePlain;
     constexpr bool GROUPED = MODE == kModeGrouped;
+    constexpr bool KGROUPED = MODE == kModeKGrouped;
     static_assert(!GROUPED || ((T::kFp4 || T::kTmemA) && T::SMEM_BYTES + kGroupTableBytes <= 232448),
                   "grouped GEMM: NVFP4 or TMEM-staged dense plans whose shared memory has room for the slice table");
+    static_assert(!KGROUPED || (T::kTmemA && T::SMEM_BYTES + kGroupTableBytes <= 232448),
+                  "K-ragged GEMM: TMEM-staged dense plans whose shared memory has room for the slice table");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -167,10 +170,11 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
         tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
         tmem_relinquish();
     }
-    if constexpr (GROUPED) {
+    if constexpr (GROUPED || KGROUPED) {
         if (warp == 2) {
-            griddep_wait();      // the routing offsets may come from the previous grid
-            build_group_table(args.group_offs, args.num_groups, args.M, s_go, s_gb, lane);
+            griddep_wait();      // the offsets may come from the previous grid
+            // slice boundaries over M (routed rows) or over K (K-ragged)
+            build_group_table(args.group_offs, args.num_groups, KGROUPED ? args.K : args.M, s_go, s_gb, lane);
         }
     }
     tc_fence_before_sync();
@@ -182,7 +186,9 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     // grouped: one 128-row tile row per 128 rows of each slice
     const int num_m_tiles = GROUPED ? s_gb[args.num_groups] : args.num_m_tiles;
-    const int num_tiles = num_m_tiles * args.num_n_tiles;
+    // K-ragged: every slice of K is a whole M x N problem of its own
+    const int tiles_per_slice = num_m_tiles * args.num_n_tiles;
+    const int num_tiles = KGROUPED ? args.num_groups * tiles_per_slice : tiles_per_slice;
     const int nkb = args.num_k_blocks;
     const bool b_f16 = args.b_f16 != 0;   // dense kind: B (and the expanded A) are FP16, not BF16
     // m tile -> its slice, first row of A, end of the slice's rows
@@ -197,6 +203,24 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
             row_end = args.M;
         }
     };
+    // tile -> its m / n tile, slice, rows, and k-blocks [kb0, kb1): all of K,
+    // or (K-ragged) the slice's k-blocks, with g the K slice
+    auto tile_pos = [&](int tile, int &mt, int &nt, int &g, int &row0, int &row_end, int &kb0, int &kb1) {
+        int ks = 0;
+        if constexpr (KGROUPED) {
+            ks = tile / tiles_per_slice;
+            tile -= ks * tiles_per_slice;
+        }
+        raster_tile(tile, args.raster_group, num_m_tiles, args.num_n_tiles, mt, nt);
+        tile_rows(mt, g, row0, row_end);
+        kb0 = 0;
+        kb1 = nkb;
+        if constexpr (KGROUPED) {
+            g = ks;
+            kb0 = s_go[ks] / T::K_BLOCK;
+            kb1 = s_go[ks + 1] / T::K_BLOCK;
+        }
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------------
@@ -207,11 +231,11 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
             uint32_t phase = 0, armed_mask = 0, armed_parity = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                int mt, nt, g, row0, row_end;
-                raster_tile(tile, args.raster_group, num_m_tiles, args.num_n_tiles, mt, nt);
-                tile_rows(mt, g, row0, row_end);
-                const uint8_t *const sfb_g = args.sfb + (size_t)g * args.sfb_group_bytes;
-                for (int kb = 0; kb < nkb; ++kb) {
+                int mt, nt, g, row0, row_end, kb0, kb1;
+                tile_pos(tile, mt, nt, g, row0, row_end, kb0, kb1);
+                const uint8_t *const sfb_g = args.sfb + (size_t)(GROUPED ? g : 0) * args.sfb_group_bytes;
+                const int b_row0 = (GROUPED ? g * args.N : 0) + nt * BN;   // a routed slice's own weights
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wd, abort_flag, 1)) {
                         ok = false;
                         break;
@@ -247,11 +271,11 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                         bulk_load(sapk + T::APK_BYTES, args.sfa + ((size_t)mt * args.sf_col_blocks + kb) * 512u,
                                   T::ASF_BYTES, sfb);
                         mbar_arrive_expect_tx(fb, T::B_BYTES);
-                        tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, g * args.N + nt * BN);
+                        tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, b_row0);
                     } else {
                         mbar_arrive_expect_tx(fb, T::A_BYTES + T::B_BYTES);
                         tma_load_2d(sa, &tmA, fb, kb * T::ROW_BYTES, row0);
-                        tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, g * args.N + nt * BN);
+                        tma_load_2d(sb, &tmB, fb, kb * T::ROW_BYTES, b_row0);
                     }
                     armed_mask |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -287,7 +311,14 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < nkb; ++kb) {
+                int kb0 = 0, kb1 = nkb;
+                if constexpr (KGROUPED) {
+                    int mt, nt, g, row0, row_end;
+                    tile_pos(tile, mt, nt, g, row0, row_end, kb0, kb1);
+                }
+                // (a K-ragged slice with no k-blocks issues no MMA: its
+                // epilogue reads the accumulator as zero)
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(full0 + 8u * stage, phase, wd, abort_flag, 3)) {
                         ok = false;
                         break;
@@ -311,26 +342,26 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                             mma_nvfp4(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
                                       desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                       sfa_t + 4u * j, sfb_t + 4u * j * T::SFB_CHUNKS,
-                                      (kb | j) != 0 ? 1u : 0u);
+                                      (kb != kb0 || j != 0) ? 1u : 0u);
                     } else if constexpr (T::kTmemA) {
                         const uint32_t a_t = tmem + (uint32_t)(NUM_ACC * BN + stage * T::A_COLS);
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_bf16_tmem_a(d_tmem, a_t + (uint32_t)(j * T::MMA_K_BYTES / 4),
                                             desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
-                                            (kb | j) != 0 ? 1u : 0u);
+                                            (kb != kb0 || j != 0) ? 1u : 0u);
                     } else if constexpr (T::kDense) {
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_bf16(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
                                      desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
-                                     (kb | j) != 0 ? 1u : 0u);
+                                     (kb != kb0 || j != 0) ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j)
                             mma_fp8(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
                                     desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
-                                    (kb | j) != 0 ? 1u : 0u);
+                                    (kb != kb0 || j != 0) ? 1u : 0u);
                     }
                     tc_commit(empty0 + 8u * stage);   // frees the stage once these MMAs finish
                     if (++stage == STAGES) {
@@ -405,7 +436,12 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                for (int kb = 0; kb < nkb; ++kb) {
+                int kb0 = 0, kb1 = nkb;
+                if constexpr (KGROUPED) {
+                    int mt, nt, g, row0, row_end;
+                    tile_pos(tile, mt, nt, g, row0, row_end, kb0, kb1);
+                }
+                for (int kb = kb0; kb < kb1; ++kb) {
                     // the stage's codes were reloaded after the MMAs that read
                     // its previous expansion completed (empty -> producer)
                     if (!warp_wait(sffull0 + 8u * stage, phase, wd, abort_flag, 6, lane)) {
@@ -459,17 +495,22 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
         int acc = 0, buf = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            int mt, nt, g, row0, row_end;
-            raster_tile(tile, args.raster_group, num_m_tiles, args.num_n_tiles, mt, nt);
-            tile_rows(mt, g, row0, row_end);
+            int mt, nt, g, row0, row_end, kb0, kb1;
+            tile_pos(tile, mt, nt, g, row0, row_end, kb0, kb1);
             const float *const bias = args.bias ? args.bias + (size_t)g * args.N : nullptr;
             const int y = row0 + q * 32;              // first row of this warp's 32
-            // rows of the warp that TMA could store past the slice's end: the
-            // warp stores its rows one by one instead (as scattered rows)
-            const bool per_row = EPI && (args.scatter || (GROUPED && y + 32 > row_end));
+            // rows of the warp that TMA could store past the slice's end (or,
+            // K-ragged, into the next slice's rows of D): the warp stores its
+            // rows one by one instead (as scattered rows)
+            const bool per_row = EPI && (args.scatter || ((GROUPED || KGROUPED) && y + 32 > row_end));
+            // K-ragged: slice g's output is rows [g*M, g*M + M) of D
+            const int y_out = KGROUPED ? g * args.M + y : y;
+            const bool zero_acc = KGROUPED && kb1 <= kb0;   // an empty slice: nothing was summed
             RowEpi re{1.0f, -1};
             if constexpr (EPI) {
                 re = load_row_epi(args, y + lane, row_end);
+                if (KGROUPED && re.dst >= 0)
+                    re.dst += g * args.M;
                 prefetch_bias(bias, args.N, nt * BN, BN, lane);
             }
             if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
@@ -483,6 +524,11 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                 tmem_ld_32x32b_x32(t_acc + ch * T::EPI_COLS + 32, v1);
                 const int x = nt * BN + ch * T::EPI_COLS;
                 tmem_ld_wait();
+                if (zero_acc) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v0[i] = v1[i] = 0u;
+                }
                 if (ch == BN / T::EPI_COLS - 1) {
                     // the whole accumulator is in registers: hand it back
                     tc_fence_before_sync();
@@ -528,7 +574,7 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
                     __syncwarp();
                     if (lane == 0) {
                         if (x < args.N && y < args.M)
-                            tma_store_2d(&tmD, sbuf, x, y);
+                            tma_store_2d(&tmD, sbuf, x, y_out);
                         bulk_commit_group();
                     }
                 }
@@ -563,7 +609,7 @@ template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MODE>
 static cudaError_t launch_mode(const GemmMaps &maps, const GemmArgs &args, int grid, cudaStream_t stream)
 {
     using T = Tile<KIND, BN, STAGES, NUM_ACC>;
-    constexpr int smem = T::SMEM_BYTES + (MODE == kModeGrouped ? kGroupTableBytes : 0);
+    constexpr int smem = T::SMEM_BYTES + ((MODE == kModeGrouped || MODE == kModeKGrouped) ? kGroupTableBytes : 0);
     auto kern = gemm_persistent_kernel<KIND, BN, STAGES, NUM_ACC, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
@@ -588,6 +634,14 @@ template <Kind KIND, int BN, int STAGES, int NUM_ACC>
 static cudaError_t launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
                                cudaStream_t stream)
 {
+    if (args.group_offs && args.k_grouped) {
+        // K-ragged GEMMs: NVFP4 x dense with A staged in TMEM
+        if constexpr (KIND == Kind::NVFP4_BF16_TMEM &&
+                      Tile<KIND, BN, STAGES, NUM_ACC>::SMEM_BYTES + kGroupTableBytes <= 232448)
+            return launch_mode<KIND, BN, STAGES, NUM_ACC, kModeKGrouped>(maps, args, grid, stream);
+        else
+            return cudaErrorInvalidValue;
+    }
     if (args.group_offs) {
         // grouped GEMMs: NVFP4, and NVFP4 x dense with A staged in TMEM
         if constexpr (KIND == Kind::NVFP4 ||

@@ -289,6 +289,38 @@ BSG_API int nvfp4_dense_f16_grouped_gemm(int E, int M, int N, int K, const void 
                                          const float *gamma, const int32_t *scatter, int m_out, void *D,
                                          bsg_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Inner-expert (K-ragged) NVFP4 x dense GEMM: the pages' K-ragged variant
+ * with a BF16 (nvfp4_dense_kgrouped_gemm) or FP16 (..._f16_...) right-hand
+ * side ("Triton #11171 - Why Two New NVFP4 Test Cases Produced Twelve
+ * Tensor-Memory Failures", section "Why `pad_a` represents the K-ragged
+ * boundary": the ragged dimension is A's K, padded per slice). K is split
+ * into E slices at koffs and slice e gives its own output:
+ *   D[e][m][n] = bf16_rn( gamma[m] * (alpha * sum_{k in slice e} a(m,k) sA(m,k/16) * b(n,k) + bias[e][n]) )
+ *   A       : uint8[M][K/2] E2M1 codes; sfA_swz: its scales, swizzled over all of K
+ *   B       : 16-bit [N][K] row-major, plain values
+ *   koffs   : DEVICE int32[E+1], 4-byte aligned: koffs[0] = 0, nondecreasing,
+ *             koffs[E] = K, each a multiple of 64 (the caller pads every
+ *             slice to whole 64-element blocks, with zero codes in A).
+ *             Read on the GPU; other sequences are clamped there to a
+ *             nondecreasing one in [0, K] (nothing is read or written out of
+ *             bounds; the result is unspecified). An empty slice gives
+ *             D[e] = bf16(gamma * (0 + bias[e])).
+ *   bias    : DEVICE float[E][N], 16-byte aligned, or NULL
+ *   gamma   : DEVICE float[M], 4-byte aligned, or NULL
+ *   D       : bf16[E][M][N], 16-byte aligned
+ * Requires K % 64 == 0, N % 8 == 0, 16-byte aligned A, sfA_swz, B, D;
+ * 1 <= E <= 1024. One launch; allocates nothing. Plans as
+ * nvfp4_dense_grouped_gemm.
+ * ------------------------------------------------------------------------- */
+BSG_API int nvfp4_dense_kgrouped_gemm(int E, int M, int N, int K, const void *A, const void *sfA_swz,
+                                      const void *B, const int32_t *koffs, float alpha, const float *bias,
+                                      const float *gamma, void *D, bsg_stream_t stream);
+
+BSG_API int nvfp4_dense_f16_kgrouped_gemm(int E, int M, int N, int K, const void *A, const void *sfA_swz,
+                                          const void *B, const int32_t *koffs, float alpha, const float *bias,
+                                          const float *gamma, void *D, bsg_stream_t stream);
+
 /* Scale layout of a grouped A: row-major uint8[M][K/16] scales -> the
  * swizzled layout of nvfp4_swizzle_scales applied to each slice on its own,
  * slice e starting at 128-row block row sum_{e'<e} ceil(rows_e' / 128), so
