@@ -236,3 +236,31 @@ def test_ingress_probe_bad_args(lib):
     assert m(32 << 20, 7, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG       # stages > 6
     assert m(64 << 10, 2, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG       # source < 128 KiB
     assert m(32 << 20, 2, None, None) == bsg.BSG_ERR_INVALID_ARG                    # no output
+
+
+@pytest.mark.parametrize("entry", ["nvfp4_dense_grouped_gemm", "nvfp4_dense_f16_grouped_gemm"])
+def test_dense_grouped_bad_args(lib, entry):
+    """The routed NVFP4 x dense entries check sizes, slice count, pointers
+    and alignment before any launch."""
+    f = getattr(lib, entry)
+    ok = (BAD, BAD, BAD, BAD, 1.0, None, None, None)
+    assert f(2, 128, 64, 96, *ok, 128, BAD, None) == bsg.BSG_ERR_INVALID_ARG        # K % 64
+    assert f(2, 128, 60, 128, *ok, 128, BAD, None) == bsg.BSG_ERR_INVALID_ARG       # N % 8
+    assert f(0, 128, 64, 128, *ok, 128, BAD, None) == bsg.BSG_ERR_INVALID_ARG       # E < 1
+    assert f(1025, 128, 64, 128, *ok, 128, BAD, None) == bsg.BSG_ERR_INVALID_ARG    # E > 1024
+    assert f(2, 128, 64, 128, BAD, BAD, BAD, None, 1.0, None, None, None, 128, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert f(2, 128, 64, 128, BAD, BAD, BAD, BAD + 2, 1.0, None, None, None, 128, BAD, None) == bsg.BSG_ERR_MISALIGNED
+    assert f(2, 128, 64, 128, BAD + 8, BAD, BAD, BAD, 1.0, None, None, None, 128, BAD, None) == bsg.BSG_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("entry", ["nvfp4_dense_kgrouped_gemm", "nvfp4_dense_f16_kgrouped_gemm"])
+def test_dense_kgrouped_bad_args(lib, entry):
+    """The K-ragged entries check sizes, slice count, pointers and alignment
+    before any launch."""
+    f = getattr(lib, entry)
+    assert f(2, 128, 64, 96, BAD, BAD, BAD, BAD, 1.0, None, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG   # K % 64
+    assert f(2, 128, 60, 128, BAD, BAD, BAD, BAD, 1.0, None, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG  # N % 8
+    assert f(0, 128, 64, 128, BAD, BAD, BAD, BAD, 1.0, None, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG  # E < 1
+    assert f(2, 128, 64, 128, BAD, BAD, BAD, None, 1.0, None, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG  # no koffs
+    assert f(2, 128, 64, 128, BAD, BAD, BAD, BAD + 2, 1.0, None, None, BAD, None) == bsg.BSG_ERR_MISALIGNED
+    assert f(2, 128, 64, 128, BAD, BAD, BAD, BAD, 1.0, BAD + 4, None, BAD, None) == bsg.BSG_ERR_MISALIGNED  # bias
