@@ -579,8 +579,9 @@ def secondary_grouped(dev, steps: int, pk: dict, psrc: str) -> dict:
 
 def secondary_dense(dev, steps: int, pk: dict, psrc: str) -> dict:
     """NVFP4 activations x dense weights (nvfp4_dense_gemm with BF16 B,
-    nvfp4_dense_f16_gemm with FP16 B): 8192^3 in both, and an 8192 x 256 x
-    8192 weight GEMM (the pages' case has N = 256) in BF16. A is expanded to
+    nvfp4_dense_f16_gemm with FP16 B): 8192^3 in both, an 8192 x 256 x 8192
+    weight GEMM (the pages' case has N = 256) in BF16, and the K-ragged form
+    (nvfp4_dense_kgrouped_gemm) over eight slices of K. A is expanded to
     B's type on the fly and the 16-bit tensor core computes, so the roofline
     is the measured BF16 GEMM peak (FP16 runs at the same nominal rate).
     CUDA graphs, median per launch."""
@@ -603,6 +604,32 @@ def secondary_dense(dev, steps: int, pk: dict, psrc: str) -> dict:
         out[f"{M}x{N}x{K}" + ("_f16" if f16 else "")] = {"plan": plan, "us": round(us, 2), "tflops": round(tf, 1),
                                                          "frac_bf16": round(tf / pk["bf16_tflops"], 4)}
         del p, sa, D
+    # K-ragged (inner-expert): K = 8192 split into 8 uneven slices (whole
+    # 64-element blocks, seeded), each slice its own 4096 x 4096 output
+    M = N = 4096
+    K = 8192
+    import numpy as np
+    rng = np.random.default_rng(8)
+    cuts = np.sort(rng.choice(np.arange(1, K // 64), 7, replace=False)) * 64
+    koffs = torch.tensor([0, *cuts.tolist(), K], dtype=torch.int32, device=dev)
+    p = workloads.make_dense(M, N, K, seed=2, device=dev)
+    sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    bsg.nvfp4_swizzle_scales(M, K, p["sfA"], sa)
+    D = torch.empty((8, M, N), dtype=torch.bfloat16, device=dev)
+
+    def kcall():
+        bsg.nvfp4_dense_kgrouped_gemm(8, M, N, K, p["A"], sa, p["B"], koffs, p["alpha"], None, None, D)
+    us = graph_us({"kragged": kcall}, 4, steps)["kragged"]
+    kcall()
+    kplan = bsg.bsg_last_plan_name()
+    flops = 2.0 * M * N * K
+    kbytes = M * K * 9 // 16 + N * K * 2 + 8 * M * N * 2
+    out["kragged_e8_4096x4096x8192"] = {
+        "plan": kplan, "us": round(us, 2), "tflops": round(flops / (us * 1e-6) / 1e12, 1),
+        "frac_bf16": round(flops / (us * 1e-6) / 1e12 / pk["bf16_tflops"], 4),
+        "hbm_gbs": round(kbytes / (us * 1e-6) / 1e9, 1), "slices_k": [0, *cuts.tolist(), K],
+        "note": "eight outputs of 4096 x 4096 (268 MB of D); FLOPs are those of the whole K"}
+    del p, sa, D
     if bsg.bsg_get_device_status() != bsg.BSG_OK:
         raise SystemExit("device status reported an error in the dense GEMM timing")
     return {"shapes": out, "roofline_peak_tflops": pk["bf16_tflops"],
