@@ -877,14 +877,14 @@ def run_case(args) -> None:
     """One GEMM shape alone (--case nvfp4:MxNxK, fp8:MxNxK, dense:MxNxK or
     densef16:MxNxK for NVFP4 x dense BF16 / FP16, optionally a forced --plan), the NVFP4 quantiser on BF16 ROWSxK (--case
     quantize:ROWSxK), or a grouped workload (--case grouped:NAME, e.g.
-    grouped:moe_e64_t1024_k8): `warmup` untimed then `steps` timed launches,
+    grouped:moe_e64_t1024_k8; groupeddense:NAME for BF16 expert weights): `warmup` untimed then `steps` timed launches,
     inputs resident. Used for profiler captures of a single kernel and for ad-hoc
     timings; prints one JSON line."""
     import __graft_entry__
     __graft_entry__.build()
     import block_scaled_precision_persistent_gb300 as bsg
     kind, shape = args.case.split(":")
-    dims = [] if kind == "grouped" else [int(x) for x in shape.lower().split("x")]
+    dims = [] if kind in ("grouped", "groupeddense") else [int(x) for x in shape.lower().split("x")]
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     s = torch.cuda.current_stream()
@@ -912,9 +912,24 @@ def run_case(args) -> None:
         print(json.dumps({"case": args.case, "us": round(us, 2), "gb_s": round(moved / (us * 1e-6) / 1e9, 1)}),
               flush=True)
         return
-    if kind == "grouped":
+    if kind in ("grouped", "groupeddense"):
         w = workloads.GROUPED_WORKLOADS[shape]
-        g = GroupedProblem(w, dev)
+        if kind == "grouped":
+            g = GroupedProblem(w, dev)
+            moved = w.algorithmic_bytes
+        else:
+            # the routed GEMM with BF16 expert weights, D in token order
+            offs, dst = workloads.routing(w.E, w.tokens, w.top_k, seed=1)
+            offs, dst = offs.to(dev), dst.to(dev)
+            pd = workloads.make_dense_grouped(w.E, w.M, w.N, w.K, seed=1, device=dev)
+            sa = torch.empty(bsg.nvfp4_grouped_scale_bytes(w.E, w.M, w.K), dtype=torch.uint8, device=dev)
+            bsg.nvfp4_swizzle_scales_grouped(w.E, w.M, w.K, offs, pd["sfA"], sa, s)
+            Dg = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+            moved = w.M * w.K * 9 // 16 + w.E * w.N * w.K * 2 + w.M * w.N * 2
+
+            def g():
+                bsg.nvfp4_dense_grouped_gemm(w.E, w.M, w.N, w.K, pd["A"], sa, pd["B"], offs, pd["alpha"], None, None,
+                                             dst, w.M, Dg, s)
         bsg.bsg_force_plan(args.plan)
         try:
             for _ in range(args.warmup):
@@ -933,8 +948,8 @@ def run_case(args) -> None:
         if bsg.bsg_get_device_status() != bsg.BSG_OK:
             raise SystemExit("device status reported an error")
         us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
-        print(json.dumps({"case": args.case, "us": round(us, 2),
-                          "gb_s": round(w.algorithmic_bytes / (us * 1e-6) / 1e9, 1)}), flush=True)
+        print(json.dumps({"case": args.case, "plan": bsg.bsg_last_plan_name(), "us": round(us, 2),
+                          "gb_s": round(moved / (us * 1e-6) / 1e9, 1)}), flush=True)
         return
     M, N, K = dims
     D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
