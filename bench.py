@@ -738,9 +738,13 @@ def ingress_roofline(bsg, w: workloads.Workload, plan: str, gemm_ms: float, cloc
         return None
     achieved = kblocks_per_cta * per_kblock / (gemm_ms * 1e-3 * mhz * 1e6)
     peak, total = bsg.bsg_measure_ingress(32 << 20, 4)
+    box, _ = bsg.bsg_measure_ingress(32 << 20, 4, tensor_boxes=True)
     return {"bound": "per-SM operand ingress", "bytes_per_kblock_per_cta": per_kblock,
             "achieved_bytes_per_cycle_per_sm": round(achieved, 2), "peak_bytes_per_cycle_per_sm": round(peak, 2),
             "frac": round(achieved / peak, 4), "probe_total_gbs": round(total, 1),
+            "tensor_box_bytes_per_cycle_per_sm": round(box, 2), "frac_of_tensor_box": round(achieved / box, 4),
+            "peak_note": "peak: contiguous bulk copies; tensor_box: 128-row x 128-byte tensor-map boxes, "
+                         "the load the kernel issues for its operand tiles",
             "cycles": f"SM clock {mhz:.0f} MHz (median sampled under load)"}
 
 

@@ -75,7 +75,8 @@ _SIGNATURES = {
     "bsg_set_raster_group": (_i, [_i]),
     "bsg_set_pdl": (_i, [_i]),
     "bsg_watchdog_selftest": (_i, [ctypes.c_uint64, _vp]),
-    "bsg_measure_ingress": (_i, [ctypes.c_size_t, _i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
+    "bsg_measure_ingress": (_i, [ctypes.c_size_t, _i, _i, ctypes.POINTER(ctypes.c_double),
+                                 ctypes.POINTER(ctypes.c_double)]),
     "bsg_force_plan": (_i, [ctypes.c_char_p]),
     "bsg_select_plan": (_i, [_i, _i, _i, _i, _i, ctypes.c_char_p, ctypes.c_size_t]),
     "bsg_last_launch_count": (_i, []),
@@ -292,11 +293,12 @@ def nvfp4_dense_f16_kgrouped_gemm(E, M, N, K, A, sfA_swz, B, koffs, alpha, bias,
            "nvfp4_dense_f16_kgrouped_gemm")
 
 
-def bsg_measure_ingress(src_bytes: int = 32 << 20, stages: int = 4) -> tuple[float, float]:
-    """Operand-ingress probe: (bytes per SM clock cycle per SM, total GB/s)."""
+def bsg_measure_ingress(src_bytes: int = 32 << 20, stages: int = 4, tensor_boxes: bool = False) -> tuple[float, float]:
+    """Operand-ingress probe: (bytes per SM clock cycle per SM, total GB/s);
+    contiguous bulk copies, or tensor-map boxes of 128 rows x 128 bytes."""
     per_sm, total = ctypes.c_double(0.0), ctypes.c_double(0.0)
-    _check(load().bsg_measure_ingress(int(src_bytes), int(stages), ctypes.byref(per_sm), ctypes.byref(total)),
-           "bsg_measure_ingress")
+    _check(load().bsg_measure_ingress(int(src_bytes), int(stages), 1 if tensor_boxes else 0, ctypes.byref(per_sm),
+                                      ctypes.byref(total)), "bsg_measure_ingress")
     return per_sm.value, total.value
 
 

@@ -1022,10 +1022,14 @@ int bsg_watchdog_selftest(uint64_t ns, bsg_stream_t stream)
     return BSG_OK;
 }
 
-int bsg_measure_ingress(size_t src_bytes, int stages, double *bytes_per_cycle_per_sm, double *total_gbs)
+int bsg_measure_ingress(size_t src_bytes, int stages, int tensor_boxes, double *bytes_per_cycle_per_sm,
+                        double *total_gbs)
 {
+    // tensor boxes: rows of 8192 bytes (an NVFP4 operand row at K = 16384),
+    // at least two 128-row tile rows of them
+    const size_t pitch = 8192;
     if (!bytes_per_cycle_per_sm || stages < 1 || stages > bsg::probe_max_stages() ||
-        src_bytes < (size_t)4 * (size_t)bsg::probe_slot_bytes())
+        src_bytes < (size_t)4 * (size_t)bsg::probe_slot_bytes() || (tensor_boxes && src_bytes < 256 * pitch))
         return BSG_ERR_INVALID_ARG;
     DeviceState *ds = nullptr;
     int rc = current_device(&ds);
@@ -1038,15 +1042,22 @@ int bsg_measure_ingress(size_t src_bytes, int stages, double *bytes_per_cycle_pe
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     float ms = 0.0f;
     rc = BSG_ERR_CUDA;
+    CUtensorMap tm;
+    std::memset(&tm, 0, sizeof tm);
+    const size_t rows = (src_bytes / pitch) / 128 * 128;
+    auto launch = [&]() {
+        if (!tensor_boxes)
+            return bsg::launch_ingress_probe(src, src_bytes, stages, iters, ds->sms, ds->status, g_watchdog_ns.load(),
+                                             cyc, st);
+        return bsg::launch_tma_ingress_probe(tm, (int)(pitch / 128), (int)(rows / 128), stages, iters, ds->sms,
+                                             ds->status, g_watchdog_ns.load(), cyc, st);
+    };
     if (cudaMalloc(&src, src_bytes) == cudaSuccess && cudaMalloc(&cyc, sizeof(unsigned long long) * ds->sms) == cudaSuccess &&
         cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess && cudaEventCreate(&e0) == cudaSuccess &&
         cudaEventCreate(&e1) == cudaSuccess && cudaMemsetAsync(src, 0x5A, src_bytes, st) == cudaSuccess &&
+        (!tensor_boxes || encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, src, pitch, rows, pitch, 128, 128) == BSG_OK) &&
         // one untimed pass (first touch of the source), then the timed one
-        bsg::launch_ingress_probe(src, src_bytes, stages, iters, ds->sms, ds->status, g_watchdog_ns.load(), cyc,
-                                  st) == cudaSuccess &&
-        cudaEventRecord(e0, st) == cudaSuccess &&
-        bsg::launch_ingress_probe(src, src_bytes, stages, iters, ds->sms, ds->status, g_watchdog_ns.load(), cyc,
-                                  st) == cudaSuccess &&
+        launch() == cudaSuccess && cudaEventRecord(e0, st) == cudaSuccess && launch() == cudaSuccess &&
         cudaEventRecord(e1, st) == cudaSuccess && cudaStreamSynchronize(st) == cudaSuccess &&
         cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess) {
         std::vector<unsigned long long> c((size_t)ds->sms);

@@ -145,6 +145,9 @@ cudaError_t launch_watchdog_probe(unsigned int *status, unsigned long long ns,
 cudaError_t launch_ingress_probe(const uint8_t *src, size_t src_bytes, int stages, int iters, int ctas,
                                  unsigned int *status, unsigned long long timeout_ns, unsigned long long *cycles,
                                  cudaStream_t stream);
+cudaError_t launch_tma_ingress_probe(const CUtensorMap &tm, int xtiles, int ytiles, int stages, int iters, int ctas,
+                                     unsigned int *status, unsigned long long timeout_ns, unsigned long long *cycles,
+                                     cudaStream_t stream);
 int probe_slot_bytes();
 int probe_max_stages();
 

@@ -382,15 +382,19 @@ BSG_API int bsg_watchdog_selftest(uint64_t ns, bsg_stream_t stream);
  * ceiling on a tile kernel's k-block period, whose loaders bring A, B and
  * their scales into shared memory ("Together AI Ports ThunderKittens GEMM
  * Kernels to NVIDIA Vera Rubin NVL72", introduction).
- *   src_bytes : source buffer size (>= 128 KiB); 32 MiB keeps it in L2
+ *   src_bytes : source buffer size (>= 128 KiB; >= 2 MiB with tensor_boxes);
+ *               32 MiB keeps it in L2
  *   stages    : 1..6 slots of 32 KiB copies in flight per SM
+ *   tensor_boxes : 0 = contiguous 16 KiB bulk copies; 1 = tensor-map copies
+ *               of 128-row x 128-byte boxes (128-byte swizzle) from rows of
+ *               8192 bytes, the pattern of the GEMMs' NVFP4 operand tiles
  *   bytes_per_cycle_per_sm : out, bytes per SM clock cycle, averaged over SMs
  *   total_gbs : out (may be NULL), bytes of all SMs per second
  * One CTA per SM, 4000 refills per slot, after one untimed pass. Blocking:
  * allocates and frees its own buffers and stream, so it is a measurement
  * routine, not one for a hot path. A wait that runs out returns
  * BSG_ERR_DEVICE_TIMEOUT (and leaves the status word set, as the GEMMs do). */
-BSG_API int bsg_measure_ingress(size_t src_bytes, int stages, double *bytes_per_cycle_per_sm,
+BSG_API int bsg_measure_ingress(size_t src_bytes, int stages, int tensor_boxes, double *bytes_per_cycle_per_sm,
                                 double *total_gbs);
 
 /* Force the planner to one named plan for later calls (NULL or "" = choose

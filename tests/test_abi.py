@@ -231,11 +231,13 @@ def test_ingress_probe_bad_args(lib):
     import ctypes
     out = ctypes.c_double(0.0)
     m = lib.bsg_measure_ingress
-    m.argtypes = [ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
-    assert m(32 << 20, 0, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG       # stages < 1
-    assert m(32 << 20, 7, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG       # stages > 6
-    assert m(64 << 10, 2, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG       # source < 128 KiB
-    assert m(32 << 20, 2, None, None) == bsg.BSG_ERR_INVALID_ARG                    # no output
+    m.argtypes = [ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                  ctypes.POINTER(ctypes.c_double)]
+    assert m(32 << 20, 0, 0, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG    # stages < 1
+    assert m(32 << 20, 7, 0, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG    # stages > 6
+    assert m(64 << 10, 2, 0, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG    # source < 128 KiB
+    assert m(1 << 20, 2, 1, ctypes.byref(out), None) == bsg.BSG_ERR_INVALID_ARG     # boxes need >= 2 MiB
+    assert m(32 << 20, 2, 0, None, None) == bsg.BSG_ERR_INVALID_ARG                 # no output
 
 
 @pytest.mark.parametrize("entry", ["nvfp4_dense_grouped_gemm", "nvfp4_dense_f16_grouped_gemm"])

@@ -28,3 +28,6 @@ def test_ingress_probe(dev):
     assert 4.0 < per_sm_l2 < 512.0 and 4.0 < per_sm_dram < 512.0
     assert total_l2 > 1000.0 and total_dram > 1000.0
     assert per_sm_l2 >= 0.9 * per_sm_dram
+    per_sm_box, total_box = bsg.bsg_measure_ingress(32 << 20, 4, tensor_boxes=True)
+    assert bsg.bsg_get_device_status() == bsg.BSG_OK
+    assert 4.0 < per_sm_box < 512.0 and total_box > 1000.0
