@@ -400,6 +400,34 @@ class Oracle:
         return out
 
 
+def packed_operand_bytes(rows: int, K: int) -> int:
+    """Bytes of an NVFP4 operand of `rows` rows in the tile-packed layout:
+    rows padded to 128, K / 2 bytes a row (K % 256 == 0)."""
+    return -(-rows // 128) * 128 * (K // 2)
+
+
+def pack_operand_tiles(X, K: int) -> np.ndarray:
+    """Tile-packed layout of a row-major NVFP4 operand X uint8[rows, K/2]
+    (the library's own format, for copies of whole tiles): tile (rb, kb)
+    holds rows 128 rb .. 128 rb + 127 and bytes 128 kb .. 128 kb + 127 of
+    each, contiguously at tile index rb * (K / 256) + kb, 16 KiB a tile; in a
+    tile, byte c of row r sits at r * 128 + ((c // 16) XOR (r % 8)) * 16 +
+    c % 16 (the 128-byte swizzle); rows past the end are zero. Written out
+    byte by byte (1-D uint8 of packed_operand_bytes(rows, K))."""
+    X = np.ascontiguousarray(X, dtype=np.uint8)
+    rows, width = X.shape
+    assert K % 256 == 0 and width == K // 2
+    kblocks = K // 256
+    out = np.zeros(packed_operand_bytes(rows, K), np.uint8)
+    for r in range(rows):
+        rb, rr = divmod(r, 128)
+        for c in range(width):
+            kb, cc = divmod(c, 128)
+            off = ((rb * kblocks + kb) * 128 + rr) * 128 + ((cc // 16) ^ (rr % 8)) * 16 + cc % 16
+            out[off] = X[r, c]
+    return out
+
+
 def default_threads() -> int:
     try:
         return max(1, len(os.sched_getaffinity(0)))

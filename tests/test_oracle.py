@@ -799,6 +799,31 @@ def test_planted_mistake_is_caught(mutant):
     assert failed, f"no pin caught the planted mistake {mutant}"
 
 
+def test_pack_operand_tiles_layout():
+    """The tile-packed operand layout against hand-computed offsets and an
+    independent restatement by reshapes; padding rows are zero."""
+    rows, K = 200, 768                      # two row blocks (one ragged), three k-blocks
+    X = np.random.default_rng(17).integers(0, 256, (rows, K // 2)).astype(np.uint8)
+    got = oracle.pack_operand_tiles(X, K)
+    assert got.size == oracle.packed_operand_bytes(rows, K) == 256 * 384
+    # byte (130, 300): row block 1, row 2 of it; k-block 2, byte 44 = chunk 2, 12 in;
+    # chunk 2 XOR row 2 = 0: offset ((1 * 3 + 2) * 128 + 2) * 128 + 0 * 16 + 12
+    assert got[((1 * 3 + 2) * 128 + 2) * 128 + 12] == X[130, 300]
+    # byte (7, 5): tile 0, row 7, chunk 0 XOR 7 = 7: offset 7 * 128 + 7 * 16 + 5
+    assert got[7 * 128 + 7 * 16 + 5] == X[7, 5]
+    # restatement: pad, split rows into (rb, r) and bytes into (kb, chunk, b),
+    # swizzle the chunk index by r % 8, reorder to (rb, kb, r, chunk, b)
+    pad = np.zeros((256, K // 2), np.uint8)
+    pad[:rows] = X
+    t = pad.reshape(2, 128, 3, 8, 16)
+    sw = np.empty_like(t)
+    for r in range(128):
+        sw[:, r, :, np.arange(8) ^ (r % 8), :] = t[:, r, :, :, :].transpose(2, 0, 1, 3)
+    want = sw.transpose(0, 2, 1, 3, 4).reshape(-1)
+    assert np.array_equal(got, want)
+    assert not got[(1 * 3 + 0) * 16384 + 72 * 128:(1 * 3 + 1) * 16384].any()   # rows 200.. of tile (1, 0)
+
+
 def test_tolerance_helper():
     b = lambda x: np.array([oracle.get().bf16_rne(v) for v in x], np.uint16)  # noqa: E731
     ref = b([100.0, 0.0, -3.0, 1.0])
