@@ -879,7 +879,8 @@ def run_reference(args, dist: Dist) -> None:
 
 def run_case(args) -> None:
     """One GEMM shape alone (--case nvfp4:MxNxK, fp8:MxNxK, dense:MxNxK or
-    densef16:MxNxK for NVFP4 x dense BF16 / FP16, optionally a forced --plan), the NVFP4 quantiser on BF16 ROWSxK (--case
+    densef16:MxNxK for NVFP4 x dense BF16 / FP16, packed:MxNxK for NVFP4 with tile-packed operands,
+    optionally a forced --plan), the NVFP4 quantiser on BF16 ROWSxK (--case
     quantize:ROWSxK), or a grouped workload (--case grouped:NAME, e.g.
     grouped:moe_e64_t1024_k8; groupeddense:NAME for BF16 expert weights): `warmup` untimed then `steps` timed launches,
     inputs resident. Used for profiler captures of a single kernel and for ad-hoc
@@ -970,6 +971,20 @@ def run_case(args) -> None:
 
         def call():
             bsg.nvfp4_gemm_ex(M, N, K, p["A"], sa, p["B"], sb, p["alpha"], eb, eg, es, M, D, s)
+    elif kind == "packed":
+        # A and B packed into 16 KiB tiles once, outside the timed launches
+        p = workloads.make_nvfp4(workloads.WORKLOADS["nvfp4_4096"], dev, M=M, N=N, K=K)
+        sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+        sb = torch.empty(bsg.nvfp4_swizzled_scale_bytes(N, K), dtype=torch.uint8, device=dev)
+        bsg.nvfp4_swizzle_scales(M, K, p["sfA"], sa, s)
+        bsg.nvfp4_swizzle_scales(N, K, p["sfB"], sb, s)
+        ap = torch.empty(bsg.nvfp4_packed_operand_bytes(M, K), dtype=torch.uint8, device=dev)
+        bp = torch.empty(bsg.nvfp4_packed_operand_bytes(N, K), dtype=torch.uint8, device=dev)
+        bsg.nvfp4_pack_operand(M, K, p["A"], ap, s)
+        bsg.nvfp4_pack_operand(N, K, p["B"], bp, s)
+
+        def call():
+            bsg.nvfp4_gemm_packed(M, N, K, ap, sa, bp, sb, p["alpha"], D, s)
     elif kind in ("dense", "densef16"):
         f16 = kind == "densef16"
         pd = workloads.make_dense(M, N, K, seed=1, device=dev, b_dtype=torch.float16 if f16 else torch.bfloat16)

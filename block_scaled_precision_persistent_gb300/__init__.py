@@ -48,6 +48,9 @@ _i = ctypes.c_int
 _SIGNATURES = {
     "nvfp4_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "nvfp4_gemm_swizzled": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
+    "nvfp4_packed_operand_bytes": (ctypes.c_size_t, [_i, _i]),
+    "nvfp4_pack_operand": (_i, [_i, _i, _vp, _vp, _vp]),
+    "nvfp4_gemm_packed": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "nvfp4_swizzle_scales": (_i, [_i, _i, _vp, _vp, _vp]),
     "nvfp4_swizzled_scale_bytes": (ctypes.c_size_t, [_i, _i]),
     "nvfp4_quantize": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -142,6 +145,23 @@ def nvfp4_gemm_swizzled(M, N, K, A, sfA_swz, B, sfB_swz, alpha, D, stream=None) 
     """As nvfp4_gemm, with scales already in the swizzled layout."""
     _check(load().nvfp4_gemm_swizzled(M, N, K, _ptr(A), _ptr(sfA_swz), _ptr(B), _ptr(sfB_swz),
                                       float(alpha), _ptr(D), _stream(stream)), "nvfp4_gemm_swizzled")
+
+
+def nvfp4_packed_operand_bytes(rows, K) -> int:
+    """Bytes of an operand of `rows` rows in the tile-packed layout (0 if invalid)."""
+    return int(load().nvfp4_packed_operand_bytes(rows, K))
+
+
+def nvfp4_pack_operand(rows, K, X, out, stream=None) -> None:
+    """uint8[rows, K/2] NVFP4 codes -> the tile-packed layout (16 KiB tiles
+    of 128 rows x 128 bytes, 128-byte swizzled inside, rows padded with zeros)."""
+    _check(load().nvfp4_pack_operand(rows, K, _ptr(X), _ptr(out), _stream(stream)), "nvfp4_pack_operand")
+
+
+def nvfp4_gemm_packed(M, N, K, A_packed, sfA_swz, B_packed, sfB_swz, alpha, D, stream=None) -> None:
+    """As nvfp4_gemm_swizzled, with A and B in the tile-packed layout."""
+    _check(load().nvfp4_gemm_packed(M, N, K, _ptr(A_packed), _ptr(sfA_swz), _ptr(B_packed), _ptr(sfB_swz),
+                                    float(alpha), _ptr(D), _stream(stream)), "nvfp4_gemm_packed")
 
 
 def nvfp4_swizzle_scales(rows, K, sf, sf_swz, stream=None) -> None:

@@ -155,7 +155,8 @@ int choose_plan(Kind kind, int M, int N, int K, int num_sms, int *plan)
     }
     if (forced >= 0) {
         const PlanInfo &fp = bsg::plan_info(forced);
-        if (fp.kind != kind || (fp.family == bsg::Family::SKINNY && M > fp.tile_m))
+        // a tile-packed plan reads operands only nvfp4_gemm_packed supplies
+        if (fp.kind != kind || fp.packed || (fp.family == bsg::Family::SKINNY && M > fp.tile_m))
             return BSG_ERR_NO_PLAN;
         *plan = forced;
         return BSG_OK;
@@ -294,12 +295,18 @@ int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A,
 // Encode the maps and launch one persistent GEMM.
 int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const uint8_t *sfa,
              const uint8_t *sfb, const float *sA, const float *sB, float alpha, void *D,
-             cudaStream_t stream, DeviceState *ds, const Epilogue &epi = Epilogue(), bool b_f16 = false)
+             cudaStream_t stream, DeviceState *ds, const Epilogue &epi = Epilogue(), bool b_f16 = false,
+             const uint8_t *a_packed = nullptr, const uint8_t *b_packed = nullptr)
 {
     int plan = -1;
-    int rc = choose_plan(kind, M, N, K, ds->sms, &plan);
-    if (rc != BSG_OK)
+    int rc = BSG_OK;
+    const bool packed = a_packed != nullptr;
+    if (packed)
+        plan = bsg::find_plan("nvfp4_tc2_256x256_s5_acc1_packed");   // the one tile-packed plan
+    else if ((rc = choose_plan(kind, M, N, K, ds->sms, &plan)) != BSG_OK)
         return rc;
+    if (plan < 0)
+        return BSG_ERR_NO_PLAN;
     const PlanInfo &pi = bsg::plan_info(plan);
     const bool dense = kind == Kind::NVFP4_BF16;
     // bytes per row: packed E2M1 (K/2), E4M3 (K), or for the dense kind packed
@@ -314,8 +321,16 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     // A: 128 rows per CTA (dense: 32 bytes of codes per row and stage,
     // unswizzled, expanded in shared memory); B: the CTA's share of the
     // tile's N rows, 128 bytes per row and stage
-    // (multicast plans: each CTA loads 128 / mc of its rows for all pairs)
-    if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes,
+    // (multicast plans: each CTA loads 128 / mc of its rows for all pairs;
+    // tile-packed plans load A and B by bulk copies and read neither map,
+    // which then repeat D's)
+    if (packed) {
+        if ((rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, d_rows(M, epi),
+                            (uint64_t)N * 2u, 64, 32)) != BSG_OK)
+            return rc;
+        maps.a = maps.d;
+        maps.b = maps.d;
+    } else if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes,
                         dense ? 32 : 128, (uint32_t)(128 / pi.mc),
                         dense ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B)) != BSG_OK ||
         (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, b_row_bytes, (uint64_t)N, b_row_bytes,
@@ -353,6 +368,8 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     a.sfb_row_blocks = (N + 127) / 128;
     a.sfa = sfa;
     a.sfb = sfb;
+    a.a_packed = a_packed;
+    a.b_packed = b_packed;
     a.alpha = alpha;
     a.sA = sA;
     a.sB = sB;
@@ -679,6 +696,47 @@ int nvfp4_gemm(int M, int N, int K, const void *A, const void *sfA, const void *
         return BSG_ERR_CUDA;
     t_last_launches = 2;
     return run_gemm(Kind::NVFP4, M, N, K, A, B, swz_a, swz_b, nullptr, nullptr, alpha, D, s, ds);
+}
+
+size_t nvfp4_packed_operand_bytes(int rows, int K)
+{
+    if (rows < 1 || K < 256 || (K % 256) != 0)
+        return 0;
+    return (size_t)((rows + 127) / 128) * 128u * (size_t)(K / 2);
+}
+
+int nvfp4_pack_operand(int rows, int K, const void *X, void *out, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    if (!X || !out || rows < 1 || K < 256 || (K % 256) != 0 || (rows + 127) / 128 > 65535)
+        return BSG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(out))
+        return BSG_ERR_MISALIGNED;
+    DeviceState *ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc != BSG_OK)
+        return rc;
+    if (bsg::launch_pack_operand(rows, K, static_cast<const uint8_t *>(X), static_cast<uint8_t *>(out),
+                                 reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    t_last_launches = 1;
+    return BSG_OK;
+}
+
+int nvfp4_gemm_packed(int M, int N, int K, const void *A_packed, const void *sfA_swz, const void *B_packed,
+                      const void *sfB_swz, float alpha, void *D, bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    int rc = check_nvfp4_args(M, N, K, A_packed, sfA_swz, B_packed, sfB_swz, D);
+    if (rc != BSG_OK)
+        return rc;
+    DeviceState *ds = nullptr;
+    if ((rc = current_device(&ds)) != BSG_OK)
+        return rc;
+    return run_gemm(Kind::NVFP4, M, N, K, nullptr, nullptr, static_cast<const uint8_t *>(sfA_swz),
+                    static_cast<const uint8_t *>(sfB_swz), nullptr, nullptr, alpha, D,
+                    reinterpret_cast<cudaStream_t>(stream), ds, Epilogue(), false,
+                    static_cast<const uint8_t *>(A_packed), static_cast<const uint8_t *>(B_packed));
 }
 
 int nvfp4_quantize(int rows, int K, const void *X, void *packed, void *sf_swz, void *sf_rowmajor,

@@ -52,6 +52,10 @@ struct GemmArgs {
     // group_offs (device int32[E+1]) splits K instead of M, and slice e
     // writes rows [e*M, e*M + M) of D with bias + e*N
     int k_grouped;
+    // tile-packed operands (PACKED pair plans): 16 KiB tiles of 128 rows x
+    // 128 bytes, 128B-swizzled inside, at tile index row_block * K/256 + kb
+    const uint8_t *a_packed;
+    const uint8_t *b_packed;
     // NVFP4 x dense kind: B holds FP16 values (A is expanded to FP16 and the
     // MMA runs kind::f16 with F16 operands) instead of BF16
     int b_f16;
@@ -83,6 +87,7 @@ struct PlanInfo {
     int threads;
     int tmem_cols;
     int mc = 1;                // CTA pairs per cluster sharing A by multicast (pair plans)
+    int packed = 0;            // 1: reads tile-packed operands (nvfp4_gemm_packed only)
 };
 
 // Encoded tensor maps of one call (sfa / sfb only for CTA-pair NVFP4 plans).
@@ -134,6 +139,10 @@ cudaError_t launch_swizzle_scales_grouped(int E, int rows, int K, const int *off
 // Two-level NVFP4 quantisation: memset of global[0], amax kernel, quantiser.
 cudaError_t launch_nvfp4_quantize(int rows, int K, const void *X, uint8_t *packed, uint8_t *sf_swz,
                                   uint8_t *sf_rm, float *global, int num_sms, cudaStream_t stream);
+
+// Tile-packed NVFP4 operand (swizzle.cu): rows x K/2 bytes -> 16 KiB tiles
+// of 128 rows x 128 bytes, 128B-swizzled inside, rows padded to 128.
+cudaError_t launch_pack_operand(int rows, int K, const uint8_t *X, uint8_t *out, cudaStream_t stream);
 
 // Watchdog probe: waits on an mbarrier nothing arrives on.
 cudaError_t launch_watchdog_probe(unsigned int *status, unsigned long long ns,

@@ -47,7 +47,7 @@
 
 namespace bsg {
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC = 1>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC = 1, bool PACKED = false>
 struct PairTile {
     static constexpr bool kFp4 = KIND == Kind::NVFP4;
     // NVFP4 activations x dense BF16 weights: each CTA expands its own 128
@@ -95,7 +95,8 @@ struct PairTile {
     static constexpr int BAR_DRAIN = BAR_TEMPTY + NUM_ACC;
     static constexpr int BAR_SFREADY = BAR_DRAIN + 1;
     static constexpr int BAR_SFFULL = BAR_SFREADY + STAGES;
-    static constexpr int NUM_BARS = BAR_SFFULL + STAGES;
+    static constexpr int BAR_PFULL = BAR_SFFULL + STAGES;   // PACKED: the peer's own A/B tiles landed
+    static constexpr int NUM_BARS = BAR_PFULL + (PACKED ? STAGES : 0);
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
     // NVFP4: one scale writer per TMEM sub-partition; dense: two expansion
     // warps per sub-partition, each taking half of every row
@@ -117,6 +118,8 @@ struct PairTile {
 
     static_assert(BN % 128 == 0 && BN <= 256, "pair tile N: B halves of 64 or 128 rows");
     static_assert(MC == 1 || (MC == 2 && !kDense), "A multicast: two pairs, operands loaded by TMA");
+    static_assert(!PACKED || (kFp4 && MC == 1 && BN == 256 && A_BYTES == 16384 && B_BYTES == 16384),
+                  "tile-packed operands: NVFP4 256-wide pairs, one 16 KiB tile of A and of B per CTA and stage");
     static_assert(TMEM_USED <= 512, "TMEM: accumulators plus scales exceed 512 columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
@@ -124,15 +127,19 @@ struct PairTile {
 
 // EPI: the epilogue-variant instantiation (bias, gamma, scattered rows).
 // MC: pairs per cluster sharing A by multicast (1 or 2).
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC, bool EPI>
-__global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREADS, 1)
+// PACKED: A and B arrive as tile-packed operands, one 16 KiB bulk copy per
+// CTA, tile and stage (a copy of contiguous bytes takes operands into an SM
+// faster than a tensor-map box of 128 rows); each CTA's copies complete on
+// its own barrier, and the peer's warp 1 relays their arrival to the leader.
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC, bool EPI, bool PACKED = false>
+__global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD,
                      const __grid_constant__ CUtensorMap tmSFA,
                      const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args)
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC>;
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -147,6 +154,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREA
     const uint32_t drain_bar = bar0 + 8u * T::BAR_DRAIN;
     const uint32_t sfready0 = bar0 + 8u * T::BAR_SFREADY;    // [STAGES] scales in TMEM (both CTAs) -> MMA (leader's)
     const uint32_t sffull0 = bar0 + 8u * T::BAR_SFFULL;      // [STAGES] own scale loads -> own scale warps
+    const uint32_t pfull0 = bar0 + 8u * T::BAR_PFULL;        // [STAGES] PACKED: own operand tiles (peer)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -161,7 +169,10 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8u * s, 1);
+            // PACKED: the leader's own arrival plus the peer's relay
+            mbar_init(full0 + 8u * s, PACKED ? 2 : 1);
+            if constexpr (PACKED)
+                mbar_init(pfull0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, MC);   // one commit per pair that reads the stage
         }
         for (int a = 0; a < NUM_ACC; ++a) {
@@ -264,6 +275,20 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREA
                                       sfb);
                         if (leader)
                             mbar_arrive_expect_tx(full0 + 8u * stage, 2u * T::B_BYTES);
+                    } else if constexpr (PACKED) {
+                        // this CTA's A tile (row block 2 pm + r) and B tile
+                        // (row block 2 nt + r) of k-block kb, one bulk copy
+                        // each, on its own barrier (the leader's full one, or
+                        // the peer's relayed one); a row block past M or N is
+                        // not loaded -- its rows are never stored
+                        const uint32_t own = leader ? full0 + 8u * stage : pfull0 + 8u * stage;
+                        const int rba = 2 * pm + (int)rank, rbb = 2 * nt + (int)rank;
+                        const bool a_in = rba * 128 < args.M, b_in = rbb * 128 < args.N;
+                        mbar_arrive_expect_tx(own, (a_in ? T::A_BYTES : 0) + (b_in ? T::B_BYTES : 0));
+                        if (a_in)
+                            bulk_load(sa, args.a_packed + ((size_t)rba * nkb + kb) * 16384u, T::A_BYTES, own);
+                        if (b_in)
+                            bulk_load(sb, args.b_packed + ((size_t)rbb * nkb + kb) * 16384u, T::B_BYTES, own);
                     } else {
                         if (leader)
                             mbar_arrive_expect_tx(full0 + 8u * stage, 2u * (T::A_BYTES + T::B_BYTES));
@@ -278,7 +303,8 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREA
                                                        (uint16_t)((1u << rank) | (1u << (2u + rank))));
                         }
                     }
-                    tma_load_2d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN + (int)rank * T::B_ROWS);
+                    if constexpr (!PACKED)
+                        tma_load_2d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN + (int)rank * T::B_ROWS);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -365,6 +391,29 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREA
             }
             tc_commit_pair(drain_bar);
             mbar_wait_quiet(drain_bar, 0, wd.limit_ns);
+        }
+        if constexpr (PACKED) {
+            // the peer's relay: its operand tiles of each stage have landed
+            // (own barrier), so the leader's full barrier gets its second
+            // arrival -- a relaxed remote arrive, as the scale writers'
+            if (!leader && lane == 0) {
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        if (!mbar_wait(pfull0 + 8u * stage, phase, wd, abort_flag, 11)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_remote_relaxed(mapa_shared(full0 + 8u * stage, lead));
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
         }
     } else if (warp < T::EPI_WARP0) {
         // ------------------------------------------------------------------
@@ -606,13 +655,14 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC>::THREA
 // ---------------------------------------------------------------------------
 // Plans and launchers
 // ---------------------------------------------------------------------------
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC, bool PACKED = false>
 static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
                                     cudaStream_t stream)
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC>;
-    auto kern = has_epilogue(args) ? gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, true>
-                                   : gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, false>;
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>;
+    // the packed form runs the plain epilogue only
+    auto kern = (!PACKED && has_epilogue(args)) ? gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, !PACKED, PACKED>
+                                                : gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, false, PACKED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_BYTES);
     if (e != cudaSuccess)
@@ -637,11 +687,11 @@ static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, 
     return cudaGetLastError();
 }
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC, bool PACKED = false>
 static int pair_clusters_impl()
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC>;
-    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, false>;   // the EPI instantiation has the same footprint
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>;
+    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, false, PACKED>;   // the EPI instantiation has the same footprint
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) !=
         cudaSuccess)
         return 0;
@@ -664,32 +714,33 @@ static int pair_clusters_impl()
     return n;
 }
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC, bool PACKED = false>
 static constexpr PlanInfo make_pair_plan(const char *name)
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC>;
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>;
     // the TMEM-staged dense pair serves calls of kind NVFP4_BF16
     constexpr Kind kind = KIND == Kind::NVFP4_BF16_TMEM ? Kind::NVFP4_BF16 : KIND;
     return PlanInfo{name, kind, Family::PAIR, 2, T::TILE_M, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
-                    T::THREADS, T::TMEM_COLS, MC};
+                    T::THREADS, T::TMEM_COLS, MC, PACKED ? 1 : 0};
 }
 
 // The first plan of each kind and shape is the planner's; the shallower
 // rings are there for the stage sweep, the "_mca" plans (two pairs per
 // cluster sharing A by multicast) for the multicast comparison
 // (bsg_force_plan).
-#define BSG_PAIR_PLANS(X)                                              \
-    X(Kind::NVFP4, 256, 5, 1, 1, "nvfp4_tc2_256x256_s5_acc1")          \
-    X(Kind::NVFP4, 128, 6, 2, 1, "nvfp4_tc2_256x128_s6_acc2")          \
-    X(Kind::FP8, 256, 6, 2, 1, "fp8_tc2_256x256_s6_acc2")              \
-    X(Kind::NVFP4, 256, 4, 1, 1, "nvfp4_tc2_256x256_s4_acc1")          \
-    X(Kind::NVFP4, 256, 3, 1, 1, "nvfp4_tc2_256x256_s3_acc1")          \
-    X(Kind::FP8, 256, 4, 2, 1, "fp8_tc2_256x256_s4_acc2")              \
-    X(Kind::NVFP4_BF16_TMEM, 256, 8, 1, 1, "nvfp4bf16_tc2_256x256_s8_acc1_tmema") \
-    X(Kind::NVFP4, 256, 5, 1, 2, "nvfp4_tc2x2_256x256_s5_acc1_mca")    \
-    X(Kind::FP8, 256, 6, 2, 2, "fp8_tc2x2_256x256_s6_acc2_mca")
+#define BSG_PAIR_PLANS(X)                                                    \
+    X(Kind::NVFP4, 256, 5, 1, 1, false, "nvfp4_tc2_256x256_s5_acc1")         \
+    X(Kind::NVFP4, 128, 6, 2, 1, false, "nvfp4_tc2_256x128_s6_acc2")         \
+    X(Kind::FP8, 256, 6, 2, 1, false, "fp8_tc2_256x256_s6_acc2")             \
+    X(Kind::NVFP4, 256, 4, 1, 1, false, "nvfp4_tc2_256x256_s4_acc1")         \
+    X(Kind::NVFP4, 256, 3, 1, 1, false, "nvfp4_tc2_256x256_s3_acc1")         \
+    X(Kind::FP8, 256, 4, 2, 1, false, "fp8_tc2_256x256_s4_acc2")             \
+    X(Kind::NVFP4_BF16_TMEM, 256, 8, 1, 1, false, "nvfp4bf16_tc2_256x256_s8_acc1_tmema") \
+    X(Kind::NVFP4, 256, 5, 1, 2, false, "nvfp4_tc2x2_256x256_s5_acc1_mca")   \
+    X(Kind::FP8, 256, 6, 2, 2, false, "fp8_tc2x2_256x256_s6_acc2_mca")       \
+    X(Kind::NVFP4, 256, 5, 1, 1, true, "nvfp4_tc2_256x256_s5_acc1_packed")
 
-#define BSG_PAIR_INFO(K, BN, S, A, MC, NAME) make_pair_plan<K, BN, S, A, MC>(NAME),
+#define BSG_PAIR_INFO(K, BN, S, A, MC, PK, NAME) make_pair_plan<K, BN, S, A, MC, PK>(NAME),
 static const PlanInfo kPairPlans[] = {BSG_PAIR_PLANS(BSG_PAIR_INFO)};
 #undef BSG_PAIR_INFO
 
@@ -701,9 +752,9 @@ cudaError_t pair_launch(int id, const GemmMaps &maps, const GemmArgs &args, int 
                         cudaStream_t stream)
 {
     int i = 0;
-#define BSG_PAIR_LAUNCH(K, BN, S, A, MC, NAME)                              \
-    if (id == i)                                                           \
-        return pair_launch_impl<K, BN, S, A, MC>(maps, args, grid, stream); \
+#define BSG_PAIR_LAUNCH(K, BN, S, A, MC, PK, NAME)                              \
+    if (id == i)                                                               \
+        return pair_launch_impl<K, BN, S, A, MC, PK>(maps, args, grid, stream); \
     ++i;
     BSG_PAIR_PLANS(BSG_PAIR_LAUNCH)
 #undef BSG_PAIR_LAUNCH
@@ -713,9 +764,9 @@ cudaError_t pair_launch(int id, const GemmMaps &maps, const GemmArgs &args, int 
 int pair_max_clusters(int id)
 {
     int i = 0;
-#define BSG_PAIR_OCC(K, BN, S, A, MC, NAME)            \
-    if (id == i)                                      \
-        return pair_clusters_impl<K, BN, S, A, MC>();  \
+#define BSG_PAIR_OCC(K, BN, S, A, MC, PK, NAME)            \
+    if (id == i)                                          \
+        return pair_clusters_impl<K, BN, S, A, MC, PK>();  \
     ++i;
     BSG_PAIR_PLANS(BSG_PAIR_OCC)
 #undef BSG_PAIR_OCC

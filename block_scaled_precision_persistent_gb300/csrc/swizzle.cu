@@ -118,6 +118,38 @@ cudaError_t launch_swizzle_scales_grouped(int E, int rows, int K, const int *off
     return cudaGetLastError();
 }
 
+// Tile-packed NVFP4 operand: tile (rb, kb) -- rows 128 rb .. +127, bytes
+// 128 kb .. +127 of each -- stored whole at tile index rb * kblocks + kb,
+// with the 128-byte swizzle applied inside (16-byte chunk c of row r at
+// chunk c ^ (r % 8)) and rows past the end zero, so that one 16 KiB bulk
+// copy into a 1024-byte-aligned buffer lands it as a 128B-swizzled
+// tensor-map load would. One CTA per tile: 256 threads x four 16-byte
+// chunks (loads coalesced along each row, stores along the tile).
+__global__ void __launch_bounds__(256)
+    pack_operand_kernel(const uint8_t *__restrict__ X, uint8_t *__restrict__ out, int rows, int width, int kblocks)
+{
+    const int kb = blockIdx.x, rb = blockIdx.y;
+    uint8_t *const tile = out + ((size_t)rb * (size_t)kblocks + (size_t)kb) * 16384u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = threadIdx.x + 256 * j;           // chunk i of the tile's 1024: row i / 8, chunk i % 8
+        const int r = i >> 3, c = i & 7;
+        const int row = rb * 128 + r;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < rows)
+            v = __ldg(reinterpret_cast<const uint4 *>(X + (size_t)row * (size_t)width + (size_t)kb * 128u + c * 16));
+        *reinterpret_cast<uint4 *>(tile + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+    }
+}
+
+cudaError_t launch_pack_operand(int rows, int K, const uint8_t *X, uint8_t *out, cudaStream_t stream)
+{
+    const int kblocks = K / 256;
+    const dim3 grid((unsigned)kblocks, (unsigned)((rows + 127) / 128));
+    pack_operand_kernel<<<grid, 256, 0, stream>>>(X, out, rows, K / 2, kblocks);
+    return cudaGetLastError();
+}
+
 // One thread waits, with the library's bounded wait, on an mbarrier that
 // nothing arrives on: after `ns` it records the timeout and returns.
 __global__ void watchdog_probe_kernel(unsigned int *status, unsigned long long ns)

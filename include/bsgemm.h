@@ -95,6 +95,37 @@ BSG_API int nvfp4_gemm_swizzled(int M, int N, int K,
                         const void *B, const void *sfB_swz,
                         float alpha, void *D, bsg_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Tile-packed NVFP4 operands (this library's own layout, made to be loaded
+ * by one contiguous 16 KiB bulk copy per tile instead of a tensor-map box:
+ * the per-SM ingest rate of contiguous copies is the higher one on sm_103a).
+ * Tile (rb, kb) holds rows 128 rb .. 128 rb + 127 and bytes 128 kb ..
+ * 128 kb + 127 of each row of a row-major uint8[rows][K/2] operand, stored
+ * at byte offset (rb * K/256 + kb) * 16384; inside a tile, byte c of row r
+ * sits at r * 128 + ((c / 16) XOR (r % 8)) * 16 + c % 16 (the 128-byte
+ * swizzle); rows past `rows` are zero.
+ *
+ * nvfp4_packed_operand_bytes: size of that layout, rows padded to 128
+ *   (0 for rows < 1 or K not a positive multiple of 256). Host only.
+ * nvfp4_pack_operand: X uint8[rows][K/2] (device, 16-byte aligned) ->
+ *   out (device, 16-byte aligned, nvfp4_packed_operand_bytes(rows, K)
+ *   bytes). Bit-exact byte permutation; one launch on `stream`. Requires
+ *   ceil(rows / 128) <= 65535.
+ * nvfp4_gemm_packed: the GEMM of nvfp4_gemm_swizzled with A and B given in
+ *   the packed layout (A_packed: nvfp4_packed_operand_bytes(M, K) bytes,
+ *   B_packed: nvfp4_packed_operand_bytes(N, K)), scales in the swizzled
+ *   layout. Always runs the plan "nvfp4_tc2_256x256_s5_acc1_packed" (a
+ *   forced plan does not apply; that plan cannot be forced on the other
+ *   entries). Same size and alignment rules and result as
+ *   nvfp4_gemm_swizzled; allocates nothing.
+ * ------------------------------------------------------------------------- */
+BSG_API size_t nvfp4_packed_operand_bytes(int rows, int K);
+BSG_API int nvfp4_pack_operand(int rows, int K, const void *X, void *out, bsg_stream_t stream);
+BSG_API int nvfp4_gemm_packed(int M, int N, int K,
+                      const void *A_packed, const void *sfA_swz,
+                      const void *B_packed, const void *sfB_swz,
+                      float alpha, void *D, bsg_stream_t stream);
+
 /* Scale-layout prep: row-major uint8[rows][K/16] -> the tcgen05 block-scale
  * layout: rows padded to a multiple of 128, K/16 padded to a multiple of 4,
  * 128x4 blocks of 512 bytes ordered row-block-major with the column block

@@ -266,3 +266,35 @@ def test_dense_kgrouped_bad_args(lib, entry):
     assert f(2, 128, 64, 128, BAD, BAD, BAD, None, 1.0, None, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG  # no koffs
     assert f(2, 128, 64, 128, BAD, BAD, BAD, BAD + 2, 1.0, None, None, BAD, None) == bsg.BSG_ERR_MISALIGNED
     assert f(2, 128, 64, 128, BAD, BAD, BAD, BAD, 1.0, BAD + 4, None, BAD, None) == bsg.BSG_ERR_MISALIGNED  # bias
+
+
+def test_packed_operand_bytes_and_bad_args(lib):
+    """Tile-packed layout: size rule, and argument checks before any launch."""
+    assert bsg.nvfp4_packed_operand_bytes(1, 256) == 128 * 128
+    assert bsg.nvfp4_packed_operand_bytes(300, 768) == 384 * 384
+    assert bsg.nvfp4_packed_operand_bytes(16384, 16384) == 16384 * 8192
+    for rows, K in ((0, 256), (8, 128), (8, 384), (-1, 256)):
+        assert bsg.nvfp4_packed_operand_bytes(rows, K) == 0
+        assert lib.nvfp4_pack_operand(rows, K, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert lib.nvfp4_pack_operand(128 * 65536, 256, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert lib.nvfp4_pack_operand(8, 256, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert lib.nvfp4_pack_operand(8, 256, BAD + 8, BAD, None) == bsg.BSG_ERR_MISALIGNED
+    assert lib.nvfp4_pack_operand(8, 256, BAD, BAD + 4, None) == bsg.BSG_ERR_MISALIGNED
+    g = lib.nvfp4_gemm_packed
+    for M, N, K in ((0, 8, 256), (8, 8, 300), (8, 12, 256)):
+        assert g(M, N, K, BAD, BAD, BAD, BAD, 1.0, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert g(8, 8, 256, None, BAD, BAD, BAD, 1.0, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert g(8, 8, 256, BAD, BAD, BAD + 8, BAD, 1.0, BAD, None) == bsg.BSG_ERR_MISALIGNED
+
+
+def test_packed_plan_is_listed_but_not_forceable(lib):
+    """The tile-packed plan exists, is never chosen by the planner, and a
+    forced packed plan is refused by the other entries' planner."""
+    bsg.bsg_force_plan("nvfp4_tc2_256x256_s5_acc1_packed")
+    try:
+        with pytest.raises(bsg.BsgError) as e:
+            bsg.bsg_select_plan(0, 16384, 16384, 16384, 152)
+        assert e.value.code == bsg.BSG_ERR_NO_PLAN
+    finally:
+        bsg.bsg_force_plan(None)
+    assert bsg.bsg_select_plan(0, 16384, 16384, 16384, 152) == "nvfp4_tc2_256x256_s5_acc1"
