@@ -637,6 +637,44 @@ def secondary_dense(dev, steps: int, pk: dict, psrc: str) -> dict:
             "timing": "CUDA graph of back-to-back launches, median over replays per launch"}
 
 
+def secondary_packed(dev, step: Nvfp4Step, pk: dict, psrc: str) -> dict:
+    """The headline shape with A and B in the tile-packed layout
+    (nvfp4_gemm_packed: operand tiles by contiguous bulk copies) against the
+    same GEMM from row-major operands (tensor-map boxes), as interleaved
+    CUDA graphs; plus the cost of packing one operand (A, as activations
+    would be each step; weights are packed once)."""
+    import block_scaled_precision_persistent_gb300 as bsg
+    w = step.w
+    M, N, K = w.M, w.N, w.K
+    s = torch.cuda.current_stream()
+    step()                                     # swizzled scales in step.swA / step.swB
+    ap = torch.empty(bsg.nvfp4_packed_operand_bytes(M, K), dtype=torch.uint8, device=dev)
+    bp = torch.empty(bsg.nvfp4_packed_operand_bytes(N, K), dtype=torch.uint8, device=dev)
+    bsg.nvfp4_pack_operand(M, K, step.A, ap, s)
+    bsg.nvfp4_pack_operand(N, K, step.B, bp, s)
+    torch.cuda.synchronize()
+    calls = {
+        "tensor_map": lambda: bsg.nvfp4_gemm_swizzled(M, N, K, step.A, step.swA, step.B, step.swB, step.alpha,
+                                                      step.D),
+        "packed": lambda: bsg.nvfp4_gemm_packed(M, N, K, ap, step.swA, bp, step.swB, step.alpha, step.D),
+        "pack_a": lambda: bsg.nvfp4_pack_operand(M, K, step.A, ap),
+    }
+    us = graph_us(calls, 8, 5)
+    if bsg.bsg_get_device_status() != bsg.BSG_OK:
+        raise SystemExit("device status reported an error in the packed-operand timing")
+    tf = {k: w.flops / (us[k] * 1e-6) / 1e12 for k in ("tensor_map", "packed")}
+    pack_bytes = 2 * (M * K // 2)
+    gbs = pack_bytes / (us["pack_a"] * 1e-6) / 1e9
+    del ap, bp
+    return {"shape": f"{M}x{N}x{K}", "plan": "nvfp4_tc2_256x256_s5_acc1_packed",
+            "us": {k: round(v, 2) for k, v in us.items()},
+            "tflops_tensor_map": round(tf["tensor_map"], 1), "tflops_packed": round(tf["packed"], 1),
+            "packed_over_tensor_map": round(us["tensor_map"] / us["packed"], 4),
+            "tflops_packed_incl_pack_a": round(w.flops / ((us["packed"] + us["pack_a"]) * 1e-6) / 1e12, 1),
+            "pack_a_gb_s": round(gbs, 1), "pack_a_frac_hbm": round(gbs / pk["hbm_gbs"], 4), "peak_source": psrc,
+            "timing": "interleaved CUDA graphs of 8 back-to-back launches, median of 5 rounds"}
+
+
 def secondary_swizzle(dev, steps: int, pk: dict, psrc: str) -> dict:
     """The scale-layout prep alone (timed separately from the GEMM): one
     operand's row-major [16384][1024] E4M3 scales into the swizzled layout;
@@ -799,6 +837,7 @@ def run_ours(args, dist: Dist) -> None:
         secondary["epilogue"] = secondary_epilogue(dev, step, 10, pk, psrc)
         secondary["grouped"] = secondary_grouped(dev, 15, pk, psrc)
         secondary["dense"] = secondary_dense(dev, 10, pk, psrc)
+        secondary["packed"] = secondary_packed(dev, step, pk, psrc)
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, host_copy(step), args.cpu_seconds)
