@@ -404,10 +404,22 @@ def secondary_quantize(dev, steps: int, pk: dict, psrc: str) -> dict:
         evs.append((a, b))
     torch.cuda.synchronize()
     us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+    # the same with the codes written in the tile-packed layout
+    evs = []
+    for i in range(steps + 3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        bsg.nvfp4_quantize_tiles(rows, K, x, packed, swz, None, gl, s)
+        b.record(s)
+        if i >= 3:
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    us_tiles = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
     moved = 2 * (2 * rows * K) + rows * K // 2 + bsg.nvfp4_swizzled_scale_bytes(rows, K)
     gbs = moved / (us * 1e-6) / 1e9
     return {"shape": f"bf16 {rows} x {K}", "us": round(us, 2), "gb_s": round(gbs, 1),
             "frac_hbm": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": moved, "peak_source": psrc,
+            "us_tile_packed_codes": round(us_tiles, 2),
             "launches": 2, "timing": "median per-call CUDA events (memset + 2 kernels), X > L2"}
 
 

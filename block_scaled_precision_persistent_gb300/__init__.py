@@ -20,6 +20,7 @@ __all__ = [
     "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes", "nvfp4_dense_gemm",
     "nvfp4_dense_f16_gemm", "nvfp4_dense_grouped_gemm", "nvfp4_dense_f16_grouped_gemm",
     "nvfp4_dense_kgrouped_gemm", "nvfp4_dense_f16_kgrouped_gemm",
+    "nvfp4_quantize_tiles", "nvfp4_pack_operand", "nvfp4_packed_operand_bytes", "nvfp4_gemm_packed",
     "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_set_pdl", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_measure_ingress",
@@ -54,6 +55,7 @@ _SIGNATURES = {
     "nvfp4_swizzle_scales": (_i, [_i, _i, _vp, _vp, _vp]),
     "nvfp4_swizzled_scale_bytes": (ctypes.c_size_t, [_i, _i]),
     "nvfp4_quantize": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "nvfp4_quantize_tiles": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_gemm_noalloc": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "fp8_gemm": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "nvfp4_gemm_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
@@ -171,6 +173,13 @@ def nvfp4_swizzle_scales(rows, K, sf, sf_swz, stream=None) -> None:
 
 def nvfp4_swizzled_scale_bytes(rows, K) -> int:
     return int(load().nvfp4_swizzled_scale_bytes(rows, K))
+
+
+def nvfp4_quantize_tiles(rows, K, X, packed_tiles, sf_swz, sf_rowmajor, global_scales, stream=None) -> None:
+    """As nvfp4_quantize, with the codes written in the tile-packed layout
+    nvfp4_gemm_packed reads (K % 256 == 0)."""
+    _check(load().nvfp4_quantize_tiles(rows, K, _ptr(X), _ptr(packed_tiles), _ptr(sf_swz), _ptr(sf_rowmajor),
+                                       _ptr(global_scales), _stream(stream)), "nvfp4_quantize_tiles")
 
 
 def nvfp4_quantize(rows, K, X, packed, sf_swz, sf_rowmajor, global_scales, stream=None) -> None:

@@ -739,11 +739,13 @@ int nvfp4_gemm_packed(int M, int N, int K, const void *A_packed, const void *sfA
                     static_cast<const uint8_t *>(A_packed), static_cast<const uint8_t *>(B_packed));
 }
 
-int nvfp4_quantize(int rows, int K, const void *X, void *packed, void *sf_swz, void *sf_rowmajor,
-                   float *global, bsg_stream_t stream)
+static int quantize(bool tiles, int rows, int K, const void *X, void *packed, void *sf_swz, void *sf_rowmajor,
+                    float *global, bsg_stream_t stream)
 {
     t_last_launches = 0;
     if (!X || !packed || !sf_swz || !global || rows < 1 || K < 16 || (K % 16) != 0)
+        return BSG_ERR_INVALID_ARG;
+    if (tiles && (K % 256) != 0)
         return BSG_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(packed) || !aligned16(sf_swz) ||
         (reinterpret_cast<uintptr_t>(global) & 7u) != 0)
@@ -754,10 +756,22 @@ int nvfp4_quantize(int rows, int K, const void *X, void *packed, void *sf_swz, v
         return rc;
     if (bsg::launch_nvfp4_quantize(rows, K, X, static_cast<uint8_t *>(packed), static_cast<uint8_t *>(sf_swz),
                                    static_cast<uint8_t *>(sf_rowmajor), global, ds->sms,
-                                   reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+                                   reinterpret_cast<cudaStream_t>(stream), tiles) != cudaSuccess)
         return BSG_ERR_CUDA;
     t_last_launches = 2;
     return BSG_OK;
+}
+
+int nvfp4_quantize(int rows, int K, const void *X, void *packed, void *sf_swz, void *sf_rowmajor,
+                   float *global, bsg_stream_t stream)
+{
+    return quantize(false, rows, K, X, packed, sf_swz, sf_rowmajor, global, stream);
+}
+
+int nvfp4_quantize_tiles(int rows, int K, const void *X, void *packed_tiles, void *sf_swz, void *sf_rowmajor,
+                         float *global, bsg_stream_t stream)
+{
+    return quantize(true, rows, K, X, packed_tiles, sf_swz, sf_rowmajor, global, stream);
 }
 
 int nvfp4_swizzle_scales(int rows, int K, const void *sf, void *sf_swz, bsg_stream_t stream)

@@ -138,7 +138,8 @@ cudaError_t launch_swizzle_scales_grouped(int E, int rows, int K, const int *off
 
 // Two-level NVFP4 quantisation: memset of global[0], amax kernel, quantiser.
 cudaError_t launch_nvfp4_quantize(int rows, int K, const void *X, uint8_t *packed, uint8_t *sf_swz,
-                                  uint8_t *sf_rm, float *global, int num_sms, cudaStream_t stream);
+                                  uint8_t *sf_rm, float *global, int num_sms, cudaStream_t stream,
+                                  bool tiles = false);
 
 // Tile-packed NVFP4 operand (swizzle.cu): rows x K/2 bytes -> 16 KiB tiles
 // of 128 rows x 128 bytes, 128B-swizzled inside, rows padded to 128.

@@ -177,9 +177,14 @@ __global__ void __launch_bounds__(kAmaxThreads)
 }
 
 // One CTA: rows [128 y, +128) x 16-element blocks [16 x, +16).
+// tiles: codes go to the tile-packed layout (16 KiB tiles of 128 rows x 128
+// bytes, tile index row_block * K/256 + k_block, 16-byte chunk c of row r at
+// chunk c ^ (r % 8)), and rows past `rows` of the last row block are written
+// as zero codes; otherwise row-major rows of K/2 bytes.
 __global__ void __launch_bounds__(kQThreads)
     quantize_kernel(const __nv_bfloat16 *__restrict__ X, int rows, int K, uint8_t *__restrict__ packed,
-                    uint8_t *__restrict__ sf_swz, uint8_t *__restrict__ sf_rm, float *__restrict__ global)
+                    uint8_t *__restrict__ sf_swz, uint8_t *__restrict__ sf_rm, float *__restrict__ global,
+                    int tiles)
 {
     __shared__ uint32_t tile[kQRows * kQPitch];
     uint8_t *t8 = reinterpret_cast<uint8_t *>(tile);
@@ -197,6 +202,13 @@ __global__ void __launch_bounds__(kQThreads)
         const int r = idx / kQBlocks, cl = idx % kQBlocks;          // 16 consecutive threads: one row
         const int row = blockIdx.y * kQRows + r, cb = blockIdx.x * kQBlocks + cl;
         uint32_t scode = 0u;
+        // byte 8 cb of row `row` in the tile-packed layout (8 bytes stay in
+        // one 16-byte chunk; 16 consecutive threads fill one 128-byte row of a tile)
+        const size_t tile_off = tiles ? (((size_t)blockIdx.y * (size_t)(K / 256) + (size_t)(cb >> 4)) * 128u + r) *
+                                                128u + (size_t)((((cb & 15) >> 1) ^ (r & 7)) << 4) + 8u * (cb & 1)
+                                      : 0;
+        if (tiles && row >= rows && cb < nb)
+            *reinterpret_cast<uint2 *>(packed + tile_off) = make_uint2(0u, 0u);
         if (row < rows && cb < nb) {
             const uint4 *src = reinterpret_cast<const uint4 *>(X + (size_t)row * (size_t)K + 16 * (size_t)cb);
             const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
@@ -249,7 +261,8 @@ __global__ void __launch_bounds__(kQThreads)
                     (h == 0 ? out.x : out.y) = c;
                 }
             }
-            *reinterpret_cast<uint2 *>(packed + (size_t)row * (size_t)(K / 2) + 8 * (size_t)cb) = out;
+            *reinterpret_cast<uint2 *>(packed + (tiles ? tile_off : (size_t)row * (size_t)(K / 2) + 8 * (size_t)cb)) =
+                out;
             if (sf_rm)
                 sf_rm[(size_t)row * (size_t)nb + cb] = (uint8_t)scode;
         }
@@ -274,7 +287,7 @@ __global__ void __launch_bounds__(kQThreads)
 }  // namespace
 
 cudaError_t launch_nvfp4_quantize(int rows, int K, const void *X, uint8_t *packed, uint8_t *sf_swz,
-                                  uint8_t *sf_rm, float *global, int num_sms, cudaStream_t stream)
+                                  uint8_t *sf_rm, float *global, int num_sms, cudaStream_t stream, bool tiles)
 {
     cudaError_t e = cudaMemsetAsync(global, 0, sizeof(float), stream);
     if (e != cudaSuccess)
@@ -291,7 +304,7 @@ cudaError_t launch_nvfp4_quantize(int rows, int K, const void *X, uint8_t *packe
     const int nb = K / 16;
     dim3 grid((unsigned)((nb + kQBlocks - 1) / kQBlocks), (unsigned)((rows + kQRows - 1) / kQRows));
     quantize_kernel<<<grid, kQThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(X), rows, K, packed,
-                                                     sf_swz, sf_rm, global);
+                                                     sf_swz, sf_rm, global, tiles ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -161,6 +161,16 @@ BSG_API size_t nvfp4_swizzled_scale_bytes(int rows, int K);
 BSG_API int nvfp4_quantize(int rows, int K, const void *X, void *packed, void *sf_swz,
                            void *sf_rowmajor, float *global, bsg_stream_t stream);
 
+/* The same quantisation with the codes written in the tile-packed operand
+ * layout that nvfp4_gemm_packed reads (see nvfp4_pack_operand), so that
+ * activations need no separate packing pass: packed_tiles holds
+ * nvfp4_packed_operand_bytes(rows, K) bytes (16-byte aligned), and the
+ * padding rows of its last row block are written as zero codes. Scales,
+ * global and every other argument as nvfp4_quantize. Requires K % 256 == 0
+ * (BSG_ERR_INVALID_ARG otherwise).                                         */
+BSG_API int nvfp4_quantize_tiles(int rows, int K, const void *X, void *packed_tiles, void *sf_swz,
+                                 void *sf_rowmajor, float *global, bsg_stream_t stream);
+
 /* NVFP4 GEMM with row-major scales that allocates nothing. The pages have no
  * counterpart to this entry point; it exists for callers that cannot call
  * cudaMalloc -- for instance a runtime that has handed all device memory to

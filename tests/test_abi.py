@@ -157,6 +157,11 @@ def test_quantize_bad_args(lib):
     assert q(8, 256, BAD, BAD + 8, BAD, None, BAD, None) == bsg.BSG_ERR_MISALIGNED       # packed
     assert q(8, 256, BAD, BAD, BAD + 4, None, BAD, None) == bsg.BSG_ERR_MISALIGNED       # sf_swz
     assert q(8, 256, BAD, BAD, BAD, None, BAD + 4, None) == bsg.BSG_ERR_MISALIGNED       # global
+    t = lib.nvfp4_quantize_tiles
+    assert t(8, 48, BAD, BAD, BAD, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG          # K % 256
+    assert t(8, 768 + 16, BAD, BAD, BAD, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert t(0, 256, BAD, BAD, BAD, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert t(8, 256, BAD, BAD + 8, BAD, None, BAD, None) == bsg.BSG_ERR_MISALIGNED       # tiles
 
 
 def test_epilogue_bad_args(lib):

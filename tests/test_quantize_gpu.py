@@ -166,3 +166,58 @@ def test_quantize_beyond_2g_elements(dev):
         assert np.array_equal(sw[off], sf_ref[i]), r
     del x, packed, swz, rm
     torch.cuda.empty_cache()
+
+
+def gpu_quantize_tiles(x: torch.Tensor, dev):
+    rows, K = x.shape
+    xd = x.to(dev).contiguous()
+    n = bsg.nvfp4_packed_operand_bytes(rows, K)
+    tiles = torch.full((n + 256,), 0xAB, dtype=torch.uint8, device=dev)
+    swz = torch.full((bsg.nvfp4_swizzled_scale_bytes(rows, K),), 0xAB, dtype=torch.uint8, device=dev)
+    gl = torch.full((2,), -1.0, dtype=torch.float32, device=dev)
+    bsg.nvfp4_quantize_tiles(rows, K, xd, tiles[:n], swz, None, gl)
+    torch.cuda.synchronize()
+    assert bsg.bsg_last_launch_count() == 2
+    t = tiles.cpu().numpy()
+    assert (t[n:] == 0xAB).all(), "quantiser wrote past the tile-packed buffer"
+    return t[:n], swz.cpu().numpy(), gl.cpu().numpy()
+
+
+@pytest.mark.parametrize("rows,K", [(1, 256), (127, 512), (128, 256), (300, 1280), (513, 4096)])
+def test_quantize_tiles_against_oracle(dev, rows, K):
+    """Codes in the tile-packed layout: the oracle's quantisation followed by
+    the oracle's tile packing, bit for bit (padding rows zero); scales and
+    the global scale as the row-major entry."""
+    x = bf16_input(rows, K, seed=rows + K, std=3.0)
+    o = oracle.get()
+    p_ref, sf_ref, amax_ref, sg_ref = o.nvfp4_quantize(x.view(torch.int16).numpy().view(np.uint16))
+    tiles, swz, gl = gpu_quantize_tiles(x, dev)
+    assert gl[0] == amax_ref and gl[1] == sg_ref
+    ref = oracle.pack_operand_tiles(p_ref, K)
+    assert np.array_equal(tiles, ref), f"tile codes differ at {np.argwhere(tiles != ref)[:4]}"
+    assert np.array_equal(swz, o.swizzle_scales(sf_ref, K)), "swizzled scales differ"
+
+
+def test_quantize_tiles_then_packed_gemm(dev):
+    """Activations quantised straight into tiles, weights quantised and
+    packed, then nvfp4_gemm_packed: the oracle GEMM over the oracle-quantised
+    operands, within the GEMM tolerance."""
+    M, N, K = 300, 392, 2048
+    a = bf16_input(M, K, seed=11)
+    b = bf16_input(N, K, seed=12)
+    ta, swa, ga = gpu_quantize_tiles(a, dev)
+    pb, rmb, swb, gb = gpu_quantize(b, dev)
+    bp = torch.empty(bsg.nvfp4_packed_operand_bytes(N, K), dtype=torch.uint8, device=dev)
+    bsg.nvfp4_pack_operand(N, K, torch.from_numpy(pb).to(dev), bp)
+    alpha = float(np.float32(1.0) / (np.float32(ga[1]) * np.float32(gb[1])))
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    bsg.nvfp4_gemm_packed(M, N, K, torch.from_numpy(ta).to(dev), torch.from_numpy(swa).to(dev), bp,
+                          torch.from_numpy(swb).to(dev), alpha, D)
+    torch.cuda.synchronize()
+    assert bsg.bsg_get_device_status() == bsg.BSG_OK
+    o = oracle.get()
+    qa = o.nvfp4_quantize(a.view(torch.int16).numpy().view(np.uint16))
+    qb = o.nvfp4_quantize(b.view(torch.int16).numpy().view(np.uint16))
+    _, T, ref = o.nvfp4_gemm(qa[0], qa[1], qb[0], qb[1], alpha, K)
+    got = D.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert oracle.within_tolerance(got, ref, T).all()
