@@ -158,15 +158,14 @@ class Nvfp4Step:
 
     def __call__(self, ev=None):
         b, w = self.bsg, self.w
-        b.nvfp4_swizzle_scales(w.M, w.K, self.sfA, self.swA, self.stream)
-        b.nvfp4_swizzle_scales(w.N, w.K, self.sfB, self.swB, self.stream)
+        b.nvfp4_swizzle_scales2(w.M, w.N, w.K, self.sfA, self.swA, self.sfB, self.swB, self.stream)
         if ev is not None:
             ev[0].record(self.stream)
         b.nvfp4_gemm_swizzled(w.M, w.N, w.K, self.A, self.swA, self.B, self.swB, self.alpha,
                               self.D, self.stream)
         if ev is not None:
             ev[1].record(self.stream)
-        self.launches += 3
+        self.launches += 2
 
     def plan(self) -> str:
         return self.bsg.bsg_select_plan(0, self.w.M, self.w.N, self.w.K,

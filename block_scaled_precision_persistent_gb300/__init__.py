@@ -20,7 +20,7 @@ __all__ = [
     "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes", "nvfp4_dense_gemm",
     "nvfp4_dense_f16_gemm", "nvfp4_dense_grouped_gemm", "nvfp4_dense_f16_grouped_gemm",
     "nvfp4_dense_kgrouped_gemm", "nvfp4_dense_f16_kgrouped_gemm",
-    "nvfp4_quantize_tiles", "nvfp4_pack_operand", "nvfp4_packed_operand_bytes", "nvfp4_gemm_packed",
+    "nvfp4_swizzle_scales2", "nvfp4_quantize_tiles", "nvfp4_pack_operand", "nvfp4_packed_operand_bytes", "nvfp4_gemm_packed",
     "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_set_pdl", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_measure_ingress",
@@ -53,6 +53,7 @@ _SIGNATURES = {
     "nvfp4_pack_operand": (_i, [_i, _i, _vp, _vp, _vp]),
     "nvfp4_gemm_packed": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "nvfp4_swizzle_scales": (_i, [_i, _i, _vp, _vp, _vp]),
+    "nvfp4_swizzle_scales2": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_swizzled_scale_bytes": (ctypes.c_size_t, [_i, _i]),
     "nvfp4_quantize": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_quantize_tiles": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -169,6 +170,12 @@ def nvfp4_gemm_packed(M, N, K, A_packed, sfA_swz, B_packed, sfB_swz, alpha, D, s
 def nvfp4_swizzle_scales(rows, K, sf, sf_swz, stream=None) -> None:
     _check(load().nvfp4_swizzle_scales(rows, K, _ptr(sf), _ptr(sf_swz), _stream(stream)),
            "nvfp4_swizzle_scales")
+
+
+def nvfp4_swizzle_scales2(M, N, K, sfA, sfA_swz, sfB, sfB_swz, stream=None) -> None:
+    """Both operands' scales of one GEMM into the swizzled layout, one launch."""
+    _check(load().nvfp4_swizzle_scales2(M, N, K, _ptr(sfA), _ptr(sfA_swz), _ptr(sfB), _ptr(sfB_swz),
+                                        _stream(stream)), "nvfp4_swizzle_scales2")
 
 
 def nvfp4_swizzled_scale_bytes(rows, K) -> int:

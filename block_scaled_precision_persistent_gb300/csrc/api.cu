@@ -549,6 +549,20 @@ int run_kgrouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, 
     return BSG_OK;
 }
 
+// Both operands' scales of one GEMM: one launch while the two grids' block
+// rows fit the grid's y limit, else one launch each.
+cudaError_t swizzle_both(int M, int N, int K, const uint8_t *sfa, uint8_t *out_a, const uint8_t *sfb,
+                         uint8_t *out_b, cudaStream_t s, int *launches)
+{
+    if ((long long)(M + 127) / 128 + (N + 127) / 128 <= 65535) {
+        *launches = 1;
+        return bsg::launch_swizzle_scales2(M, N, K, sfa, out_a, sfb, out_b, s);
+    }
+    *launches = 2;
+    cudaError_t e = bsg::launch_swizzle_scales(M, K, sfa, out_a, s);
+    return e != cudaSuccess ? e : bsg::launch_swizzle_scales(N, K, sfb, out_b, s);
+}
+
 int check_nvfp4_args(int M, int N, int K, const void *A, const void *sfA, const void *B,
                      const void *sfB, void *D)
 {
@@ -691,11 +705,33 @@ int nvfp4_gemm(int M, int N, int K, const void *A, const void *sfA, const void *
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *swz_a = ds->ws;
     uint8_t *swz_b = ds->ws + bytes_a;
-    if (bsg::launch_swizzle_scales(M, K, static_cast<const uint8_t *>(sfA), swz_a, s) != cudaSuccess ||
-        bsg::launch_swizzle_scales(N, K, static_cast<const uint8_t *>(sfB), swz_b, s) != cudaSuccess)
+    int swz_launches = 0;
+    if (swizzle_both(M, N, K, static_cast<const uint8_t *>(sfA), swz_a, static_cast<const uint8_t *>(sfB), swz_b, s,
+                     &swz_launches) != cudaSuccess)
         return BSG_ERR_CUDA;
-    t_last_launches = 2;
+    t_last_launches = swz_launches;
     return run_gemm(Kind::NVFP4, M, N, K, A, B, swz_a, swz_b, nullptr, nullptr, alpha, D, s, ds);
+}
+
+int nvfp4_swizzle_scales2(int M, int N, int K, const void *sfA, void *sfA_swz, const void *sfB, void *sfB_swz,
+                          bsg_stream_t stream)
+{
+    t_last_launches = 0;
+    if (!sfA || !sfA_swz || !sfB || !sfB_swz || M < 1 || N < 1 || K < 16 || (K % 16) != 0)
+        return BSG_ERR_INVALID_ARG;
+    if (!aligned16(sfA_swz) || !aligned16(sfB_swz))
+        return BSG_ERR_MISALIGNED;
+    DeviceState *ds = nullptr;
+    int rc = current_device(&ds);
+    if (rc != BSG_OK)
+        return rc;
+    int n = 0;
+    if (swizzle_both(M, N, K, static_cast<const uint8_t *>(sfA), static_cast<uint8_t *>(sfA_swz),
+                     static_cast<const uint8_t *>(sfB), static_cast<uint8_t *>(sfB_swz),
+                     reinterpret_cast<cudaStream_t>(stream), &n) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    t_last_launches = n;
+    return BSG_OK;
 }
 
 size_t nvfp4_packed_operand_bytes(int rows, int K)

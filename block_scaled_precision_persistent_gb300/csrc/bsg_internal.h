@@ -133,6 +133,9 @@ cudaError_t launch_swizzle_scales(int rows, int K, const uint8_t *sf, uint8_t *o
 
 // Per-slice scale-layout prep of a grouped A (offs: device int32[E+1]);
 // out holds (ceil(rows / 128) + E) block rows.
+// Both operands' scales of one GEMM (same K) in one launch.
+cudaError_t launch_swizzle_scales2(int rows_a, int rows_b, int K, const uint8_t *sfa, uint8_t *out_a,
+                                   const uint8_t *sfb, uint8_t *out_b, cudaStream_t stream);
 cudaError_t launch_swizzle_scales_grouped(int E, int rows, int K, const int *offs, const uint8_t *sf,
                                           uint8_t *out, cudaStream_t stream);
 

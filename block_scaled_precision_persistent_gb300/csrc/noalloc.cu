@@ -72,9 +72,7 @@ extern "C" int nvfp4_gemm_noalloc(int M, int N, int K, const void *A, const void
         return rc;
     // Every byte of both swizzled regions (padding included) is rewritten by
     // the swizzle, so the previous call's contents never leak into this one.
-    if ((rc = nvfp4_swizzle_scales(M, K, sfA, scratch, stream)) != BSG_OK)
-        return rc;
-    if ((rc = nvfp4_swizzle_scales(N, K, sfB, scratch + bytes_a, stream)) != BSG_OK)
+    if ((rc = nvfp4_swizzle_scales2(M, N, K, sfA, scratch, sfB, scratch + bytes_a, stream)) != BSG_OK)
         return rc;
     return nvfp4_gemm_swizzled(M, N, K, A, scratch, B, scratch + bytes_a, alpha, D, stream);
 }

@@ -27,18 +27,29 @@ constexpr int kSwzPitchWords = 17;          // 16 words per staged row + 1 (bank
 // GROUPED: the rows are E slices (offs, device); slice e is swizzled on its
 // own from block row sb[e] on (group.cuh), and block rows past the slices'
 // (grid y covers ceil(rows / 128) + E) are written as zeros.
+// Two operands of the same K in one launch (not GROUPED): grid rows
+// y >= nrb1 swizzle the second one (in2 -> out2, rows2 rows) from its block
+// row y - nrb1.
 template <bool GROUPED>
 __global__ void __launch_bounds__(kSwzThreads)
     swizzle_scales_kernel(const uint8_t *__restrict__ in, uint8_t *__restrict__ out, int rows,
-                          int cols, int ncb, int vec16, const int *offs, int E)
+                          int cols, int ncb, int vec16, const int *offs, int E,
+                          const uint8_t *__restrict__ in2, uint8_t *__restrict__ out2, int rows2, int nrb1)
 {
     __shared__ uint32_t tile[128 * kSwzPitchWords];
     uint8_t *t8 = reinterpret_cast<uint8_t *>(tile);
-    const int rb = blockIdx.y;
+    int rb = blockIdx.y;
+    if (!GROUPED && rb >= nrb1) {
+        rb -= nrb1;
+        in = in2;
+        out = out2;
+        rows = rows2;
+    }
     const int cb0 = blockIdx.x * kSwzBlocksPerCta;
     const int c0 = cb0 * 4;
     const int span = kSwzBlocksPerCta * 4;  // 64 scale columns
     int row0 = rb * 128, row_end = rows;    // source rows of this block row: [row0, row_end)
+    (void)E;
     if constexpr (GROUPED) {
         __shared__ int so[kMaxGroups + 1], sb[kMaxGroups + 1];
         if (threadIdx.x < 32)
@@ -102,7 +113,24 @@ cudaError_t launch_swizzle_scales(int rows, int K, const uint8_t *sf, uint8_t *o
     const int nrb = (rows + 127) / 128;
     dim3 grid((ncb + kSwzBlocksPerCta - 1) / kSwzBlocksPerCta, nrb);
     const int vec16 = (cols % 16) == 0 && (reinterpret_cast<uintptr_t>(sf) & 15u) == 0;
-    swizzle_scales_kernel<false><<<grid, kSwzThreads, 0, stream>>>(sf, out, rows, cols, ncb, vec16, nullptr, 0);
+    swizzle_scales_kernel<false><<<grid, kSwzThreads, 0, stream>>>(sf, out, rows, cols, ncb, vec16, nullptr, 0,
+                                                                   nullptr, nullptr, 0, nrb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swizzle_scales2(int rows_a, int rows_b, int K, const uint8_t *sfa, uint8_t *out_a,
+                                   const uint8_t *sfb, uint8_t *out_b, cudaStream_t stream)
+{
+    const int cols = K / 16;
+    const int ncb = (cols + 3) / 4;
+    const int nrb_a = (rows_a + 127) / 128, nrb_b = (rows_b + 127) / 128;
+    if ((long long)nrb_a + nrb_b > 65535)
+        return cudaErrorInvalidConfiguration;
+    dim3 grid((ncb + kSwzBlocksPerCta - 1) / kSwzBlocksPerCta, nrb_a + nrb_b);
+    const int vec16 = (cols % 16) == 0 && (reinterpret_cast<uintptr_t>(sfa) & 15u) == 0 &&
+                      (reinterpret_cast<uintptr_t>(sfb) & 15u) == 0;
+    swizzle_scales_kernel<false><<<grid, kSwzThreads, 0, stream>>>(sfa, out_a, rows_a, cols, ncb, vec16, nullptr,
+                                                                   0, sfb, out_b, rows_b, nrb_a);
     return cudaGetLastError();
 }
 
@@ -114,7 +142,8 @@ cudaError_t launch_swizzle_scales_grouped(int E, int rows, int K, const int *off
     const int nrb = (rows + 127) / 128 + E;     // bound on the slices' block rows
     dim3 grid((ncb + kSwzBlocksPerCta - 1) / kSwzBlocksPerCta, nrb);
     const int vec16 = (cols % 16) == 0 && (reinterpret_cast<uintptr_t>(sf) & 15u) == 0;
-    swizzle_scales_kernel<true><<<grid, kSwzThreads, 0, stream>>>(sf, out, rows, cols, ncb, vec16, offs, E);
+    swizzle_scales_kernel<true><<<grid, kSwzThreads, 0, stream>>>(sf, out, rows, cols, ncb, vec16, offs, E,
+                                                                  nullptr, nullptr, 0, nrb);
     return cudaGetLastError();
 }
 

@@ -135,6 +135,14 @@ BSG_API int nvfp4_gemm_packed(int M, int N, int K,
 BSG_API int nvfp4_swizzle_scales(int rows, int K, const void *sf, void *sf_swz,
                          bsg_stream_t stream);
 
+/* Both operands' scales of one GEMM in one launch: sfA uint8[M][K/16] ->
+ * sfA_swz, sfB uint8[N][K/16] -> sfB_swz, each exactly as
+ * nvfp4_swizzle_scales would write it. Requires M, N >= 1, K % 16 == 0,
+ * 16-byte aligned outputs. (Where ceil(M/128) + ceil(N/128) exceeds 65535
+ * the two operands take one launch each.) nvfp4_gemm uses it.           */
+BSG_API int nvfp4_swizzle_scales2(int M, int N, int K, const void *sfA, void *sfA_swz,
+                                  const void *sfB, void *sfB_swz, bsg_stream_t stream);
+
 /* Size in bytes of the swizzled layout (0 for invalid sizes). Host only.  */
 BSG_API size_t nvfp4_swizzled_scale_bytes(int rows, int K);
 

@@ -70,6 +70,13 @@ def test_swizzle_bad_args(lib):
     assert lib.nvfp4_swizzle_scales(0, 256, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
     assert lib.nvfp4_swizzle_scales(8, 24, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
     assert lib.nvfp4_swizzle_scales(8, 256, BAD, BAD + 4, None) == bsg.BSG_ERR_MISALIGNED
+    s2 = lib.nvfp4_swizzle_scales2
+    assert s2(0, 8, 256, BAD, BAD, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert s2(8, 0, 256, BAD, BAD, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert s2(8, 8, 24, BAD, BAD, BAD, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert s2(8, 8, 256, BAD, BAD, None, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert s2(8, 8, 256, BAD, BAD + 4, BAD, BAD, None) == bsg.BSG_ERR_MISALIGNED
+    assert s2(8, 8, 256, BAD, BAD, BAD, BAD + 8, None) == bsg.BSG_ERR_MISALIGNED
 
 
 def test_swizzled_bytes(lib):

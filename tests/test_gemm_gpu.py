@@ -68,7 +68,7 @@ def gpu_nvfp4(p, dev, entry="rowmajor", stream=None):
     flat, D = new_out(M, N, dev)
     if entry == "rowmajor":
         bsg.nvfp4_gemm(M, N, K, t["A"], t["sfA"], t["B"], t["sfB"], p["alpha"], D, stream)
-        assert bsg.bsg_last_launch_count() == 3
+        assert bsg.bsg_last_launch_count() == 2      # both scale swizzles in one launch, then the GEMM
     else:
         sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
         sb = torch.empty(bsg.nvfp4_swizzled_scale_bytes(N, K), dtype=torch.uint8, device=dev)
@@ -122,6 +122,27 @@ def test_swizzle_bit_exact(dev, rows, K):
     bsg.nvfp4_swizzle_scales(rows, K, torch.from_numpy(sf).to(dev), out)
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 16), (127, 129, 48), (300, 8, 1040), (4096, 1000, 4096),
+                                   (16384, 16384, 16384)])
+def test_swizzle_two_operands_bit_exact(dev, M, N, K):
+    """nvfp4_swizzle_scales2: both operands in one launch, each exactly the
+    oracle's layout (padding zeroed), guard bytes untouched."""
+    rng = np.random.default_rng(M * 3 + N + K)
+    sa = rng.integers(0, 256, (M, K // 16)).astype(np.uint8)
+    sb = rng.integers(0, 256, (N, K // 16)).astype(np.uint8)
+    o = oracle.get()
+    wa, wb = o.swizzle_scales(sa, K), o.swizzle_scales(sb, K)
+    buf = torch.full((wa.size + wb.size + 512,), 0xAB, dtype=torch.uint8, device=dev)
+    oa, ob = buf[: wa.size], buf[wa.size + 256: wa.size + 256 + wb.size]
+    bsg.nvfp4_swizzle_scales2(M, N, K, torch.from_numpy(sa).to(dev), oa, torch.from_numpy(sb).to(dev), ob)
+    assert bsg.bsg_last_launch_count() == 1
+    torch.cuda.synchronize()
+    h = buf.cpu().numpy()
+    assert np.array_equal(h[: wa.size], wa)
+    assert np.array_equal(h[wa.size + 256: wa.size + 256 + wb.size], wb)
+    assert (h[wa.size: wa.size + 256] == 0xAB).all() and (h[wa.size + 256 + wb.size:] == 0xAB).all()
 
 
 @pytest.mark.parametrize("offset", [1, 4, 8])
