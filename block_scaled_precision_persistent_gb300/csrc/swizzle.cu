@@ -12,17 +12,18 @@
 //
 // Each output 16-byte line holds the 4-byte column-block word of rows r0,
 // r0+32, r0+64, r0+96, so the kernel is a permutation of 32-bit words: a CTA
-// stages 128 rows x 64 scale columns in shared memory with coalesced reads and
-// writes 16 contiguous 512-byte blocks. HBM-bound; bytes in = bytes out.
+// stages 128 rows x 128 scale columns in shared memory with coalesced reads
+// (four 16-byte loads in flight per thread) and writes 32 contiguous
+// 512-byte blocks. HBM-bound; bytes in = bytes out.
 #include "bsg_internal.h"
 #include "group.cuh"
 #include "ptx.cuh"
 
 namespace bsg {
 
-constexpr int kSwzBlocksPerCta = 16;        // 4-column blocks per CTA (64 scale columns)
+constexpr int kSwzBlocksPerCta = 32;        // 4-column blocks per CTA (128 scale columns)
 constexpr int kSwzThreads = 256;
-constexpr int kSwzPitchWords = 17;          // 16 words per staged row + 1 (bank spread)
+constexpr int kSwzPitchWords = kSwzBlocksPerCta + 1;   // words per staged row + 1 (bank spread)
 
 // GROUPED: the rows are E slices (offs, device); slice e is swizzled on its
 // own from block row sb[e] on (group.cuh), and block rows past the slices'
@@ -47,7 +48,7 @@ __global__ void __launch_bounds__(kSwzThreads)
     }
     const int cb0 = blockIdx.x * kSwzBlocksPerCta;
     const int c0 = cb0 * 4;
-    const int span = kSwzBlocksPerCta * 4;  // 64 scale columns
+    constexpr int span = kSwzBlocksPerCta * 4;   // 128 scale columns
     int row0 = rb * 128, row_end = rows;    // source rows of this block row: [row0, row_end)
     (void)E;
     if constexpr (GROUPED) {
@@ -68,17 +69,25 @@ __global__ void __launch_bounds__(kSwzThreads)
         // 16-byte loads (host-checked: 16-byte aligned base, cols % 16 == 0):
         // a 16-column segment of a row is then either wholly inside or wholly
         // past the matrix
-        for (int i = threadIdx.x; i < 128 * (span / 16); i += kSwzThreads) {
-            const int r = i >> 2, q = i & 3;
-            const int row = row0 + r, col = c0 + 16 * q;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        constexpr int kLoads = 128 * (span / 16) / kSwzThreads;   // 16-byte loads per thread
+        static_assert(kLoads * kSwzThreads == 128 * (span / 16), "whole loads per thread");
+        uint4 v[kLoads];
+#pragma unroll
+        for (int j = 0; j < kLoads; ++j) {       // all loads in flight before the first shared store
+            const int i = threadIdx.x + j * kSwzThreads;
+            const int row = row0 + i / (span / 16), col = c0 + 16 * (i % (span / 16));
+            v[j] = make_uint4(0u, 0u, 0u, 0u);
             if (row < row_end && col < cols)
-                v = __ldg(reinterpret_cast<const uint4 *>(in + (size_t)row * (size_t)cols + (size_t)col));
-            uint32_t *w = tile + r * kSwzPitchWords + 4 * q;
-            w[0] = v.x;
-            w[1] = v.y;
-            w[2] = v.z;
-            w[3] = v.w;
+                v[j] = __ldg(reinterpret_cast<const uint4 *>(in + (size_t)row * (size_t)cols + (size_t)col));
+        }
+#pragma unroll
+        for (int j = 0; j < kLoads; ++j) {
+            const int i = threadIdx.x + j * kSwzThreads;
+            uint32_t *w = tile + (i / (span / 16)) * kSwzPitchWords + 4 * (i % (span / 16));
+            w[0] = v[j].x;
+            w[1] = v[j].y;
+            w[2] = v[j].z;
+            w[3] = v[j].w;
         }
     } else {
         for (int i = threadIdx.x; i < 128 * span; i += kSwzThreads) {
