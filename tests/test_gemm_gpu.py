@@ -145,6 +145,25 @@ def test_swizzle_two_operands_bit_exact(dev, M, N, K):
     assert (h[wa.size: wa.size + 256] == 0xAB).all() and (h[wa.size + 256 + wb.size:] == 0xAB).all()
 
 
+def test_swizzle_two_operands_past_grid_limit(dev):
+    """ceil(M/128) + ceil(N/128) = 65536 block rows exceed one launch's grid
+    rows: the two operands then take a launch each, with the same result.
+    K = 16 keeps it small (8 MiB of scales, 32 MiB swizzled)."""
+    M, N, K = 65535 * 128, 128, 16
+    rng = np.random.default_rng(5)
+    sa = rng.integers(0, 256, (M, 1)).astype(np.uint8)
+    sb = rng.integers(0, 256, (N, 1)).astype(np.uint8)
+    o = oracle.get()
+    wa, wb = o.swizzle_scales(sa, K), o.swizzle_scales(sb, K)
+    oa = torch.full((wa.size,), 0xAB, dtype=torch.uint8, device=dev)
+    ob = torch.full((wb.size,), 0xAB, dtype=torch.uint8, device=dev)
+    bsg.nvfp4_swizzle_scales2(M, N, K, torch.from_numpy(sa).to(dev), oa, torch.from_numpy(sb).to(dev), ob)
+    assert bsg.bsg_last_launch_count() == 2
+    torch.cuda.synchronize()
+    assert np.array_equal(oa.cpu().numpy(), wa)
+    assert np.array_equal(ob.cpu().numpy(), wb)
+
+
 @pytest.mark.parametrize("offset", [1, 4, 8])
 def test_swizzle_unaligned_input(dev, offset):
     """Row-major scales that start off a 16-byte boundary (a sliced buffer):
