@@ -20,7 +20,7 @@ __all__ = [
     "nvfp4_grouped_gemm", "nvfp4_swizzle_scales_grouped", "nvfp4_grouped_scale_bytes", "nvfp4_dense_gemm",
     "nvfp4_dense_f16_gemm", "nvfp4_dense_grouped_gemm", "nvfp4_dense_f16_grouped_gemm",
     "nvfp4_dense_kgrouped_gemm", "nvfp4_dense_f16_kgrouped_gemm",
-    "nvfp4_swizzle_scales2", "nvfp4_quantize_tiles", "nvfp4_pack_operand", "nvfp4_packed_operand_bytes", "nvfp4_gemm_packed",
+    "nvfp4_swizzle_scales2", "nvfp4_quantize_tiles", "nvfp4_pack_operand", "nvfp4_packed_operand_bytes", "nvfp4_gemm_packed", "nvfp4_gemm_packed_ex",
     "bsg_reserve_workspace", "bsg_get_device_status",
     "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_set_pdl", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_measure_ingress",
@@ -52,6 +52,7 @@ _SIGNATURES = {
     "nvfp4_packed_operand_bytes": (ctypes.c_size_t, [_i, _i]),
     "nvfp4_pack_operand": (_i, [_i, _i, _vp, _vp, _vp]),
     "nvfp4_gemm_packed": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
+    "nvfp4_gemm_packed_ex": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i, _vp, _vp]),
     "nvfp4_swizzle_scales": (_i, [_i, _i, _vp, _vp, _vp]),
     "nvfp4_swizzle_scales2": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_swizzled_scale_bytes": (ctypes.c_size_t, [_i, _i]),
@@ -165,6 +166,14 @@ def nvfp4_gemm_packed(M, N, K, A_packed, sfA_swz, B_packed, sfB_swz, alpha, D, s
     """As nvfp4_gemm_swizzled, with A and B in the tile-packed layout."""
     _check(load().nvfp4_gemm_packed(M, N, K, _ptr(A_packed), _ptr(sfA_swz), _ptr(B_packed), _ptr(sfB_swz),
                                     float(alpha), _ptr(D), _stream(stream)), "nvfp4_gemm_packed")
+
+
+def nvfp4_gemm_packed_ex(M, N, K, A_packed, sfA_swz, B_packed, sfB_swz, alpha, bias, gamma, scatter, m_out, D,
+                         stream=None) -> None:
+    """As nvfp4_gemm_packed, with the epilogue variants of nvfp4_gemm_ex."""
+    _check(load().nvfp4_gemm_packed_ex(M, N, K, _ptr(A_packed), _ptr(sfA_swz), _ptr(B_packed), _ptr(sfB_swz),
+                                       float(alpha), _ptr(bias), _ptr(gamma), _ptr(scatter), int(m_out), _ptr(D),
+                                       _stream(stream)), "nvfp4_gemm_packed_ex")
 
 
 def nvfp4_swizzle_scales(rows, K, sf, sf_swz, stream=None) -> None:

@@ -759,20 +759,33 @@ int nvfp4_pack_operand(int rows, int K, const void *X, void *out, bsg_stream_t s
     return BSG_OK;
 }
 
-int nvfp4_gemm_packed(int M, int N, int K, const void *A_packed, const void *sfA_swz, const void *B_packed,
-                      const void *sfB_swz, float alpha, void *D, bsg_stream_t stream)
+int nvfp4_gemm_packed_ex(int M, int N, int K, const void *A_packed, const void *sfA_swz, const void *B_packed,
+                         const void *sfB_swz, float alpha, const float *bias, const float *gamma,
+                         const int32_t *scatter, int m_out, void *D, bsg_stream_t stream)
 {
     t_last_launches = 0;
     int rc = check_nvfp4_args(M, N, K, A_packed, sfA_swz, B_packed, sfB_swz, D);
-    if (rc != BSG_OK)
+    if (rc != BSG_OK || (rc = check_epilogue_args(M, bias, gamma, scatter, m_out)) != BSG_OK)
         return rc;
     DeviceState *ds = nullptr;
     if ((rc = current_device(&ds)) != BSG_OK)
         return rc;
+    Epilogue e;
+    e.bias = bias;
+    e.gamma = gamma;
+    e.scatter = scatter;
+    e.m_out = m_out;
     return run_gemm(Kind::NVFP4, M, N, K, nullptr, nullptr, static_cast<const uint8_t *>(sfA_swz),
                     static_cast<const uint8_t *>(sfB_swz), nullptr, nullptr, alpha, D,
-                    reinterpret_cast<cudaStream_t>(stream), ds, Epilogue(), false,
-                    static_cast<const uint8_t *>(A_packed), static_cast<const uint8_t *>(B_packed));
+                    reinterpret_cast<cudaStream_t>(stream), ds, e, false, static_cast<const uint8_t *>(A_packed),
+                    static_cast<const uint8_t *>(B_packed));
+}
+
+int nvfp4_gemm_packed(int M, int N, int K, const void *A_packed, const void *sfA_swz, const void *B_packed,
+                      const void *sfB_swz, float alpha, void *D, bsg_stream_t stream)
+{
+    return nvfp4_gemm_packed_ex(M, N, K, A_packed, sfA_swz, B_packed, sfB_swz, alpha, nullptr, nullptr, nullptr, M,
+                                D, stream);
 }
 
 static int quantize(bool tiles, int rows, int K, const void *X, void *packed, void *sf_swz, void *sf_rowmajor,

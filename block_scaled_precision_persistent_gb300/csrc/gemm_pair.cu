@@ -660,9 +660,8 @@ static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, 
                                     cudaStream_t stream)
 {
     using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>;
-    // the packed form runs the plain epilogue only
-    auto kern = (!PACKED && has_epilogue(args)) ? gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, !PACKED, PACKED>
-                                                : gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, false, PACKED>;
+    auto kern = has_epilogue(args) ? gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, true, PACKED>
+                                   : gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, false, PACKED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_BYTES);
     if (e != cudaSuccess)

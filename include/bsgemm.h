@@ -118,6 +118,9 @@ BSG_API int nvfp4_gemm_swizzled(int M, int N, int K,
  *   forced plan does not apply; that plan cannot be forced on the other
  *   entries). Same size and alignment rules and result as
  *   nvfp4_gemm_swizzled; allocates nothing.
+ * nvfp4_gemm_packed_ex: the same with the epilogue variants of
+ *   nvfp4_gemm_ex (bias, gamma, scatter, m_out: same meaning, layouts and
+ *   checks).
  * ------------------------------------------------------------------------- */
 BSG_API size_t nvfp4_packed_operand_bytes(int rows, int K);
 BSG_API int nvfp4_pack_operand(int rows, int K, const void *X, void *out, bsg_stream_t stream);
@@ -125,6 +128,11 @@ BSG_API int nvfp4_gemm_packed(int M, int N, int K,
                       const void *A_packed, const void *sfA_swz,
                       const void *B_packed, const void *sfB_swz,
                       float alpha, void *D, bsg_stream_t stream);
+BSG_API int nvfp4_gemm_packed_ex(int M, int N, int K,
+                         const void *A_packed, const void *sfA_swz,
+                         const void *B_packed, const void *sfB_swz, float alpha,
+                         const float *bias, const float *gamma, const int32_t *scatter,
+                         int m_out, void *D, bsg_stream_t stream);
 
 /* Scale-layout prep: row-major uint8[rows][K/16] -> the tcgen05 block-scale
  * layout: rows padded to a multiple of 128, K/16 padded to a multiple of 4,

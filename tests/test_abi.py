@@ -297,6 +297,10 @@ def test_packed_operand_bytes_and_bad_args(lib):
         assert g(M, N, K, BAD, BAD, BAD, BAD, 1.0, BAD, None) == bsg.BSG_ERR_INVALID_ARG
     assert g(8, 8, 256, None, BAD, BAD, BAD, 1.0, BAD, None) == bsg.BSG_ERR_INVALID_ARG
     assert g(8, 8, 256, BAD, BAD, BAD + 8, BAD, 1.0, BAD, None) == bsg.BSG_ERR_MISALIGNED
+    ge = lib.nvfp4_gemm_packed_ex
+    assert ge(8, 8, 256, BAD, BAD, BAD, BAD, 1.0, None, None, None, 9, BAD, None) == bsg.BSG_ERR_INVALID_ARG
+    assert ge(8, 8, 256, BAD, BAD, BAD, BAD, 1.0, BAD + 4, None, None, 8, BAD, None) == bsg.BSG_ERR_MISALIGNED
+    assert ge(8, 8, 256, BAD, BAD, BAD, BAD, 1.0, None, None, BAD, 0, BAD, None) == bsg.BSG_ERR_INVALID_ARG
 
 
 def test_packed_plan_is_listed_but_not_forceable(lib):

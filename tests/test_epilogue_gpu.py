@@ -254,3 +254,28 @@ def test_full_size_all_variants_sampled(dev):
     crow = list(range(0, M, 97))
     _, T, ref = oracle_ref("nvfp4", cpu, e["bias"], e["gamma"], rows=crow, cols=cols)
     assert oracle.within_tolerance(Dh[np.ix_(dst[crow], cols)], ref, T).all(), "sampled cols"
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("M,N,K", [(300, 392, 768), (130, 120, 1280)])
+def test_packed_plan_epilogue(dev, variant, M, N, K):
+    """The tile-packed plan (nvfp4_gemm_packed_ex) with each epilogue variant;
+    130 x 120 leaves the peer CTA's row blocks of A and B past M and N."""
+    p = nvfp4_problem(M, N, K)
+    bias, gamma, scatter, m_out = variant_inputs(variant, M, N, seed=M + N, bias_std=out_std(K))
+    flat = torch.full((m_out * N + GUARD,), SENTINEL, dtype=torch.int16, device=dev)
+    D = flat[: m_out * N].view(torch.bfloat16).view(m_out, N)
+    dv = lambda t: None if t is None else t.to(dev)  # noqa: E731
+    sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    sb = torch.empty(bsg.nvfp4_swizzled_scale_bytes(N, K), dtype=torch.uint8, device=dev)
+    bsg.nvfp4_swizzle_scales2(M, N, K, p["sfA"].to(dev), sa, p["sfB"].to(dev), sb)
+    ap = torch.empty(bsg.nvfp4_packed_operand_bytes(M, K), dtype=torch.uint8, device=dev)
+    bp = torch.empty(bsg.nvfp4_packed_operand_bytes(N, K), dtype=torch.uint8, device=dev)
+    bsg.nvfp4_pack_operand(M, K, p["A"].to(dev), ap)
+    bsg.nvfp4_pack_operand(N, K, p["B"].to(dev), bp)
+    bsg.nvfp4_gemm_packed_ex(M, N, K, ap, sa, bp, sb, p["alpha"], dv(bias), dv(gamma), dv(scatter), m_out, D)
+    assert bsg.bsg_last_plan_name() == "nvfp4_tc2_256x256_s5_acc1_packed"
+    torch.cuda.synchronize()
+    assert bsg.bsg_get_device_status() == bsg.BSG_OK
+    assert (bits(flat[-GUARD:]) == SENTINEL).all(), "kernel wrote past the end of D"
+    check(bits(D), "nvfp4", p, bias, gamma, scatter, m_out, f"packed {variant} {M}x{N}x{K}")
