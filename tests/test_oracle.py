@@ -799,12 +799,9 @@ def test_planted_mistake_is_caught(mutant):
     assert failed, f"no pin caught the planted mistake {mutant}"
 
 
-def test_pack_operand_tiles_layout():
-    """The tile-packed operand layout against hand-computed offsets and an
-    independent restatement by reshapes; padding rows are zero."""
-    rows, K = 200, 768                      # two row blocks (one ragged), three k-blocks
-    X = np.random.default_rng(17).integers(0, 256, (rows, K // 2)).astype(np.uint8)
-    got = oracle.pack_operand_tiles(X, K)
+def _check_pack_layout(got, X, K):
+    """Pins of the tile-packed layout for X uint8[200, K/2], K = 768."""
+    rows = X.shape[0]
     assert got.size == oracle.packed_operand_bytes(rows, K) == 256 * 384
     # byte (130, 300): row block 1, row 2 of it; k-block 2, byte 44 = chunk 2, 12 in;
     # chunk 2 XOR row 2 = 0: offset ((1 * 3 + 2) * 128 + 2) * 128 + 0 * 16 + 12
@@ -822,6 +819,38 @@ def test_pack_operand_tiles_layout():
     want = sw.transpose(0, 2, 1, 3, 4).reshape(-1)
     assert np.array_equal(got, want)
     assert not got[(1 * 3 + 0) * 16384 + 72 * 128:(1 * 3 + 1) * 16384].any()   # rows 200.. of tile (1, 0)
+
+
+PACK_X = np.random.default_rng(17).integers(0, 256, (200, 384)).astype(np.uint8)
+
+
+def test_pack_operand_tiles_layout():
+    """The tile-packed operand layout against hand-computed offsets and an
+    independent restatement by reshapes; padding rows are zero."""
+    _check_pack_layout(oracle.pack_operand_tiles(PACK_X, 768), PACK_X, 768)
+
+
+def _pack_mutant(X, K, kind):
+    """A plausible wrong tile layout, written out as the oracle's is."""
+    rows, width = X.shape
+    kblocks, rblocks = K // 256, -(-rows // 128)
+    out = np.zeros(rblocks * 128 * width, np.uint8)
+    for r in range(rows):
+        rb, rr = divmod(r, 128)
+        for c in range(width):
+            kb, cc = divmod(c, 128)
+            chunk = cc // 16 if kind == "no_swizzle" else (cc // 16) ^ (rr % 8)
+            tile = kb * rblocks + rb if kind == "k_major_tiles" else rb * kblocks + kb
+            out[(tile * 128 + rr) * 128 + chunk * 16 + cc % 16] = X[r, c]
+    if kind == "padding_not_zero":
+        out[(1 * kblocks) * 16384 + 100 * 128] = 1
+    return out
+
+
+@pytest.mark.parametrize("kind", ["no_swizzle", "k_major_tiles", "padding_not_zero"])
+def test_pack_layout_pins_catch_planted_mistakes(kind):
+    with pytest.raises(AssertionError):
+        _check_pack_layout(_pack_mutant(PACK_X, 768, kind), PACK_X, 768)
 
 
 def test_tolerance_helper():
