@@ -1,9 +1,9 @@
 """Benchmark of the block-scaled GEMM hot path on GB300.
 
 One step = the whole hot path on one NVFP4 problem: the scale-layout prep of
-both operands' row-major scales, then the persistent block-scaled GEMM
-(nvfp4_swizzle_scales x2 + nvfp4_gemm_swizzled, the same work as one
-nvfp4_gemm call). Default workload: M = N = K = 16384 (the pages' square
+both operands' row-major scales (one launch), then the persistent
+block-scaled GEMM (nvfp4_swizzle_scales2 + nvfp4_gemm_swizzled, the same work
+as one nvfp4_gemm call). Default workload: M = N = K = 16384 (the pages' square
 sweep shape), inputs resident in HBM, larger than L2.
 
 Prints ONE JSON line (rank 0). Besides the contract's keys it carries the
@@ -12,7 +12,8 @@ the timed region), the CPU oracle timed on a bounded sample, the clocks seen
 during the timed region, and secondary lines for the FP8 8192^3 GEMM, the
 skinny-M sweep (HBM GB/s), the scale swizzle, the NVFP4 quantiser, the
 fused epilogue variants (bias, gamma, scattered rows), the grouped (MoE)
-GEMM and the NVFP4 x dense-BF16 GEMM.
+GEMM, the NVFP4 x dense-BF16 / FP16 GEMM, and the GEMM from tile-packed
+operands against the same GEMM from row-major ones.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
