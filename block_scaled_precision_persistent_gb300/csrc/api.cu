@@ -321,8 +321,7 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     // A: 128 rows per CTA (dense: 32 bytes of codes per row and stage,
     // unswizzled, expanded in shared memory); B: the CTA's share of the
     // tile's N rows, 128 bytes per row and stage
-    // (multicast plans: each CTA loads 128 / mc of its rows for all pairs;
-    // tile-packed plans load A and B by bulk copies and read neither map,
+    // (tile-packed plans load A and B by bulk copies and read neither map,
     // which then repeat D's)
     if (packed) {
         if ((rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, d_rows(M, epi),
@@ -331,7 +330,7 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
         maps.a = maps.d;
         maps.b = maps.d;
     } else if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes,
-                        dense ? 32 : 128, (uint32_t)(128 / pi.mc),
+                        dense ? 32 : 128, 128u,
                         dense ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B)) != BSG_OK ||
         (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, b_row_bytes, (uint64_t)N, b_row_bytes,
                         128, (uint32_t)(pi.bn / pi.cta_group))) != BSG_OK ||
@@ -377,12 +376,12 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
     a.timeout_ns = g_watchdog_ns.load();
     set_epilogue(a, epi, D);
     a.pdl = g_pdl.load();
-    // scheduling units: a tile per CTA or pair, or mc adjacent N tiles per
-    // cluster of mc pairs; the grid is a whole number of clusters
-    const long long units = (long long)a.num_m_tiles * ((a.num_n_tiles + pi.mc - 1) / pi.mc);
-    const long long ctas = units * pi.cta_group * pi.mc;
+    // scheduling units: a tile per CTA or pair; the grid is a whole number
+    // of clusters
+    const long long units = (long long)a.num_m_tiles * a.num_n_tiles;
+    const long long ctas = units * pi.cta_group;
     const int resident = bsg::max_resident_ctas(plan, ds->sms);
-    if (resident < pi.cta_group * pi.mc)
+    if (resident < pi.cta_group)
         return BSG_ERR_CUDA;
     const int grid = (int)(ctas < resident ? ctas : resident);
     cudaError_t e = bsg::launch_gemm(plan, maps, a, grid, stream);
@@ -656,9 +655,22 @@ int max_resident_ctas(int id, int num_sms)
         return 0;
     std::lock_guard<std::mutex> lk(g_mu);
     if (cache[dev][j] == 0)
-        cache[dev][j] = 2 * pair_plan(j).mc * pair_max_clusters(j);
+        cache[dev][j] = 2 * pair_max_clusters(j);
     return cache[dev][j];
 }
+
+int validate_nvfp4_call(int M, int N, int K, const void *A, const void *sfA, const void *B, const void *sfB,
+                        void *D)
+{
+    t_last_launches = 0;
+    int rc = check_nvfp4_args(M, N, K, A, sfA, B, sfB, D);
+    if (rc != BSG_OK)
+        return rc;
+    DeviceState *ds = nullptr;
+    return current_device(&ds);
+}
+
+void add_launches(int n) { t_last_launches += n; }
 
 int find_plan(const char *name)
 {

@@ -86,7 +86,6 @@ struct PlanInfo {
     int smem_bytes;            // dynamic shared memory per CTA
     int threads;
     int tmem_cols;
-    int mc = 1;                // CTA pairs per cluster sharing A by multicast (pair plans)
     int packed = 0;            // 1: reads tile-packed operands (nvfp4_gemm_packed only)
 };
 
@@ -126,6 +125,14 @@ cudaError_t skinny_launch(int i, const GemmMaps &maps, const GemmArgs &args, int
 // Thread-block clusters of `splits` CTAs of skinny plan i that fit on the
 // device at once (0 if the query fails).
 int skinny_max_clusters(int i, int splits);
+
+// The checks nvfp4_gemm makes before it launches anything, in its order:
+// arguments, 16-byte alignment, then the current device (compute 10.3).
+// Resets the calling thread's launch count (bsg_last_launch_count).
+int validate_nvfp4_call(int M, int N, int K, const void *A, const void *sfA, const void *B, const void *sfB,
+                        void *D);
+// Adds n to the calling thread's launch count.
+void add_launches(int n);
 
 // Scale-layout prep kernel. Returns a cudaError_t.
 cudaError_t launch_swizzle_scales(int rows, int K, const uint8_t *sf, uint8_t *out,

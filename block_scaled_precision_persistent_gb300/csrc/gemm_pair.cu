@@ -29,25 +29,13 @@
 // barrier (TMA .cta_group::2); the leader's MMA thread issues the pair MMAs
 // and commits with multicast to both CTAs' empty / accumulator-full
 // barriers; both epilogues arrive on the leader's accumulator-empty barrier.
-//
-// Multicast of A (MC = 2; "Together AI Ports ThunderKittens GEMM Kernels to
-// NVIDIA Vera Rubin NVL72", introduction: loads shared across a cluster so
-// that each tile is fetched once for several consumers). A cluster of four
-// CTAs holds two pairs p = 0, 1 on the N tiles 2q and 2q + 1 of the same M
-// tile, so CTA r of either pair needs the same 128 rows of A. Each of the two
-// loads 64 of them and multicasts them to both (TMA .multicast::cluster with
-// .cta_group::2: each copy signals its destination pair's leader barrier),
-// which halves the A bytes each SM fetches from L2. A stage is then refilled
-// only after BOTH pairs' MMAs have read it: every MMA commit that frees a
-// stage goes to all four CTAs' empty barriers, which count two arrivals.
-// With MC = 1 each CTA fetches its own tiles.
 #include "bsg_internal.h"
 #include "gemm_common.cuh"
 #include "ptx.cuh"
 
 namespace bsg {
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC = 1, bool PACKED = false>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool PACKED = false>
 struct PairTile {
     static constexpr bool kFp4 = KIND == Kind::NVFP4;
     // NVFP4 activations x dense BF16 weights: each CTA expands its own 128
@@ -55,7 +43,7 @@ struct PairTile {
     // stage, with the warps that write NVFP4 scales in the other kind; the
     // leader's pair MMA (kind::f16) reads A from both CTAs' TMEM
     static constexpr bool kDense = KIND == Kind::NVFP4_BF16_TMEM;
-    static constexpr int CLUSTER = 2 * MC;                // CTAs per cluster (MC pairs sharing A)
+    static constexpr int CLUSTER = 2;                     // CTAs per cluster: one pair
     static constexpr int BM = 128;                        // rows per CTA
     static constexpr int TILE_M = 256;                    // rows per pair
     static constexpr int ROW_BYTES = 128;
@@ -117,8 +105,7 @@ struct PairTile {
     static constexpr uint32_t IDESC_F16 = idesc_f16(TILE_M, BN);   // dense kind with FP16 B
 
     static_assert(BN % 128 == 0 && BN <= 256, "pair tile N: B halves of 64 or 128 rows");
-    static_assert(MC == 1 || (MC == 2 && !kDense), "A multicast: two pairs, operands loaded by TMA");
-    static_assert(!PACKED || (kFp4 && MC == 1 && BN == 256 && A_BYTES == 16384 && B_BYTES == 16384),
+    static_assert(!PACKED || (kFp4 && BN == 256 && A_BYTES == 16384 && B_BYTES == 16384),
                   "tile-packed operands: NVFP4 256-wide pairs, one 16 KiB tile of A and of B per CTA and stage");
     static_assert(TMEM_USED <= 512, "TMEM: accumulators plus scales exceed 512 columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
@@ -126,20 +113,19 @@ struct PairTile {
 };
 
 // EPI: the epilogue-variant instantiation (bias, gamma, scattered rows).
-// MC: pairs per cluster sharing A by multicast (1 or 2).
 // PACKED: A and B arrive as tile-packed operands, one 16 KiB bulk copy per
 // CTA, tile and stage (a copy of contiguous bytes takes operands into an SM
 // faster than a tensor-map box of 128 rows); each CTA's copies complete on
 // its own barrier, and the peer's warp 1 relays their arrival to the leader.
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC, bool EPI, bool PACKED = false>
-__global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>::THREADS, 1)
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool EPI, bool PACKED = false>
+__global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD,
                      const __grid_constant__ CUtensorMap tmSFA,
                      const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args)
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>;
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -162,7 +148,6 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED
     const int lane = threadIdx.x & 31;
     const uint32_t crank = cluster_ctarank();
     const uint32_t rank = crank & 1u;           // within the pair: 0 leader, 1 peer
-    const uint32_t pidx = crank >> 1;           // pair within the cluster (MC = 2)
     const uint32_t lead = crank & ~1u;          // cluster rank of this pair's leader
     const bool leader = rank == 0;
     const Watchdog wd{args.status, args.timeout_ns};
@@ -173,7 +158,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED
             mbar_init(full0 + 8u * s, PACKED ? 2 : 1);
             if constexpr (PACKED)
                 mbar_init(pfull0 + 8u * s, 1);
-            mbar_init(empty0 + 8u * s, MC);   // one commit per pair that reads the stage
+            mbar_init(empty0 + 8u * s, 1);    // one commit of the pair's MMAs
         }
         for (int a = 0; a < NUM_ACC; ++a) {
             mbar_init(tfull0 + 8u * a, 1);
@@ -207,19 +192,13 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED
     if (threadIdx.x == 0)
         griddep_launch_dependents();
     const uint32_t tmem = *tmem_slot;
-    // a scheduling unit is MC adjacent N tiles of one M tile: pair p of the
-    // cluster takes N tile MC q + p (past the last N tile it computes zeros
-    // from zero-filled loads and stores nothing, but still shares its A)
-    const int num_q = (args.num_n_tiles + MC - 1) / MC;
-    const int num_tiles = args.num_m_tiles * num_q;
+    const int num_tiles = args.num_m_tiles * args.num_n_tiles;
     const int nkb = args.num_k_blocks;
     const bool b_f16 = args.b_f16 != 0;   // dense kind: B (and the expanded A) are FP16, not BF16
     const int cluster_id = blockIdx.x / T::CLUSTER;
     const int num_clusters = gridDim.x / T::CLUSTER;
     auto tile_coords = [&](int tile, int &pm, int &nt) {
-        int q;
-        raster_tile(tile, args.raster_group, args.num_m_tiles, num_q, pm, q);
-        nt = q * MC + (int)pidx;
+        raster_tile(tile, args.raster_group, args.num_m_tiles, args.num_n_tiles, pm, nt);
     };
 
     if (warp == 0) {
@@ -292,16 +271,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED
                     } else {
                         if (leader)
                             mbar_arrive_expect_tx(full0 + 8u * stage, 2u * (T::A_BYTES + T::B_BYTES));
-                        if constexpr (MC == 1) {
-                            tma_load_2d_pair(sa, &tmA, fb, kb * T::ROW_BYTES, pm * T::TILE_M + (int)rank * T::BM);
-                        } else {
-                            // rows [64 p, 64 p + 64) of this CTA's 128 A rows, into
-                            // the same offset of CTA r of both pairs
-                            constexpr int QR = T::BM / MC;
-                            tma_load_2d_pair_multicast(sa + pidx * (QR * T::ROW_BYTES), &tmA, fb, kb * T::ROW_BYTES,
-                                                       pm * T::TILE_M + (int)rank * T::BM + (int)pidx * QR,
-                                                       (uint16_t)((1u << rank) | (1u << (2u + rank))));
-                        }
+                        tma_load_2d_pair(sa, &tmA, fb, kb * T::ROW_BYTES, pm * T::TILE_M + (int)rank * T::BM);
                     }
                     if constexpr (!PACKED)
                         tma_load_2d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN + (int)rank * T::B_ROWS);
@@ -373,9 +343,8 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED
                                          desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                          (kb | j) != 0 ? 1u : 0u);
                     }
-                    // frees the stage in both CTAs (MC = 2: in all four, whose
-                    // A this pair's loads also filled)
-                    tc_commit_pair_multicast(empty0 + 8u * stage, MC == 1 ? 0x3 : 0xF);
+                    // frees the stage in both CTAs
+                    tc_commit_pair_multicast(empty0 + 8u * stage, 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -655,13 +624,13 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED
 // ---------------------------------------------------------------------------
 // Plans and launchers
 // ---------------------------------------------------------------------------
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC, bool PACKED = false>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool PACKED = false>
 static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, int grid,
                                     cudaStream_t stream)
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>;
-    auto kern = has_epilogue(args) ? gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, true, PACKED>
-                                   : gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, false, PACKED>;
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>;
+    auto kern = has_epilogue(args) ? gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, true, PACKED>
+                                   : gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, false, PACKED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_BYTES);
     if (e != cudaSuccess)
@@ -686,11 +655,11 @@ static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, 
     return cudaGetLastError();
 }
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC, bool PACKED = false>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool PACKED = false>
 static int pair_clusters_impl()
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>;
-    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, MC, false, PACKED>;   // the EPI instantiation has the same footprint
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>;
+    auto kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, false, PACKED>;   // the EPI instantiation has the same footprint
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) !=
         cudaSuccess)
         return 0;
@@ -713,33 +682,29 @@ static int pair_clusters_impl()
     return n;
 }
 
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, int MC, bool PACKED = false>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool PACKED = false>
 static constexpr PlanInfo make_pair_plan(const char *name)
 {
-    using T = PairTile<KIND, BN, STAGES, NUM_ACC, MC, PACKED>;
+    using T = PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>;
     // the TMEM-staged dense pair serves calls of kind NVFP4_BF16
     constexpr Kind kind = KIND == Kind::NVFP4_BF16_TMEM ? Kind::NVFP4_BF16 : KIND;
     return PlanInfo{name, kind, Family::PAIR, 2, T::TILE_M, BN, STAGES, NUM_ACC, T::K_BLOCK, T::SMEM_BYTES,
-                    T::THREADS, T::TMEM_COLS, MC, PACKED ? 1 : 0};
+                    T::THREADS, T::TMEM_COLS, PACKED ? 1 : 0};
 }
 
 // The first plan of each kind and shape is the planner's; the shallower
-// rings are there for the stage sweep, the "_mca" plans (two pairs per
-// cluster sharing A by multicast) for the multicast comparison
-// (bsg_force_plan).
+// rings are there for the stage sweep (bsg_force_plan).
 #define BSG_PAIR_PLANS(X)                                                    \
-    X(Kind::NVFP4, 256, 5, 1, 1, false, "nvfp4_tc2_256x256_s5_acc1")         \
-    X(Kind::NVFP4, 128, 6, 2, 1, false, "nvfp4_tc2_256x128_s6_acc2")         \
-    X(Kind::FP8, 256, 6, 2, 1, false, "fp8_tc2_256x256_s6_acc2")             \
-    X(Kind::NVFP4, 256, 4, 1, 1, false, "nvfp4_tc2_256x256_s4_acc1")         \
-    X(Kind::NVFP4, 256, 3, 1, 1, false, "nvfp4_tc2_256x256_s3_acc1")         \
-    X(Kind::FP8, 256, 4, 2, 1, false, "fp8_tc2_256x256_s4_acc2")             \
-    X(Kind::NVFP4_BF16_TMEM, 256, 8, 1, 1, false, "nvfp4bf16_tc2_256x256_s8_acc1_tmema") \
-    X(Kind::NVFP4, 256, 5, 1, 2, false, "nvfp4_tc2x2_256x256_s5_acc1_mca")   \
-    X(Kind::FP8, 256, 6, 2, 2, false, "fp8_tc2x2_256x256_s6_acc2_mca")       \
-    X(Kind::NVFP4, 256, 5, 1, 1, true, "nvfp4_tc2_256x256_s5_acc1_packed")
+    X(Kind::NVFP4, 256, 5, 1, false, "nvfp4_tc2_256x256_s5_acc1")         \
+    X(Kind::NVFP4, 128, 6, 2, false, "nvfp4_tc2_256x128_s6_acc2")         \
+    X(Kind::FP8, 256, 6, 2, false, "fp8_tc2_256x256_s6_acc2")             \
+    X(Kind::NVFP4, 256, 4, 1, false, "nvfp4_tc2_256x256_s4_acc1")         \
+    X(Kind::NVFP4, 256, 3, 1, false, "nvfp4_tc2_256x256_s3_acc1")         \
+    X(Kind::FP8, 256, 4, 2, false, "fp8_tc2_256x256_s4_acc2")             \
+    X(Kind::NVFP4_BF16_TMEM, 256, 8, 1, false, "nvfp4bf16_tc2_256x256_s8_acc1_tmema") \
+    X(Kind::NVFP4, 256, 5, 1, true, "nvfp4_tc2_256x256_s5_acc1_packed")
 
-#define BSG_PAIR_INFO(K, BN, S, A, MC, PK, NAME) make_pair_plan<K, BN, S, A, MC, PK>(NAME),
+#define BSG_PAIR_INFO(K, BN, S, A, PK, NAME) make_pair_plan<K, BN, S, A, PK>(NAME),
 static const PlanInfo kPairPlans[] = {BSG_PAIR_PLANS(BSG_PAIR_INFO)};
 #undef BSG_PAIR_INFO
 
@@ -751,9 +716,9 @@ cudaError_t pair_launch(int id, const GemmMaps &maps, const GemmArgs &args, int 
                         cudaStream_t stream)
 {
     int i = 0;
-#define BSG_PAIR_LAUNCH(K, BN, S, A, MC, PK, NAME)                              \
+#define BSG_PAIR_LAUNCH(K, BN, S, A, PK, NAME)                              \
     if (id == i)                                                               \
-        return pair_launch_impl<K, BN, S, A, MC, PK>(maps, args, grid, stream); \
+        return pair_launch_impl<K, BN, S, A, PK>(maps, args, grid, stream); \
     ++i;
     BSG_PAIR_PLANS(BSG_PAIR_LAUNCH)
 #undef BSG_PAIR_LAUNCH
@@ -763,9 +728,9 @@ cudaError_t pair_launch(int id, const GemmMaps &maps, const GemmArgs &args, int 
 int pair_max_clusters(int id)
 {
     int i = 0;
-#define BSG_PAIR_OCC(K, BN, S, A, MC, PK, NAME)            \
+#define BSG_PAIR_OCC(K, BN, S, A, PK, NAME)            \
     if (id == i)                                          \
-        return pair_clusters_impl<K, BN, S, A, MC, PK>();  \
+        return pair_clusters_impl<K, BN, S, A, PK>();  \
     ++i;
     BSG_PAIR_PLANS(BSG_PAIR_OCC)
 #undef BSG_PAIR_OCC

@@ -482,20 +482,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// As tma_load_2d_pair, multicast: the tile lands at the same offset in every
-// CTA of cta_mask, and each copy's completion is signalled on the barrier at
-// bar_cluster's offset in that destination's pair leader (bar_cluster is the
-// issuing CTA's pair-leader barrier: its pair bit selects the leader).
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap *map,
-                                                           uint32_t bar_cluster, int x, int y, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
 // TMEM allocation for a CTA pair: one warp of EACH CTA executes these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
 {

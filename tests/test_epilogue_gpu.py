@@ -32,11 +32,10 @@ SENTINEL = 0x7FC1          # a NaN pattern no computed output can have
 GUARD = 256
 
 NVFP4_PLANS = ["nvfp4_tc1_128x256_s3_acc1", "nvfp4_tc1_128x128_s5_acc2",
-               "nvfp4_tc2_256x256_s5_acc1", "nvfp4_tc2_256x128_s6_acc2", "nvfp4_tc2x2_256x256_s5_acc1_mca"]
+               "nvfp4_tc2_256x256_s5_acc1", "nvfp4_tc2_256x128_s6_acc2"]
 SKINNY_PLANS = {"nvfp4_skinny_m64_s3": 64, "nvfp4_skinny_m64_s6": 64, "nvfp4_skinny_m128_s3": 128,
                 "nvfp4_skinny_m256_s4": 256}
-FP8_PLANS = ["fp8_tc1_128x256_s4_acc2", "fp8_tc1_128x128_s6_acc2", "fp8_tc2_256x256_s6_acc2",
-             "fp8_tc2x2_256x256_s6_acc2_mca"]
+FP8_PLANS = ["fp8_tc1_128x256_s4_acc2", "fp8_tc1_128x128_s6_acc2", "fp8_tc2_256x256_s6_acc2"]
 VARIANTS = ["bias", "gamma", "bias_gamma", "scatter", "all", "all_drop"]
 
 

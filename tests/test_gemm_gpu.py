@@ -89,9 +89,8 @@ def oracle_nvfp4(p, rows=None, cols=None):
 
 
 NVFP4_PLANS = ["nvfp4_tc1_128x256_s3_acc1", "nvfp4_tc1_128x128_s5_acc2",
-               "nvfp4_tc2_256x256_s5_acc1", "nvfp4_tc2_256x128_s6_acc2", "nvfp4_tc2x2_256x256_s5_acc1_mca"]
-FP8_PLANS = ["fp8_tc1_128x256_s4_acc2", "fp8_tc1_128x128_s6_acc2", "fp8_tc2_256x256_s6_acc2",
-             "fp8_tc2x2_256x256_s6_acc2_mca"]
+               "nvfp4_tc2_256x256_s5_acc1", "nvfp4_tc2_256x128_s6_acc2"]
+FP8_PLANS = ["fp8_tc1_128x256_s4_acc2", "fp8_tc1_128x128_s6_acc2", "fp8_tc2_256x256_s6_acc2"]
 
 
 @pytest.fixture(params=[None] + NVFP4_PLANS, ids=["auto"] + NVFP4_PLANS)
