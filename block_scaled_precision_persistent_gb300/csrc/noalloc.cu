@@ -58,21 +58,26 @@ extern "C" int nvfp4_gemm_noalloc(int M, int N, int K, const void *A, const void
                                   const void *B, const void *sfB, float alpha, void *D,
                                   bsg_stream_t stream)
 {
-    if (!A || !sfA || !B || !sfB || !D)
-        return BSG_ERR_INVALID_ARG;
-    if (M < 1 || N < 1 || K < 256 || (K % 256) != 0 || (N % 8) != 0)
-        return BSG_ERR_INVALID_ARG;
+    // the same checks as nvfp4_gemm, before anything touches the scratch
+    // array or launches: a bad call returns the same status and runs nothing
+    int rc = bsg::validate_nvfp4_call(M, N, K, A, sfA, B, sfB, D);
+    if (rc != BSG_OK)
+        return rc;
     const size_t bytes_a = round_up_256(nvfp4_swizzled_scale_bytes(M, K));
     const size_t bytes_b = round_up_256(nvfp4_swizzled_scale_bytes(N, K));
     if (bytes_a + bytes_b > kNoallocScratchBytes)
         return BSG_ERR_EXCEEDS_SCRATCH;
     uint8_t *scratch = nullptr;
-    int rc = scratch_on_current_device(&scratch);
-    if (rc != BSG_OK)
+    if ((rc = scratch_on_current_device(&scratch)) != BSG_OK)
         return rc;
     // Every byte of both swizzled regions (padding included) is rewritten by
     // the swizzle, so the previous call's contents never leak into this one.
-    if ((rc = nvfp4_swizzle_scales2(M, N, K, sfA, scratch, sfB, scratch + bytes_a, stream)) != BSG_OK)
-        return rc;
-    return nvfp4_gemm_swizzled(M, N, K, A, scratch, B, scratch + bytes_a, alpha, D, stream);
+    // Both regions fit the scratch, so their block rows fit one launch's grid.
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bsg::launch_swizzle_scales2(M, N, K, static_cast<const uint8_t *>(sfA), scratch,
+                                    static_cast<const uint8_t *>(sfB), scratch + bytes_a, s) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    rc = nvfp4_gemm_swizzled(M, N, K, A, scratch, B, scratch + bytes_a, alpha, D, stream);
+    bsg::add_launches(1);   // the swizzle, after the GEMM's own count was set
+    return rc;
 }

@@ -192,7 +192,8 @@ BSG_API int nvfp4_quantize_tiles(int rows, int K, const void *X, void *packed_ti
  * cudaMalloc -- for instance a runtime that has handed all device memory to
  * its own pool allocator, or code running where a device allocation is not
  * allowed (a host callback, a loop with a no-allocation rule).
- *   Arguments, layouts and result are those of nvfp4_gemm.
+ *   Arguments, layouts, result and error codes are those of nvfp4_gemm,
+ *   checked in the same order before anything is launched or written.
  *   Scratch: the swizzled scales of A and B go to one file-scope device
  *   array of BSG_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads
  *   the library holds until the process exits. A call needs
@@ -207,7 +208,7 @@ BSG_API int nvfp4_quantize_tiles(int rows, int K, const void *X, void *packed_ti
  *   contents. Each call rewrites every byte it reads, so nothing needs
  *   clearing, but calls whose work overlaps on the GPU (different streams)
  *   race on the array and must be serialised by the caller.
- *   bsg_last_launch_count() afterwards reports the final GEMM launch only. */
+ *   bsg_last_launch_count() afterwards counts the swizzle and the GEMM.    */
 BSG_API int nvfp4_gemm_noalloc(int M, int N, int K,
                                const void *A, const void *sfA,
                                const void *B, const void *sfB,
