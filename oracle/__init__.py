@@ -104,6 +104,13 @@ class Oracle:
         L.bso_grouped_scale_bytes.argtypes = [ctypes.c_int] * 3
         L.bso_swizzle_scales_grouped.restype = ctypes.c_int
         L.bso_swizzle_scales_grouped.argtypes = [ctypes.c_int] * 3 + [i32p, u8p, u8p]
+        i8p = ctypes.POINTER(ctypes.c_int8)
+        L.bso_nvfp4_freivalds.restype = ctypes.c_int
+        L.bso_nvfp4_freivalds.argtypes = [ctypes.c_int] * 3 + [u8p] * 4 + [ctypes.c_float, i8p, ctypes.c_int] + [
+            f64p] * 4 + [ctypes.c_int]
+        L.bso_fp8_freivalds.restype = ctypes.c_int
+        L.bso_fp8_freivalds.argtypes = [ctypes.c_int] * 3 + [u8p] * 2 + [ctypes.c_float] * 3 + [
+            i8p, ctypes.c_int] + [f64p] * 4 + [ctypes.c_int]
         L.bso_nvfp4_quantize.restype = ctypes.c_int
         L.bso_nvfp4_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_uint16),
                                          u8p, u8p, ctypes.POINTER(ctypes.c_float),
@@ -335,6 +342,53 @@ class Oracle:
                                                      b_f16=b_f16)
         return S, T, D
 
+    # -- Freivalds' check of a whole product --------------------------------
+    def _freivalds_out(self, M, x):
+        x = np.ascontiguousarray(x, dtype=np.int8)
+        nv = x.shape[0]
+        return x, nv, np.empty((nv, M)), np.empty((nv, M)), np.empty(M), np.empty(M)
+
+    def nvfp4_freivalds(self, A, sfA, B, sfB, alpha, K, x, nthreads=None):
+        """Right-hand side of Freivalds' check for the NVFP4 GEMM, for the
+        int8 vectors x[nv, N]: a dict with y = alpha Adeq (Bdeq^T x_q) and
+        its rounding bound g (both [nv, M]), tsum[i] = sum_j T[i][j] and
+        t2[i] >= sum_j T[i][j]^2 ([M]); see bso_nvfp4_freivalds."""
+        A = np.ascontiguousarray(A, dtype=np.uint8)
+        B = np.ascontiguousarray(B, dtype=np.uint8)
+        sfA = np.ascontiguousarray(sfA, dtype=np.uint8)
+        sfB = np.ascontiguousarray(sfB, dtype=np.uint8)
+        M, N = A.shape[0], B.shape[0]
+        assert A.shape == (M, K // 2) and B.shape == (N, K // 2)
+        assert sfA.shape == (M, K // 16) and sfB.shape == (N, K // 16)
+        x, nv, y, g, tsum, t2 = self._freivalds_out(M, x)
+        assert x.shape == (nv, N)
+        rc = self.lib.bso_nvfp4_freivalds(M, N, K, self._p(A, ctypes.c_uint8), self._p(sfA, ctypes.c_uint8),
+                                          self._p(B, ctypes.c_uint8), self._p(sfB, ctypes.c_uint8), float(alpha),
+                                          self._p(x, ctypes.c_int8), nv, self._p(y, ctypes.c_double),
+                                          self._p(g, ctypes.c_double), self._p(tsum, ctypes.c_double),
+                                          self._p(t2, ctypes.c_double), nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"bso_nvfp4_freivalds failed (rc={rc})")
+        return dict(y=y, g=g, tsum=tsum, t2=t2, K=K)
+
+    def fp8_freivalds(self, A, B, alpha, x, sA=1.0, sB=1.0, nthreads=None):
+        """As nvfp4_freivalds, for the FP8 GEMM (A uint8[M, K], B uint8[N, K])."""
+        A = np.ascontiguousarray(A, dtype=np.uint8)
+        B = np.ascontiguousarray(B, dtype=np.uint8)
+        M, K = A.shape
+        N = B.shape[0]
+        assert B.shape == (N, K)
+        x, nv, y, g, tsum, t2 = self._freivalds_out(M, x)
+        assert x.shape == (nv, N)
+        rc = self.lib.bso_fp8_freivalds(M, N, K, self._p(A, ctypes.c_uint8), self._p(B, ctypes.c_uint8),
+                                        float(alpha), float(sA), float(sB), self._p(x, ctypes.c_int8), nv,
+                                        self._p(y, ctypes.c_double), self._p(g, ctypes.c_double),
+                                        self._p(tsum, ctypes.c_double), self._p(t2, ctypes.c_double),
+                                        nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"bso_fp8_freivalds failed (rc={rc})")
+        return dict(y=y, g=g, tsum=tsum, t2=t2, K=K)
+
     def grouped_scale_bytes(self, E: int, M: int, K: int) -> int:
         return int(self.lib.bso_grouped_scale_bytes(E, M, K))
 
@@ -463,3 +517,102 @@ def within_tolerance(d_gpu_bits, d_ref_bits, T) -> np.ndarray:
         ok = np.abs(g - r) <= REL_TOL * np.abs(r) + ABS_TOL * np.asarray(T, np.float64)
     both_inf = np.isinf(g) & np.isinf(r) & (np.sign(g) == np.sign(r))
     return (ok | both_inf) & ~np.isnan(g) & ~np.isnan(r)
+
+
+# -- Freivalds' check: the decision ------------------------------------------
+#
+# R. Freivalds (1977): D x = alpha Adeq (Bdeq^T x) for a correct D and any x.
+# The oracle computes the right-hand side y exactly up to one double dot
+# product's rounding (Oracle.nvfp4_freivalds / fp8_freivalds); here the left
+# side z = D_gpu x is formed from the GPU's BF16 bits and r = z - y is
+# compared with what the element-wise tolerance allows.
+#
+# Per element, D_gpu may differ from the exact value S by
+#     |e_ij| <= c1 |D_gpu_ij| + c2 T_ij,
+# with rho = 2^-7 + 2^-8 / (1 - 2^-8) (the tolerance against the rounded
+# D_ref plus D_ref's own BF16 rounding of S), c1 = rho / (1 - 2^-7) and
+# c2 = 2^-20 (1 + c1): D_ref is bounded through D_gpu, which is known.
+#
+# Two bounds on |r_i| are checked, both must hold:
+#   * summed (deterministic): sum_j (c1 |D_ij| + c2 T_ij) |x_j| -- what the
+#     element-wise tolerance allows in the worst case; it can never fail for a
+#     result that is within tolerance everywhere.
+#   * Hoeffding (probabilistic): x has independent +-1 entries drawn
+#     independently of D, so P(|sum_j e_ij x_j| >= C s_i) <= 2 exp(-C^2 / 2)
+#     with s_i^2 = sum_j e_ij^2 <= (c1 sqrt(sum_j D_ij^2) + c2 sqrt(t2_i))^2
+#     (Minkowski). With C = 9 a result within tolerance fails one row test with
+#     probability below 5e-18, below 1e-12 over all rows and vectors of a
+#     16384^3 check. It catches far smaller errors than the summed bound:
+#     wrong or missing tiles, rows, columns, scale blocks, K blocks.
+# Both also allow the double rounding of y (gamma_{K+1} g) and of z
+# (gamma_N sum_j |D_ij|), and BF16's subnormal spacing (2^-133 per term).
+
+FREIVALDS_C = 9.0
+_U = 2.0 ** -53
+_RHO = REL_TOL + 2.0 ** -8 / (1.0 - 2.0 ** -8)
+_C1 = _RHO / (1.0 - REL_TOL)
+_C2 = ABS_TOL * (1.0 + _C1)
+
+
+def rademacher(nv: int, n: int, seed: int) -> np.ndarray:
+    """nv vectors of n independent +-1 entries (int8), seeded (PCG64)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return (rng.integers(0, 2, size=(nv, n), dtype=np.int8) * 2 - 1).astype(np.int8)
+
+
+def bf16_times_vectors(d_bits, x, chunk_rows: int = 1024):
+    """z = D x in double for BF16 D (uint16 bits [M, N]) and x [nv, N], and
+    the row sums the bounds need: returns (z [nv, M], abs_sum [M] =
+    sum_j |D_ij|, sq_sum [M] = sum_j D_ij^2, nonfinite [M] = count of Inf /
+    NaN in the row, which are left out of the other three). Chunked over rows."""
+    d_bits = np.asarray(d_bits, dtype=np.uint16)
+    M, N = d_bits.shape
+    xv = np.asarray(x, dtype=np.float64)
+    assert xv.shape[1] == N
+    z = np.empty((xv.shape[0], M))
+    abs_sum = np.empty(M)
+    sq_sum = np.empty(M)
+    nonfinite = np.empty(M, np.int64)
+    for r0 in range(0, M, chunk_rows):
+        d = bf16_bits_to_float(d_bits[r0:r0 + chunk_rows])
+        bad = ~np.isfinite(d)
+        nonfinite[r0:r0 + d.shape[0]] = bad.sum(axis=1)
+        d[bad] = 0.0
+        z[:, r0:r0 + d.shape[0]] = (d @ xv.T).T
+        a = np.abs(d)
+        abs_sum[r0:r0 + d.shape[0]] = a.sum(axis=1)
+        sq_sum[r0:r0 + d.shape[0]] = (a * a).sum(axis=1)
+    return z, abs_sum, sq_sum, nonfinite
+
+
+def freivalds_verdict(d_bits, x, rhs) -> dict:
+    """Decide Freivalds' check of the GPU result d_bits (BF16 bits [M, N])
+    against the oracle's right-hand side rhs (from nvfp4_freivalds /
+    fp8_freivalds with the same x). Returns a dict with 'ok' (both bounds
+    hold everywhere and every element is finite), 'ok_summed', 'ok_hoeffding',
+    the worst ratios |r| / bound of each, and the failing (vector, row) pairs
+    of the Hoeffding bound (up to 16)."""
+    x = np.asarray(x, dtype=np.int8)
+    M, N = np.asarray(d_bits).shape
+    if not np.all(np.abs(x.astype(np.int16)) == 1):
+        raise ValueError("Freivalds vectors must hold +-1 entries only")
+    z, abs_sum, sq_sum, nonfinite = bf16_times_vectors(d_bits, x)
+    y, g, tsum, t2, K = rhs["y"], rhs["g"], rhs["tsum"], rhs["t2"], rhs["K"]
+    gam_n = N * _U / (1.0 - N * _U)
+    gam_k = (K + 2) * _U / (1.0 - (K + 2) * _U)
+    r = np.abs(z - y)
+    rounding = gam_n * abs_sum[None, :] + gam_k * g + N * 2.0 ** -133
+    summed = _C1 * abs_sum + _C2 * tsum * (1.0 + gam_k)
+    summed = summed[None, :] + rounding
+    sigma = _C1 * np.sqrt(sq_sum) + _C2 * np.sqrt(t2 * (1.0 + gam_k))
+    hoeff = FREIVALDS_C * sigma[None, :] + rounding
+    with np.errstate(invalid="ignore", divide="ignore"):
+        ratio_s = np.where(summed > 0, r / summed, np.where(r > 0, np.inf, 0.0))
+        ratio_h = np.where(hoeff > 0, r / hoeff, np.where(r > 0, np.inf, 0.0))
+    ok_s = bool((ratio_s <= 1.0).all())
+    ok_h = bool((ratio_h <= 1.0).all())
+    finite = bool((nonfinite == 0).all())
+    fails = np.argwhere(~(ratio_h <= 1.0))[:16]
+    return dict(ok=ok_s and ok_h and finite, ok_summed=ok_s, ok_hoeffding=ok_h, finite=finite,
+                worst_summed=float(np.nanmax(ratio_s)), worst_hoeffding=float(np.nanmax(ratio_h)),
+                fails=[(int(q), int(i)) for q, i in fails])

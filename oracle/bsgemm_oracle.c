@@ -765,3 +765,298 @@ int bso_nvfp4_quantize(int rows, int K, const uint16_t *X, uint8_t *packed, uint
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Freivalds' check of a whole product without forming it                   */
+/* ------------------------------------------------------------------------ */
+
+/* R. Freivalds, "Probabilistic machines can use less running time" (IFIP
+ * Congress 1977): a correct D = alpha * Adeq Bdeq^T satisfies, for every
+ * vector x of length N,
+ *     D x = alpha * Adeq (Bdeq^T x),
+ * and the right-hand side costs O((M + N) K) instead of the product's
+ * O(M N K). So every element of a full-size result (16384^3: hours of the
+ * element-wise definition above) enters a check that takes seconds. Adeq /
+ * Bdeq hold the decoded elements times their block scales (NVFP4) or the
+ * decoded E4M3 elements (FP8, whose per-tensor scales fold into `scale`).
+ *
+ * For each of the nv vectors x_q (int8[nv][N]) this returns
+ *     v_q[k]   = sum_j bdeq[j][k] * x_q[j]
+ *     y[q][i]  = scale * sum_k adeq[i][k] * v_q[k]
+ *     g[q][i]  = |scale| * sum_k |adeq[i][k]| * |v_q[k]|
+ * and, for the tolerance, per row i
+ *     tsum[i]  = |scale| * sum_k |adeq[i][k]| * sum_j |bdeq[j][k]|
+ *              = sum_j T[i][j]            (T of the element-wise oracle)
+ *     t2[i]    = scale^2 * (sum_k adeq[i][k]^2) * (sum_j sum_k bdeq[j][k]^2)
+ *              >= sum_j T[i][j]^2         (Cauchy-Schwarz on each T[i][j])
+ * Exactness: NVFP4 elements are multiples of 2^-10 below 2^12 in magnitude,
+ * E4M3 ones multiples of 2^-9 below 2^9; with |x| <= 127 and N < 2^20 every
+ * v_q[k] and every sum_j |bdeq[j][k]| is an integer multiple of that unit
+ * below 2^53 of them, so exact in double whatever the summation order. y,
+ * tsum and t2 carry the rounding of a K-term double sum; g bounds y's.     */
+
+typedef struct {
+    int kind;                     /* 0 = NVFP4, 1 = FP8 */
+    int is_b;                     /* decoding B (the first phase)          */
+    int N, K, nv;
+    const uint8_t *X, *sfX;       /* the operand of this phase             */
+    const int8_t *x;              /* [nv][N] (B phase)                     */
+    const double *v, *w;          /* [nv][K], [K]   (A phase)              */
+    double scale;
+    double *pv, *pw, *pb2;        /* B phase: this worker's partial sums   */
+    double *y, *g, *tsum, *a2;    /* A phase outputs, [nv][M] / [M]        */
+    int M;
+    int r0, r1;
+    double e2m1_tab[16];
+    double e4m3_tab[256];
+} fv_job_t;
+
+/* Row r of an operand, decoded with its block scales into out[K]. */
+static void fv_decode_row(const fv_job_t *jb, int r, double *out)
+{
+    const int K = jb->K;
+    if (jb->kind == 0) {
+        const uint8_t *row = jb->X + (size_t)r * (size_t)(K / 2);
+        const uint8_t *sf = jb->sfX + (size_t)r * (size_t)(K / 16);
+#ifdef BSO_MUTANT_FV_DROP_SFB
+        if (jb->is_b) {
+            for (int k = 0; k < K; ++k)
+                out[k] = jb->e2m1_tab[nib(row, k)];
+            return;
+        }
+#endif
+        for (int k = 0; k < K; ++k)
+            out[k] = jb->e2m1_tab[nib(row, k)] * jb->e4m3_tab[sf[k / 16]];
+    } else {
+        const uint8_t *row = jb->X + (size_t)r * (size_t)K;
+        for (int k = 0; k < K; ++k)
+            out[k] = jb->e4m3_tab[row[k]];
+    }
+}
+
+/* B phase: rows [r0, r1) of B into this worker's partial v, w, b2. */
+static void *fv_b_worker(void *arg)
+{
+    fv_job_t *jb = (fv_job_t *)arg;
+    const int K = jb->K, nv = jb->nv;
+    double *row = (double *)malloc(sizeof(double) * (size_t)K);
+    if (!row)
+        return (void *)1;
+    for (int j = jb->r0; j < jb->r1; ++j) {
+        fv_decode_row(jb, j, row);
+        for (int k = 0; k < K; ++k) {
+#ifdef BSO_MUTANT_FV_TSUM_SIGNED
+            jb->pw[k] += row[k];
+#else
+            jb->pw[k] += fabs(row[k]);
+#endif
+            *jb->pb2 += row[k] * row[k];
+        }
+        for (int q = 0; q < nv; ++q) {
+#ifdef BSO_MUTANT_FV_X_REVERSED
+            const double xq = (double)jb->x[(size_t)q * (size_t)jb->N + (size_t)(jb->N - 1 - j)];
+#else
+            const double xq = (double)jb->x[(size_t)q * (size_t)jb->N + (size_t)j];
+#endif
+            double *vq = jb->pv + (size_t)q * (size_t)K;
+            if (xq != 0.0)
+                for (int k = 0; k < K; ++k)
+                    vq[k] += row[k] * xq;
+        }
+    }
+    free(row);
+    return NULL;
+}
+
+/* A phase: rows [r0, r1) of A against the finished v and w. */
+static void *fv_a_worker(void *arg)
+{
+    fv_job_t *jb = (fv_job_t *)arg;
+    const int K = jb->K, nv = jb->nv, M = jb->M;
+    double *row = (double *)malloc(sizeof(double) * (size_t)K);
+    if (!row)
+        return (void *)1;
+    for (int i = jb->r0; i < jb->r1; ++i) {
+        fv_decode_row(jb, i, row);
+        double t = 0.0, s2 = 0.0;
+        for (int k = 0; k < K; ++k) {
+            t += fabs(row[k]) * jb->w[k];
+            s2 += row[k] * row[k];
+        }
+        jb->tsum[i] = fabs(jb->scale) * t;
+        jb->a2[i] = s2;
+        for (int q = 0; q < nv; ++q) {
+            const double *vq = jb->v + (size_t)q * (size_t)K;
+            double s = 0.0, a = 0.0;
+            for (int k = 0; k < K; ++k) {
+                s += row[k] * vq[k];
+                a += fabs(row[k]) * fabs(vq[k]);
+            }
+            jb->y[(size_t)q * (size_t)M + (size_t)i] = jb->scale * s;
+            jb->g[(size_t)q * (size_t)M + (size_t)i] = fabs(jb->scale) * a;
+        }
+    }
+    free(row);
+    return NULL;
+}
+
+/* Runs `fn` over rows [0, rows) split across nthreads copies of proto. */
+static int fv_run(fv_job_t *proto, int rows, int nthreads, void *(*fn)(void *), fv_job_t **jobs_out,
+                  int *njobs)
+{
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > rows)
+        nthreads = rows > 0 ? rows : 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    fv_job_t *jobs = (fv_job_t *)calloc((size_t)nthreads, sizeof(fv_job_t));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    int *started = (int *)calloc((size_t)nthreads, sizeof(int));
+    *jobs_out = NULL;
+    *njobs = 0;
+    if (!jobs || !th || !started) {
+        free(jobs);
+        free(th);
+        free(started);
+        return -2;
+    }
+    int rc = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = *proto;
+        jobs[t].r0 = (int)((long long)rows * t / nthreads);
+        jobs[t].r1 = (int)((long long)rows * (t + 1) / nthreads);
+    }
+    if (fn == fv_b_worker) {
+        const size_t nvk = (size_t)proto->nv * (size_t)proto->K;
+        for (int t = 0; t < nthreads; ++t) {
+            jobs[t].pv = (double *)calloc(nvk + (size_t)proto->K + 1u, sizeof(double));
+            if (!jobs[t].pv)
+                rc = -2;
+            else {
+                jobs[t].pw = jobs[t].pv + nvk;
+                jobs[t].pb2 = jobs[t].pw + proto->K;
+            }
+        }
+    }
+    if (rc == 0) {
+        for (int t = 0; t < nthreads; ++t)
+            started[t] = nthreads > 1 && pthread_create(&th[t], NULL, fn, &jobs[t]) == 0;
+        for (int t = 0; t < nthreads; ++t) {
+            void *ret = NULL;
+            if (started[t])
+                pthread_join(th[t], &ret);
+            else
+                ret = fn(&jobs[t]);
+            if (ret)
+                rc = -2;
+        }
+    }
+    free(th);
+    free(started);
+    *jobs_out = jobs;
+    *njobs = nthreads;
+    return rc;
+}
+
+static int fv_check(fv_job_t *proto, int M, const uint8_t *A, const uint8_t *sfA, const uint8_t *B,
+                    const uint8_t *sfB, double *y, double *g, double *tsum, double *t2, int nthreads)
+{
+    for (int c = 0; c < 16; ++c)
+        proto->e2m1_tab[c] = bso_e2m1((unsigned)c);
+    for (int c = 0; c < 256; ++c)
+        proto->e4m3_tab[c] = bso_e4m3((unsigned)c);
+    const int K = proto->K, nv = proto->nv, N = proto->N;
+    const size_t nvk = (size_t)nv * (size_t)K;
+    double *v = (double *)calloc(nvk + (size_t)K, sizeof(double));
+    double *a2 = (double *)calloc((size_t)(M > 0 ? M : 1), sizeof(double));
+    if (!v || !a2) {
+        free(v);
+        free(a2);
+        return -2;
+    }
+    double *w = v + nvk;
+    double b2 = 0.0;
+
+    /* B phase: partial sums per worker, added afterwards (exact: see above) */
+    proto->X = B;
+    proto->sfX = sfB;
+    proto->is_b = 1;
+    fv_job_t *jobs = NULL;
+    int nj = 0;
+    int rc = fv_run(proto, N, nthreads, fv_b_worker, &jobs, &nj);
+    for (int t = 0; t < nj; ++t) {
+        if (jobs[t].pv) {
+            for (size_t u = 0; u < nvk; ++u)
+                v[u] += jobs[t].pv[u];
+            for (int k = 0; k < K; ++k)
+                w[k] += jobs[t].pw[k];
+            b2 += *jobs[t].pb2;
+            free(jobs[t].pv);
+        }
+    }
+    free(jobs);
+    if (rc != 0) {
+        free(v);
+        free(a2);
+        return rc;
+    }
+
+    /* A phase */
+    proto->X = A;
+    proto->sfX = sfA;
+    proto->is_b = 0;
+    proto->v = v;
+    proto->w = w;
+    proto->y = y;
+    proto->g = g;
+    proto->tsum = tsum;
+    proto->a2 = a2;
+    proto->M = M;
+    rc = fv_run(proto, M, nthreads, fv_a_worker, &jobs, &nj);
+    free(jobs);
+    if (rc == 0)
+        for (int i = 0; i < M; ++i)
+            t2[i] = proto->scale * proto->scale * a2[i] * b2;
+    free(v);
+    free(a2);
+    return rc;
+}
+
+/* NVFP4: A uint8[M][K/2], sfA uint8[M][K/16], B uint8[N][K/2], sfB
+ * uint8[N][K/16] (row-major scales); x int8[nv][N]; outputs y, g [nv][M],
+ * tsum, t2 [M]. Returns 0, -1 for bad sizes, -2 if memory ran out.        */
+int bso_nvfp4_freivalds(int M, int N, int K, const uint8_t *A, const uint8_t *sfA, const uint8_t *B,
+                        const uint8_t *sfB, float alpha, const int8_t *x, int nv, double *y, double *g,
+                        double *tsum, double *t2, int nthreads)
+{
+    if (M < 1 || N < 1 || K < 16 || (K % 16) != 0 || nv < 1 || N >= (1 << 20))
+        return -1;
+    fv_job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.kind = 0;
+    jb.N = N;
+    jb.K = K;
+    jb.nv = nv;
+    jb.x = x;
+    jb.scale = (double)alpha;
+    return fv_check(&jb, M, A, sfA, B, sfB, y, g, tsum, t2, nthreads);
+}
+
+/* FP8: A uint8[M][K], B uint8[N][K] E4M3; the multiplier is the double
+ * product alpha * sA * sB, as in bso_fp8_gemm.                              */
+int bso_fp8_freivalds(int M, int N, int K, const uint8_t *A, const uint8_t *B, float alpha, float sA, float sB,
+                      const int8_t *x, int nv, double *y, double *g, double *tsum, double *t2, int nthreads)
+{
+    if (M < 1 || N < 1 || K < 1 || nv < 1 || N >= (1 << 20))
+        return -1;
+    fv_job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.kind = 1;
+    jb.N = N;
+    jb.K = K;
+    jb.nv = nv;
+    jb.x = x;
+    jb.scale = (double)alpha * (double)sA * (double)sB;
+    return fv_check(&jb, M, A, NULL, B, NULL, y, g, tsum, t2, nthreads);
+}

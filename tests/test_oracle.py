@@ -11,8 +11,9 @@ scale layout; in the quantiser, ties rounded away from zero, a dropped global
 scale, swapped nibbles, block scales rounded up; in the epilogue, gamma
 applied before the bias, bias indexed by row; in the grouped GEMM, a slice
 multiplied by the next slice's right-hand side; in the NVFP4 x dense GEMM,
-A's block scales dropped) and shows that at least one
-pin fails for each.
+A's block scales dropped; in Freivalds' full-product check, B's block scales
+dropped, the random vector read backwards, magnitudes summed with their
+signs) and shows that at least one pin fails for each.
 """
 from __future__ import annotations
 
@@ -765,6 +766,60 @@ def pin_quantize_dequant_bound(o):
     assert np.all(np.abs(deq - x) <= 1.001 * step)
 
 
+def pin_freivalds_worked(o):
+    """Freivalds' right-hand side on the hand-worked 2x2x32 case: D =
+    [[96, 54], [-48, -27]] (every B value >= 0, so T = |D|), hence D x for
+    x = (1, -1) and (1, 1) is (42, -21) and (150, -75), and sum_j T[i][j] =
+    (150, 75) -- values worked by hand, not by the oracle's GEMM."""
+    A = pack(np.array([[0x2] * 32, [0xA] * 32], np.uint8))
+    B = pack(np.array([[0x4] * 32, [k % 8 for k in range(32)]], np.uint8))
+    sfA = np.array([[0x38, 0x40], [0x30, 0x38]], np.uint8)
+    sfB = np.array([[0x38, 0x38], [0x38, 0x28]], np.uint8)
+    x = np.array([[1, -1], [1, 1]], np.int8)
+    r = o.nvfp4_freivalds(A, sfA, B, sfB, 1.0, 32, x)
+    assert np.array_equal(r["y"], [[42.0, -21.0], [150.0, -75.0]]), r["y"]
+    assert np.array_equal(r["tsum"], [150.0, 75.0]), r["tsum"]
+    assert np.all(r["g"] >= np.abs(r["y"]))
+
+
+def _freivalds_vs_gemm(o, S, T, r, x):
+    ref = S @ x.astype(np.float64).T
+    assert np.all(np.abs(r["y"] - ref.T) <= 1e-12 * (r["g"] + np.abs(S).sum(axis=1)[None, :])), "y != S x"
+    assert np.allclose(r["tsum"], T.sum(axis=1), rtol=1e-12, atol=0), "tsum != sum_j T"
+    assert np.all(r["t2"] >= (T * T).sum(axis=1) * (1 - 1e-12)), "t2 below sum_j T^2"
+
+
+def pin_freivalds_matches_gemm(o):
+    """Freivalds' right-hand side y = alpha Adeq (Bdeq^T x) against the
+    pinned element-wise oracle's S x, on ragged shapes of both kinds: the
+    same product, associated the other way. Also sum_j T = tsum and the
+    Cauchy-Schwarz bound t2 >= sum_j T^2."""
+    x = oracle.rademacher(3, 136, seed=5)
+    w = workloads.WORKLOADS["nvfp4_4096"]
+    p = workloads.make_nvfp4(w, "cpu", M=72, N=136, K=512)
+    A, sfA, B, sfB = (p[k].numpy() for k in ("A", "sfA", "B", "sfB"))
+    S, T, _ = o.nvfp4_gemm(A, sfA, B, sfB, p["alpha"], 512)
+    _freivalds_vs_gemm(o, S, T, o.nvfp4_freivalds(A, sfA, B, sfB, p["alpha"], 512, x), x)
+    w8 = workloads.WORKLOADS["fp8_8192"]
+    q = workloads.make_fp8(w8, "cpu", M=40, N=136, K=96)
+    A8, B8 = q["A"].numpy(), q["B"].numpy()
+    S8, T8, _ = o.fp8_gemm(A8, B8, q["alpha"], 0.5, 3.0)
+    _freivalds_vs_gemm(o, S8, T8, o.fp8_freivalds(A8, B8, q["alpha"], x, 0.5, 3.0), x)
+
+
+def pin_freivalds_gram(o):
+    """With B = A the product is the Gram matrix: S_ii = alpha sum_k adeq_ik^2,
+    so t2_i = alpha^2 a2_i b2 must equal S_ii * sum_j S_jj exactly up to
+    rounding -- a check of t2's two sums through the pinned GEMM."""
+    w = workloads.WORKLOADS["nvfp4_4096"]
+    p = workloads.make_nvfp4(w, "cpu", M=48, N=48, K=256)
+    A, sfA = p["A"].numpy(), p["sfA"].numpy()
+    S, _, _ = o.nvfp4_gemm(A, sfA, A, sfA, 0.75, 256)
+    r = o.nvfp4_freivalds(A, sfA, A, sfA, 0.75, 256, oracle.rademacher(1, 48, seed=2))
+    d = np.diag(S)
+    assert np.allclose(r["t2"], d * d.sum(), rtol=1e-12, atol=0)
+
+
 PINS = [pin_e2m1_table, pin_e4m3_codes, pin_bf16_cases, pin_worked_1x1x16, pin_worked_2x2x32,
         pin_one_hot, pin_brute_force_k16, pin_scale_linearity, pin_numpy_definition,
         pin_fraction_exact, pin_fp8_numpy, pin_swizzle, pin_quantize_worked,
@@ -773,7 +828,7 @@ PINS = [pin_e2m1_table, pin_e4m3_codes, pin_bf16_cases, pin_worked_1x1x16, pin_w
         pin_grouped_worked, pin_grouped_single_slice_is_plain, pin_grouped_numpy, pin_grouped_scale_layout,
         pin_dense_worked, pin_dense_reduces_to_nvfp4, pin_dense_numpy, pin_dense_f16_worked,
         pin_dense_f16_numpy, pin_dense_grouped_worked, pin_dense_grouped_numpy, pin_dense_kragged_worked,
-        pin_dense_kragged_partition]
+        pin_dense_kragged_partition, pin_freivalds_worked, pin_freivalds_matches_gemm, pin_freivalds_gram]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -784,7 +839,7 @@ def test_oracle_pin(pin):
 MUTANTS = ["E2M1_BIAS0", "E2M1_NOSIGN", "E4M3_BIAS8", "SWAP_NIBBLES_A", "DROP_SFB",
            "DROP_LAST_BLOCK", "TRANSPOSE_B", "SWIZZLE_ROWMAJOR_BLOCK", "Q_TIES_AWAY", "Q_NO_SG",
            "Q_SWAP_NIBBLES", "Q_E4M3_CEIL", "EPI_GAMMA_FIRST", "EPI_BIAS_BY_ROW",
-           "GROUP_SHIFT", "DENSE_DROP_SFA", "F16_BIAS16"]
+           "GROUP_SHIFT", "DENSE_DROP_SFA", "F16_BIAS16", "FV_DROP_SFB", "FV_X_REVERSED", "FV_TSUM_SIGNED"]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
