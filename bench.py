@@ -9,11 +9,14 @@ sweep shape), inputs resident in HBM, larger than L2.
 Prints ONE JSON line (rank 0). Besides the contract's keys it carries the
 dominant kernel's roofline (CUDA-event duration of the GEMM launches inside
 the timed region), the CPU oracle timed on a bounded sample, the clocks seen
-during the timed region, and secondary lines for the FP8 8192^3 GEMM, the
+during the timed region, the sustained rate (CUDA-graph replays, median of
+15 x 20 iterations, clocks sampled alongside), the host link's copy rates
+beside the end-to-end figure, and secondary lines for the FP8 8192^3 GEMM, the
 skinny-M sweep (HBM GB/s), the scale swizzle, the NVFP4 quantiser, the
 fused epilogue variants (bias, gamma, scattered rows), the grouped (MoE)
 GEMM, the NVFP4 x dense-BF16 / FP16 GEMM, and the GEMM from tile-packed
-operands against the same GEMM from row-major ones.
+operands against the same GEMM from row-major ones. A compact "summary"
+object closes the line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -42,13 +45,26 @@ FP4_PER_BF16 = 13.5 / 2.25
 FP8_PER_BF16 = 4.5 / 2.25
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes per GEMM launch from an ncu capture of the current kernel
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (plan, workload);
-# the summary it comes from is named in the comment. None = not captured.
-NCU_TRAFFIC_BYTES: dict[tuple[str, str], float] = {
-    # profiles/gemm_pair_nvfp4_256x256_s5_acc1_16384.md (raster group 16): 1.118 GB read + 0.520 GB written
-    ("nvfp4_tc2_256x256_s5_acc1", "nvfp4_16384"): 1118412544 + 520391680,
-}
+# DRAM bytes per GEMM launch (dram__bytes_read.sum + dram__bytes_write.sum)
+# from one ncu capture, keyed by (plan, workload) and stored with the digest
+# of the kernel sources it was taken on (kernel_digest()): once any of them
+# changes the figure no longer describes the kernel and traffic reads null.
+NCU_TRAFFIC_BYTES: dict[tuple[str, str], tuple[str, float]] = {}
+KERNEL_SOURCES = ("gemm_pair.cu", "gemm_common.cuh", "ptx.cuh", "bsg_internal.h")
+
+
+def kernel_digest() -> str:
+    """sha256 (first 16 hex digits) of the pair kernel's sources."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update((ROOT / "block_scaled_precision_persistent_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(plan: str, workload: str) -> float | None:
+    rec = NCU_TRAFFIC_BYTES.get((plan, workload))
+    return rec[1] if rec is not None and rec[0] == kernel_digest() else None
 
 
 def peaks() -> tuple[dict, str]:
@@ -73,67 +89,136 @@ def Dist(gpus: int):
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
+    """SM clock, power and clock-event reasons of this rank's GPU, sampled
+    every 5 ms from a background thread through NVML (ctypes on the driver's
+    libnvidia-ml; read-only queries), or every 10 ms by nvidia-smi where NVML
+    cannot be loaded. The GPU is found by UUID (CUDA's ordinal and NVML's
+    index differ under CUDA_VISIBLE_DEVICES)."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReason* bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
 
-    def __init__(self, index: int):
-        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-        ids = [v.strip() for v in vis.split(",") if v.strip()]
-        self.index = ids[index] if index < len(ids) and ids[index].isdigit() else index
+    def __init__(self, index: int, period_s: float = 0.005):
+        self.index = index
+        self.period = period_s
+        self.rows: list[tuple[float, float, int]] = []     # (sm MHz, power W, reason bits)
+        self.max_mhz = None
+        self.backend = None
         self.proc = None
         self.file = None
+        self.thread = None
+        self.stop = False
+
+    # -- NVML -----------------------------------------------------------------
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        want = str(torch.cuda.get_device_properties(self.index).uuid).lower().replace("gpu-", "")
+        count = ctypes.c_uint(0)
+        lib.nvmlDeviceGetCount_v2(ctypes.byref(count))
+        handle = None
+        for i in range(count.value):
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(i, ctypes.byref(h)) != 0:
+                continue
+            buf = ctypes.create_string_buffer(96)
+            if lib.nvmlDeviceGetUUID(h, buf, 96) == 0 and \
+                    buf.value.decode().lower().replace("gpu-", "") == want:
+                handle = h
+        if handle is None:
+            raise OSError("no NVML device with this GPU's UUID")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        if lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        return lib, handle, reasons
+
+    def _nvml_loop(self, lib, handle, reasons):
+        import ctypes
+        mhz, mw, bits = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while not self.stop:
+            ok = lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(mhz)) == 0
+            ok = ok and lib.nvmlDeviceGetPowerUsage(handle, ctypes.byref(mw)) == 0
+            ok = ok and reasons(handle, ctypes.byref(bits)) == 0
+            if ok:
+                self.rows.append((float(mhz.value), mw.value / 1000.0, int(bits.value)))
+            time.sleep(self.period)
 
     def __enter__(self):
+        import threading
+        try:
+            lib, handle, reasons = self._nvml_open()
+            self.backend = "nvml, 5 ms"
+            self.thread = threading.Thread(target=self._nvml_loop, args=(lib, handle, reasons), daemon=True)
+            self.thread.start()
+            time.sleep(0.05)
+            return self
+        except (OSError, AttributeError, RuntimeError):
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        smi_index = ids[self.index] if self.index < len(ids) and ids[self.index].isdigit() else self.index
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                ["nvidia-smi", f"--id={smi_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
+            self.backend = "nvidia-smi, 10 ms"
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def __exit__(self, *exc):
+        if self.thread is not None:
+            time.sleep(0.02)
+            self.stop = True
+            self.thread.join(timeout=5)
         if self.proc is not None:
-            time.sleep(0.2)
+            time.sleep(0.05)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            self._read_smi()
         return False
 
-    def summary(self) -> dict:
-        if self.proc is None or self.file is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        for line in Path(self.file.name).read_text().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) >= 9:
-                rows.append(f)
-        os.unlink(self.file.name)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-
+    def _read_smi(self):
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        power = [num(r[3]) for r in rows if num(r[3]) is not None]
-        # samples under load: power well above idle
-        pmax = max(power) if power else 0.0
-        loaded = [num(r[1]) for r in rows if num(r[3]) is not None and num(r[3]) > 0.5 * pmax
-                  and num(r[1]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k] == "Active"})
-        return {"sm_mhz": statistics.median(loaded or sm), "sm_max_mhz": num(rows[0][2]),
-                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
-                "power_w_max": pmax}
+        names = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                 "hw_thermal_slowdown": 0x40}
+        cols = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in Path(self.file.name).read_text().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9 and num(f[1]) is not None and num(f[3]) is not None:
+                bits = sum(names[c] for k, c in enumerate(cols) if f[5 + k] == "Active")
+                self.rows.append((num(f[1]), num(f[3]), bits))
+                self.max_mhz = num(f[2])
+        os.unlink(self.file.name)
+
+    def summary(self) -> dict:
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz,
+                    "reasons": ["no samples" if self.backend else "no clock source"]}
+        pmax = max(r[1] for r in self.rows)
+        loaded = [r for r in self.rows if r[1] > 0.5 * pmax]          # samples under load
+        use = loaded or self.rows
+        reasons = sorted({name for r in use for bit, name in self.REASONS.items() if r[2] & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in use), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min_under_load": min(r[0] for r in use), "reasons": reasons,
+                "samples": len(self.rows), "samples_under_load": len(loaded), "power_w_max": round(pmax, 1),
+                "source": self.backend}
 
 
 # ---------------------------------------------------------------------------
@@ -154,19 +239,22 @@ class Nvfp4Step:
         self.swA = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
         self.swB = torch.empty(bsg.nvfp4_swizzled_scale_bytes(N, K), dtype=torch.uint8, device=dev)
         self.D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        self.stream = torch.cuda.current_stream()
         self.launches = 0
 
     def __call__(self, ev=None):
         b, w = self.bsg, self.w
-        b.nvfp4_swizzle_scales2(w.M, w.N, w.K, self.sfA, self.swA, self.sfB, self.swB, self.stream)
+        st = torch.cuda.current_stream()         # the launching stream (a capture stream in a graph)
+        b.nvfp4_swizzle_scales2(w.M, w.N, w.K, self.sfA, self.swA, self.sfB, self.swB, st)
         if ev is not None:
-            ev[0].record(self.stream)
-        b.nvfp4_gemm_swizzled(w.M, w.N, w.K, self.A, self.swA, self.B, self.swB, self.alpha,
-                              self.D, self.stream)
+            ev[0].record(st)
+        b.nvfp4_gemm_swizzled(w.M, w.N, w.K, self.A, self.swA, self.B, self.swB, self.alpha, self.D, st)
         if ev is not None:
-            ev[1].record(self.stream)
+            ev[1].record(st)
         self.launches += 2
+
+    def gemm(self):
+        w = self.w
+        self.bsg.nvfp4_gemm_swizzled(w.M, w.N, w.K, self.A, self.swA, self.B, self.swB, self.alpha, self.D)
 
     def plan(self) -> str:
         return self.bsg.bsg_select_plan(0, self.w.M, self.w.N, self.w.K,
@@ -192,6 +280,59 @@ def time_steps(step, steps: int, warmup: int, dist: Dist, gemm_events=True):
     total_ms = start.elapsed_time(end)
     gemm_ms = [a.elapsed_time(b) for a, b in evs] if gemm_events else []
     return total_ms, gemm_ms
+
+
+def sustained(step: Nvfp4Step, pk: dict, psrc: str, index: int, repeats: int = 15, iters: int = 20) -> dict:
+    """The timing practice of the pages (TokenSpeed MLA 2 page, benchmark
+    setup): CUDA-graph replays, the median of `repeats` replays of a graph of
+    `iters` back-to-back iterations -- here of the whole step (swizzle +
+    GEMM) and of the GEMM alone, the two graphs interleaved, with the clocks
+    sampled over all of it. Back to back, the GPU runs under its power cap:
+    this is the sustained rate, the timed loop's `value` the burst rate."""
+    w = step.w
+    with ClockSampler(index) as clk:
+        us = graph_us({"step": step, "gemm": step.gemm}, iters, repeats)
+    clocks = clk.summary()
+    if step.bsg.bsg_get_device_status() != step.bsg.BSG_OK:
+        raise SystemExit("device status reported an error in the sustained timing")
+    peak = pk["bf16_tflops"] * FP4_PER_BF16
+    out = {"timing": f"median of {repeats} replays of a CUDA graph of {iters} back-to-back iterations, "
+                     "step and GEMM graphs interleaved", "clocks": clocks}
+    for k in ("step", "gemm"):
+        tf = w.flops / (us[k] * 1e-6) / 1e12
+        out[k] = {"us": round(us[k], 2), "tflops": round(tf, 1), "frac_of_9pf": round(tf / 9000.0, 4),
+                  "frac": round(tf / peak, 4)}
+    out["peak_source"] = f"{psrc} bf16 burst x {FP4_PER_BF16:g}"
+    return out
+
+
+def copy_bandwidth(host: dict, dev_bufs: dict, hD, dD, reps: int = 3) -> dict:
+    """Plain pinned-memory copy rates of this host link, for the e2e bound:
+    the step's H2D copies alone, its D2H copy alone, and both at once on two
+    streams (GB/s, best of `reps`)."""
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    nin = sum(t.numel() * t.element_size() for t in host.values())
+    nout = hD.numel() * hD.element_size()
+
+    def timed(which):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            if which in ("in", "both"):
+                with torch.cuda.stream(h2d):
+                    for k, t in host.items():
+                        dev_bufs[k].copy_(t, non_blocking=True)
+            if which in ("out", "both"):
+                with torch.cuda.stream(d2h):
+                    hD.copy_(dD, non_blocking=True)
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
+    t_in, t_out, t_both = timed("in"), timed("out"), timed("both")
+    return {"h2d_gbs": round(nin / t_in / 1e9, 1), "d2h_gbs": round(nout / t_out / 1e9, 1),
+            "both_gbs": round((nin + nout) / t_both / 1e9, 1),
+            "copy_bound_ms": round(max(t_in, t_out, t_both) * 1e3, 3)}
 
 
 def e2e_nvfp4(w: workloads.Workload, step: Nvfp4Step, steps: int, warmup: int) -> dict:
@@ -251,10 +392,14 @@ def e2e_nvfp4(w: workloads.Workload, step: Nvfp4Step, steps: int, warmup: int) -
             raise SystemExit("e2e: D copied back differs from the device-only result")
     h2d_bytes = sum(t.numel() * t.element_size() for t in host.values())
     d2h_bytes = hD[0].numel() * hD[0].element_size()
+    link = copy_bandwidth(host, slots[1], hD[1], slots[1]["D"])
     del slots[1]
+    # the pipeline overlaps the GEMM with both copies, so a step cannot take
+    # less than its copies alone (both directions at once): the bound
+    link["frac_of_copy_bound"] = round(link["copy_bound_ms"] / ms, 4)
     return {"value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
-            "pipelined": "two buffer sets; H2D, compute and D2H on three streams"}
+            "pipelined": "two buffer sets; H2D, compute and D2H on three streams", "host_link": link}
 
 
 def secondary_fp8(dev, steps: int, warmup: int, pk: dict, psrc: str) -> dict:
@@ -823,6 +968,7 @@ def run_ours(args, dist: Dist) -> None:
     with ClockSampler(dist.local) as clk:
         total_ms, gemm_ms = time_steps(step, args.steps, args.warmup, dist)
     clocks = clk.summary()
+    sus = sustained(step, pk, psrc, dist.local) if dist.rank == 0 else None
     launches = step.launches
     ms = dist.max(total_ms / args.steps)
     value = dist.world * w.flops / (ms * 1e-3) / 1e12
@@ -830,7 +976,7 @@ def run_ours(args, dist: Dist) -> None:
     achieved = w.flops / (gemm_avg * 1e-3) / 1e12
     peak = pk["bf16_tflops"] * FP4_PER_BF16
     plan = step.plan()
-    traffic = NCU_TRAFFIC_BYTES.get((plan, w.name))
+    traffic = ncu_traffic(plan, w.name)
     ingress = None
     if dist.rank == 0:
         ingress = ingress_roofline(bsg, w, plan, gemm_avg, clocks)
@@ -879,8 +1025,30 @@ def run_ours(args, dist: Dist) -> None:
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "sustained": sus,
         "secondary": secondary,
     }
+    # compact figures last on the line, where a record that keeps only the
+    # line's end still holds them
+    summary = {"gemm_burst_tflops": round(achieved, 1), "gemm_burst_frac_9pf": round(achieved / 9000.0, 4)}
+    if sus is not None:
+        summary.update(gemm_sustained_us=sus["gemm"]["us"], gemm_sustained_frac_9pf=sus["gemm"]["frac_of_9pf"],
+                       step_sustained_us=sus["step"]["us"], sustained_sm_mhz=sus["clocks"].get("sm_mhz"))
+    if "fp8" in secondary:
+        f = secondary["fp8"]
+        summary.update(fp8_8192_tflops=round(f["tflops"], 1), fp8_frac_4p5pf=round(f["tflops"] / 4500.0, 4))
+    if "skinny" in secondary:
+        fr = {k: v["frac_hbm"] for k, v in secondary["skinny"]["cells"].items()}
+        summary.update(skinny_frac_hbm_min=min(fr.values()), skinny_frac_hbm_max=max(fr.values()),
+                       skinny_worst_cell=min(fr, key=fr.get))
+    if "swizzle" in secondary:
+        summary["swizzle_frac_hbm"] = secondary["swizzle"]["frac_hbm"]
+    if "grouped" in secondary:
+        summary["moe_frac_hbm"] = secondary["grouped"]["variants"]["scatter"]["frac_hbm"]
+    if e2e is not None:
+        summary.update(e2e_tflops=round(e2e["value"], 1),
+                       e2e_frac_of_copy_bound=e2e["host_link"]["frac_of_copy_bound"])
+    line["summary"] = summary
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
 
