@@ -49,7 +49,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from one ncu capture, keyed by (plan, workload) and stored with the digest
 # of the kernel sources it was taken on (kernel_digest()): once any of them
 # changes the figure no longer describes the kernel and traffic reads null.
-NCU_TRAFFIC_BYTES: dict[tuple[str, str], tuple[str, float]] = {}
+NCU_TRAFFIC_BYTES: dict[tuple[str, str], tuple[str, float]] = {
+    # one-pass capture of the third GEMM launch of
+    # bench.py --case nvfp4:16384x16384x16384 --steps 1 --warmup 3
+    ("nvfp4_tc2_256x256_s5_acc1", "nvfp4_16384"): ("c6a94751420a89e7", 1129157376 + 520297728),
+}
 KERNEL_SOURCES = ("gemm_pair.cu", "gemm_common.cuh", "ptx.cuh", "bsg_internal.h")
 
 
