@@ -22,7 +22,7 @@ __all__ = [
     "nvfp4_dense_kgrouped_gemm", "nvfp4_dense_f16_kgrouped_gemm",
     "nvfp4_swizzle_scales2", "nvfp4_quantize_tiles", "nvfp4_pack_operand", "nvfp4_packed_operand_bytes", "nvfp4_gemm_packed", "nvfp4_gemm_packed_ex",
     "bsg_reserve_workspace", "bsg_get_device_status",
-    "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_set_pdl", "bsg_watchdog_selftest", "bsg_force_plan",
+    "bsg_last_status_word", "bsg_set_watchdog_ns", "bsg_set_raster_group", "bsg_set_skinny_splits", "bsg_set_pdl", "bsg_watchdog_selftest", "bsg_force_plan",
     "bsg_measure_ingress",
     "bsg_select_plan", "bsg_last_launch_count", "bsg_last_plan_name", "bsg_error_string", "EXPORTED_SYMBOLS",
     "BSG_OK", "BSG_ERR_INVALID_ARG", "BSG_ERR_MISALIGNED", "BSG_ERR_UNSUPPORTED_DEVICE",
@@ -80,6 +80,7 @@ _SIGNATURES = {
     "bsg_last_status_word": (ctypes.c_uint32, []),
     "bsg_set_watchdog_ns": (_i, [ctypes.c_uint64]),
     "bsg_set_raster_group": (_i, [_i]),
+    "bsg_set_skinny_splits": (_i, [_i]),
     "bsg_set_pdl": (_i, [_i]),
     "bsg_watchdog_selftest": (_i, [ctypes.c_uint64, _vp]),
     "bsg_measure_ingress": (_i, [ctypes.c_size_t, _i, _i, ctypes.POINTER(ctypes.c_double),
@@ -300,6 +301,11 @@ def bsg_set_pdl(on: bool) -> None:
 def bsg_set_raster_group(m_tiles: int) -> None:
     """M tiles per rasterisation group for later launches (0: default 16)."""
     _check(load().bsg_set_raster_group(int(m_tiles)), "bsg_set_raster_group")
+
+
+def bsg_set_skinny_splits(splits: int) -> None:
+    """K splits of the skinny-M kernel for later launches (0: chosen per call)."""
+    _check(load().bsg_set_skinny_splits(int(splits)), "bsg_set_skinny_splits")
 
 
 def bsg_watchdog_selftest(ns: int, stream=None) -> None:

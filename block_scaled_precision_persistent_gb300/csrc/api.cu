@@ -106,12 +106,15 @@ size_t swizzled_bytes(int rows, int K)
 }
 
 // Planner: the default plan for a shape; -1 if none fits. The rules follow
-// CUDA-graph timings of every plan on the skinny cells (M 64..512 x N 3072 /
-// 12288 x K 3072 / 12288, cold L2) and the square sizes:
-//   * NVFP4, M <= 256: the swap-AB split-K kernel when the weight tiles leave
-//     room to split K at least in two with the whole grid resident (N/128
-//     tiles x 2 <= SMs); above 128 activation rows only for long K (>= 8192),
-//     where streaming the weights dominates its fixed costs;
+// CUDA-graph timings of every plan and split on the skinny cells (M 64..512
+// x N 3072 / 12288 x K 3072 / 12288, cold L2) and the square sizes:
+//   * NVFP4, the swap-AB split-K kernel when the weight tiles leave room to
+//     split K at least in two with the whole grid resident (N/128 tiles x 2
+//     <= SMs): for M <= 64, and up to 256 activation rows for long K
+//     (>= 8192), where streaming the weights dominates its fixed costs;
+//   * 129..512 activation rows with 256 x 256 pair tiles enough to give
+//     every SM a quarter of one (M/256 x N/256 x 4 >= SMs): the CTA pair,
+//     whose tile moves half the bytes per FLOP of a 1-SM 128 x 128 tile;
 //   * otherwise, while 128 x 128 output tiles number at most 4 per SM, the
 //     1-SM 128 x 128 kernel (more CTAs in flight than 256-wide tiles);
 //   * M <= 128 beyond that: the 1-SM 128 x 256 kernel; larger M: the CTA
@@ -124,8 +127,11 @@ int default_plan(Kind kind, int M, int N, int K, int num_sms)
     if (kind == Kind::NVFP4) {
         const int weight_tiles = (N + 127) / 128;
         const bool can_split = 2 * weight_tiles <= num_sms && K >= 512;
-        if (M <= 256 && can_split && (M <= 128 || K >= 8192))
+        const long long pair_tiles = (long long)((M + 255) / 256) * (long long)((N + 255) / 256);
+        if (can_split && (M <= 64 || (M <= 256 && K >= 8192)))
             name = M <= 64 ? "nvfp4_skinny_m64_s6" : M <= 128 ? "nvfp4_skinny_m128_s3" : "nvfp4_skinny_m256_s4";
+        else if (M > 128 && M <= 512 && N > 128 && 4 * pair_tiles >= num_sms)
+            name = "nvfp4_tc2_256x256_s5_acc1";
         else if (few_tiles || N <= 128)
             name = M <= 128 || few_tiles ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc2_256x128_s6_acc2";
         else
@@ -146,6 +152,10 @@ int default_plan(Kind kind, int M, int N, int K, int num_sms)
     return bsg::find_plan(name);
 }
 
+// Activation rows a skinny plan serves: one block of tile_m rows, or two
+// where a block is whole 128-row scale blocks.
+int skinny_max_rows(const PlanInfo &pi) { return pi.tile_m >= 128 ? 2 * pi.tile_m : pi.tile_m; }
+
 int choose_plan(Kind kind, int M, int N, int K, int num_sms, int *plan)
 {
     int forced;
@@ -156,7 +166,7 @@ int choose_plan(Kind kind, int M, int N, int K, int num_sms, int *plan)
     if (forced >= 0) {
         const PlanInfo &fp = bsg::plan_info(forced);
         // a tile-packed plan reads operands only nvfp4_gemm_packed supplies
-        if (fp.kind != kind || fp.packed || (fp.family == bsg::Family::SKINNY && M > fp.tile_m))
+        if (fp.kind != kind || fp.packed || (fp.family == bsg::Family::SKINNY && M > skinny_max_rows(fp)))
             return BSG_ERR_NO_PLAN;
         *plan = forced;
         return BSG_OK;
@@ -199,19 +209,44 @@ int encode_3d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t mid, u
     return r == CUDA_SUCCESS ? BSG_OK : BSG_ERR_CUDA;
 }
 
-// Resident clusters of `splits` CTAs for skinny plan id on the current
-// device (cached; splits a power of two <= 8).
+// Resident clusters of `splits` CTAs (1..8) for skinny plan id on the
+// current device (cached).
 int skinny_cluster_capacity(int id, int splits)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || id < 0 || id >= 8)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || id < 0 || id >= 8 || splits < 1 ||
+        splits > 8)
         return 0;
-    static int cache[kMaxDevices][8][4] = {};
-    const int j = splits == 2 ? 1 : splits == 4 ? 2 : splits == 8 ? 3 : 0;
+    static int cache[kMaxDevices][8][9] = {};
     std::lock_guard<std::mutex> lk(g_mu);
-    if (cache[dev][id][j] == 0)
-        cache[dev][id][j] = bsg::skinny_max_clusters(id, splits);
-    return cache[dev][id][j];
+    if (cache[dev][id][splits] == 0)
+        cache[dev][id][splits] = bsg::skinny_max_clusters(id, splits);
+    return cache[dev][id][splits];
+}
+
+// K splits of the skinny kernel (a cluster of that many CTAs per weight tile
+// and activation block); 0 = chosen per call.
+std::atomic<int> g_skinny_splits{0};
+
+// The split count of a skinny launch: among the splits S the plan takes, S
+// <= k-blocks whose clusters all fit on the device at once, the one whose
+// busiest SM streams the fewest k-blocks (CTAs per SM x k-blocks per CTA),
+// ties going to the smaller S (less to exchange).
+int skinny_splits(int id, int mask, int units, int num_k_blocks, int num_sms)
+{
+    int best = 1;
+    long long best_cost = -1;
+    for (int s = 1; s <= 8; ++s) {
+        if (!(mask & (1 << s)) || s > num_k_blocks || units > skinny_cluster_capacity(id, s))
+            continue;
+        const long long ctas = (long long)units * s;
+        const long long cost = (ctas + num_sms - 1) / num_sms * ((num_k_blocks + s - 1) / s);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
 }
 
 // Epilogue operands of one call (all null: the plain GEMM).
@@ -248,12 +283,13 @@ int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A,
     const int id = plan - bsg::tc1_num_plans() - bsg::pair_num_plans();
     const int num_n_tiles = (N + pi.bn - 1) / pi.bn;
     const int num_k_blocks = K / pi.k_block;
-    // split K as far as the whole grid stays resident at once: the largest
-    // S in {1, 2, 4, 8}, S <= K/256, whose clusters all fit on the device
-    int splits = 1;
-    for (int s = 2; s <= 8; s *= 2)
-        if (s <= num_k_blocks && num_n_tiles <= skinny_cluster_capacity(id, s))
-            splits = s;
+    const int halves = (M + pi.tile_m - 1) / pi.tile_m;      // activation blocks (1, or 2 for tile_m >= 128)
+    const int forced = g_skinny_splits.load();
+    const int splits = forced > 0 ? forced
+                                  : skinny_splits(id, pi.splits_mask, num_n_tiles * halves, num_k_blocks, ds->sms);
+    if (!(pi.splits_mask & (1 << splits)) || splits > num_k_blocks ||
+        num_n_tiles * halves > skinny_cluster_capacity(id, splits))
+        return BSG_ERR_NO_PLAN;
     const uint64_t row_bytes = (uint64_t)K / 2u;
     GemmMaps maps;
     std::memset(&maps, 0, sizeof maps);
@@ -261,10 +297,7 @@ int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A,
     if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes,
                         128, (uint32_t)pi.tile_m)) != BSG_OK ||
         (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, (uint64_t)N, row_bytes,
-                        128, (uint32_t)pi.bn)) != BSG_OK ||
-        (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, d_rows(M, epi),
-                        (uint64_t)N * 2u, (uint32_t)(pi.bn / splits), (uint32_t)pi.tile_m,
-                        CU_TENSOR_MAP_SWIZZLE_NONE)) != BSG_OK)
+                        128, (uint32_t)pi.bn)) != BSG_OK)
         return rc;
     GemmArgs a;
     std::memset(&a, 0, sizeof a);
@@ -285,7 +318,7 @@ int run_skinny(int plan, const PlanInfo &pi, int M, int N, int K, const void *A,
     a.timeout_ns = g_watchdog_ns.load();
     set_epilogue(a, epi, D);
     a.pdl = g_pdl.load();
-    if (bsg::skinny_launch(id, maps, a, splits, stream) != cudaSuccess)
+    if (bsg::skinny_launch(id, maps, a, splits, halves, stream) != cudaSuccess)
         return BSG_ERR_CUDA;
     ++t_last_launches;
     t_last_plan = pi.name;
@@ -1138,6 +1171,14 @@ int bsg_set_raster_group(int m_tiles)
     if (m_tiles < 0 || m_tiles > 1024)
         return BSG_ERR_INVALID_ARG;
     g_raster_group.store(m_tiles == 0 ? kDefaultRasterGroup : m_tiles);
+    return BSG_OK;
+}
+
+int bsg_set_skinny_splits(int splits)
+{
+    if (splits < 0 || splits > 8 || splits == 7)
+        return BSG_ERR_INVALID_ARG;
+    g_skinny_splits.store(splits);
     return BSG_OK;
 }
 

@@ -87,6 +87,7 @@ struct PlanInfo {
     int threads;
     int tmem_cols;
     int packed = 0;            // 1: reads tile-packed operands (nvfp4_gemm_packed only)
+    int splits_mask = 0;       // skinny plans: bit S set for each K split the kernel takes
 };
 
 // Encoded tensor maps of one call (sfa / sfb only for CTA-pair NVFP4 plans).
@@ -119,8 +120,10 @@ cudaError_t pair_launch(int i, const GemmMaps &maps, const GemmArgs &args, int g
 int pair_max_clusters(int i);
 int skinny_num_plans();
 const PlanInfo &skinny_plan(int i);
-// maps.d: D with a {128 / splits, tile_m} box (no swizzle).
-cudaError_t skinny_launch(int i, const GemmMaps &maps, const GemmArgs &args, int splits,
+// Grid: weight tiles x splits (one cluster of `splits` CTAs per weight tile
+// and activation block) x halves (activation blocks of tile_m rows); maps.d
+// is not read (D is written with plain stores).
+cudaError_t skinny_launch(int i, const GemmMaps &maps, const GemmArgs &args, int splits, int halves,
                           cudaStream_t stream);
 // Thread-block clusters of `splits` CTAs of skinny plan i that fit on the
 // device at once (0 if the query fails).

@@ -1,5 +1,5 @@
-// Skinny-M NVFP4 GEMM (M <= 256 activation rows, large N x K weights): the
-// memory-bound weight-streaming shape of a projection layer.
+// Skinny-M NVFP4 GEMM (up to 2 x 256 activation rows, large N x K weights):
+// the memory-bound weight-streaming shape of a projection layer.
 //
 // A regular 128 x 256 output tiling gives such shapes only ceil(N/256) tiles
 // per 128 rows -- 12 to 48 CTAs on a 152-SM GPU -- and every CTA walks all of
@@ -7,20 +7,23 @@
 // kernel instead
 //   * swaps the operands: it computes D^T = (B * sB)(A * sA)^T, so 128 weight
 //     rows are the MMA's M side and the (padded) activation rows its N side;
-//   * splits K across a thread-block cluster of S CTAs (S in {1, 2, 4, 8},
-//     chosen by the host so that the whole grid is resident at once) so that
-//     (N/128) * S CTAs stream disjoint weight bytes in parallel;
+//     more activation rows than the tile holds (up to two tiles) run as a
+//     third grid dimension, each CTA taking one half of the rows;
+//   * splits K across a thread-block cluster of S CTAs (any S from 1 to 8,
+//     chosen by the host so that the whole grid is resident at once and
+//     fills the SMs) so that (N/128) * S CTAs stream disjoint weight bytes in
+//     parallel;
 //   * reduces the S partial accumulators inside the cluster, with no partials
-//     in HBM and no cluster-wide barrier on the critical path: weight row n of
-//     the tile belongs to CTA n / (128/S). Every CTA pushes the rows it does
-//     not own straight from TMEM into the owner's shared memory (st.async,
-//     16 bytes at a time, each completing bytes on the owner's mbarrier); the
-//     owner sums the S terms of its rows in rank order (deterministic),
-//     stages them as BF16 in shared memory and writes its [M x 128/S] block
-//     of D with one TMA store. The receive area aliases the owner's drained
-//     stage ring, so a sender pushes only after every peer has said that its
-//     ring is free (one relaxed remote arrive per peer once its MMAs have
-//     completed).
+//     in HBM and no cluster-wide barrier on the critical path: the tile's 128
+//     weight rows are cut into 16 groups of 8, CTA o owning groups
+//     [16 o / S, 16 (o + 1) / S). Every CTA pushes the rows it does not own
+//     straight from TMEM into the owner's shared memory (st.async, 16 bytes
+//     at a time, each completing bytes on the owner's mbarrier); the owner
+//     sums the S terms of its rows in rank order (deterministic), stages them
+//     as BF16 and writes its columns of D with 16-byte stores. Where shared
+//     memory is short the receive area aliases the drained stage ring, and a
+//     sender pushes only after every peer has said that its ring is free (one
+//     relaxed remote arrive per peer once its MMAs have completed).
 // The first stages' loads are issued by the initialising thread before the
 // block-wide setup barrier, so HBM latency overlaps TMEM allocation.
 // Everything else follows the persistent 1-SM kernel: TMA producer warp, one
@@ -50,27 +53,41 @@ struct SkinnyTile {
     static constexpr int SFX_BYTES = SFX_CHUNKS * SF_BLOCK_BYTES;
     static constexpr int STAGE_BYTES = W_BYTES + X_BYTES + SFW_BYTES + SFX_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    // receive area: FP32 [sender rank][column / 4][owned row][column % 4]
-    // (S x 128/S = 128 rows): 32 lanes pushing or reading the same 4 columns
-    // of consecutive rows touch 512 consecutive bytes
-    static constexpr int RECV_BYTES = BW * M_PAD * 4;
-    // output staging, BF16 [M_PAD][128/S], placed after the receive area
+    // receive area: FP32 [sender rank][column / 4][owned row][column % 4];
+    // owners hold 8 * ceil(16 / S) rows at most, so S senders fill at most
+    // recv_rows(S) = S * 8 * ceil(16 / S) rows: 128 for S = 1, 2, 4, 8, 144
+    // for S = 3, 6 and 160 for S = 5 (168 for S = 7, never used). The area
+    // holds 160 rows where shared memory allows, else 144 (no S = 5). 32
+    // lanes pushing or reading the same 4 columns of consecutive rows touch
+    // 512 consecutive bytes
+    static constexpr int recv_rows(int S) { return S * 8 * ((16 + S - 1) / S); }
+    // output staging, BF16 [M_PAD][owned rows] (all 128 without a split),
+    // placed after the receive area
     static constexpr int OUT_BYTES = M_PAD * BW * 2;
     static constexpr int NUM_BARS = 3 * STAGES + 4;
     static constexpr int BAR_BYTES = NUM_BARS * 8 + 16;
     // epilogue-variant operands, staged once per CTA: gamma and destination
     // row of the M_PAD activation rows, bias of the tile's BW weight rows
     static constexpr int EPI_BYTES = (2 * M_PAD + BW) * 4;
-    // the receive and staging areas get shared memory of their own when it
-    // fits beside the ring (peers may then push as soon as their own MMAs are
-    // done); otherwise they alias the drained ring and a sender first waits
-    // for every peer to report its ring free
-    static constexpr bool OWN_RECV = 1024 + RING_BYTES + RECV_BYTES + OUT_BYTES + EPI_BYTES + BAR_BYTES <= 232448;
+    // the receive and staging areas get shared memory of their own where it
+    // fits beside the ring (peers may then push as soon as their own MMAs
+    // are done); otherwise they alias the drained ring and a sender first
+    // waits for every peer to report its ring free
+    static constexpr int smem_own(int rows) { return 1024 + RING_BYTES + rows * M_PAD * 4 + OUT_BYTES + EPI_BYTES + BAR_BYTES; }
+    static constexpr int area_alias(int rows)
+    {
+        return RING_BYTES > rows * M_PAD * 4 + OUT_BYTES ? RING_BYTES : rows * M_PAD * 4 + OUT_BYTES;
+    }
+    static constexpr int smem_alias(int rows) { return 1024 + area_alias(rows) + EPI_BYTES + BAR_BYTES; }
+    static constexpr int RECV_ROWS = smem_alias(160) <= 232448 ? 160 : 144;
+    static constexpr int RECV_BYTES = RECV_ROWS * M_PAD * 4;
+    static constexpr bool OWN_RECV = smem_own(RECV_ROWS) <= 232448;
     static constexpr int RECV_OFF = OWN_RECV ? RING_BYTES : 0;
-    static constexpr int AREA = OWN_RECV ? RING_BYTES + RECV_BYTES + OUT_BYTES
-                                         : (RING_BYTES > RECV_BYTES + OUT_BYTES ? RING_BYTES
-                                                                                : RECV_BYTES + OUT_BYTES);
+    static constexpr int AREA = OWN_RECV ? RING_BYTES + RECV_BYTES + OUT_BYTES : area_alias(RECV_ROWS);
     static constexpr int SMEM_BYTES = 1024 + AREA + EPI_BYTES + BAR_BYTES;
+    // split counts the receive area holds (bit S set): S <= 8, S != 7
+    static constexpr int SPLITS_MASK = (1 << 1) | (1 << 2) | (1 << 3) | (1 << 4) | (1 << 6) | (1 << 8) |
+                                       (recv_rows(5) <= RECV_ROWS ? 1 << 5 : 0);
     static constexpr int SCALE_WARPS = 4;
     static constexpr int EPI_WARP0 = 2 + SCALE_WARPS;
     static constexpr int EPI_WARPS = 4;
@@ -84,45 +101,49 @@ struct SkinnyTile {
                                      : TMEM_USED <= 128 ? 128
                                      : TMEM_USED <= 256 ? 256
                                                         : 512;
-    // CTAs per SM the shared memory and TMEM budgets allow (228 KiB and 512
-    // columns per SM, 1 KiB of shared memory reserved per CTA)
-    static constexpr int CTAS_PER_SM = (2 * (SMEM_BYTES + 1024) <= 233472 && 2 * TMEM_COLS <= 512) ? 2 : 1;
     static constexpr uint32_t IDESC = idesc_nvfp4(BW, M_PAD);
 
     static_assert(M_PAD % 32 == 0 && M_PAD >= 32 && M_PAD <= 256, "activation tile");
+    static_assert(RECV_BYTES + OUT_BYTES <= AREA - RECV_OFF, "receive and staging areas");
     static_assert(TMEM_USED <= 512, "TMEM: accumulator plus scales exceed 512 columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KiB");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
 };
 
 // args: num_n_tiles = weight tiles (N/128), num_k_blocks = K/256 (whole K);
-// the split count S is the cluster size (gridDim.y), a power of two <= 8 and
-// <= num_k_blocks.
+// the split count S is the cluster size (gridDim.y): 1 to 6 or 8, and <=
+// num_k_blocks; gridDim.z is the number of M_PAD-row activation blocks.
+
+// First weight row (of the tile's 128) owned by cluster rank o of S: the
+// rows go in 16 groups of 8, rank o taking groups [16 o / S, 16 (o+1) / S).
+__device__ __forceinline__ int skinny_own_lo(int o, int S) { return 8 * ((16 * o) / S); }
+
+// Cluster rank that owns weight row n (the last rank whose first group is
+// at or below n's group).
+__device__ __forceinline__ int skinny_owner(int n, int S) { return (S * ((n >> 3) + 1) - 1) >> 4; }
+
 // The owned block's reduction, spread over the epilogue's threads: item
 // (cq, r) sums columns [4 cq, 4 cq + 4) of owned row r over the S partials in
 // the receive area, in rank order, scales them and stages them as BF16
 // [m][r] (row stride rpo) for the store. EPI: s_bias[r] is the bias of
 // owned row r (an output column), s_gamma[m] the gamma of output row m.
-template <int S, bool EPI>
-__device__ __forceinline__ void reduce_owned(const uint8_t *recv, __nv_bfloat16 *out, int rpo, int live_cols,
-                                             float alpha, int t, int nthreads, const float *s_gamma,
+template <bool EPI>
+__device__ __forceinline__ void reduce_owned(const uint8_t *recv, __nv_bfloat16 *out, int S, int rpo,
+                                             int live_cols, float alpha, int t, int nthreads, const float *s_gamma,
                                              const float *s_bias)
 {
     const int items = (live_cols / 4) * rpo;
     const int slot_bytes = rpo * live_cols * 4;
     for (int idx = t; idx < items; idx += nthreads) {
         const uint8_t *p = recv + idx * 16;          // [cq][r] with r fastest: idx == cq * rpo + r
-        float4 v[S];
-#pragma unroll
-        for (int s = 0; s < S; ++s)
-            v[s] = *reinterpret_cast<const float4 *>(p + s * slot_bytes);
-        float4 a = v[0];
-#pragma unroll
+        float4 a = *reinterpret_cast<const float4 *>(p);
+#pragma unroll 1
         for (int s = 1; s < S; ++s) {
-            a.x += v[s].x;
-            a.y += v[s].y;
-            a.z += v[s].z;
-            a.w += v[s].w;
+            const float4 v = *reinterpret_cast<const float4 *>(p + s * slot_bytes);
+            a.x += v.x;
+            a.y += v.y;
+            a.z += v.z;
+            a.w += v.w;
         }
         const int r = idx % rpo;
         const int m0 = (idx / rpo) * 4;
@@ -143,16 +164,14 @@ __device__ __forceinline__ void reduce_owned(const uint8_t *recv, __nv_bfloat16 
 
 // EPI: the epilogue-variant instantiation (bias, gamma, scattered rows).
 template <int M_PAD, int STAGES, bool EPI>
-__global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
-                                  SkinnyTile<M_PAD, STAGES>::CTAS_PER_SM)
+__global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS, 1)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       const __grid_constant__ CUtensorMap tmD, const GemmArgs args)
+                       const GemmArgs args)
 {
     using T = SkinnyTile<M_PAD, STAGES>;
     if (threadIdx.x == 0) {              // before any parameter read: the descriptor fetches overlap it
         prefetch_tensormap(&tmW);
         prefetch_tensormap(&tmX);
-        prefetch_tensormap(&tmD);
     }
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -183,8 +202,11 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
     const int kb0 = (int)((long long)args.num_k_blocks * split / S);
     const int kb1 = (int)((long long)args.num_k_blocks * (split + 1) / S);
     const int nkb = kb1 - kb0;
-    const int rpo = T::BW / S;                          // weight rows each CTA owns
-    const int live_cols = min(M_PAD, (args.M + 31) / 32 * 32);   // accumulator columns in use
+    const int m_off = blockIdx.z * M_PAD;               // first activation row of this CTA
+    const int m_rows = min(M_PAD, args.M - m_off);      // activation rows it computes (>= 1)
+    const int live_cols = min(M_PAD, (m_rows + 31) / 32 * 32);   // accumulator columns in use
+    const int own_lo = skinny_own_lo((int)rank, S);     // weight rows this CTA owns: [own_lo, own_hi)
+    const int rpo = skinny_own_lo((int)rank + 1, S) - own_lo;
 
     // Producer step i: weights, activations and both scale blocks of k-block
     // kb0 + i into ring stage i % STAGES, all counted on that stage's full
@@ -200,16 +222,17 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
         const uint32_t ssw = sx + T::X_BYTES;
         const uint32_t ssx = ssw + T::SFW_BYTES;
         const uint32_t fb = full0 + 8u * stage;
-        const int nchunks = min(T::SFX_CHUNKS, args.sfx_row_blocks);
+        const int rb0 = m_off / 128;                      // first 128-row scale block of the activations
+        const int nchunks = min(T::SFX_CHUNKS, args.sfx_row_blocks - rb0);
         mbar_arrive_expect_tx(fb, T::W_BYTES + T::X_BYTES + T::SF_BLOCK_BYTES * (1 + nchunks));
         const size_t cb = (size_t)kb * 4u;
-        // weights' scales (row block nt), activations' scales (row blocks 0..)
+        // weights' scales (row block nt), activations' scales (row blocks rb0..)
         bulk_load(ssw, args.sfb + ((size_t)nt * args.sf_col_blocks + cb) * 512u, T::SF_BLOCK_BYTES, fb);
         for (int c = 0; c < nchunks; ++c)
-            bulk_load(ssx + c * T::SF_BLOCK_BYTES, args.sfa + ((size_t)c * args.sf_col_blocks + cb) * 512u,
+            bulk_load(ssx + c * T::SF_BLOCK_BYTES, args.sfa + ((size_t)(rb0 + c) * args.sf_col_blocks + cb) * 512u,
                       T::SF_BLOCK_BYTES, fb);
         tma_load_2d(sw, &tmW, fb, kb * T::ROW_BYTES, nt * T::BW);
-        tma_load_2d(sx, &tmX, fb, kb * T::ROW_BYTES, 0);
+        tma_load_2d(sx, &tmX, fb, kb * T::ROW_BYTES, m_off);
         return true;
     };
 
@@ -312,36 +335,38 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
     } else {
         // ------------------------------------------------------------------
         // Epilogue: TMEM lane n (warp q = n / 32) holds weight row n of the
-        // tile, column m its dot product with activation row m. Receive area:
-        // FP32 [sender rank][column / 4][owned row][column % 4], one slot of
-        // rpo * live_cols floats per rank.
+        // tile, column m its dot product with activation row m_off + m.
+        // Receive area of the owner of rows [lo, lo + rpo): FP32 [sender
+        // rank][column / 4][row - lo][column % 4], one slot of rpo *
+        // live_cols floats per rank.
         // ------------------------------------------------------------------
         const int q = warp & 3;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const int n = q * 32 + lane;
-        const int owner = n / rpo;
-        const int orow = n - owner * rpo;               // row within the owner's share
+        const int owner = skinny_owner(n, S);
+        const int o_lo = skinny_own_lo(owner, S);
+        const int o_rpo = skinny_own_lo(owner + 1, S) - o_lo;
+        const int orow = n - o_lo;                      // row within the owner's share
         const int et = threadIdx.x - 32 * T::EPI_WARP0; // 0 .. 127
         const float alpha = args.alpha;
         uint8_t *const recv = gbase + T::RECV_OFF;
         __nv_bfloat16 *const out = reinterpret_cast<__nv_bfloat16 *>(recv + T::RECV_BYTES);
-        const int own_lo = (int)rank * rpo;             // rows this CTA owns: [own_lo, own_lo + rpo)
         if constexpr (EPI) {
             griddep_wait();
             // the epilogue operands into shared memory while the MMAs run:
             // gamma and destination row (-1: not written) of every
             // activation row, bias of the owned weight rows
             for (int m = et; m < M_PAD; m += 32 * T::EPI_WARPS) {
-                s_gamma[m] = epi_gamma(args, m);
-                int d = m < args.M ? m : -1;
-                if (args.scatter && m < args.M) {
-                    d = __ldg(args.scatter + m);
+                s_gamma[m] = epi_gamma(args, m_off + m);
+                int d = m < m_rows ? m_off + m : -1;
+                if (args.scatter && m < m_rows) {
+                    d = __ldg(args.scatter + m_off + m);
                     d = (d >= 0 && d < args.m_out) ? d : -1;
                 }
                 s_dst[m] = d;
             }
-            for (int r = et; r < T::BW; r += 32 * T::EPI_WARPS)
-                s_bias[r] = epi_bias(args, nt * T::BW + (S > 1 ? own_lo : 0) + r);
+            for (int r = et; r < rpo; r += 32 * T::EPI_WARPS)
+                s_bias[r] = epi_bias(args, nt * T::BW + own_lo + r);
             named_bar_sync(1, 32 * T::EPI_WARPS);
         }
         const bool have = nkb > 0 && warp_wait(tfull, 0, wd, abort_flag, 4, lane);
@@ -376,8 +401,8 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
             }
             // every row of the partial into its owner's slot for this rank:
             // the owned rows locally, the others pushed to their CTA
-            const int slot_bytes = rpo * live_cols * 4;
-            const uint32_t group_bytes = (uint32_t)rpo * 16u;
+            const int slot_bytes = o_rpo * live_cols * 4;
+            const uint32_t group_bytes = (uint32_t)o_rpo * 16u;
             if (have && may_push) {
                 const uint32_t my_slot = smem_u32(recv) + (uint32_t)((int)rank * slot_bytes) + (uint32_t)orow * 16u;
                 const uint32_t dst = mapa_shared(my_slot, (uint32_t)owner);
@@ -391,7 +416,7 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
                     if (owner == (int)rank) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            local[(c0 / 4 + j) * rpo] =
+                            local[(c0 / 4 + j) * o_rpo] =
                                 make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                     } else {
@@ -404,38 +429,26 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
             }
             const bool rows_in = warp_wait(rx, 0, wd, abort_flag, 8, lane);
             named_bar_sync(1, 32 * T::EPI_WARPS);        // the owned rows' local writes
-            if (have && rows_in) {
-                switch (S) {
-                case 2: reduce_owned<2, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, s_gamma, s_bias); break;
-                case 4: reduce_owned<4, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, s_gamma, s_bias); break;
-                default: reduce_owned<8, EPI>(recv, out, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, s_gamma, s_bias); break;
-                }
-            }
+            if (have && rows_in)
+                reduce_owned<EPI>(recv, out, S, rpo, live_cols, alpha, et, 32 * T::EPI_WARPS, s_gamma, s_bias);
         }
-        if (EPI && args.scatter) {
-            // scattered rows: staged row m (128/S BF16) to row scatter[m] of
-            // D, in 16-byte pieces; consecutive threads take consecutive
-            // pieces of one row
-            named_bar_sync(1, 32 * T::EPI_WARPS);
+        // this CTA's [m_rows x rpo] block of D (columns nt * 128 + own_lo ..)
+        // from the BF16 staging (row stride rpo), in 16-byte pieces:
+        // consecutive threads take consecutive pieces of one row; a
+        // scattered row goes to row scatter[m], a dropped one nowhere
+        named_bar_sync(1, 32 * T::EPI_WARPS);
+        if (have) {
             const int pieces = rpo / 8;
             const int col0 = nt * T::BW + own_lo;
-            for (int p = et; p < args.M * pieces; p += 32 * T::EPI_WARPS) {
+            for (int p = et; p < m_rows * pieces; p += 32 * T::EPI_WARPS) {
                 const int m = p / pieces;
                 const int col = col0 + 8 * (p - m * pieces);
-                const int d = s_dst[m];
+                int d = m_off + m;
+                if constexpr (EPI)
+                    d = s_dst[m];
                 if (d >= 0 && col < args.N)
                     *reinterpret_cast<uint4 *>(args.d + (size_t)d * (size_t)args.N + (size_t)col) =
                         *reinterpret_cast<const uint4 *>(out + m * rpo + (col - col0));
-            }
-        } else {
-            // one TMA store of this CTA's [M x 128/S] block of D (rows >= M
-            // and columns >= N are clipped by the tensor map)
-            fence_proxy_async_smem();
-            named_bar_sync(1, 32 * T::EPI_WARPS);
-            if (warp == T::EPI_WARP0 && lane == 0) {
-                tma_store_2d(&tmD, smem_u32(out), nt * T::BW + own_lo, 0);
-                bulk_commit_group();
-                bulk_wait_group_read<0>();   // the staging must outlive the read
             }
         }
     }
@@ -453,7 +466,7 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS,
 // Plans and launchers
 // ---------------------------------------------------------------------------
 template <int M_PAD, int STAGES>
-static cudaError_t skinny_launch_impl(const GemmMaps &maps, const GemmArgs &args, int splits,
+static cudaError_t skinny_launch_impl(const GemmMaps &maps, const GemmArgs &args, int splits, int halves,
                                       cudaStream_t stream)
 {
     using T = SkinnyTile<M_PAD, STAGES>;
@@ -466,7 +479,7 @@ static cudaError_t skinny_launch_impl(const GemmMaps &maps, const GemmArgs &args
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)args.num_n_tiles, (unsigned)splits, 1);
+    cfg.gridDim = dim3((unsigned)args.num_n_tiles, (unsigned)splits, (unsigned)halves);
     cfg.blockDim = dim3(T::THREADS, 1, 1);
     cfg.dynamicSmemBytes = T::SMEM_BYTES;
     cfg.stream = stream;
@@ -479,7 +492,7 @@ static cudaError_t skinny_launch_impl(const GemmMaps &maps, const GemmArgs &args
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = args.pdl ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, kern, maps.b, maps.a, maps.d, args);
+    e = cudaLaunchKernelEx(&cfg, kern, maps.b, maps.a, args);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -519,11 +532,13 @@ static constexpr PlanInfo make_skinny_plan(const char *name)
 {
     using T = SkinnyTile<M_PAD, STAGES>;
     return PlanInfo{name, Kind::NVFP4, Family::SKINNY, 1, M_PAD, T::BW, STAGES, 1, T::K_BLOCK,
-                    T::SMEM_BYTES, T::THREADS, T::TMEM_COLS};
+                    T::SMEM_BYTES, T::THREADS, T::TMEM_COLS, 0, T::SPLITS_MASK};
 }
 
-// activation rows covered (M <= M_PAD), stages; m64_s3 and m128_s3 fit two
-// CTAs per SM
+// activation rows covered per CTA, stages. Kernels that allocate tensor
+// memory were measured to run one CTA per SM whatever their shared memory
+// (the occupancy query gives 1 even for 32 threads and no shared memory),
+// so the 3-stage plans differ from the deeper ones only in ring depth.
 #define BSG_SKINNY_PLANS(X)                                   \
     X(64, 3, "nvfp4_skinny_m64_s3")                           \
     X(64, 6, "nvfp4_skinny_m64_s6")                           \
@@ -538,13 +553,13 @@ int skinny_num_plans() { return (int)(sizeof(kSkinnyPlans) / sizeof(kSkinnyPlans
 
 const PlanInfo &skinny_plan(int i) { return kSkinnyPlans[i]; }
 
-cudaError_t skinny_launch(int id, const GemmMaps &maps, const GemmArgs &args, int splits,
+cudaError_t skinny_launch(int id, const GemmMaps &maps, const GemmArgs &args, int splits, int halves,
                           cudaStream_t stream)
 {
     int i = 0;
 #define BSG_SKINNY_LAUNCH(MP, S, NAME)                                          \
     if (id == i)                                                               \
-        return skinny_launch_impl<MP, S>(maps, args, splits, stream);        \
+        return skinny_launch_impl<MP, S>(maps, args, splits, halves, stream); \
     ++i;
     BSG_SKINNY_PLANS(BSG_SKINNY_LAUNCH)
 #undef BSG_SKINNY_LAUNCH

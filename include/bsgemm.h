@@ -429,6 +429,15 @@ BSG_API int bsg_set_pdl(int on);
  * default of 16. 1 <= m_tiles <= 1024. Process-wide.                       */
 BSG_API int bsg_set_raster_group(int m_tiles);
 
+/* Tuning lever: K splits of the skinny-M kernel (the thread-block cluster
+ * that shares one weight tile) for later launches: 1 to 6 or 8, or 0
+ * (the default) to let each call choose the split whose busiest SM streams
+ * the fewest k-blocks. A forced split that the plan's receive area cannot
+ * hold (5 with 256 activation rows) or that leaves the grid unable to be
+ * resident at once makes those calls return BSG_ERR_NO_PLAN. Process-wide;
+ * BSG_ERR_INVALID_ARG for other values.                                    */
+BSG_API int bsg_set_skinny_splits(int splits);
+
 /* Launch a one-thread probe that waits, with the library's bounded wait, on
  * an mbarrier that nothing ever arrives on. After `ns` nanoseconds it records
  * BSG_ERR_DEVICE_TIMEOUT in the status word and returns: a test of the

@@ -103,9 +103,12 @@ def test_planner_enumeration(lib):
                         assert ("_tc2_" in name) == (M > 128 and N > 128), (M, N, name)
                         continue
                     split = 2 * -(-N // 128) <= sms and K >= 512
-                    if M <= 256 and split and (M <= 128 or K >= 8192):
+                    pair_tiles = -(-M // 256) * -(-N // 256)
+                    if split and (M <= 64 or (M <= 256 and K >= 8192)):
                         mpad = 64 if M <= 64 else 128 if M <= 128 else 256
                         assert name.startswith(f"nvfp4_skinny_m{mpad}_"), (M, N, K, name)
+                    elif 128 < M <= 512 and N > 128 and 4 * pair_tiles >= sms:
+                        assert name == "nvfp4_tc2_256x256_s5_acc1", (M, N, K, name)
                     elif few or N <= 128:
                         want = "tc1_128x128" if (M <= 128 or few) else "tc2_256x128"
                         assert want in name, (M, N, K, name)
@@ -121,7 +124,10 @@ def test_planner_headline_shapes(lib):
     assert bsg.bsg_select_plan(0, 64, 3072, 3072, 152) == "nvfp4_skinny_m64_s6"
     assert bsg.bsg_select_plan(0, 256, 3072, 12288, 152) == "nvfp4_skinny_m256_s4"
     assert bsg.bsg_select_plan(0, 256, 3072, 3072, 152) == "nvfp4_tc1_128x128_s5_acc2"
-    assert bsg.bsg_select_plan(0, 512, 12288, 3072, 152) == "nvfp4_tc1_128x128_s5_acc2"
+    assert bsg.bsg_select_plan(0, 128, 3072, 3072, 152) == "nvfp4_tc1_128x128_s5_acc2"
+    assert bsg.bsg_select_plan(0, 256, 12288, 3072, 152) == "nvfp4_tc2_256x256_s5_acc1"
+    assert bsg.bsg_select_plan(0, 512, 12288, 3072, 152) == "nvfp4_tc2_256x256_s5_acc1"
+    assert bsg.bsg_select_plan(0, 512, 3072, 12288, 152) == "nvfp4_tc1_128x128_s5_acc2"
 
 
 def test_forced_skinny_plan_needs_small_m(lib):
@@ -132,6 +138,22 @@ def test_forced_skinny_plan_needs_small_m(lib):
             bsg.bsg_select_plan(0, 65, 3072, 3072, 152)
     finally:
         bsg.bsg_force_plan(None)
+    bsg.bsg_force_plan("nvfp4_skinny_m256_s4")   # two blocks of 256 activation rows
+    try:
+        assert bsg.bsg_select_plan(0, 512, 3072, 3072, 152) == "nvfp4_skinny_m256_s4"
+        with pytest.raises(bsg.BsgError):
+            bsg.bsg_select_plan(0, 513, 3072, 3072, 152)
+    finally:
+        bsg.bsg_force_plan(None)
+
+
+def test_skinny_splits_lever(lib):
+    for bad in (-1, 7, 9):
+        with pytest.raises(bsg.BsgError) as e:
+            bsg.bsg_set_skinny_splits(bad)
+        assert e.value.code == bsg.BSG_ERR_INVALID_ARG
+    for good in (1, 2, 3, 4, 5, 6, 8, 0):
+        bsg.bsg_set_skinny_splits(good)
 
 
 def test_forced_plan(lib):

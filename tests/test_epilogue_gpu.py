@@ -33,8 +33,8 @@ GUARD = 256
 
 NVFP4_PLANS = ["nvfp4_tc1_128x256_s3_acc1", "nvfp4_tc1_128x128_s5_acc2",
                "nvfp4_tc2_256x256_s5_acc1", "nvfp4_tc2_256x128_s6_acc2"]
-SKINNY_PLANS = {"nvfp4_skinny_m64_s3": 64, "nvfp4_skinny_m64_s6": 64, "nvfp4_skinny_m128_s3": 128,
-                "nvfp4_skinny_m256_s4": 256}
+SKINNY_PLANS = {"nvfp4_skinny_m64_s3": 64, "nvfp4_skinny_m64_s6": 64, "nvfp4_skinny_m128_s3": 256,
+                "nvfp4_skinny_m256_s4": 512}
 FP8_PLANS = ["fp8_tc1_128x256_s4_acc2", "fp8_tc1_128x128_s6_acc2", "fp8_tc2_256x256_s6_acc2"]
 VARIANTS = ["bias", "gamma", "bias_gamma", "scatter", "all", "all_drop"]
 
@@ -152,10 +152,11 @@ def test_nvfp4_epilogue_plans(dev, forced, plan, variant):
 @pytest.mark.parametrize("variant", ["bias_gamma", "all_drop"])
 @pytest.mark.parametrize("plan", list(SKINNY_PLANS))
 @pytest.mark.parametrize("M,N,K", [(1, 136, 256), (37, 392, 1280), (64, 3072, 3072), (200, 520, 4096),
-                                   (100, 1000, 2304)])
+                                   (100, 1000, 2304), (400, 264, 3072)])
 def test_nvfp4_epilogue_skinny(dev, forced, plan, M, N, K, variant):
     """The swap-AB split-K kernel (bias per weight row, gamma and scatter per
-    activation row), over its 1, 2, 4 and 8 K splits."""
+    activation row), over the splits chosen per call and two activation
+    blocks."""
     if M > SKINNY_PLANS[plan]:
         pytest.skip("activation rows exceed the plan's tile")
     bsg.bsg_force_plan(plan)

@@ -343,18 +343,21 @@ def test_nvfp4_skinny_cells(dev, name):
     assert_close(got, ref, T, name)
 
 
-SKINNY_PLANS = {"nvfp4_skinny_m64_s3": 64, "nvfp4_skinny_m64_s6": 64, "nvfp4_skinny_m128_s3": 128,
-                "nvfp4_skinny_m256_s4": 256}
+# activation rows each skinny plan serves: one block of its tile, or two
+# blocks where the tile is whole 128-row scale blocks
+SKINNY_PLANS = {"nvfp4_skinny_m64_s3": 64, "nvfp4_skinny_m64_s6": 64, "nvfp4_skinny_m128_s3": 256,
+                "nvfp4_skinny_m256_s4": 512}
 
 
 @pytest.mark.parametrize("plan", list(SKINNY_PLANS))
 @pytest.mark.parametrize("M,N,K", [(1, 136, 256), (16, 256, 512), (48, 1024, 1024), (37, 392, 1280),
                                    (64, 3072, 3072), (100, 1000, 2304), (256, 520, 4096), (200, 8, 512),
-                                   (64, 16384, 512)])
+                                   (64, 16384, 512), (300, 264, 1536), (512, 392, 1024)])
 def test_nvfp4_skinny_kernel(dev, plan, M, N, K):
     """The swap-AB split-K kernel forced on every shape it can serve: ragged
-    M and N, every cluster size (1, 2, 4 and 8 K splits, some not dividing
-    the k-blocks evenly), and a wide N whose split is capped by residency."""
+    M and N, the split chosen per call (cluster sizes from 1 to 8, some not
+    dividing the k-blocks evenly), a wide N whose split is capped by
+    residency, and two activation blocks (M past the plan's tile)."""
     if M > SKINNY_PLANS[plan]:
         pytest.skip("activation rows exceed the plan's tile")
     bsg.bsg_force_plan(plan)
@@ -416,6 +419,28 @@ def test_fp8_full_size_sampled(dev):
     assert_close(Dh[rows], ref, T, "fp8 8192 rows")
     _, T, ref = oracle.get().fp8_gemm(A, B, q["alpha"], cols=cols)
     assert_close(Dh[:, cols], ref, T, "fp8 8192 cols")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 5, 6, 8])
+@pytest.mark.parametrize("plan,M", [("nvfp4_skinny_m64_s3", 64), ("nvfp4_skinny_m64_s6", 40),
+                                    ("nvfp4_skinny_m128_s3", 200), ("nvfp4_skinny_m256_s4", 384)])
+def test_nvfp4_skinny_every_split(dev, plan, M, splits):
+    """Every cluster size the kernel takes, forced: weight rows owned in 8-row
+    groups, unevenly for 3, 5 and 6 splits; k-blocks (18) split unevenly for
+    4, 5 and 8; two activation blocks for the m128 and m256 plans."""
+    N, K = 392, 4608
+    if plan == "nvfp4_skinny_m256_s4" and splits == 5:
+        pytest.skip("the m256 plan's receive area holds no five-way split")
+    bsg.bsg_force_plan(plan)
+    bsg.bsg_set_skinny_splits(splits)
+    try:
+        p = workloads.make_nvfp4(workloads.WORKLOADS["nvfp4_4096"], "cpu", M=M, N=N, K=K)
+        got = gpu_nvfp4(p, dev)
+    finally:
+        bsg.bsg_set_skinny_splits(0)
+        bsg.bsg_force_plan(None)
+    _, T, ref = oracle_nvfp4(p)
+    assert_close(got, ref, T, f"{plan} S={splits} {M}x{N}x{K}")
 
 
 # ---------------------------------------------------------------------------
