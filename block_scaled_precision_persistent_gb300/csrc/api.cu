@@ -426,9 +426,10 @@ int run_gemm(Kind kind, int M, int N, int K, const void *A, const void *B, const
 }
 
 // Grouped (ragged) NVFP4 GEMM: the 1-SM kernel's grouped instantiation, one
-// 128-row tile row per 128 rows of each slice. The slice table is built on
-// the device from offs, so the grid is sized for the bound on the tile rows,
-// ceil(M/128) + E; CTAs past the actual tiles exit at once.
+// 128-row tile row per 128 rows of each slice, or the CTA pair's (above).
+// The slice table is built on the device from offs, so the grid is sized
+// for the bound on the tile rows, ceil(M/128) + E; CTAs past the actual
+// tiles exit at once.
 // True for the dense (NVFP4 x 16-bit) plans the grouped GEMM runs: A staged
 // in TMEM, and room beside the ring for the slice table.
 static bool grouped_dense_plan(const PlanInfo &pi)
@@ -436,6 +437,74 @@ static bool grouped_dense_plan(const PlanInfo &pi)
     const size_t n = std::strlen(pi.name);
     return pi.kind == Kind::NVFP4_BF16 && pi.family == bsg::Family::TC1 && n > 6 &&
            std::strcmp(pi.name + n - 6, "_tmema") == 0 && pi.smem_bytes + bsg::kGroupTableBytes <= 232448;
+}
+
+// The grouped mode of the CTA pair (NVFP4, up to kPairMaxGroups slices):
+// one 256-row pair tile row per 256 rows of each slice, so the ~128-row
+// slices of a routed MoE layer stream each weight tile once, half into each
+// SM of the pair. Grid: the bound ceil(M/256) + E on the tile rows.
+bool grouped_pair_plan(const PlanInfo &pi, int E)
+{
+    return E <= bsg::kPairMaxGroups && std::strcmp(pi.name, "nvfp4_tc2_256x256_s5_acc1") == 0;
+}
+
+int run_grouped_pair(int plan, int E, int M, int N, int K, const void *A, const uint8_t *sfa, const void *B,
+                     const uint8_t *sfb, const int32_t *offs, float alpha, const Epilogue &epi, void *D,
+                     cudaStream_t stream, DeviceState *ds)
+{
+    const PlanInfo &pi = bsg::plan_info(plan);
+    const long long pt_bound = (long long)(M + 255) / 256 + E;
+    const uint64_t row_bytes = (uint64_t)K / 2u;
+    const uint64_t nrb = ((uint64_t)N + 127u) / 128u;       // 128-row scale blocks of one slice's weights
+    const size_t sfa_bytes = ((size_t)(M + 127) / 128u + (size_t)E) * 128u * ((size_t)(K / 16 + 3) / 4u * 4u);
+    GemmMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    int rc;
+    if ((rc = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, (uint64_t)M, row_bytes, 128,
+                        128u)) != BSG_OK ||
+        (rc = encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, (uint64_t)E * (uint64_t)N,
+                        row_bytes, 128, (uint32_t)(pi.bn / 2))) != BSG_OK ||
+        (rc = encode_2d(&maps.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, d_rows(M, epi),
+                        (uint64_t)N * 2u, 64, 32)) != BSG_OK ||
+        // the per-slice swizzled A scales as 256-byte rows; the E slices'
+        // swizzled weight scales as one 3-D view whose row blocks run
+        // through all slices (slice e's first block is e * nrb)
+        (rc = encode_2d(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, sfa, 256, sfa_bytes / 256u, 256, 256, 8,
+                        CU_TENSOR_MAP_SWIZZLE_NONE)) != BSG_OK ||
+        (rc = encode_3d(&maps.sfb, sfb, 256, (uint64_t)K / 32u, (uint64_t)E * nrb, 256, (uint64_t)K / 32u * 256u,
+                        256, 8, 2)) != BSG_OK)
+        return rc;
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.num_m_tiles = (int)pt_bound;      // bound only: the kernel counts the slices' tile rows
+    a.num_n_tiles = (N + pi.bn - 1) / pi.bn;
+    a.num_k_blocks = K / pi.k_block;
+    a.raster_group = g_raster_group.load();
+    a.sf_col_blocks = (K / 16 + 3) / 4;
+    a.sfb_row_blocks = (int)nrb;
+    a.sfa = sfa;
+    a.sfb = sfb;
+    a.alpha = alpha;
+    a.status = ds->status;
+    a.timeout_ns = g_watchdog_ns.load();
+    set_epilogue(a, epi, D);
+    a.num_groups = E;
+    a.group_offs = offs;
+    a.sfb_group_bytes = swizzled_bytes(N, K);
+    a.pdl = g_pdl.load();
+    const long long ctas = pt_bound * a.num_n_tiles * 2;
+    const int resident = bsg::max_resident_ctas(plan, ds->sms);
+    if (resident < 2)
+        return BSG_ERR_CUDA;
+    const int grid = (int)(ctas < resident ? ctas : resident);
+    if (bsg::launch_gemm(plan, maps, a, grid, stream) != cudaSuccess)
+        return BSG_ERR_CUDA;
+    ++t_last_launches;
+    t_last_plan = pi.name;
+    return BSG_OK;
 }
 
 // dense: the right-hand sides are 16-bit (BF16, or FP16 with b_f16) [E][N][K]
@@ -451,12 +520,24 @@ int run_grouped(int E, int M, int N, int K, const void *A, const uint8_t *sfa, c
     }
     if (plan >= 0) {
         const PlanInfo &fp = bsg::plan_info(plan);
+        if (!dense && grouped_pair_plan(fp, E))
+            return run_grouped_pair(plan, E, M, N, K, A, sfa, B, sfb, offs, alpha, epi, D, stream, ds);
         if (dense ? !grouped_dense_plan(fp) : (fp.kind != Kind::NVFP4 || fp.family != bsg::Family::TC1))
             return BSG_ERR_NO_PLAN;
     } else {
-        // 128-wide tiles while they number at most 4 per SM, else 256-wide
+        // 128-wide tiles while they number at most 4 per SM; beyond that,
+        // NVFP4 slices go to the CTA pair's 256-row tile rows (up to its
+        // slice bound; on the 64-expert MoE workload 8 % faster than the
+        // 1-SM 128 x 256 tiles, which give a slice of 129..256 rows a
+        // second tile row that streams its weights again), else 256-wide
+        // 1-SM tiles
         const long long tiles128 = mt_bound * (long long)((N + 127) / 128);
         const bool few = tiles128 <= 4LL * ds->sms;
+        if (!dense && !few && N > 128 && E <= bsg::kPairMaxGroups) {
+            plan = bsg::find_plan("nvfp4_tc2_256x256_s5_acc1");
+            if (plan >= 0)
+                return run_grouped_pair(plan, E, M, N, K, A, sfa, B, sfb, offs, alpha, epi, D, stream, ds);
+        }
         plan = bsg::find_plan(dense ? (few ? "nvfp4bf16_tc1_128x128_s8_acc2_tmema" : "nvfp4bf16_tc1_128x256_s5_acc1_tmema")
                                     : (few ? "nvfp4_tc1_128x128_s5_acc2" : "nvfp4_tc1_128x256_s3_acc1"));
         if (plan < 0)

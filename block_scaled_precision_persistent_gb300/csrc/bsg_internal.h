@@ -90,6 +90,10 @@ struct PlanInfo {
     int splits_mask = 0;       // skinny plans: bit S set for each K split the kernel takes
 };
 
+// Most slices the CTA-pair plan's grouped mode takes (its slice table sits
+// in the shared memory left beside the ring).
+constexpr int kPairMaxGroups = 256;
+
 // Encoded tensor maps of one call (sfa / sfb only for CTA-pair NVFP4 plans).
 struct GemmMaps {
     CUtensorMap a, b, d, sfa, sfb;

@@ -31,6 +31,7 @@
 // barriers; both epilogues arrive on the leader's accumulator-empty barrier.
 #include "bsg_internal.h"
 #include "gemm_common.cuh"
+#include "group.cuh"
 #include "ptx.cuh"
 
 namespace bsg {
@@ -112,12 +113,21 @@ struct PairTile {
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned (128B swizzle)");
 };
 
+// Grouped (routed MoE) mode of the pair: one 256-row pair tile row per 256
+// rows of each slice, so a slice of up to 256 rows is one tile row whose
+// weight tile each CTA streams half of. The slice table (boundaries, first
+// 128-row scale block and first pair tile row of every slice) sits beside
+// the barriers; it bounds the slices to kPairMaxGroups (bsg_internal.h).
+constexpr int kPairGroupTableBytes = 3 * (kPairMaxGroups + 1) * 4;
+
 // EPI: the epilogue-variant instantiation (bias, gamma, scattered rows).
+// GROUPED: the grouped GEMM over ragged row slices (with the variants'
+// epilogue; NVFP4 256-wide tiles).
 // PACKED: A and B arrive as tile-packed operands, one 16 KiB bulk copy per
 // CTA, tile and stage (a copy of contiguous bytes takes operands into an SM
 // faster than a tensor-map box of 128 rows); each CTA's copies complete on
 // its own barrier, and the peer's warp 1 relays their arrival to the leader.
-template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool EPI, bool PACKED = false>
+template <Kind KIND, int BN, int STAGES, int NUM_ACC, bool EPI, bool PACKED = false, bool GROUPED = false>
 __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
@@ -126,6 +136,9 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
                      const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args)
 {
     using T = PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>;
+    static_assert(!GROUPED || (EPI && T::kFp4 && BN == 256 && !PACKED &&
+                               T::SMEM_BYTES + kPairGroupTableBytes <= 232448),
+                  "grouped pair: NVFP4 256-wide tiles with room for the slice table");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -143,6 +156,11 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
     const uint32_t pfull0 = bar0 + 8u * T::BAR_PFULL;        // [STAGES] PACKED: own operand tiles (peer)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // grouped: slice boundaries, first 128-row block and first pair tile row
+    // of each slice (group.cuh)
+    int *const s_go = reinterpret_cast<int *>(tmem_slot + 4);
+    int *const s_gb = s_go + (kPairMaxGroups + 1);
+    int *const s_gp = s_gb + (kPairMaxGroups + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -184,6 +202,13 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
         tmem_alloc_pair(smem_u32(tmem_slot), T::TMEM_COLS);
         tmem_relinquish_pair();
     }
+    if constexpr (GROUPED) {
+        if (warp == 2) {
+            griddep_wait();      // the offsets may come from the previous grid
+            build_group_table(args.group_offs, args.num_groups, args.M, s_go, s_gb, lane);
+            build_block_prefix(s_go, args.num_groups, T::TILE_M, s_gp, lane);
+        }
+    }
     tc_fence_before_sync();
     __syncthreads();
     cluster_sync_all();          // both CTAs' barriers exist before any remote use
@@ -192,13 +217,31 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
     if (threadIdx.x == 0)
         griddep_launch_dependents();
     const uint32_t tmem = *tmem_slot;
-    const int num_tiles = args.num_m_tiles * args.num_n_tiles;
+    // grouped: one pair tile row per 256 rows of each slice
+    const int num_m_tiles = GROUPED ? s_gp[args.num_groups] : args.num_m_tiles;
+    const int num_tiles = num_m_tiles * args.num_n_tiles;
     const int nkb = args.num_k_blocks;
     const bool b_f16 = args.b_f16 != 0;   // dense kind: B (and the expanded A) are FP16, not BF16
     const int cluster_id = blockIdx.x / T::CLUSTER;
     const int num_clusters = gridDim.x / T::CLUSTER;
     auto tile_coords = [&](int tile, int &pm, int &nt) {
-        raster_tile(tile, args.raster_group, args.num_m_tiles, args.num_n_tiles, pm, nt);
+        raster_tile(tile, args.raster_group, num_m_tiles, args.num_n_tiles, pm, nt);
+    };
+    // pair tile row pm -> its slice g, first row of A, end of the slice's
+    // rows and first 128-row block of the (per-slice) swizzled A scales
+    auto pair_rows = [&](int pm, int &g, int &row0, int &row_end, int &ablk0) {
+        if constexpr (GROUPED) {
+            g = group_of_block(s_gp, args.num_groups, pm);
+            const int t = pm - s_gp[g];
+            row0 = s_go[g] + t * T::TILE_M;
+            row_end = s_go[g + 1];
+            ablk0 = s_gb[g] + 2 * t;
+        } else {
+            g = 0;
+            row0 = pm * T::TILE_M;
+            row_end = args.M;
+            ablk0 = 2 * pm;
+        }
     };
 
     if (warp == 0) {
@@ -210,8 +253,16 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
             uint32_t phase = 0;
             bool ok = true;
             for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
-                int pm, nt;
+                int pm, nt, g, row0, row_end, ablk0;
                 tile_coords(tile, pm, nt);
+                pair_rows(pm, g, row0, row_end, ablk0);
+                // grouped: a CTA whose 128 rows all lie past its slice loads
+                // no A and no A scales (its rows are never stored); B comes
+                // from the slice's own weights
+                const bool a_in = !GROUPED || row0 + (int)rank * T::BM < row_end;
+                const bool peer_a_in = !GROUPED || row0 + T::BM < row_end;
+                const int b_row0 = (GROUPED ? g * args.N : 0) + nt * BN + (int)rank * T::B_ROWS;
+                const int sfb_blk0 = (GROUPED ? g * args.sfb_row_blocks : 0) + nt * T::SFB_CHUNKS;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wd, abort_flag, 1)) {
                         ok = false;
@@ -226,14 +277,15 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
                         // 256-byte rows of the swizzled scale layout: a stage is
                         // the 8 rows starting at (row_block * ncb + 4 kb) * 2.
                         const uint32_t sfb = sffull0 + 8u * stage;
-                        mbar_arrive_expect_tx(sfb, T::SFA_BYTES + T::SFB_BYTES);
+                        mbar_arrive_expect_tx(sfb, (a_in ? T::SFA_BYTES : 0) + T::SFB_BYTES);
                         const uint32_t ssfa = sb + T::B_BYTES;
-                        const int rba = 2 * pm + (int)rank;
-                        tma_load_2d(ssfa, &tmSFA, sfb, 0, (rba * args.sf_col_blocks + 4 * kb) * 2);
+                        const int rba = ablk0 + (int)rank;
+                        if (a_in)
+                            tma_load_2d(ssfa, &tmSFA, sfb, 0, (rba * args.sf_col_blocks + 4 * kb) * 2);
                         // all SFB_CHUNKS 128-row blocks of B's scales in one
                         // copy: a 3-D view (256-byte rows, rows of a row block,
                         // row blocks), box 8 rows x SFB_CHUNKS row blocks
-                        tma_load_3d(ssfa + T::SFA_BYTES, &tmSFB, sfb, 0, 8 * kb, nt * T::SFB_CHUNKS);
+                        tma_load_3d(ssfa + T::SFA_BYTES, &tmSFB, sfb, 0, 8 * kb, sfb_blk0);
                     }
                     if constexpr (T::kDense) {
                         // this CTA's codes and scales on its own expansion
@@ -270,11 +322,14 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
                             bulk_load(sb, args.b_packed + ((size_t)rbb * nkb + kb) * 16384u, T::B_BYTES, own);
                     } else {
                         if (leader)
-                            mbar_arrive_expect_tx(full0 + 8u * stage, 2u * (T::A_BYTES + T::B_BYTES));
-                        tma_load_2d_pair(sa, &tmA, fb, kb * T::ROW_BYTES, pm * T::TILE_M + (int)rank * T::BM);
+                            mbar_arrive_expect_tx(full0 + 8u * stage, (a_in ? T::A_BYTES : 0) +
+                                                                          (peer_a_in ? T::A_BYTES : 0) +
+                                                                          2u * T::B_BYTES);
+                        if (a_in)
+                            tma_load_2d_pair(sa, &tmA, fb, kb * T::ROW_BYTES, row0 + (int)rank * T::BM);
                     }
                     if constexpr (!PACKED)
-                        tma_load_2d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, nt * BN + (int)rank * T::B_ROWS);
+                        tma_load_2d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, b_row0);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -490,13 +545,19 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
-            int pm, nt;
+            int pm, nt, g, row0, row_end, ablk0;
             tile_coords(tile, pm, nt);
+            pair_rows(pm, g, row0, row_end, ablk0);
             const int x0 = nt * BN + h * COLS_PER_WARP;            // first column of this warp
+            const int y = row0 + (int)rank * T::BM + q * 32;       // first row of this warp's 32
+            // grouped: a slice's own bias; rows of the warp that TMA could
+            // store past the slice's end go one by one (as scattered rows)
+            const float *const bias = (GROUPED && args.bias) ? args.bias + (size_t)g * args.N : args.bias;
+            const bool per_row = EPI && (args.scatter || (GROUPED && y + 32 > row_end));
             RowEpi re{1.0f, -1};
             if constexpr (EPI) {
-                re = load_row_epi(args, pm * T::TILE_M + (int)rank * T::BM + q * 32 + lane, args.M);
-                prefetch_bias(args.bias, args.N, x0, COLS_PER_WARP, lane);
+                re = load_row_epi(args, y + lane, row_end);
+                prefetch_bias(bias, args.N, x0, COLS_PER_WARP, lane);
             }
             if (!warp_wait(tfull0 + 8u * acc, acc_phase, wd, abort_flag, 4, lane))
                 break;
@@ -512,7 +573,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
             auto convert_chunk = [&](int ch, const uint32_t (&v0)[32], const uint32_t (&v1)[32],
                                      uint32_t (&pk)[32]) {
                 if constexpr (EPI) {
-                    convert64_epi(v0, v1, pk, scale, re, args, args.bias, x0 + ch * T::EPI_COLS);
+                    convert64_epi(v0, v1, pk, scale, re, args, bias, x0 + ch * T::EPI_COLS);
                 } else {
                     convert32(v0, pk, scale);
                     convert32(v1, pk + 16, scale);
@@ -538,10 +599,9 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
             };
             auto store_chunk = [&](int ch, uint32_t sbuf) {
                 const int x = x0 + ch * T::EPI_COLS;
-                if (EPI && args.scatter) {
+                if (per_row) {
                     scatter_chunk(gbase + (sbuf - base), re.dst, args.d, args.N, x, lane);
                 } else if (lane == 0) {
-                    const int y = pm * T::TILE_M + (int)rank * T::BM + q * 32;
                     if (x < args.N && y < args.M)
                         tma_store_2d(&tmD, sbuf, x, y);
                     bulk_commit_group();
@@ -631,14 +691,23 @@ static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, 
     using T = PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>;
     auto kern = has_epilogue(args) ? gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, true, PACKED>
                                    : gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, false, PACKED>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         T::SMEM_BYTES);
+    int smem = T::SMEM_BYTES;
+    if (args.group_offs) {
+        // the grouped instantiation: the 5-stage NVFP4 256-wide plan only
+        if constexpr (KIND == Kind::NVFP4 && BN == 256 && STAGES == 5 && !PACKED) {
+            kern = gemm_pair_kernel<KIND, BN, STAGES, NUM_ACC, true, PACKED, true>;
+            smem += kPairGroupTableBytes;
+        } else {
+            return cudaErrorInvalidValue;
+        }
+    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(T::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = T::SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

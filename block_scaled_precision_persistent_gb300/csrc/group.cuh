@@ -70,6 +70,34 @@ __device__ __forceinline__ void build_group_table(const int *offs, int E, int M,
     __syncwarp();
 }
 
+// After build_group_table: one warp fills, for the boundaries so[0..E],
+//   sp[e] = sum_{e' < e} ceil((so[e'+1] - so[e']) / rows)   e = 0..E
+// the first block of `rows` rows of slice e (the CTA pair's 256-row tile
+// rows). The caller synchronises before other warps read.
+__device__ __forceinline__ void build_block_prefix(const int *so, int E, int rows, int *sp, int lane)
+{
+    const int n = E + 1;
+    const int per = (n + 31) / 32;
+    const int lo = min(lane * per, n), hi = min(lo + per, n);
+    int sum = 0;
+    for (int i = max(lo, 1); i < hi; ++i)
+        sum += (so[i] - so[i - 1] + rows - 1) / rows;
+    int isum = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, isum, d);
+        if (lane >= d)
+            isum += v;
+    }
+    int run = isum - sum;
+    for (int i = lo; i < hi; ++i) {
+        if (i >= 1)
+            run += (so[i] - so[i - 1] + rows - 1) / rows;
+        sp[i] = run;
+    }
+    __syncwarp();
+}
+
 // The slice that block row b (0 <= b < sb[E]) belongs to: the largest e with
 // sb[e] <= b (empty slices share their sb with the next one and are skipped).
 __device__ __forceinline__ int group_of_block(const int *sb, int E, int b)

@@ -310,7 +310,10 @@ BSG_API int nvfp4_dense_f16_gemm(int M, int N, int K, const void *A, const void 
  *             unspecified.
  *   bias    : DEVICE float[E][N], 16-byte aligned, or NULL
  * 1 <= E <= 1024 slices; slices may be empty. Sizes, alignment and errors as
- * nvfp4_gemm_ex. One launch; allocates nothing.
+ * nvfp4_gemm_ex. One launch; allocates nothing. Plans: with many tiles and
+ * E <= 256, the CTA pair with one 256-row tile row per 256 rows of a slice;
+ * otherwise the 1-SM plans with 128-row tile rows. A forced CTA-pair plan
+ * with E > 256 gives BSG_ERR_NO_PLAN.
  * ------------------------------------------------------------------------- */
 BSG_API int nvfp4_grouped_gemm(int E, int M, int N, int K,
                                const void *A, const void *sfA_swz,

@@ -7,7 +7,9 @@ routed rows form slices, each multiplied by its own right-hand side. The
 per-slice scale swizzle is compared bit for bit. The GEMM is compared
 element by element under the GEMM tolerance on ragged splits: empty slices,
 slices of a few rows, slices that end inside a warp's 32 rows or cross 128-row
-tiles, ragged N, both 1-SM plans, and the epilogue variants (a bias per
+tiles, ragged N, both 1-SM plans and the CTA pair's grouped mode (256-row
+tile rows, a peer CTA whose rows lie past its slice loading no A), and the
+epilogue variants (a bias per
 slice, gamma, and the scatter back to token order). Rows of D that no row
 names keep their prefill. The hand-worked case of
 tests/golden/nvfp4_grouped_case.txt is checked exactly, and the MoE workload
@@ -31,7 +33,7 @@ pytestmark = pytest.mark.gpu
 GOLDEN = Path(__file__).resolve().parent / "golden"
 SENTINEL = 0x7FC1
 GUARD = 256
-PLANS = [None, "nvfp4_tc1_128x128_s5_acc2", "nvfp4_tc1_128x256_s3_acc1"]
+PLANS = [None, "nvfp4_tc1_128x128_s5_acc2", "nvfp4_tc1_128x256_s3_acc1", "nvfp4_tc2_256x256_s5_acc1"]
 
 
 @pytest.fixture(scope="module")
@@ -199,10 +201,10 @@ def test_grouped_worked_case(dev):
         assert got[int(r[0]), :2].tolist() == [float(v) for v in r[1:]], ("D", r[0], got[int(r[0])])
 
 
-@pytest.mark.parametrize("plan", ["nvfp4_tc1_128x128_s5_acc2", "nvfp4_tc1_128x256_s3_acc1"])
+@pytest.mark.parametrize("plan", ["nvfp4_tc1_128x128_s5_acc2", "nvfp4_tc1_128x256_s3_acc1", "nvfp4_tc2_256x256_s5_acc1"])
 def test_single_slice_matches_plain_gemm(dev, forced, plan):
-    """One slice over every row: the grouped kernel equals the plain 1-SM
-    kernel of the same plan bit for bit (zeros compared without sign)."""
+    """One slice over every row: the grouped kernel equals the plain kernel
+    of the same plan bit for bit (zeros compared without sign)."""
     M, N, K = 520, 392, 2048
     bsg.bsg_force_plan(plan)
     p = workloads.make_grouped(1, M, N, K, seed=11)
@@ -218,10 +220,24 @@ def test_single_slice_matches_plain_gemm(dev, forced, plan):
     assert np.array_equal(nz(got), nz(bits(D)))
 
 
-def test_moe_workload_sampled(dev):
+def test_grouped_pair_slice_bound(dev, forced):
+    """The pair's grouped mode takes at most 256 slices: forced beyond that,
+    the call is refused before any launch."""
+    E, N, K = 257, 136, 256
+    offs = offsets([1] * E)
+    p = workloads.make_grouped(E, E, N, K, seed=3)
+    bsg.bsg_force_plan("nvfp4_tc2_256x256_s5_acc1")
+    with pytest.raises(bsg.BsgError) as e:
+        gpu_grouped(p, offs, dev)
+    assert e.value.code == bsg.BSG_ERR_NO_PLAN
+
+
+@pytest.mark.parametrize("plan", [None, "nvfp4_tc2_256x256_s5_acc1"])
+def test_moe_workload_sampled(dev, forced, plan):
     """64 experts, 1024 tokens x top-8 (8192 routed rows), 4096 x 7168, in the
     launch configuration the benchmark times, with the scatter back to token
     order: sampled rows of every slice against the oracle."""
+    bsg.bsg_force_plan(plan)
     w = workloads.GROUPED_WORKLOADS["moe_e64_t1024_k8"]
     offs, dst = workloads.routing(w.E, w.tokens, w.top_k, seed=1)
     p = workloads.make_grouped(w.E, w.M, w.N, w.K, seed=1, device=dev)     # 0.94 GB of weights
