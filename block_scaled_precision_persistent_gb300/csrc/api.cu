@@ -110,8 +110,10 @@ size_t swizzled_bytes(int rows, int K)
 // x N 3072 / 12288 x K 3072 / 12288, cold L2) and the square sizes:
 //   * NVFP4, the swap-AB split-K kernel when the weight tiles leave room to
 //     split K at least in two with the whole grid resident (N/128 tiles x 2
-//     <= SMs): for M <= 64, and up to 256 activation rows for long K
-//     (>= 8192), where streaming the weights dominates its fixed costs;
+//     <= SMs): for M <= 64 (the 3-stage ring up to K = 4096, where a CTA
+//     streams a few k-blocks, else the 6-stage one), and up to 256
+//     activation rows for long K (>= 8192), where streaming the weights
+//     dominates its fixed costs;
 //   * 129..512 activation rows with 256 x 256 pair tiles enough to give
 //     every SM a quarter of one (M/256 x N/256 x 4 >= SMs): the CTA pair,
 //     whose tile moves half the bytes per FLOP of a 1-SM 128 x 128 tile;
@@ -129,7 +131,8 @@ int default_plan(Kind kind, int M, int N, int K, int num_sms)
         const bool can_split = 2 * weight_tiles <= num_sms && K >= 512;
         const long long pair_tiles = (long long)((M + 255) / 256) * (long long)((N + 255) / 256);
         if (can_split && (M <= 64 || (M <= 256 && K >= 8192)))
-            name = M <= 64 ? "nvfp4_skinny_m64_s6" : M <= 128 ? "nvfp4_skinny_m128_s3" : "nvfp4_skinny_m256_s4";
+            name = M <= 64 ? (K <= 4096 ? "nvfp4_skinny_m64_s3" : "nvfp4_skinny_m64_s6")
+                           : M <= 128 ? "nvfp4_skinny_m128_s3" : "nvfp4_skinny_m256_s4";
         else if (M > 128 && M <= 512 && N > 128 && 4 * pair_tiles >= num_sms)
             name = "nvfp4_tc2_256x256_s5_acc1";
         else if (few_tiles || N <= 128)

@@ -121,7 +121,8 @@ def test_planner_headline_shapes(lib):
     # the shapes the benchmarks time
     assert bsg.bsg_select_plan(0, 16384, 16384, 16384, 152) == "nvfp4_tc2_256x256_s5_acc1"
     assert bsg.bsg_select_plan(1, 8192, 8192, 8192, 152) == "fp8_tc2_256x256_s6_acc2"
-    assert bsg.bsg_select_plan(0, 64, 3072, 3072, 152) == "nvfp4_skinny_m64_s6"
+    assert bsg.bsg_select_plan(0, 64, 3072, 3072, 152) == "nvfp4_skinny_m64_s3"
+    assert bsg.bsg_select_plan(0, 64, 3072, 12288, 152) == "nvfp4_skinny_m64_s6"
     assert bsg.bsg_select_plan(0, 256, 3072, 12288, 152) == "nvfp4_skinny_m256_s4"
     assert bsg.bsg_select_plan(0, 256, 3072, 3072, 152) == "nvfp4_tc1_128x128_s5_acc2"
     assert bsg.bsg_select_plan(0, 128, 3072, 3072, 152) == "nvfp4_tc1_128x128_s5_acc2"
