@@ -585,7 +585,7 @@ def bf16_times_vectors(d_bits, x, chunk_rows: int = 1024):
     return z, abs_sum, sq_sum, nonfinite
 
 
-def freivalds_verdict(d_bits, x, rhs) -> dict:
+def freivalds_outcome(d_bits, x, rhs) -> dict:
     """Decide Freivalds' check of the GPU result d_bits (BF16 bits [M, N])
     against the oracle's right-hand side rhs (from nvfp4_freivalds /
     fp8_freivalds with the same x). Returns a dict with 'ok' (both bounds

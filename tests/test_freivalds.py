@@ -32,7 +32,7 @@ def case():
 
 
 def test_accepts_the_oracle_result(case):
-    v = oracle.freivalds_verdict(case["D"], case["x"], case["rhs"])
+    v = oracle.freivalds_outcome(case["D"], case["x"], case["rhs"])
     assert v["ok"], v
     assert v["worst_hoeffding"] < 0.5
 
@@ -47,7 +47,7 @@ def test_accepts_errors_inside_the_tolerance(case):
     moved = np.where((D & 0x7FFF) != 0, D + step, D).astype(np.uint16)
     assert oracle.within_tolerance(moved, case["D"], case["T"]).all()
     assert (moved != case["D"]).mean() > 0.99
-    v = oracle.freivalds_verdict(moved, case["x"], case["rhs"])
+    v = oracle.freivalds_outcome(moved, case["x"], case["rhs"])
     assert v["ok"], v
 
 
@@ -59,7 +59,7 @@ def test_rejects_one_flipped_exponent_bit(case):
     cand = np.argwhere((np.abs(ref) >= 8.0) & ((D & (1 << 10)) == 0))
     i, j = cand[len(cand) // 2]
     D[i, j] ^= np.uint16(1 << 10)
-    v = oracle.freivalds_verdict(D, case["x"], case["rhs"])
+    v = oracle.freivalds_outcome(D, case["x"], case["rhs"])
     assert not v["ok"] and not v["ok_summed"] and not v["ok_hoeffding"], v
     assert all(row == i for _, row in v["fails"])
 
@@ -71,7 +71,7 @@ def test_rejects_two_swapped_blocks(case):
     a = D[64:96, 0:32].copy()
     D[64:96, 0:32] = D[64:96, 256:288]
     D[64:96, 256:288] = a
-    v = oracle.freivalds_verdict(D, case["x"], case["rhs"])
+    v = oracle.freivalds_outcome(D, case["x"], case["rhs"])
     assert not v["ok_hoeffding"], v
     assert {row for _, row in v["fails"]} <= set(range(64, 96))
 
@@ -85,7 +85,7 @@ def test_rejects_a_dropped_k_block():
     bad = oracle.Oracle(defines=("BSO_MUTANT_DROP_LAST_BLOCK",))
     _, _, D = bad.nvfp4_gemm(*ops, p["alpha"], 512)
     x = oracle.rademacher(4, 256, seed=9)
-    v = oracle.freivalds_verdict(D, x, oracle.get().nvfp4_freivalds(*ops, p["alpha"], 512, x))
+    v = oracle.freivalds_outcome(D, x, oracle.get().nvfp4_freivalds(*ops, p["alpha"], 512, x))
     assert not v["ok_hoeffding"], v
 
 
@@ -96,14 +96,14 @@ def test_rejects_a_transposed_operand():
     bad = oracle.Oracle(defines=("BSO_MUTANT_TRANSPOSE_B",))
     _, _, D = bad.nvfp4_gemm(*ops, p["alpha"], 512)
     x = oracle.rademacher(4, 256, seed=10)
-    v = oracle.freivalds_verdict(D, x, oracle.get().nvfp4_freivalds(*ops, p["alpha"], 512, x))
+    v = oracle.freivalds_outcome(D, x, oracle.get().nvfp4_freivalds(*ops, p["alpha"], 512, x))
     assert not v["ok"], v
 
 
 def test_rejects_a_nan(case):
     D = case["D"].copy()
     D[5, 7] = 0x7FC1
-    v = oracle.freivalds_verdict(D, case["x"], case["rhs"])
+    v = oracle.freivalds_outcome(D, case["x"], case["rhs"])
     assert not v["ok"] and not v["finite"]
 
 
@@ -114,12 +114,12 @@ def test_fp8_accepts_and_rejects():
     _, _, D = oracle.get().fp8_gemm(A, B, p["alpha"])
     x = oracle.rademacher(4, 256, seed=11)
     rhs = oracle.get().fp8_freivalds(A, B, p["alpha"], x)
-    assert oracle.freivalds_verdict(D, x, rhs)["ok"]
+    assert oracle.freivalds_outcome(D, x, rhs)["ok"]
     D2 = D.copy()
     D2[100:132, 64:96] = D[100:132, 96:128]
-    assert not oracle.freivalds_verdict(D2, x, rhs)["ok_hoeffding"]
+    assert not oracle.freivalds_outcome(D2, x, rhs)["ok_hoeffding"]
 
 
 def test_rejects_vectors_that_are_not_signs(case):
     with pytest.raises(ValueError):
-        oracle.freivalds_verdict(case["D"], case["x"] * 2, case["rhs"])
+        oracle.freivalds_outcome(case["D"], case["x"] * 2, case["rhs"])

@@ -7,7 +7,7 @@ oracle (hours at 16384^3), so:
 
   * Freivalds' check covers every element: D x against alpha Adeq (Bdeq^T x)
     for four random +-1 vectors x, with the summed per-element bound and the
-    sharper Hoeffding bound (oracle.freivalds_verdict);
+    sharper Hoeffding bound (oracle.freivalds_outcome);
   * eight whole 256 x 256 output tiles are compared element by element with
     the oracle: the first and the last, both sides of a rasterisation-group
     boundary (at the first and the last N tile), and both sides of the
@@ -69,7 +69,7 @@ def _bits(t):
 
 
 def _check(D_bits, rhs, x, tile_ref, what):
-    v = oracle.freivalds_verdict(D_bits, x, rhs)
+    v = oracle.freivalds_outcome(D_bits, x, rhs)
     assert v["finite"], f"{what}: non-finite outputs"
     assert v["ok_summed"], f"{what}: Freivalds summed bound exceeded (worst ratio {v['worst_summed']:.3g})"
     assert v["ok_hoeffding"], (f"{what}: Freivalds Hoeffding bound exceeded (worst ratio "
