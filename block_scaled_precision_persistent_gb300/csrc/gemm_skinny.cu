@@ -136,15 +136,21 @@ __device__ __forceinline__ void reduce_owned(const uint8_t *recv, __nv_bfloat16 
     const int slot_bytes = rpo * live_cols * 4;
     for (int idx = t; idx < items; idx += nthreads) {
         const uint8_t *p = recv + idx * 16;          // [cq][r] with r fastest: idx == cq * rpo + r
-        float4 a = *reinterpret_cast<const float4 *>(p);
-#pragma unroll 1
-        for (int s = 1; s < S; ++s) {
-            const float4 v = *reinterpret_cast<const float4 *>(p + s * slot_bytes);
-            a.x += v.x;
-            a.y += v.y;
-            a.z += v.z;
-            a.w += v.w;
-        }
+        // the S (<= 8) partials' loads all in flight, then summed in rank order
+        float4 v[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (s < S)
+                v[s] = *reinterpret_cast<const float4 *>(p + s * slot_bytes);
+        float4 a = v[0];
+#pragma unroll
+        for (int s = 1; s < 8; ++s)
+            if (s < S) {
+                a.x += v[s].x;
+                a.y += v[s].y;
+                a.z += v[s].z;
+                a.w += v[s].w;
+            }
         const int r = idx % rpo;
         const int m0 = (idx / rpo) * 4;
         if constexpr (EPI) {
