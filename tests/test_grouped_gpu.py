@@ -220,6 +220,18 @@ def test_single_slice_matches_plain_gemm(dev, forced, plan):
     assert np.array_equal(nz(got), nz(bits(D)))
 
 
+def test_grouped_pair_most_slices(dev, forced):
+    """The pair's slice table at its bound: 256 slices of 0 to 5 rows (about
+    a third empty), ragged N, against the oracle."""
+    sizes = [(7 * e) % 6 for e in range(256)]
+    offs = offsets(sizes)
+    E, M, N, K = 256, int(offs[-1]), 136, 512
+    bsg.bsg_force_plan("nvfp4_tc2_256x256_s5_acc1")
+    p = workloads.make_grouped(E, M, N, K, seed=256)
+    got = gpu_grouped(p, offs, dev)
+    check(got, p, offs, None, None, None, M, "pair, 256 slices")
+
+
 def test_grouped_pair_slice_bound(dev, forced):
     """The pair's grouped mode takes at most 256 slices: forced beyond that,
     the call is refused before any launch."""
