@@ -211,7 +211,11 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
     }
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync_all();          // both CTAs' barriers exist before any remote use
+    // both CTAs' barriers exist before any remote use: thread 0's
+    // fence.mbarrier_init.release.cluster orders its initialisations before
+    // its (relaxed) cluster arrival
+    cluster_arrive_relaxed();
+    cluster_wait();
     tc_fence_after_sync();
     griddep_wait();              // a dependent launch: the previous grid's writes are visible
     if (threadIdx.x == 0)
