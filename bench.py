@@ -222,6 +222,8 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r[0] for r in use), "sm_max_mhz": self.max_mhz,
                 "sm_mhz_min_under_load": min(r[0] for r in use), "reasons": reasons,
                 "samples": len(self.rows), "samples_under_load": len(loaded), "power_w_max": round(pmax, 1),
+                "power_note": "the driver's averaged board power (about a 1 s window): a burst shorter than "
+                              "that reads low; the clock samples are instantaneous",
                 "source": self.backend}
 
 
