@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -915,8 +916,30 @@ def cpu_baseline(w: workloads.Workload, p_host: dict, budget_s: float = 15.0) ->
     flops = 2.0 * len(sel) * w.N * w.K
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(sel)} of {w.M} output rows x all {w.N} columns, K={w.K} "
-                      f"({dt:.1f} s of CPU work)", "seconds": dt,
+                      f"({dt:.1f} s of CPU work)", "seconds": dt, "cpu": host_cpu(),
             "full_matrix_seconds_extrapolated": round(dt * w.M / len(sel), 1)}
+
+
+def host_cpu() -> dict:
+    """The host's CPU as /proc/cpuinfo names it (x86: "model name"; Arm:
+    implementer and part codes), its online CPU count and the CPUs this
+    process may run on."""
+    model = None
+    ids = {}
+    try:
+        for line in Path("/proc/cpuinfo").read_text().splitlines():
+            k, _, v = line.partition(":")
+            k, v = k.strip(), v.strip()
+            if k == "model name" and not model:
+                model = v
+            elif k in ("CPU implementer", "CPU part") and k not in ids:
+                ids[k] = v
+    except OSError:
+        pass
+    if not model and ids:
+        model = "implementer {} part {}".format(ids.get("CPU implementer", "?"), ids.get("CPU part", "?"))
+    return {"model": model or platform.processor() or platform.machine(), "nproc": os.cpu_count(),
+            "affinity": len(os.sched_getaffinity(0))}
 
 
 def cpu_configs() -> dict:
@@ -1122,7 +1145,7 @@ def run_reference(args, dist: Dist) -> None:
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K},
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu": host_cpu()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
