@@ -1099,6 +1099,10 @@ def run_ours(args, dist: Dist) -> None:
         summary["swizzle_frac_hbm"] = secondary["swizzle"]["frac_hbm"]
     if "grouped" in secondary:
         summary["moe_frac_hbm"] = secondary["grouped"]["variants"]["scatter"]["frac_hbm"]
+    if "packed" in secondary and "us" in secondary["packed"]:
+        pu = secondary["packed"]["us"]
+        summary.update(packed_gemm_graph_us=pu["packed"], row_major_gemm_graph_us=pu["tensor_map"],
+                       packed_frac_9pf=round(w.flops / (pu["packed"] * 1e-6) / 1e12 / 9000.0, 4))
     if e2e is not None:
         summary.update(e2e_tflops=round(e2e["value"], 1),
                        e2e_frac_of_copy_bound=e2e["host_link"]["frac_of_copy_bound"])
