@@ -70,6 +70,19 @@ __device__ __forceinline__ uint32_t e4m3_code2(float a, float b)
     return lo == hi ? lo : 0x100u;
 }
 
+// (d0, d1) = (a0 * b, a1 * b), each rounded to nearest: one paired FP32
+// multiply
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float b, float &d0, float &d1)
+{
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %4};\n\t"
+        "mul.rn.f32x2 pd, pa, pb;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b));
+}
+
 // approximate reciprocal (within one unit in the last place)
 __device__ __forceinline__ float rcp_approx(float v)
 {
@@ -249,10 +262,8 @@ __global__ void __launch_bounds__(kQThreads)
                     for (int j = 0; j < 4; ++j) {
                         const float xa = bf16_bits_to_float(w[4 * h + j] & 0xFFFFu);
                         const float xb = __uint_as_float(w[4 * h + j] & 0xFFFF0000u);
-                        lo[2 * j] = xa * k_lo;
-                        lo[2 * j + 1] = xb * k_lo;
-                        hi[2 * j] = xa * k_hi;
-                        hi[2 * j + 1] = xb * k_hi;
+                        mul2_rn(xa, xb, k_lo, lo[2 * j], lo[2 * j + 1]);
+                        mul2_rn(xa, xb, k_hi, hi[2 * j], hi[2 * j + 1]);
                     }
                     uint32_t c = e2m1_pack8(lo);
                     const uint32_t ch = e2m1_pack8(hi);
