@@ -256,6 +256,12 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            // A's row panels and their scales are re-read by the later tiles
+            // of the raster group (its M tiles sweep every N tile), so they
+            // are kept in L2 first; B's panels, read by the group's M tiles
+            // one after another, keep the default policy (evict-first for
+            // them measured 0.7 % slower)
+            const uint64_t pol_a = l2_policy_evict_last();
             for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
                 int pm, nt, g, row0, row_end, ablk0;
                 tile_coords(tile, pm, nt);
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
                         const uint32_t ssfa = sb + T::B_BYTES;
                         const int rba = ablk0 + (int)rank;
                         if (a_in)
-                            tma_load_2d(ssfa, &tmSFA, sfb, 0, (rba * args.sf_col_blocks + 4 * kb) * 2);
+                            tma_load_2d_hint(ssfa, &tmSFA, sfb, 0, (rba * args.sf_col_blocks + 4 * kb) * 2, pol_a);
                         // all SFB_CHUNKS 128-row blocks of B's scales in one
                         // copy: a 3-D view (256-byte rows, rows of a row block,
                         // row blocks), box 8 rows x SFB_CHUNKS row blocks
@@ -330,7 +336,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
                                                                           (peer_a_in ? T::A_BYTES : 0) +
                                                                           2u * T::B_BYTES);
                         if (a_in)
-                            tma_load_2d_pair(sa, &tmA, fb, kb * T::ROW_BYTES, row0 + (int)rank * T::BM);
+                            tma_load_2d_pair_hint(sa, &tmA, fb, kb * T::ROW_BYTES, row0 + (int)rank * T::BM, pol_a);
                     }
                     if constexpr (!PACKED)
                         tma_load_2d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, b_row0);
@@ -548,6 +554,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
         }
         int acc = 0;
         uint32_t acc_phase = 0;
+        const uint64_t pol_d = l2_policy_evict_first();
         for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
             int pm, nt, g, row0, row_end, ablk0;
             tile_coords(tile, pm, nt);
@@ -607,7 +614,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
                     scatter_chunk(gbase + (sbuf - base), re.dst, args.d, args.N, x, lane);
                 } else if (lane == 0) {
                     if (x < args.N && y < args.M)
-                        tma_store_2d(&tmD, sbuf, x, y);
+                        tma_store_2d_hint(&tmD, sbuf, x, y, pol_d);   // D is not read again here
                     bulk_commit_group();
                 }
             };
