@@ -52,6 +52,12 @@ struct PairTile {
     static constexpr int MMA_K_BYTES = 32;
     static constexpr int MMAS = ROW_BYTES / MMA_K_BYTES;
     static constexpr int B_ROWS = BN / 2;                 // B rows held by each CTA
+    // FP8 tiles 512 wide: two pair MMAs of N = 256 per K step, into
+    // accumulator columns [0, 256) and [256, 512); each CTA holds 128 B rows
+    // of each N half (one 3-D copy of 2 x 128 rows), the whole accumulator
+    // filling TMEM (no block scales in this kind)
+    static constexpr bool kWideN = BN == 512;
+    static constexpr int MMA_N = kWideN ? 256 : BN;
     static constexpr int A_BYTES = kDense ? 0 : BM * ROW_BYTES;
     static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
     static constexpr int APK_BYTES = kDense ? BM * 32 : 0;   // dense: this CTA's codes (128 rows x 32 bytes)
@@ -69,10 +75,10 @@ struct PairTile {
     // drain overlapped) and 128-wide tiles use one.
     // (dense: 4, since its eight expansion warps would otherwise leave too
     // few registers per thread for the epilogue variants)
-    static constexpr int EPI_WARPS = (kFp4 && BN == 256) ? 8 : 4;
+    static constexpr int EPI_WARPS = ((kFp4 && BN == 256) || kWideN) ? 8 : 4;
     static constexpr int EPI_COLS = 64;
     static constexpr int EPI_CHUNKS = BN * 4 / EPI_WARPS / EPI_COLS;   // 64-column chunks per warp (2 or 4)
-    static constexpr int EPI_BUFS = EPI_CHUNKS == 2 ? 1 : 2;           // 4 KiB staging buffers per warp
+    static constexpr int EPI_BUFS = (EPI_CHUNKS == 2 || kWideN) ? 1 : 2;   // 4 KiB staging buffers per warp
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
     // mbarrier layout (8 bytes each): full, empty per stage; full, empty per
@@ -102,10 +108,11 @@ struct PairTile {
                                      : TMEM_USED <= 256 ? 256
                                                         : 512;
     static constexpr uint32_t IDESC =
-        kFp4 ? idesc_nvfp4(TILE_M, BN) : kDense ? idesc_bf16(TILE_M, BN) : idesc_fp8(TILE_M, BN);
+        kFp4 ? idesc_nvfp4(TILE_M, BN) : kDense ? idesc_bf16(TILE_M, BN) : idesc_fp8(TILE_M, MMA_N);
     static constexpr uint32_t IDESC_F16 = idesc_f16(TILE_M, BN);   // dense kind with FP16 B
 
-    static_assert(BN % 128 == 0 && BN <= 256, "pair tile N: B halves of 64 or 128 rows");
+    static_assert(BN % 128 == 0 && (BN <= 256 || (BN == 512 && KIND == Kind::FP8 && NUM_ACC == 1 && !PACKED)),
+                  "pair tile N: B halves of 64 or 128 rows, or FP8 tiles of two 256-wide halves");
     static_assert(!PACKED || (kFp4 && BN == 256 && A_BYTES == 16384 && B_BYTES == 16384),
                   "tile-packed operands: NVFP4 256-wide pairs, one 16 KiB tile of A and of B per CTA and stage");
     static_assert(TMEM_USED <= 512, "TMEM: accumulators plus scales exceed 512 columns");
@@ -338,7 +345,12 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
                         if (a_in)
                             tma_load_2d_pair_hint(sa, &tmA, fb, kb * T::ROW_BYTES, row0 + (int)rank * T::BM, pol_a);
                     }
-                    if constexpr (!PACKED)
+                    if constexpr (T::kWideN)
+                        // rows nt * 512 + h * 256 + rank * 128 .. + 128 of
+                        // both halves h: a 3-D view (k bytes, rows of a half,
+                        // halves), one copy into two 16 KiB tiles
+                        tma_load_3d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, (int)rank * 128, 2 * nt);
+                    else if constexpr (!PACKED)
                         tma_load_2d_pair(sb, &tmB, fb, kb * T::ROW_BYTES, b_row0);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -403,10 +415,15 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
                                                  (kb | j) != 0 ? 1u : 0u);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < T::MMAS; ++j)
+                        for (int j = 0; j < T::MMAS; ++j) {
                             mma_fp8_pair(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
                                          desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                          (kb | j) != 0 ? 1u : 0u);
+                            if constexpr (T::kWideN)
+                                mma_fp8_pair(d_tmem + (uint32_t)T::MMA_N, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
+                                             desc_kmajor_sw128(sb + T::B_BYTES / 2 + T::MMA_K_BYTES * j), idesc,
+                                             (kb | j) != 0 ? 1u : 0u);
+                        }
                     }
                     // frees the stage in both CTAs
                     tc_commit_pair_multicast(empty0 + 8u * stage, 0x3);
@@ -664,7 +681,7 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
                             release();
                         convert_chunk(ch, v0, v1, pk);
                     }
-                    const uint32_t sbuf = ebuf + (uint32_t)(ch & 1) * T::EPI_BUF_BYTES;
+                    const uint32_t sbuf = ebuf + (uint32_t)(T::EPI_BUFS == 2 ? (ch & 1) : 0) * T::EPI_BUF_BYTES;
                     stage_out(pk, sbuf);
                     store_chunk(ch, sbuf);
                 }
@@ -782,7 +799,8 @@ static constexpr PlanInfo make_pair_plan(const char *name)
     X(Kind::NVFP4, 256, 3, 1, false, "nvfp4_tc2_256x256_s3_acc1")         \
     X(Kind::FP8, 256, 4, 2, false, "fp8_tc2_256x256_s4_acc2")             \
     X(Kind::NVFP4_BF16_TMEM, 256, 8, 1, false, "nvfp4bf16_tc2_256x256_s8_acc1_tmema") \
-    X(Kind::NVFP4, 256, 5, 1, true, "nvfp4_tc2_256x256_s5_acc1_packed")
+    X(Kind::NVFP4, 256, 5, 1, true, "nvfp4_tc2_256x256_s5_acc1_packed") \
+    X(Kind::FP8, 512, 4, 1, false, "fp8_tc2_256x512_s4_acc1")
 
 #define BSG_PAIR_INFO(K, BN, S, A, PK, NAME) make_pair_plan<K, BN, S, A, PK>(NAME),
 static const PlanInfo kPairPlans[] = {BSG_PAIR_PLANS(BSG_PAIR_INFO)};

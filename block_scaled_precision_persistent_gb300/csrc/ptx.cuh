@@ -531,6 +531,18 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, uint32
                  : "memory");
 }
 
+// 3-D tiled load, CTA-pair form of tma_load_2d_pair (completion on the
+// leader's barrier).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int x, int y, int z)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 // TMEM allocation for a CTA pair: one warp of EACH CTA executes these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
 {

@@ -120,7 +120,9 @@ def test_planner_enumeration(lib):
 def test_planner_headline_shapes(lib):
     # the shapes the benchmarks time
     assert bsg.bsg_select_plan(0, 16384, 16384, 16384, 152) == "nvfp4_tc2_256x256_s5_acc1"
-    assert bsg.bsg_select_plan(1, 8192, 8192, 8192, 152) == "fp8_tc2_256x256_s6_acc2"
+    assert bsg.bsg_select_plan(1, 8192, 8192, 8192, 152) == "fp8_tc2_256x512_s4_acc1"
+    assert bsg.bsg_select_plan(1, 8192, 8448, 8192, 152) == "fp8_tc2_256x256_s6_acc2"   # N not whole 512s
+    assert bsg.bsg_select_plan(1, 128, 8192, 8192, 152) == "fp8_tc1_128x256_s4_acc2"
     assert bsg.bsg_select_plan(0, 64, 3072, 3072, 152) == "nvfp4_skinny_m64_s3"
     assert bsg.bsg_select_plan(0, 64, 3072, 12288, 152) == "nvfp4_skinny_m64_s6"
     assert bsg.bsg_select_plan(0, 256, 3072, 12288, 152) == "nvfp4_skinny_m256_s4"

@@ -177,6 +177,19 @@ def test_fp8_epilogue_plans(dev, forced, plan, variant):
     check(got, "fp8", q, bias, gamma, scatter, m_out, f"{plan} {variant}")
 
 
+@pytest.mark.parametrize("variant", ["bias_gamma", "all", "all_drop"])
+def test_fp8_epilogue_wide_plan(dev, forced, variant):
+    """The 512-wide FP8 pair plan (eight epilogue warps of 256 columns, one
+    staging buffer each): N = 768 leaves the second tile's upper half past N."""
+    M, N, K = 300, 768, 1024
+    bsg.bsg_force_plan("fp8_tc2_256x512_s4_acc1")
+    q = workloads.make_fp8(workloads.WORKLOADS["fp8_8192"], "cpu", M=M, N=N, K=K)
+    bias, gamma, scatter, m_out = variant_inputs(variant, M, N, seed=7, bias_std=out_std(K))
+    got = run_gpu("fp8", q, dev, bias, gamma, scatter, m_out)
+    assert bsg.bsg_last_plan_name() == "fp8_tc2_256x512_s4_acc1"
+    check(got, "fp8", q, bias, gamma, scatter, m_out, f"fp8 wide {variant}")
+
+
 def test_epilogue_worked_case(dev):
     """tests/golden/nvfp4_epilogue_case.txt on the GPU, exactly: K padded
     from 16 to 256 with zero codes (the sums do not change) and N from 4 to

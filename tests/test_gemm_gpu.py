@@ -395,6 +395,42 @@ def test_fp8_parity(dev, fp8_plan, M, N, K):
     assert_close(got, ref, T, f"fp8 {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (300, 768, 1024), (520, 1024, 2048), (1, 512, 128)])
+def test_fp8_wide_pair_plan(dev, M, N, K):
+    """The 512-wide FP8 pair plan (each CTA's 128 rows of both 256-row B
+    halves in one 3-D copy, two N = 256 MMAs per K step into one accumulator
+    that fills TMEM): oracle parity, and bit for bit the 256-wide pair plan,
+    since every output accumulates over K in the same order. N = 768 leaves
+    the second tile's upper half past N (zero-filled, not stored)."""
+    q = workloads.make_fp8(workloads.WORKLOADS["fp8_8192"], "cpu", M=M, N=N, K=K)
+    got = {}
+    for plan in ("fp8_tc2_256x512_s4_acc1", "fp8_tc2_256x256_s6_acc2"):
+        bsg.bsg_force_plan(plan)
+        try:
+            got[plan] = gpu_fp8(q, dev)
+            assert bsg.bsg_last_plan_name() == plan
+        finally:
+            bsg.bsg_force_plan(None)
+    assert np.array_equal(got["fp8_tc2_256x512_s4_acc1"], got["fp8_tc2_256x256_s6_acc2"])
+    _, T, ref = oracle.get().fp8_gemm(q["A"].numpy(), q["B"].numpy(), q["alpha"])
+    assert_close(got["fp8_tc2_256x512_s4_acc1"], ref, T, f"fp8 wide {M}x{N}x{K}")
+
+
+def test_fp8_wide_pair_plan_needs_whole_halves(dev):
+    """Forced with N not a multiple of 256, the 512-wide plan (whose B view
+    tiles N in 256-row halves) is refused before any launch."""
+    q = workloads.make_fp8(workloads.WORKLOADS["fp8_8192"], "cpu", M=256, N=520, K=256)
+    flat, D = new_out(256, 520, dev)
+    bsg.bsg_force_plan("fp8_tc2_256x512_s4_acc1")
+    try:
+        rc = bsg.load().fp8_gemm(256, 520, 256, q["A"].to(dev).data_ptr(), None, q["B"].to(dev).data_ptr(), None,
+                                 q["alpha"], D.data_ptr(), None)
+    finally:
+        bsg.bsg_force_plan(None)
+    assert rc == bsg.BSG_ERR_NO_PLAN
+    assert bsg.bsg_last_launch_count() == 0
+
+
 def test_fp8_device_scales(dev):
     """alpha * sA * sB with sA, sB read from device memory."""
     q = workloads.make_fp8(workloads.WORKLOADS["fp8_8192"], "cpu", M=256, N=384, K=512)
