@@ -293,9 +293,11 @@ def bsg_set_watchdog_ns(ns: int) -> None:
     _check(load().bsg_set_watchdog_ns(ns), "bsg_set_watchdog_ns")
 
 
-def bsg_set_pdl(on: bool) -> None:
-    """Programmatic dependent launch for later GEMM launches (off by default)."""
-    _check(load().bsg_set_pdl(1 if on else 0), "bsg_set_pdl")
+def bsg_set_pdl(on: "bool | int") -> None:
+    """Programmatic dependent launch for later GEMM launches (off by default):
+    False/0 off, True/1 on, 2 on with B's codes read before the wait for the
+    previous kernel (the caller promises that kernel does not write them)."""
+    _check(load().bsg_set_pdl(int(on)), "bsg_set_pdl")
 
 
 def bsg_set_raster_group(m_tiles: int) -> None:

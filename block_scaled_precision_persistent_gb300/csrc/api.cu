@@ -1261,7 +1261,7 @@ int bsg_set_watchdog_ns(uint64_t ns)
 
 int bsg_set_pdl(int on)
 {
-    if (on != 0 && on != 1)
+    if (on < 0 || on > 2)
         return BSG_ERR_INVALID_ARG;
     g_pdl.store(on);
     return BSG_OK;

@@ -59,8 +59,10 @@ struct GemmArgs {
     // NVFP4 x dense kind: B holds FP16 values (A is expanded to FP16 and the
     // MMA runs kind::f16 with F16 operands) instead of BF16
     int b_f16;
-    // host only: launch with programmatic stream serialisation (the kernel's
-    // prologue may overlap the previous kernel on the stream)
+    // launch with programmatic stream serialisation (the kernel's prologue
+    // may overlap the previous kernel on the stream): 0 off, 1 on, 2 on and
+    // B's codes are not written by the previous kernel, so the skinny-M and
+    // 1-SM kernels start reading their first k-blocks of B before waiting
     int pdl;
 };
 

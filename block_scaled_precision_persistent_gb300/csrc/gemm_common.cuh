@@ -29,6 +29,11 @@ __device__ __forceinline__ void raster_tile(int tile, const GemmArgs &a, int &mt
     raster_tile(tile, a.raster_group, a.num_m_tiles, a.num_n_tiles, mt, nt);
 }
 
+// k-blocks of the first tile's B that a 1-SM dependent launch whose B is not
+// written by the previous kernel (GemmArgs::pdl == 2) warms in L2 before it
+// waits for that kernel.
+constexpr int kEarlyKBlocks = 8;
+
 // Bounded wait with no status side effect, used only while draining.
 __device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity,
                                                 unsigned long long limit_ns)

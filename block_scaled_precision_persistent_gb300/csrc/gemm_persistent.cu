@@ -164,6 +164,17 @@ __global__ void __launch_bounds__(Tile<KIND, BN, STAGES, NUM_ACC>::THREADS, 1)
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
         prefetch_tensormap(&tmD);
+        if constexpr (!GROUPED && !KGROUPED) {
+            // B not written by the previous kernel: warm L2 with the first
+            // tile's B while that kernel finishes
+            if (args.pdl == 2 && (int)blockIdx.x < args.num_m_tiles * args.num_n_tiles) {
+                int mt, nt;
+                raster_tile((int)blockIdx.x, args, mt, nt);
+                const int nkb = min(args.num_k_blocks, kEarlyKBlocks);
+                for (int kb = 0; kb < nkb; ++kb)
+                    tma_prefetch_2d(&tmB, kb * T::ROW_BYTES, nt * BN);
+            }
+        }
     }
     __syncwarp();
     if (warp == 1) {

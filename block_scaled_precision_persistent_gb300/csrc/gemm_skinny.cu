@@ -118,6 +118,9 @@ struct SkinnyTile {
 // rows go in 16 groups of 8, rank o taking groups [16 o / S, 16 (o+1) / S).
 __device__ __forceinline__ int skinny_own_lo(int o, int S) { return 8 * ((16 * o) / S); }
 
+// Parts of one producer step (see the producer in gemm_skinny_kernel).
+constexpr int kStepAll = 0, kStepWeights = 1, kStepRest = 2;
+
 // Cluster rank that owns weight row n (the last rank whose first group is
 // at or below n's group).
 __device__ __forceinline__ int skinny_owner(int n, int S) { return (S * ((n >> 3) + 1) - 1) >> 4; }
@@ -216,11 +219,14 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS, 1)
 
     // Producer step i: weights, activations and both scale blocks of k-block
     // kb0 + i into ring stage i % STAGES, all counted on that stage's full
-    // barrier (the scale writers wait on it too).
-    auto produce = [&](int i) -> bool {
+    // barrier (the scale writers wait on it too). `part`: the whole step
+    // (kStepAll), or split around the wait for the previous grid when the
+    // weights' codes are not written by it -- the barrier armed and the
+    // weights' codes first (kStepWeights), the rest after (kStepRest).
+    auto produce = [&](int i, int part) -> bool {
         const int stage = i % STAGES;
         const uint32_t phase = (uint32_t)(i / STAGES) & 1u;
-        if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wd, abort_flag, 1))
+        if (part != kStepRest && !mbar_wait(empty0 + 8u * stage, phase ^ 1u, wd, abort_flag, 1))
             return false;
         const int kb = kb0 + i;
         const uint32_t sw = base + stage * T::STAGE_BYTES;
@@ -230,14 +236,21 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS, 1)
         const uint32_t fb = full0 + 8u * stage;
         const int rb0 = m_off / 128;                      // first 128-row scale block of the activations
         const int nchunks = min(T::SFX_CHUNKS, args.sfx_row_blocks - rb0);
-        mbar_arrive_expect_tx(fb, T::W_BYTES + T::X_BYTES + T::SF_BLOCK_BYTES * (1 + nchunks));
+        if (part != kStepRest) {
+            mbar_arrive_expect_tx(fb, T::W_BYTES + T::X_BYTES + T::SF_BLOCK_BYTES * (1 + nchunks));
+            if (part == kStepWeights) {
+                tma_load_2d(sw, &tmW, fb, kb * T::ROW_BYTES, nt * T::BW);
+                return true;
+            }
+        }
         const size_t cb = (size_t)kb * 4u;
         // weights' scales (row block nt), activations' scales (row blocks rb0..)
         bulk_load(ssw, args.sfb + ((size_t)nt * args.sf_col_blocks + cb) * 512u, T::SF_BLOCK_BYTES, fb);
         for (int c = 0; c < nchunks; ++c)
             bulk_load(ssx + c * T::SF_BLOCK_BYTES, args.sfa + ((size_t)(rb0 + c) * args.sf_col_blocks + cb) * 512u,
                       T::SF_BLOCK_BYTES, fb);
-        tma_load_2d(sw, &tmW, fb, kb * T::ROW_BYTES, nt * T::BW);
+        if (part == kStepAll)
+            tma_load_2d(sw, &tmW, fb, kb * T::ROW_BYTES, nt * T::BW);
         tma_load_2d(sx, &tmX, fb, kb * T::ROW_BYTES, m_off);
         return true;
     };
@@ -256,9 +269,25 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS, 1)
         mbar_init(rx, 1);
         *abort_flag = 0;
         fence_mbar_init();               // initialised barriers: visible to the TMA unit and the peers
-        griddep_wait();                  // a dependent launch: the previous grid's writes are visible
-        for (int i = 0; i < first && producing; ++i)
-            producing = produce(i);
+        if (args.pdl == 2) {
+            // the weights' codes are not written by the previous grid: the
+            // first stages' codes into the ring while it finishes (warming
+            // L2 with later k-blocks too measured slower when the previous
+            // grid streams weights of its own); their scales may be written
+            // by it (a scale swizzle launched just before), so they wait
+            // with the activations
+            int armed = 0;
+            while (armed < first && producing)
+                if ((producing = produce(armed, kStepWeights)))
+                    ++armed;
+            griddep_wait();
+            for (int i = 0; i < armed; ++i)
+                produce(i, kStepRest);
+        } else {
+            griddep_wait();              // a dependent launch: the previous grid's writes are visible
+            for (int i = 0; i < first && producing; ++i)
+                producing = produce(i, kStepAll);
+        }
         griddep_launch_dependents();     // the whole grid is resident: the next launch may set up
         if (S > 1)                       // the peers' rows, pushed with complete_tx
             mbar_arrive_expect_tx(rx, (uint32_t)((S - 1) * rpo * live_cols * 4));
@@ -278,7 +307,7 @@ __global__ void __launch_bounds__(SkinnyTile<M_PAD, STAGES>::THREADS, 1)
     if (warp == 0) {
         if (lane == 0)
             for (int i = first; i < nkb && producing; ++i)
-                producing = produce(i);
+                producing = produce(i, kStepAll);
     } else if (warp == 1) {
         // ------------------------------------------------------------------
         // MMA issuer

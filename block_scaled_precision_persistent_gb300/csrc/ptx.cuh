@@ -110,6 +110,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// Warm L2 with one box of a 2-D tensor map: no shared memory, no barrier,
+// nothing to wait for (a box past the tensor's edge reads nothing).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled load global -> shared; completion counted in bytes on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                             int x, int y)

@@ -423,7 +423,14 @@ BSG_API int bsg_set_watchdog_ns(uint64_t ns);
  * allocation, descriptor prefetch) may then overlap the end of the previous
  * kernel on the same stream; every kernel still waits for that kernel's
  * completion before its first dependent global access, so results do not
- * change. Process-wide.                                                    */
+ * change. 2: on, and the caller promises that the previous kernel on the
+ * stream does not write B's codes (the weights of an inference chain whose
+ * previous kernel produced the activations): the skinny-M kernel then loads
+ * its first ring stages of B's codes, and the 1-SM tile kernel warms L2 with
+ * the first k-blocks of its first tile's B codes, before that wait. B's
+ * scales, A and everything else still wait; the other kernels behave as
+ * with 1. A chain that breaks the promise reads stale weights. Returns
+ * BSG_ERR_INVALID_ARG for other values. Process-wide.                      */
 BSG_API int bsg_set_pdl(int on);
 
 /* Tuning lever: M tiles per rasterisation group of the tile kernels (the

@@ -159,6 +159,14 @@ def test_skinny_splits_lever(lib):
         bsg.bsg_set_skinny_splits(good)
 
 
+def test_pdl_lever(lib):
+    for bad in (-1, 3):
+        assert lib.bsg_set_pdl(bad) == bsg.BSG_ERR_INVALID_ARG
+    for good in (2, True, 1, False):
+        bsg.bsg_set_pdl(good)
+    bsg.bsg_set_pdl(False)
+
+
 def test_forced_plan(lib):
     with pytest.raises(bsg.BsgError) as e:
         bsg.bsg_force_plan("no_such_plan")

@@ -86,3 +86,85 @@ def test_pdl_skinny_and_grouped_chains(dev):
         outs.append([D.view(torch.int16).cpu().numpy() for D in Ds])
     for a, b in zip(*outs):
         assert np.array_equal(a, b)
+
+
+def _quantised(rows, K, seed, dev):
+    """NVFP4 codes and swizzled scales of a seeded N(0, 1) BF16 matrix, from
+    the library's quantiser (alpha is not needed: the test compares bits)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    x = torch.randn((rows, K), generator=g).to(torch.bfloat16).to(dev)
+    packed = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    swz = torch.empty(bsg.nvfp4_swizzled_scale_bytes(rows, K), dtype=torch.uint8, device=dev)
+    gl = torch.empty(2, dtype=torch.float32, device=dev)
+    bsg.nvfp4_quantize(rows, K, x, packed, swz, None, gl)
+    return x, packed, swz, gl
+
+
+@pytest.mark.parametrize("M,N,K,family", [(64, 3072, 12288, "skinny"), (128, 3072, 3072, "tc1"),
+                                          (4096, 4096, 1024, "tc2")])
+def test_pdl_weights_early_chain(dev, M, N, K, family):
+    """bsg_set_pdl(2): the skinny-M and 1-SM kernels read B's codes before
+    waiting for the previous kernel (the pair kernel behaves as with 1),
+    which here is the quantiser rewriting A's codes and scales every
+    iteration (from one of two activation matrices). Each iteration's D must
+    equal the GEMM of that iteration's activations run after a full
+    synchronisation, bit for bit."""
+    xs = [_quantised(M, K, 100 + j, dev)[0] for j in range(2)]
+    _, B, sb, _ = _quantised(N, K, 7, dev)
+    A = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    gl = torch.empty(2, dtype=torch.float32, device=dev)
+    Ds = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(6)]
+    torch.cuda.synchronize()
+    bsg.bsg_set_pdl(2)
+    try:
+        for it, D in enumerate(Ds):
+            bsg.nvfp4_quantize(M, K, xs[it % 2], A, sa, None, gl)
+            bsg.nvfp4_gemm_swizzled(M, N, K, A, sa, B, sb, 0.25, D)
+        torch.cuda.synchronize()
+        plan = bsg.bsg_last_plan_name()
+    finally:
+        bsg.bsg_set_pdl(False)
+    assert bsg.bsg_get_device_status() == bsg.BSG_OK
+    assert family in plan, plan
+    want = []
+    for j in range(2):
+        bsg.nvfp4_quantize(M, K, xs[j], A, sa, None, gl)
+        Dw = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        bsg.nvfp4_gemm_swizzled(M, N, K, A, sa, B, sb, 0.25, Dw)
+        torch.cuda.synchronize()
+        want.append(Dw.view(torch.int16).cpu().numpy())
+    assert not np.array_equal(want[0], want[1])
+    for it, D in enumerate(Ds):
+        assert np.array_equal(D.view(torch.int16).cpu().numpy(), want[it % 2]), it
+
+
+def test_pdl_weights_early_fp8_wide(dev):
+    """The same promise on the 512-wide FP8 pair plan, A rewritten by a copy
+    kernel before every GEMM: the mode changes no result."""
+    M, N, K = 512, 1024, 2048
+    g = torch.Generator(device="cpu").manual_seed(11)
+    srcs = [(torch.randn((M, K), generator=g) * 0.5).to(torch.float8_e4m3fn).to(dev) for _ in range(2)]
+    B = (torch.randn((N, K), generator=g) * 0.5).to(torch.float8_e4m3fn).to(dev)
+    A = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    Ds = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(6)]
+    torch.cuda.synchronize()
+    bsg.bsg_set_pdl(2)
+    try:
+        for it, D in enumerate(Ds):
+            A.copy_(srcs[it % 2])
+            bsg.fp8_gemm(M, N, K, A, None, B, None, 1.0, D)
+        torch.cuda.synchronize()
+        plan = bsg.bsg_last_plan_name()
+    finally:
+        bsg.bsg_set_pdl(False)
+    assert bsg.bsg_get_device_status() == bsg.BSG_OK
+    assert plan == "fp8_tc2_256x512_s4_acc1", plan
+    want = []
+    for j in range(2):
+        Dw = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        bsg.fp8_gemm(M, N, K, srcs[j], None, B, None, 1.0, Dw)
+        torch.cuda.synchronize()
+        want.append(Dw.view(torch.int16).cpu().numpy())
+    for it, D in enumerate(Ds):
+        assert np.array_equal(D.view(torch.int16).cpu().numpy(), want[it % 2]), it
