@@ -416,13 +416,21 @@ __global__ void __launch_bounds__(PairTile<KIND, BN, STAGES, NUM_ACC, PACKED>::T
                     } else {
 #pragma unroll
                         for (int j = 0; j < T::MMAS; ++j) {
-                            mma_fp8_pair(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
-                                         desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
-                                         (kb | j) != 0 ? 1u : 0u);
-                            if constexpr (T::kWideN)
-                                mma_fp8_pair(d_tmem + (uint32_t)T::MMA_N, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
-                                             desc_kmajor_sw128(sb + T::B_BYTES / 2 + T::MMA_K_BYTES * j), idesc,
+                            if constexpr (T::kWideN) {
+                                // one A slice, both N halves: the second MMA
+                                // reads A from the collector buffer
+                                mma_fp8_pair_a_fill(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
+                                                    desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
+                                                    (kb | j) != 0 ? 1u : 0u);
+                                mma_fp8_pair_a_lastuse(d_tmem + (uint32_t)T::MMA_N,
+                                                       desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
+                                                       desc_kmajor_sw128(sb + T::B_BYTES / 2 + T::MMA_K_BYTES * j),
+                                                       idesc, (kb | j) != 0 ? 1u : 0u);
+                            } else {
+                                mma_fp8_pair(d_tmem, desc_kmajor_sw128(sa + T::MMA_K_BYTES * j),
+                                             desc_kmajor_sw128(sb + T::MMA_K_BYTES * j), idesc,
                                              (kb | j) != 0 ? 1u : 0u);
+                            }
                         }
                     }
                     // frees the stage in both CTAs

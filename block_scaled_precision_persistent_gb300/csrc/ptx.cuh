@@ -634,6 +634,31 @@ __device__ __forceinline__ void mma_fp8_pair(uint32_t d_tmem, uint64_t a_desc, u
         : "memory");
 }
 
+// The same MMA keeping A in the tensor core's collector buffer for the next
+// MMA (fill), or reading it from there and releasing it (lastuse): two MMAs
+// with one A and different B read A from shared memory once.
+__device__ __forceinline__ void mma_fp8_pair_a_fill(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                    uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4.collector::a::fill [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_fp8_pair_a_lastuse(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                       uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4.collector::a::lastuse [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 }  // namespace bsg
 
 // ---------------------------------------------------------------------------
