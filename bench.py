@@ -383,11 +383,11 @@ def e2e_nvfp4(w: workloads.Workload, step: Nvfp4Step, steps: int, warmup: int) -
     for i in range(warmup):
         issue(i)
     torch.cuda.synchronize()
-    # three timed runs of `steps` steps each, the median per step: the host
-    # link is shared with the rest of the machine, and one run can catch
-    # another job's copies
+    # five timed runs of `steps` steps each, the median per step: the host
+    # link and host memory are shared with the rest of the machine, and a
+    # run can catch another job's copies
     runs = []
-    for _ in range(3):
+    for _ in range(5):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(h2d)
         for i in range(steps):
@@ -413,7 +413,7 @@ def e2e_nvfp4(w: workloads.Workload, step: Nvfp4Step, steps: int, warmup: int) -
     return {"value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
             "pipelined": "two buffer sets; H2D, compute and D2H on three streams",
-            "runs_ms_per_step": [round(r, 4) for r in runs], "timing": "median of three timed runs", "host_link": link}
+            "runs_ms_per_step": [round(r, 4) for r in runs], "timing": "median of five timed runs", "host_link": link}
 
 
 def secondary_fp8(dev, steps: int, warmup: int, pk: dict, psrc: str) -> dict:
@@ -662,6 +662,17 @@ def secondary_epilogue(dev, step: Nvfp4Step, steps: int, pk: dict, psrc: str) ->
                     "bias_gamma_scatter": (e["bias"], e["gamma"], e["scatter"])}
         calls = {v: (lambda b=b, g=g, sc=sc: bsg.nvfp4_gemm_ex(M, N, K, A, sa, B, sb, alpha, b, g, sc, M, D))
                  for v, (b, g, sc) in variants.items()}
+
+        def plain_pdl():
+            # the plain call with programmatic dependent launch: each launch's
+            # prologue overlaps the previous one's tail (reported beside the
+            # plain figure, which keeps it off)
+            bsg.bsg_set_pdl(True)
+            try:
+                bsg.nvfp4_gemm_ex(M, N, K, A, sa, B, sb, alpha, None, None, None, M, D)
+            finally:
+                bsg.bsg_set_pdl(False)
+        calls["plain_pdl"] = plain_pdl
         times = graph_us(calls, launches, steps)
         cells = {v: {"us": round(us, 3), "tflops": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1)}
                  for v, us in times.items()}
@@ -1111,6 +1122,9 @@ def run_ours(args, dist: Dist) -> None:
         fr = {k: v["frac_hbm"] for k, v in secondary["skinny"]["cells"].items()}
         summary.update(skinny_frac_hbm_min=min(fr.values()), skinny_frac_hbm_max=max(fr.values()),
                        skinny_worst_cell=min(fr, key=fr.get))
+    if "epilogue" in secondary and "nvfp4_4096" in secondary["epilogue"]["shapes"]:
+        c2 = secondary["epilogue"]["shapes"]["nvfp4_4096"]
+        summary.update(nvfp4_4096_graph_us=c2["plain"]["us"], nvfp4_4096_graph_us_pdl=c2["plain_pdl"]["us"])
     if "swizzle" in secondary:
         summary["swizzle_frac_hbm"] = secondary["swizzle"]["frac_hbm"]
     if "grouped" in secondary:
