@@ -168,3 +168,46 @@ def test_pdl_weights_early_fp8_wide(dev):
         want.append(Dw.view(torch.int16).cpu().numpy())
     for it, D in enumerate(Ds):
         assert np.array_equal(D.view(torch.int16).cpu().numpy(), want[it % 2]), it
+
+
+def test_pdl_weights_early_epilogue_chain(dev):
+    """Mode 2 on the skinny kernel's epilogue-variant instantiation: the
+    previous kernel rewrites A and this iteration's gamma (a copy kernel),
+    the GEMM reads B's codes early and everything else after the wait;
+    bias, gamma and a row permutation fused. Every D must equal the
+    synchronised GEMM of its iteration, bit for bit."""
+    M, N, K = 64, 3072, 12288
+    xs = [_quantised(M, K, 300 + j, dev)[0] for j in range(2)]
+    _, B, sb, _ = _quantised(N, K, 17, dev)
+    g = torch.Generator(device="cpu").manual_seed(5)
+    bias = torch.randn(N, generator=g).to(dev)
+    gammas = [(torch.rand(M, generator=g) + 0.5).to(dev) for _ in range(2)]
+    scatter = torch.randperm(M, generator=g).to(torch.int32).to(dev)
+    A = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    sa = torch.empty(bsg.nvfp4_swizzled_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    gl = torch.empty(2, dtype=torch.float32, device=dev)
+    gamma = torch.empty(M, dtype=torch.float32, device=dev)
+    Ds = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(6)]
+    torch.cuda.synchronize()
+    bsg.bsg_set_pdl(2)
+    try:
+        for it, D in enumerate(Ds):
+            bsg.nvfp4_quantize(M, K, xs[it % 2], A, sa, None, gl)
+            gamma.copy_(gammas[it % 2])
+            bsg.nvfp4_gemm_ex(M, N, K, A, sa, B, sb, 0.25, bias, gamma, scatter, M, D)
+        torch.cuda.synchronize()
+        plan = bsg.bsg_last_plan_name()
+    finally:
+        bsg.bsg_set_pdl(False)
+    assert bsg.bsg_get_device_status() == bsg.BSG_OK
+    assert "skinny" in plan, plan
+    want = []
+    for j in range(2):
+        bsg.nvfp4_quantize(M, K, xs[j], A, sa, None, gl)
+        Dw = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        bsg.nvfp4_gemm_ex(M, N, K, A, sa, B, sb, 0.25, bias, gammas[j], scatter, M, Dw)
+        torch.cuda.synchronize()
+        want.append(Dw.view(torch.int16).cpu().numpy())
+    assert not np.array_equal(want[0], want[1])
+    for it, D in enumerate(Ds):
+        assert np.array_equal(D.view(torch.int16).cpu().numpy(), want[it % 2]), it
