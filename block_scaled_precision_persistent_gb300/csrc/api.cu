@@ -186,21 +186,83 @@ int choose_plan(Kind kind, int M, int N, int K, int num_sms, int *plan)
     return *plan >= 0 ? BSG_OK : BSG_ERR_NO_PLAN;
 }
 
+// Everything a tiled tensor map is encoded from (the other encode
+// arguments are fixed: unit element strides, no interleave, 256-byte L2
+// promotion, zero fill). Unused dimensions are zero; the struct is cleared
+// byte by byte before it is filled, so keys compare with memcmp.
+struct MapKey {
+    const void *ptr;
+    uint64_t dims[3];
+    uint64_t strides[2];
+    uint32_t box[3];
+    int32_t dtype, rank, swizzle, zero;
+};
+
+// The last kMapCacheSize maps this thread encoded: a map is a pure function
+// of its key, so a repeated call (the same buffers and shape, the usual case
+// for a layer run again) copies the 128 bytes instead of encoding them.
+constexpr int kMapCacheSize = 32;
+struct MapCacheEntry {
+    MapKey key;
+    CUtensorMap map;
+};
+thread_local MapCacheEntry t_maps[kMapCacheSize];
+thread_local int t_maps_used = 0;
+thread_local int t_maps_next = 0;
+
+int encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, int rank, const void *ptr, const uint64_t *dims,
+                 const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle swizzle)
+{
+    MapKey key;
+    std::memset(&key, 0, sizeof key);
+    key.ptr = ptr;
+    for (int i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i)
+        key.strides[i] = strides[i];
+    key.dtype = (int32_t)dtype;
+    key.rank = rank;
+    key.swizzle = (int32_t)swizzle;
+    for (int i = 0; i < t_maps_used; ++i)
+        if (std::memcmp(&t_maps[i].key, &key, sizeof key) == 0) {
+            *map = t_maps[i].map;
+            return BSG_OK;
+        }
+    auto fn = encode_fn();
+    if (!fn)
+        return BSG_ERR_CUDA;
+    cuuint64_t d[3], st[2];
+    cuuint32_t b[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i)
+        st[i] = strides[i];
+    CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void *>(ptr), d, st, b, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return BSG_ERR_CUDA;
+    MapCacheEntry &e = t_maps[t_maps_next];
+    e.key = key;
+    e.map = *map;
+    t_maps_next = (t_maps_next + 1) % kMapCacheSize;
+    if (t_maps_used < kMapCacheSize)
+        ++t_maps_used;
+    return BSG_OK;
+}
+
 int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *ptr, uint64_t inner,
               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
-    auto fn = encode_fn();
-    if (!fn)
-        return BSG_ERR_CUDA;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t elem_strides[2] = {1, 1};
-    CUresult r = fn(map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, elem_strides,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? BSG_OK : BSG_ERR_CUDA;
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {box_inner, box_outer};
+    return encode_tiled(map, dtype, 2, ptr, dims, strides, box, swizzle);
 }
 
 // A 3-D view: inner x mid x outer elements, byte strides of mid and outer.
@@ -208,17 +270,10 @@ int encode_3d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t mid, u
               uint64_t outer_stride, uint32_t box_inner, uint32_t box_mid, uint32_t box_outer,
               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE)
 {
-    auto fn = encode_fn();
-    if (!fn)
-        return BSG_ERR_CUDA;
-    cuuint64_t dims[3] = {inner, mid, outer};
-    cuuint64_t strides[2] = {mid_stride, outer_stride};
-    cuuint32_t box[3] = {box_inner, box_mid, box_outer};
-    cuuint32_t elem_strides[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, elem_strides,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? BSG_OK : BSG_ERR_CUDA;
+    const uint64_t dims[3] = {inner, mid, outer};
+    const uint64_t strides[2] = {mid_stride, outer_stride};
+    const uint32_t box[3] = {box_inner, box_mid, box_outer};
+    return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, ptr, dims, strides, box, swizzle);
 }
 
 // Resident clusters of `splits` CTAs (1..8) for skinny plan id on the
@@ -774,6 +829,31 @@ cudaError_t launch_gemm(int id, const GemmMaps &maps, const GemmArgs &args, int 
     if (id < tc1_num_plans())
         return tc1_launch(id, maps, args, grid, stream);
     return pair_launch(id - tc1_num_plans(), maps, args, grid, stream);
+}
+
+cudaError_t set_max_dynamic_smem(const void *kern, int bytes)
+{
+    struct Done {
+        int dev;
+        const void *kern;
+        int bytes;
+    };
+    static std::vector<Done> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (const Done &d : done)
+        if (d.dev == dev && d.kern == kern && d.bytes == bytes)
+            return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        done.push_back(Done{dev, kern, bytes});
+    return e;
 }
 
 int max_resident_ctas(int id, int num_sms)

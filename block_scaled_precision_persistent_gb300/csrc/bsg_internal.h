@@ -115,6 +115,12 @@ cudaError_t launch_gemm(int id, const GemmMaps &maps, const GemmArgs &args, int 
 // device (clusters x 2 for pair plans, SMs for 1-SM plans); 0 on error.
 int max_resident_ctas(int id, int num_sms);
 
+// cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, bytes), and the
+// shared-memory carveout to its maximum, on the current device, once per
+// (device, kernel, bytes): the attributes belong to the device's context,
+// and setting them again on every launch cost host time.
+cudaError_t set_max_dynamic_smem(const void *kern, int bytes);
+
 int tc1_num_plans();
 const PlanInfo &tc1_plan(int i);
 cudaError_t tc1_launch(int i, const GemmMaps &maps, const GemmArgs &args, int grid,

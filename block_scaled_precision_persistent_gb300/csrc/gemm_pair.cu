@@ -737,7 +737,7 @@ static cudaError_t pair_launch_impl(const GemmMaps &maps, const GemmArgs &args, 
             return cudaErrorInvalidValue;
         }
     }
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

@@ -622,7 +622,7 @@ static cudaError_t launch_mode(const GemmMaps &maps, const GemmArgs &args, int g
     using T = Tile<KIND, BN, STAGES, NUM_ACC>;
     constexpr int smem = T::SMEM_BYTES + ((MODE == kModeGrouped || MODE == kModeKGrouped) ? kGroupTableBytes : 0);
     auto kern = gemm_persistent_kernel<KIND, BN, STAGES, NUM_ACC, MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

@@ -506,11 +506,7 @@ static cudaError_t skinny_launch_impl(const GemmMaps &maps, const GemmArgs &args
 {
     using T = SkinnyTile<M_PAD, STAGES>;
     auto kern = has_epilogue(args) ? gemm_skinny_kernel<M_PAD, STAGES, true> : gemm_skinny_kernel<M_PAD, STAGES, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         T::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), T::SMEM_BYTES);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
