@@ -656,6 +656,10 @@ def secondary_epilogue(dev, step: Nvfp4Step, steps: int, pk: dict, psrc: str) ->
     }
     out = {}
     for wname, ((M, N, K, A, sa, B, sb, alpha, D, std), launches) in shapes.items():
+        # let the clock recover from the previous shape's power-capped
+        # graphs, so that each shape runs at its own clock
+        torch.cuda.synchronize()
+        time.sleep(0.5)
         e = workloads.make_epilogue(M, N, seed=3, bias_std=float(K) ** 0.5 * std * std, device=dev)
         variants = {"plain": (None, None, None), "bias": (e["bias"], None, None), "gamma": (None, e["gamma"], None),
                     "bias_gamma": (e["bias"], e["gamma"], None),
